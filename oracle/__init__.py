@@ -1,0 +1,108 @@
+"""fp64 CPU oracle for the gated delta rule -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its cpu_baseline
+leg and the reference arm) may import this package.  The library's product path
+never calls it, and the two share no code: the oracle is an independent
+restatement of the pages, written to check the CUDA kernels.
+
+Contents:
+* ``recurrence``: the token-by-token recurrence in C (``gdn_oracle.c``), fp64,
+  OpenMP over independent (sequence, head) chains.  This is the oracle the GPU
+  results are compared with.  It handles the scalar gate (GDN) and the
+  per-key-channel gate (KDA).  The decode step is the same recurrence, one
+  token per call.
+* ``reference``: numpy twins that pin the oracle.  They are the literal d x d
+  matrix recurrence, the DeltaNet and Mamba2 limits, and brute-force
+  chunkwise / WY / UT evaluators with three triangular solves.
+
+Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
+facts the pages and the mathematics fix.  One value is parity unpinned: the
+absolute output of the five configurations.  The pages print no input or
+output values for them, only error magnitudes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+__all__ = ["recurrence", "load", "max_threads"]
+
+_lib = None
+
+
+def load():
+    """Build (if needed) and load the C oracle."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        d = ctypes.POINTER(ctypes.c_double)
+        i32 = ctypes.POINTER(ctypes.c_int)
+        lib.gdn_oracle_forward.restype = ctypes.c_int
+        lib.gdn_oracle_forward.argtypes = [d, d, d, d, d, ctypes.c_double, d, d, d, i32, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int]
+        lib.gdn_oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(load().gdn_oracle_max_threads())
+
+
+def _f64(x) -> np.ndarray:
+    """Exact upcast of a torch tensor (bf16/fp32) or array to a contiguous fp64 numpy array."""
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def recurrence(q, k, v, g, beta, scale: float, initial_state=None, cu_seqlens=None,
+               gate_per_channel: Optional[bool] = None, n_threads: int = 0):
+    """Run the fp64 token recurrence.
+
+    Shapes: q, k [B, T, H, dk]; v [B, T, H, dv]; g [B, T, H] (GDN) or
+    [B, T, H, dk] (KDA); beta [B, T, H]; initial_state [N, H, dk, dv] or None;
+    cu_seqlens int [n+1] or None (then B must be 1).
+    Returns (o [B, T, H, dv], final_state [N, H, dk, dv]) as fp64 numpy arrays.
+    """
+    qd, kd, vd, gd, bd = (_f64(x) for x in (q, k, v, g, beta))
+    B, T, H, dk = qd.shape
+    dv = vd.shape[-1]
+    if gate_per_channel is None:
+        gate_per_channel = gd.ndim == 4
+    cu = None
+    N = B
+    if cu_seqlens is not None:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().cpu().numpy()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+        N = cu.shape[0] - 1
+    h0 = _f64(initial_state)
+    o = np.zeros((B, T, H, dv), dtype=np.float64)
+    hT = np.zeros((N, H, dk, dv), dtype=np.float64)
+    rc = load().gdn_oracle_forward(
+        _ptr(qd), _ptr(kd), _ptr(vd), _ptr(gd), _ptr(bd), float(scale), _ptr(h0), _ptr(o), _ptr(hT),
+        cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int)) if cu is not None else ctypes.POINTER(ctypes.c_int)(),
+        int(N if cu is not None else 0), B, T, H, dk, dv, int(bool(gate_per_channel)), int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return o, hT
