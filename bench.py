@@ -1,0 +1,377 @@
+#!/usr/bin/env python3
+"""Benchmark: GDN chunk forward on B4 T4096 H16 d128 C64, bf16, one GB300 per rank.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one gdn_chunk_fwd call over the whole workload.  That is the
+whole hot path: gate prefix, beta-scaled masked K K^T, the UT solve, the WY
+products, the serial state pass and the output, all in one kernel launch.
+Inputs are seeded and synthetic, drawn by gated_delta_rule_gdn_gb300.workloads.
+
+* value: tokens/s (B*T per step).  Inputs are resident in HBM and timed with
+  CUDA events around each launch.  Before each timed step a 256 MiB device
+  write flushes L2; the flush is outside the events.
+* e2e: the same metric through the public API, from pinned host buffers.
+  Every step copies the inputs host->device, runs the call, and copies o and
+  the final state device->host.
+* roofline: algorithmic bytes of one launch / the mean launch time, against
+  the measured HBM copy bandwidth.  The bytes are 1,288 B per token-head (q,
+  k, v in bf16, o in fp32, g and beta in fp32), plus the fp32 state read and
+  write per sequence-head.
+* cpu_baseline: the fp64 C oracle on the host cores (rank 0, N = 1).
+* --impl reference: the oracle alone, timed as the reference arm.
+With N > 1 (torchrun), every rank runs its own replica: weak scaling, and no
+collective on the data path.  A barrier and a max over ranks bracket the
+timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunk-fwd tokens/s (B4·T4096·H16·d128 bf16) and % of roofline, 1×GB300"
+UNIT = "tokens/s"
+WORKLOAD = 1          # index of the workload in gated_delta_rule_gdn_gb300.workloads.CONFIGS
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _alg_bytes(w) -> int:
+    """Algorithmic HBM bytes of one chunk-forward launch over workload w (o written in fp32)."""
+    token_heads = w.B * w.T * w.H
+    es = 2 if w.dtype == "bf16" else 4
+    per_token_head = es * (2 * w.dk + w.dv) + 4 * w.dv + 4 + 4      # q, k, v + o (fp32) + g, beta
+    N = w.n_seqs if w.n_seqs else w.B
+    state = 2 * N * w.H * w.dk * w.dv * 4 if w.h0_std > 0 else N * w.H * w.dk * w.dv * 4
+    return token_heads * per_token_head + state
+
+
+def _traffic_for(kernel: str):
+    """ncu DRAM bytes per launch for `kernel`, if profiled for the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        src = os.path.join(ROOT, "gated_delta_rule_gdn_gb300", "csrc", rec["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        return int(rec["dram_bytes_per_launch"]) if sha == rec["source_sha256"] else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons for one GPU in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t0 is None or t >= self.t0]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _init_pg(ws: int, backend: str):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """Max of a scalar over the ranks of the default process group (identity for one rank)."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _oracle_inputs(x, heads):
+    import numpy as np
+    import torch
+    hs = torch.as_tensor(heads)
+    arr = {k: np.ascontiguousarray(x[k].index_select(2, hs).to(torch.float64).numpy())
+           for k in ("q", "k", "v", "g", "beta")}
+    h0 = x["initial_state"]
+    arr["h0"] = None if h0 is None else np.ascontiguousarray(h0.index_select(1, hs).to(torch.float64).numpy())
+    return arr
+
+
+def cpu_baseline(x, w, min_seconds=8.0, max_passes=5, heads=None):
+    """Time the fp64 oracle on the host cores (bounded sample of the workload); returns a dict."""
+    import oracle
+    heads = list(range(w.H)) if heads is None else heads
+    arr = _oracle_inputs(x, heads)
+    oracle.load()
+    passes, t_total = 0, 0.0
+    while passes < max_passes and (passes == 0 or t_total < min_seconds):
+        t0 = time.perf_counter()
+        oracle.recurrence(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], x["scale"], arr["h0"])
+        t_total += time.perf_counter() - t0
+        passes += 1
+    frac = len(heads) / w.H
+    tokens = w.B * w.T * frac * passes
+    return {"value": tokens / t_total, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{w.B * len(heads)} (sequence, head) chains of {w.T} tokens ({len(heads)}/{w.H} heads), "
+                      f"{passes} pass(es), {t_total:.1f} s; tokens/s scaled to all {w.H} heads"}
+
+
+def run_reference(args):
+    ws, rank, local = _dist()
+    if ws > 1:
+        if rank != 0:
+            return 0
+    from gated_delta_rule_gdn_gb300 import workloads as W
+    import oracle
+    w = W.config(WORKLOAD)
+    x = W.chunk_inputs(w, seed=0)
+    heads = [0, 1, 2, 3]                 # one step = 16 (sequence, head) chains of 4096 tokens
+    arr = _oracle_inputs(x, heads)
+    oracle.load()
+    run = lambda: oracle.recurrence(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], x["scale"], arr["h0"])
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = w.B * w.T * (len(heads) / w.H) / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                       "chunk_size": w.chunk_size},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"per step {w.B * len(heads)} (sequence, head) chains of {w.T} tokens "
+                                       f"({len(heads)}/{w.H} heads); tokens/s scaled to all {w.H} heads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _init_pg(ws, "nccl")
+    import gated_delta_rule_gdn_gb300 as gdn
+    from gated_delta_rule_gdn_gb300 import build as libbuild, workloads as W
+    if local == 0:
+        libbuild.build()
+    barrier(ws)
+    gdn.load()
+    w = W.config(WORKLOAD)
+    x = W.chunk_inputs(w, seed=0)
+    host = {k: x[k].pin_memory() for k in ("q", "k", "v", "g", "beta", "initial_state")}
+    d = {k: v.to(dev) for k, v in host.items()}
+    o = torch.empty((w.B, w.T, w.H, w.dv), dtype=torch.float32, device=dev)
+    hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(dd, oo, hh):
+        gdn.gdn_chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], scale=w.scale,
+                          initial_state=dd["initial_state"], output_final_state=True, chunk_size=w.chunk_size,
+                          algo=args.algo, o=oo, final_state=hh, stream=stream, o_dtype=torch.float32)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call(d, o, hT)
+    torch.cuda.synchronize(dev)
+    assert gdn.device_status() == 0
+
+    sampler = ClockSampler(int(os.environ.get("GDN_BENCH_GPU_INDEX", local))) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        # keep the GPU busy (untimed) while the sampler starts, so clock samples reflect load
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            flush.fill_(1)
+            call(d, o, hT)
+            torch.cuda.synchronize(dev)
+        sampler.mark()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_wall = time.perf_counter()
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record(stream)
+        call(d, o, hT)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    launch_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    ms = max_over_ranks(sum(launch_ms) / len(launch_ms), ws, dev)
+    clocks = sampler.stop() if sampler else None
+    assert gdn.device_status() == 0
+
+    # end to end through the public API: pinned host -> device, call, device -> host, every step
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_host = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size() + h_host.numel() * h_host.element_size()
+    dd = {k: torch.empty_like(v) for k, v in d.items()}
+    o2, h2 = torch.empty_like(o), torch.empty_like(hT)
+
+    def e2e_step():
+        for k in dd:
+            dd[k].copy_(host[k], non_blocking=True)
+        call(dd, o2, h2)
+        o_host.copy_(o2, non_blocking=True)
+        h_host.copy_(h2, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+
+    tokens = w.B * w.T
+    value = tokens * ws / (ms / 1e3)
+    peak, peak_kind = _peaks()
+    alg = _alg_bytes(w)
+    achieved = alg / (ms / 1e3) / 1e9
+    kernel = "chunk_tc" if gdn.chunk_plan(False, w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16,
+                                           False, args.algo) == "tcgen05" else "chunk_generic"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k unit-norm N(0,1), v N(0,1), beta=sigmoid(N), log alpha=-A softplus(N+dt_bias))",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "chunk_size": w.chunk_size, "initial_state": True, "output_final_state": True,
+                   "o_dtype": "f32",
+                   "l2": "flushed before each timed step (256 MiB device write, outside the events)",
+                   "kernel": kernel, "timed_region_wall_ms": t_wall * 1e3},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": _traffic_for(kernel), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6800 GB/s",
+                     "algorithmic_bytes_per_launch": alg},
+        "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x, w)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--algo", choices=["auto", "generic", "tcgen05"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,200 @@
+"""ctypes binding of libgdn_gb300.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels.  torch is
+used for device memory and streams.  If the library is missing, the calls
+raise; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_LIB = None
+
+GDN_OK = 0
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA",
+                4: "GDN_ERR_TIMEOUT"}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _declare(lib):
+    vp, fp, i = ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+    chunk = [vp, vp, vp, vp, vp, fp, vp, i, vp, vp, i, vp, i, i, i, i, i, i, i, i]
+    for name in ("gdn_chunk_fwd", "kda_chunk_fwd"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i, chunk + [vp]
+    for name in ("gdn_chunk_fwd_algo", "kda_chunk_fwd_algo"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i, chunk + [i, vp]
+    lib.gdn_recurrent_step.restype = i
+    lib.gdn_recurrent_step.argtypes = [vp, vp, vp, vp, vp, fp, vp, vp, i, i, i, i, i, i, vp]
+    lib.gdn_chunk_plan.restype = i
+    lib.gdn_chunk_plan.argtypes = [i, i, i, i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_last_error.argtypes = []
+    lib.gdn_device_status.restype = i
+    lib.gdn_device_status.argtypes = [i]
+    lib.gdn_version.restype = ctypes.c_char_p
+    lib.gdn_version.argtypes = []
+    return lib
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libgdn_gb300.so (built by gated_delta_rule_gdn_gb300.build.build()); raise if missing."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libgdn_gb300.so is not built ({path}); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        _LIB = _declare(ctypes.CDLL(path))
+    return _LIB
+
+
+def last_error() -> str:
+    return load().gdn_last_error().decode()
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        raise GdnError(status, last_error())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
+           cu_seqlens=None, chunk_size=64, algo="auto", o=None, final_state=None, stream=None,
+           o_dtype=torch.float32):
+    lib = load()
+    if q.dtype not in DTYPES:
+        raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
+    dev = q.device
+    for name, t, dt in (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32)):
+        _need(t, name, dt, dev)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, T, H):
+        raise ValueError("q, k, v shapes do not match")
+    if g.shape != ((B, T, H, dk) if per_channel else (B, T, H)) or beta.shape != (B, T, H):
+        raise ValueError("g / beta shapes do not match")
+    n_seqs = 0
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        n_seqs = cu_seqlens.numel() - 1
+    N = n_seqs if cu_seqlens is not None else B
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev)
+        if initial_state.shape != (N, H, dk, dv):
+            raise ValueError(f"initial_state must be {(N, H, dk, dv)}")
+    if o_dtype not in DTYPES:
+        raise ValueError(f"o_dtype must be float32 or bfloat16 (got {o_dtype})")
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=dev)
+    _need(o, "o", o_dtype, dev)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, dev)
+    if scale is None:
+        scale = dk ** -0.5
+    fn = lib.kda_chunk_fwd_algo if per_channel else lib.gdn_chunk_fwd_algo
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(initial_state),
+            int(final_state is not None), _ptr(final_state), _ptr(cu_seqlens), n_seqs, _ptr(o),
+            B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[o_dtype], ALGOS[algo],
+            _stream_handle(stream, dev))
+    _check(st)
+    return o, final_state
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False, cu_seqlens=None,
+                  chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32):
+    """Chunkwise gated delta rule forward (C ABI gdn_chunk_fwd).  Returns (o, final_state or None).
+
+    o is fp32 unless o_dtype=torch.bfloat16 (then it is the round-to-nearest-even of the fp32 result).
+    """
+    return _chunk(False, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens, chunk_size, algo,
+                  o, final_state, stream, o_dtype)
+
+
+def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False, cu_seqlens=None,
+                  chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32):
+    """Chunkwise KDA forward, g per key channel (C ABI kda_chunk_fwd).  Returns (o, final_state or None)."""
+    return _chunk(True, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens, chunk_size, algo,
+                  o, final_state, stream, o_dtype)
+
+
+def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
+    """One decode token for N sequences (C ABI gdn_recurrent_step); updates ``state`` in place, returns o."""
+    lib = load()
+    if q.dtype not in DTYPES:
+        raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
+    dev = q.device
+    for name, t, dt in (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32), ("state", state, torch.float32)):
+        _need(t, name, dt, dev)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if state.shape != (N, H, dk, dv) or k.shape != q.shape or g.shape != (N, H) or beta.shape != (N, H):
+        raise ValueError("decode shapes do not match")
+    if o_dtype not in DTYPES:
+        raise ValueError(f"o_dtype must be float32 or bfloat16 (got {o_dtype})")
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=o_dtype, device=dev)
+    _need(o, "o", o_dtype, dev)
+    if scale is None:
+        scale = dk ** -0.5
+    st = lib.gdn_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(o),
+                                N, H, dk, dv, DTYPES[q.dtype], DTYPES[o_dtype], _stream_handle(stream, dev))
+    _check(st)
+    return o
+
+
+def chunk_plan(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chunk_size: int, dtype,
+               varlen: bool = False, algo: str = "auto", o_dtype=torch.float32) -> str:
+    """Name of the kernel ("generic" or "tcgen05") a chunk-forward call with these sizes runs."""
+    out = ctypes.c_int(-1)
+    _check(load().gdn_chunk_plan(int(per_channel), B, T, H, dk, dv, chunk_size, DTYPES[dtype], DTYPES[o_dtype],
+                                 int(varlen), ALGOS[algo], ctypes.byref(out)))
+    return {v: k for k, v in ALGOS.items()}[out.value]
+
+
+def device_status(clear: bool = True) -> int:
+    """GDN_OK, or GDN_ERR_TIMEOUT if a kernel gave up a bounded wait (synchronises the device)."""
+    return int(load().gdn_device_status(int(clear)))

@@ -1,0 +1,202 @@
+// C ABI of libgdn_gb300.so (declared in include/gdn.h): argument checks, error reporting and
+// kernel dispatch.  No entry point allocates device memory; all buffers belong to the caller.
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/gdn.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gdn_status fail(gdn_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+gdn_status ok() {
+    g_last_error.clear();
+    return GDN_OK;
+}
+
+gdn_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(GDN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool dtype_ok(gdn_dtype d) { return d == GDN_F32 || d == GDN_BF16; }
+
+gdn_status check_chunk(const gdn::ChunkArgs& a, gdn_dtype dtype, gdn_dtype o_dtype, int output_final_state,
+                       const char* fn) {
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!dtype_ok(o_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown o_dtype %d", fn, (int)o_dtype);
+    if (a.B < 1 || a.T < 0 || a.H < 1)
+        return fail(GDN_ERR_INVALID_ARG, "%s: need B >= 1, T >= 0, H >= 1 (got B=%d T=%d H=%d)", fn, a.B, a.T, a.H);
+    if (a.dk < 1 || a.dv < 1 || a.dk > 128 || a.dv > 128)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..128 (got d_k=%d d_v=%d)", fn, a.dk, a.dv);
+    if (a.C != 16 && a.C != 32 && a.C != 64)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: chunk_size must be 16, 32 or 64 (got %d)", fn, a.C);
+    if (!std::isfinite(a.scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if ((output_final_state != 0) != (a.hT != nullptr))
+        return fail(GDN_ERR_INVALID_ARG, "%s: final_state must be non-NULL exactly when output_final_state is set", fn);
+    if (a.cu) {
+        if (a.B != 1) return fail(GDN_ERR_INVALID_ARG, "%s: cu_seqlens needs B == 1 (got B=%d)", fn, a.B);
+        if (a.n_seqs < 1) return fail(GDN_ERR_INVALID_ARG, "%s: cu_seqlens needs n_seqs >= 1 (got %d)", fn, a.n_seqs);
+        if (!aligned(a.cu, 4)) return fail(GDN_ERR_INVALID_ARG, "%s: cu_seqlens is not 4-byte aligned", fn);
+    }
+    const bool any_tokens = (long)a.B * a.T > 0;
+    if (any_tokens && (!a.q || !a.k || !a.v || !a.g || !a.beta || !a.o))
+        return fail(GDN_ERR_INVALID_ARG, "%s: q, k, v, g, beta and o must be non-NULL", fn);
+    const size_t es = dtype == GDN_BF16 ? 2 : 4;
+    const size_t oes = o_dtype == GDN_BF16 ? 2 : 4;
+    if (any_tokens && (!aligned(a.q, es) || !aligned(a.k, es) || !aligned(a.v, es) || !aligned(a.o, oes) ||
+                       !aligned(a.g, 4) || !aligned(a.beta, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "%s: a tensor is not aligned to its element size", fn);
+    if ((a.h0 && !aligned(a.h0, 4)) || (a.hT && !aligned(a.hT, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "%s: a state buffer is not 4-byte aligned", fn);
+    if ((long)a.B * a.T * a.H > (1L << 31) / (a.dk > a.dv ? a.dk : a.dv))
+        return fail(GDN_ERR_UNSUPPORTED, "%s: tensor has 2^31 elements or more", fn);
+    return GDN_OK;
+}
+
+gdn_status resolve_algo(const gdn::ChunkArgs& a, gdn_algo algo, const char* fn, bool* use_tc) {
+    if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_GENERIC && algo != GDN_ALGO_TCGEN05)
+        return fail(GDN_ERR_INVALID_ARG, "%s: unknown algo %d", fn, (int)algo);
+    const char* why = gdn::tc_chunk_unsupported_reason(a);
+    *use_tc = false;
+    if (algo == GDN_ALGO_TCGEN05) {
+        if (why) return fail(GDN_ERR_UNSUPPORTED, "%s: the tcgen05 kernel does not apply: %s", fn, why);
+        *use_tc = true;
+    } else if (algo == GDN_ALGO_AUTO) {
+        *use_tc = (why == nullptr);
+    }
+    return GDN_OK;
+}
+
+gdn_status chunk_common(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                        const float* initial_state, int output_final_state, float* final_state,
+                        const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
+                        int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, gdn_algo algo, void* stream,
+                        bool per_channel, const char* fn) {
+    gdn::ChunkArgs a{q, k, v, g, beta, scale, initial_state, final_state, cu_seqlens, n_seqs, o,
+                     B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0,
+                     o_dtype == GDN_F32 ? 1 : 0};
+    gdn_status st = check_chunk(a, dtype, o_dtype, output_final_state, fn);
+    if (st != GDN_OK) return st;
+    bool use_tc = false;
+    st = resolve_algo(a, algo, fn, &use_tc);
+    if (st != GDN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = use_tc ? gdn::launch_chunk_tc(a, s) : gdn::launch_chunk_generic(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_fwd_algo(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              float scale, const float* initial_state, int output_final_state,
+                              float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T,
+                              int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype,
+                              gdn_algo algo, void* stream) {
+    return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
+                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, stream, false, "gdn_chunk_fwd");
+}
+
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                         const float* initial_state, int output_final_state, float* final_state,
+                         const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
+                         int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, void* stream) {
+    return gdn_chunk_fwd_algo(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens,
+                              n_seqs, o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, GDN_ALGO_AUTO, stream);
+}
+
+gdn_status kda_chunk_fwd_algo(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              float scale, const float* initial_state, int output_final_state,
+                              float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T,
+                              int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype,
+                              gdn_algo algo, void* stream) {
+    return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
+                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, stream, true, "kda_chunk_fwd");
+}
+
+gdn_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                         const float* initial_state, int output_final_state, float* final_state,
+                         const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
+                         int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, void* stream) {
+    return kda_chunk_fwd_algo(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens,
+                              n_seqs, o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, GDN_ALGO_AUTO, stream);
+}
+
+gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              float scale, float* state, void* o, int N, int H, int d_k, int d_v, gdn_dtype dtype,
+                              gdn_dtype o_dtype, void* stream) {
+    const char* fn = "gdn_recurrent_step";
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!dtype_ok(o_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown o_dtype %d", fn, (int)o_dtype);
+    if (N < 1 || H < 1) return fail(GDN_ERR_INVALID_ARG, "%s: need N >= 1, H >= 1 (got N=%d H=%d)", fn, N, H);
+    if (d_k < 1 || d_v < 1 || d_k > 128 || d_v > 128)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..128 (got d_k=%d d_v=%d)", fn, d_k, d_v);
+    if (!q || !k || !v || !g || !beta || !state || !o)
+        return fail(GDN_ERR_INVALID_ARG, "%s: q, k, v, g, beta, state and o must be non-NULL", fn);
+    if (!std::isfinite(scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    const size_t es = dtype == GDN_BF16 ? 2 : 4;
+    const size_t oes = o_dtype == GDN_BF16 ? 2 : 4;
+    if (!aligned(q, es) || !aligned(k, es) || !aligned(v, es) || !aligned(o, oes) || !aligned(g, 4) ||
+        !aligned(beta, 4) || !aligned(state, 4))
+        return fail(GDN_ERR_INVALID_ARG, "%s: a tensor is not aligned to its element size", fn);
+    if ((long)N * H > (1L << 31) / ((long)d_k * d_v))
+        return fail(GDN_ERR_UNSUPPORTED, "%s: state has 2^31 elements or more", fn);
+    gdn::StepArgs a{q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype == GDN_BF16 ? 1 : 0,
+                    o_dtype == GDN_F32 ? 1 : 0};
+    cudaError_t e = gdn::launch_recurrent_step(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+}
+
+gdn_status gdn_chunk_plan(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                          gdn_dtype o_dtype, int varlen, gdn_algo requested, gdn_algo* chosen) {
+    const char* fn = "gdn_chunk_plan";
+    if (!chosen) return fail(GDN_ERR_INVALID_ARG, "%s: chosen is NULL", fn);
+    // stand-in pointers, 256-byte aligned and never dereferenced: nothing is launched here
+    const void* p = reinterpret_cast<const void*>(uintptr_t(1) << 20);
+    float* fp = reinterpret_cast<float*>(uintptr_t(1) << 20);
+    gdn::ChunkArgs a{p, p, p, fp, fp, 1.0f, nullptr, nullptr, varlen ? reinterpret_cast<const int32_t*>(p) : nullptr,
+                     varlen ? 1 : 0, const_cast<void*>(p), B, T, H, d_k, d_v, chunk_size,
+                     dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0, o_dtype == GDN_F32 ? 1 : 0};
+    gdn_status st = check_chunk(a, dtype, o_dtype, 0, fn);
+    if (st != GDN_OK) return st;
+    bool use_tc = false;
+    st = resolve_algo(a, requested, fn, &use_tc);
+    if (st != GDN_OK) return st;
+    *chosen = use_tc ? GDN_ALGO_TCGEN05 : GDN_ALGO_GENERIC;
+    return ok();
+}
+
+const char* gdn_last_error(void) { return g_last_error.c_str(); }
+
+gdn_status gdn_device_status(int clear) {
+    unsigned v = 0;
+    cudaError_t e = gdn::tc_read_and_clear_status(&v, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_device_status");
+    if (v != 0) return fail(GDN_ERR_TIMEOUT, "gdn_device_status: a kernel gave up a bounded wait (code 0x%x)", v);
+    return ok();
+}
+
+const char* gdn_version(void) { return "gdn_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

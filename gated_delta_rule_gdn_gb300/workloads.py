@@ -110,7 +110,7 @@ def _softplus(x: np.ndarray) -> np.ndarray:
 def _unit_rows(x: np.ndarray) -> np.ndarray:
     """L2-normalise the last axis in fp32 (the recipe's key/query normalisation)."""
     x = x.astype(np.float32, copy=False)
-    n = np.sqrt(np.sum(x.astype(np.float64) ** 2, axis=-1, keepdims=True)).astype(np.float32)
+    n = np.sqrt(np.einsum("...i,...i->...", x, x))[..., None]
     return x / np.maximum(n, np.float32(1e-12))
 
 

@@ -1,0 +1,200 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta rule library, libgdn_gb300.so.
+ *
+ * The operation is the gated delta rule.  In the paper's orientation the state
+ * S_t is d_v x d_k:
+ *
+ *     S_t = S_{t-1} ( alpha_t (I - beta_t k_t k_t^T) ) + beta_t v_t k_t^T,
+ *     o_t = scale * S_t q_t
+ *
+ * Sources:
+ *   - "TileLang 实战：KDA 从零到一 -- Gated DeltaNet", the opening equation
+ *     and §2.3 (chunkwise algorithm, paper eqs 11-12).
+ *   - "Gated Delta Network (GDN)", eq. 4 (the recurrence), eq. 12 (decode)
+ *     and §4 (chunkwise training / prefill).
+ *   - "You Could Have Come Up With Kimi Delta Attention", the KDA variant
+ *     with a per-key-channel retention.
+ *
+ * Conventions shared by every entry point
+ *   - Gates are natural logs: g = log alpha <= 0.  GDN has one gate per
+ *     (token, head); KDA has one per (token, head, key channel).
+ *   - beta is the writing strength.  The pages' range is (0, 1); (0, 2) is
+ *     accepted as written, and no range check is made.
+ *   - States use the transposed layout, like the pages' kernels:
+ *     h = S^T, shape [N, H, d_k, d_v], fp32, row-major.  Row c is key
+ *     channel c.
+ *   - All tensors are contiguous row-major device buffers.  The caller
+ *     allocates them and keeps ownership.  The library keeps no pointer
+ *     after a call returns.
+ *   - Each call is asynchronous on `stream`, a cudaStream_t (NULL means the
+ *     legacy default stream).  A GDN_OK return means the work was enqueued.
+ *     Kernel-side faults surface at the next synchronising CUDA call.
+ *     Bounded waits that gave up are reported by gdn_device_status().
+ *   - Arguments are checked on the host before any launch.  On an error
+ *     nothing is launched, the status code says why, and gdn_last_error()
+ *     holds a message (thread-local).
+ *   - dtype is the element type of q, k and v (GDN_F32 or GDN_BF16); o_dtype
+ *     is the element type of o (GDN_F32 or GDN_BF16; a bf16 output is the
+ *     round-to-nearest-even of the fp32 result).  g, beta and the states are
+ *     always fp32.
+ *   - Buffers the call reads may not alias buffers it writes.  The one
+ *     exception is gdn_recurrent_step's in-place state.
+ *
+ * No entry point allocates device memory.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, inconsistent flags: nothing launched */
+    GDN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement: nothing launched */
+    GDN_ERR_CUDA = 3,         /* a CUDA runtime call failed (device query, attribute, launch) */
+    GDN_ERR_TIMEOUT = 4       /* a kernel's bounded wait gave up (see gdn_device_status) */
+} gdn_status;
+
+typedef enum gdn_dtype {
+    GDN_F32 = 0,   /* q, k, v, o are float */
+    GDN_BF16 = 1   /* q, k, v, o are bfloat16 (round-to-nearest-even on output) */
+} gdn_dtype;
+
+/* Kernel choice for the chunk forward. */
+typedef enum gdn_algo {
+    GDN_ALGO_AUTO = 0,     /* the fused tensor-core kernel where it applies, else the generic one */
+    GDN_ALGO_GENERIC = 1,  /* fp32 SIMT chunk kernel: any dtype, 1 <= d_k, d_v <= 128 */
+    GDN_ALGO_TCGEN05 = 2   /* fused tcgen05/TMA kernel: bf16, d_k = d_v = 128, chunk 64;
+                              GDN_ERR_UNSUPPORTED when the request does not fit it */
+} gdn_algo;
+
+/*
+ * gdn_chunk_fwd -- chunkwise forward of the gated delta rule: training and
+ * prefill, any sequence length.
+ *
+ * Sources: "TileLang 实战：KDA 从零到一 -- Gated DeltaNet", §2.3 (paper eqs
+ * 11-12; the per-chunk triangular system and the UT transform), and
+ * "Gated Delta Network (GDN)", §4(b3)-(d) (intra-chunk WY/UT products, then
+ * the serial inter-chunk state pass).  The result is that of the token
+ * recurrence above; only rounding depends on chunk_size.
+ *
+ *   q, k        [B, T, H, d_k]   dtype
+ *   v           [B, T, H, d_v]   dtype
+ *   g           [B, T, H]        fp32, log alpha (natural log)
+ *   beta        [B, T, H]        fp32
+ *   scale       output scale (commonly 1/sqrt(d_k))
+ *   initial_state  [N, H, d_k, d_v] fp32, or NULL for zeros
+ *   output_final_state  nonzero: write the state after each sequence's last token
+ *   final_state [N, H, d_k, d_v] fp32; must be non-NULL iff output_final_state
+ *   cu_seqlens  NULL: B independent sequences of T tokens (N = B).
+ *               Otherwise int32 device array [n_seqs + 1] of packed sequence
+ *               offsets: B must be 1, N = n_seqs >= 1, cu_seqlens[0] = 0,
+ *               non-decreasing, cu_seqlens[n_seqs] = T.  Each sequence starts
+ *               from its own initial state; chunks align to each sequence's
+ *               start ("Gated Delta Network (GDN)", §6: chunk boundaries are
+ *               not sequence boundaries).  Zero-length sequences are allowed
+ *               (final = initial).  The contents are on the device and are not
+ *               checked on the host.  The kernels clamp every offset into
+ *               [0, T], so a malformed array cannot make them touch memory out
+ *               of bounds, but the results are then unspecified.
+ *   o           [B, T, H, d_v]   o_dtype (output)
+ *   chunk_size  16, 32 or 64 (the pages' kernels use these; 64 is the default there)
+ *   sizes       B >= 1, T >= 0, H >= 1, 1 <= d_k, d_v <= 128
+ *
+ * Packed sequences give results bitwise equal to running each sequence alone.
+ */
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         float scale, const float* initial_state, int output_final_state, float* final_state,
+                         const int32_t* cu_seqlens, int n_seqs, void* o,
+                         int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype,
+                         void* stream);
+
+/* gdn_chunk_fwd with an explicit kernel choice (for tests and measurement). */
+gdn_status gdn_chunk_fwd_algo(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              float scale, const float* initial_state, int output_final_state,
+                              float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o,
+                              int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                              gdn_dtype o_dtype, gdn_algo algo, void* stream);
+
+/*
+ * kda_chunk_fwd -- chunkwise forward of Kimi Delta Attention.  The retention
+ * is a per-key-channel vector exp(g_t), applied as Diag(exp g_t) on the key
+ * side of the state before the delta update.
+ *
+ * Source: "You Could Have Come Up With Kimi Delta Attention": the recurrent
+ * five-step update (decay, predict, residual, rank-1 write, read) and its
+ * chunkwise form, with per-channel decays between tokens, the strictly lower
+ * key-key system and the read matrix that includes the diagonal.
+ *
+ * Arguments and layouts are those of gdn_chunk_fwd, except that g is
+ * [B, T, H, d_k] fp32.  With g equal on every channel the result is the GDN
+ * result.
+ */
+gdn_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         float scale, const float* initial_state, int output_final_state, float* final_state,
+                         const int32_t* cu_seqlens, int n_seqs, void* o,
+                         int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype,
+                         void* stream);
+
+gdn_status kda_chunk_fwd_algo(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              float scale, const float* initial_state, int output_final_state,
+                              float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o,
+                              int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                              gdn_dtype o_dtype, gdn_algo algo, void* stream);
+
+/*
+ * gdn_recurrent_step -- one decode token for N independent sequences.
+ *
+ * Sources: "Gated Delta Network (GDN)", eq. 12 and §4.4 (decode runs the
+ * recurrent form, one token at a time, at a constant cost per token), and
+ * the fused recurrent kernel on "You Could Have Come Up With Kimi Delta
+ * Attention" (decay, predict, residual, rank-1 write, read).
+ *
+ *   q, k   [N, H, d_k] dtype      v  [N, H, d_v] dtype      o  [N, H, d_v] o_dtype
+ *   g      [N, H] fp32 (log alpha)   beta [N, H] fp32
+ *   state  [N, H, d_k, d_v] fp32, updated in place (the only aliasing allowed)
+ *   o      output: o = scale * S_t q_t, read after the write
+ *   sizes  N >= 1, H >= 1, 1 <= d_k, d_v <= 128
+ */
+gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              float scale, float* state, void* o, int N, int H, int d_k, int d_v,
+                              gdn_dtype dtype, gdn_dtype o_dtype, void* stream);
+
+/*
+ * gdn_chunk_plan -- which kernel a chunk-forward call with these sizes would run.
+ * The buffers are assumed to be 16-byte aligned.  per_channel nonzero stands
+ * for kda_chunk_fwd; varlen nonzero stands for a call with cu_seqlens.
+ * requested is resolved into *chosen: GDN_ALGO_AUTO becomes
+ * GDN_ALGO_TCGEN05 or GDN_ALGO_GENERIC.  The status is the one the call
+ * itself would return for these sizes, and *chosen is written only on GDN_OK.
+ * Nothing is launched.
+ */
+gdn_status gdn_chunk_plan(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
+                          gdn_dtype dtype, gdn_dtype o_dtype, int varlen, gdn_algo requested,
+                          gdn_algo* chosen);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* gdn_last_error(void);
+
+/*
+ * Device-side status of the kernels that use bounded waits (the tcgen05 path).
+ * Synchronises the current device.  It returns GDN_OK, or GDN_ERR_TIMEOUT if
+ * any CTA gave up a bounded wait since the status was last cleared.  A CTA
+ * that gives up drops its work and its outputs are unspecified.  With clear
+ * nonzero, the status is reset.  GDN_ERR_CUDA if the query itself failed.
+ */
+gdn_status gdn_device_status(int clear);
+
+/* Library version string. */
+const char* gdn_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* GDN_GB300_H */

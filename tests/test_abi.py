@@ -1,0 +1,92 @@
+"""The C-ABI library builds, loads and exports every entry point include/gdn.h declares.
+
+Host-side argument checking is exercised too.  Every call here is rejected
+before any CUDA work, so no GPU is needed and none is touched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_gdn_gb300 import _binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _binding.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*)\s+(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_three_entry_points():
+    names = _declared_functions()
+    for n in ("gdn_chunk_fwd", "kda_chunk_fwd", "gdn_recurrent_step", "gdn_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(_binding.lib_path())
+    missing = [n for n in _declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_version(lib):
+    assert b"sm_103a" in lib.gdn_version()
+
+
+FAKE = 0x10000  # an aligned, never-dereferenced address: every call below fails validation first
+
+
+def _chunk(lib, fn="gdn_chunk_fwd_algo", **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=1.0, h0=None, ofs=0, hT=None, cu=None, n=0, o=FAKE,
+             B=1, T=64, H=1, dk=64, dv=64, C=64, dtype=1, odt=0, algo=0)
+    a.update(kw)
+    f = getattr(lib, fn)
+    return f(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["h0"], a["ofs"], a["hT"], a["cu"], a["n"],
+             a["o"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["C"], a["dtype"], a["odt"], a["algo"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(dk=0), 2), (dict(dv=129), 2), (dict(C=48), 2),
+    (dict(C=128), 2), (dict(dtype=7), 1), (dict(q=None), 1), (dict(o=None), 1), (dict(ofs=1), 1),
+    (dict(hT=FAKE), 1), (dict(cu=FAKE, B=2, n=2), 1), (dict(cu=FAKE, n=0), 1), (dict(q=FAKE + 1), 1),
+    (dict(scale=float("nan")), 1), (dict(algo=9), 1), (dict(odt=3), 1), (dict(o=FAKE + 2), 1), (dict(algo=2, dtype=0), 2), (dict(algo=2, dk=64, dv=32), 2),
+])
+def test_chunk_argument_checks(lib, kw, status):
+    assert _chunk(lib, **kw) == status
+    assert _binding.last_error()
+    assert _chunk(lib, fn="kda_chunk_fwd_algo", **kw) == status
+
+
+def test_step_argument_checks(lib):
+    f = lib.gdn_recurrent_step
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, b=FAKE, s=1.0, st=FAKE, o=FAKE, N=4, H=2, dk=128, dv=128, dt=1, odt=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["k"], a["v"], a["g"], a["b"], a["s"], a["st"], a["o"], a["N"], a["H"], a["dk"], a["dv"],
+                 a["dt"], a["odt"], None)
+    assert call(N=0) == 1
+    assert call(st=None) == 1
+    assert call(dk=256) == 2
+    assert call(dt=5) == 1
+    assert call(q=FAKE + 2, dt=0) == 1
+    assert call(s=float("inf")) == 1
+    assert call(odt=2) == 1
+    assert call(o=FAKE + 2) == 1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import gated_delta_rule_gdn_gb300 as gdn
+    x = torch.zeros(1, 4, 1, 8)
+    with pytest.raises(ValueError):
+        gdn.gdn_chunk_fwd(x, x, x, torch.zeros(1, 4, 1), torch.zeros(1, 4, 1))

@@ -1,0 +1,201 @@
+"""GPU parity of the chunk forward (gdn_chunk_fwd, kda_chunk_fwd) against the fp64 oracle.
+
+Every call goes through the C ABI (ctypes binding), on seeded synthetic inputs
+from gated_delta_rule_gdn_gb300.workloads, in element-by-element comparison:
+* small cases the oracle runs whole, spanning several chunks and a ragged tail;
+* the full-size workloads, with the oracle run on all heads (config 1) or a
+  sample of heads (configs 2 and 3);
+* edge cases: T < C, T = 0, zero-length packed sequences, extreme decay, beta
+  near 0 and 1.
+Packed sequences must match separate runs bitwise; so must a state hand-off at
+a chunk boundary.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_gdn_gb300 as gdn
+from gated_delta_rule_gdn_gb300 import workloads as W
+from parity_util import assert_close, oracle_on_heads, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from gated_delta_rule_gdn_gb300 import build
+    build.build()
+    gdn.load()
+
+
+def _tc_fits(x, dtype):
+    q = x["q"]
+    return dtype == torch.bfloat16 and q.shape[-1] == 128 and x["v"].shape[-1] == 128 and x["chunk_size"] == 64
+
+
+def _run(x, algo="auto", out_final=True, o_dtype=torch.float32):
+    d = to_dev(x)
+    fn = gdn.kda_chunk_fwd if x["gate_per_channel"] else gdn.gdn_chunk_fwd
+    o, hT = fn(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["initial_state"],
+               output_final_state=out_final, cu_seqlens=d["cu_seqlens"], chunk_size=x["chunk_size"], algo=algo,
+               o_dtype=o_dtype)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    return o.double().cpu().numpy(), (None if hT is None else hT.double().cpu().numpy())
+
+
+def _algos(x):
+    return ["generic", "tcgen05"] if _tc_fits(x, x["q"].dtype) else ["generic"]
+
+
+def _workload(kind, dtype, dk, dv, C, h0_std):
+    return W.ChunkWorkload("t", kind, 1, 1, 1, dk, dv, C, dtype, h0_std=h0_std)
+
+
+def test_config0_tiny_fp32():
+    x = W.chunk_inputs(W.config(0), seed=0)
+    o_ref, h_ref = oracle_on_heads(x)
+    o, hT = _run(x, "auto")
+    assert_close(o, o_ref, torch.float32, "o")
+    assert_close(hT, h_ref, torch.float32, "final state")
+
+
+SMALL = [
+    # kind, dtype, B, T, H, dk, dv, C, h0
+    ("gdn", "f32", 2, 200, 2, 32, 48, 64, 0.1),
+    ("gdn", "f32", 1, 77, 3, 16, 16, 16, 0.0),
+    ("gdn", "bf16", 2, 333, 2, 128, 128, 64, 0.02),
+    ("gdn", "bf16", 1, 64, 2, 128, 128, 64, 0.02),
+    ("gdn", "bf16", 3, 5, 2, 128, 128, 64, 0.02),
+    ("gdn", "bf16", 1, 1, 1, 128, 128, 64, 0.02),
+    ("gdn", "bf16", 2, 130, 2, 64, 96, 32, 0.05),
+    ("gdn", "bf16", 1, 100, 2, 100, 72, 16, 0.0),
+    ("kda", "f32", 1, 150, 2, 32, 32, 32, 0.1),
+    ("kda", "bf16", 2, 200, 2, 128, 128, 64, 0.02),
+    ("kda", "bf16", 1, 70, 2, 64, 128, 16, 0.0),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "-".join(map(str, c)))
+def test_small_shapes(case):
+    kind, dt, B, T, H, dk, dv, C, h0 = case
+    x = W.chunk_inputs(_workload(kind, dt, dk, dv, C, h0), seed=1, B=B, T=T, H=H)
+    dtype = x["q"].dtype
+    o_ref, h_ref = oracle_on_heads(x)
+    for algo in _algos(x):
+        o, hT = _run(x, algo)
+        assert_close(o, o_ref, dtype, f"o [{algo}]")
+        assert_close(hT, h_ref, dtype, f"final state [{algo}]")
+
+
+def test_extreme_gates_and_betas():
+    # A up to 16 drives gamma^r to 0 within a chunk (a correct underflow, never NaN); beta near 0 and 1
+    x = W.chunk_inputs(W.config(1), seed=2, B=1, T=256, H=4)
+    x["g"] = torch.clamp(x["g"] * 4.0, min=-80.0)
+    x["beta"][..., 0] = 1e-6
+    x["beta"][..., 1] = 1.0 - 1e-6
+    o_ref, h_ref = oracle_on_heads(x)
+    for algo in _algos(x):
+        o, hT = _run(x, algo)
+        assert_close(o, o_ref, torch.bfloat16, f"o [{algo}]")
+        assert_close(hT, h_ref, torch.bfloat16, f"final state [{algo}]")
+
+
+def test_zero_length_input_keeps_initial_state():
+    x = W.chunk_inputs(W.config(1), seed=3, B=2, T=0, H=2)
+    for algo in _algos(x):
+        o, hT = _run(x, algo)
+        assert o.shape == (2, 0, 2, 128)
+        assert np.array_equal(hT, x["initial_state"].double().numpy())
+
+
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_packed_sequences_match_separate_runs_bitwise(kind):
+    lens = [130, 0, 64, 1, 200, 63, 65]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    x = W.chunk_inputs(_workload(kind, "bf16", 128, 128, 64, 0.02), seed=4, B=1, T=int(cu[-1]), H=3)
+    x["cu_seqlens"] = torch.from_numpy(cu)
+    x["initial_state"] = torch.randn(len(lens), 3, 128, 128, generator=torch.Generator().manual_seed(0)) * 0.02
+    for algo in _algos(x):
+        o, hT = _run(x, algo)
+        for n, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+            xn = {**x, "cu_seqlens": None, "initial_state": x["initial_state"][n:n + 1]}
+            for key in ("q", "k", "v", "g", "beta"):
+                xn[key] = x[key][:, a:b].contiguous()
+            on, hn = _run(xn, algo)
+            assert np.array_equal(o[:, a:b], on), (algo, n)
+            assert np.array_equal(hT[n], hn[0]), (algo, n)
+        # perturbing one sequence leaves every other sequence's outputs bitwise unchanged
+        x2 = {**x, "v": x["v"].clone()}
+        x2["v"][:, cu[4]:cu[5]] += 1.0
+        o2, h2 = _run(x2, algo)
+        keep = np.ones(int(cu[-1]), bool)
+        keep[cu[4]:cu[5]] = False
+        assert np.array_equal(o2[:, keep], o[:, keep]) and np.array_equal(np.delete(h2, 4, 0), np.delete(hT, 4, 0))
+        o_ref, h_ref = oracle_on_heads(x)
+        assert_close(o, o_ref, torch.bfloat16, f"o [{algo}]")
+        assert_close(hT, h_ref, torch.bfloat16, f"final state [{algo}]")
+
+
+def test_state_handoff_at_chunk_boundary_is_bitwise():
+    x = W.chunk_inputs(W.config(1), seed=5, B=1, T=320, H=2)
+    for algo in _algos(x):
+        o, hT = _run(x, algo)
+        T1 = 192
+        xa = {**x}
+        xb = {**x}
+        for key in ("q", "k", "v", "g", "beta"):
+            xa[key] = x[key][:, :T1].contiguous()
+            xb[key] = x[key][:, T1:].contiguous()
+        oa, ha = _run(xa, algo)
+        xb["initial_state"] = torch.from_numpy(ha).float()
+        ob, hb = _run(xb, algo)
+        assert np.array_equal(np.concatenate([oa, ob], axis=1), o) and np.array_equal(hb, hT)
+
+
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_bf16_output_is_the_rounded_fp32_output(kind):
+    # a bf16 o is the round-to-nearest-even of the same fp32 result, bit for bit
+    x = W.chunk_inputs(_workload(kind, "bf16", 128, 128, 64, 0.02), seed=7, B=2, T=150, H=2)
+    for algo in _algos(x):
+        o32, h32 = _run(x, algo)
+        o16, h16 = _run(x, algo, o_dtype=torch.bfloat16)
+        expect = torch.from_numpy(o32).float().to(torch.bfloat16).double().numpy()
+        assert np.array_equal(o16, expect) and np.array_equal(h16, h32)
+
+
+def test_kda_with_equal_channels_matches_gdn():
+    x = W.chunk_inputs(W.config(1), seed=6, B=1, T=200, H=2)
+    xk = {**x, "g": x["g"][..., None].expand(*x["g"].shape, 128).contiguous(), "gate_per_channel": True}
+    og, hg = _run(x, "generic")
+    ok, hk = _run(xk, "generic")
+    assert_close(ok, og, torch.bfloat16, "o")
+    assert_close(hk, hg, torch.bfloat16, "final state")
+
+
+# --- full-size workloads, in the launch configuration the benchmark times -------------------
+
+def test_full_config1_all_chains():
+    x = W.chunk_inputs(W.config(1), seed=0)
+    o_ref, h_ref = oracle_on_heads(x)
+    o, hT = _run(x, "auto")
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
+def test_full_config2_varlen_sampled_heads():
+    x = W.chunk_inputs(W.config(2), seed=0)
+    heads = [0, 9, 22, 31]
+    o_ref, h_ref = oracle_on_heads(x, heads)
+    o, hT = _run(x, "auto")
+    assert_close(o[:, :, heads], o_ref, torch.bfloat16, "o")
+    assert_close(hT[:, heads], h_ref, torch.bfloat16, "final state")
+
+
+def test_full_config3_kda_sampled_heads():
+    x = W.chunk_inputs(W.config(3), seed=0)
+    heads = [0, 13, 31]
+    o_ref, h_ref = oracle_on_heads(x, heads)
+    o, hT = _run(x, "auto")
+    assert_close(o[:, :, heads], o_ref, torch.bfloat16, "o")
+    assert_close(hT[:, heads], h_ref, torch.bfloat16, "final state")

@@ -1,0 +1,87 @@
+"""GPU parity of the decode step (gdn_recurrent_step) against the fp64 oracle.
+
+The decode step is the token recurrence, one token per call.  So a run of S
+steps must match the oracle on those S tokens:
+* every step's output;
+* the state after the last step.
+The full-size case has 256 sequences, 32 heads and d = 128, and runs all 1024
+steps.  There, the oracle follows a sample of (sequence, head) chains.
+"""
+import concurrent.futures as cf
+
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_gdn_gb300 as gdn
+import oracle
+from gated_delta_rule_gdn_gb300 import workloads as W
+from parity_util import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from gated_delta_rule_gdn_gb300 import build
+    build.build()
+    gdn.load()
+
+
+def _decode_and_compare(w: W.DecodeWorkload, steps: int, sample=None):
+    consts = W.decode_constants(w, seed=0)
+    state = consts["state"].cuda()
+    NH = w.N * w.H
+    idx = np.arange(NH) if sample is None else np.asarray(sample)
+    tidx = torch.as_tensor(idx)
+    h0s = consts["state"].reshape(NH, w.dk, w.dv)[tidx][:, None].clone()
+    kept = {key: [] for key in ("q", "k", "v", "g", "beta")}
+    outs = []
+    # inputs are drawn on host threads a few steps ahead; only the sampled chains are kept for the oracle
+    with cf.ThreadPoolExecutor(8) as ex:
+        pending = {s: ex.submit(W.decode_step_inputs, w, consts, s) for s in range(min(steps, 16))}
+        for s in range(steps):
+            x = pending.pop(s).result()
+            if s + 16 < steps:
+                pending[s + 16] = ex.submit(W.decode_step_inputs, w, consts, s + 16)
+            for key in kept:
+                kept[key].append(x[key].reshape(NH, -1)[tidx].clone())
+            d = {key: t.cuda() for key, t in x.items()}
+            o = gdn.gdn_recurrent_step(d["q"], d["k"], d["v"], d["g"], d["beta"], state, scale=w.scale)
+            outs.append(o.reshape(NH, w.dv)[tidx.cuda()].float().cpu())
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    # oracle: the sampled chains as independent sequences of T = steps tokens
+    q, k, v = (torch.stack(kept[key], dim=1)[:, :, None] for key in ("q", "k", "v"))
+    g, beta = (torch.stack(kept[key], dim=1)[:, :, :1] for key in ("g", "beta"))
+    o_ref, h_ref = oracle.recurrence(q, k, v, g, beta, w.scale, h0s)
+    o_gpu = torch.stack(outs, dim=1).double().numpy()
+    dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    for s in range(steps):
+        assert_close(o_gpu[:, s], o_ref[:, s, 0], dtype, f"o at step {s}")
+    st = state.reshape(NH, w.dk, w.dv)[tidx.cuda()].double().cpu().numpy()
+    assert_close(st, h_ref[:, 0], dtype, "state after the last step")
+
+
+@pytest.mark.parametrize("N,H,dk,dv,dtype", [(3, 2, 16, 8, "f32"), (4, 2, 128, 128, "f32"), (5, 3, 128, 128, "bf16"),
+                                             (2, 2, 64, 100, "bf16")])
+def test_small_decode(N, H, dk, dv, dtype):
+    _decode_and_compare(W.DecodeWorkload("t", N, H, dk, dv, 40, dtype=dtype), 40)
+
+
+def test_bf16_output_is_the_rounded_fp32_output():
+    w = W.DecodeWorkload("t", 8, 4, 128, 128, 1)
+    c = W.decode_constants(w, seed=1)
+    x = {k: v.cuda() for k, v in W.decode_step_inputs(w, c, 0).items()}
+    s32, s16 = c["state"].cuda(), c["state"].cuda()
+    o32 = gdn.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], s32, scale=w.scale)
+    o16 = gdn.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], s16, scale=w.scale,
+                                 o_dtype=torch.bfloat16)
+    assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(s16, s32)
+
+
+def test_full_decode_1024_steps_sampled_chains():
+    w = W.config(4)
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(w.N * w.H, size=64, replace=False))
+    _decode_and_compare(w, w.steps, sample=list(sample))
