@@ -1,15 +1,874 @@
-// Fused tcgen05/TMA chunk kernel (scalar gate): placeholder until the kernel lands.
+// Fused chunkwise gated delta rule forward on tcgen05 tensor cores (sm_103a): scalar gate, bf16 q/k/v,
+// d_k = d_v = 128, chunk C = 64, fp32 state, o in fp32 or bf16.
+//
+// The algorithm is the gated chunk form of "TileLang 实战：KDA 从零到一 -- Gated DeltaNet", §2.3
+// (paper eqs 11-12), organised as in "Gated Delta Network (GDN)", §4(b3)-(d): the S-independent
+// intra-chunk products, then the serial inter-chunk state pass.  Per chunk of C tokens, with G the
+// within-chunk cumulative log gate, gamma = exp(G), Gamma_ij = exp(G_i - G_j) (j <= i), and L valid rows:
+//   A    = diag(beta) (Gamma * K K^T), strictly lower        P = scale (Gamma * Q K^T), lower incl. diag
+//   T    = (I + A)^{-1}                                      (UT transform, blocked triangular inverse)
+//   W    = T diag(beta gamma) K      U  = T diag(beta) V     (WY pseudo-keys / pseudo-values)
+//   Q'   = scale diag(gamma) Q - P W U' = P U                (read side folded through T, S-independent)
+// and the serial pass over chunks, with h = S^T (d_k x d_v tile) kept in fp32 registers:
+//   Delta = U - W h                     (solved corrections, "V_new")
+//   O     = U' + Q' h                   (= scale gamma Q h + P Delta, the read of eq. 12)
+//   h    <- gamma_C h + Ktilde^T Delta  Ktilde = diag(exp(G_C - G)) K   (eq. 11)
+// The stacking [W; Q'] makes both S-dependent products one M = 128 MMA against h.
+//
+// One CTA owns one (sequence, head, d_v half of 64 columns) and walks the sequence's chunks in order.
+// Warp roles (288 threads):
+//   warp 0      TMA producer (K, Q, V tiles through a 2-stage ring; g and beta by plain loads), TMEM owner
+//   warps 1-4   "prep" warpgroup: everything that does not depend on h, one chunk ahead of the serial pass
+//   warps 5-8   "serial" warpgroup: the state pass; each thread keeps one row of h in registers
+// MMAs (tcgen05.mma kind::f16, fp32 accumulators in TMEM, one issuing thread per warpgroup):
+//   MMA0  D0 = [K; Q] K^T          M=128 N=64  K=128  bf16 operands straight from the TMA tiles
+//   MMA1  D1 = [I; P] T            M=128 N=64  K=64   -> [T; P T]
+//   MMA2  D2 = [T; PT] [beta gamma K | beta V]   M=128 N=192 K=64  -> [W | U ; P W | P U]
+//   MMA3  D3 = [W; Q'] h           M=128 N=64  K=128  (serial)
+//   MMA4  D4 = Ktilde^T Delta      M=128 N=64  K=64   (serial)
+// Internal operands are fp16 (11-bit significand): with bf16 operands the error of the state pass alone
+// exceeds the 2e-2 max-error bound the output is held to; the inputs' bf16 values convert exactly.
+// Decay exponents are differences masked before exp2, so no factor exceeds 1 (TileLang page §4.1).
+// Rows past a sequence's end get beta = 0 and g = 0 and are zeroed where they would enter a product, so
+// packed sequences give bit-identical results to separate runs.
+//
+// Every mbarrier wait is bounded (2 s of wall time).  A wait that gives up sets a status bit
+// (read by gdn_device_status), and its warpgroup skips the rest of its work while still passing every
+// named barrier, so the CTA drains, frees its TMEM and exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace gdn {
 
-const char* tc_chunk_unsupported_reason(const ChunkArgs&) { return "the tcgen05 kernel is not built yet"; }
+__device__ unsigned g_tc_status;
 
-cudaError_t launch_chunk_tc(const ChunkArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
 
-cudaError_t tc_read_and_clear_status(unsigned* value, bool) {
-    *value = 0;
-    return cudaSuccess;
+using namespace tc;
+
+constexpr int C = 64;        // chunk
+constexpr int DK = 128;
+constexpr int DV = 128;
+constexpr int DVT = 64;      // d_v columns per CTA
+constexpr int NTHREADS = 288;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_KQ = 0;                       // 2 stages x 32 KB: [K; Q] rows, 2 K-slabs of 16 KB
+constexpr uint32_t STAGE_KQ = 32768;
+constexpr uint32_t OFF_V = OFF_KQ + 2 * STAGE_KQ;    // 2 stages x 8 KB: V tile [64 tok][64 col]
+constexpr uint32_t STAGE_V = 8192;
+constexpr uint32_t OFF_A1 = OFF_V + 2 * STAGE_V;     // [I; P] then [T; PT], fp16 K-major 128 x 64
+constexpr uint32_t OFF_B1 = OFF_A1 + 16384;          // T, fp16 MN-major [j][n] 64 x 64
+constexpr uint32_t OFF_B2 = OFF_B1 + 8192;           // X = [beta gamma K | beta V], fp16 MN-major 64 x 192
+constexpr uint32_t OFF_WQ = OFF_B2 + 24576;          // [W; Q'], fp16 K-major 128 x 128
+constexpr uint32_t OFF_KT = OFF_WQ + 32768;          // Ktilde, fp16 MN-major [j][c] 64 x 128
+constexpr uint32_t OFF_H = OFF_KT + 16384;           // h, fp16 MN-major [d][n] 128 x 64
+constexpr uint32_t OFF_D = OFF_H + 16384;            // Delta, fp16 MN-major [j][n] 64 x 64
+constexpr uint32_t OFF_T32 = OFF_D + 8192;           // T in fp32, row stride 68 floats
+constexpr int TS = 68;
+constexpr uint32_t OFF_SMALL = OFF_T32 + 64 * TS * 4;
+// the fp32 A of the solve lives in the X buffer (X is built only after the solve)
+constexpr uint32_t OFF_AM = OFF_B2;
+constexpr uint32_t OFF_RT = OFF_B2 + 64 * TS * 4;   // 32 x 36 fp32 scratch of the solve
+static_assert(64 * TS * 4 + 32 * 36 * 4 <= 24576, "A and the solve scratch must fit in the X buffer");
+
+struct Small {
+    uint64_t full[2];        // producer -> prep: stage loaded (TMA tx + 32 producer lanes)
+    uint64_t empty[2];       // prep -> producer: stage free
+    uint64_t m0, m1, m2;     // prep MMA commits
+    uint64_t m3, m4;         // serial MMA commits
+    uint64_t prep_done;      // prep -> serial: [W; Q'], Ktilde, D2 ready for the chunk
+    uint64_t d2_free;        // serial -> prep: U, U' read out of TMEM
+    uint32_t tmem_base;
+    uint32_t pad;
+    float gbuf[2][C];        // stage: g (0 past the end)
+    float bbuf[2][C];        // stage: beta (0 past the end)
+    float lg[C];             // log2 of the within-chunk cumulative retention
+    float gam[C];            // gamma_j
+    float kdec[C];           // gamma_C / gamma_j
+    float info_gC[2];        // per-chunk gamma_C for the serial pass
+    int info_L[2];           // per-chunk valid rows
+};
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + sizeof(Small) + 1024;  // + alignment slack
+
+// TMEM columns
+constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_D2 = 128, TM_D3 = 320, TM_D4 = 384, TM_COLS = 512;
+
+struct TcParams {
+    const float* g;
+    const float* beta;
+    float scale;
+    const float* h0;
+    float* hT;
+    const int32_t* cu;
+    int n_seqs;
+    void* o;
+    int B, T, H;
+    int o_f32;
+};
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 16-byte shared-memory accesses through pointers into the shared array (the compiler emits STS/LDS and
+// schedules them freely; ordering against the async proxy comes from the explicit fences and barriers)
+__device__ __forceinline__ void st16(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+__device__ __forceinline__ uint4 ld16(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// Scaled copy of a row chunk of 8 bf16 values into 8 fp16 values (scale 0 writes exact zeros).
+__device__ __forceinline__ void copy_scaled_chunk(const uint8_t* src, uint8_t* dst, float s, bool zero) {
+    float f[8];
+    bf16x8_to_f32(ld16(src), f);
+    const uint32_t m = zero ? 0u : 0xFFFFFFFFu;     // exact zeros for rows past the sequence end
+    st16(dst, pack_h2(f[0] * s, f[1] * s) & m, pack_h2(f[2] * s, f[3] * s) & m, pack_h2(f[4] * s, f[5] * s) & m,
+         pack_h2(f[6] * s, f[7] * s) & m);
+}
+
+// 2^x by the hardware's ex2.approx (flush-to-zero): |relative error| ~2^-22; large negative x gives +0
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void set_status(unsigned bit) { atomicOr(&g_tc_status, bit); }
+
+// Resolve (sequence, head, half) for this CTA and the sequence's token range.
+struct Work {
+    int n, h, half;
+    long row0;   // first token row in the [B*T] dimension
+    int len;
+};
+
+__device__ Work resolve_work(const TcParams& p) {
+    Work w;
+    const int per_seq = p.H * 2;
+    int seq_rank = blockIdx.x / per_seq;
+    const int rem = blockIdx.x % per_seq;
+    w.h = rem / 2;
+    w.half = rem % 2;
+    if (p.cu) {
+        // longest sequences first (their chains are the longest serial paths); ties by index
+        int n = seq_rank;
+        if (p.n_seqs <= 32) {
+            // lane m ranks sequence m; the lane whose rank equals this CTA's slot names the sequence
+            const int lane = threadIdx.x & 31;
+            int rank = -1;
+            if (lane < p.n_seqs) {
+                const int lm = p.cu[lane + 1] - p.cu[lane];
+                rank = 0;
+                for (int m2 = 0; m2 < p.n_seqs; ++m2) {
+                    const int l2 = p.cu[m2 + 1] - p.cu[m2];
+                    rank += (l2 > lm) || (l2 == lm && m2 < lane);
+                }
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, rank == seq_rank);
+            if (hit) n = __ffs(hit) - 1;
+        }
+        long s0 = p.cu[n], s1 = p.cu[n + 1];
+        s0 = s0 < 0 ? 0 : (s0 > p.T ? p.T : s0);
+        s1 = s1 < s0 ? s0 : (s1 > p.T ? p.T : s1);
+        w.n = n;
+        w.row0 = s0;
+        w.len = (int)(s1 - s0);
+    } else {
+        w.n = seq_rank;
+        w.row0 = (long)seq_rank * p.T;
+        w.len = p.T;
+    }
+    return w;
+}
+
+// Blocked inverse of the unit lower-triangular (I + A), 64 x 64, by the 128 prep threads.
+// A (strictly lower) is in Am (fp32, row stride TS); T is written to the lower triangle of T32 (fp32, row
+// stride TS), whose upper triangle stays zero, so every product below can run over full, unrolled ranges.
+// Rt is a 32 x RS fp32 scratch tile for the intermediate products.
+// Level 0: the four 16 x 16 diagonal blocks by right-looking forward substitution, one column per thread.
+// Levels 1 and 2: T_ab = -T_aa (A_ab T_bb), first for the 16-wide then for the 32-wide off-diagonal block
+// (block rows of (I + A) T = I), as register-tiled products.
+constexpr int RS = 36;
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+__device__ void solve_unit_lower(const float* Am, float* T32, float* Rt, int t) {
+    if (t < 64) {
+        const int b = t >> 4, c = t & 15, o = 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+#pragma unroll
+            for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-Am[(o + r) * TS + o + j], x[j], x[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) T32[(o + r) * TS + o + c] = x[r];
+    }
+    named_bar(1, 128);
+    {   // level 1, stage 1: R_p = A[o+16..][o..o+15] T[o..o+15][o..o+15], o = 32 p
+        const int pr = t >> 6, r = (t & 63) >> 2, c0 = (t & 3) * 4, o = 32 * pr;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float a = Am[(o + 16 + r) * TS + o + k];
+            const float4 b = ld4(T32 + (o + k) * TS + o + c0);
+            a0 = fmaf(a, b.x, a0); a1 = fmaf(a, b.y, a1); a2 = fmaf(a, b.z, a2); a3 = fmaf(a, b.w, a3);
+        }
+        *reinterpret_cast<float4*>(Rt + (16 * pr + r) * RS + c0) = make_float4(a0, a1, a2, a3);
+    }
+    named_bar(1, 128);
+    {   // level 1, stage 2: T[o+16..][o..o+15] = -T[o+16..][o+16..] R_p
+        const int pr = t >> 6, r = (t & 63) >> 2, c0 = (t & 3) * 4, o = 32 * pr;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float a = T32[(o + 16 + r) * TS + o + 16 + k];
+            const float4 b = ld4(Rt + (16 * pr + k) * RS + c0);
+            a0 = fmaf(a, b.x, a0); a1 = fmaf(a, b.y, a1); a2 = fmaf(a, b.z, a2); a3 = fmaf(a, b.w, a3);
+        }
+        *reinterpret_cast<float4*>(T32 + (o + 16 + r) * TS + o + c0) = make_float4(-a0, -a1, -a2, -a3);
+    }
+    named_bar(1, 128);
+    const int r0 = (t >> 3) * 2, c0 = (t & 7) * 4;
+    {   // level 2, stage 1: R = A[32..63][0..31] T[0..31][0..31]
+        float acc[2][4] = {};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float x0 = Am[(32 + r0) * TS + k], x1 = Am[(33 + r0) * TS + k];
+            const float4 b = ld4(T32 + k * TS + c0);
+            acc[0][0] = fmaf(x0, b.x, acc[0][0]); acc[0][1] = fmaf(x0, b.y, acc[0][1]);
+            acc[0][2] = fmaf(x0, b.z, acc[0][2]); acc[0][3] = fmaf(x0, b.w, acc[0][3]);
+            acc[1][0] = fmaf(x1, b.x, acc[1][0]); acc[1][1] = fmaf(x1, b.y, acc[1][1]);
+            acc[1][2] = fmaf(x1, b.z, acc[1][2]); acc[1][3] = fmaf(x1, b.w, acc[1][3]);
+        }
+        *reinterpret_cast<float4*>(Rt + r0 * RS + c0) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+        *reinterpret_cast<float4*>(Rt + (r0 + 1) * RS + c0) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+    }
+    named_bar(1, 128);
+    {   // level 2, stage 2: T[32..63][0..31] = -T[32..63][32..63] R
+        float acc[2][4] = {};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float x0 = T32[(32 + r0) * TS + 32 + k], x1 = T32[(33 + r0) * TS + 32 + k];
+            const float4 b = ld4(Rt + k * RS + c0);
+            acc[0][0] = fmaf(x0, b.x, acc[0][0]); acc[0][1] = fmaf(x0, b.y, acc[0][1]);
+            acc[0][2] = fmaf(x0, b.z, acc[0][2]); acc[0][3] = fmaf(x0, b.w, acc[0][3]);
+            acc[1][0] = fmaf(x1, b.x, acc[1][0]); acc[1][1] = fmaf(x1, b.y, acc[1][1]);
+            acc[1][2] = fmaf(x1, b.z, acc[1][2]); acc[1][3] = fmaf(x1, b.w, acc[1][3]);
+        }
+        *reinterpret_cast<float4*>(T32 + (32 + r0) * TS + c0) = make_float4(-acc[0][0], -acc[0][1], -acc[0][2], -acc[0][3]);
+        *reinterpret_cast<float4*>(T32 + (33 + r0) * TS + c0) = make_float4(-acc[1][0], -acc[1][1], -acc[1][2], -acc[1][3]);
+    }
+    named_bar(1, 128);
+}
+
+
+// 8 fp32 values to fp16, one 16-byte shared store
+__device__ __forceinline__ void st_h8(uint8_t* p, const float* f) {
+    st16(p, pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+}
+
+// Epilogue of D0 = [K; Q] K^T.  Rows 0-63 (token i): A[i][j] = beta_i 2^(lg_i - lg_j) (K K^T)_ij for j < i, in
+// fp32 for the solve, plus row i of the identity in [I; P].  Rows 64-127 (token i = row - 64):
+// P[i][j] = scale 2^(lg_i - lg_j) (Q K^T)_ij for j <= i, in fp16 in [I; P].  Column blocks wholly above the
+// diagonal for every row of the warp are skipped (warp-uniform); the solve never reads A above the diagonal.
+__device__ __forceinline__ void epilogue_kkt(uint32_t tl, int row, int q4, const Small& S, int s, float scale,
+                                             float* Am, uint8_t* a1) {
+    uint32_t r[4][16];
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + TM_D0 + cb * 16, r[cb]);
+    tmem_ld_wait();
+    const int i = row & 63;
+    const int imax = 32 * (q4 & 1) + 31;
+    const float li = S.lg[i];
+    if (row < 64) {
+        const float bi = S.bbuf[s][i];
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            if (cb * 16 > imax) break;
+            float v[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int j = cb * 16 + q;
+                const float e = ex2(li - S.lg[j]);
+                v[q] = (j < i) ? bi * e * __uint_as_float(r[cb][q]) : 0.f;
+            }
+            float4* dst = reinterpret_cast<float4*>(Am + i * TS + cb * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+        const uint32_t one = (i & 1) ? 0x3C000000u : 0x00003C00u;     // fp16 1.0 in the low or high half
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            const bool here = (i >> 3) == c8;
+            const int qw = (i & 7) >> 1;
+            st16(a1 + sw128_off(row, c8 * 8), here && qw == 0 ? one : 0u, here && qw == 1 ? one : 0u,
+                 here && qw == 2 ? one : 0u, here && qw == 3 ? one : 0u);
+        }
+    } else {
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            float v[16];
+            if (cb * 16 > imax) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[q] = 0.f;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int j = cb * 16 + q;
+                    const float e = ex2(li - S.lg[j]);
+                    v[q] = (j <= i) ? scale * e * __uint_as_float(r[cb][q]) : 0.f;
+                }
+            }
+            st_h8(a1 + sw128_off(row, cb * 16), v);
+            st_h8(a1 + sw128_off(row, cb * 16 + 8), v + 8);
+        }
+    }
+}
+
+// Epilogue of D2 columns 0-127: W rows (0-63) and Q' = scale gamma Q - P W rows (64-127) to fp16 into [W; Q']
+// (K-major, two 64-column slabs).  Q comes from the stage's TMA tile, rows 64-127 of each slab.
+__device__ __forceinline__ void epilogue_wq(uint32_t tl, int row, const Small& S, float scale, const uint8_t* kqp,
+                                            uint8_t* wq) {
+    const int i = row & 63;
+    const float qs = scale * S.gam[i];
+#pragma unroll
+    for (int slab = 0; slab < 2; ++slab) {
+        uint32_t r[4][16];
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + TM_D2 + slab * 64 + cb * 16, r[cb]);
+        tmem_ld_wait();
+        if (row < 64) {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float f[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
+                st_h8(wq + slab * 16384 + sw128_off(row, c8 * 8), f);
+            }
+        } else {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float qv[8], f[8];
+                bf16x8_to_f32(ld16(kqp + slab * 16384 + sw128_off(row, c8 * 8)), qv);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] = fmaf(qs, qv[q], -__uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]));
+                st_h8(wq + slab * 16384 + sw128_off(row, c8 * 8), f);
+            }
+        }
+    }
+}
+
+template <bool O_F32>
+__global__ void __launch_bounds__(NTHREADS, 1)
+chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // align by offsetting the shared array itself, so the compiler keeps every access in the shared space
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    Small& S = *reinterpret_cast<Small*>(smem + OFF_SMALL);
+    float* Am = reinterpret_cast<float*>(smem + OFF_AM);
+    float* T32 = reinterpret_cast<float*>(smem + OFF_T32);
+    float* Rt = reinterpret_cast<float*>(smem + OFF_RT);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const Work w = resolve_work(p);
+    const int n_chunks = (w.len + C - 1) / C;
+
+    if (warp == 0) {
+        tmem_alloc(&S.tmem_base, TM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        mbar_init(&S.full[0], 33);
+        mbar_init(&S.full[1], 33);
+        mbar_init(&S.empty[0], 1);
+        mbar_init(&S.empty[1], 1);
+        mbar_init(&S.m0, 1);
+        mbar_init(&S.m1, 1);
+        mbar_init(&S.m2, 1);
+        mbar_init(&S.m3, 1);
+        mbar_init(&S.m4, 1);
+        mbar_init(&S.prep_done, 1);
+        mbar_init(&S.d2_free, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        prefetch_tmap(&tmap_q);
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+        bool ok = true;
+        int issued = 0;
+        for (int t = 0; t < n_chunks; ++t) {
+            const int s = t & 1;
+            if (t >= 2 && ok) ok = mbar_wait(&S.empty[s], ((t >> 1) - 1) & 1, kWaitNs);
+            if (!ok) { if (lane == 0) set_status(1u); break; }
+            const int row = (int)(w.row0 + (long)t * C);
+            const int L = min(C, w.len - t * C);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&S.full[s], STAGE_KQ + STAGE_V);
+                uint8_t* kq = smem + OFF_KQ + s * STAGE_KQ;
+                tma_load_3d(kq, &tmap_k, &S.full[s], 0, w.h, row);
+                tma_load_3d(kq + 8192, &tmap_q, &S.full[s], 0, w.h, row);
+                tma_load_3d(kq + 16384, &tmap_k, &S.full[s], 64, w.h, row);
+                tma_load_3d(kq + 16384 + 8192, &tmap_q, &S.full[s], 64, w.h, row);
+                tma_load_3d(smem + OFF_V + s * STAGE_V, &tmap_v, &S.full[s], w.half * DVT, w.h, row);
+            }
+            for (int r = lane; r < C; r += 32) {
+                const size_t tok = (size_t)(row + r) * p.H + w.h;
+                S.gbuf[s][r] = r < L ? p.g[tok] : 0.f;
+                S.bbuf[s][r] = r < L ? p.beta[tok] : 0.f;
+            }
+            mbar_arrive(&S.full[s]);
+            issued = t + 1;
+        }
+        // drain: the last stage issued must have landed before the CTA can exit
+        if (issued > 0) {
+            const int t = issued - 1;
+            if (!mbar_wait(&S.full[t & 1], (t >> 1) & 1, kWaitNs) && lane == 0) set_status(2u);
+        }
+    } else if (warp <= 4) {
+        // ------------------------------------------------------------ prep warpgroup
+        const int t128 = tid - 32;                     // 0..127
+        const int q4 = warp & 3;                       // TMEM lane quarter of this warp
+        const int row = 32 * q4 + lane;                // TMEM lane this thread reads
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        const bool leader = (t128 == 96);              // warp 4 lane 0
+        const int jrow = t128 & 63, hc = t128 >> 6;    // (row, column half) for the elementwise builds
+        bool ok = true;
+        const float LOG2E = 1.4426950408889634f;
+        for (int e = t128; e < 64 * TS; e += 128) T32[e] = 0.f;   // the upper triangle stays zero
+        named_bar(1, 128);
+        for (int t = 0; t < n_chunks; ++t) {
+            const int s = t & 1;
+            const int L = min(C, w.len - t * C);
+            const uint32_t kq = sbase + OFF_KQ + s * STAGE_KQ;
+            uint8_t* kqp = smem + OFF_KQ + s * STAGE_KQ;
+            uint8_t* vsp = smem + OFF_V + s * STAGE_V;
+            if (ok) ok = mbar_wait(&S.full[s], (t >> 1) & 1, kWaitNs);
+            if (!ok && t128 == 0) set_status(4u);
+            // MMA0: D0 = [K; Q] K^T
+            if (ok && leader) {
+                tc_fence_after();
+                const uint32_t id = idesc_f16(128, 64, true, false, false);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t a = kq + (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_f16(tmem + TM_D0, sdesc(a, 16, 1024), sdesc(a, 16, 1024), id, ks > 0);
+                }
+                mma_commit(&S.m0);
+            }
+            // gate prefix (warp 1): log2 of the cumulative retention, gamma, gamma_C / gamma
+            if (warp == 1) {
+                const float g0 = S.gbuf[s][2 * lane], g1 = S.gbuf[s][2 * lane + 1];
+                float x = g0 + g1;
+#pragma unroll
+                for (int m = 1; m < 32; m <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, m);
+                    if (lane >= m) x += y;
+                }
+                const float G1 = x * LOG2E, G0 = (x - g1) * LOG2E;
+                S.lg[2 * lane] = G0;
+                S.lg[2 * lane + 1] = G1;
+                const float Glast = __shfl_sync(0xffffffffu, G1, 31);   // rows past L add 0
+                S.gam[2 * lane] = ex2(G0);
+                S.gam[2 * lane + 1] = ex2(G1);
+                S.kdec[2 * lane] = ex2(Glast - G0);
+                S.kdec[2 * lane + 1] = ex2(Glast - G1);
+                if (lane == 31) {
+                    S.info_gC[s] = ex2(Glast);
+                    S.info_L[s] = L;
+                }
+            }
+            named_bar(1, 128);
+            // epilogue 0: A (rows 0-63) to fp32 for the solve, P (rows 64-127) and the identity rows to A1
+            if (ok) ok = mbar_wait(&S.m0, t & 1, kWaitNs);
+            if (!ok && t128 == 0) set_status(8u);
+            tc_fence_after();
+            if (ok) epilogue_kkt(tl, row, q4, S, s, p.scale, Am, smem + OFF_A1);
+            tc_fence_before();
+            named_bar(1, 128);
+            // UT transform: T = (I + A)^{-1}
+            if (ok) solve_unit_lower(Am, T32, Rt, t128);
+            else { named_bar(1, 128); named_bar(1, 128); named_bar(1, 128); named_bar(1, 128); named_bar(1, 128); }
+            // T to fp16, MN-major [j][n] (operand B of MMA1)
+            if (ok) {
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int e = t128 + 128 * it, j = e >> 3, c8 = e & 7;
+                    const float4 x0 = ld4(T32 + j * TS + c8 * 8), x1 = ld4(T32 + j * TS + c8 * 8 + 4);
+                    const float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    float g[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) g[q] = (c8 * 8 + q <= j) ? f[q] : 0.f;
+                    st_h8(smem + OFF_B1 + sw128_off(j, c8 * 8), g);
+                }
+            }
+            fence_async_smem();
+            named_bar(1, 128);
+            // MMA1: D1 = [I; P] T
+            if (ok && leader) {
+                tc_fence_after();
+                const uint32_t id = idesc_f16(128, 64, false, false, true);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tmem + TM_D1, sdesc(sbase + OFF_A1 + ks * 32, 16, 1024),
+                            sdesc(sbase + OFF_B1 + ks * 2048, 8192, 1024), id, ks > 0);
+                mma_commit(&S.m1);
+            }
+            // X = [beta gamma K | beta V] (operand B of MMA2), fp16 MN-major [j][n], 3 atoms of 64 columns.
+            // Thread (jrow, hc): chunk columns 12 hc .. 12 hc + 11 of row jrow (K slab 0, K slab 1, V).
+            if (ok) {
+                const bool zero = jrow >= L;
+                const float sk = S.bbuf[s][jrow] * S.gam[jrow], sv = S.bbuf[s][jrow];
+                if (hc == 0) {
+#pragma unroll
+                    for (int c = 0; c < 12; ++c) {
+                        const uint32_t o8 = sw128_off(jrow, (c & 7) * 8);
+                        copy_scaled_chunk(kqp + (c >> 3) * 16384 + o8, smem + OFF_B2 + (c >> 3) * 8192 + o8, sk, zero);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 12; c < 16; ++c) {
+                        const uint32_t o8 = sw128_off(jrow, (c & 7) * 8);
+                        copy_scaled_chunk(kqp + 16384 + o8, smem + OFF_B2 + 8192 + o8, sk, zero);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t o8 = sw128_off(jrow, c * 8);
+                        copy_scaled_chunk(vsp + o8, smem + OFF_B2 + 2 * 8192 + o8, sv, zero);
+                    }
+                }
+            }
+            // epilogue 1: [T; PT] to fp16 into A1 (operand A of MMA2)
+            if (ok) ok = mbar_wait(&S.m1, t & 1, kWaitNs);
+            if (!ok && t128 == 0) set_status(16u);
+            tc_fence_after();
+            if (ok) {
+                uint32_t r[4][16];
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + TM_D1 + cb * 16, r[cb]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float f[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
+                    st_h8(smem + OFF_A1 + sw128_off(row, c8 * 8), f);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_bar(1, 128);
+            // MMA2: D2 = [T; PT] X, once the serial pass has read U, U' of the previous chunk
+            if (ok && leader) {
+                if (t > 0) ok = mbar_wait(&S.d2_free, (t - 1) & 1, kWaitNs);
+                if (!ok) set_status(32u);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t id = idesc_f16(128, 192, false, false, true);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tmem + TM_D2, sdesc(sbase + OFF_A1 + ks * 32, 16, 1024),
+                                sdesc(sbase + OFF_B2 + ks * 2048, 8192, 1024), id, ks > 0);
+                    mma_commit(&S.m2);
+                }
+            }
+            // Ktilde = diag(gamma_C / gamma) K (operand A of MMA4), once MMA4 of the previous chunk is done.
+            // Thread (jrow, hc): the 8 chunks of K slab hc of row jrow.
+            if (ok && t > 0) ok = mbar_wait(&S.m4, (t - 1) & 1, kWaitNs);
+            if (!ok && t128 == 0) set_status(64u);
+            if (ok) {
+                const bool zero = jrow >= L;
+                const float sd = S.kdec[jrow];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t o8 = sw128_off(jrow, c * 8);
+                    copy_scaled_chunk(kqp + hc * 16384 + o8, smem + OFF_KT + hc * 8192 + o8, sd, zero);
+                }
+            }
+            // epilogue 2: W (rows 0-63) and Q' = scale gamma Q - P W (rows 64-127) into [W; Q'], once MMA3 of the
+            // previous chunk has consumed the buffer
+            named_bar(1, 128);   // the leader's MMA2 issue precedes every thread's wait on m2
+            if (ok && t > 0) ok = mbar_wait(&S.m3, (t - 1) & 1, kWaitNs);
+            if (ok) ok = mbar_wait(&S.m2, t & 1, kWaitNs);
+            if (!ok && t128 == 0) set_status(128u);
+            tc_fence_after();
+            if (ok) epilogue_wq(tl, row, S, p.scale, kqp, smem + OFF_WQ);
+            fence_async_smem();
+            tc_fence_before();
+            named_bar(1, 128);
+            if (t128 == 0) {
+                mbar_arrive(&S.empty[s]);      // the stage's K, Q, V, g, beta are no longer read
+                mbar_arrive(&S.prep_done);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ serial warpgroup
+        // Warps with TMEM lane quarters 0 and 1 own the Delta rows (tokens 0-63) of D3; the other two own the
+        // output rows.  The Delta warps issue MMA4 as soon as Delta is in shared memory.
+        const int t128 = tid - 160;
+        const int q4 = warp & 3;
+        const int row = 32 * q4 + lane;                // TMEM lane: token (D3 rows) and d_k row (D4 rows)
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        const bool leader = (t128 == 96);              // warp 8 lane 0 (quarter 0, a Delta warp)
+        const bool delta_warp = q4 < 2;
+        bool ok = true;
+        const size_t sidx = ((size_t)w.n * p.H + w.h) * DK * DV + (size_t)row * DV + w.half * DVT;
+        float hreg[DVT];
+#pragma unroll
+        for (int q = 0; q < DVT / 4; ++q) {
+            float4 x = p.h0 ? reinterpret_cast<const float4*>(p.h0 + sidx)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            hreg[4 * q] = x.x; hreg[4 * q + 1] = x.y; hreg[4 * q + 2] = x.z; hreg[4 * q + 3] = x.w;
+        }
+        // h to fp16, MN-major [d][n] (operand B of MMA3)
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + OFF_H + sw128_off(row, c8 * 8), hreg + c8 * 8);
+        fence_async_smem();
+        named_bar(2, 128);
+        for (int t = 0; t < n_chunks; ++t) {
+            const int s = t & 1;
+            if (ok) ok = mbar_wait(&S.prep_done, t & 1, kWaitNs);
+            if (!ok && t128 == 0) set_status(256u);
+            const int L = S.info_L[s];
+            const float gC = S.info_gC[s];
+            // MMA3: D3 = [W; Q'] h
+            if (ok && leader) {
+                tc_fence_after();
+                const uint32_t id = idesc_f16(128, 64, false, false, true);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_f16(tmem + TM_D3, sdesc(sbase + OFF_WQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                            sdesc(sbase + OFF_H + ks * 2048, 1024, 1024), id, ks > 0);
+                mma_commit(&S.m3);
+            }
+            if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
+            if (!ok && t128 == 0) set_status(512u);
+            tc_fence_after();
+            const int i = row - 64;
+            const bool store_o = !delta_warp && i < L;
+            const size_t orow = ((size_t)(w.row0 + (long)t * C + (row & 63)) * p.H + w.h) * DV + w.half * DVT;
+            // two passes of 32 columns keep the live TMEM tiles small (h stays in registers throughout)
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+                uint32_t a[2][16], u[2][16];
+                if (ok) {
+#pragma unroll
+                    for (int cb = 0; cb < 2; ++cb) {
+                        tmem_ld16(tl + TM_D3 + hp * 32 + cb * 16, a[cb]);
+                        tmem_ld16(tl + TM_D2 + 128 + hp * 32 + cb * 16, u[cb]);
+                    }
+                    tmem_ld_wait();
+                }
+                if (ok && delta_warp) {
+                    // Delta = U - W h (token rows 0-63) to fp16 MN-major [j][n] (operand B of MMA4)
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float f[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int k = (c8 & 1) * 8 + q;
+                            f[q] = __uint_as_float(u[c8 >> 1][k]) - __uint_as_float(a[c8 >> 1][k]);
+                        }
+                        st_h8(smem + OFF_D + sw128_off(row, hp * 32 + c8 * 8), f);
+                    }
+                } else if (ok && store_o) {
+                    // O = U' + Q' h (token rows 64-127) to HBM
+                    float f[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(u[k >> 4][k & 15]) + __uint_as_float(a[k >> 4][k & 15]);
+                    if (O_F32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + hp * 32);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow + hp * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * q + 2 * m], f[8 * q + 2 * m + 1]);
+                                pk[m] = *reinterpret_cast<uint32_t*>(&b2);
+                            }
+                            dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                }
+            }
+            if (delta_warp) {
+                fence_async_smem();
+                tc_fence_before();
+                named_bar(3, 64);
+                // MMA4: D4 = Ktilde^T Delta
+                if (ok && leader) {
+                    tc_fence_after();
+                    const uint32_t id = idesc_f16(128, 64, false, true, true);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tmem + TM_D4, sdesc(sbase + OFF_KT + ks * 2048, 8192, 1024),
+                                sdesc(sbase + OFF_D + ks * 2048, 1024, 1024), id, ks > 0);
+                    mma_commit(&S.m4);
+                }
+            }
+            tc_fence_before();
+            named_bar(2, 128);
+            if (ok && leader) mbar_arrive(&S.d2_free);    // U and U' have been read out of TMEM
+            if (ok) ok = mbar_wait(&S.m4, t & 1, kWaitNs);
+            if (!ok && t128 == 0) set_status(1024u);
+            tc_fence_after();
+            // epilogue 2: h <- gamma_C h + Ktilde^T Delta; fp16 copy for the next MMA3
+            if (ok) {
+                uint32_t r[4][16];
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + TM_D4 + cb * 16, r[cb]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 64; ++k) hreg[k] = fmaf(gC, hreg[k], __uint_as_float(r[k >> 4][k & 15]));
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + OFF_H + sw128_off(row, c8 * 8), hreg + c8 * 8);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_bar(2, 128);
+        }
+        if (p.hT && ok) {
+#pragma unroll
+            for (int q = 0; q < DVT / 4; ++q)
+                reinterpret_cast<float4*>(p.hT + sidx)[q] =
+                    make_float4(hreg[4 * q], hreg[4 * q + 1], hreg[4 * q + 2], hreg[4 * q + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [rows][H][d] bf16 tensor, box = 64 d-elements x 1 head x 64 rows, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, long rows, int H, int d) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool device_is_sm100_family() {
+    int dev = 0, major = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    return major == 10;
+}
+
+}  // namespace
+
+const char* tc_chunk_unsupported_reason(const ChunkArgs& a) {
+    if (a.per_channel) return "per-channel (KDA) gates use another kernel";
+    if (!a.bf16) return "q, k, v must be bf16";
+    if (a.dk != DK || a.dv != DV) return "d_k and d_v must be 128";
+    if (a.C != C) return "chunk_size must be 64";
+    auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0; };
+    if (!al16(a.q) || !al16(a.k) || !al16(a.v) || !al16(a.o) || (a.h0 && !al16(a.h0)) || (a.hT && !al16(a.hT)))
+        return "tensors must be 16-byte aligned";
+    return nullptr;
+}
+
+cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s) {
+    const long ctas = (long)a.N() * a.H * 2;
+    if (ctas == 0) return cudaSuccess;
+    if (!device_is_sm100_family()) return cudaErrorNoKernelImageForDevice;
+    const long rows = (long)a.B * a.T;
+    if (rows == 0) {
+        // no tokens: the final state is the initial state
+        if (a.hT) {
+            const size_t bytes = (size_t)a.N() * a.H * DK * DV * sizeof(float);
+            return a.h0 ? cudaMemcpyAsync(a.hT, a.h0, bytes, cudaMemcpyDeviceToDevice, s)
+                        : cudaMemsetAsync(a.hT, 0, bytes, s);
+        }
+        return cudaSuccess;
+    }
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.q, rows, a.H, DK) || !make_map(&mk, a.k, rows, a.H, DK) || !make_map(&mv, a.v, rows, a.H, DV))
+        return cudaErrorInvalidValue;
+    TcParams p{a.g, a.beta, a.scale, a.h0, a.hT, a.cu, a.n_seqs, a.o, a.B, a.T, a.H, a.o_f32};
+    cudaError_t e;
+    if (a.o_f32) {
+        e = cudaFuncSetAttribute(chunk_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        chunk_tc_kernel<true><<<(unsigned)ctas, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+    } else {
+        e = cudaFuncSetAttribute(chunk_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        chunk_tc_kernel<false><<<(unsigned)ctas, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t tc_read_and_clear_status(unsigned* value, bool clear) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(value, g_tc_status, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    if (clear && *value) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(unsigned));
+    }
+    return e;
 }
 
 }  // namespace gdn

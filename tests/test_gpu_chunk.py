@@ -28,9 +28,15 @@ def _lib():
     gdn.load()
 
 
-def _tc_fits(x, dtype):
-    q = x["q"]
-    return dtype == torch.bfloat16 and q.shape[-1] == 128 and x["v"].shape[-1] == 128 and x["chunk_size"] == 64
+def _tc_fits(x):
+    """True if the library's tcgen05 kernel accepts this problem (asked through gdn_chunk_plan)."""
+    B, T, H, dk = x["q"].shape
+    try:
+        gdn.chunk_plan(x["gate_per_channel"], B, T, H, dk, x["v"].shape[-1], x["chunk_size"], x["q"].dtype,
+                       x["cu_seqlens"] is not None, "tcgen05")
+        return True
+    except gdn.GdnError:
+        return False
 
 
 def _run(x, algo="auto", out_final=True, o_dtype=torch.float32):
@@ -45,7 +51,7 @@ def _run(x, algo="auto", out_final=True, o_dtype=torch.float32):
 
 
 def _algos(x):
-    return ["generic", "tcgen05"] if _tc_fits(x, x["q"].dtype) else ["generic"]
+    return ["generic", "tcgen05"] if _tc_fits(x) else ["generic"]
 
 
 def _workload(kind, dtype, dk, dv, C, h0_std):
@@ -174,6 +180,11 @@ def test_kda_with_equal_channels_matches_gdn():
 
 
 # --- full-size workloads, in the launch configuration the benchmark times -------------------
+
+def test_benchmark_workload_runs_the_tcgen05_kernel():
+    w = W.config(1)
+    assert gdn.chunk_plan(False, w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16) == "tcgen05"
+
 
 def test_full_config1_all_chains():
     x = W.chunk_inputs(W.config(1), seed=0)
