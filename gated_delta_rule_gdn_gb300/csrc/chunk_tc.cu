@@ -16,10 +16,12 @@
 // The stacking [W; Q'] makes both S-dependent products one M = 128 MMA against h.
 //
 // One CTA owns one (sequence, head, d_v half of 64 columns) and walks the sequence's chunks in order.
-// Warp roles (288 threads):
-//   warp 0      TMA producer (K, Q, V tiles through a 2-stage ring; g and beta by plain loads), TMEM owner
-//   warps 1-4   "prep" warpgroup: everything that does not depend on h, one chunk ahead of the serial pass
-//   warps 5-8   "serial" warpgroup: the state pass; each thread keeps one row of h in registers
+// Warp roles (384 threads; 12 warps = 3 per SM sub-partition, so each thread can hold up to 168 registers):
+//   warps 0-7   "prep" (two warpgroups, 256 threads): everything that does not depend on h, one chunk ahead of
+//               the serial pass; the two warps that share a TMEM lane quarter split the columns of each row.
+//               Warp 2 also loads the inputs: at the end of chunk t it issues the TMA loads of chunk t + 2 into
+//               the stage chunk t has released (2-stage ring), and reads g and beta into registers.
+//   warps 8-11  "serial" warpgroup: the state pass; each thread keeps one row of h in registers
 // MMAs (tcgen05.mma kind::f16, fp32 accumulators in TMEM, one issuing thread per warpgroup):
 //   MMA0  D0 = [K; Q] K^T          M=128 N=64  K=128  bf16 operands straight from the TMA tiles
 //   MMA1  D1 = [I; P] T            M=128 N=64  K=64   -> [T; P T]
@@ -60,7 +62,8 @@ constexpr int C = 64;        // chunk
 constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr int DVT = 64;      // d_v columns per CTA
-constexpr int NTHREADS = 288;
+constexpr int NTHREADS = 384;
+constexpr int NPREP = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // shared memory map (bytes from a 1024-aligned base)
@@ -84,26 +87,26 @@ constexpr uint32_t OFF_RT = OFF_B2 + 64 * TS * 4;   // 32 x 36 fp32 scratch of t
 static_assert(64 * TS * 4 + 32 * 36 * 4 <= 24576, "A and the solve scratch must fit in the X buffer");
 
 struct Small {
-    uint64_t full[2];        // producer -> prep: stage loaded (TMA tx + 32 producer lanes)
-    uint64_t empty[2];       // prep -> producer: stage free
+    uint64_t full[2];        // stage loaded (TMA transaction bytes)
     uint64_t m0, m1, m2;     // prep MMA commits
     uint64_t m3, m4;         // serial MMA commits
     uint64_t prep_done;      // prep -> serial: [W; Q'], Ktilde, D2 ready for the chunk
     uint64_t d2_free;        // serial -> prep: U, U' read out of TMEM
     uint32_t tmem_base;
     uint32_t pad;
-    float gbuf[2][C];        // stage: g (0 past the end)
-    float bbuf[2][C];        // stage: beta (0 past the end)
-    float lg[C];             // log2 of the within-chunk cumulative retention
-    float gam[C];            // gamma_j
-    float kdec[C];           // gamma_C / gamma_j
-    float info_gC[2];        // per-chunk gamma_C for the serial pass
-    int info_L[2];           // per-chunk valid rows
+    float gbuf[2][C];        // per stage: g (0 past the end)
+    float bbuf[2][C];        // per stage: beta (0 past the end)
+    float lg[2][C];          // per chunk parity: log2 of the within-chunk cumulative retention
+    float gam[2][C];         // gamma_j
+    float kdec[2][C];        // gamma_C / gamma_j
+    float info_gC[4];        // per-chunk gamma_C for the serial pass (4 slots: written two chunks ahead)
+    int info_L[4];           // per-chunk valid rows
 };
 constexpr uint32_t SMEM_BYTES = OFF_SMALL + sizeof(Small) + 1024;  // + alignment slack
 
 // TMEM columns
-constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_D2 = 128, TM_D3 = 320, TM_D4 = 384, TM_COLS = 512;
+// D0 is double-buffered (columns 0 and 64) so MMA0 of the next chunk can run ahead
+constexpr uint32_t TM_D0 = 0, TM_D1 = 128, TM_D2 = 192, TM_D3 = 384, TM_D4 = 448, TM_COLS = 512;
 
 struct TcParams {
     const float* g;
@@ -209,16 +212,112 @@ __device__ Work resolve_work(const TcParams& p) {
 
 // Blocked inverse of the unit lower-triangular (I + A), 64 x 64, by the 128 prep threads.
 // A (strictly lower) is in Am (fp32, row stride TS); T is written to the lower triangle of T32 (fp32, row
-// stride TS), whose upper triangle stays zero, so every product below can run over full, unrolled ranges.
+// stride TS), whose upper triangle stays zero, so every product below can run over full tiles.
 // Rt is a 32 x RS fp32 scratch tile for the intermediate products.
-// Level 0: the four 16 x 16 diagonal blocks by right-looking forward substitution, one column per thread.
-// Levels 1 and 2: T_ab = -T_aa (A_ab T_bb), first for the 16-wide then for the 32-wide off-diagonal block
-// (block rows of (I + A) T = I), as register-tiled products.
+// Level 0: the four 16 x 16 diagonal blocks by right-looking forward substitution in fp32, one column per
+// thread.  Levels 1 and 2: T_ab = -T_aa (A_ab T_bb), first for the 16-wide then for the 32-wide off-diagonal
+// block (block rows of (I + A) T = I), as warp-level tensor-core products (mma.sync m16n8k8, TF32 inputs,
+// fp32 accumulation): these tiles are far below the 64-row minimum of tcgen05.
 constexpr int RS = 36;
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-__device__ void solve_unit_lower(const float* Am, float* T32, float* Rt, int t) {
-    if (t < 64) {
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// d (16 x 8, fp32) += A (16 x 8) B (8 x 8); A and B are fp32 row-major tiles in shared memory.
+// Fragment ownership (lane = 4 g + t): A rows g, g + 8 and columns t, t + 4; B rows t, t + 4 and column g;
+// d rows g, g + 8 and columns 2 t, 2 t + 1.
+__device__ __forceinline__ void mma_tile_tf32(float (&d)[4], const float* A, int lda, const float* B, int ldb,
+                                              int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t a0 = to_tf32(A[g * lda + t]), a1 = to_tf32(A[(g + 8) * lda + t]);
+    const uint32_t a2 = to_tf32(A[g * lda + t + 4]), a3 = to_tf32(A[(g + 8) * lda + t + 4]);
+    const uint32_t b0 = to_tf32(B[t * ldb + g]), b1 = to_tf32(B[(t + 4) * ldb + g]);
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void st_tile(float* D, int ldd, const float (&d)[4], int lane, float sgn) {
+    const int g = lane >> 2, t = lane & 3;
+    D[g * ldd + 2 * t] = sgn * d[0];
+    D[g * ldd + 2 * t + 1] = sgn * d[1];
+    D[(g + 8) * ldd + 2 * t] = sgn * d[2];
+    D[(g + 8) * ldd + 2 * t + 1] = sgn * d[3];
+}
+
+
+// Loads of one chunk's inputs.  K and Q arrive as 2 x 2 boxes of 64 tokens x 64 columns into the rows 0-63 / 64-127
+// of the two K-slabs of the stage; the V box is this CTA's 64 columns.  All transaction bytes count on full[s].
+__device__ __forceinline__ void issue_stage(uint8_t* smem, Small& S, const CUtensorMap* mq, const CUtensorMap* mk,
+                                            const CUtensorMap* mv, const Work& w, int t, int lane) {
+    if (lane != 0) return;
+    const int s = t & 1;
+    const int row = (int)(w.row0 + (long)t * C);
+    mbar_arrive_expect_tx(&S.full[s], STAGE_KQ + STAGE_V);
+    uint8_t* kq = smem + OFF_KQ + s * STAGE_KQ;
+    tma_load_3d(kq, mk, &S.full[s], 0, w.h, row);
+    tma_load_3d(kq + 8192, mq, &S.full[s], 0, w.h, row);
+    tma_load_3d(kq + 16384, mk, &S.full[s], 64, w.h, row);
+    tma_load_3d(kq + 16384 + 8192, mq, &S.full[s], 64, w.h, row);
+    tma_load_3d(smem + OFF_V + s * STAGE_V, mv, &S.full[s], w.half * DVT, w.h, row);
+}
+// g and beta of chunk t (0 past the sequence end): lane l holds tokens l and l + 32
+__device__ __forceinline__ void load_gb(const TcParams& p, const Work& w, int t, int lane, float (&g)[2],
+                                        float (&b)[2]) {
+    const int L = min(C, w.len - t * C);
+    const long row = w.row0 + (long)t * C;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int r = lane + 32 * k;
+        const size_t tok = (size_t)(row + r) * p.H + w.h;
+        g[k] = r < L ? __ldg(p.g + tok) : 0.f;
+        b[k] = r < L ? __ldg(p.beta + tok) : 0.f;
+    }
+}
+__device__ __forceinline__ void store_gb(Small& S, int t, int lane, const float (&g)[2], const float (&b)[2]) {
+    const int s = t & 1;
+    S.gbuf[s][lane] = g[0];
+    S.gbuf[s][lane + 32] = g[1];
+    S.bbuf[s][lane] = b[0];
+    S.bbuf[s][lane + 32] = b[1];
+}
+
+
+// Gate prefix of chunk t (one warp): log2 cumulative retention lg, gamma = 2^lg, gamma_C / gamma, and gamma_C / L
+// for the serial pass.  Rows past the sequence end have g = 0.
+__device__ __forceinline__ void gate_prefix(Small& S, int t, int L, int lane) {
+    const int s = t & 1;
+    const float LOG2E = 1.4426950408889634f;
+    const float g0 = S.gbuf[s][2 * lane], g1 = S.gbuf[s][2 * lane + 1];
+    float x = g0 + g1;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, m);
+        if (lane >= m) x += y;
+    }
+    const float G1 = x * LOG2E, G0 = (x - g1) * LOG2E;
+    S.lg[s][2 * lane] = G0;
+    S.lg[s][2 * lane + 1] = G1;
+    const float Glast = __shfl_sync(0xffffffffu, G1, 31);
+    S.gam[s][2 * lane] = ex2(G0);
+    S.gam[s][2 * lane + 1] = ex2(G1);
+    S.kdec[s][2 * lane] = ex2(Glast - G0);
+    S.kdec[s][2 * lane + 1] = ex2(Glast - G1);
+    if (lane == 31) {
+        S.info_gC[t & 3] = ex2(Glast);
+        S.info_L[t & 3] = L;
+    }
+}
+
+// Every thread passes the same four named barriers whether or not it computes (work = false after an
+// aborted wait), so the warpgroup can never fall out of step.
+__device__ void solve_unit_lower(const float* Am, float* T32, float* Rt, int t, bool work) {
+    const int w = t >> 5, lane = t & 31;   // 8 warps
+    if (work && t < 64) {
         const int b = t >> 4, c = t & 15, o = 16 * b;
         float x[16];
 #pragma unroll
@@ -231,64 +330,40 @@ __device__ void solve_unit_lower(const float* Am, float* T32, float* Rt, int t) 
 #pragma unroll
         for (int r = 0; r < 16; ++r) T32[(o + r) * TS + o + c] = x[r];
     }
-    named_bar(1, 128);
-    {   // level 1, stage 1: R_p = A[o+16..][o..o+15] T[o..o+15][o..o+15], o = 32 p
-        const int pr = t >> 6, r = (t & 63) >> 2, c0 = (t & 3) * 4, o = 32 * pr;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    named_bar(1, NPREP);
+    if (work && w < 4) {   // level 1: warp w -> pair p (o = 32 p), columns 8 nt .. 8 nt + 7 of the 16-wide block
+        const int pr = w >> 1, nt = w & 1, o = 32 * pr;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float a = Am[(o + 16 + r) * TS + o + k];
-            const float4 b = ld4(T32 + (o + k) * TS + o + c0);
-            a0 = fmaf(a, b.x, a0); a1 = fmaf(a, b.y, a1); a2 = fmaf(a, b.z, a2); a3 = fmaf(a, b.w, a3);
-        }
-        *reinterpret_cast<float4*>(Rt + (16 * pr + r) * RS + c0) = make_float4(a0, a1, a2, a3);
-    }
-    named_bar(1, 128);
-    {   // level 1, stage 2: T[o+16..][o..o+15] = -T[o+16..][o+16..] R_p
-        const int pr = t >> 6, r = (t & 63) >> 2, c0 = (t & 3) * 4, o = 32 * pr;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int ks = 0; ks < 2; ++ks)
+            mma_tile_tf32(d, Am + (o + 16) * TS + o + 8 * ks, TS, T32 + (o + 8 * ks) * TS + o + 8 * nt, TS, lane);
+        st_tile(Rt + (16 * pr) * RS + 8 * nt, RS, d, lane, 1.f);
+        __syncwarp();
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float a = T32[(o + 16 + r) * TS + o + 16 + k];
-            const float4 b = ld4(Rt + (16 * pr + k) * RS + c0);
-            a0 = fmaf(a, b.x, a0); a1 = fmaf(a, b.y, a1); a2 = fmaf(a, b.z, a2); a3 = fmaf(a, b.w, a3);
-        }
-        *reinterpret_cast<float4*>(T32 + (o + 16 + r) * TS + o + c0) = make_float4(-a0, -a1, -a2, -a3);
+        for (int ks = 0; ks < 2; ++ks)
+            mma_tile_tf32(e, T32 + (o + 16) * TS + o + 16 + 8 * ks, TS, Rt + (16 * pr + 8 * ks) * RS + 8 * nt, RS, lane);
+        st_tile(T32 + (o + 16) * TS + o + 8 * nt, TS, e, lane, -1.f);
     }
-    named_bar(1, 128);
-    const int r0 = (t >> 3) * 2, c0 = (t & 7) * 4;
-    {   // level 2, stage 1: R = A[32..63][0..31] T[0..31][0..31]
-        float acc[2][4] = {};
+    named_bar(1, NPREP);
+    const int mt = w & 1, nq = w >> 1;   // 2 row tiles x 4 column tiles of 8
+    if (work) {   // level 2, stage 1: R = A[32..63][0..31] T[0..31][0..31]; warp -> rows 16 mt, columns 8 nq .. + 7
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const float x0 = Am[(32 + r0) * TS + k], x1 = Am[(33 + r0) * TS + k];
-            const float4 b = ld4(T32 + k * TS + c0);
-            acc[0][0] = fmaf(x0, b.x, acc[0][0]); acc[0][1] = fmaf(x0, b.y, acc[0][1]);
-            acc[0][2] = fmaf(x0, b.z, acc[0][2]); acc[0][3] = fmaf(x0, b.w, acc[0][3]);
-            acc[1][0] = fmaf(x1, b.x, acc[1][0]); acc[1][1] = fmaf(x1, b.y, acc[1][1]);
-            acc[1][2] = fmaf(x1, b.z, acc[1][2]); acc[1][3] = fmaf(x1, b.w, acc[1][3]);
-        }
-        *reinterpret_cast<float4*>(Rt + r0 * RS + c0) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-        *reinterpret_cast<float4*>(Rt + (r0 + 1) * RS + c0) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+        for (int ks = 0; ks < 4; ++ks)
+            mma_tile_tf32(d, Am + (32 + 16 * mt) * TS + 8 * ks, TS, T32 + (8 * ks) * TS + 8 * nq, TS, lane);
+        st_tile(Rt + (16 * mt) * RS + 8 * nq, RS, d, lane, 1.f);
     }
-    named_bar(1, 128);
-    {   // level 2, stage 2: T[32..63][0..31] = -T[32..63][32..63] R
-        float acc[2][4] = {};
+    named_bar(1, NPREP);
+    if (work) {   // level 2, stage 2: T[32..63][0..31] = -T[32..63][32..63] R
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const float x0 = T32[(32 + r0) * TS + 32 + k], x1 = T32[(33 + r0) * TS + 32 + k];
-            const float4 b = ld4(Rt + k * RS + c0);
-            acc[0][0] = fmaf(x0, b.x, acc[0][0]); acc[0][1] = fmaf(x0, b.y, acc[0][1]);
-            acc[0][2] = fmaf(x0, b.z, acc[0][2]); acc[0][3] = fmaf(x0, b.w, acc[0][3]);
-            acc[1][0] = fmaf(x1, b.x, acc[1][0]); acc[1][1] = fmaf(x1, b.y, acc[1][1]);
-            acc[1][2] = fmaf(x1, b.z, acc[1][2]); acc[1][3] = fmaf(x1, b.w, acc[1][3]);
-        }
-        *reinterpret_cast<float4*>(T32 + (32 + r0) * TS + c0) = make_float4(-acc[0][0], -acc[0][1], -acc[0][2], -acc[0][3]);
-        *reinterpret_cast<float4*>(T32 + (33 + r0) * TS + c0) = make_float4(-acc[1][0], -acc[1][1], -acc[1][2], -acc[1][3]);
+        for (int ks = 0; ks < 4; ++ks)
+            mma_tile_tf32(d, T32 + (32 + 16 * mt) * TS + 32 + 8 * ks, TS, Rt + (8 * ks) * RS + 8 * nq, RS, lane);
+        st_tile(T32 + (32 + 16 * mt) * TS + 8 * nq, TS, d, lane, -1.f);
     }
-    named_bar(1, 128);
+    named_bar(1, NPREP);
 }
-
 
 // 8 fp32 values to fp16, one 16-byte shared store
 __device__ __forceinline__ void st_h8(uint8_t* p, const float* f) {
@@ -299,34 +374,39 @@ __device__ __forceinline__ void st_h8(uint8_t* p, const float* f) {
 // fp32 for the solve, plus row i of the identity in [I; P].  Rows 64-127 (token i = row - 64):
 // P[i][j] = scale 2^(lg_i - lg_j) (Q K^T)_ij for j <= i, in fp16 in [I; P].  Column blocks wholly above the
 // diagonal for every row of the warp are skipped (warp-uniform); the solve never reads A above the diagonal.
-__device__ __forceinline__ void epilogue_kkt(uint32_t tl, int row, int q4, const Small& S, int s, float scale,
+__device__ __forceinline__ void epilogue_kkt(uint32_t tl, int row, int q4, int pw, const Small& S, int s, float scale,
                                              float* Am, uint8_t* a1) {
-    uint32_t r[4][16];
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + TM_D0 + cb * 16, r[cb]);
+    // this thread: row `row`, columns [32 pw, 32 pw + 32)
+    const int c0 = 32 * pw;
+    uint32_t r[2][16];
+    tmem_ld16(tl + c0, r[0]);
+    tmem_ld16(tl + c0 + 16, r[1]);
     tmem_ld_wait();
     const int i = row & 63;
-    const int imax = 32 * (q4 & 1) + 31;
-    const float li = S.lg[i];
+    const int imax = 32 * (q4 & 1) + 31;      // last row of this warp, within its 64-row half
+    const bool live = c0 <= imax;             // warp-uniform: some column of the half can be on or below the diagonal
+    const float li = S.lg[s][i];
     if (row < 64) {
-        const float bi = S.bbuf[s][i];
+        if (live) {
+            const float bi = S.bbuf[s][i];
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-            if (cb * 16 > imax) break;
-            float v[16];
+            for (int cb = 0; cb < 2; ++cb) {
+                float v[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const int j = cb * 16 + q;
-                const float e = ex2(li - S.lg[j]);
-                v[q] = (j < i) ? bi * e * __uint_as_float(r[cb][q]) : 0.f;
+                for (int q = 0; q < 16; ++q) {
+                    const int j = c0 + cb * 16 + q;
+                    const float e = ex2(li - S.lg[s][j]);
+                    v[q] = (j < i) ? bi * e * __uint_as_float(r[cb][q]) : 0.f;
+                }
+                float4* dst = reinterpret_cast<float4*>(Am + i * TS + c0 + cb * 16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
-            float4* dst = reinterpret_cast<float4*>(Am + i * TS + cb * 16);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
         const uint32_t one = (i & 1) ? 0x3C000000u : 0x00003C00u;     // fp16 1.0 in the low or high half
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int cc = 0; cc < 4; ++cc) {
+            const int c8 = 4 * pw + cc;
             const bool here = (i >> 3) == c8;
             const int qw = (i & 7) >> 1;
             st16(a1 + sw128_off(row, c8 * 8), here && qw == 0 ? one : 0u, here && qw == 1 ? one : 0u,
@@ -334,54 +414,52 @@ __device__ __forceinline__ void epilogue_kkt(uint32_t tl, int row, int q4, const
         }
     } else {
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; cb < 2; ++cb) {
             float v[16];
-            if (cb * 16 > imax) {
+            if (!live) {
 #pragma unroll
                 for (int q = 0; q < 16; ++q) v[q] = 0.f;
             } else {
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
-                    const int j = cb * 16 + q;
-                    const float e = ex2(li - S.lg[j]);
+                    const int j = c0 + cb * 16 + q;
+                    const float e = ex2(li - S.lg[s][j]);
                     v[q] = (j <= i) ? scale * e * __uint_as_float(r[cb][q]) : 0.f;
                 }
             }
-            st_h8(a1 + sw128_off(row, cb * 16), v);
-            st_h8(a1 + sw128_off(row, cb * 16 + 8), v + 8);
+            st_h8(a1 + sw128_off(row, c0 + cb * 16), v);
+            st_h8(a1 + sw128_off(row, c0 + cb * 16 + 8), v + 8);
         }
     }
 }
 
 // Epilogue of D2 columns 0-127: W rows (0-63) and Q' = scale gamma Q - P W rows (64-127) to fp16 into [W; Q']
 // (K-major, two 64-column slabs).  Q comes from the stage's TMA tile, rows 64-127 of each slab.
-__device__ __forceinline__ void epilogue_wq(uint32_t tl, int row, const Small& S, float scale, const uint8_t* kqp,
-                                            uint8_t* wq) {
+__device__ __forceinline__ void epilogue_wq(uint32_t tl, int row, int slab, const Small& S, int s, float scale,
+                                            const uint8_t* kqp, uint8_t* wq) {
+    // this thread: row `row`, the 64 columns of slab `slab`
     const int i = row & 63;
-    const float qs = scale * S.gam[i];
+    const float qs = scale * S.gam[s][i];
+    uint32_t r[4][16];
 #pragma unroll
-    for (int slab = 0; slab < 2; ++slab) {
-        uint32_t r[4][16];
+    for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + TM_D2 + slab * 64 + cb * 16, r[cb]);
+    tmem_ld_wait();
+    if (row < 64) {
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + TM_D2 + slab * 64 + cb * 16, r[cb]);
-        tmem_ld_wait();
-        if (row < 64) {
+        for (int c8 = 0; c8 < 8; ++c8) {
+            float f[8];
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                float f[8];
+            for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
+            st_h8(wq + slab * 16384 + sw128_off(row, c8 * 8), f);
+        }
+    } else {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
-                st_h8(wq + slab * 16384 + sw128_off(row, c8 * 8), f);
-            }
-        } else {
+        for (int c8 = 0; c8 < 8; ++c8) {
+            float qv[8], f[8];
+            bf16x8_to_f32(ld16(kqp + slab * 16384 + sw128_off(row, c8 * 8)), qv);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                float qv[8], f[8];
-                bf16x8_to_f32(ld16(kqp + slab * 16384 + sw128_off(row, c8 * 8)), qv);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) f[q] = fmaf(qs, qv[q], -__uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]));
-                st_h8(wq + slab * 16384 + sw128_off(row, c8 * 8), f);
-            }
+            for (int q = 0; q < 8; ++q) f[q] = fmaf(qs, qv[q], -__uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]));
+            st_h8(wq + slab * 16384 + sw128_off(row, c8 * 8), f);
         }
     }
 }
@@ -409,10 +487,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         tmem_relinquish();
     }
     if (tid == 32) {
-        mbar_init(&S.full[0], 33);
-        mbar_init(&S.full[1], 33);
-        mbar_init(&S.empty[0], 1);
-        mbar_init(&S.empty[1], 1);
+        mbar_init(&S.full[0], 1);
+        mbar_init(&S.full[1], 1);
         mbar_init(&S.m0, 1);
         mbar_init(&S.m1, 1);
         mbar_init(&S.m2, 1);
@@ -427,110 +503,96 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        prefetch_tmap(&tmap_q);
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_v);
-        bool ok = true;
-        int issued = 0;
-        for (int t = 0; t < n_chunks; ++t) {
-            const int s = t & 1;
-            if (t >= 2 && ok) ok = mbar_wait(&S.empty[s], ((t >> 1) - 1) & 1, kWaitNs);
-            if (!ok) { if (lane == 0) set_status(1u); break; }
-            const int row = (int)(w.row0 + (long)t * C);
-            const int L = min(C, w.len - t * C);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&S.full[s], STAGE_KQ + STAGE_V);
-                uint8_t* kq = smem + OFF_KQ + s * STAGE_KQ;
-                tma_load_3d(kq, &tmap_k, &S.full[s], 0, w.h, row);
-                tma_load_3d(kq + 8192, &tmap_q, &S.full[s], 0, w.h, row);
-                tma_load_3d(kq + 16384, &tmap_k, &S.full[s], 64, w.h, row);
-                tma_load_3d(kq + 16384 + 8192, &tmap_q, &S.full[s], 64, w.h, row);
-                tma_load_3d(smem + OFF_V + s * STAGE_V, &tmap_v, &S.full[s], w.half * DVT, w.h, row);
-            }
-            for (int r = lane; r < C; r += 32) {
-                const size_t tok = (size_t)(row + r) * p.H + w.h;
-                S.gbuf[s][r] = r < L ? p.g[tok] : 0.f;
-                S.bbuf[s][r] = r < L ? p.beta[tok] : 0.f;
-            }
-            mbar_arrive(&S.full[s]);
-            issued = t + 1;
-        }
-        // drain: the last stage issued must have landed before the CTA can exit
-        if (issued > 0) {
-            const int t = issued - 1;
-            if (!mbar_wait(&S.full[t & 1], (t >> 1) & 1, kWaitNs) && lane == 0) set_status(2u);
-        }
-    } else if (warp <= 4) {
-        // ------------------------------------------------------------ prep warpgroup
-        const int t128 = tid - 32;                     // 0..127
+    if (warp < 8) {
+        // ------------------------------------------------------------ prep (two warpgroups)
+        const int t256 = tid;                          // 0..255
         const int q4 = warp & 3;                       // TMEM lane quarter of this warp
+        const int pw = warp >> 2;                      // which of the two warps on this quarter
         const int row = 32 * q4 + lane;                // TMEM lane this thread reads
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-        const bool leader = (t128 == 96);              // warp 4 lane 0
-        const int jrow = t128 & 63, hc = t128 >> 6;    // (row, column half) for the elementwise builds
+        const bool leader = (t256 == 0);               // warp 0 lane 0 issues the prep MMAs
+        const bool loader = (warp == 2);
+        float ldg[2] = {0.f, 0.f}, ldb[2] = {0.f, 0.f};   // g, beta of chunk t + 2 (loader warp, in flight)
+        int issued = 0;                                // chunks whose TMA loads have been issued
+        const int jrow = t256 & 63, part = t256 >> 6;  // (row, quarter of the columns) for the elementwise builds
         bool ok = true;
         const float LOG2E = 1.4426950408889634f;
-        for (int e = t128; e < 64 * TS; e += 128) T32[e] = 0.f;   // the upper triangle stays zero
-        named_bar(1, 128);
+        for (int e = t256; e < 64 * TS; e += NPREP) T32[e] = 0.f;   // the upper triangle stays zero
+        if (loader) {
+            prefetch_tmap(&tmap_q);
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+            for (int t = 0; t < 2 && t < n_chunks; ++t) {
+                issue_stage(smem, S, &tmap_q, &tmap_k, &tmap_v, w, t, lane);
+                float gg[2], bb[2];
+                load_gb(p, w, t, lane, gg, bb);
+                store_gb(S, t, lane, gg, bb);
+                issued = t + 1;
+            }
+        }
+        named_bar(1, NPREP);   // g and beta of chunks 0 and 1 are in shared memory
+        if (warp == 1 && n_chunks > 0) gate_prefix(S, 0, min(C, w.len), lane);
+        named_bar(1, NPREP);
         for (int t = 0; t < n_chunks; ++t) {
             const int s = t & 1;
             const int L = min(C, w.len - t * C);
             const uint32_t kq = sbase + OFF_KQ + s * STAGE_KQ;
             uint8_t* kqp = smem + OFF_KQ + s * STAGE_KQ;
             uint8_t* vsp = smem + OFF_V + s * STAGE_V;
+            const uint32_t d0 = TM_D0 + 64u * (uint32_t)(t & 1);
             if (ok) ok = mbar_wait(&S.full[s], (t >> 1) & 1, kWaitNs);
-            if (!ok && t128 == 0) set_status(4u);
-            // MMA0: D0 = [K; Q] K^T
-            if (ok && leader) {
+            if (!ok && t256 == 0) set_status(4u);
+            // MMA0: D0 = [K; Q] K^T (for t > 0 it was issued during the previous chunk)
+            if (ok && leader && t == 0) {
                 tc_fence_after();
                 const uint32_t id = idesc_f16(128, 64, true, false, false);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t a = kq + (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_f16(tmem + TM_D0, sdesc(a, 16, 1024), sdesc(a, 16, 1024), id, ks > 0);
+                    mma_f16(tmem + d0, sdesc(a, 16, 1024), sdesc(a, 16, 1024), id, ks > 0);
                 }
                 mma_commit(&S.m0);
             }
-            // gate prefix (warp 1): log2 of the cumulative retention, gamma, gamma_C / gamma
-            if (warp == 1) {
-                const float g0 = S.gbuf[s][2 * lane], g1 = S.gbuf[s][2 * lane + 1];
-                float x = g0 + g1;
+            // MMA0 of chunk 0 is awaited here; for later chunks the leader awaited it during the previous chunk,
+            // and the barriers since then carry its completion to every thread
+            if (ok && leader && t == 0) ok = mbar_wait(&S.m0, 0, kWaitNs);
+            if (!ok && leader) set_status(8u);
+            named_bar(1, NPREP);
+            // epilogue 0: A (rows 0-63) to fp32 for the solve, P (rows 64-127) and the identity rows to A1
+            tc_fence_after();
+            if (ok) epilogue_kkt(tl + d0, row, q4, pw, S, s, p.scale, Am, smem + OFF_A1);
+            tc_fence_before();
+            named_bar(1, NPREP);
+            // MMA0 of the next chunk runs ahead into the other D0 buffer while this chunk is solved
+            if (ok && leader && t + 1 < n_chunks) {
+                const int s1 = (t + 1) & 1;
+                ok = mbar_wait(&S.full[s1], ((t + 1) >> 1) & 1, kWaitNs);
+                if (!ok) set_status(2048u);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t kq1 = sbase + OFF_KQ + s1 * STAGE_KQ;
+                    const uint32_t id = idesc_f16(128, 64, true, false, false);
 #pragma unroll
-                for (int m = 1; m < 32; m <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, x, m);
-                    if (lane >= m) x += y;
-                }
-                const float G1 = x * LOG2E, G0 = (x - g1) * LOG2E;
-                S.lg[2 * lane] = G0;
-                S.lg[2 * lane + 1] = G1;
-                const float Glast = __shfl_sync(0xffffffffu, G1, 31);   // rows past L add 0
-                S.gam[2 * lane] = ex2(G0);
-                S.gam[2 * lane + 1] = ex2(G1);
-                S.kdec[2 * lane] = ex2(Glast - G0);
-                S.kdec[2 * lane + 1] = ex2(Glast - G1);
-                if (lane == 31) {
-                    S.info_gC[s] = ex2(Glast);
-                    S.info_L[s] = L;
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t a = kq1 + (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_f16(tmem + TM_D0 + 64u * (uint32_t)((t + 1) & 1), sdesc(a, 16, 1024), sdesc(a, 16, 1024),
+                                id, ks > 0);
+                    }
+                    mma_commit(&S.m0);
+                    ok = mbar_wait(&S.m0, (t + 1) & 1, kWaitNs);
+                    if (!ok) set_status(8u);
                 }
             }
-            named_bar(1, 128);
-            // epilogue 0: A (rows 0-63) to fp32 for the solve, P (rows 64-127) and the identity rows to A1
-            if (ok) ok = mbar_wait(&S.m0, t & 1, kWaitNs);
-            if (!ok && t128 == 0) set_status(8u);
-            tc_fence_after();
-            if (ok) epilogue_kkt(tl, row, q4, S, s, p.scale, Am, smem + OFF_A1);
-            tc_fence_before();
-            named_bar(1, 128);
             // UT transform: T = (I + A)^{-1}
-            if (ok) solve_unit_lower(Am, T32, Rt, t128);
-            else { named_bar(1, 128); named_bar(1, 128); named_bar(1, 128); named_bar(1, 128); named_bar(1, 128); }
+            solve_unit_lower(Am, T32, Rt, t256, ok);
+            // g and beta of chunk t + 1 (loaded at the end of chunk t - 1) go to the slot chunk t - 1 used; the
+            // gate prefix of chunk t + 1 reads them after the next barrier
+            if (loader && t >= 1 && t + 1 < issued) store_gb(S, t + 1, lane, ldg, ldb);
             // T to fp16, MN-major [j][n] (operand B of MMA1)
             if (ok) {
 #pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int e = t128 + 128 * it, j = e >> 3, c8 = e & 7;
+                for (int it = 0; it < 2; ++it) {
+                    const int e = t256 + NPREP * it, j = e >> 3, c8 = e & 7;
                     const float4 x0 = ld4(T32 + j * TS + c8 * 8), x1 = ld4(T32 + j * TS + c8 * 8 + 4);
                     const float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
                     float g[8];
@@ -540,7 +602,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
             }
             fence_async_smem();
-            named_bar(1, 128);
+            named_bar(1, NPREP);
             // MMA1: D1 = [I; P] T
             if (ok && leader) {
                 tc_fence_after();
@@ -552,49 +614,45 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 mma_commit(&S.m1);
             }
             // X = [beta gamma K | beta V] (operand B of MMA2), fp16 MN-major [j][n], 3 atoms of 64 columns.
-            // Thread (jrow, hc): chunk columns 12 hc .. 12 hc + 11 of row jrow (K slab 0, K slab 1, V).
+            // Thread (jrow, part): chunk columns 6 part .. 6 part + 5 of row jrow (0-7 K slab 0, 8-15 K slab 1,
+            // 16-23 V); part is warp-uniform.
             if (ok) {
                 const bool zero = jrow >= L;
-                const float sk = S.bbuf[s][jrow] * S.gam[jrow], sv = S.bbuf[s][jrow];
-                if (hc == 0) {
+                const float sk = S.bbuf[s][jrow] * S.gam[s][jrow], sv = S.bbuf[s][jrow];
 #pragma unroll
-                    for (int c = 0; c < 12; ++c) {
+                for (int cc = 0; cc < 6; ++cc) {
+                    const int c = 6 * part + cc;
+                    if (c < 16) {
                         const uint32_t o8 = sw128_off(jrow, (c & 7) * 8);
                         copy_scaled_chunk(kqp + (c >> 3) * 16384 + o8, smem + OFF_B2 + (c >> 3) * 8192 + o8, sk, zero);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 12; c < 16; ++c) {
-                        const uint32_t o8 = sw128_off(jrow, (c & 7) * 8);
-                        copy_scaled_chunk(kqp + 16384 + o8, smem + OFF_B2 + 8192 + o8, sk, zero);
-                    }
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t o8 = sw128_off(jrow, c * 8);
+                    } else {
+                        const uint32_t o8 = sw128_off(jrow, (c - 16) * 8);
                         copy_scaled_chunk(vsp + o8, smem + OFF_B2 + 2 * 8192 + o8, sv, zero);
                     }
                 }
             }
-            // epilogue 1: [T; PT] to fp16 into A1 (operand A of MMA2)
+            // gate prefix of the next chunk (its g and beta are already in shared memory), one chunk ahead
+            if (warp == 1 && t + 1 < n_chunks) gate_prefix(S, t + 1, min(C, w.len - (t + 1) * C), lane);
+            // epilogue 1: [T; PT] to fp16 into A1 (operand A of MMA2); columns [32 pw, 32 pw + 32)
             if (ok) ok = mbar_wait(&S.m1, t & 1, kWaitNs);
-            if (!ok && t128 == 0) set_status(16u);
+            if (!ok && t256 == 0) set_status(16u);
             tc_fence_after();
             if (ok) {
-                uint32_t r[4][16];
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + TM_D1 + cb * 16, r[cb]);
+                uint32_t r[2][16];
+                tmem_ld16(tl + TM_D1 + 32 * pw, r[0]);
+                tmem_ld16(tl + TM_D1 + 32 * pw + 16, r[1]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
+                for (int cc = 0; cc < 4; ++cc) {
                     float f[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
-                    st_h8(smem + OFF_A1 + sw128_off(row, c8 * 8), f);
+                    for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[cc >> 1][(cc & 1) * 8 + q]);
+                    st_h8(smem + OFF_A1 + sw128_off(row, 32 * pw + cc * 8), f);
                 }
             }
             fence_async_smem();
             tc_fence_before();
-            named_bar(1, 128);
+            named_bar(1, NPREP);
             // MMA2: D2 = [T; PT] X, once the serial pass has read U, U' of the previous chunk
             if (ok && leader) {
                 if (t > 0) ok = mbar_wait(&S.d2_free, (t - 1) & 1, kWaitNs);
@@ -610,43 +668,52 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
             }
             // Ktilde = diag(gamma_C / gamma) K (operand A of MMA4), once MMA4 of the previous chunk is done.
-            // Thread (jrow, hc): the 8 chunks of K slab hc of row jrow.
+            // Thread (jrow, part): chunks 4 (part & 1) .. + 3 of K slab part >> 1, row jrow.
             if (ok && t > 0) ok = mbar_wait(&S.m4, (t - 1) & 1, kWaitNs);
-            if (!ok && t128 == 0) set_status(64u);
+            if (!ok && t256 == 0) set_status(64u);
             if (ok) {
                 const bool zero = jrow >= L;
-                const float sd = S.kdec[jrow];
+                const float sd = S.kdec[s][jrow];
+                const int slab = part >> 1;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t o8 = sw128_off(jrow, c * 8);
-                    copy_scaled_chunk(kqp + hc * 16384 + o8, smem + OFF_KT + hc * 8192 + o8, sd, zero);
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint32_t o8 = sw128_off(jrow, (4 * (part & 1) + cc) * 8);
+                    copy_scaled_chunk(kqp + slab * 16384 + o8, smem + OFF_KT + slab * 8192 + o8, sd, zero);
                 }
             }
             // epilogue 2: W (rows 0-63) and Q' = scale gamma Q - P W (rows 64-127) into [W; Q'], once MMA3 of the
-            // previous chunk has consumed the buffer
-            named_bar(1, 128);   // the leader's MMA2 issue precedes every thread's wait on m2
+            // previous chunk has consumed the buffer; this thread does the 64 columns of slab pw
+            named_bar(1, NPREP);   // the leader's MMA2 issue precedes every thread's wait on m2
             if (ok && t > 0) ok = mbar_wait(&S.m3, (t - 1) & 1, kWaitNs);
             if (ok) ok = mbar_wait(&S.m2, t & 1, kWaitNs);
-            if (!ok && t128 == 0) set_status(128u);
+            if (!ok && t256 == 0) set_status(128u);
             tc_fence_after();
-            if (ok) epilogue_wq(tl, row, S, p.scale, kqp, smem + OFF_WQ);
+            if (ok) epilogue_wq(tl, row, pw, S, s, p.scale, kqp, smem + OFF_WQ);
             fence_async_smem();
             tc_fence_before();
-            named_bar(1, 128);
-            if (t128 == 0) {
-                mbar_arrive(&S.empty[s]);      // the stage's K, Q, V, g, beta are no longer read
-                mbar_arrive(&S.prep_done);
+            named_bar(1, NPREP);
+            if (t256 == 0) mbar_arrive(&S.prep_done);
+            // the stage of chunk t is free: load chunk t + 2 into it
+            if (loader && ok && t + 2 < n_chunks) {
+                issue_stage(smem, S, &tmap_q, &tmap_k, &tmap_v, w, t + 2, lane);
+                load_gb(p, w, t + 2, lane, ldg, ldb);
+                issued = t + 3;
             }
+        }
+        // drain: a stage whose TMA was issued but never waited on (after an abort) must land before exit
+        if (loader && issued > 0 && !ok) {
+            const int t = issued - 1;
+            mbar_wait(&S.full[t & 1], (t >> 1) & 1, kWaitNs);
         }
     } else {
         // ------------------------------------------------------------ serial warpgroup
         // Warps with TMEM lane quarters 0 and 1 own the Delta rows (tokens 0-63) of D3; the other two own the
         // output rows.  The Delta warps issue MMA4 as soon as Delta is in shared memory.
-        const int t128 = tid - 160;
+        const int t128 = tid - 256;
         const int q4 = warp & 3;
         const int row = 32 * q4 + lane;                // TMEM lane: token (D3 rows) and d_k row (D4 rows)
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-        const bool leader = (t128 == 96);              // warp 8 lane 0 (quarter 0, a Delta warp)
+        const bool leader = (t128 == 0);               // warp 8 lane 0 (quarter 0, a Delta warp)
         const bool delta_warp = q4 < 2;
         bool ok = true;
         const size_t sidx = ((size_t)w.n * p.H + w.h) * DK * DV + (size_t)row * DV + w.half * DVT;
@@ -665,8 +732,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const int s = t & 1;
             if (ok) ok = mbar_wait(&S.prep_done, t & 1, kWaitNs);
             if (!ok && t128 == 0) set_status(256u);
-            const int L = S.info_L[s];
-            const float gC = S.info_gC[s];
+            const int L = S.info_L[t & 3];
+            const float gC = S.info_gC[t & 3];
             // MMA3: D3 = [W; Q'] h
             if (ok && leader) {
                 tc_fence_after();
@@ -683,43 +750,37 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const int i = row - 64;
             const bool store_o = !delta_warp && i < L;
             const size_t orow = ((size_t)(w.row0 + (long)t * C + (row & 63)) * p.H + w.h) * DV + w.half * DVT;
-            // two passes of 32 columns keep the live TMEM tiles small (h stays in registers throughout)
+            // four passes of 16 columns keep the live TMEM tiles small (h stays in registers throughout)
 #pragma unroll
-            for (int hp = 0; hp < 2; ++hp) {
-                uint32_t a[2][16], u[2][16];
+            for (int hp = 0; hp < 4; ++hp) {
+                uint32_t a[16], u[16];
                 if (ok) {
-#pragma unroll
-                    for (int cb = 0; cb < 2; ++cb) {
-                        tmem_ld16(tl + TM_D3 + hp * 32 + cb * 16, a[cb]);
-                        tmem_ld16(tl + TM_D2 + 128 + hp * 32 + cb * 16, u[cb]);
-                    }
+                    tmem_ld16(tl + TM_D3 + hp * 16, a);
+                    tmem_ld16(tl + TM_D2 + 128 + hp * 16, u);
                     tmem_ld_wait();
                 }
                 if (ok && delta_warp) {
                     // Delta = U - W h (token rows 0-63) to fp16 MN-major [j][n] (operand B of MMA4)
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
+                    for (int h8 = 0; h8 < 2; ++h8) {
                         float f[8];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int k = (c8 & 1) * 8 + q;
-                            f[q] = __uint_as_float(u[c8 >> 1][k]) - __uint_as_float(a[c8 >> 1][k]);
-                        }
-                        st_h8(smem + OFF_D + sw128_off(row, hp * 32 + c8 * 8), f);
+                        for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(u[h8 * 8 + q]) - __uint_as_float(a[h8 * 8 + q]);
+                        st_h8(smem + OFF_D + sw128_off(row, hp * 16 + h8 * 8), f);
                     }
                 } else if (ok && store_o) {
                     // O = U' + Q' h (token rows 64-127) to HBM
-                    float f[32];
+                    float f[16];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(u[k >> 4][k & 15]) + __uint_as_float(a[k >> 4][k & 15]);
+                    for (int k = 0; k < 16; ++k) f[k] = __uint_as_float(u[k]) + __uint_as_float(a[k]);
                     if (O_F32) {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + hp * 32);
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + hp * 16);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                        for (int q = 0; q < 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
                     } else {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow + hp * 32);
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow + hp * 16);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
+                        for (int q = 0; q < 2; ++q) {
                             uint32_t pk[4];
 #pragma unroll
                             for (int m = 0; m < 4; ++m) {
