@@ -5,7 +5,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step is one gdn_chunk_fwd call over the whole workload.  That is the
 whole hot path: gate prefix, beta-scaled masked K K^T, the UT solve, the WY
-products, the serial state pass and the output, all in one kernel launch.
+products, the serial state pass and the output.  The default (auto) path is
+two launches per call: the per-chunk kernel over all SMs, then the state
+kernel; --algo tcgen05 times the fused single-launch kernel instead.
 Inputs are seeded and synthetic, drawn by gated_delta_rule_gdn_gb300.workloads.
 
 * value: tokens/s (B*T per step).  Inputs are resident in HBM and timed with
@@ -14,8 +16,9 @@ Inputs are seeded and synthetic, drawn by gated_delta_rule_gdn_gb300.workloads.
 * e2e: the same metric through the public API, from pinned host buffers.
   Every step copies the inputs host->device, runs the call, and copies o and
   the final state device->host.
-* roofline: algorithmic bytes of one launch / the mean launch time, against
-  the measured HBM copy bandwidth.  The bytes are 1,288 B per token-head (q,
+* roofline: algorithmic bytes of one call / the mean call time (all of the
+  call's launches, on the launching stream), against the measured HBM copy
+  bandwidth.  The bytes are 1,288 B per token-head (q,
   k, v in bf16, o in fp32, g and beta in fp32), plus the fp32 state read and
   write per sequence-head.
 * cpu_baseline: the fp64 C oracle on the host cores (rank 0, N = 1).
@@ -327,8 +330,8 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     alg = _alg_bytes(w)
     achieved = alg / (ms / 1e3) / 1e9
-    kernel = "chunk_tc" if gdn.chunk_plan(False, w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16,
-                                           False, args.algo) == "tcgen05" else "chunk_generic"
+    plan = gdn.chunk_plan(False, w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16, False, args.algo)
+    kernel, launches = {"tcgen05": ("chunk_tc", 1), "two_pass": ("chunk_two_pass", 2)}.get(plan, ("chunk_generic", 1))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -337,14 +340,14 @@ def run_ours(args):
                    "chunk_size": w.chunk_size, "initial_state": True, "output_final_state": True,
                    "o_dtype": "f32",
                    "l2": "flushed before each timed step (256 MiB device write, outside the events)",
-                   "kernel": kernel, "timed_region_wall_ms": t_wall * 1e3},
+                   "kernel": kernel, "launches_per_step": launches, "timed_region_wall_ms": t_wall * 1e3},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": _traffic_for(kernel), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6800 GB/s",
                      "algorithmic_bytes_per_launch": alg},
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches,
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -363,7 +366,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--algo", choices=["auto", "generic", "tcgen05"], default="auto")
+    ap.add_argument("--algo", choices=["auto", "generic", "tcgen05", "two_pass"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

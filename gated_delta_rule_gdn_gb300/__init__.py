@@ -7,7 +7,7 @@ supplies device memory and streams.  Build the library with
 missing.
 """
 from ._binding import (GdnError, chunk_plan, device_status, gdn_chunk_fwd, gdn_recurrent_step, kda_chunk_fwd, last_error,
-                       lib_path, load)
+                       lib_path, load, workspace_size)
 
 __all__ = ["gdn_chunk_fwd", "kda_chunk_fwd", "gdn_recurrent_step", "device_status", "chunk_plan", "last_error", "load",
-           "lib_path", "GdnError"]
+           "lib_path", "GdnError", "workspace_size"]

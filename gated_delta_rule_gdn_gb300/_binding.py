@@ -20,7 +20,7 @@ GDN_OK = 0
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA",
                 4: "GDN_ERR_TIMEOUT"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
-ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2}
+ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "two_pass": 3}
 
 
 class GdnError(RuntimeError):
@@ -38,6 +38,11 @@ def _declare(lib):
     for name in ("gdn_chunk_fwd_algo", "kda_chunk_fwd_algo"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i, chunk + [i, vp]
+    for name in ("gdn_chunk_fwd_ws", "kda_chunk_fwd_ws"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i, chunk + [i, vp, ctypes.c_size_t, vp]
+    lib.gdn_chunk_workspace_size.restype = i
+    lib.gdn_chunk_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.gdn_recurrent_step.restype = i
     lib.gdn_recurrent_step.argtypes = [vp, vp, vp, vp, vp, fp, vp, vp, i, i, i, i, i, i, vp]
     lib.gdn_chunk_plan.restype = i
@@ -98,9 +103,18 @@ def _need(t: torch.Tensor, name: str, dtype=None, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def workspace_size(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chunk_size: int, dtype,
+                   n_seqs: int = 0, algo: str = "auto", o_dtype=torch.float32) -> int:
+    """Device workspace bytes a chunk-forward call with these sizes needs (0 if its kernel needs none)."""
+    out = ctypes.c_size_t(0)
+    _check(load().gdn_chunk_workspace_size(int(per_channel), B, T, H, dk, dv, chunk_size, DTYPES[dtype],
+                                           DTYPES[o_dtype], int(n_seqs), ALGOS[algo], ctypes.byref(out)))
+    return int(out.value)
+
+
 def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
            cu_seqlens=None, chunk_size=64, algo="auto", o=None, final_state=None, stream=None,
-           o_dtype=torch.float32):
+           o_dtype=torch.float32, workspace=None):
     lib = load()
     if q.dtype not in DTYPES:
         raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
@@ -134,30 +148,40 @@ def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, 
         _need(final_state, "final_state", torch.float32, dev)
     if scale is None:
         scale = dk ** -0.5
-    fn = lib.kda_chunk_fwd_algo if per_channel else lib.gdn_chunk_fwd_algo
+    if workspace is None:
+        need = workspace_size(per_channel, B, T, H, dk, dv, int(chunk_size), q.dtype, n_seqs, algo, o_dtype)
+        if need > 0:
+            # torch's caching allocator keeps the block for the next call
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, dev)
+    fn = lib.kda_chunk_fwd_ws if per_channel else lib.gdn_chunk_fwd_ws
     st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(initial_state),
             int(final_state is not None), _ptr(final_state), _ptr(cu_seqlens), n_seqs, _ptr(o),
             B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[o_dtype], ALGOS[algo],
-            _stream_handle(stream, dev))
+            _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream_handle(stream, dev))
     _check(st)
     return o, final_state
 
 
 def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False, cu_seqlens=None,
-                  chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32):
-    """Chunkwise gated delta rule forward (C ABI gdn_chunk_fwd).  Returns (o, final_state or None).
+                  chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32,
+                  workspace=None):
+    """Chunkwise gated delta rule forward (C ABI gdn_chunk_fwd_ws).  Returns (o, final_state or None).
 
     o is fp32 unless o_dtype=torch.bfloat16 (then it is the round-to-nearest-even of the fp32 result).
+    ``workspace`` (uint8 device tensor, see workspace_size) is allocated here when the kernel needs one.
     """
     return _chunk(False, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens, chunk_size, algo,
-                  o, final_state, stream, o_dtype)
+                  o, final_state, stream, o_dtype, workspace)
 
 
 def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False, cu_seqlens=None,
-                  chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32):
-    """Chunkwise KDA forward, g per key channel (C ABI kda_chunk_fwd).  Returns (o, final_state or None)."""
+                  chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32,
+                  workspace=None):
+    """Chunkwise KDA forward, g per key channel (C ABI kda_chunk_fwd_ws).  Returns (o, final_state or None)."""
     return _chunk(True, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens, chunk_size, algo,
-                  o, final_state, stream, o_dtype)
+                  o, final_state, stream, o_dtype, workspace)
 
 
 def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
@@ -188,7 +212,7 @@ def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None,
 
 def chunk_plan(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chunk_size: int, dtype,
                varlen: bool = False, algo: str = "auto", o_dtype=torch.float32) -> str:
-    """Name of the kernel ("generic" or "tcgen05") a chunk-forward call with these sizes runs."""
+    """Name of the kernel ("generic", "tcgen05" or "two_pass") a chunk-forward call with these sizes runs."""
     out = ctypes.c_int(-1)
     _check(load().gdn_chunk_plan(int(per_channel), B, T, H, dk, dv, chunk_size, DTYPES[dtype], DTYPES[o_dtype],
                                  int(varlen), ALGOS[algo], ctypes.byref(out)))

@@ -1,5 +1,6 @@
 // C ABI of libgdn_gb300.so (declared in include/gdn.h): argument checks, error reporting and
-// kernel dispatch.  No entry point allocates device memory; all buffers belong to the caller.
+// kernel dispatch.  All buffers belong to the caller; the only allocation is the two-pass workspace when
+// the caller passes none, made and freed on the call's stream.
 
 #include <cuda_runtime.h>
 
@@ -71,37 +72,73 @@ gdn_status check_chunk(const gdn::ChunkArgs& a, gdn_dtype dtype, gdn_dtype o_dty
     return GDN_OK;
 }
 
-gdn_status resolve_algo(const gdn::ChunkArgs& a, gdn_algo algo, const char* fn, bool* use_tc) {
-    if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_GENERIC && algo != GDN_ALGO_TCGEN05)
+// Resolve a kernel request against what each kernel supports.  AUTO takes the two-pass tcgen05 path where it
+// applies, then the fused tcgen05 kernel, then the generic one.
+gdn_status resolve_algo(const gdn::ChunkArgs& a, gdn_algo algo, const char* fn, gdn_algo* chosen) {
+    if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_GENERIC && algo != GDN_ALGO_TCGEN05 && algo != GDN_ALGO_TWO_PASS)
         return fail(GDN_ERR_INVALID_ARG, "%s: unknown algo %d", fn, (int)algo);
-    const char* why = gdn::tc_chunk_unsupported_reason(a);
-    *use_tc = false;
-    if (algo == GDN_ALGO_TCGEN05) {
-        if (why) return fail(GDN_ERR_UNSUPPORTED, "%s: the tcgen05 kernel does not apply: %s", fn, why);
-        *use_tc = true;
-    } else if (algo == GDN_ALGO_AUTO) {
-        *use_tc = (why == nullptr);
-    }
+    const char* why_tc = gdn::tc_chunk_unsupported_reason(a);
+    const char* why_tp = gdn::two_pass_unsupported_reason(a);
+    if (algo == GDN_ALGO_TCGEN05 && why_tc)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the tcgen05 kernel does not apply: %s", fn, why_tc);
+    if (algo == GDN_ALGO_TWO_PASS && why_tp)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the two-pass kernels do not apply: %s", fn, why_tp);
+    if (algo == GDN_ALGO_AUTO)
+        algo = !why_tp ? GDN_ALGO_TWO_PASS : (!why_tc ? GDN_ALGO_TCGEN05 : GDN_ALGO_GENERIC);
+    *chosen = algo;
     return GDN_OK;
 }
 
 gdn_status chunk_common(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
                         const float* initial_state, int output_final_state, float* final_state,
                         const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
-                        int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, gdn_algo algo, void* stream,
-                        bool per_channel, const char* fn) {
+                        int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, gdn_algo algo, void* workspace,
+                        size_t workspace_bytes, void* stream, bool per_channel, const char* fn) {
     gdn::ChunkArgs a{q, k, v, g, beta, scale, initial_state, final_state, cu_seqlens, n_seqs, o,
                      B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0,
                      o_dtype == GDN_F32 ? 1 : 0};
     gdn_status st = check_chunk(a, dtype, o_dtype, output_final_state, fn);
     if (st != GDN_OK) return st;
-    bool use_tc = false;
-    st = resolve_algo(a, algo, fn, &use_tc);
+    gdn_algo chosen = GDN_ALGO_GENERIC;
+    st = resolve_algo(a, algo, fn, &chosen);
     if (st != GDN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = use_tc ? gdn::launch_chunk_tc(a, s) : gdn::launch_chunk_generic(a, s);
+    cudaError_t e = cudaSuccess;
+    if (chosen == GDN_ALGO_TWO_PASS) {
+        const size_t need = gdn::two_pass_workspace_bytes(a);
+        if (workspace && workspace_bytes < need)
+            return fail(GDN_ERR_INVALID_ARG, "%s: workspace of %zu bytes is smaller than the %zu needed", fn,
+                        workspace_bytes, need);
+        if (workspace && !aligned(workspace, 256))
+            return fail(GDN_ERR_INVALID_ARG, "%s: workspace is not 256-byte aligned", fn);
+        void* ws = workspace;
+        if (!ws && need > 0) {
+            e = cudaMallocAsync(&ws, need, s);
+            if (e != cudaSuccess) return cuda_fail(e, fn);
+        }
+        e = gdn::launch_chunk_two_pass(a, ws, ws ? (workspace ? workspace_bytes : need) : 0, s);
+        if (!workspace && ws) {
+            const cudaError_t e2 = cudaFreeAsync(ws, s);
+            if (e == cudaSuccess) e = e2;
+        }
+    } else if (chosen == GDN_ALGO_TCGEN05) {
+        e = gdn::launch_chunk_tc(a, s);
+    } else {
+        e = gdn::launch_chunk_generic(a, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return ok();
+}
+
+// Stand-in arguments for the planning queries: pointers 256-byte aligned and never dereferenced.
+gdn::ChunkArgs plan_args(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                         gdn_dtype o_dtype, int n_seqs) {
+    const void* p = reinterpret_cast<const void*>(uintptr_t(1) << 20);
+    float* fp = reinterpret_cast<float*>(uintptr_t(1) << 20);
+    return gdn::ChunkArgs{p, p, p, fp, fp, 1.0f, nullptr, nullptr,
+                          n_seqs > 0 ? reinterpret_cast<const int32_t*>(p) : nullptr, n_seqs > 0 ? n_seqs : 0,
+                          const_cast<void*>(p), B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0,
+                          per_channel ? 1 : 0, o_dtype == GDN_F32 ? 1 : 0};
 }
 
 }  // namespace
@@ -114,7 +151,8 @@ gdn_status gdn_chunk_fwd_algo(const void* q, const void* k, const void* v, const
                               int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype,
                               gdn_algo algo, void* stream) {
     return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
-                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, stream, false, "gdn_chunk_fwd");
+                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, nullptr, 0, stream, false,
+                        "gdn_chunk_fwd");
 }
 
 gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
@@ -131,7 +169,8 @@ gdn_status kda_chunk_fwd_algo(const void* q, const void* k, const void* v, const
                               int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype,
                               gdn_algo algo, void* stream) {
     return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
-                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, stream, true, "kda_chunk_fwd");
+                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, nullptr, 0, stream, true,
+                        "kda_chunk_fwd");
 }
 
 gdn_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
@@ -140,6 +179,26 @@ gdn_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, void* stream) {
     return kda_chunk_fwd_algo(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens,
                               n_seqs, o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, GDN_ALGO_AUTO, stream);
+}
+
+gdn_status gdn_chunk_fwd_ws(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            float scale, const float* initial_state, int output_final_state, float* final_state,
+                            const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
+                            int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, gdn_algo algo, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
+                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, workspace, workspace_bytes, stream,
+                        false, "gdn_chunk_fwd");
+}
+
+gdn_status kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            float scale, const float* initial_state, int output_final_state, float* final_state,
+                            const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
+                            int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, gdn_algo algo, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
+                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, workspace, workspace_bytes, stream,
+                        true, "kda_chunk_fwd");
 }
 
 gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -172,27 +231,40 @@ gdn_status gdn_chunk_plan(int per_channel, int B, int T, int H, int d_k, int d_v
                           gdn_dtype o_dtype, int varlen, gdn_algo requested, gdn_algo* chosen) {
     const char* fn = "gdn_chunk_plan";
     if (!chosen) return fail(GDN_ERR_INVALID_ARG, "%s: chosen is NULL", fn);
-    // stand-in pointers, 256-byte aligned and never dereferenced: nothing is launched here
-    const void* p = reinterpret_cast<const void*>(uintptr_t(1) << 20);
-    float* fp = reinterpret_cast<float*>(uintptr_t(1) << 20);
-    gdn::ChunkArgs a{p, p, p, fp, fp, 1.0f, nullptr, nullptr, varlen ? reinterpret_cast<const int32_t*>(p) : nullptr,
-                     varlen ? 1 : 0, const_cast<void*>(p), B, T, H, d_k, d_v, chunk_size,
-                     dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0, o_dtype == GDN_F32 ? 1 : 0};
+    const gdn::ChunkArgs a = plan_args(per_channel, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, varlen ? 1 : 0);
     gdn_status st = check_chunk(a, dtype, o_dtype, 0, fn);
     if (st != GDN_OK) return st;
-    bool use_tc = false;
-    st = resolve_algo(a, requested, fn, &use_tc);
+    gdn_algo c = GDN_ALGO_GENERIC;
+    st = resolve_algo(a, requested, fn, &c);
     if (st != GDN_OK) return st;
-    *chosen = use_tc ? GDN_ALGO_TCGEN05 : GDN_ALGO_GENERIC;
+    *chosen = c;
+    return ok();
+}
+
+gdn_status gdn_chunk_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
+                                    gdn_dtype dtype, gdn_dtype o_dtype, int n_seqs, gdn_algo requested,
+                                    size_t* bytes) {
+    const char* fn = "gdn_chunk_workspace_size";
+    if (!bytes) return fail(GDN_ERR_INVALID_ARG, "%s: bytes is NULL", fn);
+    if (n_seqs < 0) return fail(GDN_ERR_INVALID_ARG, "%s: n_seqs must be >= 0 (got %d)", fn, n_seqs);
+    const gdn::ChunkArgs a = plan_args(per_channel, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, n_seqs);
+    gdn_status st = check_chunk(a, dtype, o_dtype, 0, fn);
+    if (st != GDN_OK) return st;
+    gdn_algo c = GDN_ALGO_GENERIC;
+    st = resolve_algo(a, requested, fn, &c);
+    if (st != GDN_OK) return st;
+    *bytes = c == GDN_ALGO_TWO_PASS ? gdn::two_pass_workspace_bytes(a) : 0;
     return ok();
 }
 
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 gdn_status gdn_device_status(int clear) {
-    unsigned v = 0;
+    unsigned v = 0, v2 = 0;
     cudaError_t e = gdn::tc_read_and_clear_status(&v, clear != 0);
+    if (e == cudaSuccess) e = gdn::tp_read_and_clear_status(&v2, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_status");
+    v |= v2 << 16;
     if (v != 0) return fail(GDN_ERR_TIMEOUT, "gdn_device_status: a kernel gave up a bounded wait (code 0x%x)", v);
     return ok();
 }

@@ -1,0 +1,879 @@
+// Two-pass chunkwise gated delta rule forward on tcgen05 tensor cores (sm_103a): scalar gate, bf16 q/k/v,
+// d_k = d_v = 128, chunk C = 64, fp32 state, o in fp32 or bf16.
+//
+// The chunk algebra is the one of the fused kernel (chunk_tc.cu), from "TileLang 实战：KDA 从零到一 -- Gated
+// DeltaNet", §2.3, split the way "Gated Delta Network (GDN)", §4(b3)-(d) splits it: every product that does not
+// depend on the state first, for all chunks at once, then the serial state pass.
+//
+// Pass 1, chunk_intra_kernel: one work item per (chunk, head), spread over every SM (two CTAs per SM,
+// persistent).  Per item, with G the within-chunk cumulative log gate, gamma = exp(G), L valid rows:
+//   A  = diag(beta)(Gamma * K K^T) (strictly lower)   P = scale Gamma * Q K^T (lower incl. diagonal)
+//   T  = (I + A)^{-1}                                 (blocked inverse, solved in place over A)
+//   [W | U ; P W | P U] = [T; P T] [beta gamma K | beta V]
+//   Q' = scale diag(gamma) Q - P W,  U' = P U,  Ktilde = diag(gamma_C / gamma) K
+// and writes [W; Q'], Ktilde, [U; U'] (fp16, already in the shared-memory operand layouts of pass 2) and
+// gamma_C to the workspace.  MMAs: D0 = [K; Q] K^T, D1 = [I; P] T, D2a = [T; PT] beta gamma K,
+// D2b = [T; PT] beta V (the last reuses the columns of D0 and D1), 256 TMEM columns per CTA.
+//
+// Pass 2, chunk_state_kernel: one CTA per (sequence, head, 64-column d_v half), 4 warps, h = S^T tile in fp32
+// registers (thread = d_k row).  Per chunk the workspace slot arrives by bulk copy (2-stage ring), then
+//   D3 = [W; Q'] h (M=128 N=64 K=128):  Delta = U - W h,  O = U' + Q' h
+//   D4 = Ktilde^T Delta (M=128 N=64 K=64):  h <- gamma_C h + D4.
+//
+// Workspace (caller-owned or allocated for the call): per (slot, head) item 32 KB [W; Q'] + 16 KB Ktilde +
+// 32 KB [U; U'] (two d_v halves) + 512 B gamma_C, where sequence n's chunk t has slot floor(start_n / C) + n + t.
+//
+// Every mbarrier wait is bounded (2 s); a wait that gives up sets a bit in the status word read by
+// gdn_device_status, and the CTA skips the rest of its work, drains its copies, frees TMEM and exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "tc_common.cuh"
+#include "chunk_common.cuh"
+
+namespace gdn {
+
+__device__ unsigned g_tp_status;
+
+namespace {
+
+using namespace tc;
+
+constexpr int C = 64;
+constexpr int DK = 128;
+constexpr int DV = 128;
+constexpr int DVT = 64;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// workspace, per item
+constexpr uint32_t WS_WQ = 32768;   // [W; Q'] fp16 K-major 128 x 128, two 64-column slabs, 128-byte swizzle
+constexpr uint32_t WS_KT = 16384;   // Ktilde fp16 [j][c] 64 x 128, two 64-column slabs, 128-byte swizzle
+constexpr uint32_t WS_UU = 32768;   // per d_v half: [U; U'] fp16 128 rows x 64 columns, rows 128 B, 16-byte chunks swizzled
+constexpr uint32_t WS_GC = 512;     // gamma_C per d_k row (fp32)
+constexpr size_t WS_ITEM = (size_t)WS_WQ + WS_KT + WS_UU + WS_GC;
+
+struct Ws {
+    uint8_t* wq;
+    uint8_t* kt;
+    uint8_t* uu;
+    float* gc;
+};
+
+__device__ __forceinline__ void set_status(unsigned bit) { atomicOr(&g_tp_status, bit); }
+
+// Sequence geometry: packed (cu_seqlens) or B rows of T tokens.
+struct Geo {
+    const int32_t* cu;
+    int n_seqs;
+    int B, T, H;
+    __device__ int N() const { return cu ? n_seqs : B; }
+    __device__ void seq(int n, long& s0, int& len) const {
+        if (cu) {
+            long a = cu[n], b = cu[n + 1];
+            a = a < 0 ? 0 : (a > T ? T : a);
+            b = b < a ? a : (b > T ? T : b);
+            s0 = a;
+            len = (int)(b - a);
+        } else {
+            s0 = (long)n * T;
+            len = T;
+        }
+    }
+    // first workspace slot of sequence n (strictly increasing in n for valid cu_seqlens)
+    __device__ long slot0(int n) const {
+        long s0;
+        int len;
+        seq(n, s0, len);
+        return s0 / C + n;
+    }
+};
+
+// ==================================================================== pass 1: per-chunk products
+struct IntraParams {
+    Geo geo;
+    const float* g;
+    const float* beta;
+    float scale;
+    long total;   // virtual items: slots x heads
+    Ws ws;
+};
+
+struct Item {
+    int n, h, t, L;
+    long row;     // first token row of the chunk
+    long it;      // workspace item index
+};
+
+// Virtual item vi = slot * H + head -> the sequence whose slots contain it (binary search); false for the
+// unused slots between sequences.
+__device__ bool decode_item(const Geo& g, long vi, Item& x) {
+    const long s = vi / g.H;
+    x.h = (int)(vi - s * g.H);
+    int lo = 0, hi = g.N() - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (g.slot0(mid) <= s) lo = mid;
+        else hi = mid - 1;
+    }
+    long s0;
+    int len;
+    g.seq(lo, s0, len);
+    const long t = s - (s0 / C + lo);
+    if (t < 0 || t * C >= len) return false;
+    x.n = lo;
+    x.t = (int)t;
+    x.row = s0 + t * C;
+    x.L = min(C, len - (int)t * C);
+    x.it = vi;
+    return true;
+}
+
+__device__ long next_item(const Geo& g, long vi, long total, Item& x) {
+    for (; vi < total; vi += gridDim.x)
+        if (decode_item(g, vi, x)) return vi;
+    return total;
+}
+
+// shared memory of pass 1 (bytes from a 1024-aligned base)
+constexpr uint32_t I_KQ = 0;        // [K; Q] rows, two K-slabs of 16 KB (K rows 0-63, Q rows 64-127)
+constexpr uint32_t I_V = 32768;     // V, two 64-column slabs of 8 KB
+constexpr uint32_t I_A1 = 49152;    // [I; P] then [T; PT], fp16 K-major 128 x 64
+constexpr uint32_t I_B1 = 65536;    // T, fp16 MN-major [j][n] 64 x 64
+constexpr uint32_t I_B2 = 73728;    // X = [beta gamma K | beta V], fp16 MN-major 64 x 256 (four slabs)
+constexpr uint32_t I_AM = I_B2;     // fp32 A, then T in place (row stride TS), before X is built
+constexpr uint32_t I_RT = I_B2 + 64 * TS * 4;
+constexpr uint32_t I_SMALL = I_B2 + 32768;
+static_assert(64 * TS * 4 + 32 * RS * 4 <= 32768, "A and the solve scratch must fit in the X buffer");
+
+struct ISmall {
+    uint64_t full;            // inputs of the item landed (TMA transaction bytes)
+    uint64_t m0, m1, m2a, m2b;
+    uint32_t tmem_base;
+    uint32_t pad;
+    float gbuf[C];            // g of the item (0 past the end)
+    float bbuf[C];            // beta of the item (0 past the end)
+    float lg[C];              // log2 of the within-chunk cumulative retention
+    float gam[C];             // gamma_j
+    float kdec[C];            // gamma_C / gamma_j
+    float gC;
+};
+constexpr uint32_t I_SMEM = I_SMALL + sizeof(ISmall) + 1024;
+constexpr uint32_t I_TM_D0 = 0, I_TM_D1 = 64, I_TM_D2A = 128, I_TM_D2B = 0, I_TM_COLS = 256;
+constexpr int I_THREADS = 256;
+
+// Blocked inverse of the unit lower-triangular (I + A), 64 x 64, in place: A (strictly lower, fp32, row stride
+// TS) is overwritten by T = (I + A)^{-1}.  Level 0 solves the four 16 x 16 diagonal blocks by forward
+// substitution (one column per thread); levels 1 and 2 form the off-diagonal blocks from block rows of
+// (I + A) T = I as TF32 warp-level tile products.  Each product reads A before a barrier and writes T after
+// it.  The upper triangle of the 32 x 32 diagonal blocks must hold zeros on entry (the epilogue writes them);
+// the block above the diagonal of the full matrix is never read.  Every thread passes every barrier.
+__device__ void solve_unit_lower_inplace(float* Am, float* Rt, int t, bool work) {
+    const int w = t >> 5, lane = t & 31;
+    if (work && t < 64) {
+        const int b = t >> 4, c = t & 15, o = 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+#pragma unroll
+            for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-Am[(o + r) * TS + o + j], x[j], x[r]);
+        }
+        __syncwarp();   // the 16 columns of a block belong to one half-warp: all reads before any write
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Am[(o + r) * TS + o + c] = x[r];
+    }
+    __syncthreads();
+    // level 1: pair pr of 16-blocks (rows 32 pr + 16.., columns 32 pr..), column half nt; R = A_21 T_11
+    const int pr = w >> 1, nt = w & 1, o1 = 32 * pr;
+    if (work && w < 4) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+            mma_tile_tf32(d, Am + (o1 + 16) * TS + o1 + 8 * ks, TS, Am + (o1 + 8 * ks) * TS + o1 + 8 * nt, TS, lane);
+        st_tile(Rt + (16 * pr) * RS + 8 * nt, RS, d, lane, 1.f);
+    }
+    __syncthreads();
+    if (work && w < 4) {   // T_21 = -T_22 R
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+            mma_tile_tf32(e, Am + (o1 + 16) * TS + o1 + 16 + 8 * ks, TS, Rt + (16 * pr + 8 * ks) * RS + 8 * nt, RS,
+                          lane);
+        st_tile(Am + (o1 + 16) * TS + o1 + 8 * nt, TS, e, lane, -1.f);
+    }
+    __syncthreads();
+    const int mt = w & 1, nq = w >> 1;   // level 2: 2 row tiles x 4 column tiles of 8
+    if (work) {   // R = A[32..63][0..31] T[0..31][0..31]
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_tile_tf32(d, Am + (32 + 16 * mt) * TS + 8 * ks, TS, Am + (8 * ks) * TS + 8 * nq, TS, lane);
+        st_tile(Rt + (16 * mt) * RS + 8 * nq, RS, d, lane, 1.f);
+    }
+    __syncthreads();
+    if (work) {   // T[32..63][0..31] = -T[32..63][32..63] R
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_tile_tf32(d, Am + (32 + 16 * mt) * TS + 32 + 8 * ks, TS, Rt + (8 * ks) * RS + 8 * nq, RS, lane);
+        st_tile(Am + (32 + 16 * mt) * TS + 8 * nq, TS, d, lane, -1.f);
+    }
+    __syncthreads();
+}
+
+// TMA loads of one item: K and Q as 2 x 2 boxes of 64 tokens x 64 columns, V as two boxes.
+__device__ __forceinline__ void intra_issue(uint8_t* smem, ISmall& S, const CUtensorMap* mq, const CUtensorMap* mk,
+                                            const CUtensorMap* mv, const Item& x) {
+    const int row = (int)x.row;
+    mbar_arrive_expect_tx(&S.full, 32768 + 16384);
+    uint8_t* kq = smem + I_KQ;
+    tma_load_3d(kq, mk, &S.full, 0, x.h, row);
+    tma_load_3d(kq + 8192, mq, &S.full, 0, x.h, row);
+    tma_load_3d(kq + 16384, mk, &S.full, 64, x.h, row);
+    tma_load_3d(kq + 16384 + 8192, mq, &S.full, 64, x.h, row);
+    tma_load_3d(smem + I_V, mv, &S.full, 0, x.h, row);
+    tma_load_3d(smem + I_V + 8192, mv, &S.full, 64, x.h, row);
+}
+
+// g and beta of an item (0 past its end): lane l holds tokens l and l + 32
+__device__ __forceinline__ void intra_load_gb(const IntraParams& p, const Item& x, int lane, float (&g)[2],
+                                              float (&b)[2]) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int r = lane + 32 * k;
+        const size_t tok = (size_t)(x.row + r) * p.geo.H + x.h;
+        g[k] = r < x.L ? __ldg(p.g + tok) : 0.f;
+        b[k] = r < x.L ? __ldg(p.beta + tok) : 0.f;
+    }
+}
+
+// gate prefix of the item in gbuf (one warp)
+__device__ __forceinline__ void intra_gate_prefix(ISmall& S, int lane) {
+    const float LOG2E = 1.4426950408889634f;
+    const float g0 = S.gbuf[2 * lane], g1 = S.gbuf[2 * lane + 1];
+    float x = g0 + g1;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, m);
+        if (lane >= m) x += y;
+    }
+    const float G1 = x * LOG2E, G0 = (x - g1) * LOG2E;
+    S.lg[2 * lane] = G0;
+    S.lg[2 * lane + 1] = G1;
+    const float Glast = __shfl_sync(0xffffffffu, G1, 31);
+    S.gam[2 * lane] = ex2(G0);
+    S.gam[2 * lane + 1] = ex2(G1);
+    S.kdec[2 * lane] = ex2(Glast - G0);
+    S.kdec[2 * lane + 1] = ex2(Glast - G1);
+    if (lane == 31) S.gC = ex2(Glast);
+}
+
+__global__ void __launch_bounds__(I_THREADS, 2)
+chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const IntraParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    ISmall& S = *reinterpret_cast<ISmall*>(smem + I_SMALL);
+    float* Am = reinterpret_cast<float*>(smem + I_AM);
+    float* Rt = reinterpret_cast<float*>(smem + I_RT);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3;                       // TMEM lane quarter of this warp
+    const int pw = warp >> 2;                      // which of the two warps on this quarter
+    const int row = 32 * q4 + lane;                // TMEM lane this thread reads
+    const int jrow = tid & 63, part = tid >> 6;    // (row, quarter of the columns) of the elementwise builds
+    const bool leader = (tid == 0);
+    const bool loader = (warp == 2);
+
+    if (warp == 0) {
+        tmem_alloc(&S.tmem_base, I_TM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        mbar_init(&S.full, 1);
+        mbar_init(&S.m0, 1);
+        mbar_init(&S.m1, 1);
+        mbar_init(&S.m2a, 1);
+        mbar_init(&S.m2b, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+
+    Item x;
+    long vi = next_item(p.geo, blockIdx.x, p.total, x);
+    float ng[2] = {0.f, 0.f}, nb[2] = {0.f, 0.f};   // g, beta of the next item (warp 1, in flight)
+    bool pending = false;                           // a TMA load was issued and not yet waited on
+    if (vi < p.total) {
+        if (loader && lane == 0) {
+            prefetch_tmap(&tmap_q);
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+            intra_issue(smem, S, &tmap_q, &tmap_k, &tmap_v, x);
+        }
+        pending = true;
+        if (warp == 1) {
+            float gg[2], bb[2];
+            intra_load_gb(p, x, lane, gg, bb);
+            S.gbuf[lane] = gg[0];
+            S.gbuf[lane + 32] = gg[1];
+            S.bbuf[lane] = bb[0];
+            S.bbuf[lane + 32] = bb[1];
+        }
+    }
+    bool ok = true;
+    uint32_t ic = 0;   // items done by this CTA: the parity of every barrier phase
+    while (vi < p.total) {
+        const Item cur = x;
+        Item nx;
+        const long vn = next_item(p.geo, vi + gridDim.x, p.total, nx);
+        const uint32_t par = ic & 1;
+        const int L = cur.L;
+        __syncthreads();   // g and beta of this item are in shared memory
+        if (warp == 1) {
+            intra_gate_prefix(S, lane);
+            if (vn < p.total) intra_load_gb(p, nx, lane, ng, nb);
+        }
+        if (ok) ok = mbar_wait(&S.full, par, kWaitNs);
+        if (!ok && tid == 0) set_status(1u);
+        pending = pending && !ok;
+        // MMA0: D0 = [K; Q] K^T
+        if (ok && leader) {
+            tc_fence_after();
+            const uint32_t id = idesc_f16(128, 64, true, false, false);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t a = sbase + I_KQ + (ks >> 2) * 16384 + (ks & 3) * 32;
+                mma_f16(tmem + I_TM_D0, sdesc(a, 16, 1024), sdesc(a, 16, 1024), id, ks > 0);
+            }
+            mma_commit(&S.m0);
+            ok = mbar_wait(&S.m0, par, kWaitNs);
+            if (!ok) set_status(2u);
+        }
+        __syncthreads();   // D0 ready, gate prefix ready
+        tc_fence_after();
+        if (ok) epilogue_kkt(tl + I_TM_D0, row, q4, pw, S.lg, S.bbuf, p.scale, Am, smem + I_A1);
+        tc_fence_before();
+        __syncthreads();
+        // UT transform, T = (I + A)^{-1} in place
+        solve_unit_lower_inplace(Am, Rt, tid, ok);
+        // T to fp16, MN-major [j][n] (operand B of MMA1)
+        if (ok) {
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int e = tid + I_THREADS * it, j = e >> 3, c8 = e & 7;
+                const float4 x0 = ld4(Am + j * TS + c8 * 8), x1 = ld4(Am + j * TS + c8 * 8 + 4);
+                const float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                float gq[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) gq[q] = (c8 * 8 + q <= j) ? f[q] : 0.f;
+                st_h8(smem + I_B1 + sw128_off(j, c8 * 8), gq);
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+        // MMA1: D1 = [I; P] T
+        if (ok && leader) {
+            tc_fence_after();
+            const uint32_t id = idesc_f16(128, 64, false, false, true);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16(tmem + I_TM_D1, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
+                        sdesc(sbase + I_B1 + ks * 2048, 8192, 1024), id, ks > 0);
+            mma_commit(&S.m1);
+        }
+        // X = [beta gamma K | beta V] (operand B of MMA2a/b), fp16 MN-major [j][n], four 64-column slabs; the
+        // fp32 T it overwrites was consumed before the barrier.  Thread (jrow, part): slab `part`, row jrow.
+        if (ok) {
+            const bool zero = jrow >= L;
+            const float sc = part < 2 ? S.bbuf[jrow] * S.gam[jrow] : S.bbuf[jrow];
+            const uint8_t* src = part < 2 ? smem + I_KQ + part * 16384 : smem + I_V + (part - 2) * 8192;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const uint32_t o8 = sw128_off(jrow, c8 * 8);
+                copy_scaled_chunk(src + o8, smem + I_B2 + part * 8192 + o8, sc, zero);
+            }
+        }
+        // epilogue 1: [T; PT] to fp16 into A1 (operand A of MMA2); columns [32 pw, 32 pw + 32)
+        if (ok) ok = mbar_wait(&S.m1, par, kWaitNs);
+        if (!ok && tid == 0) set_status(4u);
+        tc_fence_after();
+        if (ok) {
+            uint32_t r[2][16];
+            tmem_ld16(tl + I_TM_D1 + 32 * pw, r[0]);
+            tmem_ld16(tl + I_TM_D1 + 32 * pw + 16, r[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float f[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[cc >> 1][(cc & 1) * 8 + q]);
+                st_h8(smem + I_A1 + sw128_off(row, 32 * pw + cc * 8), f);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // MMA2a: D2a = [T; PT] beta gamma K (W | P W);  MMA2b: D2b = [T; PT] beta V (U | P U), over D0/D1
+        if (ok && leader) {
+            tc_fence_after();
+            const uint32_t id = idesc_f16(128, 128, false, false, true);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16(tmem + I_TM_D2A, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
+                        sdesc(sbase + I_B2 + ks * 2048, 8192, 1024), id, ks > 0);
+            mma_commit(&S.m2a);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16(tmem + I_TM_D2B, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
+                        sdesc(sbase + I_B2 + 16384 + ks * 2048, 8192, 1024), id, ks > 0);
+            mma_commit(&S.m2b);
+        }
+        const Ws& ws = p.ws;
+        // Ktilde = diag(gamma_C / gamma) K to the workspace, MN-major [j][c] like the K tile
+        if (ok) {
+            uint8_t* dst = ws.kt + (size_t)cur.it * WS_KT;
+            const bool zero = jrow >= L;
+            const float sd = S.kdec[jrow];
+            const int slab = part >> 1;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t o8 = sw128_off(jrow, (4 * (part & 1) + cc) * 8);
+                float f[8];
+                bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + o8), f);
+                const uint32_t m = zero ? 0u : 0xFFFFFFFFu;
+                stg16(dst + slab * 8192 + o8, pack_h2(f[0] * sd, f[1] * sd) & m, pack_h2(f[2] * sd, f[3] * sd) & m,
+                      pack_h2(f[4] * sd, f[5] * sd) & m, pack_h2(f[6] * sd, f[7] * sd) & m);
+            }
+            if (warp == 3) {
+                const float gc = S.gC;
+                __stcg(reinterpret_cast<float4*>(ws.gc + (size_t)cur.it * 128) + lane, make_float4(gc, gc, gc, gc));
+            }
+        }
+        // epilogue 2a: W (rows 0-63) and Q' = scale gamma Q - P W (rows 64-127) -> [W; Q']; thread: slab pw
+        if (ok) ok = mbar_wait(&S.m2a, par, kWaitNs);
+        if (!ok && tid == 0) set_status(8u);
+        tc_fence_after();
+        if (ok) {
+            uint8_t* dst = ws.wq + (size_t)cur.it * WS_WQ + pw * 16384;
+            const uint8_t* kqs = smem + I_KQ + pw * 16384;
+            uint32_t r[4][16];
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + I_TM_D2A + pw * 64 + cb * 16, r[cb]);
+            tmem_ld_wait();
+            if (row < 64) {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float f[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
+                    stg_h8(dst + sw128_off(row, c8 * 8), f);
+                }
+            } else {
+                const float qs = p.scale * S.gam[row - 64];
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float qv[8], f[8];
+                    bf16x8_to_f32(ld16(kqs + sw128_off(row, c8 * 8)), qv);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) f[q] = fmaf(qs, qv[q], -__uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]));
+                    stg_h8(dst + sw128_off(row, c8 * 8), f);
+                }
+            }
+        }
+        // epilogue 2b: U (rows 0-63) and U' (rows 64-127) -> [U; U'] of d_v half pw
+        if (ok) ok = mbar_wait(&S.m2b, par, kWaitNs);
+        if (!ok && tid == 0) set_status(16u);
+        tc_fence_after();
+        if (ok) {
+            uint8_t* dst = ws.uu + (size_t)cur.it * WS_UU + pw * 16384;
+            uint32_t r[4][16];
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + I_TM_D2B + pw * 64 + cb * 16, r[cb]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float f[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
+                stg_h8(dst + sw128_off(row, c8 * 8), f);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();   // the item's tiles and TMEM columns are free
+        if (ok && vn < p.total) {
+            if (loader && lane == 0) intra_issue(smem, S, &tmap_q, &tmap_k, &tmap_v, nx);
+            pending = true;
+            if (warp == 1) {
+                S.gbuf[lane] = ng[0];
+                S.gbuf[lane + 32] = ng[1];
+                S.bbuf[lane] = nb[0];
+                S.bbuf[lane + 32] = nb[1];
+            }
+        }
+        x = nx;
+        vi = ok ? vn : p.total;
+        if (ok) ++ic;   // after a timeout ic stays at the item whose load may still be in flight
+    }
+    // a load that was issued but never waited on (after a timeout) must land before the CTA exits
+    if (pending && loader && lane == 0) mbar_wait(&S.full, ic & 1, kWaitNs);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, I_TM_COLS);
+}
+
+// ==================================================================== pass 2: state pass
+struct StateParams {
+    Geo geo;
+    const float* h0;
+    float* hT;
+    void* o;
+    Ws ws;
+};
+
+constexpr uint32_t S_WQ = 0, S_KT = 32768, S_UU = 49152, S_GC = 65536;
+constexpr uint32_t S_STAGE = 66560;                 // one workspace slot (this CTA's d_v half of [U; U'])
+constexpr uint32_t S_H = 2 * S_STAGE;               // h, fp16 MN-major [d][n] 128 x 64
+constexpr uint32_t S_D = S_H + 16384;               // Delta, fp16 MN-major [j][n] 64 x 64
+constexpr uint32_t S_SMALL = S_D + 8192;
+struct SSmall {
+    uint64_t full[2];
+    uint64_t m3, m4;
+    uint32_t tmem_base;
+    uint32_t pad;
+};
+constexpr uint32_t S_SMEM = S_SMALL + sizeof(SSmall) + 1024;
+constexpr uint32_t S_TM_D3 = 0, S_TM_D4 = 64, S_TM_COLS = 128;
+constexpr int S_THREADS = 128;
+
+struct Chain {
+    int n, h, half, len;
+    long row0;
+};
+
+// CTA -> (sequence, head, d_v half); packed sequences longest first (their chains are the longest serial paths)
+__device__ Chain resolve_chain(const Geo& g) {
+    Chain c;
+    const int per_seq = g.H * 2;
+    const int seq_rank = blockIdx.x / per_seq;
+    const int rem = blockIdx.x % per_seq;
+    c.h = rem / 2;
+    c.half = rem % 2;
+    int n = seq_rank;
+    if (g.cu && g.n_seqs <= 32) {
+        const int lane = threadIdx.x & 31;
+        int rank = -1;
+        if (lane < g.n_seqs) {
+            long s0;
+            int lm;
+            g.seq(lane, s0, lm);
+            rank = 0;
+            for (int m2 = 0; m2 < g.n_seqs; ++m2) {
+                long s2;
+                int l2;
+                g.seq(m2, s2, l2);
+                rank += (l2 > lm) || (l2 == lm && m2 < lane);
+            }
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, rank == seq_rank);
+        if (hit) n = __ffs(hit) - 1;
+    }
+    c.n = n;
+    g.seq(n, c.row0, c.len);
+    return c;
+}
+
+__device__ __forceinline__ void state_issue(uint8_t* smem, SSmall& S, const Ws& ws, long it, int half, int s) {
+    uint8_t* st = smem + s * S_STAGE;
+    mbar_arrive_expect_tx(&S.full[s], WS_WQ + WS_KT + 16384 + WS_GC);
+    bulk_g2s(st + S_WQ, ws.wq + (size_t)it * WS_WQ, WS_WQ, &S.full[s]);
+    bulk_g2s(st + S_KT, ws.kt + (size_t)it * WS_KT, WS_KT, &S.full[s]);
+    bulk_g2s(st + S_UU, ws.uu + (size_t)it * WS_UU + half * 16384, 16384, &S.full[s]);
+    bulk_g2s(st + S_GC, ws.gc + (size_t)it * 128, WS_GC, &S.full[s]);
+}
+
+template <bool O_F32>
+__global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StateParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    SSmall& S = *reinterpret_cast<SSmall*>(smem + S_SMALL);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const Chain ch = resolve_chain(p.geo);
+    const int n_chunks = (ch.len + C - 1) / C;
+    const long slot0 = ch.row0 / C + ch.n;
+    const int H = p.geo.H;
+    const int row = 32 * warp + lane;           // TMEM lane: token row of D3, d_k row of D4 and of h
+    const bool leader = (tid == 0);
+    const bool delta_warp = warp < 2;
+
+    if (warp == 0) {
+        tmem_alloc(&S.tmem_base, S_TM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        mbar_init(&S.full[0], 1);
+        mbar_init(&S.full[1], 1);
+        mbar_init(&S.m3, 1);
+        mbar_init(&S.m4, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+
+    if (leader) {
+        for (int t = 0; t < 2 && t < n_chunks; ++t) state_issue(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
+    }
+    int issued = n_chunks < 2 ? n_chunks : 2;
+
+    const size_t sidx = ((size_t)ch.n * H + ch.h) * DK * DV + (size_t)row * DV + ch.half * DVT;
+    float hreg[DVT];
+#pragma unroll
+    for (int q = 0; q < DVT / 4; ++q) {
+        const float4 v = p.h0 ? reinterpret_cast<const float4*>(p.h0 + sidx)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        hreg[4 * q] = v.x;
+        hreg[4 * q + 1] = v.y;
+        hreg[4 * q + 2] = v.z;
+        hreg[4 * q + 3] = v.w;
+    }
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + S_H + sw128_off(row, c8 * 8), hreg + c8 * 8);
+    fence_async_smem();
+    __syncthreads();
+
+    bool ok = true;
+    int waited = 0;   // chunks whose stage wait completed
+    for (int t = 0; t < n_chunks; ++t) {
+        const int s = t & 1;
+        const uint8_t* st = smem + s * S_STAGE;
+        const uint32_t stb = sbase + s * S_STAGE;
+        const int L = min(C, ch.len - t * C);
+        if (ok) ok = mbar_wait(&S.full[s], (t >> 1) & 1, kWaitNs);
+        if (!ok && tid == 0) set_status(32u);
+        if (ok) waited = t + 1;
+        // MMA3: D3 = [W; Q'] h
+        if (ok && leader) {
+            tc_fence_after();
+            const uint32_t id = idesc_f16(128, 64, false, false, true);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_f16(tmem + S_TM_D3, sdesc(stb + S_WQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                        sdesc(sbase + S_H + ks * 2048, 1024, 1024), id, ks > 0);
+            mma_commit(&S.m3);
+        }
+        if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
+        if (!ok && tid == 0) set_status(64u);
+        tc_fence_after();
+        const int i = row - 64;
+        const bool store_o = !delta_warp && i < L;
+        const size_t orow = ((size_t)(ch.row0 + (long)t * C + (row & 63)) * H + ch.h) * DV + ch.half * DVT;
+#pragma unroll
+        for (int hp = 0; hp < 4; ++hp) {
+            uint32_t a[16];
+            float u[16];
+            if (ok) {
+                tmem_ld16(tl + S_TM_D3 + hp * 16, a);
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    const uint4 v = ld16(st + S_UU + sw128_off(row, hp * 16 + h8 * 8));
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&w4[m]));
+                        u[h8 * 8 + 2 * m] = f2.x;
+                        u[h8 * 8 + 2 * m + 1] = f2.y;
+                    }
+                }
+                tmem_ld_wait();
+            }
+            if (ok && delta_warp) {
+                // Delta = U - W h (token rows 0-63) to fp16 MN-major [j][n] (operand B of MMA4)
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    float f[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) f[q] = u[h8 * 8 + q] - __uint_as_float(a[h8 * 8 + q]);
+                    st_h8(smem + S_D + sw128_off(row, hp * 16 + h8 * 8), f);
+                }
+            } else if (ok && store_o) {
+                // O = U' + Q' h (token rows 64-127)
+                float f[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) f[k] = u[k] + __uint_as_float(a[k]);
+                if (O_F32) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + hp * 16);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow + hp * 16);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * q + 2 * m], f[8 * q + 2 * m + 1]);
+                            pk[m] = *reinterpret_cast<uint32_t*>(&b2);
+                        }
+                        dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            }
+        }
+        if (delta_warp) {
+            fence_async_smem();
+            tc_fence_before();
+            named_bar(1, 64);
+            // MMA4: D4 = Ktilde^T Delta
+            if (ok && leader) {
+                tc_fence_after();
+                const uint32_t id = idesc_f16(128, 64, false, true, true);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tmem + S_TM_D4, sdesc(stb + S_KT + ks * 2048, 8192, 1024),
+                            sdesc(sbase + S_D + ks * 2048, 1024, 1024), id, ks > 0);
+                mma_commit(&S.m4);
+            }
+        }
+        if (ok) ok = mbar_wait(&S.m4, t & 1, kWaitNs);
+        if (!ok && tid == 0) set_status(128u);
+        tc_fence_after();
+        // h <- gamma_C h + Ktilde^T Delta; fp16 copy for the next MMA3
+        if (ok) {
+            const float gC = reinterpret_cast<const float*>(st + S_GC)[row];
+            uint32_t r[4][16];
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + S_TM_D4 + cb * 16, r[cb]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 64; ++k) hreg[k] = fmaf(gC, hreg[k], __uint_as_float(r[k >> 4][k & 15]));
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + S_H + sw128_off(row, c8 * 8), hreg + c8 * 8);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();   // stage s, D3, D4 and Delta are free
+        if (ok && leader && t + 2 < n_chunks) {
+            state_issue(smem, S, p.ws, (slot0 + t + 2) * H + ch.h, ch.half, s);
+            issued = t + 3;
+        }
+    }
+    // stages issued but never waited on (after a timeout) must land before the CTA exits
+    if (leader) {
+        for (int t = waited; t < issued; ++t) mbar_wait(&S.full[t & 1], (t >> 1) & 1, kWaitNs);
+    }
+    if (p.hT && ok) {
+#pragma unroll
+        for (int q = 0; q < DVT / 4; ++q)
+            reinterpret_cast<float4*>(p.hT + sidx)[q] =
+                make_float4(hreg[4 * q], hreg[4 * q + 1], hreg[4 * q + 2], hreg[4 * q + 3]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, S_TM_COLS);
+}
+
+long n_slots(const ChunkArgs& a) { return (long)a.B * a.T / C + a.N() + 1; }
+
+}  // namespace
+
+const char* two_pass_unsupported_reason(const ChunkArgs& a) {
+    if (a.per_channel) return "per-channel (KDA) gates use another kernel";
+    if (!a.bf16) return "q, k, v must be bf16";
+    if (a.dk != DK || a.dv != DV) return "d_k and d_v must be 128";
+    if (a.C != C) return "chunk_size must be 64";
+    auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0; };
+    if (!al16(a.q) || !al16(a.k) || !al16(a.v) || !al16(a.o) || (a.h0 && !al16(a.h0)) || (a.hT && !al16(a.hT)))
+        return "tensors must be 16-byte aligned";
+    return nullptr;
+}
+
+size_t two_pass_workspace_bytes(const ChunkArgs& a) {
+    if ((long)a.B * a.T == 0) return 0;
+    return (size_t)n_slots(a) * a.H * WS_ITEM;
+}
+
+cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+    const long chains = (long)a.N() * a.H;
+    if (chains == 0) return cudaSuccess;
+    if (!device_is_sm100_family()) return cudaErrorNoKernelImageForDevice;
+    const long rows = (long)a.B * a.T;
+    if (rows == 0) {
+        if (a.hT) {
+            const size_t bytes = (size_t)a.N() * a.H * DK * DV * sizeof(float);
+            return a.h0 ? cudaMemcpyAsync(a.hT, a.h0, bytes, cudaMemcpyDeviceToDevice, s)
+                        : cudaMemsetAsync(a.hT, 0, bytes, s);
+        }
+        return cudaSuccess;
+    }
+    const size_t need = two_pass_workspace_bytes(a);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % 256) != 0)
+        return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.q, rows, a.H, DK) || !make_map(&mk, a.k, rows, a.H, DK) || !make_map(&mv, a.v, rows, a.H, DV))
+        return cudaErrorInvalidValue;
+    const long items = n_slots(a) * a.H;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    Ws ws;
+    ws.wq = base;
+    ws.kt = ws.wq + (size_t)items * WS_WQ;
+    ws.uu = ws.kt + (size_t)items * WS_KT;
+    ws.gc = reinterpret_cast<float*>(ws.uu + (size_t)items * WS_UU);
+    Geo geo{a.cu, a.n_seqs, a.B, a.T, a.H};
+
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    IntraParams ip{geo, a.g, a.beta, a.scale, items, ws};
+    e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)I_SMEM);
+    if (e != cudaSuccess) return e;
+    const long grid1 = items < 2L * sms ? items : 2L * sms;
+    chunk_intra_kernel<<<(unsigned)grid1, I_THREADS, I_SMEM, s>>>(mq, mk, mv, ip);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    StateParams sp{geo, a.h0, a.hT, a.o, ws};
+    const unsigned grid2 = (unsigned)(chains * 2);
+    if (a.o_f32) {
+        e = cudaFuncSetAttribute(chunk_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
+        if (e != cudaSuccess) return e;
+        chunk_state_kernel<true><<<grid2, S_THREADS, S_SMEM, s>>>(sp);
+    } else {
+        e = cudaFuncSetAttribute(chunk_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
+        if (e != cudaSuccess) return e;
+        chunk_state_kernel<false><<<grid2, S_THREADS, S_SMEM, s>>>(sp);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t tp_read_and_clear_status(unsigned* value, bool clear) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(value, g_tp_status, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    if (clear && *value) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_tp_status, &zero, sizeof(unsigned));
+    }
+    return e;
+}
+
+}  // namespace gdn

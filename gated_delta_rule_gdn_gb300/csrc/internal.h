@@ -2,7 +2,9 @@
 // Not installed; include/gdn.h is the public boundary.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cstddef>
 #include <cstdint>
 
 namespace gdn {
@@ -49,10 +51,22 @@ cudaError_t launch_chunk_generic(const ChunkArgs& a, cudaStream_t s);
 const char* tc_chunk_unsupported_reason(const ChunkArgs& a);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s);
 
+// Two-pass tcgen05 chunk path (chunk_two_pass.cu): a per-chunk kernel over all SMs writes the
+// S-independent products to a workspace, then a state kernel walks each chain.
+const char* two_pass_unsupported_reason(const ChunkArgs& a);
+size_t two_pass_workspace_bytes(const ChunkArgs& a);
+cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s);
+
+// Shared host helpers of the tcgen05 paths (chunk_tc.cu).
+// TMA map of a [rows][H][d] bf16 tensor, box 64 elements x 1 head x 64 rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, long rows, int H, int d);
+bool device_is_sm100_family();
+
 // Decode step (recurrent_step.cu).
 cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t s);
 
 // Device-side status words of kernels with bounded waits.
 cudaError_t tc_read_and_clear_status(unsigned* value, bool clear);
+cudaError_t tp_read_and_clear_status(unsigned* value, bool clear);
 
 }  // namespace gdn

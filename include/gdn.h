@@ -67,10 +67,15 @@ typedef enum gdn_dtype {
 
 /* Kernel choice for the chunk forward. */
 typedef enum gdn_algo {
-    GDN_ALGO_AUTO = 0,     /* the fused tensor-core kernel where it applies, else the generic one */
-    GDN_ALGO_GENERIC = 1,  /* fp32 SIMT chunk kernel: any dtype, 1 <= d_k, d_v <= 128 */
-    GDN_ALGO_TCGEN05 = 2   /* fused tcgen05/TMA kernel: bf16, d_k = d_v = 128, chunk 64;
-                              GDN_ERR_UNSUPPORTED when the request does not fit it */
+    GDN_ALGO_AUTO = 0,      /* the fastest tensor-core path that applies, else the generic one */
+    GDN_ALGO_GENERIC = 1,   /* fp32 SIMT chunk kernel: any dtype, 1 <= d_k, d_v <= 128 */
+    GDN_ALGO_TCGEN05 = 2,   /* fused tcgen05/TMA kernel (one CTA per chain does every stage):
+                               bf16, d_k = d_v = 128, chunk 64, scalar gate;
+                               GDN_ERR_UNSUPPORTED when the request does not fit it */
+    GDN_ALGO_TWO_PASS = 3   /* tcgen05 in two passes: a per-chunk kernel over all SMs writes the
+                               state-independent products to a device workspace, then a state
+                               kernel walks each chain.  bf16, d_k = d_v = 128, chunk 64;
+                               GDN_ERR_UNSUPPORTED when the request does not fit it */
 } gdn_algo;
 
 /*
@@ -122,6 +127,26 @@ gdn_status gdn_chunk_fwd_algo(const void* q, const void* k, const void* v, const
                               gdn_dtype o_dtype, gdn_algo algo, void* stream);
 
 /*
+ * gdn_chunk_fwd_ws -- gdn_chunk_fwd with an explicit kernel choice and a
+ * caller-provided device workspace for the kernels that need one
+ * (GDN_ALGO_TWO_PASS; see gdn_chunk_workspace_size).
+ *   workspace        device memory, 256-byte aligned, at least the size
+ *                    gdn_chunk_workspace_size reports; owned by the caller and
+ *                    used only by the work this call enqueues on `stream`, so
+ *                    it may be reused once that work is ordered before the
+ *                    reuse.  Two calls in flight at once must not share it.
+ *                    NULL: the library allocates it on `stream` for the call
+ *                    (stream-ordered allocation) and frees it after the work.
+ *   workspace_bytes  its size; GDN_ERR_INVALID_ARG if too small.
+ */
+gdn_status gdn_chunk_fwd_ws(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            float scale, const float* initial_state, int output_final_state,
+                            float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o,
+                            int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                            gdn_dtype o_dtype, gdn_algo algo, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * kda_chunk_fwd -- chunkwise forward of Kimi Delta Attention.  The retention
  * is a per-key-channel vector exp(g_t), applied as Diag(exp g_t) on the key
  * side of the state before the delta update.
@@ -147,6 +172,14 @@ gdn_status kda_chunk_fwd_algo(const void* q, const void* k, const void* v, const
                               int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
                               gdn_dtype o_dtype, gdn_algo algo, void* stream);
 
+/* kda_chunk_fwd with an explicit kernel choice and workspace, as gdn_chunk_fwd_ws. */
+gdn_status kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            float scale, const float* initial_state, int output_final_state,
+                            float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o,
+                            int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                            gdn_dtype o_dtype, gdn_algo algo, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /*
  * gdn_recurrent_step -- one decode token for N independent sequences.
  *
@@ -170,13 +203,25 @@ gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const
  * The buffers are assumed to be 16-byte aligned.  per_channel nonzero stands
  * for kda_chunk_fwd; varlen nonzero stands for a call with cu_seqlens.
  * requested is resolved into *chosen: GDN_ALGO_AUTO becomes
- * GDN_ALGO_TCGEN05 or GDN_ALGO_GENERIC.  The status is the one the call
+ * GDN_ALGO_TWO_PASS, GDN_ALGO_TCGEN05 or GDN_ALGO_GENERIC.  The status is the one the call
  * itself would return for these sizes, and *chosen is written only on GDN_OK.
  * Nothing is launched.
  */
 gdn_status gdn_chunk_plan(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
                           gdn_dtype dtype, gdn_dtype o_dtype, int varlen, gdn_algo requested,
                           gdn_algo* chosen);
+
+/*
+ * gdn_chunk_workspace_size -- device workspace bytes of a chunk-forward call
+ * with these sizes and kernel request (0 when the resolved kernel needs
+ * none).  n_seqs is 0 for a call without cu_seqlens, else its number of
+ * packed sequences.  The two-pass kernels keep, per (chunk slot, head),
+ * 82,432 bytes: [W; Q'], Ktilde, [U; U'] in fp16 and gamma_C; there are
+ * floor(B*T / 64) + N + 1 slots.  Same status rules as gdn_chunk_plan.
+ */
+gdn_status gdn_chunk_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
+                                    gdn_dtype dtype, gdn_dtype o_dtype, int n_seqs, gdn_algo requested,
+                                    size_t* bytes);
 
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* gdn_last_error(void);

@@ -90,3 +90,36 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 4, 1, 8)
     with pytest.raises(ValueError):
         gdn.gdn_chunk_fwd(x, x, x, torch.zeros(1, 4, 1), torch.zeros(1, 4, 1))
+
+
+def test_plan_and_workspace_sizes(lib):
+    import torch
+    bf = torch.bfloat16
+    # the prefill shape resolves to the two-pass tcgen05 path; fp32 and small heads to the generic kernel
+    assert _binding.chunk_plan(False, 4, 4096, 16, 128, 128, 64, bf) == "two_pass"
+    assert _binding.chunk_plan(False, 4, 4096, 16, 128, 128, 64, bf, algo="tcgen05") == "tcgen05"
+    assert _binding.chunk_plan(False, 1, 64, 1, 16, 16, 16, torch.float32) == "generic"
+    # 82,432 bytes per (chunk slot, head); floor(B T / 64) + N + 1 slots
+    assert _binding.workspace_size(False, 4, 4096, 16, 128, 128, 64, bf) == (256 + 4 + 1) * 16 * 82432
+    assert _binding.workspace_size(False, 1, 65536, 32, 128, 128, 64, bf, n_seqs=8) == (1024 + 8 + 1) * 32 * 82432
+    assert _binding.workspace_size(False, 4, 4096, 16, 128, 128, 64, bf, algo="tcgen05") == 0
+    assert _binding.workspace_size(False, 1, 64, 1, 16, 16, 16, torch.float32) == 0
+    with pytest.raises(_binding.GdnError):
+        _binding.workspace_size(False, 1, 64, 1, 64, 64, 64, bf, algo="two_pass")
+
+
+def _chunk_ws(lib, ws, ws_bytes, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=1.0, h0=None, ofs=0, hT=None, cu=None, n=0, o=FAKE,
+             B=1, T=64, H=1, dk=128, dv=128, C=64, dtype=1, odt=0, algo=3)
+    a.update(kw)
+    return lib.gdn_chunk_fwd_ws(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["h0"], a["ofs"], a["hT"],
+                                a["cu"], a["n"], a["o"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["C"], a["dtype"],
+                                a["odt"], a["algo"], ws, ws_bytes, None)
+
+
+def test_workspace_argument_checks(lib):
+    need = (1 + 1 + 1) * 1 * 82432
+    assert _chunk_ws(lib, FAKE, need - 16) == 1            # too small
+    assert "workspace" in _binding.last_error()
+    assert _chunk_ws(lib, FAKE + 16, need) == 1            # not 256-byte aligned
+    assert _chunk_ws(lib, FAKE, need, dk=64, dv=64) == 2   # the two-pass kernels need d = 128

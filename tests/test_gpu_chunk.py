@@ -28,30 +28,30 @@ def _lib():
     gdn.load()
 
 
-def _tc_fits(x):
-    """True if the library's tcgen05 kernel accepts this problem (asked through gdn_chunk_plan)."""
+def _fits(x, algo):
+    """True if the library's kernel `algo` accepts this problem (asked through gdn_chunk_plan)."""
     B, T, H, dk = x["q"].shape
     try:
         gdn.chunk_plan(x["gate_per_channel"], B, T, H, dk, x["v"].shape[-1], x["chunk_size"], x["q"].dtype,
-                       x["cu_seqlens"] is not None, "tcgen05")
+                       x["cu_seqlens"] is not None, algo)
         return True
     except gdn.GdnError:
         return False
 
 
-def _run(x, algo="auto", out_final=True, o_dtype=torch.float32):
+def _run(x, algo="auto", out_final=True, o_dtype=torch.float32, workspace=None):
     d = to_dev(x)
     fn = gdn.kda_chunk_fwd if x["gate_per_channel"] else gdn.gdn_chunk_fwd
     o, hT = fn(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["initial_state"],
                output_final_state=out_final, cu_seqlens=d["cu_seqlens"], chunk_size=x["chunk_size"], algo=algo,
-               o_dtype=o_dtype)
+               o_dtype=o_dtype, workspace=workspace)
     torch.cuda.synchronize()
     assert gdn.device_status() == 0
     return o.double().cpu().numpy(), (None if hT is None else hT.double().cpu().numpy())
 
 
 def _algos(x):
-    return ["generic", "tcgen05"] if _tc_fits(x) else ["generic"]
+    return ["generic"] + [a for a in ("tcgen05", "two_pass") if _fits(x, a)]
 
 
 def _workload(kind, dtype, dk, dv, C, h0_std):
@@ -181,26 +181,72 @@ def test_kda_with_equal_channels_matches_gdn():
 
 # --- full-size workloads, in the launch configuration the benchmark times -------------------
 
-def test_benchmark_workload_runs_the_tcgen05_kernel():
+def test_benchmark_workload_runs_a_tensor_core_kernel():
     w = W.config(1)
-    assert gdn.chunk_plan(False, w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16) == "tcgen05"
+    assert gdn.chunk_plan(False, w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16) == "two_pass"
 
 
-def test_full_config1_all_chains():
+@pytest.mark.parametrize("algo", ["auto", "tcgen05"])
+def test_full_config1_all_chains(algo):
     x = W.chunk_inputs(W.config(1), seed=0)
-    o_ref, h_ref = oracle_on_heads(x)
-    o, hT = _run(x, "auto")
+    o_ref, h_ref = _oracle_cached(1, x)
+    o, hT = _run(x, algo)
     assert_close(o, o_ref, torch.bfloat16, "o")
     assert_close(hT, h_ref, torch.bfloat16, "final state")
 
 
-def test_full_config2_varlen_sampled_heads():
+@pytest.mark.parametrize("algo", ["auto", "tcgen05"])
+def test_full_config2_varlen_sampled_heads(algo):
     x = W.chunk_inputs(W.config(2), seed=0)
     heads = [0, 9, 22, 31]
-    o_ref, h_ref = oracle_on_heads(x, heads)
-    o, hT = _run(x, "auto")
+    o_ref, h_ref = _oracle_cached(2, x, heads)
+    o, hT = _run(x, algo)
     assert_close(o[:, :, heads], o_ref, torch.bfloat16, "o")
     assert_close(hT[:, heads], h_ref, torch.bfloat16, "final state")
+
+
+_ORACLE = {}
+
+
+def _oracle_cached(key, x, heads=None):
+    if key not in _ORACLE:
+        _ORACLE[key] = oracle_on_heads(x, heads)
+    return _ORACLE[key]
+
+
+def test_two_pass_workspace_reuse_and_library_allocation():
+    """A caller workspace reused across calls, and the library's own stream-ordered allocation (C entry
+    point without a workspace), give bitwise the same result."""
+    x = W.chunk_inputs(W.config(1), seed=3, T=700, H=3)
+    B, T, H, dk = x["q"].shape
+    n = gdn.workspace_size(False, B, T, H, dk, dk, 64, torch.bfloat16, 0, "two_pass")
+    assert n == (B * T // 64 + B + 1) * H * 82432
+    ws = torch.full((n,), 0xA5, dtype=torch.uint8, device="cuda")
+    o1, h1 = _run(x, "two_pass", workspace=ws)
+    o2, h2 = _run(x, "two_pass", workspace=ws)
+    assert np.array_equal(o1, o2) and np.array_equal(h1, h2)
+    o3, h3 = _run_c_entry(x, "two_pass")
+    assert np.array_equal(o1, o3) and np.array_equal(h1, h3)
+    with pytest.raises(gdn.GdnError):
+        _run(x, "two_pass", workspace=ws[: n - 256])
+
+
+def _run_c_entry(x, algo):
+    """gdn_chunk_fwd_algo straight through ctypes: no workspace argument, so the library allocates one."""
+    import ctypes
+    lib = gdn.load()
+    d = to_dev(x)
+    B, T, H, dk = x["q"].shape
+    o = torch.empty((B, T, H, dk), dtype=torch.float32, device="cuda")
+    hT = torch.empty_like(d["initial_state"])
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = lib.gdn_chunk_fwd_algo(p(d["q"]), p(d["k"]), p(d["v"]), p(d["g"]), p(d["beta"]), float(x["scale"]),
+                                p(d["initial_state"]), 1, p(hT), None, 0, p(o), B, T, H, dk, dk, 64, 1, 0,
+                                gdn._binding.ALGOS[algo], ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, gdn.last_error()
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    return o.double().cpu().numpy(), hT.double().cpu().numpy()
 
 
 def test_full_config3_kda_sampled_heads():
