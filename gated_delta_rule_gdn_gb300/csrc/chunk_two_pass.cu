@@ -12,8 +12,8 @@
 //   [W | U ; P W | P U] = [T; P T] [beta gamma K | beta V]
 //   Q' = scale diag(gamma) Q - P W,  U' = P U,  Ktilde = diag(gamma_C / gamma) K
 // and writes [W; Q'], Ktilde, [U; U'] (fp16, already in the shared-memory operand layouts of pass 2) and
-// gamma_C to the workspace.  MMAs: D0 = [K; Q] K^T, D1 = [I; P] T, D2a = [T; PT] beta gamma K,
-// D2b = [T; PT] beta V (the last reuses the columns of D0 and D1), 256 TMEM columns per CTA.
+// gamma_C to the workspace.  MMAs: D0 = [K; Q] K^T, D1 = [I; P] T, D2 = [T; -PT] [beta V | beta gamma K] (N = 256,
+// accumulated onto [0 | 0; 0 | scale gamma Q] so that it yields [U | W; -U' | Q']), 256 TMEM columns per CTA.
 //
 // Pass 2, chunk_state_kernel: one CTA per (sequence, head, 64-column d_v half), 4 warps, h = S^T tile in fp32
 // registers (thread = d_k row).  Per chunk the workspace slot arrives by bulk copy (2-stage ring), then
@@ -98,60 +98,68 @@ struct IntraParams {
     const float* g;
     const float* beta;
     float scale;
-    long total;   // virtual items: slots x heads
+    long n_slots;
     Ws ws;
 };
 
 struct Item {
     int n, h, t, L;
     long row;     // first token row of the chunk
-    long it;      // workspace item index
+    long it;      // workspace item index (slot * H + head)
 };
 
-// Virtual item vi = slot * H + head -> the sequence whose slots contain it (binary search); false for the
-// unused slots between sequences.
-__device__ bool decode_item(const Geo& g, long vi, Item& x) {
-    const long s = vi / g.H;
-    x.h = (int)(vi - s * g.H);
-    int lo = 0, hi = g.N() - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (g.slot0(mid) <= s) lo = mid;
-        else hi = mid - 1;
+// A CTA visits the virtual items slot * H + head = blockIdx.x, blockIdx.x + gridDim.x, ...; the cursor keeps
+// (slot, head) and the sequence whose slots begin at or before the slot (non-decreasing along the walk).
+struct Cursor {
+    long s;
+    int h, n;
+};
+
+__device__ __forceinline__ void cursor_step(Cursor& c, int ds, int dh, int H) {
+    c.h += dh;
+    c.s += ds;
+    if (c.h >= H) {
+        c.h -= H;
+        ++c.s;
     }
-    long s0;
-    int len;
-    g.seq(lo, s0, len);
-    const long t = s - (s0 / C + lo);
-    if (t < 0 || t * C >= len) return false;
-    x.n = lo;
-    x.t = (int)t;
-    x.row = s0 + t * C;
-    x.L = min(C, len - (int)t * C);
-    x.it = vi;
-    return true;
 }
 
-__device__ long next_item(const Geo& g, long vi, long total, Item& x) {
-    for (; vi < total; vi += gridDim.x)
-        if (decode_item(g, vi, x)) return vi;
-    return total;
+// The first valid item at or after the cursor (slots between sequences are unused); false past the last slot.
+__device__ bool cursor_next_valid(const Geo& g, long n_slots, Cursor& c, int ds, int dh, Item& x) {
+    const int N = g.N();
+    for (; c.s < n_slots; cursor_step(c, ds, dh, g.H)) {
+        while (c.n + 1 < N && g.slot0(c.n + 1) <= c.s) ++c.n;
+        long s0;
+        int len;
+        g.seq(c.n, s0, len);
+        const long t = c.s - (s0 / C + c.n);
+        if (t < 0 || t * C >= len) continue;
+        x.n = c.n;
+        x.h = c.h;
+        x.t = (int)t;
+        x.row = s0 + t * C;
+        x.L = min(C, len - (int)t * C);
+        x.it = c.s * g.H + c.h;
+        return true;
+    }
+    return false;
 }
 
 // shared memory of pass 1 (bytes from a 1024-aligned base)
 constexpr uint32_t I_KQ = 0;        // [K; Q] rows, two K-slabs of 16 KB (K rows 0-63, Q rows 64-127)
-constexpr uint32_t I_V = 32768;     // V, two 64-column slabs of 8 KB
-constexpr uint32_t I_A1 = 49152;    // [I; P] then [T; PT], fp16 K-major 128 x 64
-constexpr uint32_t I_B1 = 65536;    // T, fp16 MN-major [j][n] 64 x 64
-constexpr uint32_t I_B2 = 73728;    // X = [beta gamma K | beta V], fp16 MN-major 64 x 256 (four slabs)
-constexpr uint32_t I_AM = I_B2;     // fp32 A, then T in place (row stride TS), before X is built
-constexpr uint32_t I_RT = I_B2 + 64 * TS * 4;
-constexpr uint32_t I_SMALL = I_B2 + 32768;
-static_assert(64 * TS * 4 + 32 * RS * 4 <= 32768, "A and the solve scratch must fit in the X buffer");
+constexpr uint32_t I_B2 = 32768;    // X = [beta V | beta gamma K], fp16 MN-major 64 x 256 in four 8 KB slabs; V
+                                    // lands in slabs 0-1 by TMA (bf16) and is scaled there in place
+constexpr uint32_t I_A1 = 65536;    // [I; P] then [T; -PT], fp16 K-major 128 x 64
+constexpr uint32_t I_B1 = 81920;    // T, fp16 MN-major [j][n] 64 x 64 (the solve's scratch before that)
+constexpr uint32_t I_AM = 90112;    // fp32 A, then T in place (row stride TS)
+constexpr uint32_t I_RT = I_B1;
+constexpr uint32_t I_SMALL = I_AM + 64 * TS * 4;
+static_assert(32 * RS * 4 <= 8192, "the solve scratch must fit in the T buffer");
 
 struct ISmall {
-    uint64_t full;            // inputs of the item landed (TMA transaction bytes)
-    uint64_t m0, m1, m2a, m2b;
+    uint64_t full_kq;         // K, Q of the item landed (TMA transaction bytes)
+    uint64_t full_v;          // V of the item landed
+    uint64_t m0, m1, m2b;
     uint32_t tmem_base;
     uint32_t pad;
     float gbuf[C];            // g of the item (0 past the end)
@@ -162,48 +170,83 @@ struct ISmall {
     float gC;
 };
 constexpr uint32_t I_SMEM = I_SMALL + sizeof(ISmall) + 1024;
-constexpr uint32_t I_TM_D0 = 0, I_TM_D1 = 64, I_TM_D2A = 128, I_TM_D2B = 0, I_TM_COLS = 256;
+// D2 = [U | W; -U' | Q'] spans all 256 columns: columns 128-255 hold [0; scale gamma Q] before MMA2 accumulates
+// onto them, columns 0-127 (D0 and D1 until then) are zeroed once D1 has been read
+constexpr uint32_t I_TM_D0 = 0, I_TM_D1 = 64, I_TM_D2 = 0, I_TM_QS = 128, I_TM_COLS = 256;
 constexpr int I_THREADS = 256;
 
+// Level 0 of the blocked inverse for the 16 x 16 diagonal block at offset o (one warp): the two 8 x 8 diagonal
+// sub-blocks by forward substitution (lane 8 s + c owns column c of sub-block s; their 28 coefficients are loaded
+// before the 8-step chain), then the block below them, T21 = -T22 (A21 T11), 8 x 8 products in fp32.  A is
+// overwritten by T in place; Rw is this warp's 64-float scratch.
+__device__ __forceinline__ void solve_block16(float* Am, float* Rw, int o, int lane) {
+    if (lane < 16) {
+        const int o8 = o + 8 * (lane >> 3), c = lane & 7;
+        float a[28];
+#pragma unroll
+        for (int r = 1; r < 8; ++r)
+#pragma unroll
+            for (int j = 0; j < r; ++j) a[r * (r - 1) / 2 + j] = Am[(o8 + r) * TS + o8 + j];
+        float x[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) x[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int r = j + 1; r < 8; ++r) x[r] = fmaf(-a[r * (r - 1) / 2 + j], x[j], x[r]);
+        __syncwarp(0x0000FFFFu);   // the sub-block's coefficients are read before any column is overwritten
+#pragma unroll
+        for (int r = 0; r < 8; ++r) Am[(o8 + r) * TS + o8 + c] = x[r];
+    }
+    __syncwarp();
+    const int i = lane >> 2, c2 = 2 * (lane & 3);   // row i, columns c2, c2 + 1 of the 8 x 8 products
+    float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float aik = Am[(o + 8 + i) * TS + o + k];
+        r0 = fmaf(aik, Am[(o + k) * TS + o + c2], r0);
+        r1 = fmaf(aik, Am[(o + k) * TS + o + c2 + 1], r1);
+    }
+    Rw[i * 8 + c2] = r0;
+    Rw[i * 8 + c2 + 1] = r1;
+    __syncwarp();   // A21 is read and R written by every lane
+    float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float tik = Am[(o + 8 + i) * TS + o + 8 + k];
+        t0 = fmaf(tik, Rw[k * 8 + c2], t0);
+        t1 = fmaf(tik, Rw[k * 8 + c2 + 1], t1);
+    }
+    Am[(o + 8 + i) * TS + o + c2] = -t0;
+    Am[(o + 8 + i) * TS + o + c2 + 1] = -t1;
+}
+
 // Blocked inverse of the unit lower-triangular (I + A), 64 x 64, in place: A (strictly lower, fp32, row stride
-// TS) is overwritten by T = (I + A)^{-1}.  Level 0 solves the four 16 x 16 diagonal blocks by forward
-// substitution (one column per thread); levels 1 and 2 form the off-diagonal blocks from block rows of
-// (I + A) T = I as TF32 warp-level tile products.  Each product reads A before a barrier and writes T after
-// it.  The upper triangle of the 32 x 32 diagonal blocks must hold zeros on entry (the epilogue writes them);
-// the block above the diagonal of the full matrix is never read.  Every thread passes every barrier.
+// TS) is overwritten by T = (I + A)^{-1}.  Level 0: the four 16 x 16 diagonal blocks, one warp each.  Level 1:
+// the 16 x 16 blocks below them in the two 32 x 32 diagonal blocks, T21 = -T22 (A21 T11).
+// Level 2: the 32 x 32 block, T21 = -T22 (A21 T11) over 8 warps with a barrier between the two products.
+// (Level 1 runs on two warps per block, column halves, with a pair barrier before T21 overwrites A21.)
+// Levels 1 and 2 are TF32 warp-level tile products with fp32 accumulation.  The upper triangle of every
+// 32 x 32 diagonal block must hold zeros on entry (the epilogue writes them); the block above the diagonal
+// of the whole matrix is never read.  Every thread passes every barrier.
 __device__ void solve_unit_lower_inplace(float* Am, float* Rt, int t, bool work) {
     const int w = t >> 5, lane = t & 31;
-    if (work && t < 64) {
-        const int b = t >> 4, c = t & 15, o = 16 * b;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-#pragma unroll
-            for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-Am[(o + r) * TS + o + j], x[j], x[r]);
-        }
-        __syncwarp();   // the 16 columns of a block belong to one half-warp: all reads before any write
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Am[(o + r) * TS + o + c] = x[r];
-    }
+    if (work && w < 4) solve_block16(Am, Rt + 64 * w, 16 * w, lane);
     __syncthreads();
-    // level 1: pair pr of 16-blocks (rows 32 pr + 16.., columns 32 pr..), column half nt; R = A_21 T_11
-    const int pr = w >> 1, nt = w & 1, o1 = 32 * pr;
-    if (work && w < 4) {
+    if (work && w < 4) {   // level 1: block pair pr, column half nt; R = A21 T11, then T21 = -T22 R
+        const int pr = w >> 1, nt = w & 1, o1 = 32 * pr;
+        float* Rw = Rt + 16 * pr * RS;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks)
             mma_tile_tf32(d, Am + (o1 + 16) * TS + o1 + 8 * ks, TS, Am + (o1 + 8 * ks) * TS + o1 + 8 * nt, TS, lane);
-        st_tile(Rt + (16 * pr) * RS + 8 * nt, RS, d, lane, 1.f);
-    }
-    __syncthreads();
-    if (work && w < 4) {   // T_21 = -T_22 R
+        st_tile(Rw + 8 * nt, RS, d, lane, 1.f);
+        if (pr == 0) named_bar(1, 64);   // both column halves have read A21 before T21 overwrites it
+        else named_bar(2, 64);
         float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks)
-            mma_tile_tf32(e, Am + (o1 + 16) * TS + o1 + 16 + 8 * ks, TS, Rt + (16 * pr + 8 * ks) * RS + 8 * nt, RS,
-                          lane);
+            mma_tile_tf32(e, Am + (o1 + 16) * TS + o1 + 16 + 8 * ks, TS, Rw + (8 * ks) * RS + 8 * nt, RS, lane);
         st_tile(Am + (o1 + 16) * TS + o1 + 8 * nt, TS, e, lane, -1.f);
     }
     __syncthreads();
@@ -226,18 +269,22 @@ __device__ void solve_unit_lower_inplace(float* Am, float* Rt, int t, bool work)
     __syncthreads();
 }
 
-// TMA loads of one item: K and Q as 2 x 2 boxes of 64 tokens x 64 columns, V as two boxes.
-__device__ __forceinline__ void intra_issue(uint8_t* smem, ISmall& S, const CUtensorMap* mq, const CUtensorMap* mk,
-                                            const CUtensorMap* mv, const Item& x) {
+// TMA loads of an item: K and Q as 2 x 2 boxes of 64 tokens x 64 columns; V as two boxes into X's V slabs.
+__device__ __forceinline__ void intra_issue_kq(uint8_t* smem, ISmall& S, const CUtensorMap* mq, const CUtensorMap* mk,
+                                               const Item& x) {
     const int row = (int)x.row;
-    mbar_arrive_expect_tx(&S.full, 32768 + 16384);
+    mbar_arrive_expect_tx(&S.full_kq, 32768);
     uint8_t* kq = smem + I_KQ;
-    tma_load_3d(kq, mk, &S.full, 0, x.h, row);
-    tma_load_3d(kq + 8192, mq, &S.full, 0, x.h, row);
-    tma_load_3d(kq + 16384, mk, &S.full, 64, x.h, row);
-    tma_load_3d(kq + 16384 + 8192, mq, &S.full, 64, x.h, row);
-    tma_load_3d(smem + I_V, mv, &S.full, 0, x.h, row);
-    tma_load_3d(smem + I_V + 8192, mv, &S.full, 64, x.h, row);
+    tma_load_3d(kq, mk, &S.full_kq, 0, x.h, row);
+    tma_load_3d(kq + 8192, mq, &S.full_kq, 0, x.h, row);
+    tma_load_3d(kq + 16384, mk, &S.full_kq, 64, x.h, row);
+    tma_load_3d(kq + 16384 + 8192, mq, &S.full_kq, 64, x.h, row);
+}
+__device__ __forceinline__ void intra_issue_v(uint8_t* smem, ISmall& S, const CUtensorMap* mv, const Item& x) {
+    const int row = (int)x.row;
+    mbar_arrive_expect_tx(&S.full_v, 16384);
+    tma_load_3d(smem + I_B2, mv, &S.full_v, 0, x.h, row);
+    tma_load_3d(smem + I_B2 + 8192, mv, &S.full_v, 64, x.h, row);
 }
 
 // g and beta of an item (0 past its end): lane l holds tokens l and l + 32
@@ -273,6 +320,16 @@ __device__ __forceinline__ void intra_gate_prefix(ISmall& S, int lane) {
     if (lane == 31) S.gC = ex2(Glast);
 }
 
+__device__ __forceinline__ uint4 scale_chunk_h(const float (&f)[8], float s, uint32_t m) {
+    return make_uint4(pack_h2(f[0] * s, f[1] * s) & m, pack_h2(f[2] * s, f[3] * s) & m, pack_h2(f[4] * s, f[5] * s) & m,
+                      pack_h2(f[6] * s, f[7] * s) & m);
+}
+
+// Per item: [A] gate prefix; [B] MMA0 = [K; Q] K^T runs while the threads build X (beta gamma K, and beta V in place),
+// write Ktilde and gamma_C, and stash [0; scale gamma Q] into TMEM columns 128-255; K and Q are then dead and the
+// next item's K, Q load is issued.  [C] epilogue of D0 -> A, [I; P]; the solve; T to fp16; MMA1 = [I; P] T;
+// [T; -P T] to fp16; MMA2 = D2 + [T; -PT] [beta V | beta gamma K] = [U | W; -U' | Q']; once MMA2 has read V the
+// next item's V load is issued; the epilogue writes [W; Q'] and [U; U'] to the workspace.
 __global__ void __launch_bounds__(I_THREADS, 2)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const IntraParams p) {
@@ -286,21 +343,21 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3;                       // TMEM lane quarter of this warp
-    const int pw = warp >> 2;                      // which of the two warps on this quarter
+    const int pw = warp >> 2;                      // which of the two warps on this quarter (64-column half)
     const int row = 32 * q4 + lane;                // TMEM lane this thread reads
-    const int jrow = tid & 63, part = tid >> 6;    // (row, quarter of the columns) of the elementwise builds
     const bool leader = (tid == 0);
-    const bool loader = (warp == 2);
+    const bool loader = (tid == 64);
+    const int H = p.geo.H;
 
     if (warp == 0) {
         tmem_alloc(&S.tmem_base, I_TM_COLS);
         tmem_relinquish();
     }
     if (tid == 32) {
-        mbar_init(&S.full, 1);
+        mbar_init(&S.full_kq, 1);
+        mbar_init(&S.full_v, 1);
         mbar_init(&S.m0, 1);
         mbar_init(&S.m1, 1);
-        mbar_init(&S.m2a, 1);
         mbar_init(&S.m2b, 1);
         fence_mbar_init();
     }
@@ -310,18 +367,21 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const uint32_t tmem = S.tmem_base;
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
 
+    const int ds = (int)(gridDim.x / H), dh = (int)(gridDim.x % H);
+    Cursor cur{(long)(blockIdx.x / H), (int)(blockIdx.x % H), 0};
     Item x;
-    long vi = next_item(p.geo, blockIdx.x, p.total, x);
+    bool have = cursor_next_valid(p.geo, p.n_slots, cur, ds, dh, x);
     float ng[2] = {0.f, 0.f}, nb[2] = {0.f, 0.f};   // g, beta of the next item (warp 1, in flight)
-    bool pending = false;                           // a TMA load was issued and not yet waited on
-    if (vi < p.total) {
-        if (loader && lane == 0) {
+    uint32_t kq_issued = 0, kq_waited = 0, v_issued = 0, v_waited = 0;   // loader's count of load phases
+    if (have) {
+        if (loader) {
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            intra_issue(smem, S, &tmap_q, &tmap_k, &tmap_v, x);
+            intra_issue_kq(smem, S, &tmap_q, &tmap_k, x);
+            intra_issue_v(smem, S, &tmap_v, x);
+            kq_issued = v_issued = 1;
         }
-        pending = true;
         if (warp == 1) {
             float gg[2], bb[2];
             intra_load_gb(p, x, lane, gg, bb);
@@ -333,20 +393,24 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
     bool ok = true;
     uint32_t ic = 0;   // items done by this CTA: the parity of every barrier phase
-    while (vi < p.total) {
-        const Item cur = x;
+    const Ws& ws = p.ws;
+    while (have) {
+        const Item it = x;
+        Cursor nc = cur;
+        cursor_step(nc, ds, dh, H);
         Item nx;
-        const long vn = next_item(p.geo, vi + gridDim.x, p.total, nx);
+        const bool have_next = cursor_next_valid(p.geo, p.n_slots, nc, ds, dh, nx);
         const uint32_t par = ic & 1;
-        const int L = cur.L;
-        __syncthreads();   // g and beta of this item are in shared memory
+        const int L = it.L;
+        __syncthreads();   // [A] g and beta of this item are in shared memory; the previous item is retired
         if (warp == 1) {
             intra_gate_prefix(S, lane);
-            if (vn < p.total) intra_load_gb(p, nx, lane, ng, nb);
+            if (have_next) intra_load_gb(p, nx, lane, ng, nb);
         }
-        if (ok) ok = mbar_wait(&S.full, par, kWaitNs);
+        if (ok) ok = mbar_wait(&S.full_kq, par, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(1u);
-        pending = pending && !ok;
+        if (ok && loader) kq_waited = ic + 1;
         // MMA0: D0 = [K; Q] K^T
         if (ok && leader) {
             tc_fence_after();
@@ -357,11 +421,71 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 mma_f16(tmem + I_TM_D0, sdesc(a, 16, 1024), sdesc(a, 16, 1024), id, ks > 0);
             }
             mma_commit(&S.m0);
-            ok = mbar_wait(&S.m0, par, kWaitNs);
-            if (!ok) set_status(2u);
         }
-        __syncthreads();   // D0 ready, gate prefix ready
+        __syncthreads();   // [B] gate prefix ready
+        if (ok) {
+            // beta gamma K -> X slabs 2-3 and Ktilde = (gamma_C / gamma) K -> workspace.  Operation e = tid + 256 cc
+            // moves the 16 bytes at physical position (slab, row, pos) of the K tile; consecutive lanes take
+            // consecutive positions, so the workspace writes are coalesced (the layouts share the swizzle).
+            uint8_t* kt = ws.kt + (size_t)it.it * WS_KT;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int e = tid + 256 * cc, slab = e >> 9, r = (e >> 3) & 63;
+                const uint32_t off = (uint32_t)(r * 128 + (e & 7) * 16);
+                const uint32_t m = r < L ? 0xFFFFFFFFu : 0u;   // exact zeros for rows past the end
+                float f[8];
+                bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + off), f);
+                const uint4 xk = scale_chunk_h(f, S.bbuf[r] * S.gam[r], m), kd = scale_chunk_h(f, S.kdec[r], m);
+                st16(smem + I_B2 + 16384 + slab * 8192 + off, xk.x, xk.y, xk.z, xk.w);
+                stg16(kt + slab * 8192 + off, kd.x, kd.y, kd.z, kd.w);
+            }
+            if (warp == 3) {
+                const float gc = S.gC;
+                __stcg(reinterpret_cast<float4*>(ws.gc + (size_t)it.it * 128) + lane, make_float4(gc, gc, gc, gc));
+            }
+            // columns 128-255 := [0; scale gamma Q] (rows 64-127: token row - 64), 64 columns of half pw
+            const float qs = row >= 64 ? p.scale * S.gam[row - 64] : 0.f;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[16];
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    float f[8];
+                    bf16x8_to_f32(ld16(smem + I_KQ + pw * 16384 + sw128_off(row, cb * 16 + h8 * 8)), f);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) r[h8 * 8 + q] = __float_as_uint(qs * f[q]);
+                }
+                tmem_st16(tl + I_TM_QS + pw * 64 + cb * 16, r);
+            }
+        }
+        if (ok) ok = mbar_wait(&S.full_v, par, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && tid == 0) set_status(2u);
+        if (ok && loader) v_waited = ic + 1;
+        if (ok) {
+            // beta V in place in X slabs 0-1
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int e = tid + 256 * cc, r = (e >> 3) & 63;
+                uint8_t* pv = smem + I_B2 + (e >> 9) * 8192 + r * 128 + (e & 7) * 16;
+                float f[8];
+                bf16x8_to_f32(ld16(pv), f);
+                const uint4 xv = scale_chunk_h(f, S.bbuf[r], r < L ? 0xFFFFFFFFu : 0u);
+                st16(pv, xv.x, xv.y, xv.z, xv.w);
+            }
+        }
+        fence_async_smem();
+        tmem_st_wait();
+        if (ok && leader) ok = mbar_wait(&S.m0, par, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);   // warp-uniform, as the warp-collective TMEM accesses need
+        if (!ok && leader) set_status(4u);
+        tc_fence_before();
+        __syncthreads();   // [C] D0 ready; K and Q are dead
         tc_fence_after();
+        if (ok && loader && have_next) {
+            intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx);
+            kq_issued = ic + 2;
+        }
         if (ok) epilogue_kkt(tl + I_TM_D0, row, q4, pw, S.lg, S.bbuf, p.scale, Am, smem + I_A1);
         tc_fence_before();
         __syncthreads();
@@ -370,8 +494,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         // T to fp16, MN-major [j][n] (operand B of MMA1)
         if (ok) {
 #pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int e = tid + I_THREADS * it, j = e >> 3, c8 = e & 7;
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int e = tid + I_THREADS * k2, j = e >> 3, c8 = e & 7;
                 const float4 x0 = ld4(Am + j * TS + c8 * 8), x1 = ld4(Am + j * TS + c8 * 8 + 4);
                 const float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
                 float gq[8];
@@ -392,141 +516,104 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         sdesc(sbase + I_B1 + ks * 2048, 8192, 1024), id, ks > 0);
             mma_commit(&S.m1);
         }
-        // X = [beta gamma K | beta V] (operand B of MMA2a/b), fp16 MN-major [j][n], four 64-column slabs; the
-        // fp32 T it overwrites was consumed before the barrier.  Thread (jrow, part): slab `part`, row jrow.
-        if (ok) {
-            const bool zero = jrow >= L;
-            const float sc = part < 2 ? S.bbuf[jrow] * S.gam[jrow] : S.bbuf[jrow];
-            const uint8_t* src = part < 2 ? smem + I_KQ + part * 16384 : smem + I_V + (part - 2) * 8192;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                const uint32_t o8 = sw128_off(jrow, c8 * 8);
-                copy_scaled_chunk(src + o8, smem + I_B2 + part * 8192 + o8, sc, zero);
-            }
-        }
-        // epilogue 1: [T; PT] to fp16 into A1 (operand A of MMA2); columns [32 pw, 32 pw + 32)
+        // epilogue 1: [T; -PT] to fp16 into A1 (operand A of MMA2); columns [32 pw, 32 pw + 32)
         if (ok) ok = mbar_wait(&S.m1, par, kWaitNs);
-        if (!ok && tid == 0) set_status(4u);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && tid == 0) set_status(8u);
         tc_fence_after();
         if (ok) {
             uint32_t r[2][16];
             tmem_ld16(tl + I_TM_D1 + 32 * pw, r[0]);
             tmem_ld16(tl + I_TM_D1 + 32 * pw + 16, r[1]);
             tmem_ld_wait();
+            const float sg = row < 64 ? 1.f : -1.f;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 float f[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[cc >> 1][(cc & 1) * 8 + q]);
+                for (int q = 0; q < 8; ++q) f[q] = sg * __uint_as_float(r[cc >> 1][(cc & 1) * 8 + q]);
                 st_h8(smem + I_A1 + sw128_off(row, 32 * pw + cc * 8), f);
+            }
+            // zero the D0 and D1 columns this warp has read (MMA2 accumulates into columns 0-127)
+            const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                tmem_st16(tl + I_TM_D0 + 32 * pw + 16 * cb, z);
+                tmem_st16(tl + I_TM_D1 + 32 * pw + 16 * cb, z);
             }
         }
         fence_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         __syncthreads();
-        // MMA2a: D2a = [T; PT] beta gamma K (W | P W);  MMA2b: D2b = [T; PT] beta V (U | P U), over D0/D1
+        // MMA2: D2 += [T; -PT] [beta V | beta gamma K] -> [U | W; -U' | Q'], one N = 256 product
         if (ok && leader) {
             tc_fence_after();
-            const uint32_t id = idesc_f16(128, 128, false, false, true);
+            const uint32_t id = idesc_f16(128, 256, false, false, true);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_f16(tmem + I_TM_D2A, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
-                        sdesc(sbase + I_B2 + ks * 2048, 8192, 1024), id, ks > 0);
-            mma_commit(&S.m2a);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16(tmem + I_TM_D2B, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
-                        sdesc(sbase + I_B2 + 16384 + ks * 2048, 8192, 1024), id, ks > 0);
+                mma_f16(tmem + I_TM_D2, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
+                        sdesc(sbase + I_B2 + ks * 2048, 8192, 1024), id, 1);
             mma_commit(&S.m2b);
         }
-        const Ws& ws = p.ws;
-        // Ktilde = diag(gamma_C / gamma) K to the workspace, MN-major [j][c] like the K tile
-        if (ok) {
-            uint8_t* dst = ws.kt + (size_t)cur.it * WS_KT;
-            const bool zero = jrow >= L;
-            const float sd = S.kdec[jrow];
-            const int slab = part >> 1;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const uint32_t o8 = sw128_off(jrow, (4 * (part & 1) + cc) * 8);
-                float f[8];
-                bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + o8), f);
-                const uint32_t m = zero ? 0u : 0xFFFFFFFFu;
-                stg16(dst + slab * 8192 + o8, pack_h2(f[0] * sd, f[1] * sd) & m, pack_h2(f[2] * sd, f[3] * sd) & m,
-                      pack_h2(f[4] * sd, f[5] * sd) & m, pack_h2(f[6] * sd, f[7] * sd) & m);
-            }
-            if (warp == 3) {
-                const float gc = S.gC;
-                __stcg(reinterpret_cast<float4*>(ws.gc + (size_t)cur.it * 128) + lane, make_float4(gc, gc, gc, gc));
-            }
-        }
-        // epilogue 2a: W (rows 0-63) and Q' = scale gamma Q - P W (rows 64-127) -> [W; Q']; thread: slab pw
-        if (ok) ok = mbar_wait(&S.m2a, par, kWaitNs);
-        if (!ok && tid == 0) set_status(8u);
-        tc_fence_after();
-        if (ok) {
-            uint8_t* dst = ws.wq + (size_t)cur.it * WS_WQ + pw * 16384;
-            const uint8_t* kqs = smem + I_KQ + pw * 16384;
-            uint32_t r[4][16];
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + I_TM_D2A + pw * 64 + cb * 16, r[cb]);
-            tmem_ld_wait();
-            if (row < 64) {
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    float f[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
-                    stg_h8(dst + sw128_off(row, c8 * 8), f);
-                }
-            } else {
-                const float qs = p.scale * S.gam[row - 64];
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    float qv[8], f[8];
-                    bf16x8_to_f32(ld16(kqs + sw128_off(row, c8 * 8)), qv);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) f[q] = fmaf(qs, qv[q], -__uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]));
-                    stg_h8(dst + sw128_off(row, c8 * 8), f);
-                }
-            }
-        }
-        // epilogue 2b: U (rows 0-63) and U' (rows 64-127) -> [U; U'] of d_v half pw
         if (ok) ok = mbar_wait(&S.m2b, par, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(16u);
+        if (ok && loader && have_next) {   // MMA2 has read V: the next item's V can land in X
+            intra_issue_v(smem, S, &tmap_v, nx);
+            v_issued = ic + 2;
+        }
         tc_fence_after();
+        // epilogue 2: [W; Q'] and [U; U'] of column half pw to the workspace.  Each warp stages its 32 rows
+        // (4 KB, the workspace's swizzled row layout) in shared memory that MMA2 has finished with, then writes
+        // them out as contiguous 512-byte runs.
         if (ok) {
-            uint8_t* dst = ws.uu + (size_t)cur.it * WS_UU + pw * 16384;
-            uint32_t r[4][16];
+            uint8_t* stg = smem + (pw == 0 ? I_A1 : I_B2 + 16384) + q4 * 4096;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tcol = which == 0 ? 128 + pw * 64 : pw * 64;        // [W; Q'] then [U; -U']
+                const float sg = (which == 1 && row >= 64) ? -1.f : 1.f;
+                uint8_t* dst = (which == 0 ? ws.wq + (size_t)it.it * WS_WQ : ws.uu + (size_t)it.it * WS_UU) +
+                               pw * 16384 + q4 * 4096;
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + I_TM_D2B + pw * 64 + cb * 16, r[cb]);
-            tmem_ld_wait();
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[16];
+                    tmem_ld16(tl + I_TM_D2 + tcol + cb * 16, r);
+                    tmem_ld_wait();
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                float f[8];
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        float f[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[c8 >> 1][(c8 & 1) * 8 + q]);
-                stg_h8(dst + sw128_off(row, c8 * 8), f);
+                        for (int q = 0; q < 8; ++q) f[q] = sg * __uint_as_float(r[h8 * 8 + q]);
+                        st_h8(stg + sw128_off(lane, cb * 16 + h8 * 8), f);
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 v = ld16(stg + k * 512 + lane * 16);
+                    stg16(dst + k * 512 + lane * 16, v.x, v.y, v.z, v.w);
+                }
+                __syncwarp();
             }
         }
         tc_fence_before();
-        __syncthreads();   // the item's tiles and TMEM columns are free
-        if (ok && vn < p.total) {
-            if (loader && lane == 0) intra_issue(smem, S, &tmap_q, &tmap_k, &tmap_v, nx);
-            pending = true;
-            if (warp == 1) {
-                S.gbuf[lane] = ng[0];
-                S.gbuf[lane + 32] = ng[1];
-                S.bbuf[lane] = nb[0];
-                S.bbuf[lane + 32] = nb[1];
-            }
+        if (warp == 1 && have_next) {   // every read of this item's g and beta is behind a barrier already
+            S.gbuf[lane] = ng[0];
+            S.gbuf[lane + 32] = ng[1];
+            S.bbuf[lane] = nb[0];
+            S.bbuf[lane + 32] = nb[1];
         }
         x = nx;
-        vi = ok ? vn : p.total;
-        if (ok) ++ic;   // after a timeout ic stays at the item whose load may still be in flight
+        cur = nc;
+        have = ok && have_next;
+        if (ok) ++ic;
     }
-    // a load that was issued but never waited on (after a timeout) must land before the CTA exits
-    if (pending && loader && lane == 0) mbar_wait(&S.full, ic & 1, kWaitNs);
+    // loads that were issued but never waited on (after a timeout) must land before the CTA exits
+    if (loader) {
+        for (uint32_t k = kq_waited; k < kq_issued; ++k) mbar_wait(&S.full_kq, k & 1, kWaitNs);
+        for (uint32_t k = v_waited; k < v_issued; ++k) mbar_wait(&S.full_v, k & 1, kWaitNs);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -665,6 +752,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
         const uint32_t stb = sbase + s * S_STAGE;
         const int L = min(C, ch.len - t * C);
         if (ok) ok = mbar_wait(&S.full[s], (t >> 1) & 1, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(32u);
         if (ok) waited = t + 1;
         // MMA3: D3 = [W; Q'] h
@@ -678,6 +766,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
             mma_commit(&S.m3);
         }
         if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(64u);
         tc_fence_after();
         const int i = row - 64;
@@ -751,6 +840,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
             }
         }
         if (ok) ok = mbar_wait(&S.m4, t & 1, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(128u);
         tc_fence_after();
         // h <- gamma_C h + Ktilde^T Delta; fp16 copy for the next MMA3
@@ -842,7 +932,7 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    IntraParams ip{geo, a.g, a.beta, a.scale, items, ws};
+    IntraParams ip{geo, a.g, a.beta, a.scale, n_slots(a), ws};
     e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)I_SMEM);
     if (e != cudaSuccess) return e;
     const long grid1 = items < 2L * sms ? items : 2L * sms;
