@@ -45,7 +45,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN chunk-fwd tokens/s (B4·T4096·H16·d128 bf16) and % of roofline, 1×GB300"
 UNIT = "tokens/s"
-WORKLOAD = 1          # index of the workload in gated_delta_rule_gdn_gb300.workloads.CONFIGS
+WORKLOAD = 1          # index of the workload in gated_delta_rule_gdn_gb300.workloads.CONFIGS (the default)
+WORKLOAD_NAMES = {"gdn_prefill_b4_t4096_h16_d128_c64_bf16": 1}
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -60,11 +61,18 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _metric(w) -> str:
+    if WORKLOAD_NAMES.get(w.name) == 1:
+        return METRIC
+    return f"{w.kind.upper()} chunk-fwd tokens/s ({w.name}) and % of roofline, 1×GB300"
+
+
 def _alg_bytes(w) -> int:
-    """Algorithmic HBM bytes of one chunk-forward launch over workload w (o written in fp32)."""
+    """Algorithmic HBM bytes of one chunk-forward call over workload w (o written in fp32)."""
     token_heads = w.B * w.T * w.H
     es = 2 if w.dtype == "bf16" else 4
-    per_token_head = es * (2 * w.dk + w.dv) + 4 * w.dv + 4 + 4      # q, k, v + o (fp32) + g, beta
+    g_bytes = 4 * w.dk if w.kind == "kda" else 4
+    per_token_head = es * (2 * w.dk + w.dv) + 4 * w.dv + g_bytes + 4   # q, k, v + o (fp32) + g + beta
     N = w.n_seqs if w.n_seqs else w.B
     state = 2 * N * w.H * w.dk * w.dv * 4 if w.h0_std > 0 else N * w.H * w.dk * w.dv * 4
     return token_heads * per_token_head + state
@@ -194,7 +202,8 @@ def cpu_baseline(x, w, min_seconds=8.0, max_passes=5, heads=None):
     passes, t_total = 0, 0.0
     while passes < max_passes and (passes == 0 or t_total < min_seconds):
         t0 = time.perf_counter()
-        oracle.recurrence(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], x["scale"], arr["h0"])
+        oracle.recurrence(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], x["scale"], arr["h0"],
+                          x["cu_seqlens"], gate_per_channel=x["gate_per_channel"])
         t_total += time.perf_counter() - t0
         passes += 1
     frac = len(heads) / w.H
@@ -211,12 +220,13 @@ def run_reference(args):
             return 0
     from gated_delta_rule_gdn_gb300 import workloads as W
     import oracle
-    w = W.config(WORKLOAD)
+    w = W.config(args.workload)
     x = W.chunk_inputs(w, seed=0)
-    heads = [0, 1, 2, 3]                 # one step = 16 (sequence, head) chains of 4096 tokens
+    heads = [0, 1, 2, 3]                 # one step = 4 heads of every sequence
     arr = _oracle_inputs(x, heads)
     oracle.load()
-    run = lambda: oracle.recurrence(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], x["scale"], arr["h0"])
+    run = lambda: oracle.recurrence(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], x["scale"], arr["h0"],
+                                    x["cu_seqlens"], gate_per_channel=x["gate_per_channel"])
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -224,7 +234,7 @@ def run_reference(args):
         run()
     dt = (time.perf_counter() - t0) / args.steps
     value = w.B * w.T * (len(heads) / w.H) / dt
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+    line = {"impl": "reference", "metric": _metric(w), "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
@@ -250,19 +260,22 @@ def run_ours(args):
         libbuild.build()
     barrier(ws)
     gdn.load()
-    w = W.config(WORKLOAD)
+    w = W.config(args.workload)
     x = W.chunk_inputs(w, seed=0)
-    host = {k: x[k].pin_memory() for k in ("q", "k", "v", "g", "beta", "initial_state")}
+    keys = [k for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens") if x[k] is not None]
+    host = {k: x[k].pin_memory() for k in keys}
     d = {k: v.to(dev) for k, v in host.items()}
+    N = x["N"]
     o = torch.empty((w.B, w.T, w.H, w.dv), dtype=torch.float32, device=dev)
-    hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    hT = torch.empty((N, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    fwd = gdn.kda_chunk_fwd if w.kind == "kda" else gdn.gdn_chunk_fwd
 
     def call(dd, oo, hh):
-        gdn.gdn_chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], scale=w.scale,
-                          initial_state=dd["initial_state"], output_final_state=True, chunk_size=w.chunk_size,
-                          algo=args.algo, o=oo, final_state=hh, stream=stream, o_dtype=torch.float32)
+        fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], scale=w.scale, initial_state=dd.get("initial_state"),
+            output_final_state=True, cu_seqlens=dd.get("cu_seqlens"), chunk_size=w.chunk_size, algo=args.algo, o=oo,
+            final_state=hh, stream=stream, o_dtype=torch.float32)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -330,14 +343,16 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     alg = _alg_bytes(w)
     achieved = alg / (ms / 1e3) / 1e9
-    plan = gdn.chunk_plan(False, w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16, False, args.algo)
+    plan = gdn.chunk_plan(w.kind == "kda", w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16,
+                          x["cu_seqlens"] is not None, args.algo)
     kernel, launches = {"tcgen05": ("chunk_tc", 1), "two_pass": ("chunk_two_pass", 2)}.get(plan, ("chunk_generic", 1))
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "metric": _metric(w), "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; q,k unit-norm N(0,1), v N(0,1), beta=sigmoid(N), log alpha=-A softplus(N+dt_bias))",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                   "chunk_size": w.chunk_size, "initial_state": True, "output_final_state": True,
+                   "chunk_size": w.chunk_size, "initial_state": x["initial_state"] is not None,
+                   "output_final_state": True, "n_seqs": N,
                    "o_dtype": "f32",
                    "l2": "flushed before each timed step (256 MiB device write, outside the events)",
                    "kernel": kernel, "launches_per_step": launches, "timed_region_wall_ms": t_wall * 1e3},
@@ -368,6 +383,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--algo", choices=["auto", "generic", "tcgen05", "two_pass"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, choices=[1, 2, 3], default=WORKLOAD,
+                    help="1: GDN B4 T4096 H16 (the headline), 2: packed GDN 8 seqs 65536 tokens H32, 3: KDA B2 T8192 H32")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -732,6 +732,18 @@ bool make_map(CUtensorMap* m, const void* base, long rows, int H, int d) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_f32_rows(CUtensorMap* m, const float* base, long rows, int H, int d) {
+    auto enc = get_encode();
+    if (!enc || d > 256) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
+    cuuint32_t box[3] = {(cuuint32_t)d, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool device_is_sm100_family() {
     int dev = 0, major = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;

@@ -147,33 +147,55 @@ __device__ bool cursor_next_valid(const Geo& g, long n_slots, Cursor& c, int ds,
 
 // shared memory of pass 1 (bytes from a 1024-aligned base)
 constexpr uint32_t I_KQ = 0;        // [K; Q] rows, two K-slabs of 16 KB (K rows 0-63, Q rows 64-127)
-constexpr uint32_t I_B2 = 32768;    // X = [beta V | beta gamma K], fp16 MN-major 64 x 256 in four 8 KB slabs; V
-                                    // lands in slabs 0-1 by TMA (bf16) and is scaled there in place
+constexpr uint32_t I_B2 = 32768;    // X = [beta V | beta gamma K], fp16 MN-major 64 x 256 in four 8 KB slabs.  GDN: V
+                                    // lands in slabs 0-1 by TMA (bf16) and is scaled there in place.  KDA: the
+                                    // [64][128] fp32 gate tile lands here first
 constexpr uint32_t I_A1 = 65536;    // [I; P] then [T; -PT], fp16 K-major 128 x 64
 constexpr uint32_t I_B1 = 81920;    // T, fp16 MN-major [j][n] 64 x 64 (the solve's scratch before that)
 constexpr uint32_t I_AM = 90112;    // fp32 A, then T in place (row stride TS)
 constexpr uint32_t I_RT = I_B1;
-constexpr uint32_t I_SMALL = I_AM + 64 * TS * 4;
+constexpr uint32_t I_END = I_AM + 64 * TS * 4;
 static_assert(32 * RS * 4 <= 8192, "the solve scratch must fit in the T buffer");
+// KDA only: V tile, and the per-element gate factors (row stride ES floats)
+constexpr int ES = 132;
+constexpr uint32_t I_VB = I_END;                      // V, two 64-column bf16 slabs (TMA)
+constexpr uint32_t I_EF = I_VB + 16384;               // E = exp(G - R_block), fp32 [64][ES]
+constexpr uint32_t I_FF = I_EF + 64 * ES * 4;         // F = exp(R_block - G) (fallback: log2 of the cumulative gate)
 
 struct ISmall {
     uint64_t full_kq;         // K, Q of the item landed (TMA transaction bytes)
-    uint64_t full_v;          // V of the item landed
-    uint64_t m0, m1, m2b;
+    uint64_t full_v;          // V (and the KDA gate tile) of the item landed
+    uint64_t m0, m1, m2;
     uint32_t tmem_base;
     uint32_t pad;
-    float gbuf[C];            // g of the item (0 past the end)
+    float gbuf[C];            // g of the item (0 past the end; scalar gate)
     float bbuf[C];            // beta of the item (0 past the end)
-    float lg[C];              // log2 of the within-chunk cumulative retention
+    float lg[C];              // log2 of the within-chunk cumulative retention (scalar gate)
     float gam[C];             // gamma_j
     float kdec[C];            // gamma_C / gamma_j
     float gC;
 };
-constexpr uint32_t I_SMEM = I_SMALL + sizeof(ISmall) + 1024;
+// KDA: per-channel vectors of the gate (log2 units; R_a = cumulative gate at the end of 16-row block a - 1)
+struct KSmall {
+    float er[4][128];         // 2^R_a
+    float esp[4][128];        // 2^(R_{a+1} - R_a), R_4 = the chunk total
+    float elp[4][128];        // 2^(G_last - R_{a+1})
+    float lg63[128];          // G_last
+    int fast;                 // every block's spread is small enough for the factored products
+};
+constexpr uint32_t I_SMALL_GDN = I_END;
+constexpr uint32_t I_SMALL_KDA = I_FF + 64 * ES * 4;
+constexpr uint32_t I_KSMALL = I_SMALL_KDA + ((sizeof(ISmall) + 127) & ~127u);   // 16-byte vector loads need alignment
+constexpr uint32_t I_SMEM_GDN = I_SMALL_GDN + sizeof(ISmall) + 1024;
+constexpr uint32_t I_SMEM_KDA = I_KSMALL + sizeof(KSmall) + 1024;
+static_assert(I_SMEM_KDA <= 227 * 1024, "KDA intra kernel shared memory");
 // D2 = [U | W; -U' | Q'] spans all 256 columns: columns 128-255 hold [0; scale gamma Q] before MMA2 accumulates
 // onto them, columns 0-127 (D0 and D1 until then) are zeroed once D1 has been read
 constexpr uint32_t I_TM_D0 = 0, I_TM_D1 = 64, I_TM_D2 = 0, I_TM_QS = 128, I_TM_COLS = 256;
 constexpr int I_THREADS = 256;
+// largest |cumulative gate - block reference| (log2 units) for the factored KDA products: 2^100 keeps every
+// factor and a 128-term sum of their products inside fp32
+constexpr float KDA_SPREAD_MAX = 100.f;
 
 // Level 0 of the blocked inverse for the 16 x 16 diagonal block at offset o (one warp): the two 8 x 8 diagonal
 // sub-blocks by forward substitution (lane 8 s + c owns column c of sub-block s; their 28 coefficients are loaded
@@ -269,7 +291,8 @@ __device__ void solve_unit_lower_inplace(float* Am, float* Rt, int t, bool work)
     __syncthreads();
 }
 
-// TMA loads of an item: K and Q as 2 x 2 boxes of 64 tokens x 64 columns; V as two boxes into X's V slabs.
+// TMA loads of an item: K and Q as 2 x 2 boxes of 64 tokens x 64 columns; V as two boxes (GDN: into X's V slabs,
+// KDA: into its own tile, with the fp32 gate tile into X).
 __device__ __forceinline__ void intra_issue_kq(uint8_t* smem, ISmall& S, const CUtensorMap* mq, const CUtensorMap* mk,
                                                const Item& x) {
     const int row = (int)x.row;
@@ -280,26 +303,31 @@ __device__ __forceinline__ void intra_issue_kq(uint8_t* smem, ISmall& S, const C
     tma_load_3d(kq + 16384, mk, &S.full_kq, 64, x.h, row);
     tma_load_3d(kq + 16384 + 8192, mq, &S.full_kq, 64, x.h, row);
 }
-__device__ __forceinline__ void intra_issue_v(uint8_t* smem, ISmall& S, const CUtensorMap* mv, const Item& x) {
+template <bool KDA>
+__device__ __forceinline__ void intra_issue_v(uint8_t* smem, ISmall& S, const CUtensorMap* mv, const CUtensorMap* mg,
+                                              const Item& x) {
     const int row = (int)x.row;
-    mbar_arrive_expect_tx(&S.full_v, 16384);
-    tma_load_3d(smem + I_B2, mv, &S.full_v, 0, x.h, row);
-    tma_load_3d(smem + I_B2 + 8192, mv, &S.full_v, 64, x.h, row);
+    mbar_arrive_expect_tx(&S.full_v, KDA ? 16384 + 32768 : 16384);
+    uint8_t* vb = smem + (KDA ? I_VB : I_B2);
+    tma_load_3d(vb, mv, &S.full_v, 0, x.h, row);
+    tma_load_3d(vb + 8192, mv, &S.full_v, 64, x.h, row);
+    if (KDA) tma_load_3d(smem + I_B2, mg, &S.full_v, 0, x.h, row);
 }
 
-// g and beta of an item (0 past its end): lane l holds tokens l and l + 32
+// g (scalar gate only) and beta of an item (0 past its end): lane l holds tokens l and l + 32
+template <bool KDA>
 __device__ __forceinline__ void intra_load_gb(const IntraParams& p, const Item& x, int lane, float (&g)[2],
                                               float (&b)[2]) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const int r = lane + 32 * k;
         const size_t tok = (size_t)(x.row + r) * p.geo.H + x.h;
-        g[k] = r < x.L ? __ldg(p.g + tok) : 0.f;
+        g[k] = (!KDA && r < x.L) ? __ldg(p.g + tok) : 0.f;
         b[k] = r < x.L ? __ldg(p.beta + tok) : 0.f;
     }
 }
 
-// gate prefix of the item in gbuf (one warp)
+// gate prefix of the item in gbuf (one warp, scalar gate)
 __device__ __forceinline__ void intra_gate_prefix(ISmall& S, int lane) {
     const float LOG2E = 1.4426950408889634f;
     const float g0 = S.gbuf[2 * lane], g1 = S.gbuf[2 * lane + 1];
@@ -324,19 +352,199 @@ __device__ __forceinline__ uint4 scale_chunk_h(const float (&f)[8], float s, uin
     return make_uint4(pack_h2(f[0] * s, f[1] * s) & m, pack_h2(f[2] * s, f[3] * s) & m, pack_h2(f[4] * s, f[5] * s) & m,
                       pack_h2(f[6] * s, f[7] * s) & m);
 }
+__device__ __forceinline__ uint4 scale_chunk_hv(const float (&f)[8], const float (&s)[8], uint32_t m) {
+    return make_uint4(pack_h2(f[0] * s[0], f[1] * s[1]) & m, pack_h2(f[2] * s[2], f[3] * s[3]) & m,
+                      pack_h2(f[4] * s[4], f[5] * s[5]) & m, pack_h2(f[6] * s[6], f[7] * s[7]) & m);
+}
+__device__ __forceinline__ void ld_f8(const float* p, float (&f)[8]) {
+    const float4 a = ld4(p), b = ld4(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+// one bf16 element (row r, column c) of a [rows][128] tile stored as two 128-byte-swizzled 64-column slabs
+__device__ __forceinline__ float ld_bf16_sw(const uint8_t* base, int r, int c) {
+    const uint16_t u = *reinterpret_cast<const uint16_t*>(base + (c >> 6) * 16384 + sw128_off(r, c & 63));
+    return __uint_as_float((uint32_t)u << 16);
+}
 
-// Per item: [A] gate prefix; [B] MMA0 = [K; Q] K^T runs while the threads build X (beta gamma K, and beta V in place),
-// write Ktilde and gamma_C, and stash [0; scale gamma Q] into TMEM columns 128-255; K and Q are then dead and the
-// next item's K, Q load is issued.  [C] epilogue of D0 -> A, [I; P]; the solve; T to fp16; MMA1 = [I; P] T;
-// [T; -P T] to fp16; MMA2 = D2 + [T; -PT] [beta V | beta gamma K] = [U | W; -U' | Q']; once MMA2 has read V the
-// next item's V load is issued; the epilogue writes [W; Q'] and [U; U'] to the workspace.
-__global__ void __launch_bounds__(I_THREADS, 2)
+// KDA: within-chunk cumulative gate per channel (thread c < 128 owns channel c), its 16-row block references
+// and the factors of the factored K K^T / Q K^T products:
+//   E[i][c] = 2^(G_ic - R_a),  F[i][c] = 2^(R_a - G_ic)   (i in block a; R_a = G at the end of block a - 1, R_0 = 0)
+// The fast path needs every gate <= 0 (G non-increasing: E <= 1, F <= 2^(block spread)) and every block spread
+// <= KDA_SPREAD_MAX.  Otherwise F keeps G itself and the products are formed exactly, one exponential per term.
+// Also writes gamma_C.
+__device__ void kda_gate_tables(uint8_t* smem, KSmall& K, int L, float* gc_out, int tid) {
+    const float LOG2E = 1.4426950408889634f;
+    bool fine = true;
+    float lg[64];
+    if (tid < 128) {
+        const float* gt = reinterpret_cast<const float*>(smem + I_B2);
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            const float gi = i < L ? gt[i * 128 + tid] : 0.f;
+            fine = fine && gi <= 0.f;   // retention <= 1: every factor below stays <= 1 or <= the block spread
+            acc += gi;
+            lg[i] = acc * LOG2E;
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float R = a == 0 ? 0.f : lg[16 * a - 1];
+            fine = fine && R - lg[16 * a + 15] <= KDA_SPREAD_MAX;
+        }
+    }
+    const bool fast = __syncthreads_and(fine) != 0;
+    if (tid < 128) {
+        const int c = tid;
+        float* E = reinterpret_cast<float*>(smem + I_EF);
+        float* F = reinterpret_cast<float*>(smem + I_FF);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float R = a == 0 ? 0.f : lg[16 * a - 1], R1 = lg[16 * a + 15];
+            K.er[a][c] = ex2(R);
+            K.esp[a][c] = ex2(R1 - R);
+            K.elp[a][c] = ex2(lg[63] - R1);
+#pragma unroll
+            for (int i = 16 * a; i < 16 * a + 16; ++i) {
+                E[i * ES + c] = fast ? ex2(lg[i] - R) : 0.f;
+                F[i * ES + c] = fast ? ex2(R - lg[i]) : lg[i];
+            }
+        }
+        K.lg63[c] = lg[63];
+        __stcg(gc_out + c, ex2(lg[63]));
+        if (c == 0) K.fast = fast ? 1 : 0;
+    }
+}
+
+// KDA, fast path: A = diag(beta)(K K^T with per-channel decays) strictly lower -> Am (fp32) and P = scale (Q K^T with
+// decays) lower incl. the diagonal -> A1 rows 64-127, plus the identity rows of A1.  Warp (a = w / 2, op = w % 2)
+// forms row block a of the K (op 0) or Q (op 1) product against column blocks b <= a with TF32 warp MMAs:
+//   row operand x_ic 2^(G_ic - R_a) = x_ic E_ic;   column operand k_jc 2^(R_a - G_jc) =
+//   k_jc F_jc (b = a),   ((k_jc F_jc 2^(R_{b+1} - R_b)) 2^(R_{b+2} - R_{b+1}) ...) (b < a, each factor <= 1).
+__device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* bb, float scale, int warp, int lane) {
+    const int a = warp >> 1, op = warp & 1;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const float* E = reinterpret_cast<const float*>(smem + I_EF);
+    const float* F = reinterpret_cast<const float*>(smem + I_FF);
+    const uint8_t* kb = smem + I_KQ;                 // K rows 0-63
+    const uint8_t* xb = smem + I_KQ + op * 8192;     // K or Q rows
+    float* Am = reinterpret_cast<float*>(smem + I_AM);
+    uint8_t* a1 = smem + I_A1;
+    const int r0 = 16 * a + g8, r1 = r0 + 8;
+    uint32_t afr[16][4];
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks) {
+        const int c0 = 8 * ks + t4, c1 = c0 + 4;
+        afr[ks][0] = to_tf32(ld_bf16_sw(xb, r0, c0) * E[r0 * ES + c0]);
+        afr[ks][1] = to_tf32(ld_bf16_sw(xb, r1, c0) * E[r1 * ES + c0]);
+        afr[ks][2] = to_tf32(ld_bf16_sw(xb, r0, c1) * E[r0 * ES + c1]);
+        afr[ks][3] = to_tf32(ld_bf16_sw(xb, r1, c1) * E[r1 * ES + c1]);
+    }
+    const float s0 = op == 0 ? bb[r0] : scale, s1 = op == 0 ? bb[r1] : scale;
+#pragma unroll 1
+    for (int b = 0; b <= a; ++b) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int j = 16 * b + 8 * nt + g8;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 16; ++ks) {
+                const int c0 = 8 * ks + t4, c1 = c0 + 4;
+                float f0 = ld_bf16_sw(kb, j, c0) * F[j * ES + c0];
+                float f1 = ld_bf16_sw(kb, j, c1) * F[j * ES + c1];
+                for (int m = b; m < a; ++m) {
+                    f0 *= K.esp[m][c0];
+                    f1 *= K.esp[m][c1];
+                }
+                const uint32_t b0 = to_tf32(f0), b1 = to_tf32(f1);
+                asm volatile(
+                    "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                    "{%0, %1, %2, %3};"
+                    : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                    : "r"(afr[ks][0]), "r"(afr[ks][1]), "r"(afr[ks][2]), "r"(afr[ks][3]), "r"(b0), "r"(b1));
+            }
+            const int cc = 16 * b + 8 * nt + 2 * t4;
+            if (op == 0) {
+                // A = beta_i (K K^T)_ij for j < i
+                *reinterpret_cast<float2*>(Am + r0 * TS + cc) =
+                    make_float2(cc < r0 ? s0 * d[0] : 0.f, cc + 1 < r0 ? s0 * d[1] : 0.f);
+                *reinterpret_cast<float2*>(Am + r1 * TS + cc) =
+                    make_float2(cc < r1 ? s1 * d[2] : 0.f, cc + 1 < r1 ? s1 * d[3] : 0.f);
+            } else {
+                // P = scale (Q K^T)_ij for j <= i
+                *reinterpret_cast<uint32_t*>(a1 + sw128_off(64 + r0, cc)) =
+                    pack_h2(cc <= r0 ? s0 * d[0] : 0.f, cc + 1 <= r0 ? s0 * d[1] : 0.f);
+                *reinterpret_cast<uint32_t*>(a1 + sw128_off(64 + r1, cc)) =
+                    pack_h2(cc <= r1 ? s1 * d[2] : 0.f, cc + 1 <= r1 ? s1 * d[3] : 0.f);
+            }
+        }
+    }
+    // zeros above the diagonal blocks: A inside the 32 x 32 diagonal blocks (what the solve reads), P everywhere
+    if (op == 0) {
+        if ((a & 1) == 0) {
+            const int zr = 16 * a + (lane >> 1), zc = 16 * (a + 1) + 8 * (lane & 1);
+            *reinterpret_cast<float4*>(Am + zr * TS + zc) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(Am + zr * TS + zc + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // identity rows 16 a .. 16 a + 15 of A1: lane -> row 16 a + lane / 2, columns 32 (lane % 2) .. + 31
+        const int ir = 16 * a + (lane >> 1);
+        const uint32_t one = (ir & 1) ? 0x3C000000u : 0x00003C00u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int c8 = 4 * (lane & 1) + q;
+            const bool here = (ir >> 3) == c8;
+            const int qw = (ir & 7) >> 1;
+            st16(a1 + sw128_off(ir, c8 * 8), here && qw == 0 ? one : 0u, here && qw == 1 ? one : 0u,
+                 here && qw == 2 ? one : 0u, here && qw == 3 ? one : 0u);
+        }
+    } else {
+        for (int e = lane; e < (3 - a) * 16 * 2; e += 32) {   // 16 rows x (3 - a) blocks x two 8-column chunks
+            const int zr = 16 * a + (e & 15), zc = 16 * (a + 1) + 8 * (e >> 4);
+            st16(a1 + sw128_off(64 + zr, zc), 0u, 0u, 0u, 0u);
+        }
+    }
+}
+
+// KDA, fallback: the same A, P and identity rows, every term with its own exponential of the gate difference
+// (G in log2 units is in F).  Exact for any gate; used only when some block's spread is too large.
+__device__ void kda_products_direct(uint8_t* smem, const float* bb, float scale, int tid) {
+    const float* G = reinterpret_cast<const float*>(smem + I_FF);
+    const uint8_t* kb = smem + I_KQ;
+    const uint8_t* qb = smem + I_KQ + 8192;
+    float* Am = reinterpret_cast<float*>(smem + I_AM);
+    uint8_t* a1 = smem + I_A1;
+    for (int e = tid; e < 64 * 64; e += I_THREADS) {
+        const int i = e >> 6, j = e & 63;
+        float ak = 0.f, aq = 0.f;
+        if (j <= i) {
+            for (int c = 0; c < 128; ++c) {
+                const float w = ex2(G[i * ES + c] - G[j * ES + c]) * ld_bf16_sw(kb, j, c);
+                ak = fmaf(ld_bf16_sw(kb, i, c), w, ak);
+                aq = fmaf(ld_bf16_sw(qb, i, c), w, aq);
+            }
+        }
+        Am[i * TS + j] = j < i ? bb[i] * ak : 0.f;
+        *reinterpret_cast<__half*>(a1 + sw128_off(64 + i, j)) = __float2half_rn(j <= i ? scale * aq : 0.f);
+        *reinterpret_cast<__half*>(a1 + sw128_off(i, j)) = __float2half_rn(i == j ? 1.f : 0.f);
+    }
+}
+
+// Per item.  Scalar gate (GDN): [A] gate prefix; [B] MMA0 = [K; Q] K^T runs while the threads build X (beta gamma K,
+// and beta V in place), write Ktilde and gamma_C, and stash [0; scale gamma Q] into TMEM columns 128-255; the epilogue
+// of D0 gives A and [I; P].  Per-channel gate (KDA): [B] the gate tables; A and [I; P] from the factored warp
+// products; X, Ktilde and the Q stash with per-element decays.  Then [C] K and Q are dead and the next item's K, Q
+// load is issued; the solve; T to fp16; MMA1 = [I; P] T; [T; -P T] to fp16; MMA2 = D2 + [T; -PT] [beta V | beta
+// gamma K] = [U | W; -U' | Q']; once MMA2 has read X the next item's V (and gate tile) load is issued; the epilogue
+// writes [W; Q'] and [U; U'] to the workspace.
+template <bool KDA>
+__global__ void __launch_bounds__(I_THREADS, KDA ? 1 : 2)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, const IntraParams p) {
+                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_g,
+                   const IntraParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    ISmall& S = *reinterpret_cast<ISmall*>(smem + I_SMALL);
+    ISmall& S = *reinterpret_cast<ISmall*>(smem + (KDA ? I_SMALL_KDA : I_SMALL_GDN));
+    KSmall& KS = *reinterpret_cast<KSmall*>(smem + I_KSMALL);   // KDA only
     float* Am = reinterpret_cast<float*>(smem + I_AM);
     float* Rt = reinterpret_cast<float*>(smem + I_RT);
 
@@ -348,6 +556,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const bool leader = (tid == 0);
     const bool loader = (tid == 64);
     const int H = p.geo.H;
+    const float LOG2E = 1.4426950408889634f;
+    (void)LOG2E;
 
     if (warp == 0) {
         tmem_alloc(&S.tmem_base, I_TM_COLS);
@@ -358,7 +568,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         mbar_init(&S.full_v, 1);
         mbar_init(&S.m0, 1);
         mbar_init(&S.m1, 1);
-        mbar_init(&S.m2b, 1);
+        mbar_init(&S.m2, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -378,13 +588,14 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
+            if (KDA) prefetch_tmap(&tmap_g);
             intra_issue_kq(smem, S, &tmap_q, &tmap_k, x);
-            intra_issue_v(smem, S, &tmap_v, x);
+            intra_issue_v<KDA>(smem, S, &tmap_v, &tmap_g, x);
             kq_issued = v_issued = 1;
         }
         if (warp == 1) {
             float gg[2], bb[2];
-            intra_load_gb(p, x, lane, gg, bb);
+            intra_load_gb<KDA>(p, x, lane, gg, bb);
             S.gbuf[lane] = gg[0];
             S.gbuf[lane + 32] = gg[1];
             S.bbuf[lane] = bb[0];
@@ -404,91 +615,190 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const int L = it.L;
         __syncthreads();   // [A] g and beta of this item are in shared memory; the previous item is retired
         if (warp == 1) {
-            intra_gate_prefix(S, lane);
-            if (have_next) intra_load_gb(p, nx, lane, ng, nb);
+            if (!KDA) intra_gate_prefix(S, lane);
+            if (have_next) intra_load_gb<KDA>(p, nx, lane, ng, nb);
         }
         if (ok) ok = mbar_wait(&S.full_kq, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(1u);
         if (ok && loader) kq_waited = ic + 1;
-        // MMA0: D0 = [K; Q] K^T
-        if (ok && leader) {
-            tc_fence_after();
-            const uint32_t id = idesc_f16(128, 64, true, false, false);
+        if constexpr (!KDA) {
+            // MMA0: D0 = [K; Q] K^T
+            if (ok && leader) {
+                tc_fence_after();
+                const uint32_t id = idesc_f16(128, 64, true, false, false);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t a = sbase + I_KQ + (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_f16(tmem + I_TM_D0, sdesc(a, 16, 1024), sdesc(a, 16, 1024), id, ks > 0);
-            }
-            mma_commit(&S.m0);
-        }
-        __syncthreads();   // [B] gate prefix ready
-        if (ok) {
-            // beta gamma K -> X slabs 2-3 and Ktilde = (gamma_C / gamma) K -> workspace.  Operation e = tid + 256 cc
-            // moves the 16 bytes at physical position (slab, row, pos) of the K tile; consecutive lanes take
-            // consecutive positions, so the workspace writes are coalesced (the layouts share the swizzle).
-            uint8_t* kt = ws.kt + (size_t)it.it * WS_KT;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int e = tid + 256 * cc, slab = e >> 9, r = (e >> 3) & 63;
-                const uint32_t off = (uint32_t)(r * 128 + (e & 7) * 16);
-                const uint32_t m = r < L ? 0xFFFFFFFFu : 0u;   // exact zeros for rows past the end
-                float f[8];
-                bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + off), f);
-                const uint4 xk = scale_chunk_h(f, S.bbuf[r] * S.gam[r], m), kd = scale_chunk_h(f, S.kdec[r], m);
-                st16(smem + I_B2 + 16384 + slab * 8192 + off, xk.x, xk.y, xk.z, xk.w);
-                stg16(kt + slab * 8192 + off, kd.x, kd.y, kd.z, kd.w);
-            }
-            if (warp == 3) {
-                const float gc = S.gC;
-                __stcg(reinterpret_cast<float4*>(ws.gc + (size_t)it.it * 128) + lane, make_float4(gc, gc, gc, gc));
-            }
-            // columns 128-255 := [0; scale gamma Q] (rows 64-127: token row - 64), 64 columns of half pw
-            const float qs = row >= 64 ? p.scale * S.gam[row - 64] : 0.f;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t r[16];
-#pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {
-                    float f[8];
-                    bf16x8_to_f32(ld16(smem + I_KQ + pw * 16384 + sw128_off(row, cb * 16 + h8 * 8)), f);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) r[h8 * 8 + q] = __float_as_uint(qs * f[q]);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t a = sbase + I_KQ + (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_f16(tmem + I_TM_D0, sdesc(a, 16, 1024), sdesc(a, 16, 1024), id, ks > 0);
                 }
-                tmem_st16(tl + I_TM_QS + pw * 64 + cb * 16, r);
+                mma_commit(&S.m0);
             }
-        }
-        if (ok) ok = mbar_wait(&S.full_v, par, kWaitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && tid == 0) set_status(2u);
-        if (ok && loader) v_waited = ic + 1;
-        if (ok) {
-            // beta V in place in X slabs 0-1
+            __syncthreads();   // [B] gate prefix ready
+            if (ok) {
+                // beta gamma K -> X slabs 2-3 and Ktilde = (gamma_C / gamma) K -> workspace.  Operation e = tid + 256
+                // cc moves the 16 bytes at physical position (slab, row, pos) of the K tile; consecutive lanes take
+                // consecutive positions, so the workspace writes are coalesced (the layouts share the swizzle).
+                uint8_t* kt = ws.kt + (size_t)it.it * WS_KT;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int e = tid + 256 * cc, r = (e >> 3) & 63;
-                uint8_t* pv = smem + I_B2 + (e >> 9) * 8192 + r * 128 + (e & 7) * 16;
-                float f[8];
-                bf16x8_to_f32(ld16(pv), f);
-                const uint4 xv = scale_chunk_h(f, S.bbuf[r], r < L ? 0xFFFFFFFFu : 0u);
-                st16(pv, xv.x, xv.y, xv.z, xv.w);
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int e = tid + 256 * cc, slab = e >> 9, r = (e >> 3) & 63;
+                    const uint32_t off = (uint32_t)(r * 128 + (e & 7) * 16);
+                    const uint32_t m = r < L ? 0xFFFFFFFFu : 0u;   // exact zeros for rows past the end
+                    float f[8];
+                    bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + off), f);
+                    const uint4 xk = scale_chunk_h(f, S.bbuf[r] * S.gam[r], m), kd = scale_chunk_h(f, S.kdec[r], m);
+                    st16(smem + I_B2 + 16384 + slab * 8192 + off, xk.x, xk.y, xk.z, xk.w);
+                    stg16(kt + slab * 8192 + off, kd.x, kd.y, kd.z, kd.w);
+                }
+                if (warp == 3) {
+                    const float gc = S.gC;
+                    __stcg(reinterpret_cast<float4*>(ws.gc + (size_t)it.it * 128) + lane, make_float4(gc, gc, gc, gc));
+                }
+                // columns 128-255 := [0; scale gamma Q] (rows 64-127: token row - 64), 64 columns of half pw
+                const float qs = row >= 64 ? p.scale * S.gam[row - 64] : 0.f;
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        float f[8];
+                        bf16x8_to_f32(ld16(smem + I_KQ + pw * 16384 + sw128_off(row, cb * 16 + h8 * 8)), f);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) r[h8 * 8 + q] = __float_as_uint(qs * f[q]);
+                    }
+                    tmem_st16(tl + I_TM_QS + pw * 64 + cb * 16, r);
+                }
+            }
+            if (ok) ok = mbar_wait(&S.full_v, par, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && tid == 0) set_status(2u);
+            if (ok && loader) v_waited = ic + 1;
+            if (ok) {
+                // beta V in place in X slabs 0-1
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int e = tid + 256 * cc, r = (e >> 3) & 63;
+                    uint8_t* pv = smem + I_B2 + (e >> 9) * 8192 + r * 128 + (e & 7) * 16;
+                    float f[8];
+                    bf16x8_to_f32(ld16(pv), f);
+                    const uint4 xv = scale_chunk_h(f, S.bbuf[r], r < L ? 0xFFFFFFFFu : 0u);
+                    st16(pv, xv.x, xv.y, xv.z, xv.w);
+                }
+            }
+            fence_async_smem();
+            tmem_st_wait();
+            if (ok && leader) ok = mbar_wait(&S.m0, par, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);   // warp-uniform, as the warp-collective TMEM accesses need
+            if (!ok && leader) set_status(4u);
+            tc_fence_before();
+            __syncthreads();   // [C] D0 ready; K and Q are dead
+            tc_fence_after();
+            if (ok && loader && have_next) {
+                intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx);
+                kq_issued = ic + 2;
+            }
+            if (ok) epilogue_kkt(tl + I_TM_D0, row, q4, pw, S.lg, S.bbuf, p.scale, Am, smem + I_A1);
+            tc_fence_before();
+            __syncthreads();
+        } else {
+            if (ok) ok = mbar_wait(&S.full_v, par, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && tid == 0) set_status(2u);
+            if (ok && loader) v_waited = ic + 1;
+            // [B] the gate tables (contains the barrier that decides the fast path)
+            kda_gate_tables(smem, KS, ok ? L : 0, ws.gc + (size_t)it.it * 128, tid);
+            __syncthreads();
+            const bool fast = KS.fast != 0;
+            if (ok) {
+                if (fast) kda_products_fast(smem, KS, S.bbuf, p.scale, warp, lane);
+                else kda_products_direct(smem, S.bbuf, p.scale, tid);
+            }
+            // X = [beta V | beta 2^G K] and Ktilde = 2^(G_last - G) K (coalesced, as in the scalar-gate path)
+            if (ok) {
+                const float* E = reinterpret_cast<const float*>(smem + I_EF);
+                const float* F = reinterpret_cast<const float*>(smem + I_FF);
+                uint8_t* kt = ws.kt + (size_t)it.it * WS_KT;
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int e = tid + 256 * cc, slab = e >> 9, r = (e >> 3) & 63, pos = e & 7;
+                    const int c = slab * 64 + ((pos ^ (r & 7)) << 3), a = r >> 4;
+                    const uint32_t off = (uint32_t)(r * 128 + pos * 16);
+                    const uint32_t m = r < L ? 0xFFFFFFFFu : 0u;
+                    float f[8], v[8], eg[8], ek[8];
+                    bf16x8_to_f32(ld16(smem + I_VB + slab * 8192 + off), v);
+                    const uint4 xv = scale_chunk_h(v, S.bbuf[r], m);
+                    st16(smem + I_B2 + slab * 8192 + off, xv.x, xv.y, xv.z, xv.w);
+                    bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + off), f);
+                    if (fast) {
+                        float e8[8], f8[8], er[8], es[8], el[8];
+                        ld_f8(E + r * ES + c, e8);
+                        ld_f8(F + r * ES + c, f8);
+                        ld_f8(&KS.er[a][c], er);
+                        ld_f8(&KS.esp[a][c], es);
+                        ld_f8(&KS.elp[a][c], el);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            eg[q] = S.bbuf[r] * (e8[q] * er[q]);
+                            ek[q] = (f8[q] * es[q]) * el[q];
+                        }
+                    } else {
+                        float g8[8], l8[8];
+                        ld_f8(F + r * ES + c, g8);
+                        ld_f8(&KS.lg63[c], l8);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            eg[q] = S.bbuf[r] * ex2(g8[q]);
+                            ek[q] = ex2(l8[q] - g8[q]);
+                        }
+                    }
+                    const uint4 xk = scale_chunk_hv(f, eg, m), kd = scale_chunk_hv(f, ek, m);
+                    st16(smem + I_B2 + 16384 + slab * 8192 + off, xk.x, xk.y, xk.z, xk.w);
+                    stg16(kt + slab * 8192 + off, kd.x, kd.y, kd.z, kd.w);
+                }
+                // columns 128-255 := [0; scale 2^G Q], 64 columns of half pw
+                const int i = row - 64, a = (row >= 64 ? i : 0) >> 4;
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        const int c = pw * 64 + cb * 16 + h8 * 8;
+                        float f[8], s8[8];
+                        if (row >= 64) {
+                            bf16x8_to_f32(ld16(smem + I_KQ + pw * 16384 + sw128_off(row, cb * 16 + h8 * 8)), f);
+                            if (fast) {
+                                float e8[8], er[8];
+                                ld_f8(E + i * ES + c, e8);
+                                ld_f8(&KS.er[a][c], er);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) s8[q] = p.scale * (e8[q] * er[q]);
+                            } else {
+                                float g8[8];
+                                ld_f8(F + i * ES + c, g8);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) s8[q] = p.scale * ex2(g8[q]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) f[q] = s8[q] = 0.f;
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) r[h8 * 8 + q] = __float_as_uint(s8[q] * f[q]);
+                    }
+                    tmem_st16(tl + I_TM_QS + pw * 64 + cb * 16, r);
+                }
+            }
+            fence_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            __syncthreads();   // [C] A, [I; P] and X are in shared memory; K and Q are dead
+            tc_fence_after();
+            if (ok && loader && have_next) {
+                intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx);
+                kq_issued = ic + 2;
             }
         }
-        fence_async_smem();
-        tmem_st_wait();
-        if (ok && leader) ok = mbar_wait(&S.m0, par, kWaitNs);
-        ok = __all_sync(0xffffffffu, ok);   // warp-uniform, as the warp-collective TMEM accesses need
-        if (!ok && leader) set_status(4u);
-        tc_fence_before();
-        __syncthreads();   // [C] D0 ready; K and Q are dead
-        tc_fence_after();
-        if (ok && loader && have_next) {
-            intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx);
-            kq_issued = ic + 2;
-        }
-        if (ok) epilogue_kkt(tl + I_TM_D0, row, q4, pw, S.lg, S.bbuf, p.scale, Am, smem + I_A1);
-        tc_fence_before();
-        __syncthreads();
         // UT transform, T = (I + A)^{-1} in place
         solve_unit_lower_inplace(Am, Rt, tid, ok);
         // T to fp16, MN-major [j][n] (operand B of MMA1)
@@ -554,21 +864,22 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             for (int ks = 0; ks < 4; ++ks)
                 mma_f16(tmem + I_TM_D2, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
                         sdesc(sbase + I_B2 + ks * 2048, 8192, 1024), id, 1);
-            mma_commit(&S.m2b);
+            mma_commit(&S.m2);
         }
-        if (ok) ok = mbar_wait(&S.m2b, par, kWaitNs);
+        if (ok) ok = mbar_wait(&S.m2, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(16u);
-        if (ok && loader && have_next) {   // MMA2 has read V: the next item's V can land in X
-            intra_issue_v(smem, S, &tmap_v, nx);
+        if (ok && loader && have_next) {   // MMA2 has read X: the next item's V (and gate tile) can land
+            intra_issue_v<KDA>(smem, S, &tmap_v, &tmap_g, nx);
             v_issued = ic + 2;
         }
         tc_fence_after();
         // epilogue 2: [W; Q'] and [U; U'] of column half pw to the workspace.  Each warp stages its 32 rows
-        // (4 KB, the workspace's swizzled row layout) in shared memory that MMA2 has finished with, then writes
-        // them out as contiguous 512-byte runs.
+        // (4 KB, the workspace's swizzled row layout) in shared memory nothing reads or loads into any more this
+        // item (A1 after MMA2; the beta gamma K half of X for the scalar gate, whose next V lands in the other half;
+        // the E table for KDA, whose next gate tile fills all of X), then writes them out as 512-byte runs.
         if (ok) {
-            uint8_t* stg = smem + (pw == 0 ? I_A1 : I_B2 + 16384) + q4 * 4096;
+            uint8_t* stg = smem + (pw == 0 ? I_A1 : (KDA ? I_EF : I_B2 + 16384)) + q4 * 4096;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 const uint32_t tcol = which == 0 ? 128 + pw * 64 : pw * 64;        // [W; Q'] then [U; -U']
@@ -884,12 +1195,12 @@ long n_slots(const ChunkArgs& a) { return (long)a.B * a.T / C + a.N() + 1; }
 }  // namespace
 
 const char* two_pass_unsupported_reason(const ChunkArgs& a) {
-    if (a.per_channel) return "per-channel (KDA) gates use another kernel";
     if (!a.bf16) return "q, k, v must be bf16";
     if (a.dk != DK || a.dv != DV) return "d_k and d_v must be 128";
     if (a.C != C) return "chunk_size must be 64";
     auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0; };
-    if (!al16(a.q) || !al16(a.k) || !al16(a.v) || !al16(a.o) || (a.h0 && !al16(a.h0)) || (a.hT && !al16(a.hT)))
+    if (!al16(a.q) || !al16(a.k) || !al16(a.v) || !al16(a.o) || (a.h0 && !al16(a.h0)) || (a.hT && !al16(a.hT)) ||
+        (a.per_channel && !al16(a.g)))
         return "tensors must be 16-byte aligned";
     return nullptr;
 }
@@ -933,10 +1244,21 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     IntraParams ip{geo, a.g, a.beta, a.scale, n_slots(a), ws};
-    e = cudaFuncSetAttribute(chunk_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)I_SMEM);
-    if (e != cudaSuccess) return e;
-    const long grid1 = items < 2L * sms ? items : 2L * sms;
-    chunk_intra_kernel<<<(unsigned)grid1, I_THREADS, I_SMEM, s>>>(mq, mk, mv, ip);
+    if (a.per_channel) {
+        CUtensorMap mg;
+        if (!make_map_f32_rows(&mg, a.g, rows, a.H, DK)) return cudaErrorInvalidValue;
+        e = cudaFuncSetAttribute(chunk_intra_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)I_SMEM_KDA);
+        if (e != cudaSuccess) return e;
+        const long grid1 = items < sms ? items : sms;
+        chunk_intra_kernel<true><<<(unsigned)grid1, I_THREADS, I_SMEM_KDA, s>>>(mq, mk, mv, mg, ip);
+    } else {
+        e = cudaFuncSetAttribute(chunk_intra_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)I_SMEM_GDN);
+        if (e != cudaSuccess) return e;
+        const long grid1 = items < 2L * sms ? items : 2L * sms;
+        chunk_intra_kernel<false><<<(unsigned)grid1, I_THREADS, I_SMEM_GDN, s>>>(mq, mk, mv, mv, ip);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

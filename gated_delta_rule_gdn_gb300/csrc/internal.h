@@ -60,6 +60,9 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
 // Shared host helpers of the tcgen05 paths (chunk_tc.cu).
 // TMA map of a [rows][H][d] bf16 tensor, box 64 elements x 1 head x 64 rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, long rows, int H, int d);
+// TMA map of a [rows][H][d] fp32 tensor (d <= 256), box d x 1 head x 64 rows, no swizzle: a 64-row tile lands
+// as a dense row-major [64][d] block.
+bool make_map_f32_rows(CUtensorMap* m, const float* base, long rows, int H, int d);
 bool device_is_sm100_family();
 
 // Decode step (recurrent_step.cu).

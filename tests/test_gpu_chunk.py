@@ -107,6 +107,31 @@ def test_extreme_gates_and_betas():
         assert_close(hT, h_ref, torch.bfloat16, f"final state [{algo}]")
 
 
+def test_kda_strong_per_channel_decay():
+    """Per-channel decays far beyond what the factored intra-chunk products take (the kernel then forms every
+    term with its own exponential), next to channels with mild decay, and chunks where only some blocks decay."""
+    x = W.chunk_inputs(W.config(3), seed=4, B=1, T=200, H=2)
+    g = x["g"].clone()
+    g[:, :, 0, :16] = -30.0                 # head 0: 16 channels lose everything within a block
+    g[:, 64:80, 1, 5] = -12.0               # head 1: one channel, one block of one chunk
+    x["g"] = g
+    o_ref, h_ref = oracle_on_heads(x)
+    for algo in _algos(x):
+        o, hT = _run(x, algo)
+        assert_close(o, o_ref, torch.bfloat16, f"o [{algo}]")
+        assert_close(hT, h_ref, torch.bfloat16, f"final state [{algo}]")
+
+
+def test_kda_several_chunks_per_cta():
+    """Enough chunks that every CTA of the per-chunk kernel walks several of them (loads of the next chunk overlap
+    the current one)."""
+    x = W.chunk_inputs(W.config(3), seed=6, B=1, T=4096 + 37, H=8)
+    o_ref, h_ref = oracle_on_heads(x)
+    o, hT = _run(x, "auto")
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
 def test_zero_length_input_keeps_initial_state():
     x = W.chunk_inputs(W.config(1), seed=3, B=2, T=0, H=2)
     for algo in _algos(x):
