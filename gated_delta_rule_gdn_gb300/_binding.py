@@ -41,6 +41,8 @@ def _declare(lib):
     for name in ("gdn_chunk_fwd_ws", "kda_chunk_fwd_ws"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i, chunk + [i, vp, ctypes.c_size_t, vp]
+    lib.gdn_chunk_fwd_noalloc.restype = i
+    lib.gdn_chunk_fwd_noalloc.argtypes = [i] + chunk + [vp]
     lib.gdn_chunk_workspace_size.restype = i
     lib.gdn_chunk_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.gdn_recurrent_step.restype = i
@@ -182,6 +184,33 @@ def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final
     """Chunkwise KDA forward, g per key channel (C ABI kda_chunk_fwd_ws).  Returns (o, final_state or None)."""
     return _chunk(True, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens, chunk_size, algo,
                   o, final_state, stream, o_dtype, workspace)
+
+
+def chunk_fwd_noalloc(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
+                      cu_seqlens=None, o=None, final_state=None, stream=None, o_dtype=torch.float32):
+    """The two-pass chunk forward with the library's static scratch (C ABI gdn_chunk_fwd_noalloc): no allocation
+    inside the call.  Returns (o, final_state or None); raises GdnError for requests above the scratch limit."""
+    lib = load()
+    dev = q.device
+    for name, t, dt in (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32)):
+        _need(t, name, dt, dev)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    n_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    N = n_seqs if cu_seqlens is not None else B
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=o_dtype, device=dev)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if scale is None:
+        scale = dk ** -0.5
+    st = lib.gdn_chunk_fwd_noalloc(int(per_channel), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                   _ptr(initial_state), int(final_state is not None), _ptr(final_state),
+                                   _ptr(cu_seqlens), n_seqs, _ptr(o), B, T, H, dk, dv, 64, DTYPES[q.dtype],
+                                   DTYPES[o_dtype], _stream_handle(stream, dev))
+    _check(st)
+    return o, final_state
 
 
 def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):

@@ -201,6 +201,32 @@ gdn_status kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const f
                         true, "kda_chunk_fwd");
 }
 
+gdn_status gdn_chunk_fwd_noalloc(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, float scale, const float* initial_state, int output_final_state,
+                                 float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T,
+                                 int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype,
+                                 void* stream) {
+    const char* fn = "gdn_chunk_fwd_noalloc";
+    gdn::ChunkArgs a{q, k, v, g, beta, scale, initial_state, final_state, cu_seqlens, n_seqs, o,
+                     B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0,
+                     o_dtype == GDN_F32 ? 1 : 0};
+    gdn_status st = check_chunk(a, dtype, o_dtype, output_final_state, fn);
+    if (st != GDN_OK) return st;
+    if (const char* why = gdn::two_pass_unsupported_reason(a))
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the two-pass kernels do not apply: %s", fn, why);
+    const size_t need = gdn::two_pass_workspace_bytes(a), cap = gdn::static_workspace_capacity();
+    if (need > cap)
+        return fail(GDN_ERR_UNSUPPORTED,
+                    "%s: the request needs %zu bytes of scratch; the static scratch holds %zu (use gdn_chunk_fwd_ws "
+                    "with a caller workspace)", fn, need, cap);
+    void* ws = nullptr;
+    cudaError_t e = gdn::static_workspace(&ws);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    e = gdn::launch_chunk_two_pass(a, ws, cap, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+}
+
 gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               float scale, float* state, void* o, int N, int H, int d_k, int d_v, gdn_dtype dtype,
                               gdn_dtype o_dtype, void* stream) {

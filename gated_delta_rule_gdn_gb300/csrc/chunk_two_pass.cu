@@ -31,6 +31,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "tc_common.cuh"
 #include "chunk_common.cuh"
@@ -38,6 +40,11 @@
 namespace gdn {
 
 __device__ unsigned g_tp_status;
+
+// Scratch of the no-allocation entry point (gdn_chunk_fwd_noalloc): the two-pass workspace of any request that needs
+// at most this much.  Every call on a device shares it.
+constexpr size_t kStaticWorkspaceBytes = 64ull << 20;
+__device__ __align__(256) unsigned char g_static_ws[kStaticWorkspaceBytes];
 
 namespace {
 
@@ -415,13 +422,40 @@ __device__ void kda_gate_tables(uint8_t* smem, KSmall& K, int L, float* gc_out, 
     }
 }
 
+// The 32 channels a lane quad t reduces over: the 8-channel chunks t, t + 4, t + 8, t + 12 (interleaved so that the
+// 16-byte loads of a quarter-warp fall in distinct bank groups).  Row r of a bf16 [rows][128] tile stored as two
+// 128-byte-swizzled 64-column slabs, as fp32:
+__device__ __forceinline__ void ld_bf16_chunks(const uint8_t* base, int r, int t, float (&f)[32]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int cidx = t + 4 * u;
+        float x[8];
+        bf16x8_to_f32(ld16(base + (cidx >> 3) * 16384 + r * 128 + (((cidx & 7) ^ (r & 7)) << 4)), x);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[8 * u + k] = x[k];
+    }
+}
+// the same channels of an fp32 row
+__device__ __forceinline__ void ld_f32_chunks(const float* row, int t, float (&f)[32]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float4 v0 = ld4(row + 8 * (t + 4 * u)), v1 = ld4(row + 8 * (t + 4 * u) + 4);
+        f[8 * u] = v0.x; f[8 * u + 1] = v0.y; f[8 * u + 2] = v0.z; f[8 * u + 3] = v0.w;
+        f[8 * u + 4] = v1.x; f[8 * u + 5] = v1.y; f[8 * u + 6] = v1.z; f[8 * u + 7] = v1.w;
+    }
+}
+
 // KDA, fast path: A = diag(beta)(K K^T with per-channel decays) strictly lower -> Am (fp32) and P = scale (Q K^T with
-// decays) lower incl. the diagonal -> A1 rows 64-127, plus the identity rows of A1.  Warp (a = w / 2, op = w % 2)
-// forms row block a of the K (op 0) or Q (op 1) product against column blocks b <= a with TF32 warp MMAs:
+// decays) lower incl. the diagonal -> A1 rows 64-127, plus the identity rows of A1.  TF32 warp MMAs over the 128
+// channels, with the channel (reduction) order permuted so that lane quad t owns the 32 channels of ld_bf16_chunks:
+// step ks reduces over its channels 2 ks and 2 ks + 1 (the same permutation on both operands leaves the sum alone),
+// which makes every operand load a 16-byte vector.  For row block a against column block b <= a:
 //   row operand x_ic 2^(G_ic - R_a) = x_ic E_ic;   column operand k_jc 2^(R_a - G_jc) =
 //   k_jc F_jc (b = a),   ((k_jc F_jc 2^(R_{b+1} - R_b)) 2^(R_{b+2} - R_{b+1}) ...) (b < a, each factor <= 1).
+// Warp w: product op = w % 2 (K or Q rows), row blocks {0, 3} or {1, 2} ((w / 2) % 2), 8-column half nt = w / 4 of
+// every column block: five 16 x 8 output tiles per warp.
 __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* bb, float scale, int warp, int lane) {
-    const int a = warp >> 1, op = warp & 1;
+    const int op = warp & 1, grp = (warp >> 1) & 1, nt = warp >> 2;
     const int g8 = lane >> 2, t4 = lane & 3;
     const float* E = reinterpret_cast<const float*>(smem + I_EF);
     const float* F = reinterpret_cast<const float*>(smem + I_FF);
@@ -429,33 +463,46 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
     const uint8_t* xb = smem + I_KQ + op * 8192;     // K or Q rows
     float* Am = reinterpret_cast<float*>(smem + I_AM);
     uint8_t* a1 = smem + I_A1;
-    const int r0 = 16 * a + g8, r1 = r0 + 8;
-    uint32_t afr[16][4];
-#pragma unroll
-    for (int ks = 0; ks < 16; ++ks) {
-        const int c0 = 8 * ks + t4, c1 = c0 + 4;
-        afr[ks][0] = to_tf32(ld_bf16_sw(xb, r0, c0) * E[r0 * ES + c0]);
-        afr[ks][1] = to_tf32(ld_bf16_sw(xb, r1, c0) * E[r1 * ES + c0]);
-        afr[ks][2] = to_tf32(ld_bf16_sw(xb, r0, c1) * E[r0 * ES + c1]);
-        afr[ks][3] = to_tf32(ld_bf16_sw(xb, r1, c1) * E[r1 * ES + c1]);
-    }
-    const float s0 = op == 0 ? bb[r0] : scale, s1 = op == 0 ? bb[r1] : scale;
 #pragma unroll 1
-    for (int b = 0; b <= a; ++b) {
+    for (int ai = 0; ai < 2; ++ai) {
+        const int a = grp == 0 ? 3 * ai : 1 + ai;    // {0, 3} or {1, 2}: five column blocks either way
+        const int r0 = 16 * a + g8, r1 = r0 + 8;
+        uint32_t afr[16][4];
+        {
+            float x0[32], x1[32], e[32];
+            ld_bf16_chunks(xb, r0, t4, x0);
+            ld_bf16_chunks(xb, r1, t4, x1);
+            ld_f32_chunks(E + r0 * ES, t4, e);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+            for (int ks = 0; ks < 16; ++ks) {
+                afr[ks][0] = to_tf32(x0[2 * ks] * e[2 * ks]);
+                afr[ks][2] = to_tf32(x0[2 * ks + 1] * e[2 * ks + 1]);
+            }
+            ld_f32_chunks(E + r1 * ES, t4, e);
+#pragma unroll
+            for (int ks = 0; ks < 16; ++ks) {
+                afr[ks][1] = to_tf32(x1[2 * ks] * e[2 * ks]);
+                afr[ks][3] = to_tf32(x1[2 * ks + 1] * e[2 * ks + 1]);
+            }
+        }
+        const float s0 = op == 0 ? bb[r0] : scale, s1 = op == 0 ? bb[r1] : scale;
+#pragma unroll 1
+        for (int b = 0; b <= a; ++b) {
             const int j = 16 * b + 8 * nt + g8;
+            float kv[32], f[32];
+            ld_bf16_chunks(kb, j, t4, kv);
+            ld_f32_chunks(F + j * ES, t4, f);
+#pragma unroll 1
+            for (int m = b; m < a; ++m) {          // 2^(R_a - G_j) = F_j 2^(R_{b+1} - R_b) ... 2^(R_a - R_{a-1})
+                float es[32];
+                ld_f32_chunks(K.esp[m], t4, es);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) f[q] *= es[q];
+            }
             float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
-                const int c0 = 8 * ks + t4, c1 = c0 + 4;
-                float f0 = ld_bf16_sw(kb, j, c0) * F[j * ES + c0];
-                float f1 = ld_bf16_sw(kb, j, c1) * F[j * ES + c1];
-                for (int m = b; m < a; ++m) {
-                    f0 *= K.esp[m][c0];
-                    f1 *= K.esp[m][c1];
-                }
-                const uint32_t b0 = to_tf32(f0), b1 = to_tf32(f1);
+                const uint32_t b0 = to_tf32(kv[2 * ks] * f[2 * ks]), b1 = to_tf32(kv[2 * ks + 1] * f[2 * ks + 1]);
                 asm volatile(
                     "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
                     "{%0, %1, %2, %3};"
@@ -477,29 +524,30 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
                     pack_h2(cc <= r1 ? s1 * d[2] : 0.f, cc + 1 <= r1 ? s1 * d[3] : 0.f);
             }
         }
-    }
-    // zeros above the diagonal blocks: A inside the 32 x 32 diagonal blocks (what the solve reads), P everywhere
-    if (op == 0) {
-        if ((a & 1) == 0) {
-            const int zr = 16 * a + (lane >> 1), zc = 16 * (a + 1) + 8 * (lane & 1);
-            *reinterpret_cast<float4*>(Am + zr * TS + zc) = make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4*>(Am + zr * TS + zc + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        // identity rows 16 a .. 16 a + 15 of A1: lane -> row 16 a + lane / 2, columns 32 (lane % 2) .. + 31
-        const int ir = 16 * a + (lane >> 1);
-        const uint32_t one = (ir & 1) ? 0x3C000000u : 0x00003C00u;
+        if (nt != 0) continue;
+        // zeros above the diagonal blocks: A inside the 32 x 32 diagonal blocks (what the solve reads), P everywhere
+        if (op == 0) {
+            if ((a & 1) == 0) {
+                const int zr = 16 * a + (lane >> 1), zc = 16 * (a + 1) + 8 * (lane & 1);
+                *reinterpret_cast<float4*>(Am + zr * TS + zc) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(Am + zr * TS + zc + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            // identity rows 16 a .. 16 a + 15 of A1: lane -> row 16 a + lane / 2, columns 32 (lane % 2) .. + 31
+            const int ir = 16 * a + (lane >> 1);
+            const uint32_t one = (ir & 1) ? 0x3C000000u : 0x00003C00u;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int c8 = 4 * (lane & 1) + q;
-            const bool here = (ir >> 3) == c8;
-            const int qw = (ir & 7) >> 1;
-            st16(a1 + sw128_off(ir, c8 * 8), here && qw == 0 ? one : 0u, here && qw == 1 ? one : 0u,
-                 here && qw == 2 ? one : 0u, here && qw == 3 ? one : 0u);
-        }
-    } else {
-        for (int e = lane; e < (3 - a) * 16 * 2; e += 32) {   // 16 rows x (3 - a) blocks x two 8-column chunks
-            const int zr = 16 * a + (e & 15), zc = 16 * (a + 1) + 8 * (e >> 4);
-            st16(a1 + sw128_off(64 + zr, zc), 0u, 0u, 0u, 0u);
+            for (int q = 0; q < 4; ++q) {
+                const int c8 = 4 * (lane & 1) + q;
+                const bool here = (ir >> 3) == c8;
+                const int qw = (ir & 7) >> 1;
+                st16(a1 + sw128_off(ir, c8 * 8), here && qw == 0 ? one : 0u, here && qw == 1 ? one : 0u,
+                     here && qw == 2 ? one : 0u, here && qw == 3 ? one : 0u);
+            }
+        } else {
+            for (int e = lane; e < (3 - a) * 16 * 2; e += 32) {   // 16 rows x (3 - a) blocks x two 8-column chunks
+                const int zr = 16 * a + (e & 15), zc = 16 * (a + 1) + 8 * (e >> 4);
+                st16(a1 + sw128_off(64 + zr, zc), 0u, 0u, 0u, 0u);
+            }
         }
     }
 }
@@ -1274,6 +1322,26 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
         chunk_state_kernel<false><<<grid2, S_THREADS, S_SMEM, s>>>(sp);
     }
     return cudaGetLastError();
+}
+
+size_t static_workspace_capacity() { return kStaticWorkspaceBytes; }
+
+cudaError_t static_workspace(void** ptr) {
+    static std::mutex mu;
+    static void* addr[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_ws);   // with this device current
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t tp_read_and_clear_status(unsigned* value, bool clear) {

@@ -56,6 +56,10 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s);
 const char* two_pass_unsupported_reason(const ChunkArgs& a);
 size_t two_pass_workspace_bytes(const ChunkArgs& a);
 cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s);
+// The statically allocated two-pass workspace: its size, and its device address on the current device (looked up
+// once per device with cudaGetSymbolAddress).
+size_t static_workspace_capacity();
+cudaError_t static_workspace(void** ptr);
 
 // Shared host helpers of the tcgen05 paths (chunk_tc.cu).
 // TMA map of a [rows][H][d] bf16 tensor, box 64 elements x 1 head x 64 rows, 128-byte swizzle.

@@ -181,6 +181,32 @@ gdn_status kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const f
                             void* stream);
 
 /*
+ * gdn_chunk_fwd_noalloc -- the two-pass chunk forward (GDN_ALGO_TWO_PASS;
+ * per_channel nonzero: the KDA gate, as kda_chunk_fwd) with its workspace in a
+ * statically allocated device array of the library instead of caller or
+ * stream-ordered memory: the call allocates and frees nothing.  The pages
+ * describe no counterpart; this entry point exists for callers that must not
+ * allocate (for example inside a captured graph's replay loop).
+ *   Limit: the static scratch holds 64 MiB, i.e. (floor(B*T / 64) + N + 1) * H
+ *   * 82,432 bytes must not exceed 67,108,864 (about 800 (chunk, head) items,
+ *   e.g. one 4096-token sequence with 12 heads).  A larger request returns
+ *   GDN_ERR_UNSUPPORTED with the sizes in the message and launches nothing.
+ *   Sharing: every call on a device uses the same scratch, so calls whose work
+ *   can overlap (different streams, or threads without ordering) race and give
+ *   unspecified results; order them on one stream.  Nothing in the scratch
+ *   needs to start at zero: each call writes every byte it later reads.
+ *   Set-up: the first call on a device looks the scratch up
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ * Other arguments, layouts and status codes are those of gdn_chunk_fwd.
+ */
+gdn_status gdn_chunk_fwd_noalloc(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, float scale, const float* initial_state, int output_final_state,
+                                 float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o,
+                                 int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                                 gdn_dtype o_dtype, void* stream);
+
+/*
  * gdn_recurrent_step -- one decode token for N independent sequences.
  *
  * Sources: "Gated Delta Network (GDN)", eq. 12 and §4.4 (decode runs the
