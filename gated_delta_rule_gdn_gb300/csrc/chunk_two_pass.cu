@@ -499,16 +499,19 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
 #pragma unroll
                 for (int q = 0; q < 32; ++q) f[q] *= es[q];
             }
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};   // two independent chains
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
                 const uint32_t b0 = to_tf32(kv[2 * ks] * f[2 * ks]), b1 = to_tf32(kv[2 * ks + 1] * f[2 * ks + 1]);
+                float (&acc)[4] = (ks & 1) ? d2 : d;
                 asm volatile(
                     "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
                     "{%0, %1, %2, %3};"
-                    : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                    : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
                     : "r"(afr[ks][0]), "r"(afr[ks][1]), "r"(afr[ks][2]), "r"(afr[ks][3]), "r"(b0), "r"(b1));
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d[q] += d2[q];
             const int cc = 16 * b + 8 * nt + 2 * t4;
             if (op == 0) {
                 // A = beta_i (K K^T)_ij for j < i
@@ -1083,7 +1086,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
     const uint32_t tmem = S.tmem_base;
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
 
-    if (leader) {
+    if (tid == 32) {
         for (int t = 0; t < 2 && t < n_chunks; ++t) state_issue(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
     }
     int issued = n_chunks < 2 ? n_chunks : 2;
@@ -1217,13 +1220,13 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
         fence_async_smem();
         tc_fence_before();
         __syncthreads();   // stage s, D3, D4 and Delta are free
-        if (ok && leader && t + 2 < n_chunks) {
+        if (ok && tid == 32 && t + 2 < n_chunks) {   // not the MMA thread: the copies' issue stays off its path
             state_issue(smem, S, p.ws, (slot0 + t + 2) * H + ch.h, ch.half, s);
             issued = t + 3;
         }
     }
     // stages issued but never waited on (after a timeout) must land before the CTA exits
-    if (leader) {
+    if (tid == 32) {
         for (int t = waited; t < issued; ++t) mbar_wait(&S.full[t & 1], (t >> 1) & 1, kWaitNs);
     }
     if (p.hT && ok) {
