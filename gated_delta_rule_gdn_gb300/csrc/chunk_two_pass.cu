@@ -937,26 +937,30 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 const float sg = (which == 1 && row >= 64) ? -1.f : 1.f;
                 uint8_t* dst = (which == 0 ? ws.wq + (size_t)it.it * WS_WQ : ws.uu + (size_t)it.it * WS_UU) +
                                pw * 16384 + q4 * 4096;
+                if (which == 1) {   // the bulk copy of [W; Q'] has read the staging rows
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
+                }
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[16];
-                    tmem_ld16(tl + I_TM_D2 + tcol + cb * 16, r);
+                for (int cp = 0; cp < 2; ++cp) {
+                    uint32_t r[2][16];
+                    tmem_ld16(tl + I_TM_D2 + tcol + cp * 32, r[0]);
+                    tmem_ld16(tl + I_TM_D2 + tcol + cp * 32 + 16, r[1]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int h8 = 0; h8 < 2; ++h8) {
+                    for (int h8 = 0; h8 < 4; ++h8) {
                         float f[8];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) f[q] = sg * __uint_as_float(r[h8 * 8 + q]);
-                        st_h8(stg + sw128_off(lane, cb * 16 + h8 * 8), f);
+                        for (int q = 0; q < 8; ++q) f[q] = sg * __uint_as_float(r[h8 >> 1][(h8 & 1) * 8 + q]);
+                        st_h8(stg + sw128_off(lane, cp * 32 + h8 * 8), f);
                     }
                 }
+                fence_async_smem();   // the staging rows are read by the bulk-copy engine
                 __syncwarp();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint4 v = ld16(stg + k * 512 + lane * 16);
-                    stg16(dst + k * 512 + lane * 16, v.x, v.y, v.z, v.w);
+                if (lane == 0) {
+                    bulk_s2g(dst, stg, 4096);
+                    bulk_commit();
                 }
-                __syncwarp();
             }
         }
         tc_fence_before();
@@ -966,11 +970,13 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             S.bbuf[lane] = nb[0];
             S.bbuf[lane + 32] = nb[1];
         }
+        if (lane == 0) bulk_wait_read();   // the staging regions are written again during the next item
         x = nx;
         cur = nc;
         have = ok && have_next;
         if (ok) ++ic;
     }
+    if (lane == 0) bulk_wait_all();       // the workspace writes are complete before the CTA exits
     // loads that were issued but never waited on (after a timeout) must land before the CTA exits
     if (loader) {
         for (uint32_t k = kq_waited; k < kq_issued; ++k) mbar_wait(&S.full_kq, k & 1, kWaitNs);
