@@ -997,34 +997,46 @@ struct StateParams {
     Ws ws;
 };
 
-constexpr uint32_t S_WQ = 0, S_KT = 32768, S_UU = 49152, S_GC = 65536;
-constexpr uint32_t S_STAGE = 66560;                 // one workspace slot (this CTA's d_v half of [U; U'])
-constexpr uint32_t S_H = 2 * S_STAGE;               // h, fp16 MN-major [d][n] 128 x 64
-constexpr uint32_t S_D = S_H + 16384;               // Delta, fp16 MN-major [j][n] 64 x 64
-constexpr uint32_t S_SMALL = S_D + 8192;
+// Shared memory of pass 2.  Narrow: one CTA per (sequence, head, 64-column d_v half), 4 warps.  Wide: one CTA per
+// (sequence, head) over all 128 columns, 8 warps (two per TMEM lane quarter, one per 64-column half), for workloads
+// with more chains than one CTA per SM can hold at once.
+template <bool WIDE>
+struct SLayout {
+    static constexpr uint32_t NCOL = WIDE ? 128 : 64;             // d_v columns of the CTA
+    static constexpr uint32_t WQ = 0, KT = 32768, UU = 49152;
+    static constexpr uint32_t GC = UU + NCOL * 256;                // [U; U'] of the CTA's columns: 16 KB per half
+    static constexpr uint32_t STAGE = (GC + 512 + 1023) & ~1023u;  // one workspace slot
+    static constexpr uint32_t H = 2 * STAGE;                       // h, fp16 MN-major [d][n], 16 KB per half
+    static constexpr uint32_t D = H + NCOL * 256;                  // Delta, fp16 MN-major [j][n], 8 KB per half
+    static constexpr uint32_t SMALL = D + NCOL * 128;
+    static constexpr int THREADS = WIDE ? 256 : 128;
+    static constexpr uint32_t TM_D3 = 0, TM_D4 = NCOL, TM_COLS = 2 * NCOL;
+};
 struct SSmall {
     uint64_t full[2];
     uint64_t m3, m4;
     uint32_t tmem_base;
     uint32_t pad;
 };
-constexpr uint32_t S_SMEM = S_SMALL + sizeof(SSmall) + 1024;
-constexpr uint32_t S_TM_D3 = 0, S_TM_D4 = 64, S_TM_COLS = 128;
-constexpr int S_THREADS = 128;
+template <bool WIDE>
+constexpr uint32_t s_smem_bytes() { return SLayout<WIDE>::SMALL + sizeof(SSmall) + 1024; }
+static_assert(s_smem_bytes<true>() <= 227 * 1024, "wide state kernel shared memory");
 
 struct Chain {
     int n, h, half, len;
     long row0;
 };
 
-// CTA -> (sequence, head, d_v half); packed sequences longest first (their chains are the longest serial paths)
+// CTA -> (sequence, head, d_v half or both); packed sequences longest first (their chains are the longest serial
+// paths)
+template <bool WIDE>
 __device__ Chain resolve_chain(const Geo& g) {
     Chain c;
-    const int per_seq = g.H * 2;
+    const int per_seq = g.H * (WIDE ? 1 : 2);
     const int seq_rank = blockIdx.x / per_seq;
     const int rem = blockIdx.x % per_seq;
-    c.h = rem / 2;
-    c.half = rem % 2;
+    c.h = WIDE ? rem : rem / 2;
+    c.half = WIDE ? 0 : rem % 2;
     int n = seq_rank;
     if (g.cu && g.n_seqs <= 32) {
         const int lane = threadIdx.x & 31;
@@ -1049,34 +1061,41 @@ __device__ Chain resolve_chain(const Geo& g) {
     return c;
 }
 
+template <bool WIDE>
 __device__ __forceinline__ void state_issue(uint8_t* smem, SSmall& S, const Ws& ws, long it, int half, int s) {
-    uint8_t* st = smem + s * S_STAGE;
-    mbar_arrive_expect_tx(&S.full[s], WS_WQ + WS_KT + 16384 + WS_GC);
-    bulk_g2s(st + S_WQ, ws.wq + (size_t)it * WS_WQ, WS_WQ, &S.full[s]);
-    bulk_g2s(st + S_KT, ws.kt + (size_t)it * WS_KT, WS_KT, &S.full[s]);
-    bulk_g2s(st + S_UU, ws.uu + (size_t)it * WS_UU + half * 16384, 16384, &S.full[s]);
-    bulk_g2s(st + S_GC, ws.gc + (size_t)it * 128, WS_GC, &S.full[s]);
+    using LY = SLayout<WIDE>;
+    uint8_t* st = smem + s * LY::STAGE;
+    mbar_arrive_expect_tx(&S.full[s], WS_WQ + WS_KT + LY::NCOL * 256 + WS_GC);
+    bulk_g2s(st + LY::WQ, ws.wq + (size_t)it * WS_WQ, WS_WQ, &S.full[s]);
+    bulk_g2s(st + LY::KT, ws.kt + (size_t)it * WS_KT, WS_KT, &S.full[s]);
+    bulk_g2s(st + LY::UU, ws.uu + (size_t)it * WS_UU + half * 16384, LY::NCOL * 256, &S.full[s]);
+    bulk_g2s(st + LY::GC, ws.gc + (size_t)it * 128, WS_GC, &S.full[s]);
 }
 
-template <bool O_F32>
-__global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StateParams p) {
+template <bool O_F32, bool WIDE>
+__global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(const StateParams p) {
+    using LY = SLayout<WIDE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    SSmall& S = *reinterpret_cast<SSmall*>(smem + S_SMALL);
+    SSmall& S = *reinterpret_cast<SSmall*>(smem + LY::SMALL);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const Chain ch = resolve_chain(p.geo);
+    const int q4 = warp & 3, pw = warp >> 2;    // TMEM lane quarter; 64-column half within the CTA (wide only)
+    const Chain ch = resolve_chain<WIDE>(p.geo);
     const int n_chunks = (ch.len + C - 1) / C;
     const long slot0 = ch.row0 / C + ch.n;
     const int H = p.geo.H;
-    const int row = 32 * warp + lane;           // TMEM lane: token row of D3, d_k row of D4 and of h
+    const int row = 32 * q4 + lane;             // TMEM lane: token row of D3, d_k row of D4 and of h
     const bool leader = (tid == 0);
-    const bool delta_warp = warp < 2;
+    const bool issuer = (tid == 32);            // issues the copies, off the MMA thread's path
+    const bool delta_warp = q4 < 2;
+    const int col0 = (WIDE ? pw : ch.half) * DVT;   // first d_v column of this thread in the full head
+    const uint32_t cs = WIDE ? pw * 64 : 0;         // this thread's column offset inside the CTA's tiles
 
     if (warp == 0) {
-        tmem_alloc(&S.tmem_base, S_TM_COLS);
+        tmem_alloc(&S.tmem_base, LY::TM_COLS);
         tmem_relinquish();
     }
     if (tid == 32) {
@@ -1090,14 +1109,15 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
-    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
 
-    if (tid == 32) {
-        for (int t = 0; t < 2 && t < n_chunks; ++t) state_issue(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
+    if (issuer) {
+        for (int t = 0; t < 2 && t < n_chunks; ++t)
+            state_issue<WIDE>(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
     }
     int issued = n_chunks < 2 ? n_chunks : 2;
 
-    const size_t sidx = ((size_t)ch.n * H + ch.h) * DK * DV + (size_t)row * DV + ch.half * DVT;
+    const size_t sidx = ((size_t)ch.n * H + ch.h) * DK * DV + (size_t)row * DV + col0;
     float hreg[DVT];
 #pragma unroll
     for (int q = 0; q < DVT / 4; ++q) {
@@ -1107,8 +1127,9 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
         hreg[4 * q + 2] = v.z;
         hreg[4 * q + 3] = v.w;
     }
+    // h to fp16, MN-major [d][n] (operand B of MMA3), one 16 KB slab per 64-column half
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + S_H + sw128_off(row, c8 * 8), hreg + c8 * 8);
+    for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + LY::H + cs * 256 + sw128_off(row, c8 * 8), hreg + c8 * 8);
     fence_async_smem();
     __syncthreads();
 
@@ -1116,8 +1137,8 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
     int waited = 0;   // chunks whose stage wait completed
     for (int t = 0; t < n_chunks; ++t) {
         const int s = t & 1;
-        const uint8_t* st = smem + s * S_STAGE;
-        const uint32_t stb = sbase + s * S_STAGE;
+        const uint8_t* st = smem + s * LY::STAGE;
+        const uint32_t stb = sbase + s * LY::STAGE;
         const int L = min(C, ch.len - t * C);
         if (ok) ok = mbar_wait(&S.full[s], (t >> 1) & 1, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
@@ -1126,11 +1147,11 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
         // MMA3: D3 = [W; Q'] h
         if (ok && leader) {
             tc_fence_after();
-            const uint32_t id = idesc_f16(128, 64, false, false, true);
+            const uint32_t id = idesc_f16(128, LY::NCOL, false, false, true);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_f16(tmem + S_TM_D3, sdesc(stb + S_WQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                        sdesc(sbase + S_H + ks * 2048, 1024, 1024), id, ks > 0);
+                mma_f16(tmem + LY::TM_D3, sdesc(stb + LY::WQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                        sdesc(sbase + LY::H + ks * 2048, 16384, 1024), id, ks > 0);
             mma_commit(&S.m3);
         }
         if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
@@ -1139,16 +1160,16 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
         tc_fence_after();
         const int i = row - 64;
         const bool store_o = !delta_warp && i < L;
-        const size_t orow = ((size_t)(ch.row0 + (long)t * C + (row & 63)) * H + ch.h) * DV + ch.half * DVT;
+        const size_t orow = ((size_t)(ch.row0 + (long)t * C + (row & 63)) * H + ch.h) * DV + col0;
 #pragma unroll
         for (int hp = 0; hp < 4; ++hp) {
             uint32_t a[16];
             float u[16];
             if (ok) {
-                tmem_ld16(tl + S_TM_D3 + hp * 16, a);
+                tmem_ld16(tl + LY::TM_D3 + cs + hp * 16, a);
 #pragma unroll
                 for (int h8 = 0; h8 < 2; ++h8) {
-                    const uint4 v = ld16(st + S_UU + sw128_off(row, hp * 16 + h8 * 8));
+                    const uint4 v = ld16(st + LY::UU + cs * 256 + sw128_off(row, hp * 16 + h8 * 8));
                     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
@@ -1166,7 +1187,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
                     float f[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) f[q] = u[h8 * 8 + q] - __uint_as_float(a[h8 * 8 + q]);
-                    st_h8(smem + S_D + sw128_off(row, hp * 16 + h8 * 8), f);
+                    st_h8(smem + LY::D + cs * 128 + sw128_off(row, hp * 16 + h8 * 8), f);
                 }
             } else if (ok && store_o) {
                 // O = U' + Q' h (token rows 64-127)
@@ -1195,15 +1216,15 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
         if (delta_warp) {
             fence_async_smem();
             tc_fence_before();
-            named_bar(1, 64);
+            named_bar(1, LY::THREADS / 2);   // the Delta warps (lane quarters 0 and 1)
             // MMA4: D4 = Ktilde^T Delta
             if (ok && leader) {
                 tc_fence_after();
-                const uint32_t id = idesc_f16(128, 64, false, true, true);
+                const uint32_t id = idesc_f16(128, LY::NCOL, false, true, true);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tmem + S_TM_D4, sdesc(stb + S_KT + ks * 2048, 8192, 1024),
-                            sdesc(sbase + S_D + ks * 2048, 1024, 1024), id, ks > 0);
+                    mma_f16(tmem + LY::TM_D4, sdesc(stb + LY::KT + ks * 2048, 8192, 1024),
+                            sdesc(sbase + LY::D + ks * 2048, 8192, 1024), id, ks > 0);
                 mma_commit(&S.m4);
             }
         }
@@ -1213,26 +1234,26 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
         tc_fence_after();
         // h <- gamma_C h + Ktilde^T Delta; fp16 copy for the next MMA3
         if (ok) {
-            const float gC = reinterpret_cast<const float*>(st + S_GC)[row];
+            const float gC = reinterpret_cast<const float*>(st + LY::GC)[row];
             uint32_t r[4][16];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + S_TM_D4 + cb * 16, r[cb]);
+            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + LY::TM_D4 + cs + cb * 16, r[cb]);
             tmem_ld_wait();
 #pragma unroll
             for (int k = 0; k < 64; ++k) hreg[k] = fmaf(gC, hreg[k], __uint_as_float(r[k >> 4][k & 15]));
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + S_H + sw128_off(row, c8 * 8), hreg + c8 * 8);
+            for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + LY::H + cs * 256 + sw128_off(row, c8 * 8), hreg + c8 * 8);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();   // stage s, D3, D4 and Delta are free
-        if (ok && tid == 32 && t + 2 < n_chunks) {   // not the MMA thread: the copies' issue stays off its path
-            state_issue(smem, S, p.ws, (slot0 + t + 2) * H + ch.h, ch.half, s);
+        if (ok && issuer && t + 2 < n_chunks) {
+            state_issue<WIDE>(smem, S, p.ws, (slot0 + t + 2) * H + ch.h, ch.half, s);
             issued = t + 3;
         }
     }
     // stages issued but never waited on (after a timeout) must land before the CTA exits
-    if (tid == 32) {
+    if (issuer) {
         for (int t = waited; t < issued; ++t) mbar_wait(&S.full[t & 1], (t >> 1) & 1, kWaitNs);
     }
     if (p.hT && ok) {
@@ -1244,7 +1265,7 @@ __global__ void __launch_bounds__(S_THREADS, 1) chunk_state_kernel(const StatePa
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, S_TM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, LY::TM_COLS);
 }
 
 long n_slots(const ChunkArgs& a) { return (long)a.B * a.T / C + a.N() + 1; }
@@ -1320,16 +1341,25 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     if (e != cudaSuccess) return e;
 
     StateParams sp{geo, a.h0, a.hT, a.o, ws};
-    const unsigned grid2 = (unsigned)(chains * 2);
-    if (a.o_f32) {
-        e = cudaFuncSetAttribute(chunk_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
-        if (e != cudaSuccess) return e;
-        chunk_state_kernel<true><<<grid2, S_THREADS, S_SMEM, s>>>(sp);
+    // The wide variant (one CTA per chain over all 128 columns) halves the CTAs of an oversubscribed grid at the cost
+    // of a longer step per chunk; it pays only when every chain has the same length (packed sequences can put one
+    // long chain on the critical path, which the narrow variant runs faster).
+    const bool wide = !a.cu && chains * 2 > sms;
+    const unsigned grid2 = (unsigned)(wide ? chains : chains * 2);
+    auto launch2 = [&](auto kern, int threads, uint32_t bytes) -> cudaError_t {
+        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e2 != cudaSuccess) return e2;
+        kern<<<grid2, threads, bytes, s>>>(sp);
+        return cudaSuccess;
+    };
+    if (wide) {
+        e = a.o_f32 ? launch2(chunk_state_kernel<true, true>, SLayout<true>::THREADS, s_smem_bytes<true>())
+                    : launch2(chunk_state_kernel<false, true>, SLayout<true>::THREADS, s_smem_bytes<true>());
     } else {
-        e = cudaFuncSetAttribute(chunk_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
-        if (e != cudaSuccess) return e;
-        chunk_state_kernel<false><<<grid2, S_THREADS, S_SMEM, s>>>(sp);
+        e = a.o_f32 ? launch2(chunk_state_kernel<true, false>, SLayout<false>::THREADS, s_smem_bytes<false>())
+                    : launch2(chunk_state_kernel<false, false>, SLayout<false>::THREADS, s_smem_bytes<false>());
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -132,6 +132,17 @@ def test_kda_several_chunks_per_cta():
     assert_close(hT, h_ref, torch.bfloat16, "final state")
 
 
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_many_chains_use_the_full_width_state_pass(kind):
+    """More (sequence, head) chains than half the SMs in a uniform batch: the state pass runs one CTA per chain
+    over all 128 value columns instead of one per half."""
+    x = W.chunk_inputs(W.config(3 if kind == "kda" else 1), seed=8, B=3, T=150, H=30)
+    o_ref, h_ref = oracle_on_heads(x)
+    o, hT = _run(x, "auto")
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
 def test_zero_length_input_keeps_initial_state():
     x = W.chunk_inputs(W.config(1), seed=3, B=2, T=0, H=2)
     for algo in _algos(x):
