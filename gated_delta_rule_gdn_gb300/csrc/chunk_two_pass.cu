@@ -1133,12 +1133,17 @@ __global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(
     fence_async_smem();
     __syncthreads();
 
+    // Operand descriptors, built once; a k-step adds its byte offset >> 4 to the start-address field (the operands
+    // lie below 256 KB, so the field never carries).
+    const uint64_t dH = sdesc(sbase + LY::H, 16384, 1024), dD = sdesc(sbase + LY::D, 8192, 1024);
+    const uint64_t dWQ = sdesc(sbase + LY::WQ, 16, 1024), dKT = sdesc(sbase + LY::KT, 8192, 1024);
+    const uint32_t id3 = idesc_f16(128, LY::NCOL, false, false, true), id4 = idesc_f16(128, LY::NCOL, false, true, true);
     bool ok = true;
     int waited = 0;   // chunks whose stage wait completed
     for (int t = 0; t < n_chunks; ++t) {
         const int s = t & 1;
         const uint8_t* st = smem + s * LY::STAGE;
-        const uint32_t stb = sbase + s * LY::STAGE;
+        const uint64_t so = (uint64_t)((s * LY::STAGE) >> 4);
         const int L = min(C, ch.len - t * C);
         if (ok) ok = mbar_wait(&S.full[s], (t >> 1) & 1, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
@@ -1147,11 +1152,10 @@ __global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(
         // MMA3: D3 = [W; Q'] h
         if (ok && leader) {
             tc_fence_after();
-            const uint32_t id = idesc_f16(128, LY::NCOL, false, false, true);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_f16(tmem + LY::TM_D3, sdesc(stb + LY::WQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                        sdesc(sbase + LY::H + ks * 2048, 16384, 1024), id, ks > 0);
+                mma_f16(tmem + LY::TM_D3, dWQ + so + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), dH + (uint64_t)(ks * 128),
+                        id3, ks > 0);
             mma_commit(&S.m3);
         }
         if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
@@ -1220,11 +1224,9 @@ __global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(
             // MMA4: D4 = Ktilde^T Delta
             if (ok && leader) {
                 tc_fence_after();
-                const uint32_t id = idesc_f16(128, LY::NCOL, false, true, true);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tmem + LY::TM_D4, sdesc(stb + LY::KT + ks * 2048, 8192, 1024),
-                            sdesc(sbase + LY::D + ks * 2048, 8192, 1024), id, ks > 0);
+                    mma_f16(tmem + LY::TM_D4, dKT + so + (uint64_t)(ks * 128), dD + (uint64_t)(ks * 128), id4, ks > 0);
                 mma_commit(&S.m4);
             }
         }
