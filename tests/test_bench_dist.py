@@ -1,0 +1,53 @@
+"""bench.py's multi-rank host logic on CPU: two gloo ranks on 127.0.0.1.
+
+Under torchrun each rank runs its own replica of the workload; the timing is the maximum over ranks, and the
+reference arm runs on rank 0 alone.  These tests exercise that logic without a GPU.
+"""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank: int, world: int, port: int, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    ws, r, _ = bench._dist()
+    assert (ws, r) == (world, rank)
+    bench._init_pg(ws, "gloo")
+    bench.barrier(ws)
+    got = bench.max_over_ranks(10.0 + rank, ws)
+    # the reference arm runs on rank 0 only: other ranks return at once, before touching any workload
+    rc = 0 if rank == 0 else bench.run_reference(type("A", (), {"workload": 1, "steps": 1, "warmup": 3})())
+    import torch.distributed as dist
+    dist.destroy_process_group()
+    out.put((rank, got, rc))
+
+
+def test_max_over_ranks_barrier_and_rank0_only_reference():
+    world = 2
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(out.get(timeout=5) for _ in range(world))
+    assert [g for _, g, _ in res] == [11.0, 11.0]
+    assert [rc for _, _, rc in res] == [0, 0]
