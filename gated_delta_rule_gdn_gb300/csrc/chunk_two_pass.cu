@@ -685,6 +685,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 }
                 mma_commit(&S.m0);
             }
+            if (lane == 0) bulk_wait_read();   // the previous item's staging rows (X, A1) have been read
             __syncthreads();   // [B] gate prefix ready
             if (ok) {
                 // beta gamma K -> X slabs 2-3 and Ktilde = (gamma_C / gamma) K -> workspace.  Operation e = tid + 256
@@ -757,6 +758,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             ok = __all_sync(0xffffffffu, ok);
             if (!ok && tid == 0) set_status(2u);
             if (ok && loader) v_waited = ic + 1;
+            if (lane == 0) bulk_wait_read();   // the previous item's staging rows (E, A1) have been read
+            __syncwarp();
             // [B] the gate tables (contains the barrier that decides the fast path)
             kda_gate_tables(smem, KS, ok ? L : 0, ws.gc + (size_t)it.it * 128, tid);
             __syncthreads();
@@ -970,7 +973,6 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             S.bbuf[lane] = nb[0];
             S.bbuf[lane + 32] = nb[1];
         }
-        if (lane == 0) bulk_wait_read();   // the staging regions are written again during the next item
         x = nx;
         cur = nc;
         have = ok && have_next;
