@@ -213,11 +213,49 @@ def cpu_baseline(x, w, min_seconds=8.0, max_passes=5, heads=None):
                       f"{passes} pass(es), {t_total:.1f} s; tokens/s scaled to all {w.H} heads"}
 
 
+def run_reference_decode(args):
+    """The oracle on a decode step: one token for a sample of the (sequence, head) chains, scaled to all of them."""
+    from gated_delta_rule_gdn_gb300 import workloads as W
+    import oracle
+    import torch
+    w = _decode_workload(args.workload)
+    consts = W.decode_constants(w, seed=0)
+    NH = w.N * w.H
+    sample = torch.arange(0, NH, 16)                  # 512 of the 8192 chains
+    x = W.decode_step_inputs(w, consts, 0)
+    h0 = consts["state"].reshape(NH, 1, w.dk, w.dv)[sample].to(torch.float64).numpy()
+    q, k, v = (x[n].reshape(NH, 1, 1, -1)[sample].to(torch.float64).numpy() for n in ("q", "k", "v"))
+    beta = x["beta"].reshape(NH, 1, 1)[sample].to(torch.float64).numpy()
+    g = (x["g"].reshape(NH, 1, 1, -1) if w.kind == "kda" else x["g"].reshape(NH, 1, 1))[sample].to(torch.float64).numpy()
+    oracle.load()
+    run = lambda: oracle.recurrence(q, k, v, g, beta, w.scale, h0, gate_per_channel=w.kind == "kda")
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps * (NH / len(sample))
+    value = w.N / dt
+    line = {"impl": "reference", "metric": f"{w.kind.upper()} decode-step tokens/s ({w.name}) and % of HBM roofline, 1×GB300",
+            "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": w.name, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"per step one token for {len(sample)} of {NH} (sequence, head) chains; "
+                                       f"time scaled to all chains"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+    return 0
+
+
 def run_reference(args):
     ws, rank, local = _dist()
     if ws > 1:
         if rank != 0:
             return 0
+    if args.workload >= 4:
+        return run_reference_decode(args)
     from gated_delta_rule_gdn_gb300 import workloads as W
     import oracle
     w = W.config(args.workload)
@@ -375,6 +413,118 @@ def run_ours(args):
     return 0
 
 
+def _decode_workload(which: int):
+    from gated_delta_rule_gdn_gb300 import workloads as W
+    w4 = W.config(4)
+    if which == 4:
+        return w4
+    return W.DecodeWorkload("kda_decode_n256_h32_d128", w4.N, w4.H, w4.dk, w4.dv, w4.steps, kind="kda")
+
+
+def _decode_alg_bytes(w) -> int:
+    """Algorithmic HBM bytes of one decode step: the fp32 state read and written, q, k, v (bf16), g, beta, o (fp32)."""
+    nh = w.N * w.H
+    g_bytes = 4 * w.dk if w.kind == "kda" else 4
+    return nh * (2 * w.dk * w.dv * 4 + 2 * (2 * w.dk + w.dv) + g_bytes + 4 + 4 * w.dv)
+
+
+def run_decode(args):
+    """One step = one decode token for every (sequence, head): the state ([N, H, 128, 128] fp32) is read and written
+    in place.  Inputs cycle through 8 pre-drawn steps; the 512 MiB state is larger than L2, so no flush is needed."""
+    import torch
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _init_pg(ws, "nccl")
+    import gated_delta_rule_gdn_gb300 as gdn
+    from gated_delta_rule_gdn_gb300 import build as libbuild, workloads as W
+    if local == 0:
+        libbuild.build()
+    barrier(ws)
+    gdn.load()
+    w = _decode_workload(args.workload)
+    consts = W.decode_constants(w, seed=0)
+    state = consts["state"].to(dev)
+    host = [W.decode_step_inputs(w, consts, s_) for s_ in range(8)]
+    host = [{k: v.pin_memory() for k, v in x.items()} for x in host]
+    dev_in = [{k: v.to(dev) for k, v in x.items()} for x in host]
+    o = torch.empty((w.N, w.H, w.dv), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = gdn.kda_recurrent_step if w.kind == "kda" else gdn.gdn_recurrent_step
+
+    def call(x, oo):
+        step(x["q"], x["k"], x["v"], x["g"], x["beta"], state, scale=w.scale, o=oo, stream=stream)
+
+    for i in range(args.warmup):
+        call(dev_in[i % 8], o)
+    torch.cuda.synchronize(dev)
+    assert gdn.device_status() == 0
+    sampler = ClockSampler(int(os.environ.get("GDN_BENCH_GPU_INDEX", local))) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for i in range(8):
+                call(dev_in[i], o)
+            torch.cuda.synchronize(dev)
+        sampler.mark()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_wall = time.perf_counter()
+    for i, (e0, e1) in enumerate(evs):
+        e0.record(stream)
+        call(dev_in[i % 8], o)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs), ws, dev)
+    clocks = sampler.stop() if sampler else None
+    assert gdn.device_status() == 0
+    # end to end: each step's inputs host -> device, the call, o device -> host (the state stays resident)
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    dd = {k: torch.empty_like(v) for k, v in dev_in[0].items()}
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = o_host.numel() * o_host.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        for k in dd:
+            dd[k].copy_(host[i % 8][k], non_blocking=True)
+        call(dd, o)
+        o_host.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+    tokens = w.N
+    peak, peak_kind = _peaks()
+    alg = _decode_alg_bytes(w)
+    achieved = alg / (ms / 1e3) / 1e9
+    line = {
+        "metric": f"{w.kind.upper()} decode-step tokens/s ({w.name}) and % of HBM roofline, 1×GB300",
+        "value": tokens * ws / (ms / 1e3), "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k unit-norm, v N(0,1), beta=sigmoid(N), gates as the chunk recipes)",
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv, "o_dtype": "f32",
+                   "l2": "not flushed: the 512 MiB state read and written every step is larger than L2",
+                   "kernel": "recurrent_step", "timed_region_wall_ms": t_wall * 1e3},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6800 GB/s", "algorithmic_bytes_per_step": alg},
+        "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -383,13 +533,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--algo", choices=["auto", "generic", "tcgen05", "two_pass"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", type=int, choices=[1, 2, 3], default=WORKLOAD,
-                    help="1: GDN B4 T4096 H16 (the headline), 2: packed GDN 8 seqs 65536 tokens H32, 3: KDA B2 T8192 H32")
+    ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4, 5], default=WORKLOAD,
+                    help="1: GDN B4 T4096 H16 (the headline), 2: packed GDN 8 seqs 65536 tokens H32, 3: KDA B2 T8192 "
+                         "H32, 4: GDN decode step 256 seqs H32, 5: KDA decode step 256 seqs H32")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload >= 4:
+        return run_decode(args)
     return run_ours(args)
 
 

@@ -6,8 +6,8 @@ supplies device memory and streams.  Build the library with
 ``gated_delta_rule_gdn_gb300.build.build()``; the calls raise if it is
 missing.
 """
-from ._binding import (GdnError, chunk_fwd_noalloc, chunk_plan, device_status, gdn_chunk_fwd, gdn_recurrent_step, kda_chunk_fwd, last_error,
+from ._binding import (GdnError, chunk_fwd_noalloc, chunk_plan, device_status, gdn_chunk_fwd, gdn_recurrent_step, kda_chunk_fwd, kda_recurrent_step, last_error,
                        lib_path, load, workspace_size)
 
-__all__ = ["gdn_chunk_fwd", "kda_chunk_fwd", "gdn_recurrent_step", "device_status", "chunk_plan", "last_error", "load",
+__all__ = ["gdn_chunk_fwd", "kda_chunk_fwd", "gdn_recurrent_step", "kda_recurrent_step", "device_status", "chunk_plan", "last_error", "load",
            "lib_path", "GdnError", "workspace_size", "chunk_fwd_noalloc"]

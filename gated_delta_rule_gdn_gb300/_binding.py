@@ -45,8 +45,9 @@ def _declare(lib):
     lib.gdn_chunk_fwd_noalloc.argtypes = [i] + chunk + [vp]
     lib.gdn_chunk_workspace_size.restype = i
     lib.gdn_chunk_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
-    lib.gdn_recurrent_step.restype = i
-    lib.gdn_recurrent_step.argtypes = [vp, vp, vp, vp, vp, fp, vp, vp, i, i, i, i, i, i, vp]
+    for name in ("gdn_recurrent_step", "kda_recurrent_step"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i, [vp, vp, vp, vp, vp, fp, vp, vp, i, i, i, i, i, i, vp]
     lib.gdn_chunk_plan.restype = i
     lib.gdn_chunk_plan.argtypes = [i, i, i, i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
     lib.gdn_last_error.restype = ctypes.c_char_p
@@ -213,8 +214,7 @@ def chunk_fwd_noalloc(per_channel: bool, q, k, v, g, beta, scale=None, initial_s
     return o, final_state
 
 
-def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
-    """One decode token for N sequences (C ABI gdn_recurrent_step); updates ``state`` in place, returns o."""
+def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
     lib = load()
     if q.dtype not in DTYPES:
         raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
@@ -224,7 +224,8 @@ def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None,
         _need(t, name, dt, dev)
     N, H, dk = q.shape
     dv = v.shape[-1]
-    if state.shape != (N, H, dk, dv) or k.shape != q.shape or g.shape != (N, H) or beta.shape != (N, H):
+    g_shape = (N, H, dk) if per_channel else (N, H)
+    if state.shape != (N, H, dk, dv) or k.shape != q.shape or g.shape != g_shape or beta.shape != (N, H):
         raise ValueError("decode shapes do not match")
     if o_dtype not in DTYPES:
         raise ValueError(f"o_dtype must be float32 or bfloat16 (got {o_dtype})")
@@ -233,10 +234,21 @@ def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None,
     _need(o, "o", o_dtype, dev)
     if scale is None:
         scale = dk ** -0.5
-    st = lib.gdn_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(o),
-                                N, H, dk, dv, DTYPES[q.dtype], DTYPES[o_dtype], _stream_handle(stream, dev))
+    fn = lib.kda_recurrent_step if per_channel else lib.gdn_recurrent_step
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(o), N, H, dk, dv,
+            DTYPES[q.dtype], DTYPES[o_dtype], _stream_handle(stream, dev))
     _check(st)
     return o
+
+
+def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
+    """One decode token for N sequences (C ABI gdn_recurrent_step); updates ``state`` in place, returns o."""
+    return _step(False, q, k, v, g, beta, state, scale, o, stream, o_dtype)
+
+
+def kda_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
+    """One KDA decode token, g per key channel [N, H, d_k] (C ABI kda_recurrent_step); updates ``state`` in place."""
+    return _step(True, q, k, v, g, beta, state, scale, o, stream, o_dtype)
 
 
 def chunk_plan(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chunk_size: int, dtype,

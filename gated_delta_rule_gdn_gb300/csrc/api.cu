@@ -141,6 +141,32 @@ gdn::ChunkArgs plan_args(int per_channel, int B, int T, int H, int d_k, int d_v,
                           per_channel ? 1 : 0, o_dtype == GDN_F32 ? 1 : 0};
 }
 
+gdn_status step_common(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                       float* state, void* o, int N, int H, int d_k, int d_v, gdn_dtype dtype, gdn_dtype o_dtype,
+                       void* stream, bool per_channel, const char* fn) {
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!dtype_ok(o_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown o_dtype %d", fn, (int)o_dtype);
+    if (N < 1 || H < 1) return fail(GDN_ERR_INVALID_ARG, "%s: need N >= 1, H >= 1 (got N=%d H=%d)", fn, N, H);
+    if (d_k < 1 || d_v < 1 || d_k > 128 || d_v > 128)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..128 (got d_k=%d d_v=%d)", fn, d_k, d_v);
+    if (!q || !k || !v || !g || !beta || !state || !o)
+        return fail(GDN_ERR_INVALID_ARG, "%s: q, k, v, g, beta, state and o must be non-NULL", fn);
+    if (!std::isfinite(scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    const size_t es = dtype == GDN_BF16 ? 2 : 4;
+    const size_t oes = o_dtype == GDN_BF16 ? 2 : 4;
+    if (!aligned(q, es) || !aligned(k, es) || !aligned(v, es) || !aligned(o, oes) || !aligned(g, 4) ||
+        !aligned(beta, 4) || !aligned(state, 4))
+        return fail(GDN_ERR_INVALID_ARG, "%s: a tensor is not aligned to its element size", fn);
+    if ((long)N * H > (1L << 31) / ((long)d_k * d_v))
+        return fail(GDN_ERR_UNSUPPORTED, "%s: state has 2^31 elements or more", fn);
+    gdn::StepArgs a{q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype == GDN_BF16 ? 1 : 0,
+                    o_dtype == GDN_F32 ? 1 : 0, per_channel ? 1 : 0};
+    cudaError_t e = gdn::launch_recurrent_step(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -230,27 +256,15 @@ gdn_status gdn_chunk_fwd_noalloc(int per_channel, const void* q, const void* k, 
 gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               float scale, float* state, void* o, int N, int H, int d_k, int d_v, gdn_dtype dtype,
                               gdn_dtype o_dtype, void* stream) {
-    const char* fn = "gdn_recurrent_step";
-    if (!dtype_ok(dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
-    if (!dtype_ok(o_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown o_dtype %d", fn, (int)o_dtype);
-    if (N < 1 || H < 1) return fail(GDN_ERR_INVALID_ARG, "%s: need N >= 1, H >= 1 (got N=%d H=%d)", fn, N, H);
-    if (d_k < 1 || d_v < 1 || d_k > 128 || d_v > 128)
-        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..128 (got d_k=%d d_v=%d)", fn, d_k, d_v);
-    if (!q || !k || !v || !g || !beta || !state || !o)
-        return fail(GDN_ERR_INVALID_ARG, "%s: q, k, v, g, beta, state and o must be non-NULL", fn);
-    if (!std::isfinite(scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
-    const size_t es = dtype == GDN_BF16 ? 2 : 4;
-    const size_t oes = o_dtype == GDN_BF16 ? 2 : 4;
-    if (!aligned(q, es) || !aligned(k, es) || !aligned(v, es) || !aligned(o, oes) || !aligned(g, 4) ||
-        !aligned(beta, 4) || !aligned(state, 4))
-        return fail(GDN_ERR_INVALID_ARG, "%s: a tensor is not aligned to its element size", fn);
-    if ((long)N * H > (1L << 31) / ((long)d_k * d_v))
-        return fail(GDN_ERR_UNSUPPORTED, "%s: state has 2^31 elements or more", fn);
-    gdn::StepArgs a{q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype == GDN_BF16 ? 1 : 0,
-                    o_dtype == GDN_F32 ? 1 : 0};
-    cudaError_t e = gdn::launch_recurrent_step(a, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, fn);
-    return ok();
+    return step_common(q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype, o_dtype, stream, false,
+                       "gdn_recurrent_step");
+}
+
+gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              float scale, float* state, void* o, int N, int H, int d_k, int d_v, gdn_dtype dtype,
+                              gdn_dtype o_dtype, void* stream) {
+    return step_common(q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype, o_dtype, stream, true,
+                       "kda_recurrent_step");
 }
 
 gdn_status gdn_chunk_plan(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,

@@ -33,7 +33,7 @@ struct StepArgs {
     const void* q;          // [N, H, dk]
     const void* k;          // [N, H, dk]
     const void* v;          // [N, H, dv]
-    const float* g;         // [N, H]
+    const float* g;         // [N, H] or [N, H, dk] (per_channel)
     const float* beta;      // [N, H]
     float scale;
     float* state;           // [N, H, dk, dv] in place
@@ -41,6 +41,7 @@ struct StepArgs {
     int N, H, dk, dv;
     int bf16;               // 1: q, k, v are bf16; 0: fp32
     int o_f32;              // 1: o is fp32; 0: o is bf16
+    int per_channel;        // 1: KDA gate [N, H, dk]
 };
 
 // Generic fp32 SIMT chunk kernel (chunk_generic.cu).

@@ -2,11 +2,12 @@
 //
 // "Gated Delta Network (GDN)", eq. 12 and §4.4: decode runs the recurrent form, one token at a
 // time.  The fused recurrent kernel on "You Could Have Come Up With Kimi Delta Attention" gives
-// the order of the steps: decay, predict, residual, rank-1 write, read.  In the transposed state
-// h = S^T (d_k x d_v), with a = exp(g):
-//     p = h^T k,   z = h^T q,   r = beta (v - a p),
-//     o = scale (a z + r (k . q)),   h <- a h + k r^T.
-// This is the same update: h' = a h + k r^T, and o = scale h'^T q expands to the line above.
+// the order of the steps: decay, predict, residual, rank-1 write, read, with the retention a
+// per-key-channel vector for KDA.  In the transposed state h = S^T (d_k x d_v), with a_c = exp(g_c)
+// (one value for every row c under the scalar gate):
+//     p = h^T (a * k),   z = h^T (a * q),   r = beta (v - p),
+//     o = scale (z + r (k . q)),   h <- diag(a) h + k r^T.
+// This is the same update: h' = diag(a) h + k r^T, and o = scale h'^T q expands to the line above.
 // So one read of h gives both reductions, and one write stores h'.  The step moves
 // 2 * d_k * d_v * 4 bytes of state per (sequence, head), so it is bound by HBM bandwidth.
 //
@@ -37,10 +38,10 @@ template <> __device__ __forceinline__ void st_f32<__nv_bfloat16>(__nv_bfloat16*
 constexpr int kD = 128;
 constexpr int kRowsPerWarp = 16;
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool PERCH>
 __global__ void __launch_bounds__(256, 2)
 step_d128_kernel(const StepArgs a) {
-    __shared__ float ks[kD], qs[kD], vs[kD], rs[kD];
+    __shared__ float ks[kD], qs[kD], vs[kD], rs[kD], as[kD];
     __shared__ float red[2][8][kD];
     __shared__ float kq_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -61,8 +62,8 @@ step_d128_kernel(const StepArgs a) {
         ks[tid] = ld_f32<Tin>(k + tid);
         qs[tid] = ld_f32<Tin>(q + tid);
         vs[tid] = ld_f32<Tin>(v + tid);
+        as[tid] = expf(PERCH ? a.g[nh * kD + tid] : a.g[nh]);
     }
-    const float alpha = expf(a.g[nh]);
     const float beta = a.beta[nh];
     __syncthreads();
     if (warp == 0) {
@@ -74,7 +75,7 @@ step_d128_kernel(const StepArgs a) {
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f), z = p;
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-        const float kr = ks[row0 + r], qr = qs[row0 + r];
+        const float ar = as[row0 + r], kr = ar * ks[row0 + r], qr = ar * qs[row0 + r];
         p.x = fmaf(hr[r].x, kr, p.x); p.y = fmaf(hr[r].y, kr, p.y);
         p.z = fmaf(hr[r].z, kr, p.z); p.w = fmaf(hr[r].w, kr, p.w);
         z.x = fmaf(hr[r].x, qr, z.x); z.y = fmaf(hr[r].y, qr, z.y);
@@ -87,15 +88,15 @@ step_d128_kernel(const StepArgs a) {
         float P = 0.f, Z = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) { P += red[0][w][tid]; Z += red[1][w][tid]; }
-        const float r = beta * (vs[tid] - alpha * P);
+        const float r = beta * (vs[tid] - P);
         rs[tid] = r;
-        st_f32<Tout>(static_cast<Tout*>(a.o) + nh * kD + tid, a.scale * fmaf(alpha, Z, r * kq_s));
+        st_f32<Tout>(static_cast<Tout*>(a.o) + nh * kD + tid, a.scale * fmaf(r, kq_s, Z));
     }
     __syncthreads();
     const float4 r4 = reinterpret_cast<const float4*>(rs)[lane];
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-        const float kr = ks[row0 + r];
+        const float kr = ks[row0 + r], alpha = as[row0 + r];
         float4 x;
         x.x = fmaf(alpha, hr[r].x, kr * r4.x);
         x.y = fmaf(alpha, hr[r].y, kr * r4.y);
@@ -105,12 +106,13 @@ step_d128_kernel(const StepArgs a) {
     }
 }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool PERCH>
 __global__ void __launch_bounds__(128)
 step_generic_kernel(const StepArgs a) {
     extern __shared__ float sh[];
     float* ks = sh;
     float* qs = ks + a.dk;
+    float* as = qs + a.dk;
     __shared__ float kq_s;
     const int tid = threadIdx.x;
     const size_t nh = blockIdx.x;
@@ -119,7 +121,11 @@ step_generic_kernel(const StepArgs a) {
     const Tin* k = static_cast<const Tin*>(a.k) + nh * dk;
     const Tin* v = static_cast<const Tin*>(a.v) + nh * dv;
     float* h = a.state + nh * (size_t)dk * dv;
-    for (int i = tid; i < dk; i += blockDim.x) { ks[i] = ld_f32<Tin>(k + i); qs[i] = ld_f32<Tin>(q + i); }
+    for (int i = tid; i < dk; i += blockDim.x) {
+        ks[i] = ld_f32<Tin>(k + i);
+        qs[i] = ld_f32<Tin>(q + i);
+        as[i] = expf(PERCH ? a.g[nh * dk + i] : a.g[nh]);
+    }
     __syncthreads();
     if (tid == 0) {
         float s = 0.f;
@@ -127,28 +133,33 @@ step_generic_kernel(const StepArgs a) {
         kq_s = s;
     }
     __syncthreads();
-    const float alpha = expf(a.g[nh]);
     const float beta = a.beta[nh];
     for (int j = tid; j < dv; j += blockDim.x) {
         float P = 0.f, Z = 0.f;
         for (int i = 0; i < dk; ++i) {
-            const float x = h[(size_t)i * dv + j];
+            const float x = as[i] * h[(size_t)i * dv + j];
             P = fmaf(x, ks[i], P);
             Z = fmaf(x, qs[i], Z);
         }
-        const float r = beta * (ld_f32<Tin>(v + j) - alpha * P);
-        st_f32<Tout>(static_cast<Tout*>(a.o) + nh * dv + j, a.scale * fmaf(alpha, Z, r * kq_s));
+        const float r = beta * (ld_f32<Tin>(v + j) - P);
+        st_f32<Tout>(static_cast<Tout*>(a.o) + nh * dv + j, a.scale * fmaf(r, kq_s, Z));
         for (int i = 0; i < dk; ++i) {
             float* p = h + (size_t)i * dv + j;
-            *p = fmaf(alpha, *p, ks[i] * r);
+            *p = fmaf(as[i], *p, ks[i] * r);
         }
     }
 }
 
 template <typename Tin, typename Tout>
 void launch_typed(const StepArgs& a, cudaStream_t s, unsigned blocks, bool fast) {
-    if (fast) step_d128_kernel<Tin, Tout><<<blocks, 256, 0, s>>>(a);
-    else step_generic_kernel<Tin, Tout><<<blocks, 128, 2 * (size_t)a.dk * sizeof(float), s>>>(a);
+    const size_t sh = 3 * (size_t)a.dk * sizeof(float);
+    if (a.per_channel) {
+        if (fast) step_d128_kernel<Tin, Tout, true><<<blocks, 256, 0, s>>>(a);
+        else step_generic_kernel<Tin, Tout, true><<<blocks, 128, sh, s>>>(a);
+    } else {
+        if (fast) step_d128_kernel<Tin, Tout, false><<<blocks, 256, 0, s>>>(a);
+        else step_generic_kernel<Tin, Tout, false><<<blocks, 128, sh, s>>>(a);
+    }
 }
 
 }  // namespace

@@ -77,6 +77,7 @@ class DecodeWorkload:
     steps: int
     dtype: str = "bf16"
     h0_std: float = 0.02
+    kind: str = "gdn"         # "gdn" (scalar gate per head) or "kda" (per-key-channel gate)
 
     @property
     def scale(self) -> float:
@@ -204,7 +205,9 @@ def decode_step_inputs(w: DecodeWorkload, consts: dict, step: int, seed: int = 0
     """Inputs of decode step ``step``, drawn from ``default_rng([seed, 1000 + step])``.
 
     Draw order: q, k, v, beta logits, gate logits.  Shapes are [N, H, d] for
-    q, k and v and [N, H] for g and beta.  ``n`` overrides N and keeps the
+    q, k and v, [N, H] for beta, and [N, H] for g (the GDN gate) or
+    [N, H, d_k] (the KDA gate, drawn as in the KDA chunk recipe:
+    -exp(N(0, 0.5)) softplus(N(0, 1))).  ``n`` overrides N and keeps the
     leading rows of each draw.
     """
     N = w.N if n is None else n
@@ -213,8 +216,13 @@ def decode_step_inputs(w: DecodeWorkload, consts: dict, step: int, seed: int = 0
     k = _unit_rows(rng.standard_normal((w.N, w.H, w.dk), dtype=np.float32))[:N]
     v = rng.standard_normal((w.N, w.H, w.dv), dtype=np.float32)[:N]
     beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((w.N, w.H), dtype=np.float32).astype(np.float64)))[:N]
-    logits = rng.standard_normal((w.N, w.H), dtype=np.float32).astype(np.float64)[:N]
-    g = -consts["A"] * _softplus(logits + consts["dt_bias"])
+    if w.kind == "kda":
+        a = rng.standard_normal((w.N, w.H, w.dk), dtype=np.float32).astype(np.float64)[:N] * 0.5
+        sp = rng.standard_normal((w.N, w.H, w.dk), dtype=np.float32).astype(np.float64)[:N]
+        g = -np.exp(a) * _softplus(sp)
+    else:
+        logits = rng.standard_normal((w.N, w.H), dtype=np.float32).astype(np.float64)[:N]
+        g = -consts["A"] * _softplus(logits + consts["dt_bias"])
     dt = _torch_dtype(w.dtype)
     return {
         "q": torch.from_numpy(np.ascontiguousarray(q)).to(dt),

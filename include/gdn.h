@@ -225,6 +225,21 @@ gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const
                               gdn_dtype dtype, gdn_dtype o_dtype, void* stream);
 
 /*
+ * kda_recurrent_step -- one decode token of Kimi Delta Attention for N
+ * independent sequences: the retention is the per-key-channel vector exp(g),
+ * applied as Diag(exp g) on the key side of the state before the delta update.
+ *
+ * Source: "You Could Have Come Up With Kimi Delta Attention", the fused
+ * recurrent form (decay per channel, predict, residual, rank-1 write, read).
+ *
+ * Arguments and layouts are those of gdn_recurrent_step, except that g is
+ * [N, H, d_k] fp32.  With g equal on every channel the result is the GDN step.
+ */
+gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              float scale, float* state, void* o, int N, int H, int d_k, int d_v,
+                              gdn_dtype dtype, gdn_dtype o_dtype, void* stream);
+
+/*
  * gdn_chunk_plan -- which kernel a chunk-forward call with these sizes would run.
  * The buffers are assumed to be 16-byte aligned.  per_channel nonzero stands
  * for kda_chunk_fwd; varlen nonzero stands for a call with cu_seqlens.

@@ -47,14 +47,16 @@ def _decode_and_compare(w: W.DecodeWorkload, steps: int, sample=None):
             for key in kept:
                 kept[key].append(x[key].reshape(NH, -1)[tidx].clone())
             d = {key: t.cuda() for key, t in x.items()}
-            o = gdn.gdn_recurrent_step(d["q"], d["k"], d["v"], d["g"], d["beta"], state, scale=w.scale)
+            step = gdn.kda_recurrent_step if w.kind == "kda" else gdn.gdn_recurrent_step
+            o = step(d["q"], d["k"], d["v"], d["g"], d["beta"], state, scale=w.scale)
             outs.append(o.reshape(NH, w.dv)[tidx.cuda()].float().cpu())
     torch.cuda.synchronize()
     assert gdn.device_status() == 0
     # oracle: the sampled chains as independent sequences of T = steps tokens
     q, k, v = (torch.stack(kept[key], dim=1)[:, :, None] for key in ("q", "k", "v"))
-    g, beta = (torch.stack(kept[key], dim=1)[:, :, :1] for key in ("g", "beta"))
-    o_ref, h_ref = oracle.recurrence(q, k, v, g, beta, w.scale, h0s)
+    beta = torch.stack(kept["beta"], dim=1)[:, :, :1]
+    g = torch.stack(kept["g"], dim=1)[:, :, None] if w.kind == "kda" else torch.stack(kept["g"], dim=1)[:, :, :1]
+    o_ref, h_ref = oracle.recurrence(q, k, v, g, beta, w.scale, h0s, gate_per_channel=w.kind == "kda")
     o_gpu = torch.stack(outs, dim=1).double().numpy()
     dtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     for s in range(steps):
@@ -67,6 +69,28 @@ def _decode_and_compare(w: W.DecodeWorkload, steps: int, sample=None):
                                              (2, 2, 64, 100, "bf16")])
 def test_small_decode(N, H, dk, dv, dtype):
     _decode_and_compare(W.DecodeWorkload("t", N, H, dk, dv, 40, dtype=dtype), 40)
+
+
+@pytest.mark.parametrize("N,H,dk,dv,dtype", [(3, 2, 16, 8, "f32"), (4, 2, 128, 128, "f32"), (5, 3, 128, 128, "bf16"),
+                                             (2, 2, 64, 100, "bf16")])
+def test_small_kda_decode(N, H, dk, dv, dtype):
+    _decode_and_compare(W.DecodeWorkload("t", N, H, dk, dv, 40, dtype=dtype, kind="kda"), 40)
+
+
+def test_kda_decode_with_equal_channels_is_the_gdn_decode():
+    w = W.DecodeWorkload("t", 6, 3, 128, 128, 1)
+    c = W.decode_constants(w, seed=2)
+    x = {k: v.cuda() for k, v in W.decode_step_inputs(w, c, 0).items()}
+    s1, s2 = c["state"].cuda(), c["state"].cuda()
+    o1 = gdn.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], s1, scale=w.scale)
+    gk = x["g"][..., None].expand(6, 3, 128).contiguous()
+    o2 = gdn.kda_recurrent_step(x["q"], x["k"], x["v"], gk, x["beta"], s2, scale=w.scale)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+def test_full_kda_decode_sampled_chains():
+    w = W.DecodeWorkload("kda_decode", 256, 32, 128, 128, 64, kind="kda")
+    _decode_and_compare(w, 64, sample=np.arange(0, 256 * 32, 97))
 
 
 def test_bf16_output_is_the_rounded_fp32_output():
