@@ -23,6 +23,11 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "two_pass": 3}
 
 
+class GateAct(ctypes.Structure):
+    """C struct gdn_gate_act: the in-kernel gate / beta activation."""
+    _fields_ = [("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("beta_sigmoid", ctypes.c_int)]
+
+
 class GdnError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
@@ -41,6 +46,11 @@ def _declare(lib):
     for name in ("gdn_chunk_fwd_ws", "kda_chunk_fwd_ws"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i, chunk + [i, vp, ctypes.c_size_t, vp]
+    lib.gdn_chunk_fwd_act.restype = i
+    lib.gdn_chunk_fwd_act.argtypes = chunk + [ctypes.POINTER(GateAct), i, vp, ctypes.c_size_t, vp]
+    lib.gdn_recurrent_step_act.restype = i
+    lib.gdn_recurrent_step_act.argtypes = [vp, vp, vp, vp, vp, fp, vp, vp, i, i, i, i, i, i,
+                                           ctypes.POINTER(GateAct), vp]
     lib.gdn_chunk_fwd_noalloc.restype = i
     lib.gdn_chunk_fwd_noalloc.argtypes = [i] + chunk + [vp]
     lib.gdn_chunk_workspace_size.restype = i
@@ -115,9 +125,22 @@ def workspace_size(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, 
     return int(out.value)
 
 
+def _gate_act(dev, H, A_log, dt_bias, beta_sigmoid):
+    """The activation descriptor (or None) after checking its tensors."""
+    if A_log is None and dt_bias is None and not beta_sigmoid:
+        return None
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
+        if t is not None:
+            _need(t, name, torch.float32, dev)
+            if t.shape != (H,):
+                raise ValueError(f"{name} must have shape ({H},)")
+    return GateAct(None if A_log is None else A_log.data_ptr(), None if dt_bias is None else dt_bias.data_ptr(),
+                   int(bool(beta_sigmoid)))
+
+
 def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
            cu_seqlens=None, chunk_size=64, algo="auto", o=None, final_state=None, stream=None,
-           o_dtype=torch.float32, workspace=None):
+           o_dtype=torch.float32, workspace=None, A_log=None, dt_bias=None, beta_sigmoid=False):
     lib = load()
     if q.dtype not in DTYPES:
         raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
@@ -158,25 +181,35 @@ def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, 
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if workspace is not None:
         _need(workspace, "workspace", torch.uint8, dev)
-    fn = lib.kda_chunk_fwd_ws if per_channel else lib.gdn_chunk_fwd_ws
-    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(initial_state),
+    act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(initial_state),
             int(final_state is not None), _ptr(final_state), _ptr(cu_seqlens), n_seqs, _ptr(o),
-            B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[o_dtype], ALGOS[algo],
-            _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream_handle(stream, dev))
+            B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[o_dtype])
+    tail = (ALGOS[algo], _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream_handle(stream, dev))
+    if act is not None:
+        if per_channel:
+            raise ValueError("the gate activation applies to the scalar gate only")
+        st = lib.gdn_chunk_fwd_act(*args, ctypes.byref(act), *tail)
+    else:
+        fn = lib.kda_chunk_fwd_ws if per_channel else lib.gdn_chunk_fwd_ws
+        st = fn(*args, *tail)
     _check(st)
     return o, final_state
 
 
 def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False, cu_seqlens=None,
                   chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32,
-                  workspace=None):
-    """Chunkwise gated delta rule forward (C ABI gdn_chunk_fwd_ws).  Returns (o, final_state or None).
+                  workspace=None, A_log=None, dt_bias=None, beta_sigmoid=False):
+    """Chunkwise gated delta rule forward (C ABI gdn_chunk_fwd_ws, or gdn_chunk_fwd_act with an activation).
+    Returns (o, final_state or None).
 
     o is fp32 unless o_dtype=torch.bfloat16 (then it is the round-to-nearest-even of the fp32 result).
     ``workspace`` (uint8 device tensor, see workspace_size) is allocated here when the kernel needs one.
+    ``A_log``/``dt_bias`` ([H] fp32): g holds raw logits and the kernel applies -exp(A_log) softplus(g + dt_bias);
+    ``beta_sigmoid``: beta holds logits.
     """
     return _chunk(False, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens, chunk_size, algo,
-                  o, final_state, stream, o_dtype, workspace)
+                  o, final_state, stream, o_dtype, workspace, A_log, dt_bias, beta_sigmoid)
 
 
 def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False, cu_seqlens=None,
@@ -214,7 +247,8 @@ def chunk_fwd_noalloc(per_channel: bool, q, k, v, g, beta, scale=None, initial_s
     return o, final_state
 
 
-def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
+def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32,
+          A_log=None, dt_bias=None, beta_sigmoid=False):
     lib = load()
     if q.dtype not in DTYPES:
         raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
@@ -234,16 +268,25 @@ def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream
     _need(o, "o", o_dtype, dev)
     if scale is None:
         scale = dk ** -0.5
-    fn = lib.kda_recurrent_step if per_channel else lib.gdn_recurrent_step
-    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(o), N, H, dk, dv,
-            DTYPES[q.dtype], DTYPES[o_dtype], _stream_handle(stream, dev))
+    act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(o), N, H, dk, dv,
+            DTYPES[q.dtype], DTYPES[o_dtype])
+    if act is not None:
+        if per_channel:
+            raise ValueError("the gate activation applies to the scalar gate only")
+        st = lib.gdn_recurrent_step_act(*args, ctypes.byref(act), _stream_handle(stream, dev))
+    else:
+        fn = lib.kda_recurrent_step if per_channel else lib.gdn_recurrent_step
+        st = fn(*args, _stream_handle(stream, dev))
     _check(st)
     return o
 
 
-def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
-    """One decode token for N sequences (C ABI gdn_recurrent_step); updates ``state`` in place, returns o."""
-    return _step(False, q, k, v, g, beta, state, scale, o, stream, o_dtype)
+def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32,
+                       A_log=None, dt_bias=None, beta_sigmoid=False):
+    """One decode token for N sequences (C ABI gdn_recurrent_step, or gdn_recurrent_step_act with an activation);
+    updates ``state`` in place, returns o."""
+    return _step(False, q, k, v, g, beta, state, scale, o, stream, o_dtype, A_log, dt_bias, beta_sigmoid)
 
 
 def kda_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):

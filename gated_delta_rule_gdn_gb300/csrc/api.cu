@@ -89,19 +89,37 @@ gdn_status resolve_algo(const gdn::ChunkArgs& a, gdn_algo algo, const char* fn, 
     return GDN_OK;
 }
 
+// Validate an optional activation descriptor and copy it into the kernel arguments.
+gdn_status set_act(gdn::GateAct& dst, const gdn_gate_act* act, const char* fn) {
+    dst = gdn::GateAct{nullptr, nullptr, 0};
+    if (!act) return GDN_OK;
+    if (act->dt_bias && !act->A_log)
+        return fail(GDN_ERR_INVALID_ARG, "%s: dt_bias is given without A_log", fn);
+    if ((act->A_log && !aligned(act->A_log, 4)) || (act->dt_bias && !aligned(act->dt_bias, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "%s: A_log or dt_bias is not 4-byte aligned", fn);
+    dst = gdn::GateAct{act->A_log, act->dt_bias, act->beta_sigmoid ? 1 : 0};
+    return GDN_OK;
+}
+
 gdn_status chunk_common(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
                         const float* initial_state, int output_final_state, float* final_state,
                         const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
                         int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, gdn_algo algo, void* workspace,
-                        size_t workspace_bytes, void* stream, bool per_channel, const char* fn) {
+                        size_t workspace_bytes, void* stream, bool per_channel, const char* fn,
+                        const gdn_gate_act* act = nullptr) {
     gdn::ChunkArgs a{q, k, v, g, beta, scale, initial_state, final_state, cu_seqlens, n_seqs, o,
                      B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0,
                      o_dtype == GDN_F32 ? 1 : 0};
     gdn_status st = check_chunk(a, dtype, o_dtype, output_final_state, fn);
     if (st != GDN_OK) return st;
+    st = set_act(a.act, act, fn);
+    if (st != GDN_OK) return st;
     gdn_algo chosen = GDN_ALGO_GENERIC;
     st = resolve_algo(a, algo, fn, &chosen);
     if (st != GDN_OK) return st;
+    if (a.act.any() && chosen != GDN_ALGO_TWO_PASS)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the gate activation runs on the two-pass path only (bf16, d = 128, "
+                    "chunk 64, scalar gate)", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (chosen == GDN_ALGO_TWO_PASS) {
@@ -143,7 +161,7 @@ gdn::ChunkArgs plan_args(int per_channel, int B, int T, int H, int d_k, int d_v,
 
 gdn_status step_common(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
                        float* state, void* o, int N, int H, int d_k, int d_v, gdn_dtype dtype, gdn_dtype o_dtype,
-                       void* stream, bool per_channel, const char* fn) {
+                       void* stream, bool per_channel, const char* fn, const gdn_gate_act* act = nullptr) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
     if (!dtype_ok(o_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown o_dtype %d", fn, (int)o_dtype);
     if (N < 1 || H < 1) return fail(GDN_ERR_INVALID_ARG, "%s: need N >= 1, H >= 1 (got N=%d H=%d)", fn, N, H);
@@ -161,6 +179,10 @@ gdn_status step_common(const void* q, const void* k, const void* v, const float*
         return fail(GDN_ERR_UNSUPPORTED, "%s: state has 2^31 elements or more", fn);
     gdn::StepArgs a{q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype == GDN_BF16 ? 1 : 0,
                     o_dtype == GDN_F32 ? 1 : 0, per_channel ? 1 : 0};
+    gdn_status st = set_act(a.act, act, fn);
+    if (st != GDN_OK) return st;
+    if (per_channel && a.act.any())
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the gate activation applies to the scalar gate only", fn);
     cudaError_t e = gdn::launch_recurrent_step(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return ok();
@@ -258,6 +280,23 @@ gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const
                               gdn_dtype o_dtype, void* stream) {
     return step_common(q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype, o_dtype, stream, false,
                        "gdn_recurrent_step");
+}
+
+gdn_status gdn_chunk_fwd_act(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                             float scale, const float* initial_state, int output_final_state, float* final_state,
+                             const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
+                             int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, const gdn_gate_act* act,
+                             gdn_algo algo, void* workspace, size_t workspace_bytes, void* stream) {
+    return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
+                        o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, workspace, workspace_bytes, stream,
+                        false, "gdn_chunk_fwd_act", act);
+}
+
+gdn_status gdn_recurrent_step_act(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                  float scale, float* state, void* o, int N, int H, int d_k, int d_v,
+                                  gdn_dtype dtype, gdn_dtype o_dtype, const gdn_gate_act* act, void* stream) {
+    return step_common(q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype, o_dtype, stream, false,
+                       "gdn_recurrent_step_act", act);
 }
 
 gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,

@@ -36,6 +36,7 @@
 #include "internal.h"
 #include "tc_common.cuh"
 #include "chunk_common.cuh"
+#include "gate_act.cuh"
 
 namespace gdn {
 
@@ -107,6 +108,7 @@ struct IntraParams {
     float scale;
     long n_slots;
     Ws ws;
+    GateAct act;   // scalar gate only
 };
 
 struct Item {
@@ -329,8 +331,8 @@ __device__ __forceinline__ void intra_load_gb(const IntraParams& p, const Item& 
     for (int k = 0; k < 2; ++k) {
         const int r = lane + 32 * k;
         const size_t tok = (size_t)(x.row + r) * p.geo.H + x.h;
-        g[k] = (!KDA && r < x.L) ? __ldg(p.g + tok) : 0.f;
-        b[k] = r < x.L ? __ldg(p.beta + tok) : 0.f;
+        g[k] = (!KDA && r < x.L) ? act_gate(p.act, __ldg(p.g + tok), x.h) : 0.f;
+        b[k] = r < x.L ? act_beta(p.act, __ldg(p.beta + tok)) : 0.f;
     }
 }
 
@@ -1277,6 +1279,7 @@ long n_slots(const ChunkArgs& a) { return (long)a.B * a.T / C + a.N() + 1; }
 }  // namespace
 
 const char* two_pass_unsupported_reason(const ChunkArgs& a) {
+    if (a.per_channel && a.act.any()) return "the gate activation applies to the scalar gate only";
     if (!a.bf16) return "q, k, v must be bf16";
     if (a.dk != DK || a.dv != DV) return "d_k and d_v must be 128";
     if (a.C != C) return "chunk_size must be 64";
@@ -1325,7 +1328,7 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    IntraParams ip{geo, a.g, a.beta, a.scale, n_slots(a), ws};
+    IntraParams ip{geo, a.g, a.beta, a.scale, n_slots(a), ws, a.act};
     if (a.per_channel) {
         CUtensorMap mg;
         if (!make_map_f32_rows(&mg, a.g, rows, a.H, DK)) return cudaErrorInvalidValue;

@@ -9,6 +9,15 @@
 
 namespace gdn {
 
+// Optional in-kernel activation of the scalar gate and of beta (all null / zero: the inputs are already log alpha
+// and beta).
+struct GateAct {
+    const float* A_log;     // [H] or nullptr: g holds log alpha itself
+    const float* dt_bias;   // [H] or nullptr (zero)
+    int beta_sigmoid;       // 1: beta holds logits
+    bool any() const { return A_log != nullptr || beta_sigmoid != 0; }
+};
+
 // One chunk-forward request, already validated by api.cu.
 struct ChunkArgs {
     const void* q;          // [B, T, H, dk]
@@ -26,6 +35,7 @@ struct ChunkArgs {
     int bf16;               // 1: q, k, v are bf16; 0: fp32
     int per_channel;        // 1: KDA gate [.., dk]
     int o_f32;              // 1: o is fp32; 0: o is bf16
+    GateAct act;            // gate / beta activation (two-pass path, scalar gate only)
     int N() const { return cu ? n_seqs : B; }
 };
 
@@ -42,6 +52,7 @@ struct StepArgs {
     int bf16;               // 1: q, k, v are bf16; 0: fp32
     int o_f32;              // 1: o is fp32; 0: o is bf16
     int per_channel;        // 1: KDA gate [N, H, dk]
+    GateAct act;            // gate / beta activation (scalar gate only)
 };
 
 // Generic fp32 SIMT chunk kernel (chunk_generic.cu).

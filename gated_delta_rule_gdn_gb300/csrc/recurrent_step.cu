@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "gate_act.cuh"
 
 namespace gdn {
 namespace {
@@ -62,9 +63,9 @@ step_d128_kernel(const StepArgs a) {
         ks[tid] = ld_f32<Tin>(k + tid);
         qs[tid] = ld_f32<Tin>(q + tid);
         vs[tid] = ld_f32<Tin>(v + tid);
-        as[tid] = expf(PERCH ? a.g[nh * kD + tid] : a.g[nh]);
+        as[tid] = expf(PERCH ? a.g[nh * kD + tid] : act_gate(a.act, a.g[nh], (int)(nh % a.H)));
     }
-    const float beta = a.beta[nh];
+    const float beta = act_beta(a.act, a.beta[nh]);
     __syncthreads();
     if (warp == 0) {
         float s = 0.f;
@@ -124,7 +125,7 @@ step_generic_kernel(const StepArgs a) {
     for (int i = tid; i < dk; i += blockDim.x) {
         ks[i] = ld_f32<Tin>(k + i);
         qs[i] = ld_f32<Tin>(q + i);
-        as[i] = expf(PERCH ? a.g[nh * dk + i] : a.g[nh]);
+        as[i] = expf(PERCH ? a.g[nh * dk + i] : act_gate(a.act, a.g[nh], (int)(nh % a.H)));
     }
     __syncthreads();
     if (tid == 0) {
@@ -133,7 +134,7 @@ step_generic_kernel(const StepArgs a) {
         kq_s = s;
     }
     __syncthreads();
-    const float beta = a.beta[nh];
+    const float beta = act_beta(a.act, a.beta[nh]);
     for (int j = tid; j < dv; j += blockDim.x) {
         float P = 0.f, Z = 0.f;
         for (int i = 0; i < dk; ++i) {

@@ -147,6 +147,34 @@ gdn_status gdn_chunk_fwd_ws(const void* q, const void* k, const void* v, const f
                             void* stream);
 
 /*
+ * Optional in-kernel activation of the scalar gate and of beta ("Gated Delta
+ * Network (GDN)", §3.1 eq. 5 gives the parameterisation; §4 and §6 describe
+ * fusing it into the kernel so no separate activation pass runs):
+ *   A_log         [H] fp32 device, or NULL: g already holds log alpha.  When set,
+ *                 g holds raw logits x and the kernel uses
+ *                 log alpha = -exp(A_log[h]) * softplus(x + dt_bias[h]).
+ *   dt_bias       [H] fp32 device, or NULL (zero); needs A_log.
+ *   beta_sigmoid  nonzero: beta holds logits and the kernel uses sigmoid(beta).
+ */
+typedef struct gdn_gate_act {
+    const float* A_log;
+    const float* dt_bias;
+    int beta_sigmoid;
+} gdn_gate_act;
+
+/*
+ * gdn_chunk_fwd_act -- gdn_chunk_fwd_ws with the gate / beta activation in the
+ * kernel (act may be NULL: no activation).  The activation runs on the
+ * two-pass path only; another kernel choice returns GDN_ERR_UNSUPPORTED.
+ */
+gdn_status gdn_chunk_fwd_act(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                             float scale, const float* initial_state, int output_final_state,
+                             float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o,
+                             int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                             gdn_dtype o_dtype, const gdn_gate_act* act, gdn_algo algo, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
  * kda_chunk_fwd -- chunkwise forward of Kimi Delta Attention.  The retention
  * is a per-key-channel vector exp(g_t), applied as Diag(exp g_t) on the key
  * side of the state before the delta update.
@@ -223,6 +251,11 @@ gdn_status gdn_chunk_fwd_noalloc(int per_channel, const void* q, const void* k, 
 gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               float scale, float* state, void* o, int N, int H, int d_k, int d_v,
                               gdn_dtype dtype, gdn_dtype o_dtype, void* stream);
+
+/* gdn_recurrent_step with the gate / beta activation of gdn_gate_act in the kernel (act may be NULL). */
+gdn_status gdn_recurrent_step_act(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                  float scale, float* state, void* o, int N, int H, int d_k, int d_v,
+                                  gdn_dtype dtype, gdn_dtype o_dtype, const gdn_gate_act* act, void* stream);
 
 /*
  * kda_recurrent_step -- one decode token of Kimi Delta Attention for N

@@ -123,3 +123,17 @@ def test_workspace_argument_checks(lib):
     assert "workspace" in _binding.last_error()
     assert _chunk_ws(lib, FAKE + 16, need) == 1            # not 256-byte aligned
     assert _chunk_ws(lib, FAKE, need, dk=64, dv=64) == 2   # the two-pass kernels need d = 128
+
+
+def test_gate_activation_argument_checks(lib):
+    act = _binding.GateAct(FAKE, None, 1)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, None, 0, None, None, 0, FAKE, 1, 64, 1, 128, 128, 64, 1, 0]
+    # the fp32 inputs below resolve to the generic kernel, which has no activation: refused before any launch
+    a32 = list(args)
+    a32[18] = 0
+    assert lib.gdn_chunk_fwd_act(*a32, ctypes.byref(act), 0, None, 0, None) == 2
+    assert "two-pass" in _binding.last_error()
+    bad = _binding.GateAct(None, FAKE, 0)        # dt_bias without A_log
+    assert lib.gdn_chunk_fwd_act(*args, ctypes.byref(bad), 0, None, 0, None) == 1
+    odd = _binding.GateAct(FAKE + 2, None, 0)    # misaligned A_log
+    assert lib.gdn_chunk_fwd_act(*args, ctypes.byref(odd), 0, None, 0, None) == 1

@@ -292,3 +292,34 @@ def test_full_config3_kda_sampled_heads():
     o, hT = _run(x, "auto")
     assert_close(o[:, :, heads], o_ref, torch.bfloat16, "o")
     assert_close(hT[:, heads], h_ref, torch.bfloat16, "final state")
+
+
+def _raw_gates(x, seed):
+    """Raw gate and beta logits plus A_log, dt_bias per head, and the fp64 activation the oracle takes
+    (log alpha = -exp(A_log) softplus(x + dt_bias), beta = sigmoid(b))."""
+    rng = np.random.default_rng(seed)
+    H = x["q"].shape[2]
+    gl = rng.standard_normal(tuple(x["g"].shape), dtype=np.float32)
+    bl = rng.standard_normal(tuple(x["beta"].shape), dtype=np.float32)
+    A_log = np.log(rng.uniform(0.5, 16.0, size=H)).astype(np.float32)
+    dt_bias = rng.normal(0.0, 0.1, size=H).astype(np.float32)
+    g64 = -np.exp(A_log.astype(np.float64)) * np.logaddexp(0.0, gl.astype(np.float64) + dt_bias.astype(np.float64))
+    b64 = 1.0 / (1.0 + np.exp(-bl.astype(np.float64)))
+    return gl, bl, A_log, dt_bias, g64, b64
+
+
+def test_in_kernel_gate_and_beta_activation():
+    x = W.chunk_inputs(W.config(1), seed=9, B=2, T=333, H=3)
+    gl, bl, A_log, dt_bias, g64, b64 = _raw_gates(x, 9)
+    xr = dict(x)
+    xr["g"], xr["beta"] = torch.from_numpy(g64), torch.from_numpy(b64)   # the oracle sees the fp64 activation
+    o_ref, h_ref = oracle_on_heads(xr)
+    d = to_dev(x)
+    o, hT = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], torch.from_numpy(gl).cuda(), torch.from_numpy(bl).cuda(),
+                              scale=x["scale"], initial_state=d["initial_state"], output_final_state=True,
+                              A_log=torch.from_numpy(A_log).cuda(), dt_bias=torch.from_numpy(dt_bias).cuda(),
+                              beta_sigmoid=True)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    assert_close(o.double().cpu().numpy(), o_ref, torch.bfloat16, "o")
+    assert_close(hT.double().cpu().numpy(), h_ref, torch.bfloat16, "final state")

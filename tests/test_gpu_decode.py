@@ -109,3 +109,36 @@ def test_full_decode_1024_steps_sampled_chains():
     rng = np.random.default_rng(0)
     sample = np.sort(rng.choice(w.N * w.H, size=64, replace=False))
     _decode_and_compare(w, w.steps, sample=list(sample))
+
+
+def test_decode_with_in_kernel_gate_and_beta_activation():
+    w = W.DecodeWorkload("t", 8, 4, 128, 128, 24)
+    consts = W.decode_constants(w, seed=3)
+    rng = np.random.default_rng(3)
+    A_log = np.log(rng.uniform(0.5, 16.0, size=w.H)).astype(np.float32)
+    dt_bias = rng.normal(0.0, 0.1, size=w.H).astype(np.float32)
+    state = consts["state"].cuda()
+    NH = w.N * w.H
+    qs, ks, vs, gs, bs, outs = [], [], [], [], [], []
+    for s in range(w.steps):
+        x = W.decode_step_inputs(w, consts, s)
+        gl = rng.standard_normal((w.N, w.H), dtype=np.float32)
+        bl = rng.standard_normal((w.N, w.H), dtype=np.float32)
+        d = {k: v.cuda() for k, v in x.items()}
+        o = gdn.gdn_recurrent_step(d["q"], d["k"], d["v"], torch.from_numpy(gl).cuda(), torch.from_numpy(bl).cuda(),
+                                   state, scale=w.scale, A_log=torch.from_numpy(A_log).cuda(),
+                                   dt_bias=torch.from_numpy(dt_bias).cuda(), beta_sigmoid=True)
+        outs.append(o.reshape(NH, -1).float().cpu())
+        qs.append(x["q"].reshape(NH, -1)); ks.append(x["k"].reshape(NH, -1)); vs.append(x["v"].reshape(NH, -1))
+        gs.append(torch.from_numpy(-np.exp(A_log.astype(np.float64))[None, :]
+                                   * np.logaddexp(0.0, gl.astype(np.float64) + dt_bias[None, :])).reshape(NH, 1))
+        bs.append(torch.from_numpy(1.0 / (1.0 + np.exp(-bl.astype(np.float64)))).reshape(NH, 1))
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    q, k, v = (torch.stack(t, dim=1)[:, :, None] for t in (qs, ks, vs))
+    g, beta = torch.stack(gs, dim=1), torch.stack(bs, dim=1)
+    o_ref, h_ref = oracle.recurrence(q, k, v, g, beta, w.scale, consts["state"].reshape(NH, 1, 128, 128))
+    o_gpu = torch.stack(outs, dim=1).double().numpy()
+    for s in range(w.steps):
+        assert_close(o_gpu[:, s], o_ref[:, s, 0], torch.bfloat16, f"o at step {s}")
+    assert_close(state.reshape(NH, 128, 128).double().cpu().numpy(), h_ref[:, 0], torch.bfloat16, "state")
