@@ -187,9 +187,11 @@ struct ISmall {
 // KDA: per-channel vectors of the gate (log2 units; R_a = cumulative gate at the end of 16-row block a - 1)
 struct KSmall {
     float er[4][128];         // 2^R_a
-    float esp[4][128];        // 2^(R_{a+1} - R_a), R_4 = the chunk total
-    float elp[4][128];        // 2^(G_last - R_{a+1})
+    float espl[4][128];       // 2^(G_last - R_a)
+    float dab[6][128];        // 2^(R_a - R_b) for b < a, pair a (a - 1) / 2 + b
     float lg63[128];          // G_last
+    float p47[128], p63[128]; // the second half's partial sums at rows 47 and 63 (exchange between the halves)
+    float tot1[128];          // the first half's total (row 31)
     int fast;                 // every block's spread is small enough for the factored products
 };
 constexpr uint32_t I_SMALL_GDN = I_END;
@@ -383,43 +385,55 @@ __device__ __forceinline__ float ld_bf16_sw(const uint8_t* base, int r, int c) {
 // Also writes gamma_C.
 __device__ void kda_gate_tables(uint8_t* smem, KSmall& K, int L, float* gc_out, int tid) {
     const float LOG2E = 1.4426950408889634f;
+    // thread (half, c): channel c, rows 32 half .. 32 half + 31; the second half's sums start at row 32
+    const int c = tid & 127, half = tid >> 7, i0 = 32 * half;
+    const float* gt = reinterpret_cast<const float*>(smem + I_B2);
+    float* E = reinterpret_cast<float*>(smem + I_EF);
+    float* F = reinterpret_cast<float*>(smem + I_FF);
     bool fine = true;
-    float lg[64];
-    if (tid < 128) {
-        const float* gt = reinterpret_cast<const float*>(smem + I_B2);
-        float acc = 0.f;
+    float part[32];
+    float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            const float gi = i < L ? gt[i * 128 + tid] : 0.f;
-            fine = fine && gi <= 0.f;   // retention <= 1: every factor below stays <= 1 or <= the block spread
-            acc += gi;
-            lg[i] = acc * LOG2E;
-        }
+    for (int i = 0; i < 32; ++i) {
+        const float gi = i0 + i < L ? gt[(i0 + i) * 128 + c] : 0.f;
+        fine = fine && gi <= 0.f;   // retention <= 1: every factor below stays <= 1 or <= the block spread
+        acc += gi;
+        part[i] = acc * LOG2E;
+    }
+    // block references relative to this half's start: R_{2 half} = 0, R_{2 half + 1} = part[15]
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const float R = a == 0 ? 0.f : lg[16 * a - 1];
-            fine = fine && R - lg[16 * a + 15] <= KDA_SPREAD_MAX;
+    for (int bb = 0; bb < 2; ++bb) {
+        const float R = bb == 0 ? 0.f : part[15];
+        fine = fine && R - part[16 * bb + 15] <= KDA_SPREAD_MAX;
+#pragma unroll
+        for (int i = 16 * bb; i < 16 * bb + 16; ++i) {
+            E[(i0 + i) * ES + c] = ex2(part[i] - R);
+            F[(i0 + i) * ES + c] = ex2(R - part[i]);
         }
     }
+    if (half == 0) K.tot1[c] = part[31];
+    else {
+        K.p47[c] = part[15];
+        K.p63[c] = part[31];
+    }
     const bool fast = __syncthreads_and(fine) != 0;
-    if (tid < 128) {
-        const int c = tid;
-        float* E = reinterpret_cast<float*>(smem + I_EF);
-        float* F = reinterpret_cast<float*>(smem + I_FF);
+    const float t1 = K.tot1[c];
+    if (!fast) {   // the exact path keeps the absolute cumulative gate (log2) in F
+#pragma unroll
+        for (int i = 0; i < 32; ++i) F[(i0 + i) * ES + c] = part[i] + (half ? t1 : 0.f);
+    }
+    if (half == 0) {
+        const float R[4] = {0.f, part[15], t1, t1 + K.p47[c]};
+        const float Gl = t1 + K.p63[c];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const float R = a == 0 ? 0.f : lg[16 * a - 1], R1 = lg[16 * a + 15];
-            K.er[a][c] = ex2(R);
-            K.esp[a][c] = ex2(R1 - R);
-            K.elp[a][c] = ex2(lg[63] - R1);
+            K.er[a][c] = ex2(R[a]);
+            K.espl[a][c] = ex2(Gl - R[a]);
 #pragma unroll
-            for (int i = 16 * a; i < 16 * a + 16; ++i) {
-                E[i * ES + c] = fast ? ex2(lg[i] - R) : 0.f;
-                F[i * ES + c] = fast ? ex2(R - lg[i]) : lg[i];
-            }
+            for (int b = 0; b < a; ++b) K.dab[a * (a - 1) / 2 + b][c] = ex2(R[a] - R[b]);
         }
-        K.lg63[c] = lg[63];
-        __stcg(gc_out + c, ex2(lg[63]));
+        K.lg63[c] = Gl;
+        __stcg(gc_out + c, ex2(Gl));
         if (c == 0) K.fast = fast ? 1 : 0;
     }
 }
@@ -453,7 +467,7 @@ __device__ __forceinline__ void ld_f32_chunks(const float* row, int t, float (&f
 // step ks reduces over its channels 2 ks and 2 ks + 1 (the same permutation on both operands leaves the sum alone),
 // which makes every operand load a 16-byte vector.  For row block a against column block b <= a:
 //   row operand x_ic 2^(G_ic - R_a) = x_ic E_ic;   column operand k_jc 2^(R_a - G_jc) =
-//   k_jc F_jc (b = a),   ((k_jc F_jc 2^(R_{b+1} - R_b)) 2^(R_{b+2} - R_{b+1}) ...) (b < a, each factor <= 1).
+//   k_jc F_jc (b = a),   (k_jc F_jc) 2^(R_a - R_b) (b < a; F_jc <= 2^(block spread), 2^(R_a - R_b) <= 1).
 // Warp w: product op = w % 2 (K or Q rows), row blocks {0, 3} or {1, 2} ((w / 2) % 2), 8-column half nt = w / 4 of
 // every column block: five 16 x 8 output tiles per warp.
 __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* bb, float scale, int warp, int lane) {
@@ -494,12 +508,11 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
             float kv[32], f[32];
             ld_bf16_chunks(kb, j, t4, kv);
             ld_f32_chunks(F + j * ES, t4, f);
-#pragma unroll 1
-            for (int m = b; m < a; ++m) {          // 2^(R_a - G_j) = F_j 2^(R_{b+1} - R_b) ... 2^(R_a - R_{a-1})
-                float es[32];
-                ld_f32_chunks(K.esp[m], t4, es);
+            if (b < a) {   // 2^(R_a - G_j) = F_j 2^(R_a - R_b); where the second factor underflows the product is < 2^-26
+                float dd[32];
+                ld_f32_chunks(K.dab[a * (a - 1) / 2 + b], t4, dd);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) f[q] *= es[q];
+                for (int q = 0; q < 32; ++q) f[q] *= dd[q];
             }
             float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};   // two independent chains
 #pragma unroll
@@ -761,7 +774,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             if (!ok && tid == 0) set_status(2u);
             if (ok && loader) v_waited = ic + 1;
             if (lane == 0) bulk_wait_read();   // the previous item's staging rows (E, A1) have been read
-            __syncwarp();
+            __syncthreads();                   // ... by every warp's copies, before any thread writes E
             // [B] the gate tables (contains the barrier that decides the fast path)
             kda_gate_tables(smem, KS, ok ? L : 0, ws.gc + (size_t)it.it * 128, tid);
             __syncthreads();
@@ -787,16 +800,15 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     st16(smem + I_B2 + slab * 8192 + off, xv.x, xv.y, xv.z, xv.w);
                     bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + off), f);
                     if (fast) {
-                        float e8[8], f8[8], er[8], es[8], el[8];
+                        float e8[8], f8[8], er[8], el[8];
                         ld_f8(E + r * ES + c, e8);
                         ld_f8(F + r * ES + c, f8);
                         ld_f8(&KS.er[a][c], er);
-                        ld_f8(&KS.esp[a][c], es);
-                        ld_f8(&KS.elp[a][c], el);
+                        ld_f8(&KS.espl[a][c], el);
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             eg[q] = S.bbuf[r] * (e8[q] * er[q]);
-                            ek[q] = (f8[q] * es[q]) * el[q];
+                            ek[q] = f8[q] * el[q];   // 2^(R_a - G) 2^(G_last - R_a)
                         }
                     } else {
                         float g8[8], l8[8];
