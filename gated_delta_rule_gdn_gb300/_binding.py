@@ -46,6 +46,12 @@ def _declare(lib):
     for name in ("gdn_chunk_fwd_ws", "kda_chunk_fwd_ws"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i, chunk + [i, vp, ctypes.c_size_t, vp]
+    lib.gdn_chunk_fwd_ex.restype = i
+    lib.gdn_chunk_fwd_ex.argtypes = [i] + chunk[:14] + [i] + chunk[14:] + [ctypes.POINTER(GateAct), i, vp,
+                                                                           ctypes.c_size_t, vp]
+    lib.gdn_recurrent_step_ex.restype = i
+    lib.gdn_recurrent_step_ex.argtypes = [i, vp, vp, vp, vp, vp, fp, vp, vp, i, i, i, i, i, i, i,
+                                          ctypes.POINTER(GateAct), vp]
     lib.gdn_chunk_fwd_act.restype = i
     lib.gdn_chunk_fwd_act.argtypes = chunk + [ctypes.POINTER(GateAct), i, vp, ctypes.c_size_t, vp]
     lib.gdn_recurrent_step_act.restype = i
@@ -148,9 +154,10 @@ def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, 
     for name, t, dt in (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype), ("g", g, torch.float32),
                         ("beta", beta, torch.float32)):
         _need(t, name, dt, dev)
-    B, T, H, dk = q.shape
+    B, T, Hk, dk = q.shape
+    H = v.shape[2]            # value heads (a multiple of the key heads of q and k)
     dv = v.shape[-1]
-    if k.shape != q.shape or v.shape[:3] != (B, T, H):
+    if k.shape != q.shape or v.shape[:2] != (B, T) or H % Hk != 0:
         raise ValueError("q, k, v shapes do not match")
     if g.shape != ((B, T, H, dk) if per_channel else (B, T, H)) or beta.shape != (B, T, H):
         raise ValueError("g / beta shapes do not match")
@@ -186,10 +193,9 @@ def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, 
             int(final_state is not None), _ptr(final_state), _ptr(cu_seqlens), n_seqs, _ptr(o),
             B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[o_dtype])
     tail = (ALGOS[algo], _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream_handle(stream, dev))
-    if act is not None:
-        if per_channel:
-            raise ValueError("the gate activation applies to the scalar gate only")
-        st = lib.gdn_chunk_fwd_act(*args, ctypes.byref(act), *tail)
+    if act is not None or Hk != H:
+        ext = args[:14] + (Hk,) + args[14:]
+        st = lib.gdn_chunk_fwd_ex(int(per_channel), *ext, None if act is None else ctypes.byref(act), *tail)
     else:
         fn = lib.kda_chunk_fwd_ws if per_channel else lib.gdn_chunk_fwd_ws
         st = fn(*args, *tail)
@@ -256,10 +262,12 @@ def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream
     for name, t, dt in (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype), ("g", g, torch.float32),
                         ("beta", beta, torch.float32), ("state", state, torch.float32)):
         _need(t, name, dt, dev)
-    N, H, dk = q.shape
+    N, Hk, dk = q.shape
+    H = v.shape[1]            # value heads (a multiple of the key heads of q and k)
     dv = v.shape[-1]
     g_shape = (N, H, dk) if per_channel else (N, H)
-    if state.shape != (N, H, dk, dv) or k.shape != q.shape or g.shape != g_shape or beta.shape != (N, H):
+    if (state.shape != (N, H, dk, dv) or k.shape != q.shape or g.shape != g_shape or beta.shape != (N, H)
+            or H % Hk != 0):
         raise ValueError("decode shapes do not match")
     if o_dtype not in DTYPES:
         raise ValueError(f"o_dtype must be float32 or bfloat16 (got {o_dtype})")
@@ -271,10 +279,10 @@ def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream
     act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(o), N, H, dk, dv,
             DTYPES[q.dtype], DTYPES[o_dtype])
-    if act is not None:
-        if per_channel:
-            raise ValueError("the gate activation applies to the scalar gate only")
-        st = lib.gdn_recurrent_step_act(*args, ctypes.byref(act), _stream_handle(stream, dev))
+    if act is not None or Hk != H:
+        ext = args[:8] + (N, Hk) + args[9:]
+        st = lib.gdn_recurrent_step_ex(int(per_channel), *ext, None if act is None else ctypes.byref(act),
+                                       _stream_handle(stream, dev))
     else:
         fn = lib.kda_recurrent_step if per_channel else lib.gdn_recurrent_step
         st = fn(*args, _stream_handle(stream, dev))

@@ -106,12 +106,16 @@ gdn_status chunk_common(const void* q, const void* k, const void* v, const float
                         const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H, int d_k, int d_v,
                         int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype, gdn_algo algo, void* workspace,
                         size_t workspace_bytes, void* stream, bool per_channel, const char* fn,
-                        const gdn_gate_act* act = nullptr) {
+                        const gdn_gate_act* act = nullptr, int H_k = 0) {
     gdn::ChunkArgs a{q, k, v, g, beta, scale, initial_state, final_state, cu_seqlens, n_seqs, o,
                      B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0,
                      o_dtype == GDN_F32 ? 1 : 0};
     gdn_status st = check_chunk(a, dtype, o_dtype, output_final_state, fn);
     if (st != GDN_OK) return st;
+    if (H_k < 0 || (H_k > 0 && H % H_k != 0))
+        return fail(GDN_ERR_INVALID_ARG, "%s: the value heads (%d) must be a multiple of the key heads (%d)", fn, H,
+                    H_k);
+    a.Hk = H_k;
     st = set_act(a.act, act, fn);
     if (st != GDN_OK) return st;
     gdn_algo chosen = GDN_ALGO_GENERIC;
@@ -120,6 +124,9 @@ gdn_status chunk_common(const void* q, const void* k, const void* v, const float
     if (a.act.any() && chosen != GDN_ALGO_TWO_PASS)
         return fail(GDN_ERR_UNSUPPORTED, "%s: the gate activation runs on the two-pass path only (bf16, d = 128, "
                     "chunk 64, scalar gate)", fn);
+    if (a.HK() != a.H && chosen != GDN_ALGO_TWO_PASS)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: grouped value heads run on the two-pass path only (bf16, d = 128, "
+                    "chunk 64)", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (chosen == GDN_ALGO_TWO_PASS) {
@@ -161,7 +168,8 @@ gdn::ChunkArgs plan_args(int per_channel, int B, int T, int H, int d_k, int d_v,
 
 gdn_status step_common(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
                        float* state, void* o, int N, int H, int d_k, int d_v, gdn_dtype dtype, gdn_dtype o_dtype,
-                       void* stream, bool per_channel, const char* fn, const gdn_gate_act* act = nullptr) {
+                       void* stream, bool per_channel, const char* fn, const gdn_gate_act* act = nullptr,
+                       int H_k = 0) {
     if (!dtype_ok(dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
     if (!dtype_ok(o_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown o_dtype %d", fn, (int)o_dtype);
     if (N < 1 || H < 1) return fail(GDN_ERR_INVALID_ARG, "%s: need N >= 1, H >= 1 (got N=%d H=%d)", fn, N, H);
@@ -183,6 +191,10 @@ gdn_status step_common(const void* q, const void* k, const void* v, const float*
     if (st != GDN_OK) return st;
     if (per_channel && a.act.any())
         return fail(GDN_ERR_UNSUPPORTED, "%s: the gate activation applies to the scalar gate only", fn);
+    if (H_k < 0 || (H_k > 0 && H % H_k != 0))
+        return fail(GDN_ERR_INVALID_ARG, "%s: the value heads (%d) must be a multiple of the key heads (%d)", fn, H,
+                    H_k);
+    a.Hk = H_k;
     cudaError_t e = gdn::launch_recurrent_step(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return ok();
@@ -290,6 +302,25 @@ gdn_status gdn_chunk_fwd_act(const void* q, const void* k, const void* v, const 
     return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
                         o, B, T, H, d_k, d_v, chunk_size, dtype, o_dtype, algo, workspace, workspace_bytes, stream,
                         false, "gdn_chunk_fwd_act", act);
+}
+
+gdn_status gdn_chunk_fwd_ex(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float scale, const float* initial_state, int output_final_state,
+                            float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o, int B, int T, int H_k,
+                            int H_v, int d_k, int d_v, int chunk_size, gdn_dtype dtype, gdn_dtype o_dtype,
+                            const gdn_gate_act* act, gdn_algo algo, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    return chunk_common(q, k, v, g, beta, scale, initial_state, output_final_state, final_state, cu_seqlens, n_seqs,
+                        o, B, T, H_v, d_k, d_v, chunk_size, dtype, o_dtype, algo, workspace, workspace_bytes, stream,
+                        per_channel != 0, "gdn_chunk_fwd_ex", act, H_k);
+}
+
+gdn_status gdn_recurrent_step_ex(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, float scale, float* state, void* o, int N, int H_k, int H_v,
+                                 int d_k, int d_v, gdn_dtype dtype, gdn_dtype o_dtype, const gdn_gate_act* act,
+                                 void* stream) {
+    return step_common(q, k, v, g, beta, scale, state, o, N, H_v, d_k, d_v, dtype, o_dtype, stream, per_channel != 0,
+                       "gdn_recurrent_step_ex", act, H_k);
 }
 
 gdn_status gdn_recurrent_step_act(const void* q, const void* k, const void* v, const float* g, const float* beta,

@@ -755,6 +755,7 @@ bool device_is_sm100_family() {
 const char* tc_chunk_unsupported_reason(const ChunkArgs& a) {
     if (a.per_channel) return "per-channel (KDA) gates use another kernel";
     if (a.act.any()) return "the gate activation runs on the two-pass path";
+    if (a.HK() != a.H) return "grouped values run on the two-pass path";
     if (!a.bf16) return "q, k, v must be bf16";
     if (a.dk != DK || a.dv != DV) return "d_k and d_v must be 128";
     if (a.C != C) return "chunk_size must be 64";

@@ -109,6 +109,7 @@ struct IntraParams {
     long n_slots;
     Ws ws;
     GateAct act;   // scalar gate only
+    int group;     // value heads per key head: q and k of item head h come from key head h / group
 };
 
 struct Item {
@@ -305,14 +306,14 @@ __device__ void solve_unit_lower_inplace(float* Am, float* Rt, int t, bool work)
 // TMA loads of an item: K and Q as 2 x 2 boxes of 64 tokens x 64 columns; V as two boxes (GDN: into X's V slabs,
 // KDA: into its own tile, with the fp32 gate tile into X).
 __device__ __forceinline__ void intra_issue_kq(uint8_t* smem, ISmall& S, const CUtensorMap* mq, const CUtensorMap* mk,
-                                               const Item& x) {
-    const int row = (int)x.row;
+                                               const Item& x, int group) {
+    const int row = (int)x.row, hk = x.h / group;
     mbar_arrive_expect_tx(&S.full_kq, 32768);
     uint8_t* kq = smem + I_KQ;
-    tma_load_3d(kq, mk, &S.full_kq, 0, x.h, row);
-    tma_load_3d(kq + 8192, mq, &S.full_kq, 0, x.h, row);
-    tma_load_3d(kq + 16384, mk, &S.full_kq, 64, x.h, row);
-    tma_load_3d(kq + 16384 + 8192, mq, &S.full_kq, 64, x.h, row);
+    tma_load_3d(kq, mk, &S.full_kq, 0, hk, row);
+    tma_load_3d(kq + 8192, mq, &S.full_kq, 0, hk, row);
+    tma_load_3d(kq + 16384, mk, &S.full_kq, 64, hk, row);
+    tma_load_3d(kq + 16384 + 8192, mq, &S.full_kq, 64, hk, row);
 }
 template <bool KDA>
 __device__ __forceinline__ void intra_issue_v(uint8_t* smem, ISmall& S, const CUtensorMap* mv, const CUtensorMap* mg,
@@ -655,7 +656,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
             if (KDA) prefetch_tmap(&tmap_g);
-            intra_issue_kq(smem, S, &tmap_q, &tmap_k, x);
+            intra_issue_kq(smem, S, &tmap_q, &tmap_k, x, p.group);
             intra_issue_v<KDA>(smem, S, &tmap_v, &tmap_g, x);
             kq_issued = v_issued = 1;
         }
@@ -762,7 +763,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             __syncthreads();   // [C] D0 ready; K and Q are dead
             tc_fence_after();
             if (ok && loader && have_next) {
-                intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx);
+                intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx, p.group);
                 kq_issued = ic + 2;
             }
             if (ok) epilogue_kkt(tl + I_TM_D0, row, q4, pw, S.lg, S.bbuf, p.scale, Am, smem + I_A1);
@@ -863,7 +864,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             __syncthreads();   // [C] A, [I; P] and X are in shared memory; K and Q are dead
             tc_fence_after();
             if (ok && loader && have_next) {
-                intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx);
+                intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx, p.group);
                 kq_issued = ic + 2;
             }
         }
@@ -1324,7 +1325,8 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % 256) != 0)
         return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, rows, a.H, DK) || !make_map(&mk, a.k, rows, a.H, DK) || !make_map(&mv, a.v, rows, a.H, DV))
+    if (!make_map(&mq, a.q, rows, a.HK(), DK) || !make_map(&mk, a.k, rows, a.HK(), DK) ||
+        !make_map(&mv, a.v, rows, a.H, DV))
         return cudaErrorInvalidValue;
     const long items = n_slots(a) * a.H;
     uint8_t* base = static_cast<uint8_t*>(workspace);
@@ -1340,7 +1342,7 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    IntraParams ip{geo, a.g, a.beta, a.scale, n_slots(a), ws, a.act};
+    IntraParams ip{geo, a.g, a.beta, a.scale, n_slots(a), ws, a.act, a.H / a.HK()};
     if (a.per_channel) {
         CUtensorMap mg;
         if (!make_map_f32_rows(&mg, a.g, rows, a.H, DK)) return cudaErrorInvalidValue;

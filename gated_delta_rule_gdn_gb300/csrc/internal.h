@@ -36,7 +36,9 @@ struct ChunkArgs {
     int per_channel;        // 1: KDA gate [.., dk]
     int o_f32;              // 1: o is fp32; 0: o is bf16
     GateAct act;            // gate / beta activation (two-pass path, scalar gate only)
+    int Hk;                 // key heads of q and k (0: H); H (value heads) is a multiple of it
     int N() const { return cu ? n_seqs : B; }
+    int HK() const { return Hk > 0 ? Hk : H; }
 };
 
 struct StepArgs {
@@ -53,6 +55,7 @@ struct StepArgs {
     int o_f32;              // 1: o is fp32; 0: o is bf16
     int per_channel;        // 1: KDA gate [N, H, dk]
     GateAct act;            // gate / beta activation (scalar gate only)
+    int Hk;                 // key heads of q and k (0: H); H (value heads) is a multiple of it
 };
 
 // Generic fp32 SIMT chunk kernel (chunk_generic.cu).

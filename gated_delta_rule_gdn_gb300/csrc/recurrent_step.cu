@@ -47,8 +47,10 @@ step_d128_kernel(const StepArgs a) {
     __shared__ float kq_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t nh = blockIdx.x;
-    const Tin* q = static_cast<const Tin*>(a.q) + nh * kD;
-    const Tin* k = static_cast<const Tin*>(a.k) + nh * kD;
+    const int Hk = a.Hk > 0 ? a.Hk : a.H;   // grouped values: key head h / (H / Hk) serves value head h
+    const size_t nk = (nh / a.H) * Hk + (nh % a.H) / (a.H / Hk);
+    const Tin* q = static_cast<const Tin*>(a.q) + nk * kD;
+    const Tin* k = static_cast<const Tin*>(a.k) + nk * kD;
     const Tin* v = static_cast<const Tin*>(a.v) + nh * kD;
     float* __restrict__ h = a.state + nh * (size_t)kD * kD;
 
@@ -118,8 +120,10 @@ step_generic_kernel(const StepArgs a) {
     const int tid = threadIdx.x;
     const size_t nh = blockIdx.x;
     const int dk = a.dk, dv = a.dv;
-    const Tin* q = static_cast<const Tin*>(a.q) + nh * dk;
-    const Tin* k = static_cast<const Tin*>(a.k) + nh * dk;
+    const int Hk = a.Hk > 0 ? a.Hk : a.H;
+    const size_t nk = (nh / a.H) * Hk + (nh % a.H) / (a.H / Hk);
+    const Tin* q = static_cast<const Tin*>(a.q) + nk * dk;
+    const Tin* k = static_cast<const Tin*>(a.k) + nk * dk;
     const Tin* v = static_cast<const Tin*>(a.v) + nh * dv;
     float* h = a.state + nh * (size_t)dk * dv;
     for (int i = tid; i < dk; i += blockDim.x) {

@@ -175,6 +175,26 @@ gdn_status gdn_chunk_fwd_act(const void* q, const void* k, const void* v, const 
                              size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_chunk_fwd_ex -- the chunk forward with every option in one call:
+ *   per_channel   nonzero: the KDA gate (g [B, T, H_v, d_k]), as kda_chunk_fwd.
+ *   H_k, H_v      grouped value heads ("Gated Delta Network (GDN)", §4: more
+ *                 value heads than key heads): q and k are [B, T, H_k, d_k];
+ *                 v, o, g, beta and the states are per value head; value head
+ *                 h uses key head h / (H_v / H_k).  H_v must be a multiple of
+ *                 H_k (H_k = H_v is plain GDN).
+ *   act           the gate / beta activation (may be NULL).
+ * Grouped heads and the activation run on the two-pass path only; another
+ * kernel choice returns GDN_ERR_UNSUPPORTED.  Other arguments are those of
+ * gdn_chunk_fwd_ws.
+ */
+gdn_status gdn_chunk_fwd_ex(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float scale, const float* initial_state, int output_final_state,
+                            float* final_state, const int32_t* cu_seqlens, int n_seqs, void* o,
+                            int B, int T, int H_k, int H_v, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                            gdn_dtype o_dtype, const gdn_gate_act* act, gdn_algo algo, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * kda_chunk_fwd -- chunkwise forward of Kimi Delta Attention.  The retention
  * is a per-key-channel vector exp(g_t), applied as Diag(exp g_t) on the key
  * side of the state before the delta update.
@@ -256,6 +276,16 @@ gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const
 gdn_status gdn_recurrent_step_act(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                   float scale, float* state, void* o, int N, int H, int d_k, int d_v,
                                   gdn_dtype dtype, gdn_dtype o_dtype, const gdn_gate_act* act, void* stream);
+
+/*
+ * gdn_recurrent_step_ex -- the decode step with every option: per_channel
+ * (the KDA gate, g [N, H_v, d_k]), grouped value heads (q, k [N, H_k, d_k];
+ * value head h uses key head h / (H_v / H_k)) and the activation (may be NULL).
+ */
+gdn_status gdn_recurrent_step_ex(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, float scale, float* state, void* o, int N, int H_k, int H_v,
+                                 int d_k, int d_v, gdn_dtype dtype, gdn_dtype o_dtype, const gdn_gate_act* act,
+                                 void* stream);
 
 /*
  * kda_recurrent_step -- one decode token of Kimi Delta Attention for N

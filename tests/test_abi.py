@@ -137,3 +137,21 @@ def test_gate_activation_argument_checks(lib):
     assert lib.gdn_chunk_fwd_act(*args, ctypes.byref(bad), 0, None, 0, None) == 1
     odd = _binding.GateAct(FAKE + 2, None, 0)    # misaligned A_log
     assert lib.gdn_chunk_fwd_act(*args, ctypes.byref(odd), 0, None, 0, None) == 1
+
+
+def test_grouped_value_head_argument_checks(lib):
+    # gdn_chunk_fwd_ex: per_channel, then the chunk arguments with H_k before H_v
+    def chunk(Hk, Hv, dtype=1, algo=0):
+        return lib.gdn_chunk_fwd_ex(0, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, None, 0, None, None, 0, FAKE, 1, 64, Hk, Hv,
+                                    128, 128, 64, dtype, 0, None, algo, None, 0, None)
+    assert chunk(2, 5) == 1                      # H_v not a multiple of H_k
+    assert "key heads" in _binding.last_error()
+    assert chunk(-1, 4) == 1
+    assert chunk(2, 4, algo=2) == 2              # the fused single-kernel path reads one key head per value head
+    assert chunk(2, 4, dtype=0) == 2             # fp32 resolves to the generic kernel: refused before any launch
+
+    def step(Hk, Hv):
+        return lib.gdn_recurrent_step_ex(0, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, FAKE, 4, Hk, Hv, 128, 128, 1, 0,
+                                         None, None)
+    assert step(3, 4) == 1
+    assert "key heads" in _binding.last_error()

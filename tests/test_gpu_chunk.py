@@ -323,3 +323,21 @@ def test_in_kernel_gate_and_beta_activation():
     assert gdn.device_status() == 0
     assert_close(o.double().cpu().numpy(), o_ref, torch.bfloat16, "o")
     assert_close(hT.double().cpu().numpy(), h_ref, torch.bfloat16, "final state")
+
+
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_grouped_value_heads(kind):
+    """H_v = 3 H_k: value head h reads q and k of key head h // 3 (checked against the oracle on q, k repeated
+    per value head)."""
+    Hk, G = 2, 3
+    x = W.chunk_inputs(W.config(3 if kind == "kda" else 1), seed=10, B=2, T=200, H=Hk * G)
+    xq = dict(x)
+    xq["q"] = x["q"][:, :, ::G].contiguous()        # the key heads
+    xq["k"] = x["k"][:, :, ::G].contiguous()
+    xr = dict(x)
+    xr["q"] = xq["q"].repeat_interleave(G, dim=2)  # what each value head sees
+    xr["k"] = xq["k"].repeat_interleave(G, dim=2)
+    o_ref, h_ref = oracle_on_heads(xr)
+    o, hT = _run(xq, "auto")
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")

@@ -142,3 +142,36 @@ def test_decode_with_in_kernel_gate_and_beta_activation():
     for s in range(w.steps):
         assert_close(o_gpu[:, s], o_ref[:, s, 0], torch.bfloat16, f"o at step {s}")
     assert_close(state.reshape(NH, 128, 128).double().cpu().numpy(), h_ref[:, 0], torch.bfloat16, "state")
+
+
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_decode_grouped_value_heads(kind):
+    Hk, G = 2, 4
+    w = W.DecodeWorkload("t", 6, Hk * G, 128, 128, 12, kind=kind)
+    consts = W.decode_constants(w, seed=4)
+    state = consts["state"].cuda()
+    NH = w.N * w.H
+    qs, ks, vs, gs, bs, outs = [], [], [], [], [], []
+    step = gdn.kda_recurrent_step if kind == "kda" else gdn.gdn_recurrent_step
+    for s in range(w.steps):
+        x = W.decode_step_inputs(w, consts, s)
+        qk = {n: x[n][:, ::G].contiguous() for n in ("q", "k")}   # [N, Hk, d]
+        d = {n: t.cuda() for n, t in x.items()}
+        o = step(qk["q"].cuda(), qk["k"].cuda(), d["v"], d["g"], d["beta"], state, scale=w.scale)
+        outs.append(o.reshape(NH, -1).float().cpu())
+        qs.append(qk["q"].repeat_interleave(G, dim=1).reshape(NH, -1))
+        ks.append(qk["k"].repeat_interleave(G, dim=1).reshape(NH, -1))
+        vs.append(x["v"].reshape(NH, -1))
+        gs.append(x["g"].reshape(NH, -1))
+        bs.append(x["beta"].reshape(NH, 1))
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    q, k, v = (torch.stack(t, dim=1)[:, :, None] for t in (qs, ks, vs))
+    beta = torch.stack(bs, dim=1)
+    g = torch.stack(gs, dim=1)[:, :, None] if kind == "kda" else torch.stack(gs, dim=1)
+    o_ref, h_ref = oracle.recurrence(q, k, v, g, beta, w.scale, consts["state"].reshape(NH, 1, 128, 128),
+                                     gate_per_channel=kind == "kda")
+    o_gpu = torch.stack(outs, dim=1).double().numpy()
+    for s in range(w.steps):
+        assert_close(o_gpu[:, s], o_ref[:, s, 0], torch.bfloat16, f"o at step {s}")
+    assert_close(state.reshape(NH, 128, 128).double().cpu().numpy(), h_ref[:, 0], torch.bfloat16, "state")
