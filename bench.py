@@ -78,15 +78,26 @@ def _alg_bytes(w) -> int:
     return token_heads * per_token_head + state
 
 
-def _traffic_for(kernel: str):
-    """ncu DRAM bytes per launch for `kernel`, if profiled for the current kernel source (else None)."""
+TRAFFIC_SOURCES = ("chunk_two_pass.cu", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh", "recurrent_step.cu")
+
+
+def sources_sha256() -> str:
+    """Hash of the kernel sources the recorded ncu traffic depends on."""
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "gated_delta_rule_gdn_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic_for(workload: str):
+    """ncu DRAM bytes per call (all launches of one step) for `workload`, if they were captured from the current
+    kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)[kernel]
-        src = os.path.join(ROOT, "gated_delta_rule_gdn_gb300", "csrc", rec["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        return int(rec["dram_bytes_per_launch"]) if sha == rec["source_sha256"] else None
+            rec = json.load(f)[workload]
+        return int(rec["dram_bytes_per_call"]) if rec["sources_sha256"] == sources_sha256() else None
     except Exception:
         return None
 
@@ -395,7 +406,7 @@ def run_ours(args):
                    "l2": "flushed before each timed step (256 MiB device write, outside the events)",
                    "kernel": kernel, "launches_per_step": launches, "timed_region_wall_ms": t_wall * 1e3},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": _traffic_for(kernel), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     "traffic": _traffic_for(w.name), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6800 GB/s",
                      "algorithmic_bytes_per_launch": alg},
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -510,7 +521,7 @@ def run_decode(args):
                    "l2": "not flushed: the 512 MiB state read and written every step is larger than L2",
                    "kernel": "recurrent_step", "timed_region_wall_ms": t_wall * 1e3},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     "traffic": _traffic_for(w.name), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6800 GB/s", "algorithmic_bytes_per_step": alg},
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

@@ -131,8 +131,11 @@ def workspace_size(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, 
     return int(out.value)
 
 
-def _gate_act(dev, H, A_log, dt_bias, beta_sigmoid):
-    """The activation descriptor (or None) after checking its tensors."""
+def _gate_act(dev, H, A_log, dt_bias, beta_sigmoid, allow_neg_eigval=False):
+    """The activation descriptor (or None) after checking its tensors.  With ``allow_neg_eigval`` the sigmoid of
+    beta is doubled (beta in (0, 2))."""
+    if allow_neg_eigval and not beta_sigmoid:
+        raise ValueError("allow_neg_eigval scales the in-kernel sigmoid of beta: it needs beta_sigmoid")
     if A_log is None and dt_bias is None and not beta_sigmoid:
         return None
     for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
@@ -141,12 +144,13 @@ def _gate_act(dev, H, A_log, dt_bias, beta_sigmoid):
             if t.shape != (H,):
                 raise ValueError(f"{name} must have shape ({H},)")
     return GateAct(None if A_log is None else A_log.data_ptr(), None if dt_bias is None else dt_bias.data_ptr(),
-                   int(bool(beta_sigmoid)))
+                   (2 if allow_neg_eigval else 1) if beta_sigmoid else 0)
 
 
 def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
            cu_seqlens=None, chunk_size=64, algo="auto", o=None, final_state=None, stream=None,
-           o_dtype=torch.float32, workspace=None, A_log=None, dt_bias=None, beta_sigmoid=False):
+           o_dtype=torch.float32, workspace=None, A_log=None, dt_bias=None, beta_sigmoid=False,
+           allow_neg_eigval=False):
     lib = load()
     if q.dtype not in DTYPES:
         raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
@@ -188,7 +192,7 @@ def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, 
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if workspace is not None:
         _need(workspace, "workspace", torch.uint8, dev)
-    act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid)
+    act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(initial_state),
             int(final_state is not None), _ptr(final_state), _ptr(cu_seqlens), n_seqs, _ptr(o),
             B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[o_dtype])
@@ -205,25 +209,27 @@ def _chunk(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, 
 
 def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False, cu_seqlens=None,
                   chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32,
-                  workspace=None, A_log=None, dt_bias=None, beta_sigmoid=False):
+                  workspace=None, A_log=None, dt_bias=None, beta_sigmoid=False, allow_neg_eigval=False):
     """Chunkwise gated delta rule forward (C ABI gdn_chunk_fwd_ws, or gdn_chunk_fwd_act with an activation).
     Returns (o, final_state or None).
 
     o is fp32 unless o_dtype=torch.bfloat16 (then it is the round-to-nearest-even of the fp32 result).
     ``workspace`` (uint8 device tensor, see workspace_size) is allocated here when the kernel needs one.
     ``A_log``/``dt_bias`` ([H] fp32): g holds raw logits and the kernel applies -exp(A_log) softplus(g + dt_bias);
-    ``beta_sigmoid``: beta holds logits.
+    ``beta_sigmoid``: beta holds logits (sigmoid in the kernel; 2 sigmoid, beta in (0, 2), with
+    ``allow_neg_eigval``).  q and k may have fewer heads than v (grouped value heads).
     """
     return _chunk(False, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens, chunk_size, algo,
-                  o, final_state, stream, o_dtype, workspace, A_log, dt_bias, beta_sigmoid)
+                  o, final_state, stream, o_dtype, workspace, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
 
 
 def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False, cu_seqlens=None,
                   chunk_size=64, algo="auto", o=None, final_state=None, stream=None, o_dtype=torch.float32,
-                  workspace=None):
-    """Chunkwise KDA forward, g per key channel (C ABI kda_chunk_fwd_ws).  Returns (o, final_state or None)."""
+                  workspace=None, beta_sigmoid=False, allow_neg_eigval=False):
+    """Chunkwise KDA forward, g per key channel (C ABI kda_chunk_fwd_ws).  Returns (o, final_state or None).
+    ``beta_sigmoid``/``allow_neg_eigval`` as for gdn_chunk_fwd; the gate itself is taken as given."""
     return _chunk(True, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens, chunk_size, algo,
-                  o, final_state, stream, o_dtype, workspace)
+                  o, final_state, stream, o_dtype, workspace, None, None, beta_sigmoid, allow_neg_eigval)
 
 
 def chunk_fwd_noalloc(per_channel: bool, q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
@@ -254,7 +260,7 @@ def chunk_fwd_noalloc(per_channel: bool, q, k, v, g, beta, scale=None, initial_s
 
 
 def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32,
-          A_log=None, dt_bias=None, beta_sigmoid=False):
+          A_log=None, dt_bias=None, beta_sigmoid=False, allow_neg_eigval=False):
     lib = load()
     if q.dtype not in DTYPES:
         raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
@@ -276,7 +282,7 @@ def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream
     _need(o, "o", o_dtype, dev)
     if scale is None:
         scale = dk ** -0.5
-    act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid)
+    act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(o), N, H, dk, dv,
             DTYPES[q.dtype], DTYPES[o_dtype])
     if act is not None or Hk != H:
@@ -291,15 +297,18 @@ def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream
 
 
 def gdn_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32,
-                       A_log=None, dt_bias=None, beta_sigmoid=False):
+                       A_log=None, dt_bias=None, beta_sigmoid=False, allow_neg_eigval=False):
     """One decode token for N sequences (C ABI gdn_recurrent_step, or gdn_recurrent_step_act with an activation);
     updates ``state`` in place, returns o."""
-    return _step(False, q, k, v, g, beta, state, scale, o, stream, o_dtype, A_log, dt_bias, beta_sigmoid)
+    return _step(False, q, k, v, g, beta, state, scale, o, stream, o_dtype, A_log, dt_bias, beta_sigmoid,
+                 allow_neg_eigval)
 
 
-def kda_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32):
+def kda_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32,
+                       beta_sigmoid=False, allow_neg_eigval=False):
     """One KDA decode token, g per key channel [N, H, d_k] (C ABI kda_recurrent_step); updates ``state`` in place."""
-    return _step(True, q, k, v, g, beta, state, scale, o, stream, o_dtype)
+    return _step(True, q, k, v, g, beta, state, scale, o, stream, o_dtype, None, None, beta_sigmoid,
+                 allow_neg_eigval)
 
 
 def chunk_plan(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chunk_size: int, dtype,

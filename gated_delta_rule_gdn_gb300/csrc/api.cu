@@ -97,7 +97,9 @@ gdn_status set_act(gdn::GateAct& dst, const gdn_gate_act* act, const char* fn) {
         return fail(GDN_ERR_INVALID_ARG, "%s: dt_bias is given without A_log", fn);
     if ((act->A_log && !aligned(act->A_log, 4)) || (act->dt_bias && !aligned(act->dt_bias, 4)))
         return fail(GDN_ERR_INVALID_ARG, "%s: A_log or dt_bias is not 4-byte aligned", fn);
-    dst = gdn::GateAct{act->A_log, act->dt_bias, act->beta_sigmoid ? 1 : 0};
+    if (act->beta_sigmoid < 0 || act->beta_sigmoid > 2)
+        return fail(GDN_ERR_INVALID_ARG, "%s: beta_sigmoid must be 0, 1 or 2 (got %d)", fn, act->beta_sigmoid);
+    dst = gdn::GateAct{act->A_log, act->dt_bias, act->beta_sigmoid};
     return GDN_OK;
 }
 
@@ -122,8 +124,8 @@ gdn_status chunk_common(const void* q, const void* k, const void* v, const float
     st = resolve_algo(a, algo, fn, &chosen);
     if (st != GDN_OK) return st;
     if (a.act.any() && chosen != GDN_ALGO_TWO_PASS)
-        return fail(GDN_ERR_UNSUPPORTED, "%s: the gate activation runs on the two-pass path only (bf16, d = 128, "
-                    "chunk 64, scalar gate)", fn);
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the gate and beta activation run on the two-pass path only (bf16, d = 128, "
+                    "chunk 64)", fn);
     if (a.HK() != a.H && chosen != GDN_ALGO_TWO_PASS)
         return fail(GDN_ERR_UNSUPPORTED, "%s: grouped value heads run on the two-pass path only (bf16, d = 128, "
                     "chunk 64)", fn);
@@ -189,7 +191,7 @@ gdn_status step_common(const void* q, const void* k, const void* v, const float*
                     o_dtype == GDN_F32 ? 1 : 0, per_channel ? 1 : 0};
     gdn_status st = set_act(a.act, act, fn);
     if (st != GDN_OK) return st;
-    if (per_channel && a.act.any())
+    if (per_channel && a.act.gate())
         return fail(GDN_ERR_UNSUPPORTED, "%s: the gate activation applies to the scalar gate only", fn);
     if (H_k < 0 || (H_k > 0 && H % H_k != 0))
         return fail(GDN_ERR_INVALID_ARG, "%s: the value heads (%d) must be a multiple of the key heads (%d)", fn, H,

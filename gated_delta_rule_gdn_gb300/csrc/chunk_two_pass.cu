@@ -108,7 +108,7 @@ struct IntraParams {
     float scale;
     long n_slots;
     Ws ws;
-    GateAct act;   // scalar gate only
+    GateAct act;   // the gate activation for the scalar gate only; beta for both
     int group;     // value heads per key head: q and k of item head h come from key head h / group
 };
 
@@ -1292,7 +1292,7 @@ long n_slots(const ChunkArgs& a) { return (long)a.B * a.T / C + a.N() + 1; }
 }  // namespace
 
 const char* two_pass_unsupported_reason(const ChunkArgs& a) {
-    if (a.per_channel && a.act.any()) return "the gate activation applies to the scalar gate only";
+    if (a.per_channel && a.act.gate()) return "the gate activation applies to the scalar gate only";
     if (!a.bf16) return "q, k, v must be bf16";
     if (a.dk != DK || a.dv != DV) return "d_k and d_v must be 128";
     if (a.C != C) return "chunk_size must be 64";

@@ -1,5 +1,5 @@
 // In-kernel activation of the gate and of beta from raw logits ("Gated Delta Network (GDN)", §3.1 eq. 5: the
-// Mamba2-style parameterisation log alpha = -exp(A_log) softplus(x + dt_bias); beta = sigmoid(x); §4 and §6 describe
+// Mamba2-style parameterisation log alpha = -exp(A_log) softplus(x + dt_bias); beta = sigmoid(x), or 2 sigmoid(x) with negative eigenvalues allowed; §4 and §6 describe
 // fusing both into the chunk kernel so no separate activation pass runs).
 #pragma once
 
@@ -19,8 +19,10 @@ __device__ __forceinline__ float act_gate(const GateAct& a, float raw, int h) {
     return -expf(a.A_log[h]) * softplus_f(raw + dt);
 }
 
+// beta from its logit: sigmoid, or 2 sigmoid (beta in (0, 2), so the transition I - beta k k^T of a unit key can
+// have the eigenvalue 1 - beta < 0; "Gated Delta Network (GDN)", §5 implementation notes)
 __device__ __forceinline__ float act_beta(const GateAct& a, float raw) {
-    return a.beta_sigmoid ? 1.f / (1.f + expf(-raw)) : raw;
+    return a.beta_sigmoid ? (float)a.beta_sigmoid / (1.f + expf(-raw)) : raw;
 }
 
 }  // namespace gdn

@@ -14,8 +14,9 @@ namespace gdn {
 struct GateAct {
     const float* A_log;     // [H] or nullptr: g holds log alpha itself
     const float* dt_bias;   // [H] or nullptr (zero)
-    int beta_sigmoid;       // 1: beta holds logits
+    int beta_sigmoid;       // 1: beta = sigmoid(logit); 2: beta = 2 sigmoid(logit); 0: beta as given
     bool any() const { return A_log != nullptr || beta_sigmoid != 0; }
+    bool gate() const { return A_log != nullptr; }
 };
 
 // One chunk-forward request, already validated by api.cu.

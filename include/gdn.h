@@ -154,7 +154,13 @@ gdn_status gdn_chunk_fwd_ws(const void* q, const void* k, const void* v, const f
  *                 g holds raw logits x and the kernel uses
  *                 log alpha = -exp(A_log[h]) * softplus(x + dt_bias[h]).
  *   dt_bias       [H] fp32 device, or NULL (zero); needs A_log.
- *   beta_sigmoid  nonzero: beta holds logits and the kernel uses sigmoid(beta).
+ *   beta_sigmoid  0: beta is used as given.  1: beta holds logits and the kernel
+ *                 uses sigmoid(beta).  2: the kernel uses 2 sigmoid(beta), so beta
+ *                 lies in (0, 2) and the transition I - beta k k^T of a unit key
+ *                 may have a negative eigenvalue (the §5 implementation notes of
+ *                 the same page).  Other values: GDN_ERR_INVALID_ARG.
+ * The gate activation (A_log, dt_bias) applies to the scalar gate only; the
+ * per-channel (KDA) entries accept beta_sigmoid alone.
  */
 typedef struct gdn_gate_act {
     const float* A_log;

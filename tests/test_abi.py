@@ -155,3 +155,15 @@ def test_grouped_value_head_argument_checks(lib):
                                          None, None)
     assert step(3, 4) == 1
     assert "key heads" in _binding.last_error()
+
+
+def test_beta_activation_mode_checks(lib):
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, None, 0, None, None, 0, FAKE, 1, 64, 1, 128, 128, 64, 1, 0]
+    three = _binding.GateAct(None, None, 3)
+    assert lib.gdn_chunk_fwd_act(*args, ctypes.byref(three), 0, None, 0, None) == 1
+    assert "beta_sigmoid" in _binding.last_error()
+    # the per-channel entries take the beta activation but not the gate activation
+    gate = _binding.GateAct(FAKE, None, 0)
+    assert lib.gdn_recurrent_step_ex(1, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, FAKE, 4, 2, 2, 128, 128, 1, 0,
+                                     ctypes.byref(gate), None) == 2
+    assert "scalar gate" in _binding.last_error()

@@ -299,7 +299,7 @@ def _raw_gates(x, seed):
     (log alpha = -exp(A_log) softplus(x + dt_bias), beta = sigmoid(b))."""
     rng = np.random.default_rng(seed)
     H = x["q"].shape[2]
-    gl = rng.standard_normal(tuple(x["g"].shape), dtype=np.float32)
+    gl = rng.standard_normal(tuple(x["beta"].shape), dtype=np.float32)   # one gate logit per (token, head)
     bl = rng.standard_normal(tuple(x["beta"].shape), dtype=np.float32)
     A_log = np.log(rng.uniform(0.5, 16.0, size=H)).astype(np.float32)
     dt_bias = rng.normal(0.0, 0.1, size=H).astype(np.float32)
@@ -341,3 +341,30 @@ def test_grouped_value_heads(kind):
     o, hT = _run(xq, "auto")
     assert_close(o, o_ref, torch.bfloat16, "o")
     assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_beta_in_zero_two_from_logits(kind):
+    """beta = 2 sigmoid(b) in the kernel (negative eigenvalues of I - beta k k^T allowed); GDN also activates
+    the gate from logits, KDA takes its per-channel gate as given."""
+    x = W.chunk_inputs(W.config(3 if kind == "kda" else 1), seed=12, B=2, T=270, H=2)
+    gl, bl, A_log, dt_bias, g64, b64 = _raw_gates(x, 12)
+    xr = dict(x)
+    xr["beta"] = torch.from_numpy(2.0 * b64)
+    if kind == "gdn":
+        xr["g"] = torch.from_numpy(g64)
+    o_ref, h_ref = oracle_on_heads(xr)
+    d = to_dev(x)
+    bt = torch.from_numpy(bl).cuda()
+    common = dict(scale=x["scale"], initial_state=d["initial_state"], output_final_state=True, beta_sigmoid=True,
+                  allow_neg_eigval=True)
+    if kind == "gdn":
+        o, hT = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], torch.from_numpy(gl).cuda(), bt,
+                                  A_log=torch.from_numpy(A_log).cuda(), dt_bias=torch.from_numpy(dt_bias).cuda(),
+                                  **common)
+    else:
+        o, hT = gdn.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], bt, **common)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    assert_close(o.double().cpu().numpy(), o_ref, torch.bfloat16, "o")
+    assert_close(hT.double().cpu().numpy(), h_ref, torch.bfloat16, "final state")

@@ -175,3 +175,35 @@ def test_decode_grouped_value_heads(kind):
     for s in range(w.steps):
         assert_close(o_gpu[:, s], o_ref[:, s, 0], torch.bfloat16, f"o at step {s}")
     assert_close(state.reshape(NH, 128, 128).double().cpu().numpy(), h_ref[:, 0], torch.bfloat16, "state")
+
+
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_decode_beta_in_zero_two_from_logits(kind):
+    w = W.DecodeWorkload("t", 5, 3, 128, 128, 16, kind=kind)
+    consts = W.decode_constants(w, seed=5)
+    rng = np.random.default_rng(5)
+    state = consts["state"].cuda()
+    NH = w.N * w.H
+    step = gdn.kda_recurrent_step if kind == "kda" else gdn.gdn_recurrent_step
+    qs, ks, vs, gs, bs, outs = [], [], [], [], [], []
+    for s in range(w.steps):
+        x = W.decode_step_inputs(w, consts, s)
+        bl = rng.standard_normal((w.N, w.H), dtype=np.float32)
+        d = {n: t.cuda() for n, t in x.items()}
+        o = step(d["q"], d["k"], d["v"], d["g"], torch.from_numpy(bl).cuda(), state, scale=w.scale,
+                 beta_sigmoid=True, allow_neg_eigval=True)
+        outs.append(o.reshape(NH, -1).float().cpu())
+        qs.append(x["q"].reshape(NH, -1)); ks.append(x["k"].reshape(NH, -1)); vs.append(x["v"].reshape(NH, -1))
+        gs.append(x["g"].reshape(NH, -1))
+        bs.append(torch.from_numpy(2.0 / (1.0 + np.exp(-bl.astype(np.float64)))).reshape(NH, 1))
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    q, k, v = (torch.stack(t, dim=1)[:, :, None] for t in (qs, ks, vs))
+    beta = torch.stack(bs, dim=1)
+    g = torch.stack(gs, dim=1)[:, :, None] if kind == "kda" else torch.stack(gs, dim=1)
+    o_ref, h_ref = oracle.recurrence(q, k, v, g, beta, w.scale, consts["state"].reshape(NH, 1, 128, 128),
+                                     gate_per_channel=kind == "kda")
+    o_gpu = torch.stack(outs, dim=1).double().numpy()
+    for s in range(w.steps):
+        assert_close(o_gpu[:, s], o_ref[:, s, 0], torch.bfloat16, f"o at step {s}")
+    assert_close(state.reshape(NH, 128, 128).double().cpu().numpy(), h_ref[:, 0], torch.bfloat16, "state")

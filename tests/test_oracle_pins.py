@@ -144,6 +144,27 @@ def test_householder_eigenstructure():
     assert abs(abs(U[:, 0] @ k) - 1.0) < 1e-12
 
 
+
+def test_beta_two_is_a_reflection():
+    # beta = 2 (the top of the (0, 2) range allowed with negative eigenvalues, GDN page §5 notes) with alpha = 1,
+    # a unit key and v = 0 maps h0 to (I - 2 k k^T) h0: a Householder reflection, so two identical steps give
+    # h0 back, one step flips the component along k and keeps the rest, and the Frobenius norm never changes
+    rng = np.random.default_rng(11)
+    dk, dv = 5, 3
+    k = rng.standard_normal(dk)
+    k /= np.linalg.norm(k)
+    h0 = rng.standard_normal((1, 1, dk, dv))
+    kk = np.tile(k, (2, 1)).reshape(1, 2, 1, dk)
+    _, s1 = oracle.recurrence(np.zeros((1, 1, 1, dk)), kk[:, :1], np.zeros((1, 1, 1, dv)), np.zeros((1, 1, 1)),
+                              np.full((1, 1, 1), 2.0), 1.0, h0)
+    _, s2 = oracle.recurrence(np.zeros((1, 2, 1, dk)), kk, np.zeros((1, 2, 1, dv)), np.zeros((1, 2, 1)),
+                              np.full((1, 2, 1), 2.0), 1.0, h0)
+    assert np.allclose(s2, h0, atol=1e-14)
+    assert np.allclose(k @ s1[0, 0], -(k @ h0[0, 0]), atol=1e-14)
+    perp = np.eye(dk) - np.outer(k, k)
+    assert np.allclose(perp @ s1[0, 0], perp @ h0[0, 0], atol=1e-14)
+    assert abs(np.linalg.norm(s1) - np.linalg.norm(h0)) < 1e-13
+
 def test_test_time_sgd_identity():
     # S_t = S' - beta grad_S 1/2 |S k - v|^2 at S' = alpha S_{t-1} (TileLang page §1.3);
     # the gradient is taken by central finite differences, independent of any closed form
