@@ -204,7 +204,7 @@ def _oracle_inputs(x, heads):
     return arr
 
 
-def cpu_baseline(x, w, min_seconds=8.0, max_passes=5, heads=None):
+def cpu_baseline(x, w, min_seconds=10.0, max_passes=60, heads=None):
     """Time the fp64 oracle on the host cores (bounded sample of the workload); returns a dict."""
     import oracle
     heads = list(range(w.H)) if heads is None else heads
