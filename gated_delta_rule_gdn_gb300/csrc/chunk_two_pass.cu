@@ -118,27 +118,28 @@ struct Item {
     long it;      // workspace item index (slot * H + head)
 };
 
-// A CTA visits the virtual items slot * H + head = blockIdx.x, blockIdx.x + gridDim.x, ...; the cursor keeps
-// (slot, head) and the sequence whose slots begin at or before the slot (non-decreasing along the walk).
+// A CTA visits the virtual items slot * H + head = last - blockIdx.x, last - blockIdx.x - gridDim.x, ... (the last
+// slots first: the first chunks of every sequence are written last, and the state pass, which starts there, finds
+// them still in L2); the cursor keeps (slot, head) and the sequence whose slots begin at or before the slot
+// (non-increasing along the walk).
 struct Cursor {
     long s;
     int h, n;
 };
 
 __device__ __forceinline__ void cursor_step(Cursor& c, int ds, int dh, int H) {
-    c.h += dh;
-    c.s += ds;
-    if (c.h >= H) {
-        c.h -= H;
-        ++c.s;
+    c.h -= dh;
+    c.s -= ds;
+    if (c.h < 0) {
+        c.h += H;
+        --c.s;
     }
 }
 
-// The first valid item at or after the cursor (slots between sequences are unused); false past the last slot.
-__device__ bool cursor_next_valid(const Geo& g, long n_slots, Cursor& c, int ds, int dh, Item& x) {
-    const int N = g.N();
-    for (; c.s < n_slots; cursor_step(c, ds, dh, g.H)) {
-        while (c.n + 1 < N && g.slot0(c.n + 1) <= c.s) ++c.n;
+// The first valid item at or before the cursor (slots between sequences are unused); false below slot 0.
+__device__ bool cursor_next_valid(const Geo& g, Cursor& c, int ds, int dh, Item& x) {
+    for (; c.s >= 0; cursor_step(c, ds, dh, g.H)) {
+        while (c.n > 0 && g.slot0(c.n) > c.s) --c.n;
         long s0;
         int len;
         g.seq(c.n, s0, len);
@@ -645,9 +646,10 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
 
     const int ds = (int)(gridDim.x / H), dh = (int)(gridDim.x % H);
-    Cursor cur{(long)(blockIdx.x / H), (int)(blockIdx.x % H), 0};
+    const long first = p.n_slots * H - 1 - (long)blockIdx.x;
+    Cursor cur{first / H, (int)(first % H), p.geo.N() - 1};
     Item x;
-    bool have = cursor_next_valid(p.geo, p.n_slots, cur, ds, dh, x);
+    bool have = cursor_next_valid(p.geo, cur, ds, dh, x);
     float ng[2] = {0.f, 0.f}, nb[2] = {0.f, 0.f};   // g, beta of the next item (warp 1, in flight)
     uint32_t kq_issued = 0, kq_waited = 0, v_issued = 0, v_waited = 0;   // loader's count of load phases
     if (have) {
@@ -677,7 +679,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         Cursor nc = cur;
         cursor_step(nc, ds, dh, H);
         Item nx;
-        const bool have_next = cursor_next_valid(p.geo, p.n_slots, nc, ds, dh, nx);
+        const bool have_next = cursor_next_valid(p.geo, nc, ds, dh, nx);
         const uint32_t par = ic & 1;
         const int L = it.L;
         __syncthreads();   // [A] g and beta of this item are in shared memory; the previous item is retired
