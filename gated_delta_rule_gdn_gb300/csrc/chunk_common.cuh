@@ -41,6 +41,16 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 v, float (&f)[8]) {
     }
 }
 
+__device__ __forceinline__ void h8_to_f32(uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
 // Scaled copy of a row chunk of 8 bf16 values into 8 fp16 values (scale 0 writes exact zeros).
 __device__ __forceinline__ void copy_scaled_chunk(const uint8_t* src, uint8_t* dst, float s, bool zero) {
     float f[8];
@@ -101,9 +111,10 @@ __device__ __forceinline__ void stg_h8(uint8_t* p, const float* f) {
 }
 
 // Epilogue of D0 = [K; Q] K^T.  Rows 0-63 (token i): A[i][j] = beta_i 2^(lg_i - lg_j) (K K^T)_ij for j < i, in
-// fp32 for the solve, plus row i of the identity in [I; P].  Rows 64-127 (token i = row - 64):
+// fp32 for the solve, plus (IDENTITY) row i of the identity in [I; P].  Rows 64-127 (token i = row - 64):
 // P[i][j] = scale 2^(lg_i - lg_j) (Q K^T)_ij for j <= i, in fp16 in [I; P].  Column blocks wholly above the
 // diagonal for every row of the warp are skipped (warp-uniform); the solve never reads A above the diagonal.
+template <bool IDENTITY>
 __device__ __forceinline__ void epilogue_kkt(uint32_t tl, int row, int q4, int pw, const float* lg, const float* bb, float scale,
                                              float* Am, uint8_t* a1) {
     // this thread: row `row`, columns [32 pw, 32 pw + 32)
@@ -135,7 +146,7 @@ __device__ __forceinline__ void epilogue_kkt(uint32_t tl, int row, int q4, int p
         }
         const uint32_t one = (i & 1) ? 0x3C000000u : 0x00003C00u;     // fp16 1.0 in the low or high half
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < (IDENTITY ? 4 : 0); ++cc) {
             const int c8 = 4 * pw + cc;
             const bool here = (i >> 3) == c8;
             const int qw = (i & 7) >> 1;

@@ -421,7 +421,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             named_bar(1, NPREP);
             // epilogue 0: A (rows 0-63) to fp32 for the solve, P (rows 64-127) and the identity rows to A1
             tc_fence_after();
-            if (ok) epilogue_kkt(tl + d0, row, q4, pw, S.lg[s], S.bbuf[s], p.scale, Am, smem + OFF_A1);
+            if (ok) epilogue_kkt<true>(tl + d0, row, q4, pw, S.lg[s], S.bbuf[s], p.scale, Am, smem + OFF_A1);
             tc_fence_before();
             named_bar(1, NPREP);
             // MMA0 of the next chunk runs ahead into the other D0 buffer while this chunk is solved

@@ -58,16 +58,19 @@ constexpr int DVT = 64;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // workspace, per item
-constexpr uint32_t WS_WQ = 32768;   // [W; Q'] fp16 K-major 128 x 128, two 64-column slabs, 128-byte swizzle
+constexpr uint32_t WS_WQ = 32768;   // [Q^; W] fp16 K-major 128 x 128 (rows 0-63 Q^ = scale gamma Q, rows 64-127 W), two
+                                    // 64-column slabs, 128-byte swizzle
 constexpr uint32_t WS_KT = 16384;   // Ktilde fp16 [j][c] 64 x 128, two 64-column slabs, 128-byte swizzle
-constexpr uint32_t WS_UU = 32768;   // per d_v half: [U; U'] fp16 128 rows x 64 columns, rows 128 B, 16-byte chunks swizzled
+constexpr uint32_t WS_U = 16384;    // U fp16, two d_v halves of 64 rows x 64 columns (rows 128 B, 16-byte chunks swizzled)
+constexpr uint32_t WS_P = 8192;     // P fp16 K-major 64 x 64, 128-byte swizzle
 constexpr uint32_t WS_GC = 512;     // gamma_C per d_k row (fp32)
-constexpr size_t WS_ITEM = (size_t)WS_WQ + WS_KT + WS_UU + WS_GC;
+constexpr size_t WS_ITEM = (size_t)WS_WQ + WS_KT + WS_U + WS_P + WS_GC;
 
 struct Ws {
     uint8_t* wq;
     uint8_t* kt;
-    uint8_t* uu;
+    uint8_t* u;
+    uint8_t* pp;
     float* gc;
 };
 
@@ -161,8 +164,8 @@ constexpr uint32_t I_KQ = 0;        // [K; Q] rows, two K-slabs of 16 KB (K rows
 constexpr uint32_t I_B2 = 32768;    // X = [beta V | beta gamma K], fp16 MN-major 64 x 256 in four 8 KB slabs.  GDN: V
                                     // lands in slabs 0-1 by TMA (bf16) and is scaled there in place.  KDA: the
                                     // [64][128] fp32 gate tile lands here first
-constexpr uint32_t I_A1 = 65536;    // [I; P] then [T; -PT], fp16 K-major 128 x 64
-constexpr uint32_t I_B1 = 81920;    // T, fp16 MN-major [j][n] 64 x 64 (the solve's scratch before that)
+constexpr uint32_t I_A1 = 65536;    // [-; P] (rows 64-127, copied to the workspace) then [T; T], fp16 K-major 128 x 64
+constexpr uint32_t I_B1 = 81920;    // the solve's scratch
 constexpr uint32_t I_AM = 90112;    // fp32 A, then T in place (row stride TS)
 constexpr uint32_t I_RT = I_B1;
 constexpr uint32_t I_END = I_AM + 64 * TS * 4;
@@ -176,7 +179,7 @@ constexpr uint32_t I_FF = I_EF + 64 * ES * 4;         // F = exp(R_block - G) (f
 struct ISmall {
     uint64_t full_kq;         // K, Q of the item landed (TMA transaction bytes)
     uint64_t full_v;          // V (and the KDA gate tile) of the item landed
-    uint64_t m0, m1, m2;
+    uint64_t m0, m2;
     uint32_t tmem_base;
     uint32_t pad;
     float gbuf[C];            // g of the item (0 past the end; scalar gate)
@@ -202,9 +205,8 @@ constexpr uint32_t I_KSMALL = I_SMALL_KDA + ((sizeof(ISmall) + 127) & ~127u);   
 constexpr uint32_t I_SMEM_GDN = I_SMALL_GDN + sizeof(ISmall) + 1024;
 constexpr uint32_t I_SMEM_KDA = I_KSMALL + sizeof(KSmall) + 1024;
 static_assert(I_SMEM_KDA <= 227 * 1024, "KDA intra kernel shared memory");
-// D2 = [U | W; -U' | Q'] spans all 256 columns: columns 128-255 hold [0; scale gamma Q] before MMA2 accumulates
-// onto them, columns 0-127 (D0 and D1 until then) are zeroed once D1 has been read
-constexpr uint32_t I_TM_D0 = 0, I_TM_D1 = 64, I_TM_D2 = 0, I_TM_QS = 128, I_TM_COLS = 256;
+// D2 = [T; T] [beta V | beta gamma K] = [U | W; U | W] spans all 256 columns (D0 is read before MMA2 is issued)
+constexpr uint32_t I_TM_D0 = 0, I_TM_D2 = 0, I_TM_COLS = 256;
 constexpr int I_THREADS = 256;
 // largest |cumulative gate - block reference| (log2 units) for the factored KDA products: 2^100 keeps every
 // factor and a 128-term sum of their products inside fp32
@@ -464,7 +466,7 @@ __device__ __forceinline__ void ld_f32_chunks(const float* row, int t, float (&f
 }
 
 // KDA, fast path: A = diag(beta)(K K^T with per-channel decays) strictly lower -> Am (fp32) and P = scale (Q K^T with
-// decays) lower incl. the diagonal -> A1 rows 64-127, plus the identity rows of A1.  TF32 warp MMAs over the 128
+// decays) lower incl. the diagonal -> A1 rows 64-127.  TF32 warp MMAs over the 128
 // channels, with the channel (reduction) order permuted so that lane quad t owns the 32 channels of ld_bf16_chunks:
 // step ks reduces over its channels 2 ks and 2 ks + 1 (the same permutation on both operands leaves the sum alone),
 // which makes every operand load a 16-byte vector.  For row block a against column block b <= a:
@@ -552,17 +554,6 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
                 *reinterpret_cast<float4*>(Am + zr * TS + zc) = make_float4(0.f, 0.f, 0.f, 0.f);
                 *reinterpret_cast<float4*>(Am + zr * TS + zc + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            // identity rows 16 a .. 16 a + 15 of A1: lane -> row 16 a + lane / 2, columns 32 (lane % 2) .. + 31
-            const int ir = 16 * a + (lane >> 1);
-            const uint32_t one = (ir & 1) ? 0x3C000000u : 0x00003C00u;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int c8 = 4 * (lane & 1) + q;
-                const bool here = (ir >> 3) == c8;
-                const int qw = (ir & 7) >> 1;
-                st16(a1 + sw128_off(ir, c8 * 8), here && qw == 0 ? one : 0u, here && qw == 1 ? one : 0u,
-                     here && qw == 2 ? one : 0u, here && qw == 3 ? one : 0u);
-            }
         } else {
             for (int e = lane; e < (3 - a) * 16 * 2; e += 32) {   // 16 rows x (3 - a) blocks x two 8-column chunks
                 const int zr = 16 * a + (e & 15), zc = 16 * (a + 1) + 8 * (e >> 4);
@@ -572,7 +563,7 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
     }
 }
 
-// KDA, fallback: the same A, P and identity rows, every term with its own exponential of the gate difference
+// KDA, fallback: the same A and P, every term with its own exponential of the gate difference
 // (G in log2 units is in F).  Exact for any gate; used only when some block's spread is too large.
 __device__ void kda_products_direct(uint8_t* smem, const float* bb, float scale, int tid) {
     const float* G = reinterpret_cast<const float*>(smem + I_FF);
@@ -592,7 +583,6 @@ __device__ void kda_products_direct(uint8_t* smem, const float* bb, float scale,
         }
         Am[i * TS + j] = j < i ? bb[i] * ak : 0.f;
         *reinterpret_cast<__half*>(a1 + sw128_off(64 + i, j)) = __float2half_rn(j <= i ? scale * aq : 0.f);
-        *reinterpret_cast<__half*>(a1 + sw128_off(i, j)) = __float2half_rn(i == j ? 1.f : 0.f);
     }
 }
 
@@ -635,7 +625,6 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         mbar_init(&S.full_kq, 1);
         mbar_init(&S.full_v, 1);
         mbar_init(&S.m0, 1);
-        mbar_init(&S.m1, 1);
         mbar_init(&S.m2, 1);
         fence_mbar_init();
     }
@@ -706,38 +695,29 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             if (lane == 0) bulk_wait_read();   // the previous item's staging rows (X, A1) have been read
             __syncthreads();   // [B] gate prefix ready
             if (ok) {
-                // beta gamma K -> X slabs 2-3 and Ktilde = (gamma_C / gamma) K -> workspace.  Operation e = tid + 256
-                // cc moves the 16 bytes at physical position (slab, row, pos) of the K tile; consecutive lanes take
-                // consecutive positions, so the workspace writes are coalesced (the layouts share the swizzle).
+                // beta gamma K -> X slabs 2-3, Ktilde = (gamma_C / gamma) K and Q^ = scale gamma Q -> workspace.
+                // Operation e = tid + 256 cc moves the 16 bytes at physical position (slab, row, pos) of the K and Q
+                // tiles; consecutive lanes take consecutive positions, so the workspace writes are coalesced (the
+                // layouts share the swizzle).
                 uint8_t* kt = ws.kt + (size_t)it.it * WS_KT;
+                uint8_t* wq = ws.wq + (size_t)it.it * WS_WQ;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int e = tid + 256 * cc, slab = e >> 9, r = (e >> 3) & 63;
                     const uint32_t off = (uint32_t)(r * 128 + (e & 7) * 16);
                     const uint32_t m = r < L ? 0xFFFFFFFFu : 0u;   // exact zeros for rows past the end
-                    float f[8];
+                    float f[8], g8[8];
                     bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + off), f);
+                    bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + 8192 + off), g8);
                     const uint4 xk = scale_chunk_h(f, S.bbuf[r] * S.gam[r], m), kd = scale_chunk_h(f, S.kdec[r], m);
+                    const uint4 qh = scale_chunk_h(g8, p.scale * S.gam[r], m);
                     st16(smem + I_B2 + 16384 + slab * 8192 + off, xk.x, xk.y, xk.z, xk.w);
                     stg16(kt + slab * 8192 + off, kd.x, kd.y, kd.z, kd.w);
+                    stg16(wq + slab * 16384 + off, qh.x, qh.y, qh.z, qh.w);
                 }
                 if (warp == 3) {
                     const float gc = S.gC;
                     __stcg(reinterpret_cast<float4*>(ws.gc + (size_t)it.it * 128) + lane, make_float4(gc, gc, gc, gc));
-                }
-                // columns 128-255 := [0; scale gamma Q] (rows 64-127: token row - 64), 64 columns of half pw
-                const float qs = row >= 64 ? p.scale * S.gam[row - 64] : 0.f;
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[16];
-#pragma unroll
-                    for (int h8 = 0; h8 < 2; ++h8) {
-                        float f[8];
-                        bf16x8_to_f32(ld16(smem + I_KQ + pw * 16384 + sw128_off(row, cb * 16 + h8 * 8)), f);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) r[h8 * 8 + q] = __float_as_uint(qs * f[q]);
-                    }
-                    tmem_st16(tl + I_TM_QS + pw * 64 + cb * 16, r);
                 }
             }
             if (ok) ok = mbar_wait(&S.full_v, par, kWaitNs);
@@ -768,7 +748,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx, p.group);
                 kq_issued = ic + 2;
             }
-            if (ok) epilogue_kkt(tl + I_TM_D0, row, q4, pw, S.lg, S.bbuf, p.scale, Am, smem + I_A1);
+            if (ok) epilogue_kkt<false>(tl + I_TM_D0, row, q4, pw, S.lg, S.bbuf, p.scale, Am, smem + I_A1);
+            fence_async_smem();   // P (rows 64-127 of A1) is read by the bulk copy to the workspace
             tc_fence_before();
             __syncthreads();
         } else {
@@ -786,22 +767,25 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (fast) kda_products_fast(smem, KS, S.bbuf, p.scale, warp, lane);
                 else kda_products_direct(smem, S.bbuf, p.scale, tid);
             }
-            // X = [beta V | beta 2^G K] and Ktilde = 2^(G_last - G) K (coalesced, as in the scalar-gate path)
+            // X = [beta V | beta 2^G K], Ktilde = 2^(G_last - G) K and Q^ = scale 2^G Q (coalesced, as in the scalar-gate
+            // path)
             if (ok) {
                 const float* E = reinterpret_cast<const float*>(smem + I_EF);
                 const float* F = reinterpret_cast<const float*>(smem + I_FF);
                 uint8_t* kt = ws.kt + (size_t)it.it * WS_KT;
+                uint8_t* wq = ws.wq + (size_t)it.it * WS_WQ;
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
                     const int e = tid + 256 * cc, slab = e >> 9, r = (e >> 3) & 63, pos = e & 7;
                     const int c = slab * 64 + ((pos ^ (r & 7)) << 3), a = r >> 4;
                     const uint32_t off = (uint32_t)(r * 128 + pos * 16);
                     const uint32_t m = r < L ? 0xFFFFFFFFu : 0u;
-                    float f[8], v[8], eg[8], ek[8];
+                    float f[8], v[8], qv[8], eg[8], ek[8], eq[8];
                     bf16x8_to_f32(ld16(smem + I_VB + slab * 8192 + off), v);
                     const uint4 xv = scale_chunk_h(v, S.bbuf[r], m);
                     st16(smem + I_B2 + slab * 8192 + off, xv.x, xv.y, xv.z, xv.w);
                     bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + off), f);
+                    bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + 8192 + off), qv);
                     if (fast) {
                         float e8[8], f8[8], er[8], el[8];
                         ld_f8(E + r * ES + c, e8);
@@ -810,7 +794,9 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         ld_f8(&KS.espl[a][c], el);
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
-                            eg[q] = S.bbuf[r] * (e8[q] * er[q]);
+                            const float g2 = e8[q] * er[q];   // 2^(G - R_a) 2^(R_a)
+                            eg[q] = S.bbuf[r] * g2;
+                            eq[q] = p.scale * g2;
                             ek[q] = f8[q] * el[q];   // 2^(R_a - G) 2^(G_last - R_a)
                         }
                     } else {
@@ -819,45 +805,16 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         ld_f8(&KS.lg63[c], l8);
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
-                            eg[q] = S.bbuf[r] * ex2(g8[q]);
+                            const float g2 = ex2(g8[q]);
+                            eg[q] = S.bbuf[r] * g2;
+                            eq[q] = p.scale * g2;
                             ek[q] = ex2(l8[q] - g8[q]);
                         }
                     }
-                    const uint4 xk = scale_chunk_hv(f, eg, m), kd = scale_chunk_hv(f, ek, m);
+                    const uint4 xk = scale_chunk_hv(f, eg, m), kd = scale_chunk_hv(f, ek, m), qh = scale_chunk_hv(qv, eq, m);
                     st16(smem + I_B2 + 16384 + slab * 8192 + off, xk.x, xk.y, xk.z, xk.w);
                     stg16(kt + slab * 8192 + off, kd.x, kd.y, kd.z, kd.w);
-                }
-                // columns 128-255 := [0; scale 2^G Q], 64 columns of half pw
-                const int i = row - 64, a = (row >= 64 ? i : 0) >> 4;
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[16];
-#pragma unroll
-                    for (int h8 = 0; h8 < 2; ++h8) {
-                        const int c = pw * 64 + cb * 16 + h8 * 8;
-                        float f[8], s8[8];
-                        if (row >= 64) {
-                            bf16x8_to_f32(ld16(smem + I_KQ + pw * 16384 + sw128_off(row, cb * 16 + h8 * 8)), f);
-                            if (fast) {
-                                float e8[8], er[8];
-                                ld_f8(E + i * ES + c, e8);
-                                ld_f8(&KS.er[a][c], er);
-#pragma unroll
-                                for (int q = 0; q < 8; ++q) s8[q] = p.scale * (e8[q] * er[q]);
-                            } else {
-                                float g8[8];
-                                ld_f8(F + i * ES + c, g8);
-#pragma unroll
-                                for (int q = 0; q < 8; ++q) s8[q] = p.scale * ex2(g8[q]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) f[q] = s8[q] = 0.f;
-                        }
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) r[h8 * 8 + q] = __float_as_uint(s8[q] * f[q]);
-                    }
-                    tmem_st16(tl + I_TM_QS + pw * 64 + cb * 16, r);
+                    stg16(wq + slab * 16384 + off, qh.x, qh.y, qh.z, qh.w);
                 }
             }
             fence_async_smem();
@@ -870,9 +827,16 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 kq_issued = ic + 2;
             }
         }
+        // P (rows 64-127 of A1, fp16 K-major) to the workspace, one bulk copy; its rows are overwritten with T below
+        if (ok && tid == 96) {
+            bulk_s2g(ws.pp + (size_t)it.it * WS_P, smem + I_A1 + 8192, WS_P);
+            bulk_commit();
+        }
         // UT transform, T = (I + A)^{-1} in place
         solve_unit_lower_inplace(Am, Rt, tid, ok);
-        // T to fp16, MN-major [j][n] (operand B of MMA1)
+        if (tid == 96) bulk_wait_read();
+        __syncthreads();   // the copy of P has read A1
+        // T to fp16 into both halves of A1: [T; T], K-major (operand A of MMA2)
         if (ok) {
 #pragma unroll
             for (int k2 = 0; k2 < 2; ++k2) {
@@ -882,59 +846,22 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 float gq[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) gq[q] = (c8 * 8 + q <= j) ? f[q] : 0.f;
-                st_h8(smem + I_B1 + sw128_off(j, c8 * 8), gq);
+                st_h8(smem + I_A1 + sw128_off(j, c8 * 8), gq);
+                st_h8(smem + I_A1 + sw128_off(64 + j, c8 * 8), gq);
             }
         }
         fence_async_smem();
-        __syncthreads();
-        // MMA1: D1 = [I; P] T
-        if (ok && leader) {
-            tc_fence_after();
-            const uint32_t id = idesc_f16(128, 64, false, false, true);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16(tmem + I_TM_D1, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
-                        sdesc(sbase + I_B1 + ks * 2048, 8192, 1024), id, ks > 0);
-            mma_commit(&S.m1);
-        }
-        // epilogue 1: [T; -PT] to fp16 into A1 (operand A of MMA2); columns [32 pw, 32 pw + 32)
-        if (ok) ok = mbar_wait(&S.m1, par, kWaitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && tid == 0) set_status(8u);
-        tc_fence_after();
-        if (ok) {
-            uint32_t r[2][16];
-            tmem_ld16(tl + I_TM_D1 + 32 * pw, r[0]);
-            tmem_ld16(tl + I_TM_D1 + 32 * pw + 16, r[1]);
-            tmem_ld_wait();
-            const float sg = row < 64 ? 1.f : -1.f;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float f[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) f[q] = sg * __uint_as_float(r[cc >> 1][(cc & 1) * 8 + q]);
-                st_h8(smem + I_A1 + sw128_off(row, 32 * pw + cc * 8), f);
-            }
-            // zero the D0 and D1 columns this warp has read (MMA2 accumulates into columns 0-127)
-            const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                tmem_st16(tl + I_TM_D0 + 32 * pw + 16 * cb, z);
-                tmem_st16(tl + I_TM_D1 + 32 * pw + 16 * cb, z);
-            }
-        }
-        fence_async_smem();
-        tmem_st_wait();
         tc_fence_before();
         __syncthreads();
-        // MMA2: D2 += [T; -PT] [beta V | beta gamma K] -> [U | W; -U' | Q'], one N = 256 product
+        // MMA2: D2 = [T; T] [beta V | beta gamma K] -> [U | W; U | W], one N = 256 product (both halves of the rows
+        // alike, so that every warp's TMEM lane quarter holds a share of the epilogue)
         if (ok && leader) {
             tc_fence_after();
             const uint32_t id = idesc_f16(128, 256, false, false, true);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_f16(tmem + I_TM_D2, sdesc(sbase + I_A1 + ks * 32, 16, 1024),
-                        sdesc(sbase + I_B2 + ks * 2048, 8192, 1024), id, 1);
+                        sdesc(sbase + I_B2 + ks * 2048, 8192, 1024), id, ks > 0);
             mma_commit(&S.m2);
         }
         if (ok) ok = mbar_wait(&S.m2, par, kWaitNs);
@@ -945,42 +872,36 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             v_issued = ic + 2;
         }
         tc_fence_after();
-        // epilogue 2: [W; Q'] and [U; U'] of column half pw to the workspace.  Each warp stages its 32 rows
-        // (4 KB, the workspace's swizzled row layout) in shared memory nothing reads or loads into any more this
-        // item (A1 after MMA2; the beta gamma K half of X for the scalar gate, whose next V lands in the other half;
-        // the E table for KDA, whose next gate tile fills all of X), then writes them out as 512-byte runs.
+        // epilogue 2: U and W to the workspace, one 32-row x 64-column tile per warp.  D2's two row halves are alike,
+        // so warp (q4, pw) takes token rows 32 (q4 % 2) .. + 31 of column quarter 2 (q4 / 2) + pw: U of d_v half 0 or
+        // 1, W of d_k slab 0 or 1.  It stages the tile (4 KB, the workspace's swizzled row layout) in shared memory
+        // nothing reads or loads into any more this item (A1 after MMA2; the beta gamma K half of X for the scalar
+        // gate, whose next V lands in the other half; the E table for KDA, whose next gate tile fills all of X), then
+        // writes it out as 512-byte runs.
         if (ok) {
             uint8_t* stg = smem + (pw == 0 ? I_A1 : (KDA ? I_EF : I_B2 + 16384)) + q4 * 4096;
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t tcol = which == 0 ? 128 + pw * 64 : pw * 64;        // [W; Q'] then [U; -U']
-                const float sg = (which == 1 && row >= 64) ? -1.f : 1.f;
-                uint8_t* dst = (which == 0 ? ws.wq + (size_t)it.it * WS_WQ : ws.uu + (size_t)it.it * WS_UU) +
-                               pw * 16384 + q4 * 4096;
-                if (which == 1) {   // the bulk copy of [W; Q'] has read the staging rows
-                    if (lane == 0) bulk_wait_read();
-                    __syncwarp();
-                }
+            const int rh = q4 & 1, cq = ((q4 >> 1) << 1) | pw;
+            uint8_t* dst = cq < 2 ? ws.u + (size_t)it.it * WS_U + cq * 8192 + rh * 4096
+                                  : ws.wq + (size_t)it.it * WS_WQ + (cq - 2) * 16384 + 8192 + rh * 4096;
 #pragma unroll
-                for (int cp = 0; cp < 2; ++cp) {
-                    uint32_t r[2][16];
-                    tmem_ld16(tl + I_TM_D2 + tcol + cp * 32, r[0]);
-                    tmem_ld16(tl + I_TM_D2 + tcol + cp * 32 + 16, r[1]);
-                    tmem_ld_wait();
+            for (int cp = 0; cp < 2; ++cp) {
+                uint32_t r[2][16];
+                tmem_ld16(tl + I_TM_D2 + cq * 64 + cp * 32, r[0]);
+                tmem_ld16(tl + I_TM_D2 + cq * 64 + cp * 32 + 16, r[1]);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int h8 = 0; h8 < 4; ++h8) {
-                        float f[8];
+                for (int h8 = 0; h8 < 4; ++h8) {
+                    float f[8];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) f[q] = sg * __uint_as_float(r[h8 >> 1][(h8 & 1) * 8 + q]);
-                        st_h8(stg + sw128_off(lane, cp * 32 + h8 * 8), f);
-                    }
+                    for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[h8 >> 1][(h8 & 1) * 8 + q]);
+                    st_h8(stg + sw128_off(lane, cp * 32 + h8 * 8), f);
                 }
-                fence_async_smem();   // the staging rows are read by the bulk-copy engine
-                __syncwarp();
-                if (lane == 0) {
-                    bulk_s2g(dst, stg, 4096);
-                    bulk_commit();
-                }
+            }
+            fence_async_smem();   // the staging rows are read by the bulk-copy engine
+            __syncwarp();
+            if (lane == 0) {
+                bulk_s2g(dst, stg, 4096);
+                bulk_commit();
             }
         }
         tc_fence_before();
@@ -1016,20 +937,23 @@ struct StateParams {
     Ws ws;
 };
 
-// Shared memory of pass 2.  Narrow: one CTA per (sequence, head, 64-column d_v half), 4 warps.  Wide: one CTA per
-// (sequence, head) over all 128 columns, 8 warps (two per TMEM lane quarter, one per 64-column half), for workloads
-// with more chains than one CTA per SM can hold at once.
-template <bool WIDE>
+// Pass 2: one CTA per (sequence, head, 64-column d_v half), 4 warps; warp w reads TMEM lane quarter w.  Per chunk
+// (its workspace slot streamed by bulk copies through a two-stage ring):
+//   MMA3   D3 = [Q^; W] h~ : rows 0-63 Q^ h~ (for O), rows 64-127 W h~
+//   Delta = U - W h~ (lane quarters 2-3), to fp16 in shared memory
+//   MMA4   D4 = Ktilde^T Delta, and MMA5  D5 = P Delta (rows 0-63; an M = 128 product whose rows 64-127 read past P
+//          into U and are never used)
+//   h <- gamma_C h + D4 (all lanes: row d_k), fp16 copy h~ for the next MMA3
+//   O = Q^ h~ + P Delta (lane quarters 0-1), written one chunk later, while the next MMA3 runs (D3 and D5 are
+//   double-buffered by chunk parity)
 struct SLayout {
-    static constexpr uint32_t NCOL = WIDE ? 128 : 64;             // d_v columns of the CTA
-    static constexpr uint32_t WQ = 0, KT = 32768, UU = 49152;
-    static constexpr uint32_t GC = UU + NCOL * 256;                // [U; U'] of the CTA's columns: 16 KB per half
-    static constexpr uint32_t STAGE = (GC + 512 + 1023) & ~1023u;  // one workspace slot
-    static constexpr uint32_t H = 2 * STAGE;                       // h, fp16 MN-major [d][n], 16 KB per half
-    static constexpr uint32_t D = H + NCOL * 256;                  // Delta, fp16 MN-major [j][n], 8 KB per half
-    static constexpr uint32_t SMALL = D + NCOL * 128;
-    static constexpr int THREADS = WIDE ? 256 : 128;
-    static constexpr uint32_t TM_D3 = 0, TM_D4 = NCOL, TM_COLS = 2 * NCOL;
+    static constexpr uint32_t WQ = 0, KT = 32768, PP = 49152, U = 57344, GC = 65536;   // one workspace slot
+    static constexpr uint32_t STAGE = 66560;
+    static constexpr uint32_t H = 2 * STAGE;         // h~, fp16 MN-major [d][n] 128 x 64
+    static constexpr uint32_t D = H + 16384;         // Delta, fp16 MN-major [j][n] 64 x 64
+    static constexpr uint32_t SMALL = D + 8192;
+    static constexpr int THREADS = 128;
+    static constexpr uint32_t TM_D3 = 0, TM_D4 = 128, TM_D5 = 192, TM_COLS = 512;   // D3, D5: two each
 };
 struct SSmall {
     uint64_t full[2];
@@ -1037,25 +961,22 @@ struct SSmall {
     uint32_t tmem_base;
     uint32_t pad;
 };
-template <bool WIDE>
-constexpr uint32_t s_smem_bytes() { return SLayout<WIDE>::SMALL + sizeof(SSmall) + 1024; }
-static_assert(s_smem_bytes<true>() <= 227 * 1024, "wide state kernel shared memory");
+constexpr uint32_t s_smem_bytes() { return SLayout::SMALL + sizeof(SSmall) + 1024; }
+static_assert(s_smem_bytes() <= 227 * 1024, "state kernel shared memory");
 
 struct Chain {
     int n, h, half, len;
     long row0;
 };
 
-// CTA -> (sequence, head, d_v half or both); packed sequences longest first (their chains are the longest serial
-// paths)
-template <bool WIDE>
+// CTA -> (sequence, head, d_v half); packed sequences longest first (their chains are the longest serial paths)
 __device__ Chain resolve_chain(const Geo& g) {
     Chain c;
-    const int per_seq = g.H * (WIDE ? 1 : 2);
+    const int per_seq = g.H * 2;
     const int seq_rank = blockIdx.x / per_seq;
     const int rem = blockIdx.x % per_seq;
-    c.h = WIDE ? rem : rem / 2;
-    c.half = WIDE ? 0 : rem % 2;
+    c.h = rem / 2;
+    c.half = rem % 2;
     int n = seq_rank;
     if (g.cu && g.n_seqs <= 32) {
         const int lane = threadIdx.x & 31;
@@ -1080,20 +1001,63 @@ __device__ Chain resolve_chain(const Geo& g) {
     return c;
 }
 
-template <bool WIDE>
 __device__ __forceinline__ void state_issue(uint8_t* smem, SSmall& S, const Ws& ws, long it, int half, int s) {
-    using LY = SLayout<WIDE>;
+    using LY = SLayout;
     uint8_t* st = smem + s * LY::STAGE;
-    mbar_arrive_expect_tx(&S.full[s], WS_WQ + WS_KT + LY::NCOL * 256 + WS_GC);
+    mbar_arrive_expect_tx(&S.full[s], WS_WQ + WS_KT + WS_P + 8192 + WS_GC);
     bulk_g2s(st + LY::WQ, ws.wq + (size_t)it * WS_WQ, WS_WQ, &S.full[s]);
     bulk_g2s(st + LY::KT, ws.kt + (size_t)it * WS_KT, WS_KT, &S.full[s]);
-    bulk_g2s(st + LY::UU, ws.uu + (size_t)it * WS_UU + half * 16384, LY::NCOL * 256, &S.full[s]);
+    bulk_g2s(st + LY::PP, ws.pp + (size_t)it * WS_P, WS_P, &S.full[s]);
+    bulk_g2s(st + LY::U, ws.u + (size_t)it * WS_U + half * 8192, 8192, &S.full[s]);
     bulk_g2s(st + LY::GC, ws.gc + (size_t)it * 128, WS_GC, &S.full[s]);
 }
 
-template <bool O_F32, bool WIDE>
-__global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(const StateParams p) {
-    using LY = SLayout<WIDE>;
+// O = Q^ h~ + P Delta of chunk t (token rows 0-63: lane quarters 0 and 1), from D3 and D5 of its parity
+template <bool O_F32>
+__device__ __forceinline__ void state_output(const StateParams& p, const Chain& ch, uint32_t tl, int t, int row) {
+    using LY = SLayout;
+    const int L = min(C, ch.len - t * C);
+    const size_t orow = ((size_t)(ch.row0 + (long)t * C + row) * p.geo.H + ch.h) * DV + ch.half * DVT;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {   // 32 columns per pass: four loads, one wait
+        uint32_t a[2][16], b[2][16];
+        tmem_ld16(tl + LY::TM_D3 + (t & 1) * 64 + h2 * 32, a[0]);
+        tmem_ld16(tl + LY::TM_D3 + (t & 1) * 64 + h2 * 32 + 16, a[1]);
+        tmem_ld16(tl + LY::TM_D5 + (t & 1) * 64 + h2 * 32, b[0]);
+        tmem_ld16(tl + LY::TM_D5 + (t & 1) * 64 + h2 * 32 + 16, b[1]);
+        tmem_ld_wait();
+        if (row < L) {
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+                float f[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) f[k] = __uint_as_float(a[hq][k]) + __uint_as_float(b[hq][k]);
+                const size_t o0 = orow + h2 * 32 + hq * 16;
+                if (O_F32) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + o0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + o0);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * q + 2 * m], f[8 * q + 2 * m + 1]);
+                            pk[m] = *reinterpret_cast<uint32_t*>(&b2);
+                        }
+                        dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <bool O_F32>
+__global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const StateParams p) {
+    using LY = SLayout;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
@@ -1101,17 +1065,16 @@ __global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, pw = warp >> 2;    // TMEM lane quarter; 64-column half within the CTA (wide only)
-    const Chain ch = resolve_chain<WIDE>(p.geo);
+    const int q4 = warp;                        // TMEM lane quarter
+    const Chain ch = resolve_chain(p.geo);
     const int n_chunks = (ch.len + C - 1) / C;
     const long slot0 = ch.row0 / C + ch.n;
     const int H = p.geo.H;
-    const int row = 32 * q4 + lane;             // TMEM lane: token row of D3, d_k row of D4 and of h
-    const bool leader = (tid == 0);
-    const bool issuer = (tid == 32);            // issues the copies, off the MMA thread's path
-    const bool delta_warp = q4 < 2;
-    const int col0 = (WIDE ? pw : ch.half) * DVT;   // first d_v column of this thread in the full head
-    const uint32_t cs = WIDE ? pw * 64 : 0;         // this thread's column offset inside the CTA's tiles
+    const int row = 32 * q4 + lane;             // TMEM lane: token row of D3 and D5, d_k row of D4 and of h
+    const bool leader = (tid == 64);            // issues the products (a Delta warp)
+    const bool issuer = (tid == 32);            // issues the copies, off the leader's path
+    const bool out_warp = q4 < 2;               // O (token rows 0-63); the others form Delta (rows 64-127)
+    const int col0 = ch.half * DVT;
 
     if (warp == 0) {
         tmem_alloc(&S.tmem_base, LY::TM_COLS);
@@ -1131,8 +1094,7 @@ __global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
 
     if (issuer) {
-        for (int t = 0; t < 2 && t < n_chunks; ++t)
-            state_issue<WIDE>(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
+        for (int t = 0; t < 2 && t < n_chunks; ++t) state_issue(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
     }
     int issued = n_chunks < 2 ? n_chunks : 2;
 
@@ -1146,9 +1108,9 @@ __global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(
         hreg[4 * q + 2] = v.z;
         hreg[4 * q + 3] = v.w;
     }
-    // h to fp16, MN-major [d][n] (operand B of MMA3), one 16 KB slab per 64-column half
+    // h to fp16, MN-major [d][n] (operand B of MMA3)
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + LY::H + cs * 256 + sw128_off(row, c8 * 8), hreg + c8 * 8);
+    for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + LY::H + sw128_off(row, c8 * 8), hreg + c8 * 8);
     fence_async_smem();
     __syncthreads();
 
@@ -1156,96 +1118,66 @@ __global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(
     // lie below 256 KB, so the field never carries).
     const uint64_t dH = sdesc(sbase + LY::H, 16384, 1024), dD = sdesc(sbase + LY::D, 8192, 1024);
     const uint64_t dWQ = sdesc(sbase + LY::WQ, 16, 1024), dKT = sdesc(sbase + LY::KT, 8192, 1024);
-    const uint32_t id3 = idesc_f16(128, LY::NCOL, false, false, true), id4 = idesc_f16(128, LY::NCOL, false, true, true);
+    const uint64_t dP = sdesc(sbase + LY::PP, 16, 1024);
+    const uint32_t id3 = idesc_f16(128, 64, false, false, true), id4 = idesc_f16(128, 64, false, true, true);
     bool ok = true;
     int waited = 0;   // chunks whose stage wait completed
     for (int t = 0; t < n_chunks; ++t) {
         const int s = t & 1;
         const uint8_t* st = smem + s * LY::STAGE;
         const uint64_t so = (uint64_t)((s * LY::STAGE) >> 4);
-        const int L = min(C, ch.len - t * C);
         if (ok) ok = mbar_wait(&S.full[s], (t >> 1) & 1, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(32u);
         if (ok) waited = t + 1;
-        // MMA3: D3 = [W; Q'] h
+        // MMA3: D3[t & 1] = [Q^; W] h~
         if (ok && leader) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_f16(tmem + LY::TM_D3, dWQ + so + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), dH + (uint64_t)(ks * 128),
-                        id3, ks > 0);
+                mma_f16(tmem + LY::TM_D3 + s * 64, dWQ + so + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                        dH + (uint64_t)(ks * 128), id3, ks > 0);
             mma_commit(&S.m3);
         }
+        // meanwhile the output of the previous chunk (its D3 and D5 are the other parity)
+        if (ok && out_warp && t > 0) state_output<O_F32>(p, ch, tl, t - 1, row);
         if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(64u);
         tc_fence_after();
-        const int i = row - 64;
-        const bool store_o = !delta_warp && i < L;
-        const size_t orow = ((size_t)(ch.row0 + (long)t * C + (row & 63)) * H + ch.h) * DV + col0;
-#pragma unroll
-        for (int hp = 0; hp < 4; ++hp) {
-            uint32_t a[16];
-            float u[16];
+        if (!out_warp) {
+            // Delta = U - W h~ (token row i = row - 64) to fp16 MN-major [j][n] (operand B of MMA4 and MMA5)
+            const int i = row - 64;
             if (ok) {
-                tmem_ld16(tl + LY::TM_D3 + cs + hp * 16, a);
 #pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {
-                    const uint4 v = ld16(st + LY::UU + cs * 256 + sw128_off(row, hp * 16 + h8 * 8));
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t a[2][16];
+                    tmem_ld16(tl + LY::TM_D3 + s * 64 + h2 * 32, a[0]);
+                    tmem_ld16(tl + LY::TM_D3 + s * 64 + h2 * 32 + 16, a[1]);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&w4[m]));
-                        u[h8 * 8 + 2 * m] = f2.x;
-                        u[h8 * 8 + 2 * m + 1] = f2.y;
-                    }
-                }
-                tmem_ld_wait();
-            }
-            if (ok && delta_warp) {
-                // Delta = U - W h (token rows 0-63) to fp16 MN-major [j][n] (operand B of MMA4)
+                    for (int h8 = 0; h8 < 4; ++h8) {
+                        float u[8], f[8];
+                        h8_to_f32(ld16(st + LY::U + sw128_off(i, h2 * 32 + h8 * 8)), u);
 #pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {
-                    float f[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) f[q] = u[h8 * 8 + q] - __uint_as_float(a[h8 * 8 + q]);
-                    st_h8(smem + LY::D + cs * 128 + sw128_off(row, hp * 16 + h8 * 8), f);
-                }
-            } else if (ok && store_o) {
-                // O = U' + Q' h (token rows 64-127)
-                float f[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) f[k] = u[k] + __uint_as_float(a[k]);
-                if (O_F32) {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + hp * 16);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
-                } else {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow + hp * 16);
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * q + 2 * m], f[8 * q + 2 * m + 1]);
-                            pk[m] = *reinterpret_cast<uint32_t*>(&b2);
-                        }
-                        dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        for (int q = 0; q < 8; ++q) f[q] = u[q] - __uint_as_float(a[h8 >> 1][(h8 & 1) * 8 + q]);
+                        st_h8(smem + LY::D + sw128_off(i, h2 * 32 + h8 * 8), f);
                     }
                 }
             }
-        }
-        if (delta_warp) {
             fence_async_smem();
             tc_fence_before();
-            named_bar(1, LY::THREADS / 2);   // the Delta warps (lane quarters 0 and 1)
-            // MMA4: D4 = Ktilde^T Delta
+            named_bar(1, 64);   // the Delta warps (lane quarters 2 and 3)
+            // MMA4: D4 = Ktilde^T Delta; MMA5: D5[t & 1] = [P; -] Delta
             if (ok && leader) {
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_f16(tmem + LY::TM_D4, dKT + so + (uint64_t)(ks * 128), dD + (uint64_t)(ks * 128), id4, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(tmem + LY::TM_D5 + s * 64, dP + so + (uint64_t)(ks * 2), dD + (uint64_t)(ks * 128), id3,
+                            ks > 0);
                 mma_commit(&S.m4);
             }
         }
@@ -1258,20 +1190,24 @@ __global__ void __launch_bounds__(SLayout<WIDE>::THREADS, 1) chunk_state_kernel(
             const float gC = reinterpret_cast<const float*>(st + LY::GC)[row];
             uint32_t r[4][16];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + LY::TM_D4 + cs + cb * 16, r[cb]);
+            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + LY::TM_D4 + cb * 16, r[cb]);
             tmem_ld_wait();
 #pragma unroll
             for (int k = 0; k < 64; ++k) hreg[k] = fmaf(gC, hreg[k], __uint_as_float(r[k >> 4][k & 15]));
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + LY::H + cs * 256 + sw128_off(row, c8 * 8), hreg + c8 * 8);
+            for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + LY::H + sw128_off(row, c8 * 8), hreg + c8 * 8);
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();   // stage s, D3, D4 and Delta are free
+        __syncthreads();   // stage s, D4 and Delta are free; D3 and D5 of chunk t hold its output
         if (ok && issuer && t + 2 < n_chunks) {
-            state_issue<WIDE>(smem, S, p.ws, (slot0 + t + 2) * H + ch.h, ch.half, s);
+            state_issue(smem, S, p.ws, (slot0 + t + 2) * H + ch.h, ch.half, s);
             issued = t + 3;
         }
+    }
+    if (ok && out_warp && n_chunks > 0) {
+        tc_fence_after();
+        state_output<O_F32>(p, ch, tl, n_chunks - 1, row);
     }
     // stages issued but never waited on (after a timeout) must land before the CTA exits
     if (issuer) {
@@ -1335,8 +1271,9 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     Ws ws;
     ws.wq = base;
     ws.kt = ws.wq + (size_t)items * WS_WQ;
-    ws.uu = ws.kt + (size_t)items * WS_KT;
-    ws.gc = reinterpret_cast<float*>(ws.uu + (size_t)items * WS_UU);
+    ws.u = ws.kt + (size_t)items * WS_KT;
+    ws.pp = ws.u + (size_t)items * WS_U;
+    ws.gc = reinterpret_cast<float*>(ws.pp + (size_t)items * WS_P);
     Geo geo{a.cu, a.n_seqs, a.B, a.T, a.H};
 
     int dev = 0, sms = 0;
@@ -1364,24 +1301,14 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     if (e != cudaSuccess) return e;
 
     StateParams sp{geo, a.h0, a.hT, a.o, ws};
-    // The wide variant (one CTA per chain over all 128 columns) halves the CTAs of an oversubscribed grid at the cost
-    // of a longer step per chunk; it pays only when every chain has the same length (packed sequences can put one
-    // long chain on the critical path, which the narrow variant runs faster).
-    const bool wide = !a.cu && chains * 2 > sms;
-    const unsigned grid2 = (unsigned)(wide ? chains : chains * 2);
-    auto launch2 = [&](auto kern, int threads, uint32_t bytes) -> cudaError_t {
-        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    const unsigned grid2 = (unsigned)(chains * 2);
+    auto launch2 = [&](auto kern) -> cudaError_t {
+        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem_bytes());
         if (e2 != cudaSuccess) return e2;
-        kern<<<grid2, threads, bytes, s>>>(sp);
+        kern<<<grid2, SLayout::THREADS, s_smem_bytes(), s>>>(sp);
         return cudaSuccess;
     };
-    if (wide) {
-        e = a.o_f32 ? launch2(chunk_state_kernel<true, true>, SLayout<true>::THREADS, s_smem_bytes<true>())
-                    : launch2(chunk_state_kernel<false, true>, SLayout<true>::THREADS, s_smem_bytes<true>());
-    } else {
-        e = a.o_f32 ? launch2(chunk_state_kernel<true, false>, SLayout<false>::THREADS, s_smem_bytes<false>())
-                    : launch2(chunk_state_kernel<false, false>, SLayout<false>::THREADS, s_smem_bytes<false>());
-    }
+    e = a.o_f32 ? launch2(chunk_state_kernel<true>) : launch2(chunk_state_kernel<false>);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -242,7 +242,7 @@ gdn_status kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const f
  * describe no counterpart; this entry point exists for callers that must not
  * allocate (for example inside a captured graph's replay loop).
  *   Limit: the static scratch holds 64 MiB, i.e. (floor(B*T / 64) + N + 1) * H
- *   * 82,432 bytes must not exceed 67,108,864 (about 800 (chunk, head) items,
+ *   * 74,240 bytes must not exceed 67,108,864 (about 900 (chunk, head) items,
  *   e.g. one 4096-token sequence with 12 heads).  A larger request returns
  *   GDN_ERR_UNSUPPORTED with the sizes in the message and launches nothing.
  *   Sharing: every call on a device uses the same scratch, so calls whose work
@@ -326,7 +326,8 @@ gdn_status gdn_chunk_plan(int per_channel, int B, int T, int H, int d_k, int d_v
  * with these sizes and kernel request (0 when the resolved kernel needs
  * none).  n_seqs is 0 for a call without cu_seqlens, else its number of
  * packed sequences.  The two-pass kernels keep, per (chunk slot, head),
- * 82,432 bytes: [W; Q'], Ktilde, [U; U'] in fp16 and gamma_C; there are
+ * 74,240 bytes: [Q^; W] (Q^ = scale gamma Q), Ktilde, U and P in fp16, and
+ * gamma_C; there are
  * floor(B*T / 64) + N + 1 slots.  Same status rules as gdn_chunk_plan.
  */
 gdn_status gdn_chunk_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,

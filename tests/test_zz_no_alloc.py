@@ -15,7 +15,7 @@ import gated_delta_rule_gdn_gb300 as gdn
 from gated_delta_rule_gdn_gb300 import _binding, build, workloads as W
 
 SCRATCH_BYTES = 64 << 20
-ITEM_BYTES = 82432
+ITEM_BYTES = 74240
 
 
 @pytest.fixture(scope="module")
@@ -26,7 +26,7 @@ def lib():
 
 def test_oversized_request_is_refused_before_any_launch(lib):
     fake = 0x10000
-    B, T, H = 4, 4096, 16          # (256 + 4 + 1) * 16 items of 82,432 bytes > 64 MiB
+    B, T, H = 4, 4096, 16          # (256 + 4 + 1) * 16 items of 74,240 bytes > 64 MiB
     assert (B * T // 64 + B + 1) * H * ITEM_BYTES > SCRATCH_BYTES
     st = lib.gdn_chunk_fwd_noalloc(0, fake, fake, fake, fake, fake, 0.1, None, 0, None, None, 0, fake,
                                    B, T, H, 128, 128, 64, 1, 0, None)
