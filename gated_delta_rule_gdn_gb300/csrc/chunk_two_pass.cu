@@ -937,7 +937,8 @@ struct StateParams {
     Ws ws;
 };
 
-// Pass 2: one CTA per (sequence, head, 64-column d_v half), 4 warps; warp w reads TMEM lane quarter w.  Per chunk
+// Pass 2: one CTA per (sequence, head, 64-column d_v half), 8 warps; warp w reads TMEM lane quarter w % 4 and the 32
+// columns w / 4 of the half (the fp32 state is 32 registers per thread).  Per chunk
 // (its workspace slot streamed by bulk copies through a two-stage ring):
 //   MMA3   D3 = [Q^; W] h~ : rows 0-63 Q^ h~ (for O), rows 64-127 W h~
 //   Delta = U - W h~ (lane quarters 2-3), to fp16 in shared memory
@@ -952,7 +953,7 @@ struct SLayout {
     static constexpr uint32_t H = 2 * STAGE;         // h~, fp16 MN-major [d][n] 128 x 64
     static constexpr uint32_t D = H + 16384;         // Delta, fp16 MN-major [j][n] 64 x 64
     static constexpr uint32_t SMALL = D + 8192;
-    static constexpr int THREADS = 128;
+    static constexpr int THREADS = 256;
     static constexpr uint32_t TM_D3 = 0, TM_D4 = 128, TM_D5 = 192, TM_COLS = 512;   // D3, D5: two each
 };
 struct SSmall {
@@ -1012,14 +1013,16 @@ __device__ __forceinline__ void state_issue(uint8_t* smem, SSmall& S, const Ws& 
     bulk_g2s(st + LY::GC, ws.gc + (size_t)it * 128, WS_GC, &S.full[s]);
 }
 
-// O = Q^ h~ + P Delta of chunk t (token rows 0-63: lane quarters 0 and 1), from D3 and D5 of its parity
+// O = Q^ h~ + P Delta of chunk t (token rows 0-63: lane quarters 0 and 1), columns cs .. cs + 31 of the half, from
+// D3 and D5 of its parity
 template <bool O_F32>
-__device__ __forceinline__ void state_output(const StateParams& p, const Chain& ch, uint32_t tl, int t, int row) {
+__device__ __forceinline__ void state_output(const StateParams& p, const Chain& ch, uint32_t tl, int t, int row,
+                                             int cs) {
     using LY = SLayout;
     const int L = min(C, ch.len - t * C);
     const size_t orow = ((size_t)(ch.row0 + (long)t * C + row) * p.geo.H + ch.h) * DV + ch.half * DVT;
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {   // 32 columns per pass: four loads, one wait
+    {   // 32 columns: four loads, one wait
+        const int h2 = cs >> 5;
         uint32_t a[2][16], b[2][16];
         tmem_ld16(tl + LY::TM_D3 + (t & 1) * 64 + h2 * 32, a[0]);
         tmem_ld16(tl + LY::TM_D3 + (t & 1) * 64 + h2 * 32 + 16, a[1]);
@@ -1065,7 +1068,8 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp;                        // TMEM lane quarter
+    const int q4 = warp & 3;                    // TMEM lane quarter
+    const int cs = 32 * (warp >> 2);            // this thread's first column within the half
     const Chain ch = resolve_chain(p.geo);
     const int n_chunks = (ch.len + C - 1) / C;
     const long slot0 = ch.row0 / C + ch.n;
@@ -1074,7 +1078,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     const bool leader = (tid == 64);            // issues the products (a Delta warp)
     const bool issuer = (tid == 32);            // issues the copies, off the leader's path
     const bool out_warp = q4 < 2;               // O (token rows 0-63); the others form Delta (rows 64-127)
-    const int col0 = ch.half * DVT;
+    const int col0 = ch.half * DVT + cs;        // first d_v column of this thread in the head
 
     if (warp == 0) {
         tmem_alloc(&S.tmem_base, LY::TM_COLS);
@@ -1099,9 +1103,9 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     int issued = n_chunks < 2 ? n_chunks : 2;
 
     const size_t sidx = ((size_t)ch.n * H + ch.h) * DK * DV + (size_t)row * DV + col0;
-    float hreg[DVT];
+    float hreg[32];
 #pragma unroll
-    for (int q = 0; q < DVT / 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
         const float4 v = p.h0 ? reinterpret_cast<const float4*>(p.h0 + sidx)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
         hreg[4 * q] = v.x;
         hreg[4 * q + 1] = v.y;
@@ -1110,7 +1114,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     }
     // h to fp16, MN-major [d][n] (operand B of MMA3)
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + LY::H + sw128_off(row, c8 * 8), hreg + c8 * 8);
+    for (int c8 = 0; c8 < 4; ++c8) st_h8(smem + LY::H + sw128_off(row, cs + c8 * 8), hreg + c8 * 8);
     fence_async_smem();
     __syncthreads();
 
@@ -1140,7 +1144,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
             mma_commit(&S.m3);
         }
         // meanwhile the output of the previous chunk (its D3 and D5 are the other parity)
-        if (ok && out_warp && t > 0) state_output<O_F32>(p, ch, tl, t - 1, row);
+        if (ok && out_warp && t > 0) state_output<O_F32>(p, ch, tl, t - 1, row, cs);
         if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(64u);
@@ -1149,8 +1153,8 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
             // Delta = U - W h~ (token row i = row - 64) to fp16 MN-major [j][n] (operand B of MMA4 and MMA5)
             const int i = row - 64;
             if (ok) {
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
+                {
+                    const int h2 = cs >> 5;
                     uint32_t a[2][16];
                     tmem_ld16(tl + LY::TM_D3 + s * 64 + h2 * 32, a[0]);
                     tmem_ld16(tl + LY::TM_D3 + s * 64 + h2 * 32 + 16, a[1]);
@@ -1167,7 +1171,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
             }
             fence_async_smem();
             tc_fence_before();
-            named_bar(1, 64);   // the Delta warps (lane quarters 2 and 3)
+            named_bar(1, 128);   // the Delta warps (lane quarters 2 and 3)
             // MMA4: D4 = Ktilde^T Delta; MMA5: D5[t & 1] = [P; -] Delta
             if (ok && leader) {
                 tc_fence_after();
@@ -1188,14 +1192,14 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
         // h <- gamma_C h + Ktilde^T Delta; fp16 copy for the next MMA3
         if (ok) {
             const float gC = reinterpret_cast<const float*>(st + LY::GC)[row];
-            uint32_t r[4][16];
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tmem_ld16(tl + LY::TM_D4 + cb * 16, r[cb]);
+            uint32_t r[2][16];
+            tmem_ld16(tl + LY::TM_D4 + cs, r[0]);
+            tmem_ld16(tl + LY::TM_D4 + cs + 16, r[1]);
             tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 64; ++k) hreg[k] = fmaf(gC, hreg[k], __uint_as_float(r[k >> 4][k & 15]));
+            for (int k = 0; k < 32; ++k) hreg[k] = fmaf(gC, hreg[k], __uint_as_float(r[k >> 4][k & 15]));
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) st_h8(smem + LY::H + sw128_off(row, c8 * 8), hreg + c8 * 8);
+            for (int c8 = 0; c8 < 4; ++c8) st_h8(smem + LY::H + sw128_off(row, cs + c8 * 8), hreg + c8 * 8);
         }
         fence_async_smem();
         tc_fence_before();
@@ -1207,7 +1211,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     }
     if (ok && out_warp && n_chunks > 0) {
         tc_fence_after();
-        state_output<O_F32>(p, ch, tl, n_chunks - 1, row);
+        state_output<O_F32>(p, ch, tl, n_chunks - 1, row, cs);
     }
     // stages issued but never waited on (after a timeout) must land before the CTA exits
     if (issuer) {
@@ -1215,7 +1219,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     }
     if (p.hT && ok) {
 #pragma unroll
-        for (int q = 0; q < DVT / 4; ++q)
+        for (int q = 0; q < 8; ++q)
             reinterpret_cast<float4*>(p.hT + sidx)[q] =
                 make_float4(hreg[4 * q], hreg[4 * q + 1], hreg[4 * q + 2], hreg[4 * q + 3]);
     }
