@@ -616,6 +616,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int H = p.geo.H;
     const float LOG2E = 1.4426950408889634f;
     (void)LOG2E;
+    griddep_launch_dependents();   // the state kernel may take SMs as this grid's CTAs retire
 
     if (warp == 0) {
         tmem_alloc(&S.tmem_base, I_TM_COLS);
@@ -1097,6 +1098,9 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     const uint32_t tmem = S.tmem_base;
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
 
+    // the per-chunk kernel has completed and its workspace writes are visible (with a programmatic launch this
+    // CTA may have started before that; everything above reads only inputs)
+    griddep_wait();
     if (issuer) {
         for (int t = 0; t < 2 && t < n_chunks; ++t) state_issue(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
     }
@@ -1306,11 +1310,22 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
 
     StateParams sp{geo, a.h0, a.hT, a.o, ws};
     const unsigned grid2 = (unsigned)(chains * 2);
+    // Programmatic stream serialisation: the state kernel's CTAs may start on SMs the per-chunk kernel has left,
+    // and wait (griddepcontrol.wait) for its completion before they read the workspace.
     auto launch2 = [&](auto kern) -> cudaError_t {
         cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem_bytes());
         if (e2 != cudaSuccess) return e2;
-        kern<<<grid2, SLayout::THREADS, s_smem_bytes(), s>>>(sp);
-        return cudaSuccess;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(grid2);
+        cfg.blockDim = dim3(SLayout::THREADS);
+        cfg.dynamicSmemBytes = s_smem_bytes();
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, sp);
     };
     e = a.o_f32 ? launch2(chunk_state_kernel<true>) : launch2(chunk_state_kernel<false>);
     if (e != cudaSuccess) return e;

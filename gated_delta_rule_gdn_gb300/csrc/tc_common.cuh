@@ -109,6 +109,14 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Let the next kernel on the stream (launched with programmatic stream serialisation) be scheduled before this
+// grid completes; it still waits in griddep_wait until this grid has completed and its writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the grids this one depends on have completed and their memory operations are visible (returns at once
+// when the kernel was launched without a programmatic dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMEM
 // Allocation and deallocation are warp-wide (.sync.aligned); the address lands in shared memory.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
