@@ -45,8 +45,8 @@ gdn_status check_chunk(const gdn::ChunkArgs& a, gdn_dtype dtype, gdn_dtype o_dty
     if (!dtype_ok(o_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown o_dtype %d", fn, (int)o_dtype);
     if (a.B < 1 || a.T < 0 || a.H < 1)
         return fail(GDN_ERR_INVALID_ARG, "%s: need B >= 1, T >= 0, H >= 1 (got B=%d T=%d H=%d)", fn, a.B, a.T, a.H);
-    if (a.dk < 1 || a.dv < 1 || a.dk > 128 || a.dv > 128)
-        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..128 (got d_k=%d d_v=%d)", fn, a.dk, a.dv);
+    if (a.dk < 1 || a.dv < 1 || a.dk > 256 || a.dv > 256)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..256 (got d_k=%d d_v=%d)", fn, a.dk, a.dv);
     if (a.C != 16 && a.C != 32 && a.C != 64)
         return fail(GDN_ERR_UNSUPPORTED, "%s: chunk_size must be 16, 32 or 64 (got %d)", fn, a.C);
     if (!std::isfinite(a.scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
@@ -85,6 +85,14 @@ gdn_status resolve_algo(const gdn::ChunkArgs& a, gdn_algo algo, const char* fn, 
         return fail(GDN_ERR_UNSUPPORTED, "%s: the two-pass kernels do not apply: %s", fn, why_tp);
     if (algo == GDN_ALGO_AUTO)
         algo = !why_tp ? GDN_ALGO_TWO_PASS : (!why_tc ? GDN_ALGO_TCGEN05 : GDN_ALGO_GENERIC);
+    if (algo == GDN_ALGO_GENERIC) {
+        const size_t need = gdn::generic_smem_bytes(a);
+        if (need > gdn::kMaxSmemPerBlock)
+            return fail(GDN_ERR_UNSUPPORTED,
+                        "%s: the generic kernel would need %zu bytes of shared memory for d_k=%d, chunk_size=%d%s "
+                        "(at most %zu); use a smaller chunk_size", fn, need, a.dk, a.C,
+                        a.per_channel ? " and the per-channel gate" : "", gdn::kMaxSmemPerBlock);
+    }
     *chosen = algo;
     return GDN_OK;
 }
@@ -175,8 +183,8 @@ gdn_status step_common(const void* q, const void* k, const void* v, const float*
     if (!dtype_ok(dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
     if (!dtype_ok(o_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown o_dtype %d", fn, (int)o_dtype);
     if (N < 1 || H < 1) return fail(GDN_ERR_INVALID_ARG, "%s: need N >= 1, H >= 1 (got N=%d H=%d)", fn, N, H);
-    if (d_k < 1 || d_v < 1 || d_k > 128 || d_v > 128)
-        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..128 (got d_k=%d d_v=%d)", fn, d_k, d_v);
+    if (d_k < 1 || d_v < 1 || d_k > 256 || d_v > 256)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..256 (got d_k=%d d_v=%d)", fn, d_k, d_v);
     if (!q || !k || !v || !g || !beta || !state || !o)
         return fail(GDN_ERR_INVALID_ARG, "%s: q, k, v, g, beta, state and o must be non-NULL", fn);
     if (!std::isfinite(scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);

@@ -4,7 +4,8 @@
 // §2.3 (paper eqs 11-12), extended to per-channel decays as on "You Could Have Come Up With Kimi
 // Delta Attention" (chunkwise form).  Everything is fp32 in shared memory.  It serves:
 //   * fp32 inputs (tensor-core TF32 cannot reach the 1e-4 tolerance fp32 inputs are held to);
-//   * any 1 <= d_k, d_v <= 128 and chunk 16/32/64;
+//   * any 1 <= d_k, d_v <= 256 and chunk 16/32/64, within the shared memory of one CTA (fp32 tiles: d_k = 256
+//     takes chunk 64 with the scalar gate, chunk 32 or less with the per-channel gate);
 //   * the KDA path.
 // It is the correctness-first shape of the fused kernel.
 //
@@ -238,6 +239,10 @@ cudaError_t launch_gate(const ChunkArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+size_t generic_smem_bytes(const ChunkArgs& a) {
+    return generic_smem_floats(a.C, a.dk, a.per_channel != 0) * sizeof(float);
+}
 
 cudaError_t launch_chunk_generic(const ChunkArgs& a, cudaStream_t s) {
     if (a.bf16) return a.o_f32 ? launch_gate<__nv_bfloat16, float>(a, s) : launch_gate<__nv_bfloat16, __nv_bfloat16>(a, s);

@@ -61,6 +61,9 @@ struct StepArgs {
 
 // Generic fp32 SIMT chunk kernel (chunk_generic.cu).
 cudaError_t launch_chunk_generic(const ChunkArgs& a, cudaStream_t s);
+// Dynamic shared memory the generic kernel needs for this request, and the most one CTA may have.
+size_t generic_smem_bytes(const ChunkArgs& a);
+constexpr size_t kMaxSmemPerBlock = 227 * 1024;
 
 // Fused tcgen05/TMA chunk kernel for the scalar gate (chunk_tc.cu).
 // Returns nullptr if the request fits the kernel, else a reason.

@@ -68,7 +68,10 @@ typedef enum gdn_dtype {
 /* Kernel choice for the chunk forward. */
 typedef enum gdn_algo {
     GDN_ALGO_AUTO = 0,      /* the fastest tensor-core path that applies, else the generic one */
-    GDN_ALGO_GENERIC = 1,   /* fp32 SIMT chunk kernel: any dtype, 1 <= d_k, d_v <= 128 */
+    GDN_ALGO_GENERIC = 1,   /* fp32 SIMT chunk kernel: any dtype, 1 <= d_k, d_v <= 256 where its fp32
+                               tiles fit one CTA's shared memory (d_k = 256: chunk 64 for the
+                               scalar gate, chunk <= 32 for the per-channel gate);
+                               GDN_ERR_UNSUPPORTED otherwise */
     GDN_ALGO_TCGEN05 = 2,   /* fused tcgen05/TMA kernel (one CTA per chain does every stage):
                                bf16, d_k = d_v = 128, chunk 64, scalar gate;
                                GDN_ERR_UNSUPPORTED when the request does not fit it */
@@ -109,7 +112,8 @@ typedef enum gdn_algo {
  *               of bounds, but the results are then unspecified.
  *   o           [B, T, H, d_v]   o_dtype (output)
  *   chunk_size  16, 32 or 64 (the pages' kernels use these; 64 is the default there)
- *   sizes       B >= 1, T >= 0, H >= 1, 1 <= d_k, d_v <= 128
+ *   sizes       B >= 1, T >= 0, H >= 1, 1 <= d_k, d_v <= 256 (the pages' bound on
+ *               the head sizes; above 128 only the generic kernel applies)
  *
  * Packed sequences give results bitwise equal to running each sequence alone.
  */
@@ -272,7 +276,7 @@ gdn_status gdn_chunk_fwd_noalloc(int per_channel, const void* q, const void* k, 
  *   g      [N, H] fp32 (log alpha)   beta [N, H] fp32
  *   state  [N, H, d_k, d_v] fp32, updated in place (the only aliasing allowed)
  *   o      output: o = scale * S_t q_t, read after the write
- *   sizes  N >= 1, H >= 1, 1 <= d_k, d_v <= 128
+ *   sizes  N >= 1, H >= 1, 1 <= d_k, d_v <= 256
  */
 gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               float scale, float* state, void* o, int N, int H, int d_k, int d_v,

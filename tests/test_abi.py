@@ -55,7 +55,7 @@ def _chunk(lib, fn="gdn_chunk_fwd_algo", **kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(dk=0), 2), (dict(dv=129), 2), (dict(C=48), 2),
+    (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(dk=0), 2), (dict(dv=257), 2), (dict(C=48), 2),
     (dict(C=128), 2), (dict(dtype=7), 1), (dict(q=None), 1), (dict(o=None), 1), (dict(ofs=1), 1),
     (dict(hT=FAKE), 1), (dict(cu=FAKE, B=2, n=2), 1), (dict(cu=FAKE, n=0), 1), (dict(q=FAKE + 1), 1),
     (dict(scale=float("nan")), 1), (dict(algo=9), 1), (dict(odt=3), 1), (dict(o=FAKE + 2), 1), (dict(algo=2, dtype=0), 2), (dict(algo=2, dk=64, dv=32), 2),
@@ -76,7 +76,7 @@ def test_step_argument_checks(lib):
                  a["dt"], a["odt"], None)
     assert call(N=0) == 1
     assert call(st=None) == 1
-    assert call(dk=256) == 2
+    assert call(dk=257) == 2
     assert call(dt=5) == 1
     assert call(q=FAKE + 2, dt=0) == 1
     assert call(s=float("inf")) == 1
@@ -167,3 +167,21 @@ def test_beta_activation_mode_checks(lib):
     assert lib.gdn_recurrent_step_ex(1, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, FAKE, 4, 2, 2, 128, 128, 1, 0,
                                      ctypes.byref(gate), None) == 2
     assert "scalar gate" in _binding.last_error()
+
+
+def test_head_sizes_up_to_256_and_the_generic_kernels_shared_memory(lib):
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    # d_k = d_v = 256 runs on the generic kernel: chunk 64 for the scalar gate ...
+    assert _binding.chunk_plan(False, 1, 300, 2, 256, 256, 64, bf) == "generic"
+    assert _binding.chunk_plan(False, 1, 300, 2, 256, 64, 64, f32) == "generic"
+    # ... chunk 32 or less for the per-channel gate; chunk 64 would not fit one CTA's shared memory
+    assert _binding.chunk_plan(True, 1, 300, 2, 256, 256, 32, bf) == "generic"
+    with pytest.raises(_binding.GdnError) as e:
+        _binding.chunk_plan(True, 1, 300, 2, 256, 256, 64, bf)
+    assert "shared memory" in str(e.value) and "chunk_size" in str(e.value)
+    # the same refusal from a forward call, before any launch (fake pointers are never touched)
+    assert _chunk(lib, fn="kda_chunk_fwd_algo", dk=256, dv=256, C=64) == 2
+    assert "shared memory" in _binding.last_error()
+    with pytest.raises(_binding.GdnError):
+        _binding.chunk_plan(False, 1, 300, 2, 257, 64, 64, bf)

@@ -66,13 +66,13 @@ def _decode_and_compare(w: W.DecodeWorkload, steps: int, sample=None):
 
 
 @pytest.mark.parametrize("N,H,dk,dv,dtype", [(3, 2, 16, 8, "f32"), (4, 2, 128, 128, "f32"), (5, 3, 128, 128, "bf16"),
-                                             (2, 2, 64, 100, "bf16")])
+                                             (2, 2, 64, 100, "bf16"), (3, 2, 256, 256, "bf16"), (2, 2, 256, 96, "f32")])
 def test_small_decode(N, H, dk, dv, dtype):
     _decode_and_compare(W.DecodeWorkload("t", N, H, dk, dv, 40, dtype=dtype), 40)
 
 
 @pytest.mark.parametrize("N,H,dk,dv,dtype", [(3, 2, 16, 8, "f32"), (4, 2, 128, 128, "f32"), (5, 3, 128, 128, "bf16"),
-                                             (2, 2, 64, 100, "bf16")])
+                                             (2, 2, 64, 100, "bf16"), (3, 2, 256, 256, "bf16")])
 def test_small_kda_decode(N, H, dk, dv, dtype):
     _decode_and_compare(W.DecodeWorkload("t", N, H, dk, dv, 40, dtype=dtype, kind="kda"), 40)
 
