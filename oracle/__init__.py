@@ -11,6 +11,9 @@ Contents:
   results are compared with.  It handles the scalar gate (GDN) and the
   per-key-channel gate (KDA).  The decode step is the same recurrence, one
   token per call.
+* ``recurrence_backward``: the gradients of <dO, o> + <dhT, h_final> with respect
+  to q, k, v, g, beta and the initial state, by reverse-mode differentiation of
+  the same token steps (C, fp64).
 * ``reference``: numpy twins that pin the oracle.  They are the literal d x d
   matrix recurrence, the DeltaNet and Mamba2 limits, and brute-force
   chunkwise / WY / UT evaluators with three triangular solves.
@@ -30,7 +33,7 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["recurrence", "load", "max_threads"]
+__all__ = ["recurrence", "recurrence_backward", "load", "max_threads"]
 
 _lib = None
 
@@ -47,6 +50,10 @@ def load():
         lib.gdn_oracle_forward.argtypes = [d, d, d, d, d, ctypes.c_double, d, d, d, i32, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int]
+        lib.gdn_oracle_backward.restype = ctypes.c_int
+        lib.gdn_oracle_backward.argtypes = [d, d, d, d, d, ctypes.c_double, d, d, d, d, d, d, d, d, d, i32,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.gdn_oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -106,3 +113,37 @@ def recurrence(q, k, v, g, beta, scale: float, initial_state=None, cu_seqlens=No
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
     return o, hT
+
+
+def recurrence_backward(q, k, v, g, beta, scale: float, d_out, initial_state=None, d_final_state=None,
+                        cu_seqlens=None, gate_per_channel: Optional[bool] = None, n_threads: int = 0):
+    """Gradients of L = <d_out, o> + <d_final_state, final_state> through the fp64 token recurrence.
+
+    Shapes as ``recurrence``; d_out [B, T, H, dv]; d_final_state [N, H, dk, dv] or None (zero).
+    Returns a dict of fp64 numpy arrays: dq, dk [B, T, H, dk]; dv [B, T, H, dv]; dg (the shape of g);
+    dbeta [B, T, H]; dh0 [N, H, dk, dv].
+    """
+    qd, kd, vd, gd, bd, dod = (_f64(x) for x in (q, k, v, g, beta, d_out))
+    B, T, H, dk = qd.shape
+    dv = vd.shape[-1]
+    if gate_per_channel is None:
+        gate_per_channel = gd.ndim == 4
+    cu = None
+    N = B
+    if cu_seqlens is not None:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().cpu().numpy()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+        N = cu.shape[0] - 1
+    h0 = _f64(initial_state)
+    dhT = _f64(d_final_state)
+    out = {"dq": np.zeros_like(qd), "dk": np.zeros_like(kd), "dv": np.zeros_like(vd), "dg": np.zeros_like(gd),
+           "dbeta": np.zeros_like(bd), "dh0": np.zeros((N, H, dk, dv), dtype=np.float64)}
+    rc = load().gdn_oracle_backward(
+        _ptr(qd), _ptr(kd), _ptr(vd), _ptr(gd), _ptr(bd), float(scale), _ptr(h0), _ptr(dod), _ptr(dhT),
+        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dh0"]),
+        cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int)) if cu is not None else ctypes.POINTER(ctypes.c_int)(),
+        int(N if cu is not None else 0), B, T, H, dk, dv, int(bool(gate_per_channel)), int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out
