@@ -23,6 +23,11 @@ Inputs are seeded and synthetic, drawn by gated_delta_rule_gdn_gb300.workloads.
   write per sequence-head.
 * cpu_baseline: the fp64 C oracle on the host cores (rank 0, N = 1).
 * --impl reference: the oracle alone, timed as the reference arm.
+Workloads 6 and 7 time the chunk backward (gdn_chunk_bwd) on the shapes of
+workloads 1 and 3: one step is one backward call (the checkpoint kernel, then
+the backward walk).  It is fp32 SIMT arithmetic, so its roofline is the fp32
+FMA rate (152 SMs x 128 lanes x 2 flops x 2.07 GHz), against the algorithmic
+flops of the chunkwise backward given in _bwd_flops.
 With N > 1 (torchrun), every rank runs its own replica: weak scaling, and no
 collective on the data path.  A barrier and a max over ranks bracket the
 timing.
@@ -297,6 +302,216 @@ def run_reference(args):
     return 0
 
 
+BWD_OF = {6: 1, 7: 3}      # backward workload -> the forward workload it differentiates
+ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def _bwd_name(w) -> str:
+    return w.name.replace("_prefill", "").replace("_c64", "").replace(w.kind + "_", w.kind + "_bwd_", 1)
+
+
+def _bwd_flops(w, C: int) -> int:
+    """Algorithmic flops of one chunk-backward call (2 per multiply-add), per chunk of C rows and head:
+    the recomputed forward (K K^T and Q K^T: C^2 d_k; Z: C d_k d_v; the solve: C^2 d_v / 2; the state update:
+    C d_k d_v), and the backward (dDelta: C d_k d_v + C^2 d_v / 2; the back solve: C^2 d_v / 2; dP and dA: C^2 d_v;
+    the state products h dO, h Y, dh Delta: 3 C d_k d_v; the four pair sums of dQ / dK: 2 C^2 d_k; the state
+    gradient: 2 C d_k d_v).  Per-channel exponentials are not counted."""
+    dk, dv = w.dk, w.dv
+    macs = 3 * C * C * dk + 9 * C * dk * dv + 5 * C * C * dv // 2
+    N = w.n_seqs if w.n_seqs else w.B
+    chunks = N * math.ceil(w.T / C) if not w.n_seqs else math.ceil(w.T / C) + N
+    return 2 * macs * chunks * w.H
+
+
+def _bwd_chains_oracle(x, g, chains):
+    """Arrays of the (b, h) chains for the oracle's backward."""
+    import numpy as np
+    out = []
+    for b, h in chains:
+        sl = lambda t: np.ascontiguousarray(t[b:b + 1, :, h:h + 1].double().numpy())
+        st = lambda t: None if t is None else np.ascontiguousarray(t[b:b + 1, h:h + 1].double().numpy())
+        out.append((sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["g"]), sl(x["beta"]), sl(g["d_o"]),
+                    st(x["initial_state"]), st(g["d_final_state"])))
+    return out
+
+
+def _bwd_oracle_run(arrs, scale, per_channel):
+    import oracle
+    for q, k, v, gg, beta, do, h0, dhT in arrs:
+        oracle.recurrence_backward(q, k, v, gg, beta, scale, do, h0, dhT, gate_per_channel=per_channel)
+
+
+def cpu_baseline_bwd(x, g, w, min_seconds=10.0, max_passes=60):
+    import oracle
+    oracle.load()
+    chains = [(b, h) for b in range(w.B) for h in range(0, w.H, max(1, w.H // 4))][:4]
+    arrs = _bwd_chains_oracle(x, g, chains)
+    passes, t_total = 0, 0.0
+    while passes < max_passes and (passes == 0 or t_total < min_seconds):
+        t0 = time.perf_counter()
+        _bwd_oracle_run(arrs, x["scale"], x["gate_per_channel"])
+        t_total += time.perf_counter() - t0
+        passes += 1
+    tokens = w.T * len(chains) * passes / w.H
+    return {"value": tokens / t_total, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"the oracle's backward on {len(chains)} (sequence, head) chains of {w.T} tokens, {passes} "
+                      f"pass(es), {t_total:.1f} s; tokens/s scaled to all {w.B * w.H} chains"}
+
+
+def run_reference_bwd(args):
+    """The oracle's backward: one (sequence, head) chain per step, scaled to all chains."""
+    from gated_delta_rule_gdn_gb300 import workloads as W
+    import oracle
+    w = W.config(BWD_OF[args.workload])
+    x = W.chunk_inputs(w, seed=0)
+    g = W.chunk_output_grads(x, seed=1, dhT_std=0.02)
+    arrs = _bwd_chains_oracle(x, g, [(0, 0)])
+    oracle.load()
+    for _ in range(args.warmup):
+        _bwd_oracle_run(arrs, x["scale"], x["gate_per_channel"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _bwd_oracle_run(arrs, x["scale"], x["gate_per_channel"])
+    dt = (time.perf_counter() - t0) / args.steps * (w.B * w.H)
+    value = w.B * w.T / dt
+    line = {"impl": "reference", "metric": f"{w.kind.upper()} chunk-bwd tokens/s ({_bwd_name(w)}), 1×GB300",
+            "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": _bwd_name(w), "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"per step one (sequence, head) chain of {w.T} tokens; time scaled to all "
+                                       f"{w.B * w.H} chains"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+    return 0
+
+
+def run_bwd(args):
+    """One step = one chunk-backward call over the whole workload (inputs and upstream gradients resident)."""
+    import torch
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _init_pg(ws, "nccl")
+    import gated_delta_rule_gdn_gb300 as gdn
+    from gated_delta_rule_gdn_gb300 import build as libbuild, workloads as W
+    if local == 0:
+        libbuild.build()
+    barrier(ws)
+    gdn.load()
+    w = W.config(BWD_OF[args.workload])
+    x = W.chunk_inputs(w, seed=0)
+    grads = W.chunk_output_grads(x, seed=1, dhT_std=0.02)
+    x.update(grads)
+    keys = [k for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens", "d_o", "d_final_state")
+            if x[k] is not None]
+    host = {k: x[k].pin_memory() for k in keys}
+    d = {k: v.to(dev) for k, v in host.items()}
+    per_channel = w.kind == "kda"
+    n_seqs = 0 if x["cu_seqlens"] is None else x["cu_seqlens"].numel() - 1
+    C = 0
+    ws_bytes = gdn.bwd_workspace_size(per_channel, w.B, w.T, w.H, w.dk, w.dv, C, n_seqs)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(dd):
+        return gdn.chunk_bwd(per_channel, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["d_o"], scale=w.scale,
+                             initial_state=dd.get("initial_state"), d_final_state=dd.get("d_final_state"),
+                             cu_seqlens=dd.get("cu_seqlens"), chunk_size=C, stream=stream, workspace=workspace)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call(d)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(int(os.environ.get("GDN_BENCH_GPU_INDEX", local))) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            call(d)
+            torch.cuda.synchronize(dev)
+        sampler.mark()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_wall = time.perf_counter()
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record(stream)
+        call(d)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs), ws, dev)
+    clocks = sampler.stop() if sampler else None
+
+    # end to end: inputs and upstream gradients host -> device, the call, the six gradients device -> host
+    dd = {k: torch.empty_like(v) for k, v in d.items()}
+    outs = call(d)
+    outs_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs if t is not None]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_host)
+
+    def e2e_step():
+        for k in dd:
+            dd[k].copy_(host[k], non_blocking=True)
+        res = [t for t in call(dd) if t is not None]
+        for hst, t in zip(outs_host, res):
+            hst.copy_(t, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+
+    tokens = w.B * w.T
+    try:   # the chunk the call took: 32 where it fits one CTA's shared memory, else 16
+        gdn.bwd_workspace_size(per_channel, 1, 64, 1, w.dk, w.dv, 32)
+        C_used = 32
+    except gdn.GdnError:
+        C_used = 16
+    flops = _bwd_flops(w, C_used)
+    achieved = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": f"{w.kind.upper()} chunk-bwd tokens/s ({_bwd_name(w)}) and % of fp32 ALU roofline, 1×GB300",
+        "value": tokens * ws / (ms / 1e3), "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; the forward recipe of the workload, dO N(0,1) bf16, dhT N(0,0.02))",
+        "config": {"workload": _bwd_name(w), "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "chunk_size": C_used, "input_dtype": "bf16", "grad_dtype": "f32",
+                   "l2": "flushed before each timed step (256 MiB device write, outside the events)",
+                   "kernel": "chunk_bwd", "launches_per_step": 2, "timed_region_wall_ms": t_wall * 1e3},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / ALU_PEAK_TFLOPS, "traffic": None,
+                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz",
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * 2,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_bwd(x, grads, w)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def run_ours(args):
     import torch
     ws, rank, local = _dist()
@@ -544,14 +759,20 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--algo", choices=["auto", "generic", "tcgen05", "two_pass"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4, 5], default=WORKLOAD,
+    ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4, 5, 6, 7], default=WORKLOAD,
                     help="1: GDN B4 T4096 H16 (the headline), 2: packed GDN 8 seqs 65536 tokens H32, 3: KDA B2 T8192 "
-                         "H32, 4: GDN decode step 256 seqs H32, 5: KDA decode step 256 seqs H32")
+                         "H32, 4: GDN decode step 256 seqs H32, 5: KDA decode step 256 seqs H32, 6: GDN chunk "
+                         "backward B4 T4096 H16, 7: KDA chunk backward B2 T8192 H32")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
+        if args.workload in BWD_OF:
+            ws, rank, _ = _dist()
+            return 0 if ws > 1 and rank != 0 else run_reference_bwd(args)
         return run_reference(args)
+    if args.workload in BWD_OF:
+        return run_bwd(args)
     if args.workload >= 4:
         return run_decode(args)
     return run_ours(args)

@@ -67,6 +67,11 @@ def _declare(lib):
     lib.gdn_chunk_plan.restype = i
     lib.gdn_chunk_plan.argtypes = [i, i, i, i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
     lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_chunk_bwd.restype = i
+    lib.gdn_chunk_bwd.argtypes = [i, vp, vp, vp, vp, vp, fp, vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp,
+                                  i, i, i, i, i, i, i, i, vp, ctypes.c_size_t, vp]
+    lib.gdn_chunk_bwd_workspace_size.restype = i
+    lib.gdn_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.gdn_last_error.argtypes = []
     lib.gdn_device_status.restype = i
     lib.gdn_device_status.argtypes = [i]
@@ -257,6 +262,77 @@ def chunk_fwd_noalloc(per_channel: bool, q, k, v, g, beta, scale=None, initial_s
                                    DTYPES[o_dtype], _stream_handle(stream, dev))
     _check(st)
     return o, final_state
+
+
+def bwd_workspace_size(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chunk_size: int = 0,
+                       n_seqs: int = 0) -> int:
+    """Device workspace bytes of a chunk-backward call (C ABI gdn_chunk_bwd_workspace_size)."""
+    out = ctypes.c_size_t(0)
+    _check(load().gdn_chunk_bwd_workspace_size(int(per_channel), B, T, H, dk, dv, int(chunk_size), int(n_seqs),
+                                               ctypes.byref(out)))
+    return int(out.value)
+
+
+def chunk_bwd(per_channel: bool, q, k, v, g, beta, d_o, scale=None, initial_state=None, d_final_state=None,
+              cu_seqlens=None, chunk_size=0, stream=None, workspace=None, want_d_initial_state=True):
+    """Gradients of <d_o, o> + <d_final_state, final_state> through the chunk forward (C ABI gdn_chunk_bwd).
+
+    Inputs as the forward (per_channel: KDA gate [B, T, H, dk]); d_o [B, T, H, dv] fp32 or bf16; d_final_state
+    [N, H, dk, dv] fp32 or None.  Returns (dq, dk, dv, dg, dbeta, d_initial_state or None), all fp32."""
+    lib = load()
+    if q.dtype not in DTYPES:
+        raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
+    dev = q.device
+    for name, t, dt in (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32), ("d_o", d_o, None)):
+        _need(t, name, dt, dev)
+    if d_o.dtype not in DTYPES:
+        raise ValueError(f"d_o must be float32 or bfloat16 (got {d_o.dtype})")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, T, H) or d_o.shape != v.shape:
+        raise ValueError("q, k, v, d_o shapes do not match")
+    if g.shape != ((B, T, H, dk) if per_channel else (B, T, H)) or beta.shape != (B, T, H):
+        raise ValueError("g / beta shapes do not match")
+    n_seqs = 0
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        n_seqs = cu_seqlens.numel() - 1
+    N = n_seqs if cu_seqlens is not None else B
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None:
+            _need(t, name, torch.float32, dev)
+            if t.shape != (N, H, dk, dv):
+                raise ValueError(f"{name} must be {(N, H, dk, dv)}")
+    if scale is None:
+        scale = dk ** -0.5
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dkk, dvv = torch.empty(q.shape, **f32), torch.empty(k.shape, **f32), torch.empty(v.shape, **f32)
+    dg, dbeta = torch.empty(g.shape, **f32), torch.empty(beta.shape, **f32)
+    dh0 = torch.empty((N, H, dk, dv), **f32) if want_d_initial_state else None
+    if workspace is None:
+        need = bwd_workspace_size(per_channel, B, T, H, dk, dv, chunk_size, n_seqs)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, dev)
+    _check(lib.gdn_chunk_bwd(int(per_channel), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                             _ptr(initial_state), _ptr(d_o), _ptr(d_final_state), _ptr(cu_seqlens), n_seqs,
+                             _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
+                             B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[d_o.dtype],
+                             _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                             _stream_handle(stream, dev)))
+    return dq, dkk, dvv, dg, dbeta, dh0
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, d_o, **kw):
+    """Backward of gdn_chunk_fwd (scalar gate): see chunk_bwd."""
+    return chunk_bwd(False, q, k, v, g, beta, d_o, **kw)
+
+
+def kda_chunk_bwd(q, k, v, g, beta, d_o, **kw):
+    """Backward of kda_chunk_fwd (per-channel gate): see chunk_bwd."""
+    return chunk_bwd(True, q, k, v, g, beta, d_o, **kw)
 
 
 def _step(per_channel: bool, q, k, v, g, beta, state, scale=None, o=None, stream=None, o_dtype=torch.float32,

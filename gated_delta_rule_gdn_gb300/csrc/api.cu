@@ -211,6 +211,38 @@ gdn_status step_common(const void* q, const void* k, const void* v, const float*
 }
 
 
+// Validate a backward request (everything except the pointers' contents) and settle its chunk.
+gdn_status check_bwd(gdn::BwdArgs& a, gdn_dtype dtype, gdn_dtype do_dtype, const char* fn) {
+    if (!dtype_ok(dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, (int)dtype);
+    if (!dtype_ok(do_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: unknown do_dtype %d", fn, (int)do_dtype);
+    if (a.B < 1 || a.T < 0 || a.H < 1)
+        return fail(GDN_ERR_INVALID_ARG, "%s: need B >= 1, T >= 0, H >= 1 (got B=%d T=%d H=%d)", fn, a.B, a.T, a.H);
+    if (a.dk < 1 || a.dv < 1 || a.dk > 256 || a.dv > 256)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: head sizes must be 1..256 (got d_k=%d d_v=%d)", fn, a.dk, a.dv);
+    if (a.C == 0) {
+        a.C = gdn::bwd_auto_chunk(a.dk, a.per_channel != 0);
+        if (a.C == 0)
+            return fail(GDN_ERR_UNSUPPORTED, "%s: no chunk_size fits the shared memory of one CTA for d_k=%d", fn,
+                        a.dk);
+    }
+    if (a.C != 16 && a.C != 32)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: chunk_size must be 16, 32 or 0 (got %d)", fn, a.C);
+    const size_t need = gdn::bwd_smem_bytes(a.C, a.dk, a.per_channel != 0);
+    if (need > gdn::kMaxSmemPerBlock)
+        return fail(GDN_ERR_UNSUPPORTED,
+                    "%s: the backward would need %zu bytes of shared memory for d_k=%d, chunk_size=%d (at most %zu); "
+                    "use a smaller chunk_size", fn, need, a.dk, a.C, gdn::kMaxSmemPerBlock);
+    if (!std::isfinite(a.scale)) return fail(GDN_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if (a.cu) {
+        if (a.B != 1) return fail(GDN_ERR_INVALID_ARG, "%s: cu_seqlens needs B == 1 (got B=%d)", fn, a.B);
+        if (a.n_seqs < 1) return fail(GDN_ERR_INVALID_ARG, "%s: cu_seqlens needs n_seqs >= 1 (got %d)", fn, a.n_seqs);
+        if (!aligned(a.cu, 4)) return fail(GDN_ERR_INVALID_ARG, "%s: cu_seqlens is not 4-byte aligned", fn);
+    }
+    if ((long)a.B * a.T * a.H > (1L << 31) / (a.dk > a.dv ? a.dk : a.dv))
+        return fail(GDN_ERR_UNSUPPORTED, "%s: tensor has 2^31 elements or more", fn);
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -374,6 +406,69 @@ gdn_status gdn_chunk_workspace_size(int per_channel, int B, int T, int H, int d_
     st = resolve_algo(a, requested, fn, &c);
     if (st != GDN_OK) return st;
     *bytes = c == GDN_ALGO_TWO_PASS ? gdn::two_pass_workspace_bytes(a) : 0;
+    return ok();
+}
+
+gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, float scale, const float* initial_state, const void* grad_o,
+                         const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
+                         float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
+                         int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                         gdn_dtype do_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "gdn_chunk_bwd";
+    gdn::BwdArgs a{q, k, v, g, beta, scale, initial_state, grad_o, grad_final_state, cu_seqlens, n_seqs,
+                   grad_q, grad_k, grad_v, grad_g, grad_beta, grad_initial_state, nullptr,
+                   B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, do_dtype == GDN_BF16 ? 1 : 0,
+                   per_channel ? 1 : 0};
+    gdn_status st = check_bwd(a, dtype, do_dtype, fn);
+    if (st != GDN_OK) return st;
+    const bool any_tokens = (long)a.B * a.T > 0;
+    if (any_tokens && (!q || !k || !v || !g || !beta || !grad_o || !grad_q || !grad_k || !grad_v || !grad_g ||
+                       !grad_beta))
+        return fail(GDN_ERR_INVALID_ARG, "%s: q, k, v, g, beta, grad_o and the token gradients must be non-NULL", fn);
+    const size_t es = dtype == GDN_BF16 ? 2 : 4, des = do_dtype == GDN_BF16 ? 2 : 4;
+    if (any_tokens && (!aligned(q, es) || !aligned(k, es) || !aligned(v, es) || !aligned(grad_o, des) ||
+                       !aligned(g, 4) || !aligned(beta, 4) || !aligned(grad_q, 4) || !aligned(grad_k, 4) ||
+                       !aligned(grad_v, 4) || !aligned(grad_g, 4) || !aligned(grad_beta, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "%s: a tensor is not aligned to its element size", fn);
+    if ((initial_state && !aligned(initial_state, 4)) || (grad_final_state && !aligned(grad_final_state, 4)) ||
+        (grad_initial_state && !aligned(grad_initial_state, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "%s: a state buffer is not 4-byte aligned", fn);
+    const size_t need = gdn::bwd_workspace_bytes(a);
+    if (workspace && workspace_bytes < need)
+        return fail(GDN_ERR_INVALID_ARG, "%s: workspace of %zu bytes is smaller than the %zu needed", fn,
+                    workspace_bytes, need);
+    if (workspace && !aligned(workspace, 256))
+        return fail(GDN_ERR_INVALID_ARG, "%s: workspace is not 256-byte aligned", fn);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ws = workspace;
+    cudaError_t e = cudaSuccess;
+    if (!ws && need > 0) {
+        e = cudaMallocAsync(&ws, need, s);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    a.ck = static_cast<float*>(ws);
+    e = gdn::launch_chunk_bwd(a, s);
+    if (!workspace && ws) {
+        const cudaError_t e2 = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+}
+
+gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
+                                        int n_seqs, size_t* bytes) {
+    const char* fn = "gdn_chunk_bwd_workspace_size";
+    if (!bytes) return fail(GDN_ERR_INVALID_ARG, "%s: bytes is NULL", fn);
+    if (n_seqs < 0) return fail(GDN_ERR_INVALID_ARG, "%s: n_seqs must be >= 0 (got %d)", fn, n_seqs);
+    const int32_t* cu = n_seqs > 0 ? reinterpret_cast<const int32_t*>(uintptr_t(1) << 20) : nullptr;
+    gdn::BwdArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, 1.0f, nullptr, nullptr, nullptr, cu, n_seqs,
+                   nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                   B, T, H, d_k, d_v, chunk_size, 0, 0, per_channel ? 1 : 0};
+    gdn_status st = check_bwd(a, GDN_F32, GDN_F32, fn);
+    if (st != GDN_OK) return st;
+    *bytes = gdn::bwd_workspace_bytes(a);
     return ok();
 }
 

@@ -95,4 +95,39 @@ cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t s);
 cudaError_t tc_read_and_clear_status(unsigned* value, bool clear);
 cudaError_t tp_read_and_clear_status(unsigned* value, bool clear);
 
+// One chunk-backward request, already validated by api.cu.  Gradients are of
+// L = <dO, o> + <dhT, final state> with respect to every input of the forward.
+struct BwdArgs {
+    const void* q;          // [B, T, H, dk]
+    const void* k;          // [B, T, H, dk]
+    const void* v;          // [B, T, H, dv]
+    const float* g;         // [B, T, H] or [B, T, H, dk] (per_channel)
+    const float* beta;      // [B, T, H]
+    float scale;
+    const float* h0;        // [N, H, dk, dv] or nullptr
+    const void* dO;         // [B, T, H, dv]
+    const float* dhT;       // [N, H, dk, dv] or nullptr (zero)
+    const int32_t* cu;      // [n_seqs + 1] device or nullptr
+    int n_seqs;
+    float* gq;              // [B, T, H, dk]
+    float* gk;              // [B, T, H, dk]
+    float* gv;              // [B, T, H, dv]
+    float* gg;              // like g
+    float* gbeta;           // [B, T, H]
+    float* gh0;             // [N, H, dk, dv] or nullptr
+    float* ck;              // chunk-entry state checkpoints (workspace)
+    int B, T, H, dk, dv, C;
+    int bf16;               // q, k, v dtype: 1 bf16, 0 fp32
+    int do_bf16;            // dO dtype
+    int per_channel;
+    int N() const { return cu ? n_seqs : B; }
+};
+
+// Chunk backward (chunk_bwd.cu).
+size_t bwd_smem_bytes(int C, int dk, bool per_channel);
+// The chunk the backward takes when the caller leaves it open (0 if none fits one CTA's shared memory).
+int bwd_auto_chunk(int dk, bool per_channel);
+size_t bwd_workspace_bytes(const BwdArgs& a);
+cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t s);
+
 }  // namespace gdn

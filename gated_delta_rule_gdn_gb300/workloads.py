@@ -23,6 +23,8 @@ stand-ins for model activations: no dataset or trained weights are involved.
   §3.1, eq. 5.
 * KDA gate: log gamma = -exp(N(0, 0.5)) * softplus(N(0, 1)), per key channel.
 * Initial states ~ N(0, sigma), where sigma is a standard deviation.
+* Upstream gradients of a backward problem: dO ~ N(0, 1) in the storage dtype,
+  and the final-state gradient ~ N(0, sigma) in fp32.
 """
 from __future__ import annotations
 
@@ -34,7 +36,7 @@ import numpy as np
 import torch
 
 __all__ = [
-    "ChunkWorkload", "DecodeWorkload", "CONFIGS", "chunk_inputs", "decode_constants",
+    "ChunkWorkload", "DecodeWorkload", "CONFIGS", "chunk_inputs", "chunk_output_grads", "decode_constants",
     "decode_step_inputs", "varlen_lengths", "config",
 ]
 
@@ -190,6 +192,23 @@ def chunk_inputs(w: ChunkWorkload, seed: int = 0, *, T: Optional[int] = None, H:
         "N": N,
     }
     return out
+
+
+def chunk_output_grads(x: dict, seed: int = 1, dhT_std: float = 1.0) -> dict:
+    """Draw the upstream gradients for the chunk problem ``x`` (from chunk_inputs).
+
+    From ``np.random.default_rng(seed)``, in this order: d_o ~ N(0, 1) with v's shape and dtype, then
+    d_final_state ~ N(0, dhT_std) [N, H, dk, dv] fp32 (None when dhT_std is 0).
+    """
+    rng = np.random.default_rng(seed)
+    B, T, H, dv = x["v"].shape
+    dk = x["q"].shape[-1]
+    d_o = rng.standard_normal((B, T, H, dv), dtype=np.float32)
+    dhT = None
+    if dhT_std > 0:
+        dhT = rng.standard_normal((x["N"], H, dk, dv), dtype=np.float32) * np.float32(dhT_std)
+    return {"d_o": torch.from_numpy(d_o).to(x["v"].dtype),
+            "d_final_state": None if dhT is None else torch.from_numpy(dhT)}
 
 
 def decode_constants(w: DecodeWorkload, seed: int = 0) -> dict:

@@ -338,6 +338,58 @@ gdn_status gdn_chunk_workspace_size(int per_channel, int B, int T, int H, int d_
                                     gdn_dtype dtype, gdn_dtype o_dtype, int n_seqs, gdn_algo requested,
                                     size_t* bytes);
 
+/*
+ * gdn_chunk_bwd -- gradients of the chunk forward (gdn_chunk_fwd with
+ * per_channel = 0, kda_chunk_fwd with per_channel = 1).  The pages give the
+ * chunkwise backward of the ungated delta rule ("阅读笔记：DeltaNet 在 FLA 中的
+ * 代码实现", 二、反向传播, steps 1-6); this call computes the same gradients for
+ * the gated forms.  It computes the gradients of
+ *     L = sum <grad_o, o> + sum <grad_final_state, final state>
+ * with respect to q, k, v, g, beta and initial_state, where o and the final
+ * state are those of the forward with the same inputs.  It takes the forward's
+ * inputs, not its outputs: a first kernel recomputes the state entering every
+ * chunk into the workspace, a second walks the chunks from the last to the
+ * first.  All arithmetic is fp32.
+ *   q, k, v, g, beta, scale, initial_state, cu_seqlens, n_seqs, B, T, H, d_k,
+ *   d_v, dtype: as gdn_chunk_fwd / kda_chunk_fwd (g [B, T, H] or
+ *   [B, T, H, d_k] by per_channel).
+ *   grad_o            [B, T, H, d_v] device, of type do_dtype (GDN_F32 or GDN_BF16).
+ *   grad_final_state  [N, H, d_k, d_v] fp32 device, or NULL (zero).
+ *   grad_q, grad_k    [B, T, H, d_k] fp32 device, written.
+ *   grad_v            [B, T, H, d_v] fp32 device, written.
+ *   grad_g            fp32 device, the shape of g, written.
+ *   grad_beta         [B, T, H] fp32 device, written.
+ *   grad_initial_state  [N, H, d_k, d_v] fp32 device, or NULL (not written).
+ *   chunk_size        16 or 32, or 0: the largest that fits one CTA's shared
+ *                     memory.  It sets the granularity of the recomputation,
+ *                     not the result (which is exact up to rounding).
+ *   workspace         device memory for the chunk-entry states, 256-byte
+ *                     aligned, at least gdn_chunk_bwd_workspace_size bytes;
+ *                     NULL: allocated and freed on `stream` for the call.
+ * Tokens of a packed sequence only see their own sequence, as in the forward.
+ * Every output is written in full (rows of empty sequences have none).
+ * Errors: GDN_ERR_INVALID_ARG for NULL or misaligned buffers, bad sizes or a
+ * short workspace; GDN_ERR_UNSUPPORTED for head sizes above 256 or a
+ * (chunk_size, d_k) pair whose shared memory does not fit one CTA; GDN_ERR_CUDA
+ * if a launch fails.  Nothing is written unless the status is GDN_OK.
+ */
+gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, float scale, const float* initial_state, const void* grad_o,
+                         const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
+                         float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
+                         int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                         gdn_dtype do_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_chunk_bwd_workspace_size -- bytes of the gdn_chunk_bwd workspace: one
+ * fp32 [d_k, d_v] state per (chunk slot, head), with B * (ceil(T / C) + 1)
+ * slots for a batch and floor(T / C) + 2 n_seqs for packed sequences (C the
+ * chunk the call takes; chunk_size 0 as in gdn_chunk_bwd).  n_seqs is 0 for a
+ * call without cu_seqlens.
+ */
+gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
+                                        int n_seqs, size_t* bytes);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* gdn_last_error(void);
 

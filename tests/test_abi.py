@@ -185,3 +185,43 @@ def test_head_sizes_up_to_256_and_the_generic_kernels_shared_memory(lib):
     assert "shared memory" in _binding.last_error()
     with pytest.raises(_binding.GdnError):
         _binding.chunk_plan(False, 1, 300, 2, 257, 64, 64, bf)
+
+
+def _bwd(lib, **kw):
+    a = dict(pc=0, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=1.0, h0=None, do=FAKE, dhT=None, cu=None, n=0,
+             gq=FAKE, gk=FAKE, gv=FAKE, gg=FAKE, gb=FAKE, gh0=None, B=1, T=64, H=1, dk=64, dv=64, C=0, dtype=1,
+             dodt=1, ws=FAKE, wsb=16)
+    a.update(kw)
+    return lib.gdn_chunk_bwd(a["pc"], a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["h0"], a["do"],
+                             a["dhT"], a["cu"], a["n"], a["gq"], a["gk"], a["gv"], a["gg"], a["gb"], a["gh0"], a["B"],
+                             a["T"], a["H"], a["dk"], a["dv"], a["C"], a["dtype"], a["dodt"], a["ws"], a["wsb"], None)
+
+
+# The default arguments above carry a 16-byte workspace, too small for any request, so each call fails its
+# checks before a launch even where the case under test would pass.
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(dk=0), 2), (dict(dv=257), 2), (dict(dk=257), 2),
+    (dict(C=48), 2), (dict(C=64), 2), (dict(pc=1, dk=256, C=32), 2), (dict(dtype=7), 1), (dict(dodt=5), 1),
+    (dict(q=None), 1), (dict(do=None), 1), (dict(gq=None), 1), (dict(gg=None), 1), (dict(gb=None), 1),
+    (dict(do=FAKE + 1), 1), (dict(gq=FAKE + 2), 1), (dict(gh0=FAKE + 2), 1), (dict(h0=FAKE + 1), 1),
+    (dict(scale=float("nan")), 1), (dict(cu=FAKE, B=2, n=2), 1), (dict(cu=FAKE, n=0), 1), (dict(cu=FAKE + 1, n=1), 1),
+    (dict(), 1), (dict(ws=FAKE + 16, wsb=1 << 40), 1),
+])
+def test_backward_argument_checks(lib, kw, status):
+    assert _bwd(lib, **kw) == status
+    assert _binding.last_error()
+    if "pc" not in kw:
+        assert _bwd(lib, pc=1, **kw) == status
+
+
+def test_backward_workspace_sizes(lib):
+    # one fp32 [d_k, d_v] state per (chunk slot, head)
+    state = 128 * 128 * 4
+    assert _binding.bwd_workspace_size(False, 4, 4096, 16, 128, 128) == 4 * (4096 // 32 + 1) * 16 * state
+    assert _binding.bwd_workspace_size(False, 4, 4096, 16, 128, 128, 16) == 4 * (4096 // 16 + 1) * 16 * state
+    assert _binding.bwd_workspace_size(True, 1, 65536, 32, 128, 128, 0, 8) == (65536 // 32 + 16) * 32 * state
+    assert _binding.bwd_workspace_size(False, 2, 0, 3, 64, 32) == 2 * 1 * 3 * 64 * 32 * 4
+    # d_k = 256 with the per-channel gate takes chunk 16 on its own; chunk 32 does not fit one CTA
+    assert _binding.bwd_workspace_size(True, 1, 100, 2, 256, 128) == 1 * (-(-100 // 16) + 1) * 2 * 256 * 128 * 4
+    with pytest.raises(_binding.GdnError, match="shared memory"):
+        _binding.bwd_workspace_size(True, 1, 100, 2, 256, 128, 32)
