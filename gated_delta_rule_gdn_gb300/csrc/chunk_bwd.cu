@@ -75,27 +75,28 @@ __host__ __device__ inline long checkpoint_slots(int B, int T, int C, int n_seqs
     return varlen ? (long)(T / C) + 2L * n_seqs : (long)B * ((T + C - 1) / C + 1);
 }
 
-// Shared-memory carve-up, in floats.  The backward kernel uses all of it; the checkpoint kernel the K, V, gate,
+// Shared-memory carve-up, in floats.  Q and K rows (and the per-channel gate rows) are padded to d_k + 1 floats, so
+// that lanes reading one column of consecutive rows hit distinct banks.  The backward kernel uses all of it; the checkpoint kernel the K, V, gate,
 // beta, KK, state and Delta parts.
 struct Lay {
     int Q, K, V, dO, G, E, F, Bt, KK, P, Ex, dP, dA, H, dH, Z, D, Y, pq, pk, pb, pw, pbeta, us, red, total;
 };
 
 __host__ __device__ inline Lay make_lay(int C, int dk, bool per_channel) {
-    const int gc = per_channel ? dk : 1, cc = C * (C + 1), ct = C * kTS, ht = dk * kTS;
+    const int lg = per_channel ? dk + 1 : 1, cc = C * (C + 1), ct = C * kTS, ht = dk * kTS;
     Lay l;
     int o = 0;
-    l.Q = o; o += C * dk;
-    l.K = o; o += C * dk;
+    l.Q = o; o += C * (dk + 1);
+    l.K = o; o += C * (dk + 1);
     l.V = o; o += ct;
     l.dO = o; o += ct;
-    l.G = o; o += C * gc;
-    l.E = o; o += C * gc;
-    l.F = o; o += C * gc;
+    l.G = o; o += C * lg;
+    l.E = o; o += C * lg;
+    l.F = o; o += C * lg;
     l.Bt = o; o += C;
     l.KK = o; o += cc;
     l.P = o; o += cc;
-    l.Ex = o; o += cc;
+    l.Ex = o; o += per_channel ? 0 : cc;   // exp(G_r - G_s), scalar gate only
     l.dP = o; o += cc;
     l.dA = o; o += cc;
     l.H = o; o += ht;
@@ -109,14 +110,14 @@ __host__ __device__ inline Lay make_lay(int C, int dk, bool per_channel) {
     l.pw = o; o += C * dk;
     l.pbeta = o; o += C;
     l.us = o; o += dk;
-    l.red = o; o += 2 * C;
+    l.red = o; o += 2 * C + 1;
     l.total = o;
     return l;
 }
 
 __host__ __device__ inline int ck_floats(int C, int dk, bool per_channel) {
-    const int gc = per_channel ? dk : 1;
-    return C * dk + C * kTS + 3 * C * gc + C + C * (C + 1) + dk * kTS + C * kTS;
+    const int lg = per_channel ? dk + 1 : 1;
+    return C * (dk + 1) + C * kTS + 3 * C * lg + C + C * (C + 1) + dk * kTS + C * kTS;
 }
 
 // ---- steps shared by both kernels -------------------------------------------------------------------
@@ -126,7 +127,7 @@ __host__ __device__ inline int ck_floats(int C, int dk, bool per_channel) {
 template <typename Tin, typename Tdo, bool PERCH, bool WITH_Q>
 __device__ __forceinline__ void load_chunk(const BwdArgs& a, const Geo& geo, int hh, long cs, int L, int j0, int bw,
                                            float* Qs, float* Ks, float* Vs, float* Os, float* Gs, float* Bs) {
-    const int C = a.C, dk = a.dk, dv = a.dv, H = a.H, gc = PERCH ? dk : 1;
+    const int C = a.C, dk = a.dk, dv = a.dv, H = a.H, gc = PERCH ? dk : 1, ld = dk + 1, lg = PERCH ? dk + 1 : 1;
     const Tin* q = static_cast<const Tin*>(a.q);
     const Tin* k = static_cast<const Tin*>(a.k);
     const Tin* v = static_cast<const Tin*>(a.v);
@@ -140,8 +141,8 @@ __device__ __forceinline__ void load_chunk(const BwdArgs& a, const Geo& geo, int
             kv = ld_f32<Tin>(k, off);
             if (WITH_Q) qv = ld_f32<Tin>(q, off);
         }
-        Ks[idx] = kv;
-        if (WITH_Q) Qs[idx] = qv;
+        Ks[r * ld + c] = kv;
+        if (WITH_Q) Qs[r * ld + c] = qv;
     }
     for (int idx = threadIdx.x; idx < C * kBV; idx += kThreads) {
         const int r = idx / kBV, j = idx % kBV;
@@ -157,7 +158,7 @@ __device__ __forceinline__ void load_chunk(const BwdArgs& a, const Geo& geo, int
     for (int idx = threadIdx.x; idx < C * gc; idx += kThreads) {
         const int r = idx / gc, c = idx % gc;
         const size_t tok = tok0 + (size_t)r * H;
-        Gs[idx] = (r < L) ? a.g[PERCH ? tok * dk + c : tok] : 0.f;
+        Gs[r * lg + c] = (r < L) ? a.g[PERCH ? tok * dk + c : tok] : 0.f;
     }
     for (int r = threadIdx.x; r < C; r += kThreads) Bs[r] = (r < L) ? a.beta[tok0 + (size_t)r * H] : 0.f;
 }
@@ -178,21 +179,21 @@ __device__ __forceinline__ void store_state(float* dst, const float* Hs, int dk,
 }
 
 // Within-chunk prefix sum of the log gate, one channel per thread.
-__device__ __forceinline__ void gate_prefix(float* Gs, int C, int gc) {
+__device__ __forceinline__ void gate_prefix(float* Gs, int C, int gc, int lg) {
     for (int c = threadIdx.x; c < gc; c += kThreads) {
         float acc = 0.f;
-        for (int r = 0; r < C; ++r) { acc += Gs[r * gc + c]; Gs[r * gc + c] = acc; }
+        for (int r = 0; r < C; ++r) { acc += Gs[r * lg + c]; Gs[r * lg + c] = acc; }
     }
 }
 
 // E = exp(G), F = exp(G_L - G) (G_L: the last valid row).
-__device__ __forceinline__ void gate_factors(const float* Gs, float* Es, float* Fs, int C, int gc, int L) {
+__device__ __forceinline__ void gate_factors(const float* Gs, float* Es, float* Fs, int C, int gc, int lg, int L) {
     for (int c = threadIdx.x; c < gc; c += kThreads) {
-        const float gl = Gs[(L - 1) * gc + c];
+        const float gl = Gs[(L - 1) * lg + c];
         for (int r = 0; r < C; ++r) {
-            const float gr = Gs[r * gc + c];
-            Es[r * gc + c] = expf(gr);
-            Fs[r * gc + c] = expf(gl - gr);
+            const float gr = Gs[r * lg + c];
+            Es[r * lg + c] = expf(gr);
+            Fs[r * lg + c] = expf(gl - gr);
         }
     }
 }
@@ -202,17 +203,17 @@ __device__ __forceinline__ void gate_factors(const float* Gs, float* Es, float* 
 template <bool PERCH, bool WITH_P>
 __device__ __forceinline__ void pair_products(const float* Qs, const float* Ks, const float* Gs, float* KK, float* Pm,
                                               float* Ex, int C, int dk, float scale) {
-    const int gc = PERCH ? dk : 1;
+    const int ld = dk + 1, lg = PERCH ? dk + 1 : 1;
     for (int idx = threadIdx.x; idx < C * C; idx += kThreads) {
         const int r = idx / C, s = idx % C;
         float kk = 0.f, qk = 0.f, e0 = 0.f;
         if (s <= r) {
             for (int c = 0; c < dk; ++c) {
-                const float ks = Ks[s * dk + c];
+                const float ks = Ks[s * ld + c];
                 float e = 1.f;
-                if (PERCH) e = expf(Gs[r * gc + c] - Gs[s * gc + c]);
-                kk = fmaf(Ks[r * dk + c] * e, ks, kk);
-                if (WITH_P) qk = fmaf(Qs[r * dk + c] * e, ks, qk);
+                if (PERCH) e = expf(Gs[r * lg + c] - Gs[s * lg + c]);
+                kk = fmaf(Ks[r * ld + c] * e, ks, kk);
+                if (WITH_P) qk = fmaf(Qs[r * ld + c] * e, ks, qk);
             }
             if (!PERCH) {
                 e0 = expf(Gs[r] - Gs[s]);
@@ -232,11 +233,11 @@ __device__ __forceinline__ void pair_products(const float* Qs, const float* Ks, 
 template <bool PERCH>
 __device__ __forceinline__ void residual(const float* Ks, const float* Es, const float* Vs, const float* Hs,
                                          const float* Bs, float* Zs, float* Ds, int C, int dk) {
-    const int gc = PERCH ? dk : 1;
+    const int ld = dk + 1, lg = PERCH ? dk + 1 : 1;
     for (int idx = threadIdx.x; idx < C * kBV; idx += kThreads) {
         const int i = idx / kBV, j = idx % kBV;
         float s = 0.f;
-        for (int c = 0; c < dk; ++c) s = fmaf(Ks[i * dk + c] * Es[i * gc + (PERCH ? c : 0)], Hs[c * kTS + j], s);
+        for (int c = 0; c < dk; ++c) s = fmaf(Ks[i * ld + c] * Es[i * lg + (PERCH ? c : 0)], Hs[c * kTS + j], s);
         const float z = Vs[i * kTS + j] - s;
         if (Zs) Zs[i * kTS + j] = z;
         Ds[i * kTS + j] = Bs[i] * z;
@@ -279,13 +280,13 @@ __device__ __forceinline__ void solve_upper_t(const float* KK, const float* Bs, 
 template <typename Tin, bool PERCH>
 __global__ void __launch_bounds__(kThreads) bwd_checkpoint_kernel(const BwdArgs a, int n_tiles) {
     extern __shared__ float smem[];
-    const int C = a.C, dk = a.dk, dv = a.dv, H = a.H, gc = PERCH ? dk : 1;
+    const int C = a.C, dk = a.dk, dv = a.dv, H = a.H, gc = PERCH ? dk : 1, ld = dk + 1, lg = PERCH ? dk + 1 : 1;
     float* Ks = smem;
-    float* Vs = Ks + C * dk;
+    float* Vs = Ks + C * ld;
     float* Gs = Vs + C * kTS;
-    float* Es = Gs + C * gc;
-    float* Fs = Es + C * gc;
-    float* Bs = Fs + C * gc;
+    float* Es = Gs + C * lg;
+    float* Fs = Es + C * lg;
+    float* Bs = Fs + C * lg;
     float* KK = Bs + C;
     float* Hs = KK + C * (C + 1);
     float* Ds = Hs + dk * kTS;
@@ -308,9 +309,9 @@ __global__ void __launch_bounds__(kThreads) bwd_checkpoint_kernel(const BwdArgs 
         __syncthreads();
         load_chunk<Tin, Tin, PERCH, false>(a, geo, hh, cs, L, j0, bw, nullptr, Ks, Vs, nullptr, Gs, Bs);
         __syncthreads();
-        gate_prefix(Gs, C, gc);
+        gate_prefix(Gs, C, gc, lg);
         __syncthreads();
-        gate_factors(Gs, Es, Fs, C, gc, L);
+        gate_factors(Gs, Es, Fs, C, gc, lg, L);
         pair_products<PERCH, false>(nullptr, Ks, Gs, KK, nullptr, nullptr, C, dk, 0.f);
         __syncthreads();
         residual<PERCH>(Ks, Es, Vs, Hs, Bs, nullptr, Ds, C, dk);
@@ -320,8 +321,8 @@ __global__ void __launch_bounds__(kThreads) bwd_checkpoint_kernel(const BwdArgs 
         // h <- diag(E_L) h + (K * F)^T Delta
         for (int idx = threadIdx.x; idx < dk * kBV; idx += kThreads) {
             const int c = idx / kBV, j = idx % kBV, cc = PERCH ? c : 0;
-            float s = Es[(L - 1) * gc + cc] * Hs[c * kTS + j];
-            for (int m = 0; m < L; ++m) s = fmaf(Ks[m * dk + c] * Fs[m * gc + cc], Ds[m * kTS + j], s);
+            float s = Es[(L - 1) * lg + cc] * Hs[c * kTS + j];
+            for (int m = 0; m < L; ++m) s = fmaf(Ks[m * ld + c] * Fs[m * lg + cc], Ds[m * kTS + j], s);
             Hs[c * kTS + j] = s;
         }
         __syncthreads();
@@ -335,7 +336,7 @@ template <typename Tin, typename Tdo, bool PERCH>
 __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdArgs a, int n_tiles) {
     extern __shared__ float smem[];
     cg::cluster_group cluster = cg::this_cluster();
-    const int C = a.C, dk = a.dk, dv = a.dv, H = a.H, gc = PERCH ? dk : 1;
+    const int C = a.C, dk = a.dk, dv = a.dv, H = a.H, gc = PERCH ? dk : 1, ld = dk + 1, lg = PERCH ? dk + 1 : 1;
     const Lay ly = make_lay(C, dk, PERCH);
     float* Qs = smem + ly.Q;  float* Ks = smem + ly.K;  float* Vs = smem + ly.V;  float* Os = smem + ly.dO;
     float* Gs = smem + ly.G;  float* Es = smem + ly.E;  float* Fs = smem + ly.F;  float* Bs = smem + ly.Bt;
@@ -369,9 +370,9 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdArgs a, in
         load_chunk<Tin, Tdo, PERCH, true>(a, geo, hh, cs, L, j0, bw, Qs, Ks, Vs, Os, Gs, Bs);
         load_state(Hs, ck + (size_t)ci * sstride, dk, dv, j0, bw);
         __syncthreads();
-        gate_prefix(Gs, C, gc);
+        gate_prefix(Gs, C, gc, lg);
         __syncthreads();
-        gate_factors(Gs, Es, Fs, C, gc, L);
+        gate_factors(Gs, Es, Fs, C, gc, lg, L);
         pair_products<PERCH, true>(Qs, Ks, Gs, KK, Pm, Ex, C, dk, scale);
         __syncthreads();
         // Z, R = beta Z (into Delta), and dDelta = P^T dO + (K * F) dh (into Y)
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdArgs a, in
             float s = 0.f;
             for (int r = i; r < L; ++r) s = fmaf(Pm[r * (C + 1) + i], Os[r * kTS + j], s);
             for (int c = 0; c < dk; ++c)
-                s = fmaf(Ks[i * dk + c] * Fs[i * gc + (PERCH ? c : 0)], dHs[c * kTS + j], s);
+                s = fmaf(Ks[i * ld + c] * Fs[i * lg + (PERCH ? c : 0)], dHs[c * kTS + j], s);
             Ys[i * kTS + j] = s;
         }
         __syncthreads();
@@ -431,21 +432,21 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdArgs a, in
             }
             float sq = 0.f, sar = 0.f, skp = 0.f, sac = 0.f;
             for (int s = 0; s < r; ++s) {
-                const float e = PERCH ? expf(Gs[r * gc + c] - Gs[s * gc + c]) : Ex[r * (C + 1) + s];
-                const float ke = Ks[s * dk + c] * e;
+                const float e = PERCH ? expf(Gs[r * lg + c] - Gs[s * lg + c]) : Ex[r * (C + 1) + s];
+                const float ke = Ks[s * ld + c] * e;
                 sq = fmaf(dPm[r * (C + 1) + s], ke, sq);
                 sar = fmaf(dAm[r * (C + 1) + s], ke, sar);
             }
             for (int u = r + 1; u < L; ++u) {
-                const float e = PERCH ? expf(Gs[u * gc + c] - Gs[r * gc + c]) : Ex[u * (C + 1) + r];
-                skp = fmaf(dPm[u * (C + 1) + r], Qs[u * dk + c] * e, skp);
-                sac = fmaf(dAm[u * (C + 1) + r] * Bs[u], Ks[u * dk + c] * e, sac);
+                const float e = PERCH ? expf(Gs[u * lg + c] - Gs[r * lg + c]) : Ex[u * (C + 1) + r];
+                skp = fmaf(dPm[u * (C + 1) + r], Qs[u * ld + c] * e, skp);
+                sac = fmaf(dAm[u * (C + 1) + r] * Bs[u], Ks[u * ld + c] * e, sac);
             }
             sq *= scale;
             skp *= scale;
             sar *= Bs[r];
-            const float E = Es[r * gc + cc], F = Fs[r * gc + cc], br = Bs[r];
-            const float qr = Qs[r * dk + c], kr = Ks[r * dk + c];
+            const float E = Es[r * lg + cc], F = Fs[r * lg + cc], br = Bs[r];
+            const float qr = Qs[r * ld + c], kr = Ks[r * ld + c];
             const float dg0 = scale * dPm[r * (C + 1) + r];
             const float read = scale * E * xo;
             pq[idx] = read + sq + dg0 * kr;
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdArgs a, in
         for (int c = tid; c < dk; c += kThreads) {
             float s = 0.f;
             for (int j = 0; j < kBV; ++j) s = fmaf(dHs[c * kTS + j], Hs[c * kTS + j], s);
-            us[c] = Es[(L - 1) * gc + (PERCH ? c : 0)] * s;
+            us[c] = Es[(L - 1) * lg + (PERCH ? c : 0)] * s;
         }
         // tile part of dbeta: Y_r . Z_r + sum_{s<r} dA[r][s] KK[r][s]
         for (int r = tid; r < L; r += kThreads) {
@@ -470,13 +471,32 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdArgs a, in
         // dh <- diag(E_L) dh + scale (Q * E)^T dO - (K * E)^T diag(beta) Y
         for (int idx = tid; idx < dk * kBV; idx += kThreads) {
             const int c = idx / kBV, j = idx % kBV, cc = PERCH ? c : 0;
-            float s = Es[(L - 1) * gc + cc] * dHs[c * kTS + j];
+            float s = Es[(L - 1) * lg + cc] * dHs[c * kTS + j];
             for (int r = 0; r < L; ++r) {
-                const float e = Es[r * gc + cc];
-                s = fmaf(scale * Qs[r * dk + c] * e, Os[r * kTS + j], s);
-                s = fmaf(-Ks[r * dk + c] * e * Bs[r], Ys[r * kTS + j], s);
+                const float e = Es[r * lg + cc];
+                s = fmaf(scale * Qs[r * ld + c] * e, Os[r * kTS + j], s);
+                s = fmaf(-Ks[r * ld + c] * e * Bs[r], Ys[r * kTS + j], s);
             }
             dHs[c * kTS + j] = s;
+        }
+        if (!PERCH) {
+            // scalar gate: this tile's sums over the channels, per row (red[r], red[C + r]) and of us (red[2C])
+            const int warp = tid >> 5, lane = tid & 31;
+            for (int r = warp; r <= L; r += kThreads / 32) {
+                float sb = 0.f, sw = 0.f;
+                if (r < L) {
+                    for (int c = lane; c < dk; c += 32) { sb += pb[r * dk + c]; sw += pw[r * dk + c]; }
+                } else {
+                    for (int c = lane; c < dk; c += 32) sb += us[c];
+                }
+                for (int o = 16; o > 0; o >>= 1) {
+                    sb += __shfl_xor_sync(0xffffffffu, sb, o);
+                    sw += __shfl_xor_sync(0xffffffffu, sw, o);
+                }
+                if (lane == 0) {
+                    if (r < L) { red[r] = sb; red[C + r] = sw; } else { red[2 * C] = sb; }
+                }
+            }
         }
         cluster.sync();  // every tile part of this chunk is in shared memory
         {
@@ -500,51 +520,58 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdArgs a, in
             // dg[u] = sum_{r >= u} pb[r] + sum_{s < u} pw[s] + us, over the tiles (and the channels for the scalar
             // gate)
             if (PERCH) {
-                for (int c = rank * kThreads + tid; c < dk; c += stride) {
+                // this CTA takes channels [c0, c0 + cw): first the tile sums of pb and pw for every (row, channel),
+                // all loads independent, into the Q / K space (no other CTA reads it), then one thread per channel
+                // runs the two prefix sums over the rows
+                const int cw0 = (dk + n_tiles - 1) / n_tiles, c0 = rank * cw0, cw = max(0, min(dk - c0, cw0));
+                float* sbuf = Qs;
+                float* wbuf = Qs + C * cw0;
+                for (int idx = tid; idx < L * cw; idx += kThreads) {
+                    const int r = idx / cw, c = c0 + idx % cw;
+                    float sb = 0.f, sw = 0.f;
+                    for (int t = 0; t < n_tiles; ++t) {
+                        sb += cluster.map_shared_rank(pb, t)[r * dk + c];
+                        sw += cluster.map_shared_rank(pw, t)[r * dk + c];
+                    }
+                    sbuf[idx] = sb;
+                    wbuf[idx] = sw;
+                }
+                __syncthreads();
+                for (int cl = tid; cl < cw; cl += kThreads) {
+                    const int c = c0 + cl;
                     float pre = 0.f;
                     for (int t = 0; t < n_tiles; ++t) pre += cluster.map_shared_rank(us, t)[c];
                     for (int u = 0; u < L; ++u) {
-                        a.gg[(tok0 + (size_t)u * H) * dk + c] = pre;
-                        for (int t = 0; t < n_tiles; ++t) pre += cluster.map_shared_rank(pw, t)[u * dk + c];
-                    }
-                    float acc = 0.f;
-                    for (int r = L - 1; r >= 0; --r) {
-                        for (int t = 0; t < n_tiles; ++t) acc += cluster.map_shared_rank(pb, t)[r * dk + c];
-                        a.gg[(tok0 + (size_t)r * H) * dk + c] += acc;
-                    }
-                }
-            } else if (rank == 0 && tid < 32) {
-                // one warp: each row's sums over channels and tiles, then the two prefix sums over rows
-                float ut = 0.f;
-                for (int c = tid; c < dk; c += 32)
-                    for (int t = 0; t < n_tiles; ++t) ut += cluster.map_shared_rank(us, t)[c];
-                for (int o = 16; o > 0; o >>= 1) ut += __shfl_xor_sync(0xffffffffu, ut, o);
-                for (int r = 0; r < L; ++r) {
-                    float sb = 0.f, sw = 0.f;
-                    for (int c = tid; c < dk; c += 32)
-                        for (int t = 0; t < n_tiles; ++t) {
-                            sb += cluster.map_shared_rank(pb, t)[r * dk + c];
-                            sw += cluster.map_shared_rank(pw, t)[r * dk + c];
-                        }
-                    for (int o = 16; o > 0; o >>= 1) {
-                        sb += __shfl_xor_sync(0xffffffffu, sb, o);
-                        sw += __shfl_xor_sync(0xffffffffu, sw, o);
-                    }
-                    if (tid == 0) { red[r] = sb; red[C + r] = sw; }
-                }
-                if (tid == 0) {
-                    float pre = ut;
-                    for (int u = 0; u < L; ++u) {
-                        const float w = red[C + u];
-                        red[C + u] = pre;
+                        const float w = wbuf[u * cw + cl];
+                        wbuf[u * cw + cl] = pre;
                         pre += w;
                     }
                     float acc = 0.f;
                     for (int r = L - 1; r >= 0; --r) {
-                        acc += red[r];
-                        a.gg[tok0 + (size_t)r * H] = acc + red[C + r];
+                        acc += sbuf[r * cw + cl];
+                        a.gg[(tok0 + (size_t)r * H) * dk + c] = acc + wbuf[r * cw + cl];
                     }
                 }
+            } else if (rank == 0 && tid < 32) {
+                // one warp, lane r = row r (L <= 32): the tile sums of the per-row channel sums, then a reverse
+                // inclusive scan of pb and a forward exclusive scan of pw across the lanes
+                const int lane = tid;
+                float sb = 0.f, sw = 0.f, ut = 0.f;
+                for (int t = 0; t < n_tiles; ++t) {
+                    const float* rr = cluster.map_shared_rank(red, t);
+                    if (lane < L) { sb += rr[lane]; sw += rr[C + lane]; }
+                    ut += rr[2 * C];
+                }
+                float rev = sb, fwd = sw;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float x = __shfl_down_sync(0xffffffffu, rev, o);
+                    const float y = __shfl_up_sync(0xffffffffu, fwd, o);
+                    if (lane + o < 32) rev += x;
+                    if (lane >= o) fwd += y;
+                }
+                float ex = __shfl_up_sync(0xffffffffu, fwd, 1);   // exclusive: the inclusive sum of the lane before
+                if (lane == 0) ex = 0.f;
+                if (lane < L) a.gg[tok0 + (size_t)lane * H] = rev + ex + ut;
             }
         }
         cluster.sync();  // no CTA overwrites its tile parts while another still reads them
