@@ -24,8 +24,8 @@ Inputs are seeded and synthetic, drawn by gated_delta_rule_gdn_gb300.workloads.
 * cpu_baseline: the fp64 C oracle on the host cores (rank 0, N = 1).
 * --impl reference: the oracle alone, timed as the reference arm.
 Workloads 6 and 7 time the chunk backward (gdn_chunk_bwd) on the shapes of
-workloads 1 and 3: one step is one backward call (the checkpoint kernel, then
-the backward walk).  It is fp32 SIMT arithmetic, so its roofline is the fp32
+workloads 1 and 3: one step is one backward call (three launches: the
+per-chunk prep, the two state walks, the per-chunk gradients).  It is fp32 SIMT arithmetic, so its roofline is the fp32
 FMA rate (152 SMs x 128 lanes x 2 flops x 2.07 GHz), against the algorithmic
 flops of the chunkwise backward given in _bwd_flops.
 With N > 1 (torchrun), every rank runs its own replica: weak scaling, and no
@@ -411,7 +411,7 @@ def run_bwd(args):
     d = {k: v.to(dev) for k, v in host.items()}
     per_channel = w.kind == "kda"
     n_seqs = 0 if x["cu_seqlens"] is None else x["cu_seqlens"].numel() - 1
-    C = 0
+    C = 16     # the chunk the library takes by default for d_k <= 256
     ws_bytes = gdn.bwd_workspace_size(per_channel, w.B, w.T, w.H, w.dk, w.dv, C, n_seqs)
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -477,11 +477,7 @@ def run_bwd(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
 
     tokens = w.B * w.T
-    try:   # the chunk the call took: 32 where it fits one CTA's shared memory, else 16
-        gdn.bwd_workspace_size(per_channel, 1, 64, 1, w.dk, w.dv, 32)
-        C_used = 32
-    except gdn.GdnError:
-        C_used = 16
+    C_used = C
     flops = _bwd_flops(w, C_used)
     achieved = flops / (ms / 1e3) / 1e12
     line = {
@@ -492,14 +488,15 @@ def run_bwd(args):
         "config": {"workload": _bwd_name(w), "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "chunk_size": C_used, "input_dtype": "bf16", "grad_dtype": "f32",
                    "l2": "flushed before each timed step (256 MiB device write, outside the events)",
-                   "kernel": "chunk_bwd", "launches_per_step": 2, "timed_region_wall_ms": t_wall * 1e3},
+                   "kernel": "chunk_bwd (prep, walks, gradients)", "launches_per_step": 3,
+                   "timed_region_wall_ms": t_wall * 1e3},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
                      "frac": achieved / ALU_PEAK_TFLOPS, "traffic": None,
                      "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz",
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * 2,
+        "gpu_launches": args.steps * 3,
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -475,11 +475,12 @@ gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, in
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 gdn_status gdn_device_status(int clear) {
-    unsigned v = 0, v2 = 0;
+    unsigned v = 0, v2 = 0, v3 = 0;
     cudaError_t e = gdn::tc_read_and_clear_status(&v, clear != 0);
     if (e == cudaSuccess) e = gdn::tp_read_and_clear_status(&v2, clear != 0);
+    if (e == cudaSuccess) e = gdn::bwd_read_and_clear_status(&v3, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_status");
-    v |= v2 << 16;
+    v |= (v2 << 16) | (v3 << 28);
     if (v != 0) return fail(GDN_ERR_TIMEOUT, "gdn_device_status: a kernel gave up a bounded wait (code 0x%x)", v);
     return ok();
 }

@@ -129,5 +129,6 @@ size_t bwd_smem_bytes(int C, int dk, bool per_channel);
 int bwd_auto_chunk(int dk, bool per_channel);
 size_t bwd_workspace_bytes(const BwdArgs& a);
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t s);
+cudaError_t bwd_read_and_clear_status(unsigned* value, bool clear);
 
 }  // namespace gdn

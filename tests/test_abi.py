@@ -215,13 +215,23 @@ def test_backward_argument_checks(lib, kw, status):
 
 
 def test_backward_workspace_sizes(lib):
-    # one fp32 [d_k, d_v] state per (chunk slot, head)
-    state = 128 * 128 * 4
-    assert _binding.bwd_workspace_size(False, 4, 4096, 16, 128, 128) == 4 * (4096 // 32 + 1) * 16 * state
-    assert _binding.bwd_workspace_size(False, 4, 4096, 16, 128, 128, 16) == 4 * (4096 // 16 + 1) * 16 * state
-    assert _binding.bwd_workspace_size(True, 1, 65536, 32, 128, 128, 0, 8) == (65536 // 32 + 16) * 32 * state
-    assert _binding.bwd_workspace_size(False, 2, 0, 3, 64, 32) == 2 * 1 * 3 * 64 * 32 * 4
-    # d_k = 256 with the per-channel gate takes chunk 16 on its own; chunk 32 does not fit one CTA
-    assert _binding.bwd_workspace_size(True, 1, 100, 2, 256, 128) == 1 * (-(-100 // 16) + 1) * 2 * 256 * 128 * 4
+    # per (chunk slot, head): the entry state and the gradient of h_out (fp32 [d_k, d_v] each); Delta, Y and Z
+    # (fp32 [C, d_v] each); a per-chunk record of the state-independent products.  So the size is affine in the
+    # number of slots and above the states and tiles alone.  The default chunk is 16.
+    def floor_bytes(slots, H, dk, dv, C):
+        return slots * H * (2 * dk * dv + 3 * C * dv) * 4
+    size = lambda *a: _binding.bwd_workspace_size(*a)
+    s1 = size(False, 4, 4096, 16, 128, 128)              # chunk 16: 4 x 257 slots
+    assert s1 == size(False, 4, 4096, 16, 128, 128, 16)
+    s2 = size(False, 8, 4096, 16, 128, 128)              # twice the slots
+    assert s2 == 2 * s1 and s1 > floor_bytes(4 * 257, 16, 128, 128, 16)
+    s32 = size(False, 4, 4096, 16, 128, 128, 32)         # chunk 32: 4 x 129 slots
+    assert s32 > floor_bytes(4 * 129, 16, 128, 128, 32)
+    sv = size(True, 1, 65536, 32, 128, 128, 0, 8)        # packed: floor(T / C) + 2 n_seqs slots
+    assert sv > floor_bytes(65536 // 16 + 16, 32, 128, 128, 16)
+    assert size(True, 1, 65536, 32, 128, 128, 0, 16) - sv == 16 * (sv // (65536 // 16 + 16))
+    assert size(False, 2, 0, 3, 64, 32) > 0
+    # d_k = 256 with the per-channel gate: chunk 32 does not fit one CTA
+    assert size(True, 1, 100, 2, 256, 128) == size(True, 1, 100, 2, 256, 128, 16)
     with pytest.raises(_binding.GdnError, match="shared memory"):
-        _binding.bwd_workspace_size(True, 1, 100, 2, 256, 128, 32)
+        size(True, 1, 100, 2, 256, 128, 32)
