@@ -83,13 +83,21 @@ def _alg_bytes(w) -> int:
     return token_heads * per_token_head + state
 
 
-TRAFFIC_SOURCES = ("chunk_two_pass.cu", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh", "recurrent_step.cu")
+# The kernel sources each recorded traffic figure depends on (the files that make the timed kernels' code).
+TRAFFIC_SOURCES = {
+    "chunk": ("chunk_two_pass.cu", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh"),
+    "decode": ("recurrent_step.cu", "gate_act.cuh"),
+}
 
 
-def sources_sha256() -> str:
-    """Hash of the kernel sources the recorded ncu traffic depends on."""
+def _traffic_kind(workload: str) -> str:
+    return "decode" if workload.startswith("decode") or "_decode_" in workload else "chunk"
+
+
+def sources_sha256(kind: str = "chunk") -> str:
+    """Hash of the kernel sources a recorded ncu traffic figure of this kind depends on."""
     h = hashlib.sha256()
-    for name in TRAFFIC_SOURCES:
+    for name in TRAFFIC_SOURCES[kind]:
         with open(os.path.join(ROOT, "gated_delta_rule_gdn_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -102,7 +110,8 @@ def _traffic_for(workload: str):
     try:
         with open(path) as f:
             rec = json.load(f)[workload]
-        return int(rec["dram_bytes_per_call"]) if rec["sources_sha256"] == sources_sha256() else None
+        ok = rec["sources_sha256"] == sources_sha256(_traffic_kind(workload))
+        return int(rec["dram_bytes_per_call"]) if ok else None
     except Exception:
         return None
 

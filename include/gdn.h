@@ -40,7 +40,8 @@
  *   - Buffers the call reads may not alias buffers it writes.  The one
  *     exception is gdn_recurrent_step's in-place state.
  *
- * No entry point allocates device memory.
+ * Device memory is allocated only where an entry point says so: a chunk call
+ * given no workspace allocates one on its stream and frees it there.
  */
 #ifndef GDN_GB300_H
 #define GDN_GB300_H
