@@ -57,6 +57,32 @@ template <> __device__ __forceinline__ float ld_f32<__nv_bfloat16>(const __nv_bf
 }
 
 __host__ __device__ inline int round4(int x) { return (x + 3) & ~3; }
+
+// x = hi + lo with hi and lo TF32 (the high part rounded to nearest, the low part the rounded remainder)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    const float r = x - __uint_as_float(hi);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// d (16 x 8) += A (16 x 8) B (8 x 8) to about fp32 accuracy from three TF32 warp products: A_hi B_hi + A_hi B_lo
+// + A_lo B_hi (the dropped A_lo B_lo is below fp32 rounding).  Fragments as in the PTX m16n8k8 layout
+// (lane = 4 g + t): A rows g, g + 8 and columns t, t + 4; B rows t, t + 4 and column g; d rows g, g + 8 and
+// columns 2 t, 2 t + 1.
+__device__ __forceinline__ void mma3_tf32(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                          const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+    mma_tf32(d, al, bh);
+    mma_tf32(d, ah, bl);
+    mma_tf32(d, ah, bh);
+}
 // Channels of the state each walk thread keeps in registers (8 channel groups of kThreads / 32 warps).
 __host__ __device__ inline int walk_cpt(int dk) { return dk <= 128 ? 16 : 32; }
 
@@ -726,9 +752,13 @@ struct GradLay {
     int Q, K, G, B, KK, P, Ex, dP, dA, H, dH, Ot, Dt, Yt, Zt, XO, HY, DD, pbeta, us, red, total;
 };
 
-// Tiles of dO, Delta, Y and Z are kept transposed ([kBV][C + 4]) so that one column's rows load four at a time.
+// Tiles of dO, Delta, Y and Z are kept transposed, [kBV][kTT]; the state tiles [8 walk_cpt(dk)][kHS].  Both strides
+// make the warp-MMA fragment loads conflict-free (8 t + g and 4 g + t banks).
+constexpr int kTT = 40;
+constexpr int kHS = 36;
+
 __host__ __device__ inline GradLay grad_lay(int C, int dk, bool perch) {
-    const int ldk = 8 * walk_cpt(dk) + 4, lg = perch ? ldk : 1, cc = C * (C + 1), tt = kBV * (C + 4);
+    const int ldk = 8 * walk_cpt(dk) + 4, lg = perch ? ldk : 1, cc = C * (C + 1), tt = kBV * kTT;
     GradLay l;
     int o = 0;
     l.Q = o; o += C * ldk; o = round4(o);
@@ -740,8 +770,8 @@ __host__ __device__ inline GradLay grad_lay(int C, int dk, bool perch) {
     l.Ex = o; o += perch ? 0 : cc; o = round4(o);
     l.dP = o; o += cc; o = round4(o);
     l.dA = o; o += cc; o = round4(o);
-    l.H = o; o += dk * kTS; o = round4(o);
-    l.dH = o; o += dk * kTS; o = round4(o);
+    l.H = o; o += 8 * walk_cpt(dk) * kHS; o = round4(o);
+    l.dH = o; o += 8 * walk_cpt(dk) * kHS; o = round4(o);
     l.Ot = o; o += tt; o = round4(o);
     l.Dt = o; o += tt; o = round4(o);
     l.Yt = o; o += tt; o = round4(o);
@@ -771,11 +801,11 @@ __host__ __device__ inline GradLay grad_lay(int C, int dk, bool perch) {
 // keeps the gate gradient accurate under strong decay.  Then
 //   dg[u] = sum_{r >= u} pb[r] + sum_{s < u} pw[s] + us,   us = E_L sum_j dh[c][j] h[c][j],
 //   dbeta_r = Y_r . Z_r + sum_{s<r} dA[r][s] KK[r][s],   dV = diag(beta) Y.
-template <typename Tin, typename Tdo, bool PERCH, int CC>
+template <typename Tin, typename Tdo, bool PERCH, int CC, int NTW>
 __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws ws, int n_tiles) {
     extern __shared__ __align__(16) float smem[];
-    constexpr int RH = CC / 2;        // rows per thread in the state products
-    constexpr int TT = CC + 4;        // stride of the transposed tiles
+    constexpr int TT = kTT;           // stride of the transposed tiles
+    constexpr int MT = CC / 16;       // 16-row blocks of the chunk
     constexpr int NP = (CC * CC + kThreads - 1) / kThreads;
     const int dk = a.dk, dv = a.dv, H = a.H, ldk = 8 * walk_cpt(dk) + 4, lg = PERCH ? ldk : 1, dkp = round4(dk);
     const GradLay ly = grad_lay(CC, dk, PERCH);
@@ -826,18 +856,32 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
         }
     }
 
-    float dp[NP], da[NP], ubeta = 0.f, uh = 0.f;
+    float dp[NP], da[NP], ubeta = 0.f;
 #pragma unroll
     for (int k = 0; k < NP; ++k) { dp[k] = 0.f; da[k] = 0.f; }
+    // the state products xo = dO h^T, hy = Y h^T, dd = Delta dh^T ([C][channel]) on warp MMAs: warp w owns
+    // channel blocks (w NTW + n) * 8, all rows; the accumulators stay in registers across the d_v tiles
+    const int warp = tid >> 5, lane = tid & 31, fg = lane >> 2, ft = lane & 3;
+    float acc[3][MT][NTW][4];
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int nn = 0; nn < NTW; ++nn)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[p][m][nn][i] = 0.f;
+    for (int c = tid; c < dk; c += kThreads) us[c] = 0.f;
     const Tdo* dO = static_cast<const Tdo*>(a.dO);
+    const int hrows = 8 * NTW * (kThreads / 32);
     for (int t = 0; t < n_tiles; ++t) {
         const int j0 = t * kBV, bw = min(kBV, dv - j0);
         __syncthreads();
-        for (int idx = tid; idx < dk * kBV; idx += kThreads) {
+        for (int idx = tid; idx < hrows * kBV; idx += kThreads) {
             const int c = idx / kBV, j = idx % kBV;
-            const bool in = j < bw;
-            Hs[c * kTS + j] = in ? ws.h[sbase + (size_t)c * dv + j0 + j] : 0.f;
-            dHs[c * kTS + j] = in ? ws.dh[sbase + (size_t)c * dv + j0 + j] : 0.f;
+            const bool in = j < bw && c < dk;
+            Hs[c * kHS + j] = in ? ws.h[sbase + (size_t)c * dv + j0 + j] : 0.f;
+            dHs[c * kHS + j] = in ? ws.dh[sbase + (size_t)c * dv + j0 + j] : 0.f;
         }
         for (int idx = tid; idx < CC * kBV; idx += kThreads) {
             const int r = idx / kBV, j = idx % kBV;
@@ -874,40 +918,62 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
         if (tid < CC) {
             for (int j = 0; j < kBV; ++j) ubeta = fmaf(Yt[j * TT + tid], Zt[j * TT + tid], ubeta);
         }
-        if (tid < dk) {
-            for (int j = 0; j < kBV; ++j) uh = fmaf(dHs[tid * kTS + j], Hs[tid * kTS + j], uh);
+        // us[c] += sum_j dh[c][j] h[c][j]: one warp per channel, lane = column (each channel always meets the
+        // same warp, so the sum needs no atomics)
+        for (int c = warp; c < dk; c += kThreads / 32) {
+            float x = dHs[c * kHS + lane] * Hs[c * kHS + lane];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) us[c] += x;
         }
-        // xo, hy, dd: thread (channel c, rows r0 ..), RH rows four at a time from the transposed tiles
-        for (int c0 = 0; c0 < dk; c0 += kThreads / 2) {
-            const int c = c0 + (tid & (kThreads / 2 - 1)), r0 = (tid / (kThreads / 2)) * RH;
-            if (c >= dk) continue;
-            float xo[RH], hy[RH], dd[RH];
+        // the state products, 8 columns of the tile per step
 #pragma unroll
-            for (int m = 0; m < RH; ++m) { xo[m] = 0.f; hy[m] = 0.f; dd[m] = 0.f; }
-            for (int j = 0; j < kBV; ++j) {
-                const float hv = Hs[c * kTS + j], dhv = dHs[c * kTS + j];
+        for (int k0 = 0; k0 < kBV; k0 += 8) {
+            uint32_t bhh[NTW][2], bhl[NTW][2], bdh[NTW][2], bdl[NTW][2];
 #pragma unroll
-                for (int m = 0; m < RH; m += 4) {
-                    const float4 o = *reinterpret_cast<const float4*>(Ot + j * TT + r0 + m);
-                    const float4 y = *reinterpret_cast<const float4*>(Yt + j * TT + r0 + m);
-                    const float4 d = *reinterpret_cast<const float4*>(Dt + j * TT + r0 + m);
-                    xo[m] = fmaf(hv, o.x, xo[m]); xo[m + 1] = fmaf(hv, o.y, xo[m + 1]);
-                    xo[m + 2] = fmaf(hv, o.z, xo[m + 2]); xo[m + 3] = fmaf(hv, o.w, xo[m + 3]);
-                    hy[m] = fmaf(hv, y.x, hy[m]); hy[m + 1] = fmaf(hv, y.y, hy[m + 1]);
-                    hy[m + 2] = fmaf(hv, y.z, hy[m + 2]); hy[m + 3] = fmaf(hv, y.w, hy[m + 3]);
-                    dd[m] = fmaf(dhv, d.x, dd[m]); dd[m + 1] = fmaf(dhv, d.y, dd[m + 1]);
-                    dd[m + 2] = fmaf(dhv, d.z, dd[m + 2]); dd[m + 3] = fmaf(dhv, d.w, dd[m + 3]);
-                }
+            for (int nn = 0; nn < NTW; ++nn) {
+                const int c = (warp * NTW + nn) * 8 + fg;
+                split_tf32(Hs[c * kHS + k0 + ft], bhh[nn][0], bhl[nn][0]);
+                split_tf32(Hs[c * kHS + k0 + ft + 4], bhh[nn][1], bhl[nn][1]);
+                split_tf32(dHs[c * kHS + k0 + ft], bdh[nn][0], bdl[nn][0]);
+                split_tf32(dHs[c * kHS + k0 + ft + 4], bdh[nn][1], bdl[nn][1]);
             }
 #pragma unroll
-            for (int m = 0; m < RH; ++m) {
-                const int i = (r0 + m) * dk + c;
-                XO[i] = (t ? XO[i] : 0.f) + xo[m];
-                HY[i] = (t ? HY[i] : 0.f) + hy[m];
-                DD[i] = (t ? DD[i] : 0.f) + dd[m];
+            for (int m = 0; m < MT; ++m) {
+                const int r0 = 16 * m + fg;
+                uint32_t oh[4], ol[4], yh[4], yl[4], dh4[4], dl4[4];
+                const int i0 = (k0 + ft) * TT + r0, i1 = (k0 + ft + 4) * TT + r0;
+                split_tf32(Ot[i0], oh[0], ol[0]); split_tf32(Ot[i0 + 8], oh[1], ol[1]);
+                split_tf32(Ot[i1], oh[2], ol[2]); split_tf32(Ot[i1 + 8], oh[3], ol[3]);
+                split_tf32(Yt[i0], yh[0], yl[0]); split_tf32(Yt[i0 + 8], yh[1], yl[1]);
+                split_tf32(Yt[i1], yh[2], yl[2]); split_tf32(Yt[i1 + 8], yh[3], yl[3]);
+                split_tf32(Dt[i0], dh4[0], dl4[0]); split_tf32(Dt[i0 + 8], dh4[1], dl4[1]);
+                split_tf32(Dt[i1], dh4[2], dl4[2]); split_tf32(Dt[i1 + 8], dh4[3], dl4[3]);
+#pragma unroll
+                for (int nn = 0; nn < NTW; ++nn) {
+                    mma3_tf32(acc[0][m][nn], oh, ol, bhh[nn], bhl[nn]);
+                    mma3_tf32(acc[1][m][nn], yh, yl, bhh[nn], bhl[nn]);
+                    mma3_tf32(acc[2][m][nn], dh4, dl4, bdh[nn], bdl[nn]);
+                }
             }
         }
     }
+    // the accumulators to [C][dk] (channels below d_k only)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int nn = 0; nn < NTW; ++nn) {
+            const int c = (warp * NTW + nn) * 8 + 2 * ft, r = 16 * m + fg;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = r + 8 * (i >> 1), cc2 = c + (i & 1);
+                if (cc2 < dk) {
+                    XO[rr * dk + cc2] = acc[0][m][nn][i];
+                    HY[rr * dk + cc2] = acc[1][m][nn][i];
+                    DD[rr * dk + cc2] = acc[2][m][nn][i];
+                }
+            }
+        }
 #pragma unroll
     for (int k = 0; k < NP; ++k) {
         const int idx = tid + k * kThreads;
@@ -918,7 +984,8 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
         }
     }
     if (tid < CC) pbeta[tid] = ubeta;
-    if (tid < dk) us[tid] = expf(PERCH ? Gs[(L - 1) * lg + tid] : Gs[L - 1]) * uh;
+    __syncthreads();
+    if (tid < dk) us[tid] *= expf(PERCH ? Gs[(L - 1) * lg + tid] : Gs[L - 1]);
     __syncthreads();
 
     // per (row, channel): dQ, dK written; the gate terms pb, pw kept in place of xo, hy
@@ -1048,9 +1115,15 @@ cudaError_t launch_c(const BwdArgs& a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((long)a.B * a.T == 0) return cudaSuccess;
     const size_t gbytes = (size_t)grad_lay(CC, a.dk, PERCH).total * sizeof(float);
-    auto g = bwd_grad_kernel<Tin, Tdo, PERCH, CC>;
-    if ((e = set_smem(g, gbytes)) != cudaSuccess) return e;
-    g<<<(unsigned)(slots * a.H), kThreads, gbytes, s>>>(a, ws, n_tiles);
+    if (walk_cpt(a.dk) == 16) {
+        auto g = bwd_grad_kernel<Tin, Tdo, PERCH, CC, 2>;
+        if ((e = set_smem(g, gbytes)) != cudaSuccess) return e;
+        g<<<(unsigned)(slots * a.H), kThreads, gbytes, s>>>(a, ws, n_tiles);
+    } else {
+        auto g = bwd_grad_kernel<Tin, Tdo, PERCH, CC, 4>;
+        if ((e = set_smem(g, gbytes)) != cudaSuccess) return e;
+        g<<<(unsigned)(slots * a.H), kThreads, gbytes, s>>>(a, ws, n_tiles);
+    }
     return cudaGetLastError();
 }
 
