@@ -47,8 +47,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kThreads = 256;
 constexpr int kBV = 32;        // d_v columns per tile of the gradient kernel
 constexpr int kTS = kBV + 1;   // padded row stride of [rows][kBV] tiles
-constexpr int kWB = 64;        // d_v columns per walk CTA: two per thread
-constexpr int kWS = kWB + 1;   // padded row stride of the walk's [rows][kWB] tiles
+constexpr int kWB = 64;        // d_v columns per walk CTA
+constexpr int kWS = 72;        // row stride of the walk's [rows][kWB] tiles: MMA fragment loads hit banks 8 t + g
 
 template <typename T> __device__ __forceinline__ float ld_f32(const T* p, size_t i);
 template <> __device__ __forceinline__ float ld_f32<float>(const float* p, size_t i) { return p[i]; }
@@ -255,32 +255,31 @@ __device__ __forceinline__ void pair_products(const float* Qs, const float* Ks, 
 
 // (I + A) X = X0 in place, A = diag(beta) KK strictly lower: rows in order.  X is [rows][NCOL] with row stride
 // NCOL + 1.  LPC = 256 / NCOL lanes per column (8 for 32 columns, 4 for 64): every column in one sweep.
-template <int NCOL>
+template <int NCOL, int XS>
 __device__ __forceinline__ void solve_lower(const float* KK, const float* Bs, float* X, int C, int L) {
     constexpr int LPC = kThreads / NCOL;
     const int col = threadIdx.x / LPC, sub = threadIdx.x % LPC;
     for (int r = 1; r < L; ++r) {
         float acc = 0.f;
-        for (int j = sub; j < r; j += LPC) acc = fmaf(KK[r * (C + 1) + j], X[j * (NCOL + 1) + col], acc);
+        for (int j = sub; j < r; j += LPC) acc = fmaf(KK[r * (C + 1) + j], X[j * XS + col], acc);
 #pragma unroll
         for (int o = 1; o < LPC; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (sub == 0) X[r * (NCOL + 1) + col] -= Bs[r] * acc;
+        if (sub == 0) X[r * XS + col] -= Bs[r] * acc;
         __syncwarp();
     }
 }
 
 // (I + A)^T X = X0 in place: rows from the last valid one down.
-template <int NCOL>
+template <int NCOL, int XS>
 __device__ __forceinline__ void solve_upper_t(const float* KK, const float* Bs, float* X, int C, int L) {
     constexpr int LPC = kThreads / NCOL;
     const int col = threadIdx.x / LPC, sub = threadIdx.x % LPC;
     for (int s = L - 2; s >= 0; --s) {
         float acc = 0.f;
-        for (int r = s + 1 + sub; r < L; r += LPC)
-            acc = fmaf(Bs[r] * KK[r * (C + 1) + s], X[r * (NCOL + 1) + col], acc);
+        for (int r = s + 1 + sub; r < L; r += LPC) acc = fmaf(Bs[r] * KK[r * (C + 1) + s], X[r * XS + col], acc);
 #pragma unroll
         for (int o = 1; o < LPC; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (sub == 0) X[s * (NCOL + 1) + col] -= acc;
+        if (sub == 0) X[s * XS + col] -= acc;
         __syncwarp();
     }
 }
@@ -389,28 +388,56 @@ __device__ __forceinline__ void prefetch_rows(float (&v)[NV], const T* src, size
     }
 }
 
-// The forward walk: per chunk, store the entry state, Z and Delta.  Thread (j = lane, channel group cg = warp)
-// keeps state channels [cg * CPT, cg * CPT + CPT) of columns j and j + 32 of its 64-column tile.
+// Operand fragments of m16n8k8 (lane = 4 g + t), split into TF32 heads and tails for mma3_tf32.
+// A (16 x 8) at (row, col) = (r0 + g [+ 8], k0 + t [+ 4]) of a row-major matrix with row stride ld.
+__device__ __forceinline__ void frag_a(const float* M, int ld, int r0, int k0, int g, int t, uint32_t (&h)[4],
+                                       uint32_t (&l)[4]) {
+    split_tf32(M[(r0 + g) * ld + k0 + t], h[0], l[0]);
+    split_tf32(M[(r0 + g + 8) * ld + k0 + t], h[1], l[1]);
+    split_tf32(M[(r0 + g) * ld + k0 + t + 4], h[2], l[2]);
+    split_tf32(M[(r0 + g + 8) * ld + k0 + t + 4], h[3], l[3]);
+}
+// A (16 x 8) = the transpose of a row-major matrix N: A(row m, col k) = N[k][m].
+__device__ __forceinline__ void frag_at(const float* N, int ld, int m0, int k0, int g, int t, uint32_t (&h)[4],
+                                        uint32_t (&l)[4]) {
+    split_tf32(N[(k0 + t) * ld + m0 + g], h[0], l[0]);
+    split_tf32(N[(k0 + t) * ld + m0 + g + 8], h[1], l[1]);
+    split_tf32(N[(k0 + t + 4) * ld + m0 + g], h[2], l[2]);
+    split_tf32(N[(k0 + t + 4) * ld + m0 + g + 8], h[3], l[3]);
+}
+// B (8 x 8) at (row, col) = (k0 + t [+ 4], n0 + g) of a row-major matrix, each element times s.
+__device__ __forceinline__ void frag_b(const float* M, int ld, int k0, int n0, int g, int t, float s0, float s1,
+                                       uint32_t (&h)[2], uint32_t (&l)[2]) {
+    split_tf32(s0 * M[(k0 + t) * ld + n0 + g], h[0], l[0]);
+    split_tf32(s1 * M[(k0 + t + 4) * ld + n0 + g], h[1], l[1]);
+}
+
+// The forward walk: per chunk, store the entry state, Z and Delta.  The state tile h [channels][64 columns] lives in
+// m16n8 accumulator fragments: warp w owns channels [w CPT, w CPT + CPT) (CPT / 16 row blocks) and all eight
+// 8-column blocks.  Per chunk, on 3xTF32 warp MMAs:
+//   Z = V - (K*E) h       rows of the chunk x the warp's 8 columns, over the channels
+//   h <- diag(E_L) h + (K*F)^T Delta       the warp's channels x 64 columns, over the chunk's rows
 template <typename Tin, bool PERCH, int CC, int CPT>
 __device__ __forceinline__ void walk_forward(const BwdArgs& a, const Ws& ws, float* smem, long chain, int tile) {
-    constexpr int RPT = CC / 8, NV = CC * kWB / kThreads;
-    const int dk = a.dk, dv = a.dv, H = a.H, ldk = 8 * CPT + 4, dkp = round4(dk);
+    constexpr int MTW = CPT / 16, MTC = CC / 16;
+    const int dk = a.dk, dv = a.dv, H = a.H, ldk = 8 * CPT + 4, dk8 = (dk + 7) & ~7;
     const Rec rc = rec_lay(CC, dk, PERCH);
     const WalkLay ly = walk_lay(CC, dk, PERCH);
-    float* Hs = smem + ly.S;  float* Vs = smem + ly.V;  float* Ds = smem + ly.D;
+    float* Hs = smem + ly.S;  float* Ds = smem + ly.D;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ly.bar);
-    const int tid = threadIdx.x, j = tid & 31, cg = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     const long n = chain / H;
     const int hh = (int)(chain % H);
     const Geo geo = chain_geo(a, n);
     const int j0 = tile * kWB, bw = min(kWB, dv - j0);
-    const bool in0 = j < bw, in1 = j + 32 < bw;
     const size_t sstride = (size_t)H * dk * dv, cstride = (size_t)H * CC * dv, rstride = (size_t)H * rc.total;
-    const size_t sbase = (size_t)geo.slot0 * sstride + (size_t)hh * dk * dv + j0 + j;
-    const size_t cbase = (size_t)geo.slot0 * cstride + (size_t)hh * CC * dv + j0 + j;
+    const size_t sbase = (size_t)geo.slot0 * sstride + (size_t)hh * dk * dv + j0;
+    const size_t cbase = (size_t)geo.slot0 * cstride + (size_t)hh * CC * dv + j0;
     const float* recs = ws.rec + ((size_t)geo.slot0 * H + hh) * rc.total;
     const long n_chunks = (geo.len + CC - 1) / CC;
     const Tin* v = static_cast<const Tin*>(a.v);
+    const int cw = warp * CPT;          // first channel of this warp
+    const int jz = 8 * warp + 2 * t4;   // this thread's two columns of Z
 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -431,44 +458,54 @@ __device__ __forceinline__ void walk_forward(const BwdArgs& a, const Ws& ws, flo
     if (tid == 0) {
         for (; issued < 2 && issued < n_chunks; ++issued) issue(issued);
     }
-    float h0r[CPT], h1r[CPT];
+    float hacc[MTW][8][4];
     {
-        const float* src = a.h0 ? a.h0 + ((size_t)n * H + hh) * dk * dv + j0 + j : nullptr;
+        const float* src = a.h0 ? a.h0 + ((size_t)n * H + hh) * dk * dv + j0 : nullptr;
 #pragma unroll
-        for (int m = 0; m < CPT; ++m) {
-            const int c = cg * CPT + m;
-            h0r[m] = (src && c < dk && in0) ? src[(size_t)c * dv] : 0.f;
-            h1r[m] = (src && c < dk && in1) ? src[(size_t)c * dv + 32] : 0.f;
-        }
+        for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = cw + 16 * mt + g + 8 * (i >> 1), j = 8 * nt + 2 * t4 + (i & 1);
+                    hacc[mt][nt][i] = (src && c < dk && j < bw) ? src[(size_t)c * dv + j] : 0.f;
+                }
     }
-    float vpre[NV];
-    if (n_chunks > 0)
-        prefetch_rows<Tin, NV>(vpre, v, ((size_t)geo.b * a.T + geo.bos) * H + hh, H, dv, j0, bw,
-                               (int)min((long)CC, geo.len));
+    // V at this thread's Z positions (rows 16 m + g [+ 8], columns jz, jz + 1), loaded one chunk ahead
+    float vpre[MTC][4];
+    auto prefetch_v = [&](long c) {
+        const size_t tok0 = ((size_t)geo.b * a.T + geo.bos + c * CC) * H + hh;
+        const int L = (int)min((long)CC, geo.len - c * CC);
+#pragma unroll
+        for (int mc = 0; mc < MTC; ++mc)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 16 * mc + g + 8 * (i >> 1), j = jz + (i & 1);
+                vpre[mc][i] = (r < L && j < bw) ? ld_f32<Tin>(v, (tok0 + (size_t)r * H) * dv + j0 + j) : 0.f;
+            }
+    };
+    if (n_chunks > 0) prefetch_v(0);
     bool ok = true;
     for (long ci = 0;; ++ci) {
-        // the state entering chunk ci (ci = n_chunks: the final state)
+        // the state entering chunk ci (ci = n_chunks: the final state), to shared memory and the workspace
 #pragma unroll
-        for (int m = 0; m < CPT; ++m) {
-            const int c = cg * CPT + m;
-            Hs[c * kWS + j] = h0r[m];
-            Hs[c * kWS + j + 32] = h1r[m];
-            if (c < dk) {
-                const size_t o = sbase + (size_t)ci * sstride + (size_t)c * dv;
-                if (in0) ws.h[o] = h0r[m];
-                if (in1) ws.h[o + 32] = h1r[m];
-            }
-        }
+        for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = cw + 16 * mt + g + 8 * (i >> 1), j = 8 * nt + 2 * t4 + (i & 1);
+                    Hs[c * kWS + j] = hacc[mt][nt][i];
+                    if (c < dk && j < bw) ws.h[sbase + (size_t)ci * sstride + (size_t)c * dv + j] = hacc[mt][nt][i];
+                }
         if (ci == n_chunks) break;
         const int L = (int)min((long)CC, geo.len - ci * CC);
+        float vcur[MTC][4];
 #pragma unroll
-        for (int k = 0; k < NV / 2; ++k) {
-            Vs[(cg + 8 * k) * kWS + j] = vpre[2 * k];
-            Vs[(cg + 8 * k) * kWS + j + 32] = vpre[2 * k + 1];
-        }
-        if (ci + 1 < n_chunks)
-            prefetch_rows<Tin, NV>(vpre, v, ((size_t)geo.b * a.T + geo.bos + (ci + 1) * CC) * H + hh, H, dv, j0, bw,
-                                   (int)min((long)CC, geo.len - (ci + 1) * CC));
+        for (int mc = 0; mc < MTC; ++mc)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vcur[mc][i] = vpre[mc][i];
+        if (ci + 1 < n_chunks) prefetch_v(ci + 1);
         const float* st = smem + ((ci & 1) ? ly.st1 : ly.st0);
         if (ok) ok = mbar_wait(&bars[ci & 1], (uint32_t)((ci >> 1) & 1), kWaitNs);
         ok = !__syncthreads_or(!ok);
@@ -482,65 +519,64 @@ __device__ __forceinline__ void walk_forward(const BwdArgs& a, const Ws& ws, flo
         const float* KK = st + rc.KK;
         const float* EL = st + rc.EL;
         const float* Bs = st + rc.B;
-        // Z = V - (K*E) h, R = beta Z: thread (columns j, j + 32; rows cg*RPT ..)
+        // Z = V - (K*E) h, then R = beta Z into Ds
         {
-            float a0[RPT], a1[RPT];
+            float z[MTC][4];
 #pragma unroll
-            for (int m = 0; m < RPT; ++m) { a0[m] = 0.f; a1[m] = 0.f; }
-            for (int c = 0; c < dkp; c += 4) {
-                float x[4], y[4];
+            for (int mc = 0; mc < MTC; ++mc)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) z[mc][i] = 0.f;
+            for (int k0 = 0; k0 < dk8; k0 += 8) {
+                uint32_t bh[2], bl[2];
+                frag_b(Hs, kWS, k0, 8 * warp, g, t4, 1.f, 1.f, bh, bl);
+#pragma unroll
+                for (int mc = 0; mc < MTC; ++mc) {
+                    uint32_t ah[4], al[4];
+                    frag_a(KE, ldk, 16 * mc, k0, g, t4, ah, al);
+                    mma3_tf32(z[mc], ah, al, bh, bl);
+                }
+            }
+#pragma unroll
+            for (int mc = 0; mc < MTC; ++mc)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    x[i] = Hs[(c + i) * kWS + j];
-                    y[i] = Hs[(c + i) * kWS + j + 32];
+                    const int r = 16 * mc + g + 8 * (i >> 1), j = jz + (i & 1);
+                    const float zz = vcur[mc][i] - z[mc][i];
+                    if (r < L && j < bw) ws.Z[cbase + (size_t)ci * cstride + (size_t)r * dv + j] = zz;
+                    Ds[r * kWS + j] = Bs[r] * zz;
                 }
-#pragma unroll
-                for (int m = 0; m < RPT; ++m) {
-                    const float4 ke = *reinterpret_cast<const float4*>(KE + (cg * RPT + m) * ldk + c);
-                    a0[m] = fmaf(ke.x, x[0], fmaf(ke.y, x[1], fmaf(ke.z, x[2], fmaf(ke.w, x[3], a0[m]))));
-                    a1[m] = fmaf(ke.x, y[0], fmaf(ke.y, y[1], fmaf(ke.z, y[2], fmaf(ke.w, y[3], a1[m]))));
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < RPT; ++m) {
-                const int r = cg * RPT + m;
-                const float z0 = Vs[r * kWS + j] - a0[m], z1 = Vs[r * kWS + j + 32] - a1[m];
-                if (r < L) {
-                    const size_t o = cbase + (size_t)ci * cstride + (size_t)r * dv;
-                    if (in0) ws.Z[o] = z0;
-                    if (in1) ws.Z[o + 32] = z1;
-                }
-                Ds[r * kWS + j] = Bs[r] * z0;
-                Ds[r * kWS + j + 32] = Bs[r] * z1;
-            }
         }
         __syncthreads();
-        solve_lower<kWB>(KK, Bs, Ds, CC, L);
+        solve_lower<kWB, kWS>(KK, Bs, Ds, CC, L);
         __syncthreads();
         // store Delta; h <- diag(E_L) h + (K*F)^T Delta
-        for (int r = cg; r < L; r += 8) {
-            const size_t o = cbase + (size_t)ci * cstride + (size_t)r * dv;
-            if (in0) ws.D[o] = Ds[r * kWS + j];
-            if (in1) ws.D[o + 32] = Ds[r * kWS + j + 32];
+        for (int idx = tid; idx < L * kWB; idx += kThreads) {
+            const int r = idx / kWB, j = idx % kWB;
+            if (j < bw) ws.D[cbase + (size_t)ci * cstride + (size_t)r * dv + j] = Ds[r * kWS + j];
         }
 #pragma unroll
-        for (int m = 0; m < CPT; ++m) {
-            const float el = EL[PERCH ? cg * CPT + m : 0];
-            h0r[m] *= el;
-            h1r[m] *= el;
-        }
-        for (int r = 0; r < L; ++r) {
-            const float d0 = Ds[r * kWS + j], d1 = Ds[r * kWS + j + 32];
+        for (int mt = 0; mt < MTW; ++mt) {
+            const float e0 = EL[PERCH ? cw + 16 * mt + g : 0], e1 = EL[PERCH ? cw + 16 * mt + g + 8 : 0];
 #pragma unroll
-            for (int m = 0; m < CPT; m += 4) {
-                const float4 kf = *reinterpret_cast<const float4*>(KF + r * ldk + cg * CPT + m);
-                h0r[m] = fmaf(kf.x, d0, h0r[m]);         h1r[m] = fmaf(kf.x, d1, h1r[m]);
-                h0r[m + 1] = fmaf(kf.y, d0, h0r[m + 1]); h1r[m + 1] = fmaf(kf.y, d1, h1r[m + 1]);
-                h0r[m + 2] = fmaf(kf.z, d0, h0r[m + 2]); h1r[m + 2] = fmaf(kf.z, d1, h1r[m + 2]);
-                h0r[m + 3] = fmaf(kf.w, d0, h0r[m + 3]); h1r[m + 3] = fmaf(kf.w, d1, h1r[m + 3]);
+            for (int nt = 0; nt < 8; ++nt) {
+                hacc[mt][nt][0] *= e0; hacc[mt][nt][1] *= e0;
+                hacc[mt][nt][2] *= e1; hacc[mt][nt][3] *= e1;
             }
         }
-        __syncthreads();   // every thread is done with this stage
+#pragma unroll
+        for (int k0 = 0; k0 < CC; k0 += 8) {
+            uint32_t ah[MTW][4], al[MTW][4];
+#pragma unroll
+            for (int mt = 0; mt < MTW; ++mt) frag_at(KF, ldk, cw + 16 * mt, k0, g, t4, ah[mt], al[mt]);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                uint32_t bh[2], bl[2];
+                frag_b(Ds, kWS, k0, 8 * nt, g, t4, 1.f, 1.f, bh, bl);
+#pragma unroll
+                for (int mt = 0; mt < MTW; ++mt) mma3_tf32(hacc[mt][nt], ah[mt], al[mt], bh, bl);
+            }
+        }
+        __syncthreads();   // every thread is done with this stage and with Hs, Ds
         if (tid == 0 && ci + 2 < n_chunks) {
             issue(ci + 2);
             ++issued;
@@ -552,28 +588,31 @@ __device__ __forceinline__ void walk_forward(const BwdArgs& a, const Ws& ws, flo
 }
 
 // The backward walk: per chunk (last to first), store the gradient of h_out and Y; finally the gradient of the
-// initial state.  Thread layout as in the forward walk.
+// initial state.  Layout as in the forward walk; per chunk:
+//   dDelta = P^T dO + (K*F) dh        rows x the warp's 8 columns
+//   dh <- diag(E_L) dh + scale (Q*E)^T dO - (K*E)^T diag(beta) Y        the warp's channels x 64 columns
 template <typename Tin, typename Tdo, bool PERCH, int CC, int CPT>
 __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, float* smem, long chain, int tile) {
-    constexpr int RPT = CC / 8, NV = CC * kWB / kThreads;
-    const int dk = a.dk, dv = a.dv, H = a.H, ldk = 8 * CPT + 4, dkp = round4(dk);
+    constexpr int MTW = CPT / 16, MTC = CC / 16, NV = CC * kWB / kThreads;
+    const int dk = a.dk, dv = a.dv, H = a.H, ldk = 8 * CPT + 4, dk8 = (dk + 7) & ~7;
     const Rec rc = rec_lay(CC, dk, PERCH);
     const WalkLay ly = walk_lay(CC, dk, PERCH);
     float* dHs = smem + ly.S; float* Os = smem + ly.V;  float* Ys = smem + ly.D;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ly.bar);
-    const int tid = threadIdx.x, j = tid & 31, cg = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     const long n = chain / H;
     const int hh = (int)(chain % H);
     const Geo geo = chain_geo(a, n);
     const int j0 = tile * kWB, bw = min(kWB, dv - j0);
-    const bool in0 = j < bw, in1 = j + 32 < bw;
     const size_t sstride = (size_t)H * dk * dv, cstride = (size_t)H * CC * dv, rstride = (size_t)H * rc.total;
-    const size_t sbase = (size_t)geo.slot0 * sstride + (size_t)hh * dk * dv + j0 + j;
-    const size_t cbase = (size_t)geo.slot0 * cstride + (size_t)hh * CC * dv + j0 + j;
-    const size_t own = ((size_t)n * H + hh) * dk * dv + j0 + j;
+    const size_t sbase = (size_t)geo.slot0 * sstride + (size_t)hh * dk * dv + j0;
+    const size_t cbase = (size_t)geo.slot0 * cstride + (size_t)hh * CC * dv + j0;
+    const size_t own = ((size_t)n * H + hh) * dk * dv + j0;
     const float* recs = ws.rec + ((size_t)geo.slot0 * H + hh) * rc.total;
     const long n_chunks = (geo.len + CC - 1) / CC;
     const Tdo* dO = static_cast<const Tdo*>(a.dO);
+    const int cw = warp * CPT;
+    const int jz = 8 * warp + 2 * t4;
 
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -593,13 +632,16 @@ __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, fl
     if (tid == 0) {
         for (; issued < 2 && issued < n_chunks; ++issued) issue(issued);
     }
-    float d0r[CPT], d1r[CPT];
+    float dacc[MTW][8][4];
 #pragma unroll
-    for (int m = 0; m < CPT; ++m) {
-        const int c = cg * CPT + m;
-        d0r[m] = (a.dhT && c < dk && in0) ? a.dhT[own + (size_t)c * dv] : 0.f;
-        d1r[m] = (a.dhT && c < dk && in1) ? a.dhT[own + (size_t)c * dv + 32] : 0.f;
-    }
+    for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = cw + 16 * mt + g + 8 * (i >> 1), j = 8 * nt + 2 * t4 + (i & 1);
+                dacc[mt][nt][i] = (a.dhT && c < dk && j < bw) ? a.dhT[own + (size_t)c * dv + j] : 0.f;
+            }
     float opre[NV];
     if (n_chunks > 0) {
         const long cl = n_chunks - 1;
@@ -610,22 +652,24 @@ __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, fl
     for (long k = 0; k < n_chunks; ++k) {
         const long ci = n_chunks - 1 - k;
         const int L = (int)min((long)CC, geo.len - ci * CC);
-        // the gradient of this chunk's h_out
+        // the gradient of this chunk's h_out, to shared memory and the workspace
 #pragma unroll
-        for (int m = 0; m < CPT; ++m) {
-            const int c = cg * CPT + m;
-            dHs[c * kWS + j] = d0r[m];
-            dHs[c * kWS + j + 32] = d1r[m];
-            if (c < dk) {
-                const size_t o = sbase + (size_t)ci * sstride + (size_t)c * dv;
-                if (in0) ws.dh[o] = d0r[m];
-                if (in1) ws.dh[o + 32] = d1r[m];
+        for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = cw + 16 * mt + g + 8 * (i >> 1), j = 8 * nt + 2 * t4 + (i & 1);
+                    dHs[c * kWS + j] = dacc[mt][nt][i];
+                    if (c < dk && j < bw) ws.dh[sbase + (size_t)ci * sstride + (size_t)c * dv + j] = dacc[mt][nt][i];
+                }
+        {
+            const int jl = tid & 31, r0 = tid >> 5;
+#pragma unroll
+            for (int q = 0; q < NV / 2; ++q) {
+                Os[(r0 + 8 * q) * kWS + jl] = opre[2 * q];
+                Os[(r0 + 8 * q) * kWS + jl + 32] = opre[2 * q + 1];
             }
-        }
-#pragma unroll
-        for (int q = 0; q < NV / 2; ++q) {
-            Os[(cg + 8 * q) * kWS + j] = opre[2 * q];
-            Os[(cg + 8 * q) * kWS + j + 32] = opre[2 * q + 1];
         }
         if (ci > 0)
             prefetch_rows<Tdo, NV>(opre, dO, ((size_t)geo.b * a.T + geo.bos + (ci - 1) * CC) * H + hh, H, dv, j0, bw,
@@ -645,76 +689,78 @@ __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, fl
         const float* KF = st + rc.KF;
         const float* EL = st + rc.EL;
         const float* Bs = st + rc.B;
-        // dDelta = P^T dO + (K*F) dh: thread (columns j, j + 32; rows cg*RPT ..)
+        // dDelta = P^T dO + (K*F) dh into Ys
         {
-            float a0[RPT], a1[RPT];
+            float z[MTC][4];
 #pragma unroll
-            for (int m = 0; m < RPT; ++m) { a0[m] = 0.f; a1[m] = 0.f; }
-            for (int r = cg * RPT; r < L; ++r) {
-                const float o0 = Os[r * kWS + j], o1 = Os[r * kWS + j + 32];
+            for (int mc = 0; mc < MTC; ++mc)
 #pragma unroll
-                for (int m = 0; m < RPT; ++m) {
-                    const int i = cg * RPT + m;
-                    if (r >= i) {
-                        const float p = Pm[r * (CC + 1) + i];
-                        a0[m] = fmaf(p, o0, a0[m]);
-                        a1[m] = fmaf(p, o1, a1[m]);
-                    }
+                for (int i = 0; i < 4; ++i) z[mc][i] = 0.f;
+#pragma unroll
+            for (int k0 = 0; k0 < CC; k0 += 8) {
+                uint32_t bh[2], bl[2];
+                frag_b(Os, kWS, k0, 8 * warp, g, t4, 1.f, 1.f, bh, bl);
+#pragma unroll
+                for (int mc = 0; mc < MTC; ++mc) {
+                    uint32_t ah[4], al[4];
+                    frag_at(Pm, CC + 1, 16 * mc, k0, g, t4, ah, al);
+                    mma3_tf32(z[mc], ah, al, bh, bl);
                 }
             }
-            for (int c = 0; c < dkp; c += 4) {
-                float x[4], y[4];
+            for (int k0 = 0; k0 < dk8; k0 += 8) {
+                uint32_t bh[2], bl[2];
+                frag_b(dHs, kWS, k0, 8 * warp, g, t4, 1.f, 1.f, bh, bl);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    x[i] = dHs[(c + i) * kWS + j];
-                    y[i] = dHs[(c + i) * kWS + j + 32];
-                }
-#pragma unroll
-                for (int m = 0; m < RPT; ++m) {
-                    const float4 kf = *reinterpret_cast<const float4*>(KF + (cg * RPT + m) * ldk + c);
-                    a0[m] = fmaf(kf.x, x[0], fmaf(kf.y, x[1], fmaf(kf.z, x[2], fmaf(kf.w, x[3], a0[m]))));
-                    a1[m] = fmaf(kf.x, y[0], fmaf(kf.y, y[1], fmaf(kf.z, y[2], fmaf(kf.w, y[3], a1[m]))));
+                for (int mc = 0; mc < MTC; ++mc) {
+                    uint32_t ah[4], al[4];
+                    frag_a(KF, ldk, 16 * mc, k0, g, t4, ah, al);
+                    mma3_tf32(z[mc], ah, al, bh, bl);
                 }
             }
 #pragma unroll
-            for (int m = 0; m < RPT; ++m) {
-                Ys[(cg * RPT + m) * kWS + j] = a0[m];
-                Ys[(cg * RPT + m) * kWS + j + 32] = a1[m];
-            }
+            for (int mc = 0; mc < MTC; ++mc)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Ys[(16 * mc + g + 8 * (i >> 1)) * kWS + jz + (i & 1)] = z[mc][i];
         }
         __syncthreads();
-        solve_upper_t<kWB>(KK, Bs, Ys, CC, L);
+        solve_upper_t<kWB, kWS>(KK, Bs, Ys, CC, L);
         __syncthreads();
-        for (int r = cg; r < L; r += 8) {
-            const size_t o = cbase + (size_t)ci * cstride + (size_t)r * dv;
-            if (in0) ws.Y[o] = Ys[r * kWS + j];
-            if (in1) ws.Y[o + 32] = Ys[r * kWS + j + 32];
+        for (int idx = tid; idx < L * kWB; idx += kThreads) {
+            const int r = idx / kWB, j = idx % kWB;
+            if (j < bw) ws.Y[cbase + (size_t)ci * cstride + (size_t)r * dv + j] = Ys[r * kWS + j];
         }
         // dh <- diag(E_L) dh + scale (Q*E)^T dO - (K*E)^T diag(beta) Y
 #pragma unroll
-        for (int m = 0; m < CPT; ++m) {
-            const float el = EL[PERCH ? cg * CPT + m : 0];
-            d0r[m] *= el;
-            d1r[m] *= el;
-        }
-        for (int r = 0; r < L; ++r) {
-            const float o0 = Os[r * kWS + j], o1 = Os[r * kWS + j + 32];
-            const float y0 = Bs[r] * Ys[r * kWS + j], y1 = Bs[r] * Ys[r * kWS + j + 32];
+        for (int mt = 0; mt < MTW; ++mt) {
+            const float e0 = EL[PERCH ? cw + 16 * mt + g : 0], e1 = EL[PERCH ? cw + 16 * mt + g + 8 : 0];
 #pragma unroll
-            for (int m = 0; m < CPT; m += 4) {
-                const float4 qe = *reinterpret_cast<const float4*>(QE + r * ldk + cg * CPT + m);
-                const float4 ke = *reinterpret_cast<const float4*>(KE + r * ldk + cg * CPT + m);
-                d0r[m] = fmaf(qe.x, o0, fmaf(-ke.x, y0, d0r[m]));
-                d0r[m + 1] = fmaf(qe.y, o0, fmaf(-ke.y, y0, d0r[m + 1]));
-                d0r[m + 2] = fmaf(qe.z, o0, fmaf(-ke.z, y0, d0r[m + 2]));
-                d0r[m + 3] = fmaf(qe.w, o0, fmaf(-ke.w, y0, d0r[m + 3]));
-                d1r[m] = fmaf(qe.x, o1, fmaf(-ke.x, y1, d1r[m]));
-                d1r[m + 1] = fmaf(qe.y, o1, fmaf(-ke.y, y1, d1r[m + 1]));
-                d1r[m + 2] = fmaf(qe.z, o1, fmaf(-ke.z, y1, d1r[m + 2]));
-                d1r[m + 3] = fmaf(qe.w, o1, fmaf(-ke.w, y1, d1r[m + 3]));
+            for (int nt = 0; nt < 8; ++nt) {
+                dacc[mt][nt][0] *= e0; dacc[mt][nt][1] *= e0;
+                dacc[mt][nt][2] *= e1; dacc[mt][nt][3] *= e1;
             }
         }
-        __syncthreads();   // every thread is done with this stage
+#pragma unroll
+        for (int k0 = 0; k0 < CC; k0 += 8) {
+            uint32_t qh[MTW][4], ql[MTW][4], kh[MTW][4], kl[MTW][4];
+#pragma unroll
+            for (int mt = 0; mt < MTW; ++mt) {
+                frag_at(QE, ldk, cw + 16 * mt, k0, g, t4, qh[mt], ql[mt]);
+                frag_at(KE, ldk, cw + 16 * mt, k0, g, t4, kh[mt], kl[mt]);
+            }
+            const float nb0 = -Bs[k0 + t4], nb1 = -Bs[k0 + t4 + 4];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                uint32_t oh[2], ol[2], yh[2], yl[2];
+                frag_b(Os, kWS, k0, 8 * nt, g, t4, 1.f, 1.f, oh, ol);
+                frag_b(Ys, kWS, k0, 8 * nt, g, t4, nb0, nb1, yh, yl);
+#pragma unroll
+                for (int mt = 0; mt < MTW; ++mt) {
+                    mma3_tf32(dacc[mt][nt], qh[mt], ql[mt], oh, ol);
+                    mma3_tf32(dacc[mt][nt], kh[mt], kl[mt], yh, yl);
+                }
+            }
+        }
+        __syncthreads();   // every thread is done with this stage and with dHs, Os, Ys
         if (tid == 0 && k + 2 < n_chunks) {
             issue(k + 2);
             ++issued;
@@ -724,13 +770,14 @@ __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, fl
         for (long c = waited; c < issued; ++c) mbar_wait(&bars[c & 1], (uint32_t)((c >> 1) & 1), kWaitNs);
     if (a.gh0 && ok) {
 #pragma unroll
-        for (int m = 0; m < CPT; ++m) {
-            const int c = cg * CPT + m;
-            if (c < dk) {
-                if (in0) a.gh0[own + (size_t)c * dv] = d0r[m];
-                if (in1) a.gh0[own + (size_t)c * dv + 32] = d1r[m];
-            }
-        }
+        for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = cw + 16 * mt + g + 8 * (i >> 1), j = 8 * nt + 2 * t4 + (i & 1);
+                    if (c < dk && j < bw) a.gh0[own + (size_t)c * dv + j] = dacc[mt][nt][i];
+                }
     }
 }
 
