@@ -87,10 +87,13 @@ def _alg_bytes(w) -> int:
 TRAFFIC_SOURCES = {
     "chunk": ("chunk_two_pass.cu", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh"),
     "decode": ("recurrent_step.cu", "gate_act.cuh"),
+    "bwd": ("chunk_bwd.cu", "tc_common.cuh"),
 }
 
 
 def _traffic_kind(workload: str) -> str:
+    if "_bwd_" in workload:
+        return "bwd"
     return "decode" if workload.startswith("decode") or "_decode_" in workload else "chunk"
 
 
@@ -500,7 +503,7 @@ def run_bwd(args):
                    "kernel": "chunk_bwd (prep, walks, gradients)", "launches_per_step": 3,
                    "timed_region_wall_ms": t_wall * 1e3},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / ALU_PEAK_TFLOPS, "traffic": None,
+                     "frac": achieved / ALU_PEAK_TFLOPS, "traffic": _traffic_for(_bwd_name(w)),
                      "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz",
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
