@@ -83,6 +83,15 @@ __device__ __forceinline__ void mma3_tf32(float (&d)[4], const uint32_t (&ah)[4]
     mma_tf32(d, ah, bl);
     mma_tf32(d, ah, bh);
 }
+
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), in the calling thread's cp.async group
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's committed groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 // Channels of the state each walk thread keeps in registers (8 channel groups of kThreads / 32 warps).
 __host__ __device__ inline int walk_cpt(int dk) { return dk <= 128 ? 16 : 32; }
 
@@ -796,20 +805,20 @@ __global__ void __launch_bounds__(kThreads) bwd_walk_kernel(const BwdArgs a, Ws 
 // ---- the per-chunk gradients ---------------------------------------------------------------------------------
 
 struct GradLay {
-    int Q, K, G, B, KK, P, Ex, dP, dA, H, dH, Ot, Dt, Yt, Zt, XO, HY, DD, pbeta, us, red, total;
+    int G, B, KK, P, Ex, dP, dA, HB, TB, pbeta, us, red, total;
+    // inside the scratch region HB .. (after the tile loop): raw Q and K rows, then xo, hy, dd
+    int Q, K, XO, HY, DD;
 };
 
-// Tiles of dO, Delta, Y and Z are kept transposed, [kBV][kTT]; the state tiles [8 walk_cpt(dk)][kHS].  Both strides
-// make the warp-MMA fragment loads conflict-free (8 t + g and 4 g + t banks).
-constexpr int kTT = 40;
+// The d_v tiles are double-buffered: the entry state and the exit-state gradient ([8 walk_cpt(dk)][kHS] each) and the
+// dO, Delta, Y and Z tiles ([C][kHS] each, row-major), two of each.  kHS = 36 keeps the warp-MMA fragment loads
+// conflict-free (4 g + t banks).  After the tile loop the same space holds raw Q, K and the state products.
 constexpr int kHS = 36;
 
 __host__ __device__ inline GradLay grad_lay(int C, int dk, bool perch) {
-    const int ldk = 8 * walk_cpt(dk) + 4, lg = perch ? ldk : 1, cc = C * (C + 1), tt = kBV * kTT;
+    const int ldk = 8 * walk_cpt(dk) + 4, lg = perch ? ldk : 1, cc = C * (C + 1), hr = 8 * walk_cpt(dk);
     GradLay l;
     int o = 0;
-    l.Q = o; o += C * ldk; o = round4(o);
-    l.K = o; o += C * ldk; o = round4(o);
     l.G = o; o += C * lg; o = round4(o);
     l.B = o; o += C; o = round4(o);
     l.KK = o; o += cc; o = round4(o);
@@ -817,15 +826,11 @@ __host__ __device__ inline GradLay grad_lay(int C, int dk, bool perch) {
     l.Ex = o; o += perch ? 0 : cc; o = round4(o);
     l.dP = o; o += cc; o = round4(o);
     l.dA = o; o += cc; o = round4(o);
-    l.H = o; o += 8 * walk_cpt(dk) * kHS; o = round4(o);
-    l.dH = o; o += 8 * walk_cpt(dk) * kHS; o = round4(o);
-    l.Ot = o; o += tt; o = round4(o);
-    l.Dt = o; o += tt; o = round4(o);
-    l.Yt = o; o += tt; o = round4(o);
-    l.Zt = o; o += tt; o = round4(o);
-    l.XO = o; o += C * dk; o = round4(o);
-    l.HY = o; o += C * dk; o = round4(o);
-    l.DD = o; o += C * dk; o = round4(o);
+    const int tiles = 4 * hr * kHS + 8 * C * kHS;
+    l.Q = 0; l.K = round4(C * ldk); l.XO = l.K + round4(C * ldk); l.HY = l.XO + C * dk; l.DD = l.HY + C * dk;
+    const int after = l.DD + C * dk;
+    l.HB = o; o += tiles > after ? tiles : after; o = round4(o);
+    l.TB = l.HB + 4 * hr * kHS;
     l.pbeta = o; o += C; o = round4(o);
     l.us = o; o += dk; o = round4(o);
     l.red = o; o += 2 * C + 1; o = round4(o);
@@ -851,19 +856,21 @@ __host__ __device__ inline GradLay grad_lay(int C, int dk, bool perch) {
 template <typename Tin, typename Tdo, bool PERCH, int CC, int NTW>
 __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws ws, int n_tiles) {
     extern __shared__ __align__(16) float smem[];
-    constexpr int TT = kTT;           // stride of the transposed tiles
     constexpr int MT = CC / 16;       // 16-row blocks of the chunk
     constexpr int NP = (CC * CC + kThreads - 1) / kThreads;
+    constexpr int NO = CC * kBV / kThreads;   // dO elements per thread and tile
     const int dk = a.dk, dv = a.dv, H = a.H, ldk = 8 * walk_cpt(dk) + 4, lg = PERCH ? ldk : 1, dkp = round4(dk);
     const GradLay ly = grad_lay(CC, dk, PERCH);
     const Rec rc = rec_lay(CC, dk, PERCH);
-    float* Qs = smem + ly.Q;  float* Ks = smem + ly.K;  float* Gs = smem + ly.G;  float* Bs = smem + ly.B;
+    const int hrows = 8 * NTW * (kThreads / 32);
+    float* Gs = smem + ly.G;  float* Bs = smem + ly.B;
     float* KK = smem + ly.KK; float* Pm = smem + ly.P;  float* Ex = smem + ly.Ex;
     float* dPm = smem + ly.dP; float* dAm = smem + ly.dA;
-    float* Hs = smem + ly.H;  float* dHs = smem + ly.dH;
-    float* Ot = smem + ly.Ot; float* Dt = smem + ly.Dt; float* Yt = smem + ly.Yt; float* Zt = smem + ly.Zt;
-    float* XO = smem + ly.XO; float* HY = smem + ly.HY; float* DD = smem + ly.DD;
     float* pbeta = smem + ly.pbeta; float* us = smem + ly.us; float* red = smem + ly.red;
+    // tile buffers b = 0, 1: state, state gradient, then the dO, Delta, Y, Z tiles
+    auto Hb = [&](int b) { return smem + ly.HB + b * hrows * kHS; };
+    auto dHb = [&](int b) { return smem + ly.HB + (2 + b) * hrows * kHS; };
+    auto Tb = [&](int which, int b) { return smem + ly.TB + (2 * which + b) * CC * kHS; };   // 0 dO, 1 D, 2 Y, 3 Z
     const int tid = threadIdx.x;
     const long slot = blockIdx.x / H;
     const int hh = (int)(blockIdx.x % H);
@@ -875,18 +882,69 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
     const size_t tok0 = ((size_t)geo.b * a.T + geo.bos + cs) * H + hh;
     const float scale = a.scale;
     const size_t sbase = ((size_t)slot * H + hh) * dk * dv, cbase = ((size_t)slot * H + hh) * CC * dv;
+    const bool vec = (dv & 3) == 0;   // 16-byte copies need every row start on 16 bytes
+    const Tdo* dO = static_cast<const Tdo*>(a.dO);
 
-    // raw q, k rows; KK, P, the cumulative gate and beta from the chunk record
-    {
-        const Tin* q = static_cast<const Tin*>(a.q);
-        const Tin* k = static_cast<const Tin*>(a.k);
-        for (int idx = tid; idx < CC * dkp; idx += kThreads) {
-            const int r = idx / dkp, c = idx % dkp;
-            const bool in = r < L && c < dk;
-            const size_t off = (tok0 + (size_t)r * H) * dk + c;
-            Qs[r * ldk + c] = in ? ld_f32<Tin>(q, off) : 0.f;
-            Ks[r * ldk + c] = in ? ld_f32<Tin>(k, off) : 0.f;
+    // the tile's state rows and D, Y, Z rows into buffer b, as one cp.async group (plain loads where a 16-byte
+    // copy does not apply: the tile's ragged edge, or d_v not a multiple of 4)
+    auto issue_tile = [&](int t, int b) {
+        const int j0 = t * kBV, bw = min(kBV, dv - j0);
+        float* h_ = Hb(b);
+        float* dh_ = dHb(b);
+        for (int idx = tid; idx < hrows * 8; idx += kThreads) {
+            const int c = idx >> 3, j = 4 * (idx & 7);
+            const size_t o = sbase + (size_t)c * dv + j0 + j;
+            if (vec && c < dk && j + 4 <= bw) {
+                cp_async16(h_ + c * kHS + j, ws.h + o);
+                cp_async16(dh_ + c * kHS + j, ws.dh + o);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const bool in = c < dk && j + u < bw;
+                    h_[c * kHS + j + u] = in ? ws.h[o + u] : 0.f;
+                    dh_[c * kHS + j + u] = in ? ws.dh[o + u] : 0.f;
+                }
+            }
         }
+        float* D_ = Tb(1, b);
+        float* Y_ = Tb(2, b);
+        float* Z_ = Tb(3, b);
+        for (int idx = tid; idx < CC * 8; idx += kThreads) {
+            const int r = idx >> 3, j = 4 * (idx & 7);
+            const size_t o = cbase + (size_t)r * dv + j0 + j;
+            if (vec && r < L && j + 4 <= bw) {
+                cp_async16(D_ + r * kHS + j, ws.D + o);
+                cp_async16(Y_ + r * kHS + j, ws.Y + o);
+                cp_async16(Z_ + r * kHS + j, ws.Z + o);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const bool in = r < L && j + u < bw;
+                    D_[r * kHS + j + u] = in ? ws.D[o + u] : 0.f;
+                    Y_[r * kHS + j + u] = in ? ws.Y[o + u] : 0.f;
+                    Z_[r * kHS + j + u] = in ? ws.Z[o + u] : 0.f;
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    // dO of tile t into registers (element k: row (tid + 256 k) / 32, column lane)
+    float opre[NO];
+    auto load_do = [&](int t) {
+        const int j0 = t * kBV, bw = min(kBV, dv - j0);
+#pragma unroll
+        for (int k = 0; k < NO; ++k) {
+            const int idx = tid + k * kThreads, r = idx / kBV, j = idx % kBV;
+            opre[k] = (r < L && j < bw) ? ld_f32<Tdo>(dO, (tok0 + (size_t)r * H) * dv + j0 + j) : 0.f;
+        }
+    };
+    if (n_tiles > 0) {
+        issue_tile(0, 0);
+        load_do(0);
+    }
+
+    // KK, P, the cumulative gate and beta from the chunk record
+    {
         const float* rec = ws.rec + ((size_t)slot * H + hh) * rc.total;
         for (int i = tid; i < CC * (CC + 1); i += kThreads) {
             KK[i] = rec[rc.KK + i];
@@ -895,6 +953,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
         for (int i = tid; i < CC * lg; i += kThreads) Gs[i] = rec[rc.G + i];
         for (int i = tid; i < CC; i += kThreads) Bs[i] = rec[rc.B + i];
     }
+    for (int c = tid; c < dk; c += kThreads) us[c] = 0.f;
     if (!PERCH) {
         __syncthreads();
         for (int idx = tid; idx < CC * CC; idx += kThreads) {
@@ -918,31 +977,31 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
             for (int nn = 0; nn < NTW; ++nn)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) acc[p][m][nn][i] = 0.f;
-    for (int c = tid; c < dk; c += kThreads) us[c] = 0.f;
-    const Tdo* dO = static_cast<const Tdo*>(a.dO);
-    const int hrows = 8 * NTW * (kThreads / 32);
     for (int t = 0; t < n_tiles; ++t) {
-        const int j0 = t * kBV, bw = min(kBV, dv - j0);
-        __syncthreads();
-        for (int idx = tid; idx < hrows * kBV; idx += kThreads) {
-            const int c = idx / kBV, j = idx % kBV;
-            const bool in = j < bw && c < dk;
-            Hs[c * kHS + j] = in ? ws.h[sbase + (size_t)c * dv + j0 + j] : 0.f;
-            dHs[c * kHS + j] = in ? ws.dh[sbase + (size_t)c * dv + j0 + j] : 0.f;
+        const int bf = t & 1, j0 = t * kBV, bw = min(kBV, dv - j0);
+        float* Hs = Hb(bf);
+        float* dHs = dHb(bf);
+        float* O_ = Tb(0, bf);
+        float* D_ = Tb(1, bf);
+        float* Y_ = Tb(2, bf);
+        float* Z_ = Tb(3, bf);
+#pragma unroll
+        for (int k = 0; k < NO; ++k) {
+            const int idx = tid + k * kThreads;
+            O_[(idx / kBV) * kHS + idx % kBV] = opre[k];
         }
-        for (int idx = tid; idx < CC * kBV; idx += kThreads) {
-            const int r = idx / kBV, j = idx % kBV;
-            const bool in = r < L && j < bw;
-            Ot[j * TT + r] = in ? ld_f32<Tdo>(dO, (tok0 + (size_t)r * H) * dv + j0 + j) : 0.f;
-            Dt[j * TT + r] = in ? ws.D[cbase + (size_t)r * dv + j0 + j] : 0.f;
-            Yt[j * TT + r] = in ? ws.Y[cbase + (size_t)r * dv + j0 + j] : 0.f;
-            Zt[j * TT + r] = in ? ws.Z[cbase + (size_t)r * dv + j0 + j] : 0.f;
+        if (t + 1 < n_tiles) {
+            issue_tile(t + 1, bf ^ 1);
+            load_do(t + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
         __syncthreads();
         // dV = diag(beta) Y
         for (int idx = tid; idx < CC * kBV; idx += kThreads) {
             const int r = idx / kBV, j = idx % kBV;
-            if (r < L && j < bw) a.gv[(tok0 + (size_t)r * H) * dv + j0 + j] = Bs[r] * Yt[j * TT + r];
+            if (r < L && j < bw) a.gv[(tok0 + (size_t)r * H) * dv + j0 + j] = Bs[r] * Y_[r * kHS + j];
         }
         // dP = dO Delta^T, dA = -Y Delta^T (pairs owned by threads across the tiles)
 #pragma unroll
@@ -953,9 +1012,9 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
                 if (s <= r) {
                     float x = dp[k], y = da[k];
                     for (int j = 0; j < kBV; ++j) {
-                        const float d = Dt[j * TT + s];
-                        x = fmaf(Ot[j * TT + r], d, x);
-                        y = fmaf(Yt[j * TT + r], d, y);
+                        const float d = D_[s * kHS + j];
+                        x = fmaf(O_[r * kHS + j], d, x);
+                        y = fmaf(Y_[r * kHS + j], d, y);
                     }
                     dp[k] = x;
                     da[k] = y;
@@ -963,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
             }
         }
         if (tid < CC) {
-            for (int j = 0; j < kBV; ++j) ubeta = fmaf(Yt[j * TT + tid], Zt[j * TT + tid], ubeta);
+            for (int j = 0; j < kBV; ++j) ubeta = fmaf(Y_[tid * kHS + j], Z_[tid * kHS + j], ubeta);
         }
         // us[c] += sum_j dh[c][j] h[c][j]: one warp per channel, lane = column (each channel always meets the
         // same warp, so the sum needs no atomics)
@@ -987,15 +1046,10 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
             }
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                const int r0 = 16 * m + fg;
                 uint32_t oh[4], ol[4], yh[4], yl[4], dh4[4], dl4[4];
-                const int i0 = (k0 + ft) * TT + r0, i1 = (k0 + ft + 4) * TT + r0;
-                split_tf32(Ot[i0], oh[0], ol[0]); split_tf32(Ot[i0 + 8], oh[1], ol[1]);
-                split_tf32(Ot[i1], oh[2], ol[2]); split_tf32(Ot[i1 + 8], oh[3], ol[3]);
-                split_tf32(Yt[i0], yh[0], yl[0]); split_tf32(Yt[i0 + 8], yh[1], yl[1]);
-                split_tf32(Yt[i1], yh[2], yl[2]); split_tf32(Yt[i1 + 8], yh[3], yl[3]);
-                split_tf32(Dt[i0], dh4[0], dl4[0]); split_tf32(Dt[i0 + 8], dh4[1], dl4[1]);
-                split_tf32(Dt[i1], dh4[2], dl4[2]); split_tf32(Dt[i1 + 8], dh4[3], dl4[3]);
+                frag_a(O_, kHS, 16 * m, k0, fg, ft, oh, ol);
+                frag_a(Y_, kHS, 16 * m, k0, fg, ft, yh, yl);
+                frag_a(D_, kHS, 16 * m, k0, fg, ft, dh4, dl4);
 #pragma unroll
                 for (int nn = 0; nn < NTW; ++nn) {
                     mma3_tf32(acc[0][m][nn], oh, ol, bhh[nn], bhl[nn]);
@@ -1004,8 +1058,25 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
                 }
             }
         }
+        __syncthreads();   // this tile's buffers are free for the tile after next
     }
-    // the accumulators to [C][dk] (channels below d_k only)
+    // the tile space now holds raw q, k rows and the state products [C][dk] (channels below d_k only)
+    float* Qs = smem + ly.HB + ly.Q;
+    float* Ks = smem + ly.HB + ly.K;
+    float* XO = smem + ly.HB + ly.XO;
+    float* HY = smem + ly.HB + ly.HY;
+    float* DD = smem + ly.HB + ly.DD;
+    {
+        const Tin* q = static_cast<const Tin*>(a.q);
+        const Tin* k = static_cast<const Tin*>(a.k);
+        for (int idx = tid; idx < CC * dkp; idx += kThreads) {
+            const int r = idx / dkp, c = idx % dkp;
+            const bool in = r < L && c < dk;
+            const size_t off = (tok0 + (size_t)r * H) * dk + c;
+            Qs[r * ldk + c] = in ? ld_f32<Tin>(q, off) : 0.f;
+            Ks[r * ldk + c] = in ? ld_f32<Tin>(k, off) : 0.f;
+        }
+    }
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
