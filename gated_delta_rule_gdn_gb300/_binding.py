@@ -72,6 +72,8 @@ def _declare(lib):
                                   i, i, i, i, i, i, i, i, vp, ctypes.c_size_t, vp]
     lib.gdn_chunk_bwd_workspace_size.restype = i
     lib.gdn_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.gdn_test_inject.restype = i
+    lib.gdn_test_inject.argtypes = [i]
     lib.gdn_last_error.argtypes = []
     lib.gdn_device_status.restype = i
     lib.gdn_device_status.argtypes = [i]

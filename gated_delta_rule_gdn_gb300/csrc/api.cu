@@ -15,6 +15,7 @@
 namespace {
 
 thread_local std::string g_last_error;
+thread_local int g_test_injection = 0;
 
 gdn_status fail(gdn_status s, const char* fmt, ...) {
     char buf[512];
@@ -245,6 +246,14 @@ gdn_status check_bwd(gdn::BwdArgs& a, gdn_dtype dtype, gdn_dtype do_dtype, const
 
 }  // namespace
 
+namespace gdn {
+int take_test_injection() {
+    const int v = g_test_injection;
+    g_test_injection = 0;
+    return v;
+}
+}  // namespace gdn
+
 extern "C" {
 
 gdn_status gdn_chunk_fwd_algo(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -419,7 +428,7 @@ gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const vo
     gdn::BwdArgs a{q, k, v, g, beta, scale, initial_state, grad_o, grad_final_state, cu_seqlens, n_seqs,
                    grad_q, grad_k, grad_v, grad_g, grad_beta, grad_initial_state, nullptr,
                    B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, do_dtype == GDN_BF16 ? 1 : 0,
-                   per_channel ? 1 : 0};
+                   per_channel ? 1 : 0, 0};
     gdn_status st = check_bwd(a, dtype, do_dtype, fn);
     if (st != GDN_OK) return st;
     const bool any_tokens = (long)a.B * a.T > 0;
@@ -448,6 +457,7 @@ gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const vo
         if (e != cudaSuccess) return cuda_fail(e, fn);
     }
     a.ck = static_cast<float*>(ws);
+    a.test_skip_record = gdn::take_test_injection() == GDN_TEST_BWD_RECORD_STALL ? 1 : 0;
     e = gdn::launch_chunk_bwd(a, s);
     if (!workspace && ws) {
         const cudaError_t e2 = cudaFreeAsync(ws, s);
@@ -465,10 +475,17 @@ gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, in
     const int32_t* cu = n_seqs > 0 ? reinterpret_cast<const int32_t*>(uintptr_t(1) << 20) : nullptr;
     gdn::BwdArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, 1.0f, nullptr, nullptr, nullptr, cu, n_seqs,
                    nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                   B, T, H, d_k, d_v, chunk_size, 0, 0, per_channel ? 1 : 0};
+                   B, T, H, d_k, d_v, chunk_size, 0, 0, per_channel ? 1 : 0, 0};
     gdn_status st = check_bwd(a, GDN_F32, GDN_F32, fn);
     if (st != GDN_OK) return st;
     *bytes = gdn::bwd_workspace_bytes(a);
+    return ok();
+}
+
+gdn_status gdn_test_inject(int what) {
+    if (what != 0 && what != GDN_TEST_BWD_RECORD_STALL)
+        return fail(GDN_ERR_INVALID_ARG, "gdn_test_inject: unknown injection %d", what);
+    g_test_injection = what;
     return ok();
 }
 

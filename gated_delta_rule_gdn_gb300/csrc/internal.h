@@ -120,8 +120,12 @@ struct BwdArgs {
     int bf16;               // q, k, v dtype: 1 bf16, 0 fp32
     int do_bf16;            // dO dtype
     int per_channel;
+    int test_skip_record;   // test of the bounded waits: the walks leave out the copy of their first chunk record
     int N() const { return cu ? n_seqs : B; }
 };
+
+// One-shot test injection armed by gdn_test_inject (api.cu), consumed by the calling thread's next backward call.
+int take_test_injection();
 
 // Chunk backward (chunk_bwd.cu).
 size_t bwd_smem_bytes(int C, int dk, bool per_channel);

@@ -391,11 +391,24 @@ gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const vo
 gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
                                         int n_seqs, size_t* bytes);
 
+/*
+ * gdn_test_inject -- arm a one-shot test of the bounded waits for the calling
+ * thread's next gdn_chunk_bwd call.  GDN_TEST_BWD_RECORD_STALL: the state walks
+ * leave out the bulk copy of their first chunk record, so the bounded wait for
+ * it gives up (after 2 s), the walk records the failure in the device status
+ * and leaves; gdn_device_status then returns GDN_ERR_TIMEOUT, and that call's
+ * gradients are unspecified.  No copy is left in flight and the context stays
+ * usable.  0 disarms.  GDN_ERR_INVALID_ARG for an unknown value.
+ */
+#define GDN_TEST_BWD_RECORD_STALL 1
+gdn_status gdn_test_inject(int what);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* gdn_last_error(void);
 
 /*
- * Device-side status of the kernels that use bounded waits (the tcgen05 path).
+ * Device-side status of the kernels that use bounded waits (the tcgen05 paths
+ * and the chunk backward's state walks).
  * Synchronises the current device.  It returns GDN_OK, or GDN_ERR_TIMEOUT if
  * any CTA gave up a bounded wait since the status was last cleared.  A CTA
  * that gives up drops its work and its outputs are unspecified.  With clear

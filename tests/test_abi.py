@@ -235,3 +235,8 @@ def test_backward_workspace_sizes(lib):
     assert size(True, 1, 100, 2, 256, 128) == size(True, 1, 100, 2, 256, 128, 16)
     with pytest.raises(_binding.GdnError, match="shared memory"):
         size(True, 1, 100, 2, 256, 128, 32)
+
+
+def test_test_injection_argument_checks(lib):
+    assert lib.gdn_test_inject(7) == 1
+    assert lib.gdn_test_inject(0) == 0

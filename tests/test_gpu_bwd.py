@@ -177,3 +177,16 @@ def test_full_size_packed_sampled_chains():
         ref = _oracle(y)
         sub = {m: (got[m][:, t0:t1, h:h + 1] if m != "dh0" else got[m][n:n + 1, h:h + 1]) for m in NAMES}
         _compare(sub, ref, x["q"].dtype, f"packed sequence {n} head {h}")
+
+
+def test_a_walk_wait_that_runs_out_is_reported_and_the_context_stays_usable():
+    # the test injection leaves out the first chunk record's copy: the walks' bounded wait gives up (about 2 s)
+    x = _problem("gdn", "bf16", 1, 64, 2, 128, 128, h0_std=0.02)
+    lib = gdn.load()
+    gdn.device_status()                       # start from a clear status
+    assert lib.gdn_test_inject(1) == 0
+    _gpu(x)                                   # this call's gradients are unspecified
+    assert gdn.device_status() == 4           # GDN_ERR_TIMEOUT, and cleared
+    assert gdn.device_status() == 0
+    _compare(_gpu(x), _oracle(x), torch.bfloat16, "after the timeout")
+    assert gdn.device_status() == 0
