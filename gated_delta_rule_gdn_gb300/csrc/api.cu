@@ -120,7 +120,7 @@ gdn_status chunk_common(const void* q, const void* k, const void* v, const float
                         const gdn_gate_act* act = nullptr, int H_k = 0) {
     gdn::ChunkArgs a{q, k, v, g, beta, scale, initial_state, final_state, cu_seqlens, n_seqs, o,
                      B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0,
-                     o_dtype == GDN_F32 ? 1 : 0};
+                     o_dtype == GDN_F32 ? 1 : 0, gdn::GateAct{nullptr, nullptr, 0}, 0};
     gdn_status st = check_chunk(a, dtype, o_dtype, output_final_state, fn);
     if (st != GDN_OK) return st;
     if (H_k < 0 || (H_k > 0 && H % H_k != 0))
@@ -174,7 +174,7 @@ gdn::ChunkArgs plan_args(int per_channel, int B, int T, int H, int d_k, int d_v,
     return gdn::ChunkArgs{p, p, p, fp, fp, 1.0f, nullptr, nullptr,
                           n_seqs > 0 ? reinterpret_cast<const int32_t*>(p) : nullptr, n_seqs > 0 ? n_seqs : 0,
                           const_cast<void*>(p), B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0,
-                          per_channel ? 1 : 0, o_dtype == GDN_F32 ? 1 : 0};
+                          per_channel ? 1 : 0, o_dtype == GDN_F32 ? 1 : 0, gdn::GateAct{nullptr, nullptr, 0}, 0};
 }
 
 gdn_status step_common(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
@@ -197,7 +197,7 @@ gdn_status step_common(const void* q, const void* k, const void* v, const float*
     if ((long)N * H > (1L << 31) / ((long)d_k * d_v))
         return fail(GDN_ERR_UNSUPPORTED, "%s: state has 2^31 elements or more", fn);
     gdn::StepArgs a{q, k, v, g, beta, scale, state, o, N, H, d_k, d_v, dtype == GDN_BF16 ? 1 : 0,
-                    o_dtype == GDN_F32 ? 1 : 0, per_channel ? 1 : 0};
+                    o_dtype == GDN_F32 ? 1 : 0, per_channel ? 1 : 0, gdn::GateAct{nullptr, nullptr, 0}, 0};
     gdn_status st = set_act(a.act, act, fn);
     if (st != GDN_OK) return st;
     if (per_channel && a.act.gate())
@@ -320,7 +320,7 @@ gdn_status gdn_chunk_fwd_noalloc(int per_channel, const void* q, const void* k, 
     const char* fn = "gdn_chunk_fwd_noalloc";
     gdn::ChunkArgs a{q, k, v, g, beta, scale, initial_state, final_state, cu_seqlens, n_seqs, o,
                      B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, per_channel ? 1 : 0,
-                     o_dtype == GDN_F32 ? 1 : 0};
+                     o_dtype == GDN_F32 ? 1 : 0, gdn::GateAct{nullptr, nullptr, 0}, 0};
     gdn_status st = check_chunk(a, dtype, o_dtype, output_final_state, fn);
     if (st != GDN_OK) return st;
     if (const char* why = gdn::two_pass_unsupported_reason(a))

@@ -46,7 +46,6 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 
 constexpr int kThreads = 256;
 constexpr int kBV = 32;        // d_v columns per tile of the gradient kernel
-constexpr int kTS = kBV + 1;   // padded row stride of [rows][kBV] tiles
 constexpr int kWB = 64;        // d_v columns per walk CTA
 constexpr int kWS = 72;        // row stride of the walk's [rows][kWB] tiles: MMA fragment loads hit banks 8 t + g
 
@@ -201,16 +200,6 @@ __device__ __forceinline__ void load_qk(const BwdArgs& a, size_t tok0, int L, in
         const bool in = r < L;
         Bs[r] = in ? a.beta[tok0 + (size_t)r * H] : 0.f;
         if (!PERCH) Gs[r] = in ? a.g[tok0 + (size_t)r * H] : 0.f;
-    }
-}
-
-// A [rows][kBV] tile of a token-major [.., H, dv] tensor (columns >= bw and rows >= L zero), row stride kTS.
-template <typename T>
-__device__ __forceinline__ void load_rows(float* dst, const T* src, size_t tok0, int H, int dv, int j0, int bw, int L,
-                                          int C) {
-    for (int idx = threadIdx.x; idx < C * kBV; idx += kThreads) {
-        const int r = idx / kBV, j = idx % kBV;
-        dst[r * kTS + j] = (r < L && j < bw) ? ld_f32<T>(src, (tok0 + (size_t)r * H) * dv + j0 + j) : 0.f;
     }
 }
 

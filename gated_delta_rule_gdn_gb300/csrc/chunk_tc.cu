@@ -377,7 +377,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         int issued = 0;                                // chunks whose TMA loads have been issued
         const int jrow = t256 & 63, part = t256 >> 6;  // (row, quarter of the columns) for the elementwise builds
         bool ok = true;
-        const float LOG2E = 1.4426950408889634f;
         for (int e = t256; e < 64 * TS; e += NPREP) T32[e] = 0.f;   // the upper triangle stays zero
         if (loader) {
             prefetch_tmap(&tmap_q);
@@ -590,7 +589,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         fence_async_smem();
         named_bar(2, 128);
         for (int t = 0; t < n_chunks; ++t) {
-            const int s = t & 1;
             if (ok) ok = mbar_wait(&S.prep_done, t & 1, kWaitNs);
             if (!ok && t128 == 0) set_status(256u);
             const int L = S.info_L[t & 3];
