@@ -14,6 +14,8 @@ Contents:
 * ``recurrence_backward``: the gradients of <dO, o> + <dhT, h_final> with respect
   to q, k, v, g, beta and the initial state, by reverse-mode differentiation of
   the same token steps (C, fp64).
+* ``gate_activation``, ``beta_activation``, ``activation_backward``: the gate and
+  beta activations from raw logits and their chain rule (numpy, fp64).
 * ``reference``: numpy twins that pin the oracle.  They are the literal d x d
   matrix recurrence, the DeltaNet and Mamba2 limits, and brute-force
   chunkwise / WY / UT evaluators with three triangular solves.
@@ -33,7 +35,8 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["recurrence", "recurrence_backward", "load", "max_threads"]
+__all__ = ["recurrence", "recurrence_backward", "gate_activation", "beta_activation", "activation_backward", "load",
+           "max_threads"]
 
 _lib = None
 
@@ -146,4 +149,48 @@ def recurrence_backward(q, k, v, g, beta, scale: float, d_out, initial_state=Non
         int(N if cu is not None else 0), B, T, H, dk, dv, int(bool(gate_per_channel)), int(n_threads))
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out
+
+
+def _sigmoid(x):
+    return 0.5 * (1.0 + np.tanh(0.5 * x))
+
+
+def gate_activation(x, A_log, dt_bias=None):
+    """log alpha = -exp(A_log[h]) softplus(x + dt_bias[h]) ("Gated Delta Network (GDN)", §3.1 eq. 5), fp64.
+    x [..., H] (the head axis last); A_log, dt_bias [H]."""
+    y = _f64(x) + (0.0 if dt_bias is None else _f64(dt_bias))
+    return -np.exp(_f64(A_log)) * np.logaddexp(0.0, y)
+
+
+def beta_activation(b, mult: int = 1):
+    """beta = mult * sigmoid(b): mult 1, or 2 for beta in (0, 2) ("Gated Delta Network (GDN)", §5 notes), fp64."""
+    return mult * _sigmoid(_f64(b))
+
+
+def activation_backward(x, b, A_log, dt_bias, mult, dg, dbeta):
+    """The chain rule through the two activations, fp64.
+
+    With y = x + dt_bias and log alpha = -exp(A_log) softplus(y):  d log alpha / dx = -exp(A_log) sigmoid(y),
+    d log alpha / dA_log = log alpha, d log alpha / d dt_bias = d log alpha / dx; with beta = mult sigmoid(b):
+    d beta / db = mult sigmoid(b) (1 - sigmoid(b)).  dg, dbeta are the gradients of log alpha and beta; A_log = None
+    skips the gate (dx = dg), mult = 0 skips beta (db = dbeta).  Returns dict(dx, db, dA_log [H], ddt_bias [H])."""
+    dg, dbeta = _f64(dg), _f64(dbeta)
+    out = {}
+    if A_log is not None:
+        y = _f64(x) + (0.0 if dt_bias is None else _f64(dt_bias))
+        e = np.exp(_f64(A_log))
+        g = -e * np.logaddexp(0.0, y)
+        dx = dg * (-e * _sigmoid(y))
+        axes = tuple(range(dx.ndim - 1))
+        out["dx"] = dx
+        out["dA_log"] = np.sum(dg * g, axis=axes)
+        out["ddt_bias"] = np.sum(dx, axis=axes)
+    else:
+        out["dx"] = dg
+    if mult:
+        sb = _sigmoid(_f64(b))
+        out["db"] = dbeta * mult * sb * (1.0 - sb)
+    else:
+        out["db"] = dbeta
     return out

@@ -178,3 +178,48 @@ def test_pins_catch_backward_mutation(name, monkeypatch):
             if max(errs.values()) > 1e-4:
                 caught = True
         assert caught, name
+
+
+# --- the activations around the backward -----------------------------------------------------------------
+
+@pytest.mark.parametrize("mult", [1, 2])
+def test_activation_chain_rule_matches_central_differences(mult):
+    # L(x, b, A_log, dt_bias) = <dO, o> + <dhT, h_T> with log alpha and beta formed from raw logits
+    c = _case(11, T=9)
+    rng = np.random.default_rng(12)
+    B, T, H = c["beta"].shape
+    x = rng.standard_normal((B, T, H))
+    b = rng.standard_normal((B, T, H))
+    A_log = np.log(rng.uniform(0.5, 4.0, H))
+    dt = rng.normal(0.0, 0.3, H)
+    scale = 0.8
+
+    def loss(x_, b_, A_, dt_):
+        d = dict(c)
+        d["g"] = oracle.gate_activation(x_, A_, dt_)
+        d["beta"] = oracle.beta_activation(b_, mult)
+        return _loss(d, scale)
+
+    d = dict(c)
+    d["g"] = oracle.gate_activation(x, A_log, dt)
+    d["beta"] = oracle.beta_activation(b, mult)
+    gr = _grads(d, scale)
+    ch = oracle.activation_backward(x, b, A_log, dt, mult, gr["dg"], gr["dbeta"])
+    eps = 1e-6
+    args = [x, b, A_log, dt]
+    names = ["dx", "db", "dA_log", "ddt_bias"]
+    for i, name in enumerate(names):
+        E = rng.standard_normal(args[i].shape)
+        ap = list(args); ap[i] = args[i] + eps * E
+        am = list(args); am[i] = args[i] - eps * E
+        fd = (loss(*ap) - loss(*am)) / (2 * eps)
+        an = float(np.sum(ch[name] * E))
+        assert abs(fd - an) <= 1e-6 * max(abs(fd), 1e-3), (name, fd, an)
+
+
+def test_activations_match_their_definitions_at_known_points():
+    # softplus(0) = log 2, sigmoid(0) = 1/2; beta doubles with mult 2
+    assert np.isclose(oracle.gate_activation(np.zeros(1), np.zeros(1), None)[0], -np.log(2.0), rtol=0, atol=1e-15)
+    assert np.isclose(oracle.beta_activation(np.zeros(1), 2)[0], 1.0, rtol=0, atol=1e-15)
+    assert np.isclose(oracle.gate_activation(np.array([30.0]), np.array([np.log(3.0)]), np.array([1.0]))[0], -93.0,
+                      rtol=1e-12)
