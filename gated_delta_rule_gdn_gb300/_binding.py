@@ -70,6 +70,9 @@ def _declare(lib):
     lib.gdn_chunk_bwd.restype = i
     lib.gdn_chunk_bwd.argtypes = [i, vp, vp, vp, vp, vp, fp, vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp,
                                   i, i, i, i, i, i, i, i, vp, ctypes.c_size_t, vp]
+    lib.gdn_chunk_bwd_act.restype = i
+    lib.gdn_chunk_bwd_act.argtypes = [i, vp, vp, vp, vp, vp, fp, vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      i, i, i, i, i, i, i, i, ctypes.POINTER(GateAct), vp, ctypes.c_size_t, vp]
     lib.gdn_chunk_bwd_workspace_size.restype = i
     lib.gdn_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.gdn_test_inject.restype = i
@@ -276,11 +279,15 @@ def bwd_workspace_size(per_channel: bool, B: int, T: int, H: int, dk: int, dv: i
 
 
 def chunk_bwd(per_channel: bool, q, k, v, g, beta, d_o, scale=None, initial_state=None, d_final_state=None,
-              cu_seqlens=None, chunk_size=0, stream=None, workspace=None, want_d_initial_state=True):
-    """Gradients of <d_o, o> + <d_final_state, final_state> through the chunk forward (C ABI gdn_chunk_bwd).
+              cu_seqlens=None, chunk_size=0, stream=None, workspace=None, want_d_initial_state=True, A_log=None,
+              dt_bias=None, beta_sigmoid=False, allow_neg_eigval=False):
+    """Gradients of <d_o, o> + <d_final_state, final_state> through the chunk forward (C ABI gdn_chunk_bwd, or
+    gdn_chunk_bwd_act with an activation).
 
     Inputs as the forward (per_channel: KDA gate [B, T, H, dk]); d_o [B, T, H, dv] fp32 or bf16; d_final_state
-    [N, H, dk, dv] fp32 or None.  Returns (dq, dk, dv, dg, dbeta, d_initial_state or None), all fp32."""
+    [N, H, dk, dv] fp32 or None.  Returns (dq, dk, dv, dg, dbeta, d_initial_state or None), all fp32.  With
+    A_log / dt_bias / beta_sigmoid as for gdn_chunk_fwd, g and beta are raw logits, dg and dbeta are their
+    gradients, and the result gains (dA_log, ddt_bias or None) at the end."""
     lib = load()
     if q.dtype not in DTYPES:
         raise ValueError(f"q must be float32 or bfloat16 (got {q.dtype})")
@@ -318,13 +325,18 @@ def chunk_bwd(per_channel: bool, q, k, v, g, beta, d_o, scale=None, initial_stat
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if workspace is not None:
         _need(workspace, "workspace", torch.uint8, dev)
-    _check(lib.gdn_chunk_bwd(int(per_channel), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
-                             _ptr(initial_state), _ptr(d_o), _ptr(d_final_state), _ptr(cu_seqlens), n_seqs,
-                             _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
-                             B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[d_o.dtype],
-                             _ptr(workspace), 0 if workspace is None else workspace.numel(),
-                             _stream_handle(stream, dev)))
-    return dq, dkk, dvv, dg, dbeta, dh0
+    act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
+    dA = torch.empty(H, **f32) if A_log is not None else None
+    ddt = torch.empty(H, **f32) if dt_bias is not None else None
+    _check(lib.gdn_chunk_bwd_act(int(per_channel), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                 _ptr(initial_state), _ptr(d_o), _ptr(d_final_state), _ptr(cu_seqlens), n_seqs,
+                                 _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(dA),
+                                 _ptr(ddt), B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[d_o.dtype],
+                                 None if act is None else ctypes.byref(act), _ptr(workspace),
+                                 0 if workspace is None else workspace.numel(), _stream_handle(stream, dev)))
+    if act is None:
+        return dq, dkk, dvv, dg, dbeta, dh0
+    return dq, dkk, dvv, dg, dbeta, dh0, dA, ddt
 
 
 def gdn_chunk_bwd(q, k, v, g, beta, d_o, **kw):

@@ -418,19 +418,29 @@ gdn_status gdn_chunk_workspace_size(int per_channel, int B, int T, int H, int d_
     return ok();
 }
 
-gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const void* v, const float* g,
-                         const float* beta, float scale, const float* initial_state, const void* grad_o,
-                         const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
-                         float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
-                         int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
-                         gdn_dtype do_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-    const char* fn = "gdn_chunk_bwd";
+gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float scale, const float* initial_state, const void* grad_o,
+                             const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
+                             float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
+                             float* grad_A_log, float* grad_dt_bias, int B, int T, int H, int d_k, int d_v,
+                             int chunk_size, gdn_dtype dtype, gdn_dtype do_dtype, const gdn_gate_act* act,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = act ? "gdn_chunk_bwd_act" : "gdn_chunk_bwd";
     gdn::BwdArgs a{q, k, v, g, beta, scale, initial_state, grad_o, grad_final_state, cu_seqlens, n_seqs,
                    grad_q, grad_k, grad_v, grad_g, grad_beta, grad_initial_state, nullptr,
                    B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, do_dtype == GDN_BF16 ? 1 : 0,
                    per_channel ? 1 : 0, 0};
     gdn_status st = check_bwd(a, dtype, do_dtype, fn);
     if (st != GDN_OK) return st;
+    gdn::GateAct ga{nullptr, nullptr, 0};
+    st = set_act(ga, act, fn);
+    if (st != GDN_OK) return st;
+    if (per_channel && ga.gate())
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the gate activation applies to the scalar gate only", fn);
+    if (ga.gate() && (!grad_A_log || !aligned(grad_A_log, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "%s: grad_A_log must be a 4-byte aligned [H] buffer when A_log is given", fn);
+    if (grad_dt_bias && (!ga.dt_bias || !aligned(grad_dt_bias, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "%s: grad_dt_bias needs dt_bias and 4-byte alignment", fn);
     const bool any_tokens = (long)a.B * a.T > 0;
     if (any_tokens && (!q || !k || !v || !g || !beta || !grad_o || !grad_q || !grad_k || !grad_v || !grad_g ||
                        !grad_beta))
@@ -458,13 +468,36 @@ gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const vo
     }
     a.ck = static_cast<float*>(ws);
     a.test_skip_record = gdn::take_test_injection() == GDN_TEST_BWD_RECORD_STALL ? 1 : 0;
-    e = gdn::launch_chunk_bwd(a, s);
+    const long n_tok = (long)a.B * a.T * a.H;
+    float* g_act = reinterpret_cast<float*>(static_cast<char*>(ws) + gdn::bwd_act_offset(a));
+    float* beta_act = g_act + n_tok;
+    if (ga.any()) {
+        e = gdn::launch_bwd_act_apply(g, beta, ga, g_act, beta_act, n_tok, H, s);
+        if (ga.gate()) a.g = g_act;
+        if (ga.beta_sigmoid) a.beta = beta_act;
+    }
+    if (e == cudaSuccess) e = gdn::launch_chunk_bwd(a, s);
+    if (e == cudaSuccess && ga.any())
+        e = gdn::launch_bwd_act_post(g, beta, g_act, ga, grad_g, grad_beta, grad_A_log, grad_dt_bias,
+                                     (long)a.B * a.T, H, s);
     if (!workspace && ws) {
         const cudaError_t e2 = cudaFreeAsync(ws, s);
         if (e == cudaSuccess) e = e2;
     }
     if (e != cudaSuccess) return cuda_fail(e, fn);
     return ok();
+}
+
+gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, float scale, const float* initial_state, const void* grad_o,
+                         const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
+                         float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
+                         int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
+                         gdn_dtype do_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    return gdn_chunk_bwd_act(per_channel, q, k, v, g, beta, scale, initial_state, grad_o, grad_final_state,
+                             cu_seqlens, n_seqs, grad_q, grad_k, grad_v, grad_g, grad_beta, grad_initial_state,
+                             nullptr, nullptr, B, T, H, d_k, d_v, chunk_size, dtype, do_dtype, nullptr, workspace,
+                             workspace_bytes, stream);
 }
 
 gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,

@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "gate_act.cuh"
 #include "tc_common.cuh"
 
 namespace gdn {
@@ -1248,7 +1249,91 @@ cudaError_t launch_in(const BwdArgs& a, cudaStream_t s) {
     return a.per_channel ? launch_gate<Tin, float, true>(a, s) : launch_gate<Tin, float, false>(a, s);
 }
 
+// ---- the gate and beta activations around the backward ------------------------------------------------------
+
+// log alpha and beta of every token from their raw logits (the activation of the forward, gate_act.cuh)
+__global__ void bwd_act_apply_kernel(const float* x, const float* b, const GateAct act, float* g_out, float* beta_out,
+                                     long n, int H) {
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int h = (int)(i % H);
+        if (act.A_log) g_out[i] = act_gate(act, x[i], h);
+        if (act.beta_sigmoid) beta_out[i] = act_beta(act, b[i]);
+    }
+}
+
+__device__ __forceinline__ float sigmoid_f(float y) { return 1.f / (1.f + expf(-y)); }
+
+// Per head h: dA_log[h] = sum_t dg_t log alpha_t and ddt_bias[h] = sum_t dg_t (-exp(A_log) sigmoid(x_t + dt_bias)),
+// over every token, in a fixed order (thread-strided sums, then a fixed tree): the result does not depend on
+// scheduling.  One CTA per head.
+__global__ void __launch_bounds__(kThreads) bwd_act_head_kernel(const float* x, const float* g_act, const float* dg,
+                                                                const GateAct act, float* dA_log, float* ddt,
+                                                                long rows, int H) {
+    __shared__ float red[2][kThreads];
+    const int h = blockIdx.x, tid = threadIdx.x;
+    const float e = expf(act.A_log[h]), dtb = act.dt_bias ? act.dt_bias[h] : 0.f;
+    float sa = 0.f, sd = 0.f;
+    for (long r = tid; r < rows; r += kThreads) {
+        const long i = r * H + h;
+        sa = fmaf(dg[i], g_act[i], sa);
+        sd = fmaf(dg[i], -e * sigmoid_f(x[i] + dtb), sd);
+    }
+    red[0][tid] = sa;
+    red[1][tid] = sd;
+    __syncthreads();
+    for (int o = kThreads / 2; o > 0; o >>= 1) {
+        if (tid < o) {
+            red[0][tid] += red[0][tid + o];
+            red[1][tid] += red[1][tid + o];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        dA_log[h] = red[0][0];
+        if (ddt) ddt[h] = red[1][0];
+    }
+}
+
+// In place: dg <- dg (-exp(A_log) sigmoid(x + dt_bias)) (gradient of the raw gate logit) and
+// dbeta <- dbeta * m sigmoid(b) (1 - sigmoid(b)) (gradient of the raw beta logit, m = 1 or 2).
+__global__ void bwd_act_chain_kernel(const float* x, const float* b, const GateAct act, float* dg, float* dbeta,
+                                     long n, int H) {
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int h = (int)(i % H);
+        if (act.A_log) {
+            const float dtb = act.dt_bias ? act.dt_bias[h] : 0.f;
+            dg[i] *= -expf(act.A_log[h]) * sigmoid_f(x[i] + dtb);
+        }
+        if (act.beta_sigmoid) {
+            const float s = sigmoid_f(b[i]);
+            dbeta[i] *= (float)act.beta_sigmoid * s * (1.f - s);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_act_apply(const float* x, const float* b, const GateAct& act, float* g_out, float* beta_out,
+                                 long n, int H, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)min((n + kThreads - 1) / kThreads, 152L * 16);
+    bwd_act_apply_kernel<<<blocks, kThreads, 0, s>>>(x, b, act, g_out, beta_out, n, H);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_act_post(const float* x, const float* b, const float* g_act, const GateAct& act, float* dg,
+                                float* dbeta, float* dA_log, float* ddt, long rows, int H, cudaStream_t s) {
+    if (act.gate()) {
+        bwd_act_head_kernel<<<(unsigned)H, kThreads, 0, s>>>(x, g_act, dg, act, dA_log, ddt, rows, H);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const long n = rows * H;
+    if (n == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)min((n + kThreads - 1) / kThreads, 152L * 16);
+    bwd_act_chain_kernel<<<blocks, kThreads, 0, s>>>(x, b, act, dg, dbeta, n, H);
+    return cudaGetLastError();
+}
 
 size_t bwd_smem_bytes(int C, int dk, bool per_channel) {
     const size_t w = (size_t)walk_lay(C, dk, per_channel).total * sizeof(float);
@@ -1264,9 +1349,14 @@ int bwd_auto_chunk(int dk, bool per_channel) {
     return 0;
 }
 
-size_t bwd_workspace_bytes(const BwdArgs& a) {
+size_t bwd_act_offset(const BwdArgs& a) {
     const long slots = workspace_slots(a.B, a.T, a.C, a.n_seqs, a.cu != nullptr);
-    return ws_floats(slots, a.H, a.C, a.dk, a.dv, a.per_channel != 0) * sizeof(float);
+    return (ws_floats(slots, a.H, a.C, a.dk, a.dv, a.per_channel != 0) * sizeof(float) + 255) & ~(size_t)255;
+}
+
+// the walks' workspace, then room for the activated log alpha and beta ([B, T, H] fp32 each)
+size_t bwd_workspace_bytes(const BwdArgs& a) {
+    return bwd_act_offset(a) + (size_t)2 * a.B * a.T * a.H * sizeof(float);
 }
 
 cudaError_t bwd_read_and_clear_status(unsigned* value, bool clear) {

@@ -132,7 +132,15 @@ size_t bwd_smem_bytes(int C, int dk, bool per_channel);
 // The chunk the backward takes when the caller leaves it open (0 if none fits one CTA's shared memory).
 int bwd_auto_chunk(int dk, bool per_channel);
 size_t bwd_workspace_bytes(const BwdArgs& a);
+// byte offset in the workspace of the activated log alpha and beta
+size_t bwd_act_offset(const BwdArgs& a);
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t s);
 cudaError_t bwd_read_and_clear_status(unsigned* value, bool clear);
+// The gate / beta activations around the backward: log alpha and beta from raw logits (into g_out, beta_out), and
+// afterwards the chain rule (dg, dbeta in place; per-head dA_log, ddt from the gradient of log alpha).
+cudaError_t launch_bwd_act_apply(const float* x, const float* b, const GateAct& act, float* g_out, float* beta_out,
+                                 long n, int H, cudaStream_t s);
+cudaError_t launch_bwd_act_post(const float* x, const float* b, const float* g_act, const GateAct& act, float* dg,
+                                float* dbeta, float* dA_log, float* ddt, long rows, int H, cudaStream_t s);
 
 }  // namespace gdn

@@ -382,11 +382,37 @@ gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const vo
                          gdn_dtype do_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * gdn_chunk_bwd_workspace_size -- bytes of the gdn_chunk_bwd workspace: one
- * fp32 [d_k, d_v] state per (chunk slot, head), with B * (ceil(T / C) + 1)
- * slots for a batch and floor(T / C) + 2 n_seqs for packed sequences (C the
- * chunk the call takes; chunk_size 0 as in gdn_chunk_bwd).  n_seqs is 0 for a
- * call without cu_seqlens.
+ * gdn_chunk_bwd_act -- gdn_chunk_bwd with the gate and beta activations of
+ * gdn_gate_act in the path (act may be NULL: plain gdn_chunk_bwd).  g and beta
+ * then hold raw logits, as for gdn_chunk_fwd_act; the forward's activations are
+ * log alpha = -exp(A_log) softplus(g + dt_bias) ("Gated Delta Network (GDN)",
+ * §3.1 eq. 5) and beta = sigmoid or 2 sigmoid of the logit.  grad_g and
+ * grad_beta receive the gradients of those raw logits, and
+ *   grad_A_log    [H] fp32 device, required when A_log is given: sum over every
+ *                 token of the gradient of log alpha times log alpha;
+ *   grad_dt_bias  [H] fp32 device or NULL (needs dt_bias): sum over every
+ *                 token of grad_g.
+ * The per-head sums are reduced in a fixed order (run-to-run identical).  The
+ * gate activation applies to the scalar gate only (GDN_ERR_UNSUPPORTED with
+ * per_channel); the beta activation to both.
+ */
+gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float scale, const float* initial_state, const void* grad_o,
+                             const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
+                             float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
+                             float* grad_A_log, float* grad_dt_bias, int B, int T, int H, int d_k, int d_v,
+                             int chunk_size, gdn_dtype dtype, gdn_dtype do_dtype, const gdn_gate_act* act,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_chunk_bwd_workspace_size -- bytes of the gdn_chunk_bwd (and
+ * gdn_chunk_bwd_act) workspace.  Per (chunk slot, head): the entry state and
+ * the exit-state gradient (fp32 [d_k, d_v] each), Delta, Y and Z (fp32
+ * [C, d_v] each) and a record of the chunk's state-independent products; then
+ * room for the activated log alpha and beta (fp32 [B, T, H] each).  A batch
+ * has B * (ceil(T / C) + 1) slots, packed sequences floor(T / C) + 2 n_seqs
+ * (C the chunk the call takes; chunk_size 0 as in gdn_chunk_bwd).  n_seqs is 0
+ * for a call without cu_seqlens.
  */
 gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
                                         int n_seqs, size_t* bytes);

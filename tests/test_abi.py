@@ -216,8 +216,9 @@ def test_backward_argument_checks(lib, kw, status):
 
 def test_backward_workspace_sizes(lib):
     # per (chunk slot, head): the entry state and the gradient of h_out (fp32 [d_k, d_v] each); Delta, Y and Z
-    # (fp32 [C, d_v] each); a per-chunk record of the state-independent products.  So the size is affine in the
-    # number of slots and above the states and tiles alone.  The default chunk is 16.
+    # (fp32 [C, d_v] each); a per-chunk record of the state-independent products; then room for the activated gate
+    # and beta ([B, T, H] each).  So the size is affine in the number of slots and above the states and tiles alone.
+    # The default chunk is 16.
     def floor_bytes(slots, H, dk, dv, C):
         return slots * H * (2 * dk * dv + 3 * C * dv) * 4
     size = lambda *a: _binding.bwd_workspace_size(*a)
@@ -229,7 +230,9 @@ def test_backward_workspace_sizes(lib):
     assert s32 > floor_bytes(4 * 129, 16, 128, 128, 32)
     sv = size(True, 1, 65536, 32, 128, 128, 0, 8)        # packed: floor(T / C) + 2 n_seqs slots
     assert sv > floor_bytes(65536 // 16 + 16, 32, 128, 128, 16)
-    assert size(True, 1, 65536, 32, 128, 128, 0, 16) - sv == 16 * (sv // (65536 // 16 + 16))
+    # affine in the packed slot count floor(T / C) + 2 n_seqs (plus the fixed room for the activated gate and beta)
+    s16, s24 = size(True, 1, 65536, 32, 128, 128, 0, 16), size(True, 1, 65536, 32, 128, 128, 0, 24)
+    assert s24 - s16 == s16 - sv > 0
     assert size(False, 2, 0, 3, 64, 32) > 0
     # d_k = 256 with the per-channel gate: chunk 32 does not fit one CTA
     assert size(True, 1, 100, 2, 256, 128) == size(True, 1, 100, 2, 256, 128, 16)
@@ -240,3 +243,19 @@ def test_backward_workspace_sizes(lib):
 def test_test_injection_argument_checks(lib):
     assert lib.gdn_test_inject(7) == 1
     assert lib.gdn_test_inject(0) == 0
+
+
+def test_backward_activation_argument_checks(lib):
+    import ctypes as ct
+
+    def call(act, gA=FAKE, gdt=None, pc=0):
+        return lib.gdn_chunk_bwd_act(pc, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, FAKE, None, None, 0, FAKE, FAKE,
+                                     FAKE, FAKE, FAKE, None, gA, gdt, 1, 64, 1, 64, 64, 0, 1, 1, act, FAKE, 16, None)
+    act = _binding.GateAct(FAKE, None, 0)
+    assert call(ct.byref(act), gA=None) == 1                      # A_log needs grad_A_log
+    assert call(ct.byref(act), gdt=FAKE) == 1                     # grad_dt_bias needs dt_bias
+    assert call(ct.byref(act), pc=1) == 2                         # the gate activation is scalar-gate only
+    bad = _binding.GateAct(None, None, 3)
+    assert call(ct.byref(bad)) == 1                               # beta_sigmoid 0..2
+    ok = _binding.GateAct(FAKE, FAKE, 1)
+    assert call(ct.byref(ok), gdt=FAKE) == 1                      # all valid but the 16-byte workspace: no launch

@@ -190,3 +190,42 @@ def test_a_walk_wait_that_runs_out_is_reported_and_the_context_stays_usable():
     assert gdn.device_status() == 0
     _compare(_gpu(x), _oracle(x), torch.bfloat16, "after the timeout")
     assert gdn.device_status() == 0
+
+
+@pytest.mark.parametrize("kind,mult", [("gdn", 1), ("gdn", 2), ("kda", 1), ("kda", 2)])
+def test_activations_in_the_path(kind, mult):
+    # g and beta as raw logits: log alpha = -exp(A_log) softplus(g + dt_bias) (scalar gate), beta = mult sigmoid(b);
+    # the oracle composes its activation, its backward and the activation's chain rule
+    x = _problem(kind, "bf16", 2, 100, 2, 64, 64, h0_std=0.02)
+    rng = np.random.default_rng(21)
+    B, T, H = x["beta"].shape
+    b_raw = rng.standard_normal((B, T, H)).astype(np.float32)
+    kw = dict(beta_sigmoid=True, allow_neg_eigval=mult == 2)
+    if kind == "gdn":
+        g_raw = rng.standard_normal((B, T, H)).astype(np.float32)
+        A_log = np.log(rng.uniform(0.5, 16.0, H)).astype(np.float32)
+        dt = rng.normal(0.0, 0.1, H).astype(np.float32)
+        g64 = oracle.gate_activation(g_raw, A_log, dt)
+        kw.update(A_log=torch.from_numpy(A_log).cuda(), dt_bias=torch.from_numpy(dt).cuda())
+    else:
+        g_raw, A_log, dt = x["g"].numpy(), None, None
+        g64 = g_raw
+    y = dict(x)
+    y["g"], y["beta"] = g64, oracle.beta_activation(b_raw, mult)
+    ref = _oracle(y)
+    ch = oracle.activation_backward(g_raw, b_raw, A_log, dt, mult, ref["dg"], ref["dbeta"])
+    d = to_dev(x)
+    out = gdn.chunk_bwd(kind == "kda", d["q"], d["k"], d["v"], torch.from_numpy(g_raw).cuda(),
+                        torch.from_numpy(b_raw).cuda(), d["d_o"], scale=x["scale"], initial_state=d["initial_state"],
+                        d_final_state=d["d_final_state"], **kw)
+    torch.cuda.synchronize()
+    got = [None if t is None else t.double().cpu().numpy() for t in out]
+    for n, i in (("dq", 0), ("dk", 1), ("dv", 2), ("dh0", 5)):
+        assert_close(got[i], ref[n], torch.bfloat16, f"{kind} act {n}")
+    assert_close(got[3], ch["dx"], torch.bfloat16, f"{kind} act d(gate logit)")
+    assert_close(got[4], ch["db"], torch.bfloat16, f"{kind} act d(beta logit)")
+    if kind == "gdn":
+        assert_close(got[6], ch["dA_log"], torch.float32, "dA_log")
+        assert_close(got[7], ch["ddt_bias"], torch.float32, "ddt_bias")
+    else:
+        assert got[6] is None and got[7] is None
