@@ -73,6 +73,11 @@ def _declare(lib):
     lib.gdn_chunk_bwd_act.restype = i
     lib.gdn_chunk_bwd_act.argtypes = [i, vp, vp, vp, vp, vp, fp, vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp,
                                       i, i, i, i, i, i, i, i, ctypes.POINTER(GateAct), vp, ctypes.c_size_t, vp]
+    lib.gdn_chunk_bwd_ex.restype = i
+    lib.gdn_chunk_bwd_ex.argtypes = [i, vp, vp, vp, vp, vp, fp, vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     i, i, i, i, i, i, i, i, i, ctypes.POINTER(GateAct), vp, ctypes.c_size_t, vp]
+    lib.gdn_chunk_bwd_workspace_size_ex.restype = i
+    lib.gdn_chunk_bwd_workspace_size_ex.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.gdn_chunk_bwd_workspace_size.restype = i
     lib.gdn_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.gdn_test_inject.restype = i
@@ -270,11 +275,11 @@ def chunk_fwd_noalloc(per_channel: bool, q, k, v, g, beta, scale=None, initial_s
 
 
 def bwd_workspace_size(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chunk_size: int = 0,
-                       n_seqs: int = 0) -> int:
-    """Device workspace bytes of a chunk-backward call (C ABI gdn_chunk_bwd_workspace_size)."""
+                       n_seqs: int = 0, Hk: int = 0) -> int:
+    """Device workspace bytes of a chunk-backward call (C ABI gdn_chunk_bwd_workspace_size_ex; Hk key heads, 0: H)."""
     out = ctypes.c_size_t(0)
-    _check(load().gdn_chunk_bwd_workspace_size(int(per_channel), B, T, H, dk, dv, int(chunk_size), int(n_seqs),
-                                               ctypes.byref(out)))
+    _check(load().gdn_chunk_bwd_workspace_size_ex(int(per_channel), B, T, int(Hk), H, dk, dv, int(chunk_size),
+                                                  int(n_seqs), ctypes.byref(out)))
     return int(out.value)
 
 
@@ -297,9 +302,10 @@ def chunk_bwd(per_channel: bool, q, k, v, g, beta, d_o, scale=None, initial_stat
         _need(t, name, dt, dev)
     if d_o.dtype not in DTYPES:
         raise ValueError(f"d_o must be float32 or bfloat16 (got {d_o.dtype})")
-    B, T, H, dk = q.shape
+    B, T, Hk, dk = q.shape
+    H = v.shape[2]            # value heads (a multiple of the key heads of q and k)
     dv = v.shape[-1]
-    if k.shape != q.shape or v.shape[:3] != (B, T, H) or d_o.shape != v.shape:
+    if k.shape != q.shape or v.shape[:2] != (B, T) or H % Hk != 0 or d_o.shape != v.shape:
         raise ValueError("q, k, v, d_o shapes do not match")
     if g.shape != ((B, T, H, dk) if per_channel else (B, T, H)) or beta.shape != (B, T, H):
         raise ValueError("g / beta shapes do not match")
@@ -320,7 +326,7 @@ def chunk_bwd(per_channel: bool, q, k, v, g, beta, d_o, scale=None, initial_stat
     dg, dbeta = torch.empty(g.shape, **f32), torch.empty(beta.shape, **f32)
     dh0 = torch.empty((N, H, dk, dv), **f32) if want_d_initial_state else None
     if workspace is None:
-        need = bwd_workspace_size(per_channel, B, T, H, dk, dv, chunk_size, n_seqs)
+        need = bwd_workspace_size(per_channel, B, T, H, dk, dv, chunk_size, n_seqs, Hk)
         if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if workspace is not None:
@@ -328,12 +334,12 @@ def chunk_bwd(per_channel: bool, q, k, v, g, beta, d_o, scale=None, initial_stat
     act = _gate_act(dev, H, A_log, dt_bias, beta_sigmoid, allow_neg_eigval)
     dA = torch.empty(H, **f32) if A_log is not None else None
     ddt = torch.empty(H, **f32) if dt_bias is not None else None
-    _check(lib.gdn_chunk_bwd_act(int(per_channel), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
-                                 _ptr(initial_state), _ptr(d_o), _ptr(d_final_state), _ptr(cu_seqlens), n_seqs,
-                                 _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(dA),
-                                 _ptr(ddt), B, T, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[d_o.dtype],
-                                 None if act is None else ctypes.byref(act), _ptr(workspace),
-                                 0 if workspace is None else workspace.numel(), _stream_handle(stream, dev)))
+    _check(lib.gdn_chunk_bwd_ex(int(per_channel), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                _ptr(initial_state), _ptr(d_o), _ptr(d_final_state), _ptr(cu_seqlens), n_seqs,
+                                _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(dA),
+                                _ptr(ddt), B, T, Hk, H, dk, dv, int(chunk_size), DTYPES[q.dtype], DTYPES[d_o.dtype],
+                                None if act is None else ctypes.byref(act), _ptr(workspace),
+                                0 if workspace is None else workspace.numel(), _stream_handle(stream, dev)))
     if act is None:
         return dq, dkk, dvv, dg, dbeta, dh0
     return dq, dkk, dvv, dg, dbeta, dh0, dA, ddt

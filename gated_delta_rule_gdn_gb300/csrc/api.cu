@@ -418,20 +418,24 @@ gdn_status gdn_chunk_workspace_size(int per_channel, int B, int T, int H, int d_
     return ok();
 }
 
-gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, const void* v, const float* g,
-                             const float* beta, float scale, const float* initial_state, const void* grad_o,
-                             const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
-                             float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
-                             float* grad_A_log, float* grad_dt_bias, int B, int T, int H, int d_k, int d_v,
-                             int chunk_size, gdn_dtype dtype, gdn_dtype do_dtype, const gdn_gate_act* act,
-                             void* workspace, size_t workspace_bytes, void* stream) {
-    const char* fn = act ? "gdn_chunk_bwd_act" : "gdn_chunk_bwd";
+gdn_status gdn_chunk_bwd_ex(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float scale, const float* initial_state, const void* grad_o,
+                            const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
+                            float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
+                            float* grad_A_log, float* grad_dt_bias, int B, int T, int H_k, int H, int d_k, int d_v,
+                            int chunk_size, gdn_dtype dtype, gdn_dtype do_dtype, const gdn_gate_act* act,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "gdn_chunk_bwd";
     gdn::BwdArgs a{q, k, v, g, beta, scale, initial_state, grad_o, grad_final_state, cu_seqlens, n_seqs,
                    grad_q, grad_k, grad_v, grad_g, grad_beta, grad_initial_state, nullptr,
                    B, T, H, d_k, d_v, chunk_size, dtype == GDN_BF16 ? 1 : 0, do_dtype == GDN_BF16 ? 1 : 0,
-                   per_channel ? 1 : 0, 0};
+                   per_channel ? 1 : 0, 0, 0, nullptr, nullptr};
     gdn_status st = check_bwd(a, dtype, do_dtype, fn);
     if (st != GDN_OK) return st;
+    if (H_k < 0 || (H_k > 0 && H % H_k != 0))
+        return fail(GDN_ERR_INVALID_ARG, "%s: the value heads (%d) must be a multiple of the key heads (%d)", fn, H,
+                    H_k);
+    a.Hk = H_k;
     gdn::GateAct ga{nullptr, nullptr, 0};
     st = set_act(ga, act, fn);
     if (st != GDN_OK) return st;
@@ -468,6 +472,10 @@ gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, cons
     }
     a.ck = static_cast<float*>(ws);
     a.test_skip_record = gdn::take_test_injection() == GDN_TEST_BWD_RECORD_STALL ? 1 : 0;
+    if (a.HK() < a.H) {
+        a.gq_part = reinterpret_cast<float*>(static_cast<char*>(ws) + gdn::bwd_part_offset(a));
+        a.gk_part = a.gq_part + (size_t)a.B * a.T * a.H * a.dk;
+    }
     const long n_tok = (long)a.B * a.T * a.H;
     float* g_act = reinterpret_cast<float*>(static_cast<char*>(ws) + gdn::bwd_act_offset(a));
     float* beta_act = g_act + n_tok;
@@ -477,6 +485,7 @@ gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, cons
         if (ga.beta_sigmoid) a.beta = beta_act;
     }
     if (e == cudaSuccess) e = gdn::launch_chunk_bwd(a, s);
+    if (e == cudaSuccess) e = gdn::launch_bwd_group_sum(a, s);
     if (e == cudaSuccess && ga.any())
         e = gdn::launch_bwd_act_post(g, beta, g_act, ga, grad_g, grad_beta, grad_A_log, grad_dt_bias,
                                      (long)a.B * a.T, H, s);
@@ -488,31 +497,53 @@ gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, cons
     return ok();
 }
 
+gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float scale, const float* initial_state, const void* grad_o,
+                             const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
+                             float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
+                             float* grad_A_log, float* grad_dt_bias, int B, int T, int H, int d_k, int d_v,
+                             int chunk_size, gdn_dtype dtype, gdn_dtype do_dtype, const gdn_gate_act* act,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    return gdn_chunk_bwd_ex(per_channel, q, k, v, g, beta, scale, initial_state, grad_o, grad_final_state,
+                            cu_seqlens, n_seqs, grad_q, grad_k, grad_v, grad_g, grad_beta, grad_initial_state,
+                            grad_A_log, grad_dt_bias, B, T, 0, H, d_k, d_v, chunk_size, dtype, do_dtype, act,
+                            workspace, workspace_bytes, stream);
+}
+
 gdn_status gdn_chunk_bwd(int per_channel, const void* q, const void* k, const void* v, const float* g,
                          const float* beta, float scale, const float* initial_state, const void* grad_o,
                          const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
                          float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
                          int B, int T, int H, int d_k, int d_v, int chunk_size, gdn_dtype dtype,
                          gdn_dtype do_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-    return gdn_chunk_bwd_act(per_channel, q, k, v, g, beta, scale, initial_state, grad_o, grad_final_state,
-                             cu_seqlens, n_seqs, grad_q, grad_k, grad_v, grad_g, grad_beta, grad_initial_state,
-                             nullptr, nullptr, B, T, H, d_k, d_v, chunk_size, dtype, do_dtype, nullptr, workspace,
-                             workspace_bytes, stream);
+    return gdn_chunk_bwd_ex(per_channel, q, k, v, g, beta, scale, initial_state, grad_o, grad_final_state,
+                            cu_seqlens, n_seqs, grad_q, grad_k, grad_v, grad_g, grad_beta, grad_initial_state,
+                            nullptr, nullptr, B, T, 0, H, d_k, d_v, chunk_size, dtype, do_dtype, nullptr, workspace,
+                            workspace_bytes, stream);
 }
 
-gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
-                                        int n_seqs, size_t* bytes) {
+gdn_status gdn_chunk_bwd_workspace_size_ex(int per_channel, int B, int T, int H_k, int H, int d_k, int d_v,
+                                           int chunk_size, int n_seqs, size_t* bytes) {
     const char* fn = "gdn_chunk_bwd_workspace_size";
     if (!bytes) return fail(GDN_ERR_INVALID_ARG, "%s: bytes is NULL", fn);
     if (n_seqs < 0) return fail(GDN_ERR_INVALID_ARG, "%s: n_seqs must be >= 0 (got %d)", fn, n_seqs);
     const int32_t* cu = n_seqs > 0 ? reinterpret_cast<const int32_t*>(uintptr_t(1) << 20) : nullptr;
     gdn::BwdArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, 1.0f, nullptr, nullptr, nullptr, cu, n_seqs,
                    nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                   B, T, H, d_k, d_v, chunk_size, 0, 0, per_channel ? 1 : 0, 0};
+                   B, T, H, d_k, d_v, chunk_size, 0, 0, per_channel ? 1 : 0, 0, 0, nullptr, nullptr};
     gdn_status st = check_bwd(a, GDN_F32, GDN_F32, fn);
     if (st != GDN_OK) return st;
+    if (H_k < 0 || (H_k > 0 && H % H_k != 0))
+        return fail(GDN_ERR_INVALID_ARG, "%s: the value heads (%d) must be a multiple of the key heads (%d)", fn, H,
+                    H_k);
+    a.Hk = H_k;
     *bytes = gdn::bwd_workspace_bytes(a);
     return ok();
+}
+
+gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
+                                        int n_seqs, size_t* bytes) {
+    return gdn_chunk_bwd_workspace_size_ex(per_channel, B, T, 0, H, d_k, d_v, chunk_size, n_seqs, bytes);
 }
 
 gdn_status gdn_test_inject(int what) {

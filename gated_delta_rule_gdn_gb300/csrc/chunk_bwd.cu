@@ -178,19 +178,20 @@ __host__ __device__ inline Ws carve_ws(float* base, long slots, int H, int C, in
 
 // Load the chunk's K (and Q) rows, zero beyond d_k up to `width`, and rows >= L zero (beta = 0, g = 0 there,
 // which leaves the state unchanged); the gate rows (stride lg) and beta.
+// q and k are read at the key head: qk0 is the (token, key head) index of row 0, rows Hk apart.
 template <typename Tin, bool PERCH, bool WITH_Q>
-__device__ __forceinline__ void load_qk(const BwdArgs& a, size_t tok0, int L, int width, int ldk, int lg,
+__device__ __forceinline__ void load_qk(const BwdArgs& a, size_t tok0, size_t qk0, int L, int width, int ldk, int lg,
                                         float* Qs, float* Ks, float* Gs, float* Bs) {
-    const int C = a.C, dk = a.dk, H = a.H;
+    const int C = a.C, dk = a.dk, H = a.H, Hk = a.HK();
     const Tin* q = static_cast<const Tin*>(a.q);
     const Tin* k = static_cast<const Tin*>(a.k);
     for (int idx = threadIdx.x; idx < C * width; idx += kThreads) {
         const int r = idx / width, c = idx % width;
         float kv = 0.f, qv = 0.f, gv = 0.f;
         if (r < L && c < dk) {
-            const size_t tok = tok0 + (size_t)r * H;
-            kv = ld_f32<Tin>(k, tok * dk + c);
-            if (WITH_Q) qv = ld_f32<Tin>(q, tok * dk + c);
+            const size_t tok = tok0 + (size_t)r * H, qt = qk0 + (size_t)r * Hk;
+            kv = ld_f32<Tin>(k, qt * dk + c);
+            if (WITH_Q) qv = ld_f32<Tin>(q, qt * dk + c);
             if (PERCH) gv = a.g[tok * dk + c];
         }
         Ks[r * ldk + c] = kv;
@@ -326,7 +327,8 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const BwdArgs a, Ws 
     const int L = (int)min((long)CC, geo.len - ci * CC);
     const size_t tok0 = ((size_t)geo.b * a.T + geo.bos + ci * CC) * H + hh;
     const float scale = a.scale;
-    load_qk<Tin, PERCH, true>(a, tok0, L, W, ldk, lg, Qs, Ks, Gs, R + rc.B);
+    const size_t qk0 = ((size_t)geo.b * a.T + geo.bos + ci * CC) * a.HK() + hh / (H / a.HK());
+    load_qk<Tin, PERCH, true>(a, tok0, qk0, L, W, ldk, lg, Qs, Ks, Gs, R + rc.B);
     __syncthreads();
     gate_prefix(Gs, CC, PERCH ? dk : 1, lg);
     __syncthreads();
@@ -872,6 +874,8 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
     const long cs = ci * CC;
     const int L = (int)min((long)CC, geo.len - cs);
     const size_t tok0 = ((size_t)geo.b * a.T + geo.bos + cs) * H + hh;
+    const int Hk = a.HK();
+    const size_t qk0 = ((size_t)geo.b * a.T + geo.bos + cs) * Hk + hh / (H / Hk);
     const float scale = a.scale;
     const size_t sbase = ((size_t)slot * H + hh) * dk * dv, cbase = ((size_t)slot * H + hh) * CC * dv;
     const bool vec = (dv & 3) == 0;   // 16-byte copies need every row start on 16 bytes
@@ -1064,7 +1068,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
         for (int idx = tid; idx < CC * dkp; idx += kThreads) {
             const int r = idx / dkp, c = idx % dkp;
             const bool in = r < L && c < dk;
-            const size_t off = (tok0 + (size_t)r * H) * dk + c;
+            const size_t off = (qk0 + (size_t)r * Hk) * dk + c;
             Qs[r * ldk + c] = in ? ld_f32<Tin>(q, off) : 0.f;
             Ks[r * ldk + c] = in ? ld_f32<Tin>(k, off) : 0.f;
         }
@@ -1123,9 +1127,10 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
         const float dg0 = scale * dPm[r * (CC + 1) + r];
         const float xo = XO[idx], hy = HY[idx], dd = DD[idx];
         const float read = scale * E * xo;
-        const size_t off = (tok0 + (size_t)r * H) * dk + c;
-        a.gq[off] = read + sq + dg0 * kr;
-        a.gk[off] = -br * E * hy + F * dd + skp + dg0 * qr + sar + sac;
+        // grouped value heads: this value head's part, summed per key head afterwards
+        const size_t off = a.gq_part ? (tok0 + (size_t)r * H) * dk + c : (qk0 + (size_t)r * Hk) * dk + c;
+        (a.gq_part ? a.gq_part : a.gq)[off] = read + sq + dg0 * kr;
+        (a.gk_part ? a.gk_part : a.gk)[off] = -br * E * hy + F * dd + skp + dg0 * qr + sar + sac;
         XO[idx] = qr * (read + sq) - kr * (br * E * hy + skp - sar + sac);   // pb
         HY[idx] = F * kr * dd;                                              // pw
     }
@@ -1311,7 +1316,29 @@ __global__ void bwd_act_chain_kernel(const float* x, const float* b, const GateA
     }
 }
 
+// Grouped value heads: dq, dk of key head hk = the sum of its value heads hk G .. hk G + G - 1, in that order.
+__global__ void bwd_group_sum_kernel(const float* part, float* out, long n_out, int Hk, int G, int dk) {
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n_out; i += (long)gridDim.x * blockDim.x) {
+        const long c = i % dk, th = i / dk, t = th / Hk;
+        const int hk = (int)(th % Hk);
+        const float* p = part + ((t * Hk * G) + (long)hk * G) * dk + c;
+        float s = 0.f;
+        for (int u = 0; u < G; ++u) s += p[(long)u * dk];
+        out[i] = s;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_group_sum(const BwdArgs& a, cudaStream_t s) {
+    const int Hk = a.HK(), G = a.H / Hk;
+    const long n_out = (long)a.B * a.T * Hk * a.dk;
+    if (n_out == 0 || !a.gq_part) return cudaSuccess;
+    const unsigned blocks = (unsigned)min((n_out + kThreads - 1) / kThreads, 152L * 16);
+    bwd_group_sum_kernel<<<blocks, kThreads, 0, s>>>(a.gq_part, a.gq, n_out, Hk, G, a.dk);
+    bwd_group_sum_kernel<<<blocks, kThreads, 0, s>>>(a.gk_part, a.gk, n_out, Hk, G, a.dk);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_act_apply(const float* x, const float* b, const GateAct& act, float* g_out, float* beta_out,
                                  long n, int H, cudaStream_t s) {
@@ -1354,9 +1381,16 @@ size_t bwd_act_offset(const BwdArgs& a) {
     return (ws_floats(slots, a.H, a.C, a.dk, a.dv, a.per_channel != 0) * sizeof(float) + 255) & ~(size_t)255;
 }
 
-// the walks' workspace, then room for the activated log alpha and beta ([B, T, H] fp32 each)
+// byte offset of the per-value-head dq, dk parts (grouped value heads only)
+size_t bwd_part_offset(const BwdArgs& a) {
+    return (bwd_act_offset(a) + (size_t)2 * a.B * a.T * a.H * sizeof(float) + 255) & ~(size_t)255;
+}
+
+// the walks' workspace, then room for the activated log alpha and beta ([B, T, H] fp32 each) and, with grouped
+// value heads, the per-value-head dq and dk ([B, T, H, dk] fp32 each)
 size_t bwd_workspace_bytes(const BwdArgs& a) {
-    return bwd_act_offset(a) + (size_t)2 * a.B * a.T * a.H * sizeof(float);
+    const size_t parts = a.HK() < a.H ? (size_t)2 * a.B * a.T * a.H * a.dk * sizeof(float) : 0;
+    return bwd_part_offset(a) + parts;
 }
 
 cudaError_t bwd_read_and_clear_status(unsigned* value, bool clear) {

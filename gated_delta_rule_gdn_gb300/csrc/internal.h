@@ -121,7 +121,11 @@ struct BwdArgs {
     int do_bf16;            // dO dtype
     int per_channel;
     int test_skip_record;   // test of the bounded waits: the walks leave out the copy of their first chunk record
+    int Hk;                 // key heads of q and k (0: H); value head h reads key head h / (H / Hk)
+    float* gq_part;         // with Hk < H: per-value-head dq, dk ([B, T, H, dk]), summed per key head afterwards
+    float* gk_part;
     int N() const { return cu ? n_seqs : B; }
+    __host__ __device__ int HK() const { return Hk > 0 ? Hk : H; }
 };
 
 // One-shot test injection armed by gdn_test_inject (api.cu), consumed by the calling thread's next backward call.
@@ -132,8 +136,11 @@ size_t bwd_smem_bytes(int C, int dk, bool per_channel);
 // The chunk the backward takes when the caller leaves it open (0 if none fits one CTA's shared memory).
 int bwd_auto_chunk(int dk, bool per_channel);
 size_t bwd_workspace_bytes(const BwdArgs& a);
-// byte offset in the workspace of the activated log alpha and beta
+// byte offsets in the workspace of the activated log alpha and beta, and of the per-value-head dq, dk parts
 size_t bwd_act_offset(const BwdArgs& a);
+size_t bwd_part_offset(const BwdArgs& a);
+// grouped value heads: dq, dk summed per key head from the parts
+cudaError_t launch_bwd_group_sum(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t s);
 cudaError_t bwd_read_and_clear_status(unsigned* value, bool clear);
 // The gate / beta activations around the backward: log alpha and beta from raw logits (into g_out, beta_out), and

@@ -405,6 +405,23 @@ gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, cons
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_chunk_bwd_ex -- the general backward: gdn_chunk_bwd_act plus grouped
+ * value heads, as gdn_chunk_fwd_ex.  q, k and grad_q, grad_k are
+ * [B, T, H_k, d_k]; v, g, beta, the states and their gradients have H_v value
+ * heads (a multiple of H_k; H_k = 0 means H_v).  Value head h reads key head
+ * h / (H_v / H_k), so grad_q and grad_k of a key head sum its value heads'
+ * parts (in head order, run-to-run identical).  The workspace then also holds
+ * those parts (gdn_chunk_bwd_workspace_size_ex).
+ */
+gdn_status gdn_chunk_bwd_ex(int per_channel, const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float scale, const float* initial_state, const void* grad_o,
+                            const float* grad_final_state, const int32_t* cu_seqlens, int n_seqs, float* grad_q,
+                            float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_initial_state,
+                            float* grad_A_log, float* grad_dt_bias, int B, int T, int H_k, int H_v, int d_k, int d_v,
+                            int chunk_size, gdn_dtype dtype, gdn_dtype do_dtype, const gdn_gate_act* act,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gdn_chunk_bwd_workspace_size -- bytes of the gdn_chunk_bwd (and
  * gdn_chunk_bwd_act) workspace.  Per (chunk slot, head): the entry state and
  * the exit-state gradient (fp32 [d_k, d_v] each), Delta, Y and Z (fp32
@@ -412,8 +429,12 @@ gdn_status gdn_chunk_bwd_act(int per_channel, const void* q, const void* k, cons
  * room for the activated log alpha and beta (fp32 [B, T, H] each).  A batch
  * has B * (ceil(T / C) + 1) slots, packed sequences floor(T / C) + 2 n_seqs
  * (C the chunk the call takes; chunk_size 0 as in gdn_chunk_bwd).  n_seqs is 0
- * for a call without cu_seqlens.
+ * for a call without cu_seqlens.  The _ex form takes the key heads H_k too: with
+ * H_k < H_v the workspace adds the per-value-head grad_q and grad_k parts (fp32
+ * [B, T, H_v, d_k] each).
  */
+gdn_status gdn_chunk_bwd_workspace_size_ex(int per_channel, int B, int T, int H_k, int H_v, int d_k, int d_v,
+                                           int chunk_size, int n_seqs, size_t* bytes);
 gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
                                         int n_seqs, size_t* bytes);
 

@@ -229,3 +229,28 @@ def test_activations_in_the_path(kind, mult):
         assert_close(got[7], ch["ddt_bias"], torch.float32, "ddt_bias")
     else:
         assert got[6] is None and got[7] is None
+
+
+@pytest.mark.parametrize("kind,dtype", [("gdn", "f32"), ("kda", "f32"), ("gdn", "bf16")])
+def test_grouped_value_heads(kind, dtype):
+    # H_v = 3 H_k: value head h reads q, k of key head h // 3; the oracle runs on q, k repeated per value head and
+    # the gradient of a shared key head is the sum over its value heads
+    Hk, G = 2, 3
+    x = _problem(kind, dtype, 2, 70, Hk * G, 64, 48, h0_std=0.3 if dtype == "f32" else 0.02)
+    qk = {n: x[n][:, :, :Hk].contiguous() for n in ("q", "k")}
+    y = dict(x)
+    for n in ("q", "k"):
+        y[n] = qk[n].repeat_interleave(G, dim=2)
+    ref = _oracle(y)
+    d = to_dev(x)
+    out = gdn.chunk_bwd(kind == "kda", qk["q"].cuda(), qk["k"].cuda(), d["v"], d["g"], d["beta"], d["d_o"],
+                        scale=x["scale"], initial_state=d["initial_state"], d_final_state=d["d_final_state"])
+    torch.cuda.synchronize()
+    got = [t.double().cpu().numpy() for t in out]
+    B, T = x["q"].shape[:2]
+    tol = torch.float32 if dtype == "f32" else torch.bfloat16
+    assert got[0].shape == (B, T, Hk, 64)
+    assert_close(got[0], ref["dq"].reshape(B, T, Hk, G, 64).sum(3), tol, f"{kind} GVA dq")
+    assert_close(got[1], ref["dk"].reshape(B, T, Hk, G, 64).sum(3), tol, f"{kind} GVA dk")
+    for n, i in (("dv", 2), ("dg", 3), ("dbeta", 4), ("dh0", 5)):
+        assert_close(got[i], ref[n], tol, f"{kind} GVA {n}")
