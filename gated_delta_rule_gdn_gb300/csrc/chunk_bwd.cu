@@ -28,6 +28,9 @@
 //     copies (cp.async.bulk, two stages), so a step waits only on its own dependent chain.
 //   * bwd_grad_kernel, one CTA per (chunk, head), over all d_v tiles: every chunk is independent once the two
 //     walks are done, so this runs over the whole GPU.  It writes dQ, dK, dV, dbeta and dg.
+// Around them, when asked for: the gate / beta activations from raw logits before, and their chain rule after
+// (bwd_act_*); with grouped value heads, the sum of the per-value-head dQ, dK parts per key head
+// (bwd_group_sum_kernel).
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
