@@ -41,6 +41,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -99,12 +100,20 @@ def _traffic_kind(workload: str) -> str:
     return "decode" if workload.startswith("decode") or "_decode_" in workload else "chunk"
 
 
+def _code_only(src: str) -> str:
+    """A CUDA source with its comments and blank lines removed (what a comment edit leaves unchanged)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def sources_sha256(kind: str = "chunk") -> str:
-    """Hash of the kernel sources a recorded ncu traffic figure of this kind depends on."""
+    """Hash of the kernel sources a recorded ncu traffic figure of this kind depends on (code only: an edit of
+    the comments keeps the record)."""
     h = hashlib.sha256()
     for name in TRAFFIC_SOURCES[kind]:
-        with open(os.path.join(ROOT, "gated_delta_rule_gdn_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "gated_delta_rule_gdn_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

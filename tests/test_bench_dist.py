@@ -51,3 +51,15 @@ def test_max_over_ranks_barrier_and_rank0_only_reference():
     res = sorted(out.get(timeout=5) for _ in range(world))
     assert [g for _, g, _ in res] == [11.0, 11.0]
     assert [rc for _, _, rc in res] == [0, 0]
+
+
+def test_traffic_record_follows_the_code_not_the_comments():
+    # a recorded ncu traffic figure stays valid through an edit of the comments and goes stale with the code
+    sys.path.insert(0, ROOT)
+    import bench
+    src = "// header\n__global__ void k(float* p) {  /* note */\n    p[0] = 1.f;   // store\n}\n"
+    assert bench._code_only(src) == bench._code_only(src.replace("// store", "// the store, reworded\n//"))
+    assert bench._code_only(src) != bench._code_only(src.replace("1.f", "2.f"))
+    assert "header" not in bench._code_only(src) and "note" not in bench._code_only(src)
+    for kind in bench.TRAFFIC_SOURCES:
+        assert len(bench.sources_sha256(kind)) == 64
