@@ -148,6 +148,38 @@ def test_more_chains_than_sms(kind):
     assert_close(hT, h_ref, torch.bfloat16, "final state")
 
 
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_short_chains_in_a_deep_grid(kind):
+    """384 short chains (768 state CTAs, five waves on 152 SMs) and 3,072 per-chunk items."""
+    x = W.chunk_inputs(_workload(kind, "bf16", 128, 128, 64, 0.02), seed=11, B=8, T=256, H=48)
+    o_ref, h_ref = oracle_on_heads(x)
+    o, hT = _run(x, "two_pass")
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
+def test_packed_long_and_short_sequences_in_a_deep_grid():
+    """One long sequence among short and empty ones, 64 heads (several waves of state CTAs, longest first): parity,
+    the empty sequence keeps its initial state, and a sequence's outputs do not depend on another's inputs."""
+    lens = [1500, 64, 100, 37, 0, 300, 129]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    H = 64
+    x = W.chunk_inputs(_workload("gdn", "bf16", 128, 128, 64, 0.02), seed=12, B=1, T=int(cu[-1]), H=H)
+    x["cu_seqlens"] = torch.from_numpy(cu)
+    x["initial_state"] = torch.randn(len(lens), H, 128, 128, generator=torch.Generator().manual_seed(1)) * 0.02
+    o, hT = _run(x, "two_pass")
+    o_ref, h_ref = oracle_on_heads(x)
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+    assert np.array_equal(hT[4], x["initial_state"][4].double().numpy())
+    x2 = {**x, "v": x["v"].clone()}
+    x2["v"][:, cu[5]:cu[6]] += 1.0
+    o2, h2 = _run(x2, "two_pass")
+    keep = np.ones(int(cu[-1]), bool)
+    keep[cu[5]:cu[6]] = False
+    assert np.array_equal(o2[:, keep], o[:, keep]) and np.array_equal(np.delete(h2, 5, 0), np.delete(hT, 5, 0))
+
+
 def test_zero_length_input_keeps_initial_state():
     x = W.chunk_inputs(W.config(1), seed=3, B=2, T=0, H=2)
     for algo in _algos(x):
