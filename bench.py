@@ -340,7 +340,7 @@ def _bwd_flops(w, C: int) -> int:
     the state products h dO, h Y, dh Delta: 3 C d_k d_v; the four pair sums of dQ / dK: 2 C^2 d_k; the state
     gradient: 2 C d_k d_v).  Per-channel exponentials are not counted."""
     dk, dv = w.dk, w.dv
-    macs = 3 * C * C * dk + 9 * C * dk * dv + 5 * C * C * dv // 2
+    macs = 3 * C * C * dk + 8 * C * dk * dv + 5 * C * C * dv // 2
     N = w.n_seqs if w.n_seqs else w.B
     chunks = N * math.ceil(w.T / C) if not w.n_seqs else math.ceil(w.T / C) + N
     return 2 * macs * chunks * w.H
