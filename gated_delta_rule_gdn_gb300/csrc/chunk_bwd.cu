@@ -1,4 +1,5 @@
-// Chunkwise backward of the gated delta rule (scalar gate) and of KDA (per-key-channel gate), fp32 SIMT.
+// Chunkwise backward of the gated delta rule (scalar gate) and of KDA (per-key-channel gate): fp32 arithmetic,
+// FMAs and 3xTF32 warp MMAs (mma.sync m16n8k8, each operand split into a TF32 head and tail).
 //
 // The pages print the chunkwise backward of the ungated delta rule ("阅读笔记：DeltaNet 在 FLA 中的代码实现",
 // 二、反向传播, steps 1-6): recompute the chunk states, walk the chunks backwards carrying the state gradient,
@@ -10,7 +11,9 @@
 //   Z = V - (K*E) h,   R = diag(beta) Z,   Delta = (I + A)^{-1} R
 //   O = scale (Q*E) h + P Delta,          h_out = diag(E_L) h + (K*F)^T Delta
 // With dh the gradient of h_out (the state gradient carried from the later chunk) the adjoint is
-//   dDelta = P^T dO + (K*F) dh,   Y = (I + A)^{-T} dDelta   (= dR: one back substitution, no inverse)
+//   dDelta = P^T dO + (K*F) dh,   Y = (I + A)^{-T} dDelta   (= dR)
+// The walks take both triangular systems as products by T = (I + A)^{-1}, which the prep kernel forms once per
+// chunk by forward substitution (Delta = T R, Y = T^T dDelta).
 //   dV = diag(beta) Y,   dA = -Y Delta^T (strictly lower),   dP = dO Delta^T (lower)
 //   dh_in = diag(E_L) dh + scale (Q*E)^T dO - (K*E)^T diag(beta) Y
 // and dQ, dK, dbeta and the gradient of G collect the terms of every product above (bwd_grad_kernel lists them
@@ -19,7 +22,8 @@
 //
 // Four kernels, in three launches:
 //   * bwd_prep_kernel, one CTA per (chunk, head): everything of a chunk that does not depend on the state -- the
-//     cumulative gate, KK, P, scale Q*E, K*E, K*F, exp(G_L) and beta -- into a per-chunk record.
+//     cumulative gate, KK, P, scale Q*E, T = (I + A)^{-1}, K*E, K*F, exp(G_L) and beta -- into a per-chunk
+//     record.
 //   * bwd_walk_kernel, one CTA per (chain, 64-column d_v tile) and role.  The state recurrence is separable in
 //     d_v columns, so each tile walks alone.  The forward role runs the chunks in order and stores, per chunk,
 //     the entry state h, Delta and Z; the backward role runs them in reverse and stores, per chunk, the
@@ -133,7 +137,7 @@ __host__ __device__ inline long workspace_slots(int B, int T, int C, int n_seqs,
 //   EL [ldk or 4]   exp(G_L) per channel (scalar gate: repeated)      B [C]   beta
 //   G  [C][lg]   the within-chunk cumulative log gate
 struct Rec {
-    int KK, P, QE, KE, KF, EL, B, G, total;
+    int KK, P, QE, T, KE, KF, EL, B, G, total;
 };
 
 __host__ __device__ inline Rec rec_lay(int C, int dk, bool perch) {
@@ -143,6 +147,7 @@ __host__ __device__ inline Rec rec_lay(int C, int dk, bool perch) {
     r.KK = o; o = round4(o + cc);
     r.P = o; o = round4(o + cc);
     r.QE = o; o = round4(o + C * ldk);
+    r.T = o; o = round4(o + cc);
     r.KE = o; o = round4(o + C * ldk);
     r.KF = o; o = round4(o + C * ldk);
     r.EL = o; o = round4(o + (perch ? ldk : 4));
@@ -256,37 +261,6 @@ __device__ __forceinline__ void pair_products(const float* Qs, const float* Ks, 
     }
 }
 
-// (I + A) X = X0 in place, A = diag(beta) KK strictly lower: rows in order.  X is [rows][NCOL] with row stride
-// NCOL + 1.  LPC = 256 / NCOL lanes per column (8 for 32 columns, 4 for 64): every column in one sweep.
-template <int NCOL, int XS>
-__device__ __forceinline__ void solve_lower(const float* KK, const float* Bs, float* X, int C, int L) {
-    constexpr int LPC = kThreads / NCOL;
-    const int col = threadIdx.x / LPC, sub = threadIdx.x % LPC;
-    for (int r = 1; r < L; ++r) {
-        float acc = 0.f;
-        for (int j = sub; j < r; j += LPC) acc = fmaf(KK[r * (C + 1) + j], X[j * XS + col], acc);
-#pragma unroll
-        for (int o = 1; o < LPC; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (sub == 0) X[r * XS + col] -= Bs[r] * acc;
-        __syncwarp();
-    }
-}
-
-// (I + A)^T X = X0 in place: rows from the last valid one down.
-template <int NCOL, int XS>
-__device__ __forceinline__ void solve_upper_t(const float* KK, const float* Bs, float* X, int C, int L) {
-    constexpr int LPC = kThreads / NCOL;
-    const int col = threadIdx.x / LPC, sub = threadIdx.x % LPC;
-    for (int s = L - 2; s >= 0; --s) {
-        float acc = 0.f;
-        for (int r = s + 1 + sub; r < L; r += LPC) acc = fmaf(Bs[r] * KK[r * (C + 1) + s], X[r * XS + col], acc);
-#pragma unroll
-        for (int o = 1; o < LPC; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (sub == 0) X[s * XS + col] -= acc;
-        __syncwarp();
-    }
-}
-
 // ---- the chunk records ---------------------------------------------------------------------------------------
 
 // Find the chunk of workspace slot `slot`: returns false for slots that hold a final state (or none).
@@ -347,6 +321,25 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const BwdArgs a, Ws 
     }
     for (int c = threadIdx.x; c < (PERCH ? W : 4); c += kThreads)
         R[rc.EL + c] = expf(PERCH ? Gs[(L - 1) * lg + c] : Gs[L - 1]);
+    __syncthreads();
+    // T = (I + A)^{-1}, A = diag(beta) KK strictly lower: column c by forward substitution on the unit vector
+    // (thread c, the column in registers; its entries above row c are exact zeros, so the sums may start at row 0).
+    // Rows past the chunk's end have beta = 0, so T is the identity there.
+    if (threadIdx.x < CC) {
+        const int c = threadIdx.x;
+        const float* KK = R + rc.KK;
+        const float* Bv = R + rc.B;
+        float* Tm = R + rc.T;
+        float tc[CC];
+#pragma unroll
+        for (int r = 0; r < CC; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < r; ++q) acc = fmaf(KK[r * (CC + 1) + q], tc[q], acc);
+            tc[r] = r == c ? 1.f : (r > c ? -Bv[r] * acc : 0.f);
+            Tm[r * (CC + 1) + c] = tc[r];
+        }
+    }
     __syncthreads();
     float4* dst = reinterpret_cast<float4*>(ws.rec + ((size_t)slot * H + hh) * rc.total);
     const float4* src = reinterpret_cast<const float4*>(R);
@@ -449,15 +442,14 @@ __device__ __forceinline__ void walk_forward(const BwdArgs& a, const Ws& ws, flo
         fence_mbar_init();
     }
     __syncthreads();
-    // thread 0: chunk c's KK and KE .. B into stage c & 1
+    // thread 0: chunk c's T, KE .. B into stage c & 1
     auto issue = [&](long c) {
         float* st = smem + ((c & 1) ? ly.st1 : ly.st0);
         const float* src = recs + (size_t)c * rstride;
-        const uint32_t b1 = (uint32_t)(rc.P - rc.KK) * 4u, b2 = (uint32_t)(rc.G - rc.KE) * 4u;
-        mbar_arrive_expect_tx(&bars[c & 1], b1 + b2);
+        const uint32_t b = (uint32_t)(rc.G - rc.T) * 4u;
+        mbar_arrive_expect_tx(&bars[c & 1], b);
         if (a.test_skip_record && c == 0) return;   // test: these bytes never arrive, the wait for them runs out
-        bulk_g2s(st + rc.KK, src + rc.KK, b1, &bars[c & 1]);
-        bulk_g2s(st + rc.KE, src + rc.KE, b2, &bars[c & 1]);
+        bulk_g2s(st + rc.T, src + rc.T, b, &bars[c & 1]);
     };
     long issued = 0, waited = 0;
     if (tid == 0) {
@@ -521,7 +513,7 @@ __device__ __forceinline__ void walk_forward(const BwdArgs& a, const Ws& ws, flo
         waited = ci + 1;
         const float* KE = st + rc.KE;
         const float* KF = st + rc.KF;
-        const float* KK = st + rc.KK;
+        const float* Tm = st + rc.T;
         const float* EL = st + rc.EL;
         const float* Bs = st + rc.B;
         // Z = V - (K*E) h, then R = beta Z into Ds
@@ -551,8 +543,31 @@ __device__ __forceinline__ void walk_forward(const BwdArgs& a, const Ws& ws, flo
                     Ds[r * kWS + j] = Bs[r] * zz;
                 }
         }
-        __syncthreads();
-        solve_lower<kWB, kWS>(KK, Bs, Ds, CC, L);
+        __syncwarp();
+        // Delta = T R, T = (I + A)^{-1} from the record: each warp on its own 8 columns
+        {
+            float dl[MTC][4];
+#pragma unroll
+            for (int mc = 0; mc < MTC; ++mc)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dl[mc][i] = 0.f;
+#pragma unroll
+            for (int k0 = 0; k0 < CC; k0 += 8) {
+                uint32_t bh[2], bl[2];
+                frag_b(Ds, kWS, k0, 8 * warp, g, t4, 1.f, 1.f, bh, bl);
+#pragma unroll
+                for (int mc = 0; mc < MTC; ++mc) {
+                    uint32_t ah[4], al[4];
+                    frag_a(Tm, CC + 1, 16 * mc, k0, g, t4, ah, al);
+                    mma3_tf32(dl[mc], ah, al, bh, bl);
+                }
+            }
+            __syncwarp();   // every lane has read R
+#pragma unroll
+            for (int mc = 0; mc < MTC; ++mc)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Ds[(16 * mc + g + 8 * (i >> 1)) * kWS + jz + (i & 1)] = dl[mc][i];
+        }
         __syncthreads();
         // store Delta; h <- diag(E_L) h + (K*F)^T Delta
         for (int idx = tid; idx < L * kWB; idx += kThreads) {
@@ -629,10 +644,10 @@ __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, fl
     auto issue = [&](long k) {
         float* st = smem + ((k & 1) ? ly.st1 : ly.st0);
         const float* src = recs + (size_t)(n_chunks - 1 - k) * rstride;
-        const uint32_t b = (uint32_t)rc.G * 4u;
+        const uint32_t b = (uint32_t)(rc.G - rc.P) * 4u;
         mbar_arrive_expect_tx(&bars[k & 1], b);
         if (a.test_skip_record && k == 0) return;   // test: these bytes never arrive, the wait for them runs out
-        bulk_g2s(st, src, b, &bars[k & 1]);
+        bulk_g2s(st + rc.P, src + rc.P, b, &bars[k & 1]);
     };
     long issued = 0, waited = 0;
     if (tid == 0) {
@@ -688,7 +703,7 @@ __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, fl
             break;
         }
         waited = k + 1;
-        const float* KK = st + rc.KK;
+        const float* Tm = st + rc.T;
         const float* Pm = st + rc.P;
         const float* QE = st + rc.QE;
         const float* KE = st + rc.KE;
@@ -728,8 +743,31 @@ __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, fl
 #pragma unroll
                 for (int i = 0; i < 4; ++i) Ys[(16 * mc + g + 8 * (i >> 1)) * kWS + jz + (i & 1)] = z[mc][i];
         }
-        __syncthreads();
-        solve_upper_t<kWB, kWS>(KK, Bs, Ys, CC, L);
+        __syncwarp();
+        // Y = T^T dDelta (the solution of (I + A)^T Y = dDelta): each warp on its own 8 columns
+        {
+            float yl[MTC][4];
+#pragma unroll
+            for (int mc = 0; mc < MTC; ++mc)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) yl[mc][i] = 0.f;
+#pragma unroll
+            for (int k0 = 0; k0 < CC; k0 += 8) {
+                uint32_t bh[2], bl[2];
+                frag_b(Ys, kWS, k0, 8 * warp, g, t4, 1.f, 1.f, bh, bl);
+#pragma unroll
+                for (int mc = 0; mc < MTC; ++mc) {
+                    uint32_t ah[4], al[4];
+                    frag_at(Tm, CC + 1, 16 * mc, k0, g, t4, ah, al);
+                    mma3_tf32(yl[mc], ah, al, bh, bl);
+                }
+            }
+            __syncwarp();   // every lane has read dDelta
+#pragma unroll
+            for (int mc = 0; mc < MTC; ++mc)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Ys[(16 * mc + g + 8 * (i >> 1)) * kWS + jz + (i & 1)] = yl[mc][i];
+        }
         __syncthreads();
         for (int idx = tid; idx < L * kWB; idx += kThreads) {
             const int r = idx / kWB, j = idx % kWB;
@@ -1372,7 +1410,7 @@ size_t bwd_smem_bytes(int C, int dk, bool per_channel) {
     return w > g ? (w > p ? w : p) : (g > p ? g : p);
 }
 
-// Chunk 16: shorter solves and smaller per-chunk tiles; it measured faster than 32 on every workload timed.
+// Chunk 16: smaller per-chunk tiles and triangular products; it measured faster than 32 on every workload timed.
 int bwd_auto_chunk(int dk, bool per_channel) {
     for (int C : {16, 32})
         if (bwd_smem_bytes(C, dk, per_channel) <= kMaxSmemPerBlock) return C;

@@ -254,3 +254,37 @@ def test_grouped_value_heads(kind, dtype):
     assert_close(got[1], ref["dk"].reshape(B, T, Hk, G, 64).sum(3), tol, f"{kind} GVA dk")
     for n, i in (("dv", 2), ("dg", 3), ("dbeta", 4), ("dh0", 5)):
         assert_close(got[i], ref[n], tol, f"{kind} GVA {n}")
+
+
+def test_grouped_value_heads_with_activations():
+    # both at once: q, k of key head h // 2 serve value heads h; g and beta are raw logits activated in the path
+    Hk, G = 2, 2
+    x = _problem("gdn", "bf16", 2, 90, Hk * G, 64, 48, h0_std=0.02)
+    rng = np.random.default_rng(23)
+    B, T, H = x["beta"].shape
+    g_raw = rng.standard_normal((B, T, H)).astype(np.float32)
+    b_raw = rng.standard_normal((B, T, H)).astype(np.float32)
+    A_log = np.log(rng.uniform(0.5, 16.0, H)).astype(np.float32)
+    dt = rng.normal(0.0, 0.1, H).astype(np.float32)
+    qk = {n: x[n][:, :, :Hk].contiguous() for n in ("q", "k")}
+    y = dict(x)
+    for n in ("q", "k"):
+        y[n] = qk[n].repeat_interleave(G, dim=2)
+    y["g"], y["beta"] = oracle.gate_activation(g_raw, A_log, dt), oracle.beta_activation(b_raw, 1)
+    ref = _oracle(y)
+    ch = oracle.activation_backward(g_raw, b_raw, A_log, dt, 1, ref["dg"], ref["dbeta"])
+    d = to_dev(x)
+    out = gdn.chunk_bwd(False, qk["q"].cuda(), qk["k"].cuda(), d["v"], torch.from_numpy(g_raw).cuda(),
+                        torch.from_numpy(b_raw).cuda(), d["d_o"], scale=x["scale"], initial_state=d["initial_state"],
+                        d_final_state=d["d_final_state"], A_log=torch.from_numpy(A_log).cuda(),
+                        dt_bias=torch.from_numpy(dt).cuda(), beta_sigmoid=True)
+    torch.cuda.synchronize()
+    got = [t.double().cpu().numpy() for t in out]
+    assert_close(got[0], ref["dq"].reshape(B, T, Hk, G, 64).sum(3), torch.bfloat16, "GVA act dq")
+    assert_close(got[1], ref["dk"].reshape(B, T, Hk, G, 64).sum(3), torch.bfloat16, "GVA act dk")
+    assert_close(got[2], ref["dv"], torch.bfloat16, "GVA act dv")
+    assert_close(got[5], ref["dh0"], torch.bfloat16, "GVA act dh0")
+    assert_close(got[3], ch["dx"], torch.bfloat16, "GVA act d(gate logit)")
+    assert_close(got[4], ch["db"], torch.bfloat16, "GVA act d(beta logit)")
+    assert_close(got[6], ch["dA_log"], torch.float32, "GVA act dA_log")
+    assert_close(got[7], ch["ddt_bias"], torch.float32, "GVA act ddt_bias")
