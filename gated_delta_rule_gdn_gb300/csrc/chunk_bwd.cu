@@ -409,6 +409,34 @@ __device__ __forceinline__ void frag_b(const float* M, int ld, int k0, int n0, i
     split_tf32(s1 * M[(k0 + t + 4) * ld + n0 + g], h[1], l[1]);
 }
 
+// The state (or state gradient) fragments of a walk -- rows c, columns j and j + 1 of each m16n8 tile -- to shared
+// memory and to the workspace rows at dst (row stride d_v): 8-byte pairs where every row starts on 8 bytes (d_v
+// even), else element by element.
+template <int MTW>
+__device__ __forceinline__ void store_state(const float (&acc)[MTW][8][4], float* S, float* dst, int cw, int g, int t4,
+                                            int dk, int dv, int bw) {
+    const bool pairs = (dv & 1) == 0;
+#pragma unroll
+    for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int c = cw + 16 * mt + g + 8 * h2, j = 8 * nt + 2 * t4;
+                const float x0 = acc[mt][nt][2 * h2], x1 = acc[mt][nt][2 * h2 + 1];
+                *reinterpret_cast<float2*>(S + c * kWS + j) = make_float2(x0, x1);
+                if (c < dk) {
+                    float* p = dst + (size_t)c * dv + j;
+                    if (pairs && j + 1 < bw) {
+                        *reinterpret_cast<float2*>(p) = make_float2(x0, x1);
+                    } else {
+                        if (j < bw) p[0] = x0;
+                        if (j + 1 < bw) p[1] = x1;
+                    }
+                }
+            }
+}
+
 // The forward walk: per chunk, store the entry state, Z and Delta.  The state tile h [channels][64 columns] lives in
 // m16n8 accumulator fragments: warp w owns channels [w CPT, w CPT + CPT) (CPT / 16 row blocks) and all eight
 // 8-column blocks.  Per chunk, on 3xTF32 warp MMAs:
@@ -485,16 +513,7 @@ __device__ __forceinline__ void walk_forward(const BwdArgs& a, const Ws& ws, flo
     bool ok = true;
     for (long ci = 0;; ++ci) {
         // the state entering chunk ci (ci = n_chunks: the final state), to shared memory and the workspace
-#pragma unroll
-        for (int mt = 0; mt < MTW; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = cw + 16 * mt + g + 8 * (i >> 1), j = 8 * nt + 2 * t4 + (i & 1);
-                    Hs[c * kWS + j] = hacc[mt][nt][i];
-                    if (c < dk && j < bw) ws.h[sbase + (size_t)ci * sstride + (size_t)c * dv + j] = hacc[mt][nt][i];
-                }
+        store_state<MTW>(hacc, Hs, ws.h + sbase + (size_t)ci * sstride, cw, g, t4, dk, dv, bw);
         if (ci == n_chunks) break;
         const int L = (int)min((long)CC, geo.len - ci * CC);
         float vcur[MTC][4];
@@ -674,16 +693,7 @@ __device__ __forceinline__ void walk_backward(const BwdArgs& a, const Ws& ws, fl
         const long ci = n_chunks - 1 - k;
         const int L = (int)min((long)CC, geo.len - ci * CC);
         // the gradient of this chunk's h_out, to shared memory and the workspace
-#pragma unroll
-        for (int mt = 0; mt < MTW; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = cw + 16 * mt + g + 8 * (i >> 1), j = 8 * nt + 2 * t4 + (i & 1);
-                    dHs[c * kWS + j] = dacc[mt][nt][i];
-                    if (c < dk && j < bw) ws.dh[sbase + (size_t)ci * sstride + (size_t)c * dv + j] = dacc[mt][nt][i];
-                }
+        store_state<MTW>(dacc, dHs, ws.dh + sbase + (size_t)ci * sstride, cw, g, t4, dk, dv, bw);
         {
             const int jl = tid & 31, r0 = tid >> 5;
 #pragma unroll
