@@ -310,35 +310,39 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const BwdArgs a, Ws 
     gate_prefix(Gs, CC, PERCH ? dk : 1, lg);
     __syncthreads();
     pair_products<PERCH, true>(Qs, Ks, Gs, R + rc.KK, R + rc.P, nullptr, CC, dkp, ldk, lg, scale);
-    for (int idx = threadIdx.x; idx < CC * W; idx += kThreads) {
-        const int r = idx / W, c = idx % W;
-        const float g = PERCH ? Gs[r * lg + c] : Gs[r];
-        const float gl = PERCH ? Gs[(L - 1) * lg + c] : Gs[L - 1];
-        const float e = expf(g), k = Ks[r * ldk + c];
-        R[rc.QE + r * ldk + c] = scale * Qs[r * ldk + c] * e;
-        R[rc.KE + r * ldk + c] = k * e;
-        R[rc.KF + r * ldk + c] = k * expf(gl - g);
-    }
-    for (int c = threadIdx.x; c < (PERCH ? W : 4); c += kThreads)
-        R[rc.EL + c] = expf(PERCH ? Gs[(L - 1) * lg + c] : Gs[L - 1]);
-    __syncthreads();
-    // T = (I + A)^{-1}, A = diag(beta) KK strictly lower: column c by forward substitution on the unit vector
-    // (thread c, the column in registers; its entries above row c are exact zeros, so the sums may start at row 0).
-    // Rows past the chunk's end have beta = 0, so T is the identity there.
-    if (threadIdx.x < CC) {
-        const int c = threadIdx.x;
-        const float* KK = R + rc.KK;
-        const float* Bv = R + rc.B;
-        float* Tm = R + rc.T;
-        float tc[CC];
+    __syncthreads();   // KK complete
+    if (threadIdx.x < 32) {
+        // warp 0: T = (I + A)^{-1}, A = diag(beta) KK strictly lower: column c by forward substitution on the unit
+        // vector (thread c, the column in registers; its entries above row c are exact zeros, so the sums may start
+        // at row 0).  Rows past the chunk's end have beta = 0, so T is the identity there.
+        if (threadIdx.x < CC) {
+            const int c = threadIdx.x;
+            const float* KK = R + rc.KK;
+            const float* Bv = R + rc.B;
+            float* Tm = R + rc.T;
+            float tc[CC];
 #pragma unroll
-        for (int r = 0; r < CC; ++r) {
-            float acc = 0.f;
+            for (int r = 0; r < CC; ++r) {
+                float acc = 0.f;
 #pragma unroll
-            for (int q = 0; q < r; ++q) acc = fmaf(KK[r * (CC + 1) + q], tc[q], acc);
-            tc[r] = r == c ? 1.f : (r > c ? -Bv[r] * acc : 0.f);
-            Tm[r * (CC + 1) + c] = tc[r];
+                for (int q = 0; q < r; ++q) acc = fmaf(KK[r * (CC + 1) + q], tc[q], acc);
+                tc[r] = r == c ? 1.f : (r > c ? -Bv[r] * acc : 0.f);
+                Tm[r * (CC + 1) + c] = tc[r];
+            }
         }
+    } else {
+        // the other warps meanwhile: scale Q*E, K*E, K*F and exp(G_L)
+        for (int idx = threadIdx.x - 32; idx < CC * W; idx += kThreads - 32) {
+            const int r = idx / W, c = idx % W;
+            const float g = PERCH ? Gs[r * lg + c] : Gs[r];
+            const float gl = PERCH ? Gs[(L - 1) * lg + c] : Gs[L - 1];
+            const float e = expf(g), k = Ks[r * ldk + c];
+            R[rc.QE + r * ldk + c] = scale * Qs[r * ldk + c] * e;
+            R[rc.KE + r * ldk + c] = k * e;
+            R[rc.KF + r * ldk + c] = k * expf(gl - g);
+        }
+        for (int c = threadIdx.x - 32; c < (PERCH ? W : 4); c += kThreads - 32)
+            R[rc.EL + c] = expf(PERCH ? Gs[(L - 1) * lg + c] : Gs[L - 1]);
     }
     __syncthreads();
     float4* dst = reinterpret_cast<float4*>(ws.rec + ((size_t)slot * H + hh) * rc.total);
