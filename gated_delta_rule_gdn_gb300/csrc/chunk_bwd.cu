@@ -881,7 +881,7 @@ __host__ __device__ inline GradLay grad_lay(int C, int dk, bool perch) {
     l.HB = o; o += tiles > after ? tiles : after; o = round4(o);
     l.TB = l.HB + 4 * hr * kHS;
     l.pbeta = o; o += C; o = round4(o);
-    l.us = o; o += dk; o = round4(o);
+    l.us = o; o += 2 * dk; o = round4(o);
     l.red = o; o += 2 * C + 1; o = round4(o);
     l.total = o;
     return l;
@@ -1004,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
         for (int i = tid; i < CC * lg; i += kThreads) Gs[i] = rec[rc.G + i];
         for (int i = tid; i < CC; i += kThreads) Bs[i] = rec[rc.B + i];
     }
-    for (int c = tid; c < dk; c += kThreads) us[c] = 0.f;
+    for (int c = tid; c < 2 * dk; c += kThreads) us[c] = 0.f;
     if (!PERCH) {
         __syncthreads();
         for (int idx = tid; idx < CC * CC; idx += kThreads) {
@@ -1062,10 +1062,14 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
                 const int r = idx / CC, s = idx % CC;
                 if (s <= r) {
                     float x = dp[k], y = da[k];
-                    for (int j = 0; j < kBV; ++j) {
-                        const float d = D_[s * kHS + j];
-                        x = fmaf(O_[r * kHS + j], d, x);
-                        y = fmaf(Y_[r * kHS + j], d, y);
+                    const float4* o4 = reinterpret_cast<const float4*>(O_ + r * kHS);
+                    const float4* y4 = reinterpret_cast<const float4*>(Y_ + r * kHS);
+                    const float4* d4 = reinterpret_cast<const float4*>(D_ + s * kHS);
+#pragma unroll
+                    for (int q = 0; q < kBV / 4; ++q) {   // columns in order, four per 16-byte load
+                        const float4 d = d4[q], o = o4[q], yv = y4[q];
+                        x = fmaf(o.x, d.x, x); x = fmaf(o.y, d.y, x); x = fmaf(o.z, d.z, x); x = fmaf(o.w, d.w, x);
+                        y = fmaf(yv.x, d.x, y); y = fmaf(yv.y, d.y, y); y = fmaf(yv.z, d.z, y); y = fmaf(yv.w, d.w, y);
                     }
                     dp[k] = x;
                     da[k] = y;
@@ -1073,15 +1077,29 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
             }
         }
         if (tid < CC) {
-            for (int j = 0; j < kBV; ++j) ubeta = fmaf(Y_[tid * kHS + j], Z_[tid * kHS + j], ubeta);
-        }
-        // us[c] += sum_j dh[c][j] h[c][j]: one warp per channel, lane = column (each channel always meets the
-        // same warp, so the sum needs no atomics)
-        for (int c = warp; c < dk; c += kThreads / 32) {
-            float x = dHs[c * kHS + lane] * Hs[c * kHS + lane];
+            const float4* y4 = reinterpret_cast<const float4*>(Y_ + tid * kHS);
+            const float4* z4 = reinterpret_cast<const float4*>(Z_ + tid * kHS);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (lane == 0) us[c] += x;
+            for (int q = 0; q < kBV / 4; ++q) {
+                const float4 yv = y4[q], zv = z4[q];
+                ubeta = fmaf(yv.x, zv.x, ubeta); ubeta = fmaf(yv.y, zv.y, ubeta);
+                ubeta = fmaf(yv.z, zv.z, ubeta); ubeta = fmaf(yv.w, zv.w, ubeta);
+            }
+        }
+        // us[half dk + c] += sum over the tile's columns 16 half .. 16 half + 15 of dh[c][j] h[c][j]: one thread per
+        // (channel, half), 16-byte loads (each pair always meets the same thread, so the sums need no atomics; the
+        // halves are added after the last tile)
+        for (int e = tid; e < 2 * dk; e += kThreads) {
+            const int hf = e / dk, c = e - hf * dk;
+            const float4* a4 = reinterpret_cast<const float4*>(dHs + c * kHS + 16 * hf);
+            const float4* b4 = reinterpret_cast<const float4*>(Hs + c * kHS + 16 * hf);
+            float x = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 u = a4[q], v = b4[q];
+                x = fmaf(u.x, v.x, x); x = fmaf(u.y, v.y, x); x = fmaf(u.z, v.z, x); x = fmaf(u.w, v.w, x);
+            }
+            us[e] += x;
         }
         // the state products, 8 columns of the tile per step
 #pragma unroll
@@ -1154,7 +1172,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
     }
     if (tid < CC) pbeta[tid] = ubeta;
     __syncthreads();
-    if (tid < dk) us[tid] *= expf(PERCH ? Gs[(L - 1) * lg + tid] : Gs[L - 1]);
+    if (tid < dk) us[tid] = (us[tid] + us[dk + tid]) * expf(PERCH ? Gs[(L - 1) * lg + tid] : Gs[L - 1]);
     __syncthreads();
 
     // per (row, channel): dQ, dK written; the gate terms pb, pw kept in place of xo, hy
