@@ -854,7 +854,8 @@ __global__ void __launch_bounds__(kThreads) bwd_walk_kernel(const BwdArgs a, Ws 
 // ---- the per-chunk gradients ---------------------------------------------------------------------------------
 
 struct GradLay {
-    int G, B, KK, P, Ex, dP, dA, HB, TB, pbeta, us, red, total;
+    int G, B, KK, AB, Ex, dP, dA, HB, TB, pbeta, us, red, total;
+    // scalar gate: Ex holds exp(G_r - G_s) until the pair factors are formed, then dA e; AB holds dA e beta_r
     // inside the scratch region HB .. (after the tile loop): raw Q and K rows, then xo, hy, dd
     int Q, K, XO, HY, DD;
 };
@@ -871,7 +872,7 @@ __host__ __device__ inline GradLay grad_lay(int C, int dk, bool perch) {
     l.G = o; o += C * lg; o = round4(o);
     l.B = o; o += C; o = round4(o);
     l.KK = o; o += cc; o = round4(o);
-    l.P = o; o += cc; o = round4(o);
+    l.AB = o; o += cc; o = round4(o);
     l.Ex = o; o += perch ? 0 : cc; o = round4(o);
     l.dP = o; o += cc; o = round4(o);
     l.dA = o; o += cc; o = round4(o);
@@ -913,7 +914,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
     const Rec rc = rec_lay(CC, dk, PERCH);
     const int hrows = 8 * NTW * (kThreads / 32);
     float* Gs = smem + ly.G;  float* Bs = smem + ly.B;
-    float* KK = smem + ly.KK; float* Pm = smem + ly.P;  float* Ex = smem + ly.Ex;
+    float* KK = smem + ly.KK; float* WAB = smem + ly.AB;  float* Ex = smem + ly.Ex;
     float* dPm = smem + ly.dP; float* dAm = smem + ly.dA;
     float* pbeta = smem + ly.pbeta; float* us = smem + ly.us; float* red = smem + ly.red;
     // tile buffers b = 0, 1: state, state gradient, then the dO, Delta, Y, Z tiles
@@ -997,10 +998,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
     // KK, P, the cumulative gate and beta from the chunk record
     {
         const float* rec = ws.rec + ((size_t)slot * H + hh) * rc.total;
-        for (int i = tid; i < CC * (CC + 1); i += kThreads) {
-            KK[i] = rec[rc.KK + i];
-            Pm[i] = rec[rc.P + i];
-        }
+        for (int i = tid; i < CC * (CC + 1); i += kThreads) KK[i] = rec[rc.KK + i];
         for (int i = tid; i < CC * lg; i += kThreads) Gs[i] = rec[rc.G + i];
         for (int i = tid; i < CC; i += kThreads) Bs[i] = rec[rc.B + i];
     }
@@ -1165,9 +1163,19 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
     for (int k = 0; k < NP; ++k) {
         const int idx = tid + k * kThreads;
         if (idx < CC * CC) {
-            const int r = idx / CC, s = idx % CC;
-            dPm[r * (CC + 1) + s] = (s <= r) ? dp[k] : 0.f;
-            dAm[r * (CC + 1) + s] = (s < r) ? -da[k] : 0.f;
+            const int r = idx / CC, s = idx % CC, o = r * (CC + 1) + s;
+            dAm[o] = (s < r) ? -da[k] : 0.f;
+            if (PERCH) {
+                dPm[o] = (s <= r) ? dp[k] : 0.f;
+            } else {
+                // the scalar gate's factors folded in once per pair: dP e, dA e (in place of e) and dA e beta_r,
+                // with e = exp(G_r - G_s) (1 on the diagonal)
+                const float e = Ex[o];
+                dPm[o] = (s <= r) ? dp[k] * e : 0.f;
+                const float ae = (s < r) ? -da[k] * e : 0.f;
+                Ex[o] = ae;
+                WAB[o] = ae * Bs[r];
+            }
         }
     }
     if (tid < CC) pbeta[tid] = ubeta;
@@ -1180,16 +1188,28 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdArgs a, Ws 
         const int r = idx / dk, c = idx % dk;
         const float gr = PERCH ? Gs[r * lg + c] : Gs[r];
         float sq = 0.f, sar = 0.f, skp = 0.f, sac = 0.f;
-        for (int s = 0; s < r; ++s) {
-            const float e = PERCH ? expf(gr - Gs[s * lg + c]) : Ex[r * (CC + 1) + s];
-            const float ke = Ks[s * ldk + c] * e;
-            sq = fmaf(dPm[r * (CC + 1) + s], ke, sq);
-            sar = fmaf(dAm[r * (CC + 1) + s], ke, sar);
-        }
-        for (int u = r + 1; u < L; ++u) {
-            const float e = PERCH ? expf(Gs[u * lg + c] - gr) : Ex[u * (CC + 1) + r];
-            skp = fmaf(dPm[u * (CC + 1) + r], Qs[u * ldk + c] * e, skp);
-            sac = fmaf(dAm[u * (CC + 1) + r] * Bs[u], Ks[u * ldk + c] * e, sac);
+        if (PERCH) {
+            for (int s = 0; s < r; ++s) {
+                const float e = expf(gr - Gs[s * lg + c]);
+                const float ke = Ks[s * ldk + c] * e;
+                sq = fmaf(dPm[r * (CC + 1) + s], ke, sq);
+                sar = fmaf(dAm[r * (CC + 1) + s], ke, sar);
+            }
+            for (int u = r + 1; u < L; ++u) {
+                const float e = expf(Gs[u * lg + c] - gr);
+                skp = fmaf(dPm[u * (CC + 1) + r], Qs[u * ldk + c] * e, skp);
+                sac = fmaf(dAm[u * (CC + 1) + r] * Bs[u], Ks[u * ldk + c] * e, sac);
+            }
+        } else {   // the pair factors carry the gate (and beta_u for sac)
+            for (int s = 0; s < r; ++s) {
+                const float kv = Ks[s * ldk + c];
+                sq = fmaf(dPm[r * (CC + 1) + s], kv, sq);
+                sar = fmaf(Ex[r * (CC + 1) + s], kv, sar);
+            }
+            for (int u = r + 1; u < L; ++u) {
+                skp = fmaf(dPm[u * (CC + 1) + r], Qs[u * ldk + c], skp);
+                sac = fmaf(WAB[u * (CC + 1) + r], Ks[u * ldk + c], sac);
+            }
         }
         sq *= scale;
         skp *= scale;
