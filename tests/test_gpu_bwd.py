@@ -99,7 +99,7 @@ def test_packed_with_an_empty_sequence(kind):
 
 
 @pytest.mark.parametrize("kind,dk,dv", [("gdn", 24, 40), ("kda", 48, 16), ("gdn", 160, 96), ("kda", 64, 256),
-                                        ("gdn", 256, 64), ("kda", 256, 32)])
+                                        ("gdn", 256, 64), ("kda", 256, 32), ("gdn", 40, 37), ("kda", 33, 13)])
 def test_head_sizes(kind, dk, dv):
     x = _problem(kind, "f32", 1, 45, 2, dk, dv, h0_std=0.3)
     _compare(_gpu(x), _oracle(x), torch.float32, f"{kind} dk{dk} dv{dv}")

@@ -79,6 +79,8 @@ SMALL = [
     ("kda", "f32", 1, 150, 2, 32, 32, 32, 0.1),
     ("kda", "bf16", 2, 200, 2, 128, 128, 64, 0.02),
     ("kda", "bf16", 1, 70, 2, 64, 128, 16, 0.0),
+    ("gdn", "f32", 1, 90, 2, 40, 37, 16, 0.1),
+    ("kda", "bf16", 1, 50, 2, 33, 13, 32, 0.0),
     # head sizes above 128 (the generic kernel; the per-channel gate at d_k = 256 takes chunk <= 32)
     ("gdn", "bf16", 2, 150, 2, 256, 256, 64, 0.02),
     ("gdn", "f32", 1, 90, 2, 256, 96, 32, 0.05),
