@@ -7,7 +7,7 @@ One step is one gdn_chunk_fwd call over the whole workload.  That is the
 whole hot path: gate prefix, beta-scaled masked K K^T, the UT solve, the WY
 products, the serial state pass and the output.  The default (auto) path is
 two launches per call: the per-chunk kernel over all SMs, then the state
-kernel; --algo tcgen05 times the fused single-launch kernel instead.
+kernel.
 Inputs are seeded and synthetic, drawn by gated_delta_rule_gdn_gb300.workloads.
 
 * value: tokens/s (B*T per step).  Inputs are resident in HBM and timed with
@@ -20,9 +20,11 @@ Inputs are seeded and synthetic, drawn by gated_delta_rule_gdn_gb300.workloads.
   computes and row b - 1 copies out.
 * roofline: algorithmic bytes of one call / the mean call time (all of the
   call's launches, on the launching stream), against the measured HBM copy
-  bandwidth.  The bytes are 1,288 B per token-head (q,
-  k, v in bf16, o in fp32, g and beta in fp32), plus the fp32 state read and
-  write per sequence-head.
+  bandwidth.  frac counts o in bf16, the survey's count: 1,032 B per
+  token-head (q, k, v and o in bf16, g and beta in fp32; KDA 4 d_k more for
+  its gate), plus the fp32 state read and write per sequence-head.  The call
+  writes o in fp32 (bf16 rounding alone breaks the max-error bound), so
+  frac_o_f32 is also given, on 1,288 B per token-head.
 * cpu_baseline: the fp64 C oracle on the host cores (rank 0, N = 1).
 * --impl reference: the oracle alone, timed as the reference arm.
 Workloads 6 and 7 time the chunk backward (gdn_chunk_bwd) on the shapes of
@@ -75,12 +77,13 @@ def _metric(w) -> str:
     return f"{w.kind.upper()} chunk-fwd tokens/s ({w.name}) and % of roofline, 1×GB300"
 
 
-def _alg_bytes(w) -> int:
-    """Algorithmic HBM bytes of one chunk-forward call over workload w (o written in fp32)."""
+def _alg_bytes(w, o_bytes: int = 2) -> int:
+    """Algorithmic HBM bytes of one chunk-forward call over workload w, o counted at o_bytes per element (2: the
+    survey's count, o in bf16; 4: o as the call writes it, fp32)."""
     token_heads = w.B * w.T * w.H
     es = 2 if w.dtype == "bf16" else 4
     g_bytes = 4 * w.dk if w.kind == "kda" else 4
-    per_token_head = es * (2 * w.dk + w.dv) + 4 * w.dv + g_bytes + 4   # q, k, v + o (fp32) + g + beta
+    per_token_head = es * (2 * w.dk + w.dv) + o_bytes * w.dv + g_bytes + 4   # q, k, v + o + g + beta
     N = w.n_seqs if w.n_seqs else w.B
     state = 2 * N * w.H * w.dk * w.dv * 4 if w.h0_std > 0 else N * w.H * w.dk * w.dv * 4
     return token_heads * per_token_head + state
@@ -88,7 +91,8 @@ def _alg_bytes(w) -> int:
 
 # The kernel sources each recorded traffic figure depends on (the files that make the timed kernels' code).
 TRAFFIC_SOURCES = {
-    "chunk": ("chunk_two_pass.cu", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh"),
+    "chunk_gdn": ("chunk_gdn_tmem.cu", "chunk_wy_common.cuh", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh"),
+    "chunk_kda": ("chunk_two_pass.cu", "chunk_wy_common.cuh", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh"),
     "decode": ("recurrent_step.cu", "gate_act.cuh"),
     "bwd": ("chunk_bwd.cu", "tc_common.cuh"),
 }
@@ -97,7 +101,9 @@ TRAFFIC_SOURCES = {
 def _traffic_kind(workload: str) -> str:
     if "_bwd_" in workload:
         return "bwd"
-    return "decode" if workload.startswith("decode") or "_decode_" in workload else "chunk"
+    if workload.startswith("decode") or "_decode_" in workload:
+        return "decode"
+    return "chunk_kda" if workload.startswith("kda") else "chunk_gdn"
 
 
 def _code_only(src: str) -> str:
@@ -107,7 +113,7 @@ def _code_only(src: str) -> str:
     return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
 
 
-def sources_sha256(kind: str = "chunk") -> str:
+def sources_sha256(kind: str = "chunk_gdn") -> str:
     """Hash of the kernel sources a recorded ncu traffic figure of this kind depends on (code only: an edit of
     the comments keeps the record)."""
     h = hashlib.sha256()
@@ -252,6 +258,38 @@ def cpu_baseline(x, w, min_seconds=10.0, max_passes=60, heads=None):
                       f"{passes} pass(es), {t_total:.1f} s; tokens/s scaled to all {w.H} heads"}
 
 
+def _decode_sample(w, consts, step: int = 0):
+    """fp64 oracle inputs of one decode step for every 16th (sequence, head) chain (512 of the 8192)."""
+    from gated_delta_rule_gdn_gb300 import workloads as W
+    import torch
+    NH = w.N * w.H
+    sample = torch.arange(0, NH, 16)
+    x = W.decode_step_inputs(w, consts, step)
+    h0 = consts["state"].reshape(NH, 1, w.dk, w.dv)[sample].to(torch.float64).numpy()
+    q, k, v = (x[n].reshape(NH, 1, 1, -1)[sample].to(torch.float64).numpy() for n in ("q", "k", "v"))
+    beta = x["beta"].reshape(NH, 1, 1)[sample].to(torch.float64).numpy()
+    g = (x["g"].reshape(NH, 1, 1, -1) if w.kind == "kda" else x["g"].reshape(NH, 1, 1))[sample].to(torch.float64).numpy()
+    return (q, k, v, g, beta, h0), len(sample), NH
+
+
+def cpu_baseline_decode(w, consts, min_seconds=10.0, max_passes=2000):
+    """Time the fp64 oracle on one decode step of a chain sample, repeated for about min_seconds; tokens/s scaled to
+    all chains."""
+    import oracle
+    (q, k, v, g, beta, h0), n, NH = _decode_sample(w, consts)
+    oracle.load()
+    passes, t_total = 0, 0.0
+    while passes < max_passes and (passes == 0 or t_total < min_seconds):
+        t0 = time.perf_counter()
+        oracle.recurrence(q, k, v, g, beta, w.scale, h0, gate_per_channel=w.kind == "kda")
+        t_total += time.perf_counter() - t0
+        passes += 1
+    dt = t_total / passes * (NH / n)
+    return {"value": w.N / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"one decode step for {n} of {NH} (sequence, head) chains, {passes} pass(es), {t_total:.1f} s; "
+                      f"time scaled to all chains"}
+
+
 def run_reference_decode(args):
     """The oracle on a decode step: one token for a sample of the (sequence, head) chains, scaled to all of them."""
     from gated_delta_rule_gdn_gb300 import workloads as W
@@ -259,13 +297,8 @@ def run_reference_decode(args):
     import torch
     w = _decode_workload(args.workload)
     consts = W.decode_constants(w, seed=0)
-    NH = w.N * w.H
-    sample = torch.arange(0, NH, 16)                  # 512 of the 8192 chains
-    x = W.decode_step_inputs(w, consts, 0)
-    h0 = consts["state"].reshape(NH, 1, w.dk, w.dv)[sample].to(torch.float64).numpy()
-    q, k, v = (x[n].reshape(NH, 1, 1, -1)[sample].to(torch.float64).numpy() for n in ("q", "k", "v"))
-    beta = x["beta"].reshape(NH, 1, 1)[sample].to(torch.float64).numpy()
-    g = (x["g"].reshape(NH, 1, 1, -1) if w.kind == "kda" else x["g"].reshape(NH, 1, 1))[sample].to(torch.float64).numpy()
+    (q, k, v, g, beta, h0), n_sample, NH = _decode_sample(w, consts)
+    sample = range(n_sample)
     oracle.load()
     run = lambda: oracle.recurrence(q, k, v, g, beta, w.scale, h0, gate_per_channel=w.kind == "kda")
     for _ in range(args.warmup):
@@ -668,10 +701,13 @@ def run_ours(args):
     value = tokens * ws / (ms / 1e3)
     peak, peak_kind = _peaks()
     alg = _alg_bytes(w)
+    alg32 = _alg_bytes(w, 4)
     achieved = alg / (ms / 1e3) / 1e9
     plan = gdn.chunk_plan(w.kind == "kda", w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16,
                           x["cu_seqlens"] is not None, args.algo)
-    kernel, launches = {"tcgen05": ("chunk_tc", 1), "two_pass": ("chunk_two_pass", 2)}.get(plan, ("chunk_generic", 1))
+    two_pass = "chunk_two_pass (chunk_intra_kernel, chunk_state_kernel)" if w.kind == "kda" else \
+        "chunk_gdn_tmem (gdn_intra_kernel, gdn_state_kernel)"
+    kernel, launches = {"two_pass": (two_pass, 2)}.get(plan, ("chunk_generic", 1))
     line = {
         "metric": _metric(w), "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -685,7 +721,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": _traffic_for(w.name), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6800 GB/s",
-                     "algorithmic_bytes_per_launch": alg},
+                     "algorithmic_bytes_per_launch": alg, "o_bytes_counted": "bf16 (the survey's count)",
+                     "frac_o_f32": alg32 / (ms / 1e3) / 1e9 / peak, "algorithmic_bytes_o_f32": alg32},
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipeline": (f"per batch row ({rows} public-API calls), copies in / compute / copies out on three "
@@ -807,6 +844,8 @@ def run_decode(args):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(w, consts)
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:
@@ -821,7 +860,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--algo", choices=["auto", "generic", "tcgen05", "two_pass"], default="auto")
+    ap.add_argument("--algo", choices=["auto", "generic", "two_pass"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4, 5, 6, 7], default=WORKLOAD,
                     help="1: GDN B4 T4096 H16 (the headline), 2: packed GDN 8 seqs 65536 tokens H32, 3: KDA B2 T8192 "

@@ -18,7 +18,7 @@ _LIB = None
 
 GDN_OK = 0
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA",
-                4: "GDN_ERR_TIMEOUT"}
+                4: "GDN_ERR_TIMEOUT", 5: "GDN_ERR_NONFINITE"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "two_pass": 3}
 
@@ -409,7 +409,7 @@ def kda_recurrent_step(q, k, v, g, beta, state, scale=None, o=None, stream=None,
 
 def chunk_plan(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chunk_size: int, dtype,
                varlen: bool = False, algo: str = "auto", o_dtype=torch.float32) -> str:
-    """Name of the kernel ("generic", "tcgen05" or "two_pass") a chunk-forward call with these sizes runs."""
+    """Name of the kernel ("generic" or "two_pass") a chunk-forward call with these sizes runs."""
     out = ctypes.c_int(-1)
     _check(load().gdn_chunk_plan(int(per_channel), B, T, H, dk, dv, chunk_size, DTYPES[dtype], DTYPES[o_dtype],
                                  int(varlen), ALGOS[algo], ctypes.byref(out)))
@@ -417,5 +417,6 @@ def chunk_plan(per_channel: bool, B: int, T: int, H: int, dk: int, dv: int, chun
 
 
 def device_status(clear: bool = True) -> int:
-    """GDN_OK, or GDN_ERR_TIMEOUT if a kernel gave up a bounded wait (synchronises the device)."""
+    """GDN_OK; GDN_ERR_TIMEOUT if a kernel gave up a bounded wait; GDN_ERR_NONFINITE if a chunk forward wrote a
+    non-finite value to o or the final state (synchronises the device)."""
     return int(load().gdn_device_status(int(clear)))

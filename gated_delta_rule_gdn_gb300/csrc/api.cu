@@ -74,18 +74,17 @@ gdn_status check_chunk(const gdn::ChunkArgs& a, gdn_dtype dtype, gdn_dtype o_dty
 }
 
 // Resolve a kernel request against what each kernel supports.  AUTO takes the two-pass tcgen05 path where it
-// applies, then the fused tcgen05 kernel, then the generic one.
+// applies, else the generic one.  GDN_ALGO_TCGEN05 (the retired single-launch kernel) is refused.
 gdn_status resolve_algo(const gdn::ChunkArgs& a, gdn_algo algo, const char* fn, gdn_algo* chosen) {
     if (algo != GDN_ALGO_AUTO && algo != GDN_ALGO_GENERIC && algo != GDN_ALGO_TCGEN05 && algo != GDN_ALGO_TWO_PASS)
         return fail(GDN_ERR_INVALID_ARG, "%s: unknown algo %d", fn, (int)algo);
-    const char* why_tc = gdn::tc_chunk_unsupported_reason(a);
+    if (algo == GDN_ALGO_TCGEN05)
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the single-launch tcgen05 kernel was retired; use GDN_ALGO_TWO_PASS or "
+                    "GDN_ALGO_AUTO", fn);
     const char* why_tp = gdn::two_pass_unsupported_reason(a);
-    if (algo == GDN_ALGO_TCGEN05 && why_tc)
-        return fail(GDN_ERR_UNSUPPORTED, "%s: the tcgen05 kernel does not apply: %s", fn, why_tc);
     if (algo == GDN_ALGO_TWO_PASS && why_tp)
         return fail(GDN_ERR_UNSUPPORTED, "%s: the two-pass kernels do not apply: %s", fn, why_tp);
-    if (algo == GDN_ALGO_AUTO)
-        algo = !why_tp ? GDN_ALGO_TWO_PASS : (!why_tc ? GDN_ALGO_TCGEN05 : GDN_ALGO_GENERIC);
+    if (algo == GDN_ALGO_AUTO) algo = !why_tp ? GDN_ALGO_TWO_PASS : GDN_ALGO_GENERIC;
     if (algo == GDN_ALGO_GENERIC) {
         const size_t need = gdn::generic_smem_bytes(a);
         if (need > gdn::kMaxSmemPerBlock)
@@ -157,8 +156,6 @@ gdn_status chunk_common(const void* q, const void* k, const void* v, const float
             const cudaError_t e2 = cudaFreeAsync(ws, s);
             if (e == cudaSuccess) e = e2;
         }
-    } else if (chosen == GDN_ALGO_TCGEN05) {
-        e = gdn::launch_chunk_tc(a, s);
     } else {
         e = gdn::launch_chunk_generic(a, s);
     }
@@ -556,13 +553,20 @@ gdn_status gdn_test_inject(int what) {
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 gdn_status gdn_device_status(int clear) {
-    unsigned v = 0, v2 = 0, v3 = 0;
-    cudaError_t e = gdn::tc_read_and_clear_status(&v, clear != 0);
-    if (e == cudaSuccess) e = gdn::tp_read_and_clear_status(&v2, clear != 0);
-    if (e == cudaSuccess) e = gdn::bwd_read_and_clear_status(&v3, clear != 0);
+    unsigned tp = 0, gt = 0, bw = 0;
+    cudaError_t e = gdn::tp_read_and_clear_status(&tp, clear != 0);
+    if (e == cudaSuccess) e = gdn::gt_read_and_clear_status(&gt, clear != 0);
+    if (e == cudaSuccess) e = gdn::bwd_read_and_clear_status(&bw, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_status");
-    v |= (v2 << 16) | (v3 << 28);
-    if (v != 0) return fail(GDN_ERR_TIMEOUT, "gdn_device_status: a kernel gave up a bounded wait (code 0x%x)", v);
+    const unsigned nf = gdn::kStatusNonfinite;
+    if (((tp | gt) & ~nf) != 0 || bw != 0)
+        return fail(GDN_ERR_TIMEOUT,
+                    "gdn_device_status: a kernel gave up a bounded wait (per-channel forward 0x%x, scalar-gate forward "
+                    "0x%x, backward 0x%x)", tp, gt, bw);
+    if (((tp | gt) & nf) != 0)
+        return fail(GDN_ERR_NONFINITE,
+                    "gdn_device_status: a chunk forward wrote a non-finite value to o or the final state (an fp16 "
+                    "operand passed 65504, or an input was not finite)");
     return ok();
 }
 

@@ -1,30 +1,33 @@
-// Two-pass chunkwise gated delta rule forward on tcgen05 tensor cores (sm_103a): scalar gate, bf16 q/k/v,
-// d_k = d_v = 128, chunk C = 64, fp32 state, o in fp32 or bf16.
+// Two-pass chunkwise forward of the per-key-channel gate (Kimi Delta Attention) on tcgen05 tensor cores (sm_103a):
+// bf16 q/k/v, d_k = d_v = 128, chunk C = 64, fp32 state, o in fp32 or bf16.  (The scalar gate has its own pair of
+// kernels in chunk_gdn_tmem.cu.)
 //
-// The chunk algebra is the one of the fused kernel (chunk_tc.cu), from "TileLang 实战：KDA 从零到一 -- Gated
-// DeltaNet", §2.3, split the way "Gated Delta Network (GDN)", §4(b3)-(d) splits it: every product that does not
-// depend on the state first, for all chunks at once, then the serial state pass.
+// The chunk algebra is "You Could Have Come Up With Kimi Delta Attention" (the chunkwise form: decays per key channel
+// between tokens, the strictly lower key-key system, the read matrix with its diagonal), in the WY/UT form of
+// "TileLang 实战：KDA 从零到一 -- Gated DeltaNet", §2.3, split the way "Gated Delta Network (GDN)", §4(b3)-(d) splits
+// the scalar-gate chunk: every state-independent product first, then the serial state pass.  Per chunk of L <= C
+// rows, with G_ic the within-chunk cumulative log gate of channel c:
+//   A_ij = beta_i sum_c k_ic k_jc 2^(G_ic - G_jc)  (j < i)     P_ij = scale sum_c q_ic k_jc 2^(G_ic - G_jc)  (j <= i)
+//   T = (I + A)^{-1},  W = T diag(beta) (K * 2^G),  U = T diag(beta) V,
+//   Q^ = scale (Q * 2^G),  Ktilde = K * 2^(G_last - G),  gamma_C = 2^(G_last) per channel.
 //
-// Pass 1, chunk_intra_kernel: one work item per (chunk, head), spread over every SM (two CTAs per SM,
-// persistent).  Per item, with G the within-chunk cumulative log gate, gamma = exp(G), L valid rows:
-//   A  = diag(beta)(Gamma * K K^T) (strictly lower)   P = scale Gamma * Q K^T (lower incl. diagonal)
-//   T  = (I + A)^{-1}                                 (blocked inverse, solved in place over A)
-//   [W | U ; P W | P U] = [T; P T] [beta gamma K | beta V]
-//   Q' = scale diag(gamma) Q - P W,  U' = P U,  Ktilde = diag(gamma_C / gamma) K
-// and writes [W; Q'], Ktilde, [U; U'] (fp16, already in the shared-memory operand layouts of pass 2) and
-// gamma_C to the workspace.  MMAs: D0 = [K; Q] K^T, D1 = [I; P] T, D2 = [T; -PT] [beta V | beta gamma K] (N = 256,
-// accumulated onto [0 | 0; 0 | scale gamma Q] so that it yields [U | W; -U' | Q']), 256 TMEM columns per CTA.
+// Pass 1, chunk_intra_kernel<true>: one item per (chunk slot, head), one persistent CTA per SM.  A and P come from
+// TF32 warp products over the channels, with the decays factored through 16-row block references (an exact per-term
+// fallback covers large spreads); the blocked inverse solves T in place; one N = 256 tcgen05 product
+// [T; T] [beta V | beta (K * 2^G)] gives U and W.  The record per item is 74,240 bytes, all fp16, already in the
+// operand layouts of pass 2: [Q^; W] (32 KB, 128 x 128 K-major), Ktilde (16 KB), U (two d_v halves, 16 KB), P (8 KB)
+// and gamma_C (512 B).
 //
-// Pass 2, chunk_state_kernel: one CTA per (sequence, head, 64-column d_v half), 4 warps, h = S^T tile in fp32
-// registers (thread = d_k row).  Per chunk the workspace slot arrives by bulk copy (2-stage ring), then
-//   D3 = [W; Q'] h (M=128 N=64 K=128):  Delta = U - W h,  O = U' + Q' h
-//   D4 = Ktilde^T Delta (M=128 N=64 K=64):  h <- gamma_C h + D4.
-//
-// Workspace (caller-owned or allocated for the call): per (slot, head) item 32 KB [W; Q'] + 16 KB Ktilde +
-// 32 KB [U; U'] (two d_v halves) + 512 B gamma_C, where sequence n's chunk t has slot floor(start_n / C) + n + t.
+// Pass 2, chunk_state_kernel: one CTA per (sequence, head, 64-column d_v half), 8 warps; the fp32 state h = S^T tile
+// sits in registers (thread = d_k row, 32 columns).  Per chunk, its record arrives by bulk copy (two-stage ring):
+//   D3 = [Q^; W] h~ (M = 128, N = 64, K = 128): rows 0-63 Q^ h~, rows 64-127 W h~;  Delta = U - W h~ (fp16)
+//   D4 = Ktilde^T Delta;  D5 = P Delta;  h <- diag(gamma_C) h + D4;  O = Q^ h~ + P Delta (written one chunk later).
+// Slot of sequence n's chunk t: floor(start_n / C) + n + t.
 //
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets a bit in the status word read by
-// gdn_device_status, and the CTA skips the rest of its work, drains its copies, frees TMEM and exits.
+// gdn_device_status, and the CTA skips the rest of its work, drains its copies, frees TMEM and exits.  The state
+// kernel checks every value it writes to o and the final state and sets the non-finite bit when one is not finite
+// (an fp16 intermediate past 65,504, or a non-finite input).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -37,6 +40,7 @@
 #include "tc_common.cuh"
 #include "chunk_common.cuh"
 #include "gate_act.cuh"
+#include "chunk_wy_common.cuh"
 
 namespace gdn {
 
@@ -51,11 +55,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int C = 64;
-constexpr int DK = 128;
-constexpr int DV = 128;
 constexpr int DVT = 64;
-constexpr uint64_t kWaitNs = 2000000000ull;
 
 // workspace, per item
 constexpr uint32_t WS_WQ = 32768;   // [Q^; W] fp16 K-major 128 x 128 (rows 0-63 Q^ = scale gamma Q, rows 64-127 W), two
@@ -76,33 +76,6 @@ struct Ws {
 
 __device__ __forceinline__ void set_status(unsigned bit) { atomicOr(&g_tp_status, bit); }
 
-// Sequence geometry: packed (cu_seqlens) or B rows of T tokens.
-struct Geo {
-    const int32_t* cu;
-    int n_seqs;
-    int B, T, H;
-    __device__ int N() const { return cu ? n_seqs : B; }
-    __device__ void seq(int n, long& s0, int& len) const {
-        if (cu) {
-            long a = cu[n], b = cu[n + 1];
-            a = a < 0 ? 0 : (a > T ? T : a);
-            b = b < a ? a : (b > T ? T : b);
-            s0 = a;
-            len = (int)(b - a);
-        } else {
-            s0 = (long)n * T;
-            len = T;
-        }
-    }
-    // first workspace slot of sequence n (strictly increasing in n for valid cu_seqlens)
-    __device__ long slot0(int n) const {
-        long s0;
-        int len;
-        seq(n, s0, len);
-        return s0 / C + n;
-    }
-};
-
 // ==================================================================== pass 1: per-chunk products
 struct IntraParams {
     Geo geo;
@@ -114,50 +87,6 @@ struct IntraParams {
     GateAct act;   // the gate activation for the scalar gate only; beta for both
     int group;     // value heads per key head: q and k of item head h come from key head h / group
 };
-
-struct Item {
-    int n, h, t, L;
-    long row;     // first token row of the chunk
-    long it;      // workspace item index (slot * H + head)
-};
-
-// A CTA visits the virtual items slot * H + head = last - blockIdx.x, last - blockIdx.x - gridDim.x, ... (the last
-// slots first: the first chunks of every sequence are written last, and the state pass, which starts there, finds
-// them still in L2); the cursor keeps (slot, head) and the sequence whose slots begin at or before the slot
-// (non-increasing along the walk).
-struct Cursor {
-    long s;
-    int h, n;
-};
-
-__device__ __forceinline__ void cursor_step(Cursor& c, int ds, int dh, int H) {
-    c.h -= dh;
-    c.s -= ds;
-    if (c.h < 0) {
-        c.h += H;
-        --c.s;
-    }
-}
-
-// The first valid item at or before the cursor (slots between sequences are unused); false below slot 0.
-__device__ bool cursor_next_valid(const Geo& g, Cursor& c, int ds, int dh, Item& x) {
-    for (; c.s >= 0; cursor_step(c, ds, dh, g.H)) {
-        while (c.n > 0 && g.slot0(c.n) > c.s) --c.n;
-        long s0;
-        int len;
-        g.seq(c.n, s0, len);
-        const long t = c.s - (s0 / C + c.n);
-        if (t < 0 || t * C >= len) continue;
-        x.n = c.n;
-        x.h = c.h;
-        x.t = (int)t;
-        x.row = s0 + t * C;
-        x.L = min(C, len - (int)t * C);
-        x.it = c.s * g.H + c.h;
-        return true;
-    }
-    return false;
-}
 
 // shared memory of pass 1 (bytes from a 1024-aligned base)
 constexpr uint32_t I_KQ = 0;        // [K; Q] rows, two K-slabs of 16 KB (K rows 0-63, Q rows 64-127)
@@ -199,112 +128,16 @@ struct KSmall {
     float tot1[128];          // the first half's total (row 31)
     int fast;                 // every block's spread is small enough for the factored products
 };
-constexpr uint32_t I_SMALL_GDN = I_END;
 constexpr uint32_t I_SMALL_KDA = I_FF + 64 * ES * 4;
 constexpr uint32_t I_KSMALL = I_SMALL_KDA + ((sizeof(ISmall) + 127) & ~127u);   // 16-byte vector loads need alignment
-constexpr uint32_t I_SMEM_GDN = I_SMALL_GDN + sizeof(ISmall) + 1024;
 constexpr uint32_t I_SMEM_KDA = I_KSMALL + sizeof(KSmall) + 1024;
 static_assert(I_SMEM_KDA <= 227 * 1024, "KDA intra kernel shared memory");
 // D2 = [T; T] [beta V | beta gamma K] = [U | W; U | W] spans all 256 columns (D0 is read before MMA2 is issued)
-constexpr uint32_t I_TM_D0 = 0, I_TM_D2 = 0, I_TM_COLS = 256;
+constexpr uint32_t I_TM_D2 = 0, I_TM_COLS = 256;
 constexpr int I_THREADS = 256;
 // largest |cumulative gate - block reference| (log2 units) for the factored KDA products: 2^100 keeps every
 // factor and a 128-term sum of their products inside fp32
 constexpr float KDA_SPREAD_MAX = 100.f;
-
-// Level 0 of the blocked inverse for the 16 x 16 diagonal block at offset o (one warp): the two 8 x 8 diagonal
-// sub-blocks by forward substitution (lane 8 s + c owns column c of sub-block s; their 28 coefficients are loaded
-// before the 8-step chain), then the block below them, T21 = -T22 (A21 T11), 8 x 8 products in fp32.  A is
-// overwritten by T in place; Rw is this warp's 64-float scratch.
-__device__ __forceinline__ void solve_block16(float* Am, float* Rw, int o, int lane) {
-    if (lane < 16) {
-        const int o8 = o + 8 * (lane >> 3), c = lane & 7;
-        float a[28];
-#pragma unroll
-        for (int r = 1; r < 8; ++r)
-#pragma unroll
-            for (int j = 0; j < r; ++j) a[r * (r - 1) / 2 + j] = Am[(o8 + r) * TS + o8 + j];
-        float x[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) x[r] = (r == c) ? 1.f : 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-            for (int r = j + 1; r < 8; ++r) x[r] = fmaf(-a[r * (r - 1) / 2 + j], x[j], x[r]);
-        __syncwarp(0x0000FFFFu);   // the sub-block's coefficients are read before any column is overwritten
-#pragma unroll
-        for (int r = 0; r < 8; ++r) Am[(o8 + r) * TS + o8 + c] = x[r];
-    }
-    __syncwarp();
-    const int i = lane >> 2, c2 = 2 * (lane & 3);   // row i, columns c2, c2 + 1 of the 8 x 8 products
-    float r0 = 0.f, r1 = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float aik = Am[(o + 8 + i) * TS + o + k];
-        r0 = fmaf(aik, Am[(o + k) * TS + o + c2], r0);
-        r1 = fmaf(aik, Am[(o + k) * TS + o + c2 + 1], r1);
-    }
-    Rw[i * 8 + c2] = r0;
-    Rw[i * 8 + c2 + 1] = r1;
-    __syncwarp();   // A21 is read and R written by every lane
-    float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float tik = Am[(o + 8 + i) * TS + o + 8 + k];
-        t0 = fmaf(tik, Rw[k * 8 + c2], t0);
-        t1 = fmaf(tik, Rw[k * 8 + c2 + 1], t1);
-    }
-    Am[(o + 8 + i) * TS + o + c2] = -t0;
-    Am[(o + 8 + i) * TS + o + c2 + 1] = -t1;
-}
-
-// Blocked inverse of the unit lower-triangular (I + A), 64 x 64, in place: A (strictly lower, fp32, row stride
-// TS) is overwritten by T = (I + A)^{-1}.  Level 0: the four 16 x 16 diagonal blocks, one warp each.  Level 1:
-// the 16 x 16 blocks below them in the two 32 x 32 diagonal blocks, T21 = -T22 (A21 T11).
-// Level 2: the 32 x 32 block, T21 = -T22 (A21 T11) over 8 warps with a barrier between the two products.
-// (Level 1 runs on two warps per block, column halves, with a pair barrier before T21 overwrites A21.)
-// Levels 1 and 2 are TF32 warp-level tile products with fp32 accumulation.  The upper triangle of every
-// 32 x 32 diagonal block must hold zeros on entry (the epilogue writes them); the block above the diagonal
-// of the whole matrix is never read.  Every thread passes every barrier.
-__device__ void solve_unit_lower_inplace(float* Am, float* Rt, int t, bool work) {
-    const int w = t >> 5, lane = t & 31;
-    if (work && w < 4) solve_block16(Am, Rt + 64 * w, 16 * w, lane);
-    __syncthreads();
-    if (work && w < 4) {   // level 1: block pair pr, column half nt; R = A21 T11, then T21 = -T22 R
-        const int pr = w >> 1, nt = w & 1, o1 = 32 * pr;
-        float* Rw = Rt + 16 * pr * RS;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-            mma_tile_tf32(d, Am + (o1 + 16) * TS + o1 + 8 * ks, TS, Am + (o1 + 8 * ks) * TS + o1 + 8 * nt, TS, lane);
-        st_tile(Rw + 8 * nt, RS, d, lane, 1.f);
-        if (pr == 0) named_bar(1, 64);   // both column halves have read A21 before T21 overwrites it
-        else named_bar(2, 64);
-        float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-            mma_tile_tf32(e, Am + (o1 + 16) * TS + o1 + 16 + 8 * ks, TS, Rw + (8 * ks) * RS + 8 * nt, RS, lane);
-        st_tile(Am + (o1 + 16) * TS + o1 + 8 * nt, TS, e, lane, -1.f);
-    }
-    __syncthreads();
-    const int mt = w & 1, nq = w >> 1;   // level 2: 2 row tiles x 4 column tiles of 8
-    if (work) {   // R = A[32..63][0..31] T[0..31][0..31]
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            mma_tile_tf32(d, Am + (32 + 16 * mt) * TS + 8 * ks, TS, Am + (8 * ks) * TS + 8 * nq, TS, lane);
-        st_tile(Rt + (16 * mt) * RS + 8 * nq, RS, d, lane, 1.f);
-    }
-    __syncthreads();
-    if (work) {   // T[32..63][0..31] = -T[32..63][32..63] R
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            mma_tile_tf32(d, Am + (32 + 16 * mt) * TS + 32 + 8 * ks, TS, Rt + (8 * ks) * RS + 8 * nq, RS, lane);
-        st_tile(Am + (32 + 16 * mt) * TS + 8 * nq, TS, d, lane, -1.f);
-    }
-    __syncthreads();
-}
 
 // TMA loads of an item: K and Q as 2 x 2 boxes of 64 tokens x 64 columns; V as two boxes (GDN: into X's V slabs,
 // KDA: into its own tile, with the fp32 gate tile into X).
@@ -340,27 +173,6 @@ __device__ __forceinline__ void intra_load_gb(const IntraParams& p, const Item& 
         g[k] = (!KDA && r < x.L) ? act_gate(p.act, __ldg(p.g + tok), x.h) : 0.f;
         b[k] = r < x.L ? act_beta(p.act, __ldg(p.beta + tok)) : 0.f;
     }
-}
-
-// gate prefix of the item in gbuf (one warp, scalar gate)
-__device__ __forceinline__ void intra_gate_prefix(ISmall& S, int lane) {
-    const float LOG2E = 1.4426950408889634f;
-    const float g0 = S.gbuf[2 * lane], g1 = S.gbuf[2 * lane + 1];
-    float x = g0 + g1;
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, m);
-        if (lane >= m) x += y;
-    }
-    const float G1 = x * LOG2E, G0 = (x - g1) * LOG2E;
-    S.lg[2 * lane] = G0;
-    S.lg[2 * lane + 1] = G1;
-    const float Glast = __shfl_sync(0xffffffffu, G1, 31);
-    S.gam[2 * lane] = ex2(G0);
-    S.gam[2 * lane + 1] = ex2(G1);
-    S.kdec[2 * lane] = ex2(Glast - G0);
-    S.kdec[2 * lane + 1] = ex2(Glast - G1);
-    if (lane == 31) S.gC = ex2(Glast);
 }
 
 __device__ __forceinline__ uint4 scale_chunk_h(const float (&f)[8], float s, uint32_t m) {
@@ -601,7 +413,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    ISmall& S = *reinterpret_cast<ISmall*>(smem + (KDA ? I_SMALL_KDA : I_SMALL_GDN));
+    ISmall& S = *reinterpret_cast<ISmall*>(smem + I_SMALL_KDA);
     KSmall& KS = *reinterpret_cast<KSmall*>(smem + I_KSMALL);   // KDA only
     float* Am = reinterpret_cast<float*>(smem + I_AM);
     float* Rt = reinterpret_cast<float*>(smem + I_RT);
@@ -610,7 +422,6 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3;                       // TMEM lane quarter of this warp
     const int pw = warp >> 2;                      // which of the two warps on this quarter (64-column half)
-    const int row = 32 * q4 + lane;                // TMEM lane this thread reads
     const bool leader = (tid == 0);
     const bool loader = (tid == 64);
     const int H = p.geo.H;
@@ -674,86 +485,12 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const int L = it.L;
         __syncthreads();   // [A] g and beta of this item are in shared memory; the previous item is retired
         if (warp == 1) {
-            if (!KDA) intra_gate_prefix(S, lane);
             if (have_next) intra_load_gb<KDA>(p, nx, lane, ng, nb);
         }
         if (ok) ok = mbar_wait(&S.full_kq, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(1u);
         if (ok && loader) kq_waited = ic + 1;
-        if constexpr (!KDA) {
-            // MMA0: D0 = [K; Q] K^T
-            if (ok && leader) {
-                tc_fence_after();
-                const uint32_t id = idesc_f16(128, 64, true, false, false);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t a = sbase + I_KQ + (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_f16(tmem + I_TM_D0, sdesc(a, 16, 1024), sdesc(a, 16, 1024), id, ks > 0);
-                }
-                mma_commit(&S.m0);
-            }
-            if (lane == 0) bulk_wait_read();   // the previous item's staging rows (X, A1) have been read
-            __syncthreads();   // [B] gate prefix ready
-            if (ok) {
-                // beta gamma K -> X slabs 2-3, Ktilde = (gamma_C / gamma) K and Q^ = scale gamma Q -> workspace.
-                // Operation e = tid + 256 cc moves the 16 bytes at physical position (slab, row, pos) of the K and Q
-                // tiles; consecutive lanes take consecutive positions, so the workspace writes are coalesced (the
-                // layouts share the swizzle).
-                uint8_t* kt = ws.kt + (size_t)it.it * WS_KT;
-                uint8_t* wq = ws.wq + (size_t)it.it * WS_WQ;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int e = tid + 256 * cc, slab = e >> 9, r = (e >> 3) & 63;
-                    const uint32_t off = (uint32_t)(r * 128 + (e & 7) * 16);
-                    const uint32_t m = r < L ? 0xFFFFFFFFu : 0u;   // exact zeros for rows past the end
-                    float f[8], g8[8];
-                    bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + off), f);
-                    bf16x8_to_f32(ld16(smem + I_KQ + slab * 16384 + 8192 + off), g8);
-                    const uint4 xk = scale_chunk_h(f, S.bbuf[r] * S.gam[r], m), kd = scale_chunk_h(f, S.kdec[r], m);
-                    const uint4 qh = scale_chunk_h(g8, p.scale * S.gam[r], m);
-                    st16(smem + I_B2 + 16384 + slab * 8192 + off, xk.x, xk.y, xk.z, xk.w);
-                    stg16(kt + slab * 8192 + off, kd.x, kd.y, kd.z, kd.w);
-                    stg16(wq + slab * 16384 + off, qh.x, qh.y, qh.z, qh.w);
-                }
-                if (warp == 3) {
-                    const float gc = S.gC;
-                    __stcg(reinterpret_cast<float4*>(ws.gc + (size_t)it.it * 128) + lane, make_float4(gc, gc, gc, gc));
-                }
-            }
-            if (ok) ok = mbar_wait(&S.full_v, par, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok && tid == 0) set_status(2u);
-            if (ok && loader) v_waited = ic + 1;
-            if (ok) {
-                // beta V in place in X slabs 0-1
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int e = tid + 256 * cc, r = (e >> 3) & 63;
-                    uint8_t* pv = smem + I_B2 + (e >> 9) * 8192 + r * 128 + (e & 7) * 16;
-                    float f[8];
-                    bf16x8_to_f32(ld16(pv), f);
-                    const uint4 xv = scale_chunk_h(f, S.bbuf[r], r < L ? 0xFFFFFFFFu : 0u);
-                    st16(pv, xv.x, xv.y, xv.z, xv.w);
-                }
-            }
-            fence_async_smem();
-            tmem_st_wait();
-            if (ok && leader) ok = mbar_wait(&S.m0, par, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);   // warp-uniform, as the warp-collective TMEM accesses need
-            if (!ok && leader) set_status(4u);
-            tc_fence_before();
-            __syncthreads();   // [C] D0 ready; K and Q are dead
-            tc_fence_after();
-            if (ok && loader && have_next) {
-                intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx, p.group);
-                kq_issued = ic + 2;
-            }
-            if (ok) epilogue_kkt<false>(tl + I_TM_D0, row, q4, pw, S.lg, S.bbuf, p.scale, Am, smem + I_A1);
-            fence_async_smem();   // P (rows 64-127 of A1) is read by the bulk copy to the workspace
-            tc_fence_before();
-            __syncthreads();
-        } else {
             if (ok) ok = mbar_wait(&S.full_v, par, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok && tid == 0) set_status(2u);
@@ -827,7 +564,6 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx, p.group);
                 kq_issued = ic + 2;
             }
-        }
         // P (rows 64-127 of A1, fp16 K-major) to the workspace, one bulk copy; its rows are overwritten with T below
         if (ok && tid == 96) {
             bulk_s2g(ws.pp + (size_t)it.it * WS_P, smem + I_A1 + 8192, WS_P);
@@ -1017,8 +753,9 @@ __device__ __forceinline__ void state_issue(uint8_t* smem, SSmall& S, const Ws& 
 // O = Q^ h~ + P Delta of chunk t (token rows 0-63: lane quarters 0 and 1), columns cs .. cs + 31 of the half, from
 // D3 and D5 of its parity
 template <bool O_F32>
-__device__ __forceinline__ void state_output(const StateParams& p, const Chain& ch, uint32_t tl, int t, int row,
+__device__ __forceinline__ bool state_output(const StateParams& p, const Chain& ch, uint32_t tl, int t, int row,
                                              int cs) {
+    bool finite = true;
     using LY = SLayout;
     const int L = min(C, ch.len - t * C);
     const size_t orow = ((size_t)(ch.row0 + (long)t * C + row) * p.geo.H + ch.h) * DV + ch.half * DVT;
@@ -1035,7 +772,10 @@ __device__ __forceinline__ void state_output(const StateParams& p, const Chain& 
             for (int hq = 0; hq < 2; ++hq) {
                 float f[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) f[k] = __uint_as_float(a[hq][k]) + __uint_as_float(b[hq][k]);
+                for (int k = 0; k < 16; ++k) {
+                    f[k] = __uint_as_float(a[hq][k]) + __uint_as_float(b[hq][k]);
+                    finite = finite && isfinite(f[k]);
+                }
                 const size_t o0 = orow + h2 * 32 + hq * 16;
                 if (O_F32) {
                     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + o0);
@@ -1057,6 +797,7 @@ __device__ __forceinline__ void state_output(const StateParams& p, const Chain& 
             }
         }
     }
+    return finite;
 }
 
 template <bool O_F32>
@@ -1129,6 +870,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     const uint64_t dP = sdesc(sbase + LY::PP, 16, 1024);
     const uint32_t id3 = idesc_f16(128, 64, false, false, true), id4 = idesc_f16(128, 64, false, true, true);
     bool ok = true;
+    bool finite = true;   // every value this thread wrote to o and the final state is finite
     int waited = 0;   // chunks whose stage wait completed
     for (int t = 0; t < n_chunks; ++t) {
         const int s = t & 1;
@@ -1148,7 +890,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
             mma_commit(&S.m3);
         }
         // meanwhile the output of the previous chunk (its D3 and D5 are the other parity)
-        if (ok && out_warp && t > 0) state_output<O_F32>(p, ch, tl, t - 1, row, cs);
+        if (ok && out_warp && t > 0) finite = state_output<O_F32>(p, ch, tl, t - 1, row, cs) && finite;
         if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(64u);
@@ -1215,7 +957,7 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     }
     if (ok && out_warp && n_chunks > 0) {
         tc_fence_after();
-        state_output<O_F32>(p, ch, tl, n_chunks - 1, row, cs);
+        finite = state_output<O_F32>(p, ch, tl, n_chunks - 1, row, cs) && finite;
     }
     // stages issued but never waited on (after a timeout) must land before the CTA exits
     if (issuer) {
@@ -1226,7 +968,10 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
         for (int q = 0; q < 8; ++q)
             reinterpret_cast<float4*>(p.hT + sidx)[q] =
                 make_float4(hreg[4 * q], hreg[4 * q + 1], hreg[4 * q + 2], hreg[4 * q + 3]);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) finite = finite && isfinite(hreg[k]);
     }
+    if (__any_sync(0xffffffffu, !finite) && lane == 0) set_status(kStatusNonfinite);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1250,11 +995,13 @@ const char* two_pass_unsupported_reason(const ChunkArgs& a) {
 }
 
 size_t two_pass_workspace_bytes(const ChunkArgs& a) {
+    if (!a.per_channel) return gdn_tmem_workspace_bytes(a);
     if ((long)a.B * a.T == 0) return 0;
     return (size_t)n_slots(a) * a.H * WS_ITEM;
 }
 
 cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+    if (!a.per_channel) return launch_chunk_gdn_tmem(a, workspace, workspace_bytes, s);
     const long chains = (long)a.N() * a.H;
     if (chains == 0) return cudaSuccess;
     if (!device_is_sm100_family()) return cudaErrorNoKernelImageForDevice;
@@ -1290,21 +1037,12 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     IntraParams ip{geo, a.g, a.beta, a.scale, n_slots(a), ws, a.act, a.H / a.HK()};
-    if (a.per_channel) {
-        CUtensorMap mg;
-        if (!make_map_f32_rows(&mg, a.g, rows, a.H, DK)) return cudaErrorInvalidValue;
-        e = cudaFuncSetAttribute(chunk_intra_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)I_SMEM_KDA);
-        if (e != cudaSuccess) return e;
-        const long grid1 = items < sms ? items : sms;
-        chunk_intra_kernel<true><<<(unsigned)grid1, I_THREADS, I_SMEM_KDA, s>>>(mq, mk, mv, mg, ip);
-    } else {
-        e = cudaFuncSetAttribute(chunk_intra_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)I_SMEM_GDN);
-        if (e != cudaSuccess) return e;
-        const long grid1 = items < 2L * sms ? items : 2L * sms;
-        chunk_intra_kernel<false><<<(unsigned)grid1, I_THREADS, I_SMEM_GDN, s>>>(mq, mk, mv, mv, ip);
-    }
+    CUtensorMap mg;
+    if (!make_map_f32_rows(&mg, a.g, rows, a.H, DK)) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(chunk_intra_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)I_SMEM_KDA);
+    if (e != cudaSuccess) return e;
+    const long grid1 = items < sms ? items : sms;
+    chunk_intra_kernel<true><<<(unsigned)grid1, I_THREADS, I_SMEM_KDA, s>>>(mq, mk, mv, mg, ip);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

@@ -65,35 +65,38 @@ cudaError_t launch_chunk_generic(const ChunkArgs& a, cudaStream_t s);
 size_t generic_smem_bytes(const ChunkArgs& a);
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;
 
-// Fused tcgen05/TMA chunk kernel for the scalar gate (chunk_tc.cu).
-// Returns nullptr if the request fits the kernel, else a reason.
-const char* tc_chunk_unsupported_reason(const ChunkArgs& a);
-cudaError_t launch_chunk_tc(const ChunkArgs& a, cudaStream_t s);
-
-// Two-pass tcgen05 chunk path (chunk_two_pass.cu): a per-chunk kernel over all SMs writes the
-// S-independent products to a workspace, then a state kernel walks each chain.
+// Two-pass tcgen05 chunk path.  The per-channel gate (chunk_two_pass.cu): a per-chunk kernel over all SMs writes the
+// state-independent products to a workspace, then a state kernel walks each (chain, d_v half).  The scalar gate
+// (chunk_gdn_tmem.cu): a per-chunk kernel writes -W, P and T diag(beta), then a transposed state kernel walks each
+// chain with its chain operands in tensor memory.  launch_chunk_two_pass and two_pass_workspace_bytes pick the pair.
 const char* two_pass_unsupported_reason(const ChunkArgs& a);
 size_t two_pass_workspace_bytes(const ChunkArgs& a);
 cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s);
+size_t gdn_tmem_workspace_bytes(const ChunkArgs& a);
+cudaError_t launch_chunk_gdn_tmem(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s);
 // The statically allocated two-pass workspace: its size, and its device address on the current device (looked up
 // once per device with cudaGetSymbolAddress).
 size_t static_workspace_capacity();
 cudaError_t static_workspace(void** ptr);
 
-// Shared host helpers of the tcgen05 paths (chunk_tc.cu).
+// Host helpers of the tcgen05 paths (tensor_map.cu).
 // TMA map of a [rows][H][d] bf16 tensor, box 64 elements x 1 head x 64 rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, long rows, int H, int d);
 // TMA map of a [rows][H][d] fp32 tensor (d <= 256), box d x 1 head x 64 rows, no swizzle: a 64-row tile lands
 // as a dense row-major [64][d] block.
 bool make_map_f32_rows(CUtensorMap* m, const float* base, long rows, int H, int d);
+// The same for fp32 or bf16 (f32 false), for loads and stores.
+bool make_map_rows(CUtensorMap* m, const void* base, long rows, int H, int d, bool f32);
 bool device_is_sm100_family();
 
 // Decode step (recurrent_step.cu).
 cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t s);
 
-// Device-side status words of kernels with bounded waits.
-cudaError_t tc_read_and_clear_status(unsigned* value, bool clear);
+// Device-side status words of the kernels with bounded waits.  Bits 0-7 and 9-15: a wait that gave up; bit 8
+// (kStatusNonfinite): a chunk-forward state kernel wrote a non-finite value to o or the final state.
+constexpr unsigned kStatusNonfinite = 1u << 8;
 cudaError_t tp_read_and_clear_status(unsigned* value, bool clear);
+cudaError_t gt_read_and_clear_status(unsigned* value, bool clear);
 
 // One chunk-backward request, already validated by api.cu.  Gradients are of
 // L = <dO, o> + <dhT, final state> with respect to every input of the forward.

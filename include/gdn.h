@@ -58,7 +58,8 @@ typedef enum gdn_status {
     GDN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, inconsistent flags: nothing launched */
     GDN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement: nothing launched */
     GDN_ERR_CUDA = 3,         /* a CUDA runtime call failed (device query, attribute, launch) */
-    GDN_ERR_TIMEOUT = 4       /* a kernel's bounded wait gave up (see gdn_device_status) */
+    GDN_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (see gdn_device_status) */
+    GDN_ERR_NONFINITE = 5     /* a chunk forward wrote a non-finite value (see gdn_device_status) */
 } gdn_status;
 
 typedef enum gdn_dtype {
@@ -73,13 +74,22 @@ typedef enum gdn_algo {
                                tiles fit one CTA's shared memory (d_k = 256: chunk 64 for the
                                scalar gate, chunk <= 32 for the per-channel gate);
                                GDN_ERR_UNSUPPORTED otherwise */
-    GDN_ALGO_TCGEN05 = 2,   /* fused tcgen05/TMA kernel (one CTA per chain does every stage):
-                               bf16, d_k = d_v = 128, chunk 64, scalar gate;
-                               GDN_ERR_UNSUPPORTED when the request does not fit it */
+    GDN_ALGO_TCGEN05 = 2,   /* retired (an earlier single-launch kernel, slower than the two-pass
+                               path): always GDN_ERR_UNSUPPORTED */
     GDN_ALGO_TWO_PASS = 3   /* tcgen05 in two passes: a per-chunk kernel over all SMs writes the
                                state-independent products to a device workspace, then a state
                                kernel walks each chain.  bf16, d_k = d_v = 128, chunk 64;
-                               GDN_ERR_UNSUPPORTED when the request does not fit it */
+                               GDN_ERR_UNSUPPORTED when the request does not fit it.
+                               Range: these kernels round some intermediates to fp16, whose
+                               largest finite value is 65,504: the k and v values (scalar
+                               gate), the per-chunk products P = scale (Gamma * Q K^T),
+                               T diag(beta) and the corrections Delta = U - W S^T of every
+                               chunk (per-channel gate also scale gamma Q, the decayed keys,
+                               W, U and T).  With unit-norm q and k, beta in (0, 2) and |v|
+                               up to about 1e3 they stay far inside it.  A value past it turns
+                               into inf, and o or the final state then holds a non-finite
+                               value: the state kernels check everything they write and
+                               gdn_device_status reports GDN_ERR_NONFINITE. */
 } gdn_algo;
 
 /*
@@ -246,9 +256,11 @@ gdn_status kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const f
  * stream-ordered memory: the call allocates and frees nothing.  The pages
  * describe no counterpart; this entry point exists for callers that must not
  * allocate (for example inside a captured graph's replay loop).
- *   Limit: the static scratch holds 64 MiB, i.e. (floor(B*T / 64) + N + 1) * H
- *   * 74,240 bytes must not exceed 67,108,864 (about 900 (chunk, head) items,
- *   e.g. one 4096-token sequence with 12 heads).  A larger request returns
+ *   Limit: the static scratch holds 64 MiB: (floor(B*T / 64) + N + 1) * H
+ *   records of gdn_chunk_workspace_size's per-item size (32,768 bytes for the
+ *   scalar gate, 74,240 for the per-channel gate) must fit in 67,108,864
+ *   bytes: 2,048 scalar-gate items (e.g. one 4096-token sequence with 31
+ *   heads) or 903 per-channel ones (e.g. 13 heads).  A larger request returns
  *   GDN_ERR_UNSUPPORTED with the sizes in the message and launches nothing.
  *   Sharing: every call on a device uses the same scratch, so calls whose work
  *   can overlap (different streams, or threads without ordering) race and give
@@ -318,7 +330,7 @@ gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const
  * The buffers are assumed to be 16-byte aligned.  per_channel nonzero stands
  * for kda_chunk_fwd; varlen nonzero stands for a call with cu_seqlens.
  * requested is resolved into *chosen: GDN_ALGO_AUTO becomes
- * GDN_ALGO_TWO_PASS, GDN_ALGO_TCGEN05 or GDN_ALGO_GENERIC.  The status is the one the call
+ * GDN_ALGO_TWO_PASS or GDN_ALGO_GENERIC.  The status is the one the call
  * itself would return for these sizes, and *chosen is written only on GDN_OK.
  * Nothing is launched.
  */
@@ -330,10 +342,12 @@ gdn_status gdn_chunk_plan(int per_channel, int B, int T, int H, int d_k, int d_v
  * gdn_chunk_workspace_size -- device workspace bytes of a chunk-forward call
  * with these sizes and kernel request (0 when the resolved kernel needs
  * none).  n_seqs is 0 for a call without cu_seqlens, else its number of
- * packed sequences.  The two-pass kernels keep, per (chunk slot, head),
- * 74,240 bytes: [Q^; W] (Q^ = scale gamma Q), Ktilde, U and P in fp16, and
- * gamma_C; there are
- * floor(B*T / 64) + N + 1 slots.  Same status rules as gdn_chunk_plan.
+ * packed sequences.  The two-pass kernels keep a record per (chunk slot,
+ * head): for the scalar gate 32,768 bytes (-W in bf16, P and T diag(beta) in
+ * fp16, with W = T diag(beta gamma) K); for the per-channel gate 74,240 bytes
+ * ([Q^; W] with Q^ = scale gamma Q, Ktilde, U and P in fp16, and gamma_C).
+ * There are floor(B*T / 64) + N + 1 slots.  Same status rules as
+ * gdn_chunk_plan.
  */
 gdn_status gdn_chunk_workspace_size(int per_channel, int B, int T, int H, int d_k, int d_v, int chunk_size,
                                     gdn_dtype dtype, gdn_dtype o_dtype, int n_seqs, gdn_algo requested,
@@ -455,10 +469,13 @@ const char* gdn_last_error(void);
 
 /*
  * Device-side status of the kernels that use bounded waits (the tcgen05 paths
- * and the chunk backward's state walks).
- * Synchronises the current device.  It returns GDN_OK, or GDN_ERR_TIMEOUT if
- * any CTA gave up a bounded wait since the status was last cleared.  A CTA
- * that gives up drops its work and its outputs are unspecified.  With clear
+ * and the chunk backward's state walks) and of the chunk forward's output
+ * check.  Synchronises the current device.  It returns GDN_OK;
+ * GDN_ERR_TIMEOUT if any CTA gave up a bounded wait since the status was last
+ * cleared (a CTA that gives up drops its work and its outputs are
+ * unspecified); else GDN_ERR_NONFINITE if a two-pass chunk forward wrote a
+ * non-finite value to o or the final state (an fp16 intermediate passed
+ * 65,504, see GDN_ALGO_TWO_PASS, or an input was not finite).  With clear
  * nonzero, the status is reset.  GDN_ERR_CUDA if the query itself failed.
  */
 gdn_status gdn_device_status(int clear);

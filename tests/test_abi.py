@@ -97,12 +97,16 @@ def test_plan_and_workspace_sizes(lib):
     bf = torch.bfloat16
     # the prefill shape resolves to the two-pass tcgen05 path; fp32 and small heads to the generic kernel
     assert _binding.chunk_plan(False, 4, 4096, 16, 128, 128, 64, bf) == "two_pass"
-    assert _binding.chunk_plan(False, 4, 4096, 16, 128, 128, 64, bf, algo="tcgen05") == "tcgen05"
+    assert _binding.chunk_plan(True, 2, 8192, 32, 128, 128, 64, bf) == "two_pass"
     assert _binding.chunk_plan(False, 1, 64, 1, 16, 16, 16, torch.float32) == "generic"
-    # 74,240 bytes per (chunk slot, head); floor(B T / 64) + N + 1 slots
-    assert _binding.workspace_size(False, 4, 4096, 16, 128, 128, 64, bf) == (256 + 4 + 1) * 16 * 74240
-    assert _binding.workspace_size(False, 1, 65536, 32, 128, 128, 64, bf, n_seqs=8) == (1024 + 8 + 1) * 32 * 74240
-    assert _binding.workspace_size(False, 4, 4096, 16, 128, 128, 64, bf, algo="tcgen05") == 0
+    with pytest.raises(_binding.GdnError) as err:      # the retired single-launch kernel is refused
+        _binding.chunk_plan(False, 4, 4096, 16, 128, 128, 64, bf, algo="tcgen05")
+    assert err.value.status == 2 and "retired" in str(err.value)
+    # per (chunk slot, head): 32,768 bytes for the scalar gate, 74,240 for the per-channel gate;
+    # floor(B T / 64) + N + 1 slots
+    assert _binding.workspace_size(False, 4, 4096, 16, 128, 128, 64, bf) == (256 + 4 + 1) * 16 * 32768
+    assert _binding.workspace_size(False, 1, 65536, 32, 128, 128, 64, bf, n_seqs=8) == (1024 + 8 + 1) * 32 * 32768
+    assert _binding.workspace_size(True, 2, 8192, 32, 128, 128, 64, bf) == (256 + 2 + 1) * 32 * 74240
     assert _binding.workspace_size(False, 1, 64, 1, 16, 16, 16, torch.float32) == 0
     with pytest.raises(_binding.GdnError):
         _binding.workspace_size(False, 1, 64, 1, 64, 64, 64, bf, algo="two_pass")
@@ -118,7 +122,7 @@ def _chunk_ws(lib, ws, ws_bytes, **kw):
 
 
 def test_workspace_argument_checks(lib):
-    need = (1 + 1 + 1) * 1 * 74240
+    need = (1 + 1 + 1) * 1 * 32768
     assert _chunk_ws(lib, FAKE, need - 16) == 1            # too small
     assert "workspace" in _binding.last_error()
     assert _chunk_ws(lib, FAKE + 16, need) == 1            # not 256-byte aligned

@@ -67,14 +67,18 @@ def test_traffic_record_follows_the_code_not_the_comments():
 
 def test_roofline_counts_of_the_headline_workloads():
     # the algorithmic bytes and flops the bench divides by time, against the figures worked out by hand:
-    # prefill: 262,144 token-heads x (3 x 256 B bf16 q, k, v + 512 B fp32 o + 4 B g + 4 B beta) plus 64 states
-    # of 64 KiB read and written; backward: per chunk-head of 16 rows, 3 C^2 d_k (Q K^T, K K^T, the dQ / dK pair
+    # prefill, the survey's count (o in bf16): 262,144 token-heads x (3 x 256 B bf16 q, k, v + 256 B o + 4 B g + 4 B
+    # beta) plus 64 states of 64 KiB read and written, 278,921,216 B; with o counted as the fp32 the call writes,
+    # 512 B of o per token-head; backward: per chunk-head of 16 rows, 3 C^2 d_k (Q K^T, K K^T, the dQ / dK pair
     # sums) + 8 C d_k d_v (Z, the state update, dDelta, the state gradient x 2, the three state products) +
     # 2.5 C^2 d_v (the two solves, P^T dO, dP and dA) multiply-adds over 16,384 chunk-heads
     sys.path.insert(0, ROOT)
     import bench
     from gated_delta_rule_gdn_gb300 import workloads as W
-    assert bench._alg_bytes(W.config(1)) == 262_144 * 1288 + 64 * 2 * 65_536 == 346_030_080
+    assert bench._alg_bytes(W.config(1)) == 262_144 * 1032 + 64 * 2 * 65_536 == 278_921_216
+    assert bench._alg_bytes(W.config(1), 4) == 262_144 * 1288 + 64 * 2 * 65_536 == 346_030_080
+    # KDA: the per-channel gate adds 4 (d_k - 1) B per token-head; no initial state, so the state is written only
+    assert bench._alg_bytes(W.config(3)) == 524_288 * (1032 + 4 * 127) + 64 * 65_536 == 811_597_824
     macs = 3 * 16 * 16 * 128 + 8 * 16 * 128 * 128 + 5 * 16 * 16 * 128 // 2
     assert macs == 2_277_376
     assert bench._bwd_flops(W.config(1), 16) == 2 * macs * 16_384 == 74_625_056_768

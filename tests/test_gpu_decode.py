@@ -130,9 +130,8 @@ def test_decode_with_in_kernel_gate_and_beta_activation():
                                    dt_bias=torch.from_numpy(dt_bias).cuda(), beta_sigmoid=True)
         outs.append(o.reshape(NH, -1).float().cpu())
         qs.append(x["q"].reshape(NH, -1)); ks.append(x["k"].reshape(NH, -1)); vs.append(x["v"].reshape(NH, -1))
-        gs.append(torch.from_numpy(-np.exp(A_log.astype(np.float64))[None, :]
-                                   * np.logaddexp(0.0, gl.astype(np.float64) + dt_bias[None, :])).reshape(NH, 1))
-        bs.append(torch.from_numpy(1.0 / (1.0 + np.exp(-bl.astype(np.float64)))).reshape(NH, 1))
+        gs.append(torch.from_numpy(oracle.gate_activation(gl, A_log, dt_bias)).reshape(NH, 1))
+        bs.append(torch.from_numpy(oracle.beta_activation(bl)).reshape(NH, 1))
     torch.cuda.synchronize()
     assert gdn.device_status() == 0
     q, k, v = (torch.stack(t, dim=1)[:, :, None] for t in (qs, ks, vs))
@@ -195,7 +194,7 @@ def test_decode_beta_in_zero_two_from_logits(kind):
         outs.append(o.reshape(NH, -1).float().cpu())
         qs.append(x["q"].reshape(NH, -1)); ks.append(x["k"].reshape(NH, -1)); vs.append(x["v"].reshape(NH, -1))
         gs.append(x["g"].reshape(NH, -1))
-        bs.append(torch.from_numpy(2.0 / (1.0 + np.exp(-bl.astype(np.float64)))).reshape(NH, 1))
+        bs.append(torch.from_numpy(oracle.beta_activation(bl, 2)).reshape(NH, 1))
     torch.cuda.synchronize()
     assert gdn.device_status() == 0
     q, k, v = (torch.stack(t, dim=1)[:, :, None] for t in (qs, ks, vs))
