@@ -448,6 +448,34 @@ __device__ __forceinline__ void tmem_st_zero16(uint32_t taddr) {
     tmem_st16(taddr, z);
 }
 
+// One 16 KB tile (two 64-column bf16 slabs of 64 rows, 128-byte swizzled) to fp16 in place by NTHR threads; rows past
+// the end become zeros.  `stride` is the distance of the second slab.  The loads of a batch of 8 chunks are issued
+// before their stores, so that their latencies overlap.
+template <int NTHR>
+__device__ __forceinline__ void tile_to_f16(uint8_t* base, uint32_t stride, int L, int idx) {
+    constexpr int PER = 1024 / NTHR, BATCH = PER < 8 ? PER : 8;
+#pragma unroll 1
+    for (int u0 = 0; u0 < PER; u0 += BATCH) {
+        uint4 v[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int e = idx + NTHR * (u0 + u);
+            v[u] = ld16(base + (e >> 9) * stride + (e & 511) * 16);
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int e = idx + NTHR * (u0 + u);
+            const bool zero = ((e >> 3) & 63) >= L;
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                o[i] = zero ? 0u : pack_h2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+            st16(base + (e >> 9) * stride + (e & 511) * 16, o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
 template <bool O_F32>
 __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_constant__ CUtensorMap tmap_q,
                                                                    const __grid_constant__ CUtensorMap tmap_k,
@@ -480,9 +508,9 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             mbar_init(&S.emptyU[s], 1);
             mbar_init(&S.emptyQ[s], 1);
             mbar_init(&S.emptyK[s], 1);
-            mbar_init(&S.convU[s], 2);
-            mbar_init(&S.convQ[s], 2);
-            mbar_init(&S.convK[s], 2);
+            mbar_init(&S.convU[s], 1);
+            mbar_init(&S.convQ[s], GL::LW / 32);
+            mbar_init(&S.convK[s], 1);
         }
         mbar_init(&S.m3, 1);
         mbar_init(&S.m4, 1);
@@ -525,14 +553,30 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.hready);
         }
+        // Q of chunk u to fp16 in place (rows past the end: zeros), in the lane warps' wait for MMA4
+        auto convert_q = [&](int u) -> bool {
+            const int su = u & 1;
+            bool okc = mbar_wait(&S.fullQ[su], (u >> 1) & 1, kWaitNs);
+            okc = __all_sync(0xffffffffu, okc);
+            if (!okc) return false;
+            tile_to_f16<GL::LW>(smem + su * GL::STAGE + GL::QW + 8192, 16384, min(C, ch.len - u * C), tid);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.convQ[su]);
+            return true;
+        };
+        if (n_chunks > 0 && !convert_q(0)) {
+            ok = false;
+            if (lane == 0) gt_status(1u << 15);
+        }
         bool finite = true;
-        for (int t = 0; t < n_chunks; ++t) {
+        for (int t = 0; t < n_chunks && ok; ++t) {
             const int s = t & 1;
             const GVec& V = vec[t & 3];
             const uint32_t d3 = tl + GL::TM_D3 + 128 * s;
             // Delta epilogue: Delta^T (columns 32 hf .. + 31 of D3) -> fp16 Delta^T and decayed Delta^T, in place:
             // Delta at columns 32 hf .. + 15, the decayed copy at 32 hf + 16 .. + 31
-            if (ok) ok = mbar_spin(&S.m3, t & 1, kWaitNs);
+            if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
             if (ok) ok = mbar_wait(&S.vready[t & 3], (t >> 2) & 1, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -562,8 +606,13 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.dready);
+            if (t + 1 < n_chunks && !convert_q(t + 1)) {   // while MMA4 runs
+                ok = false;
+                if (lane == 0) gt_status(1u << 15);
+                break;
+            }
             // state update: h <- gamma_C h + D4 (columns 64 hf .. + 63), h~^T back to tensor memory
-            if (ok) ok = mbar_spin(&S.m4, t & 1, kWaitNs);
+            if (ok) ok = mbar_wait(&S.m4, t & 1, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0) gt_status(32u);
@@ -769,25 +818,23 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             for (int t = (issK > 2 ? issK - 2 : 0); t < issK; ++t) mbar_wait(&S.fullK[t & 1], (t >> 1) & 1, kWaitNs);
         }
     } else {
-        // ---------------------------------------------------------------- converters (warps 10, 11)
-        const int ct = tid - 320;           // 0 .. 63
-        const bool gwarp = (warp == 10);
-        float gn[2] = {0.f, 0.f};
-        auto load_g = [&](int t, float (&gg)[2]) {
-            const int Lt = min(C, ch.len - t * C);
+        // ---------------------------------------------------------------- warp 10: the gate vectors and K to fp16;
+        // warp 11: V to fp16
+        if (warp == 10) {
+            float gn[2] = {0.f, 0.f};
+            auto load_g = [&](int t, float (&gg)[2]) {
+                const int Lt = min(C, ch.len - t * C);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int r = lane + 32 * k;
-                gg[k] = r < Lt ? act_gate(p.act, __ldg(p.g + (size_t)(ch.row0 + (long)t * C + r) * H + ch.h), ch.h) : 0.f;
-            }
-        };
-        if (gwarp && n_chunks > 0) load_g(0, gn);
-        for (int t = 0; t < n_chunks; ++t) {
-            const int s = t & 1;
-            const int L = min(C, ch.len - t * C);
-            uint8_t* st = smem + s * GL::STAGE;
-            if (gwarp) {
-                // gate vectors of chunk t
+                for (int k = 0; k < 2; ++k) {
+                    const int r = lane + 32 * k;
+                    gg[k] = r < Lt ? act_gate(p.act, __ldg(p.g + (size_t)(ch.row0 + (long)t * C + r) * H + ch.h), ch.h) : 0.f;
+                }
+            };
+            if (n_chunks > 0) load_g(0, gn);
+            for (int t = 0; t < n_chunks; ++t) {
+                const int s = t & 1;
+                // the gate vectors of chunk t (ring slot t % 4: its chunk t - 4 was read before the K tile of chunk t - 2
+                // could be refilled, which this warp waited for below)
                 S.gbuf[lane] = gn[0];
                 S.gbuf[lane + 32] = gn[1];
                 __syncwarp();
@@ -802,51 +849,31 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.vready[t & 3]);
                 if (t + 1 < n_chunks) load_g(t + 1, gn);
+                if (ok) ok = mbar_wait(&S.fullK[s], (t >> 1) & 1, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) gt_status(8192u);
+                    break;
+                }
+                tile_to_f16<32>(smem + s * GL::STAGE + GL::KF, 8192, min(C, ch.len - t * C), lane);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.convK[s]);
             }
-            if (ok) ok = mbar_wait(&S.fullU[s], (t >> 1) & 1, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) gt_status(4096u);
-                break;
+        } else {
+            for (int t = 0; t < n_chunks; ++t) {
+                const int s = t & 1;
+                if (ok) ok = mbar_wait(&S.fullU[s], (t >> 1) & 1, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) gt_status(4096u);
+                    break;
+                }
+                tile_to_f16<32>(smem + s * GL::STAGE + GL::VF, 8192, min(C, ch.len - t * C), lane);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.convU[s]);
             }
-            // V -> fp16 in place (rows past the end: zeros)
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int e = ct + 64 * u, r = (e >> 3) & 63;
-                bf16_to_f16_inplace(st + GL::VF + (e >> 9) * 8192 + (e & 511) * 16, r >= L);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.convU[s]);
-            if (ok) ok = mbar_wait(&S.fullQ[s], (t >> 1) & 1, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) gt_status(1u << 15);
-                break;
-            }
-            // Q -> fp16 in place: rows 64-127 of the two [-W; Q] slabs
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int e = ct + 64 * u, r = (e >> 3) & 63;
-                bf16_to_f16_inplace(st + GL::QW + (e >> 9) * 16384 + 8192 + (e & 511) * 16, r >= L);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.convQ[s]);
-            if (ok) ok = mbar_wait(&S.fullK[s], (t >> 1) & 1, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) gt_status(8192u);
-                break;
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int e = ct + 64 * u, r = (e >> 3) & 63;
-                bf16_to_f16_inplace(st + GL::KF + (e >> 9) * 8192 + (e & 511) * 16, r >= L);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.convK[s]);
         }
     }
     tc_fence_before();
