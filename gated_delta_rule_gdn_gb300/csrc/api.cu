@@ -140,6 +140,8 @@ gdn_status chunk_common(const void* q, const void* k, const void* v, const float
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (chosen == GDN_ALGO_TWO_PASS) {
+        if (gdn::take_test_injection(GDN_TEST_FWD_RECORD_STALL)) a.test_fwd = 1;
+        else if (!a.per_channel && gdn::take_test_injection(GDN_TEST_FWD_ONE_STAGE)) a.test_fwd = 2;
         const size_t need = gdn::two_pass_workspace_bytes(a);
         if (workspace && workspace_bytes < need)
             return fail(GDN_ERR_INVALID_ARG, "%s: workspace of %zu bytes is smaller than the %zu needed", fn,
@@ -244,10 +246,10 @@ gdn_status check_bwd(gdn::BwdArgs& a, gdn_dtype dtype, gdn_dtype do_dtype, const
 }  // namespace
 
 namespace gdn {
-int take_test_injection() {
-    const int v = g_test_injection;
+bool take_test_injection(int what) {
+    if (g_test_injection != what) return false;
     g_test_injection = 0;
-    return v;
+    return true;
 }
 }  // namespace gdn
 
@@ -468,7 +470,7 @@ gdn_status gdn_chunk_bwd_ex(int per_channel, const void* q, const void* k, const
         if (e != cudaSuccess) return cuda_fail(e, fn);
     }
     a.ck = static_cast<float*>(ws);
-    a.test_skip_record = gdn::take_test_injection() == GDN_TEST_BWD_RECORD_STALL ? 1 : 0;
+    a.test_skip_record = gdn::take_test_injection(GDN_TEST_BWD_RECORD_STALL) ? 1 : 0;
     if (a.HK() < a.H) {
         a.gq_part = reinterpret_cast<float*>(static_cast<char*>(ws) + gdn::bwd_part_offset(a));
         a.gk_part = a.gq_part + (size_t)a.B * a.T * a.H * a.dk;
@@ -544,7 +546,8 @@ gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, in
 }
 
 gdn_status gdn_test_inject(int what) {
-    if (what != 0 && what != GDN_TEST_BWD_RECORD_STALL)
+    if (what != 0 && what != GDN_TEST_BWD_RECORD_STALL && what != GDN_TEST_FWD_RECORD_STALL &&
+        what != GDN_TEST_FWD_ONE_STAGE)
         return fail(GDN_ERR_INVALID_ARG, "gdn_test_inject: unknown injection %d", what);
     g_test_injection = what;
     return ok();

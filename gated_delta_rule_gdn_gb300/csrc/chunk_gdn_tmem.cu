@@ -370,6 +370,7 @@ struct GStateParams {
     const uint8_t* ws;
     GateAct act;
     int group;
+    int test;     // 1: leave out the first record copy (the waits for it run out); 2: a one-chunk-deep ring
 };
 
 // Shared memory of pass 2: two stages of a chunk's operands, then a four-deep ring of its gate vectors.
@@ -787,22 +788,31 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 const uint8_t* rec = p.ws + (size_t)((slot0 + t) * H + ch.h) * GW_ITEM;
                 uint8_t* st = smem + s * GL::STAGE;
                 const uint32_t ph = ((t >> 1) + 1) & 1;   // phase of the empty barriers released by chunk t - 2
-                if (t >= 2) ok = mbar_wait(&S.emptyU[s], ph, kWaitNs);
+                // test: one chunk in flight per group (each group refilled once the products of chunk t - 1 that read
+                // the same group have completed)
+                const bool one = p.test == 2 && t >= 1;
+                const uint32_t p1 = ((t - 1) >> 1) & 1;
+                if (one) ok = mbar_wait(&S.emptyU[s ^ 1], p1, kWaitNs);
+                if (ok && t >= 2) ok = mbar_wait(&S.emptyU[s], ph, kWaitNs);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&S.fullU[s], 16384 + 8192);
                 tma_load_3d(st + GL::VF, &tmap_v, &S.fullU[s], 0, ch.h, r);
                 tma_load_3d(st + GL::VF + 8192, &tmap_v, &S.fullU[s], 64, ch.h, r);
                 bulk_g2s(st + GL::TB, rec + GW_TB, 8192, &S.fullU[s]);
                 issU = t + 1;
-                if (t >= 2) ok = mbar_wait(&S.emptyQ[s], ph, kWaitNs);
+                if (one) ok = mbar_wait(&S.emptyQ[s ^ 1], p1, kWaitNs);
+                if (ok && t >= 2) ok = mbar_wait(&S.emptyQ[s], ph, kWaitNs);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&S.fullQ[s], 32768);
-                bulk_g2s(st + GL::QW, rec + GW_W, 8192, &S.fullQ[s]);
-                bulk_g2s(st + GL::QW + 16384, rec + GW_W + 8192, 8192, &S.fullQ[s]);
-                tma_load_3d(st + GL::QW + 8192, &tmap_q, &S.fullQ[s], 0, hk, r);
-                tma_load_3d(st + GL::QW + 16384 + 8192, &tmap_q, &S.fullQ[s], 64, hk, r);
+                if (!(p.test == 1 && t == 0)) {   // test: the first chunk's Q and -W never arrive
+                    mbar_arrive_expect_tx(&S.fullQ[s], 32768);
+                    bulk_g2s(st + GL::QW, rec + GW_W, 8192, &S.fullQ[s]);
+                    bulk_g2s(st + GL::QW + 16384, rec + GW_W + 8192, 8192, &S.fullQ[s]);
+                    tma_load_3d(st + GL::QW + 8192, &tmap_q, &S.fullQ[s], 0, hk, r);
+                    tma_load_3d(st + GL::QW + 16384 + 8192, &tmap_q, &S.fullQ[s], 64, hk, r);
+                }
                 issQ = t + 1;
-                if (t >= 2) ok = mbar_wait(&S.emptyK[s], ph, kWaitNs);
+                if (one) ok = mbar_wait(&S.emptyK[s ^ 1], p1, kWaitNs);
+                if (ok && t >= 2) ok = mbar_wait(&S.emptyK[s], ph, kWaitNs);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&S.fullK[s], 16384 + 8192);
                 tma_load_3d(st + GL::KF, &tmap_k, &S.fullK[s], 0, hk, r);
@@ -814,7 +824,8 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             // copies issued whose barrier nobody waited on must land before the CTA exits: wait for every issued
             // phase (bounded)
             for (int t = (issU > 2 ? issU - 2 : 0); t < issU; ++t) mbar_wait(&S.fullU[t & 1], (t >> 1) & 1, kWaitNs);
-            for (int t = (issQ > 2 ? issQ - 2 : 0); t < issQ; ++t) mbar_wait(&S.fullQ[t & 1], (t >> 1) & 1, kWaitNs);
+            for (int t = (issQ > 2 ? issQ - 2 : 0); t < issQ; ++t)
+                if (!(p.test == 1 && t == 0)) mbar_wait(&S.fullQ[t & 1], (t >> 1) & 1, kWaitNs);
             for (int t = (issK > 2 ? issK - 2 : 0); t < issK; ++t) mbar_wait(&S.fullK[t & 1], (t >> 1) & 1, kWaitNs);
         }
     } else {
@@ -926,7 +937,8 @@ cudaError_t launch_chunk_gdn_tmem(const ChunkArgs& a, void* workspace, size_t wo
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    GStateParams sp{geo, a.g, a.scale, a.h0, a.hT, a.o, static_cast<const uint8_t*>(workspace), a.act, a.H / a.HK()};
+    GStateParams sp{geo, a.g, a.scale, a.h0, a.hT, a.o, static_cast<const uint8_t*>(workspace), a.act, a.H / a.HK(),
+                    a.test_fwd};
     CUtensorMap mo;
     if (!make_map_rows(&mo, a.o, rows, a.H, DV, a.o_f32 != 0)) return cudaErrorInvalidValue;
     auto launch2 = [&](auto kern) -> cudaError_t {

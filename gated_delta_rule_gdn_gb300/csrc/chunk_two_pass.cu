@@ -672,6 +672,7 @@ struct StateParams {
     float* hT;
     void* o;
     Ws ws;
+    int test_skip;   // test of the bounded waits: the first chunk record is never copied
 };
 
 // Pass 2: one CTA per (sequence, head, 64-column d_v half), 8 warps; warp w reads TMEM lane quarter w % 4 and the 32
@@ -843,7 +844,8 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     // CTA may have started before that; everything above reads only inputs)
     griddep_wait();
     if (issuer) {
-        for (int t = 0; t < 2 && t < n_chunks; ++t) state_issue(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
+        for (int t = 0; t < 2 && t < n_chunks; ++t)
+            if (!(p.test_skip && t == 0)) state_issue(smem, S, p.ws, (slot0 + t) * H + ch.h, ch.half, t);
     }
     int issued = n_chunks < 2 ? n_chunks : 2;
 
@@ -961,7 +963,8 @@ __global__ void __launch_bounds__(SLayout::THREADS, 1) chunk_state_kernel(const 
     }
     // stages issued but never waited on (after a timeout) must land before the CTA exits
     if (issuer) {
-        for (int t = waited; t < issued; ++t) mbar_wait(&S.full[t & 1], (t >> 1) & 1, kWaitNs);
+        for (int t = waited; t < issued; ++t)
+            if (!(p.test_skip && t == 0)) mbar_wait(&S.full[t & 1], (t >> 1) & 1, kWaitNs);
     }
     if (p.hT && ok) {
 #pragma unroll
@@ -1046,7 +1049,7 @@ cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t wo
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    StateParams sp{geo, a.h0, a.hT, a.o, ws};
+    StateParams sp{geo, a.h0, a.hT, a.o, ws, a.test_fwd == 1 ? 1 : 0};
     const unsigned grid2 = (unsigned)(chains * 2);
     // Programmatic stream serialisation: the state kernel's CTAs may start on SMs the per-chunk kernel has left,
     // and wait (griddepcontrol.wait) for its completion before they read the workspace.

@@ -38,6 +38,8 @@ struct ChunkArgs {
     int o_f32;              // 1: o is fp32; 0: o is bf16
     GateAct act;            // gate / beta activation (two-pass path, scalar gate only)
     int Hk;                 // key heads of q and k (0: H); H (value heads) is a multiple of it
+    int test_fwd;           // test of the two-pass state kernels: 1 their first record copy is left out (its bounded
+                            // waits run out); 2 the scalar-gate ring runs one chunk deep (must not change the result)
     int N() const { return cu ? n_seqs : B; }
     int HK() const { return Hk > 0 ? Hk : H; }
 };
@@ -131,8 +133,8 @@ struct BwdArgs {
     __host__ __device__ int HK() const { return Hk > 0 ? Hk : H; }
 };
 
-// One-shot test injection armed by gdn_test_inject (api.cu), consumed by the calling thread's next backward call.
-int take_test_injection();
+// One-shot test injection armed by gdn_test_inject (api.cu): true, and disarmed, if the armed injection is `what`.
+bool take_test_injection(int what);
 
 // Chunk backward (chunk_bwd.cu).
 size_t bwd_smem_bytes(int C, int dk, bool per_channel);

@@ -453,8 +453,8 @@ gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, in
                                         int n_seqs, size_t* bytes);
 
 /*
- * gdn_test_inject -- arm a one-shot test of the bounded waits for the calling
- * thread's next gdn_chunk_bwd call.  GDN_TEST_BWD_RECORD_STALL: the state walks
+ * gdn_test_inject -- arm a one-shot test of the bounded waits.
+ * GDN_TEST_BWD_RECORD_STALL, for the calling thread's next gdn_chunk_bwd call: the state walks
  * leave out the bulk copy of their first chunk record, so the bounded wait for
  * it gives up (after 2 s), the walk records the failure in the device status
  * and leaves; gdn_device_status then returns GDN_ERR_TIMEOUT, and that call's
@@ -462,6 +462,19 @@ gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, in
  * usable.  0 disarms.  GDN_ERR_INVALID_ARG for an unknown value.
  */
 #define GDN_TEST_BWD_RECORD_STALL 1
+/*
+ * GDN_TEST_FWD_RECORD_STALL: the same for the calling thread's next chunk
+ * forward on the two-pass path (either gate): the state kernels leave out the
+ * copies of the first chunk record of every chain, so their bounded waits give
+ * up, gdn_device_status reports GDN_ERR_TIMEOUT and that call's outputs are
+ * unspecified.  Nothing is left in flight and the context stays usable.
+ * GDN_TEST_FWD_ONE_STAGE: the next scalar-gate two-pass forward refills each
+ * buffer of its state kernel's two-stage ring only after the previous chunk's
+ * products have completed (one chunk in flight instead of two).  This changes
+ * the timing only: the result must be bitwise the same.
+ */
+#define GDN_TEST_FWD_RECORD_STALL 2
+#define GDN_TEST_FWD_ONE_STAGE 3
 gdn_status gdn_test_inject(int what);
 
 /* Message for the calling thread's last non-OK status ("" if none). */

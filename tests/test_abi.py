@@ -246,6 +246,9 @@ def test_backward_workspace_sizes(lib):
 
 def test_test_injection_argument_checks(lib):
     assert lib.gdn_test_inject(7) == 1
+    assert lib.gdn_test_inject(-1) == 1
+    for what in (1, 2, 3):       # backward record stall, forward record stall, one-chunk-deep forward ring
+        assert lib.gdn_test_inject(what) == 0
     assert lib.gdn_test_inject(0) == 0
 
 

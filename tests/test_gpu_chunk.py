@@ -437,3 +437,97 @@ def test_fp16_range_limit_is_reported_never_silent(kind, v_scale):
         assert_close(hT, h_ref, torch.bfloat16, "final state")
     if v_scale >= 1e6:                # v itself is past the fp16 range: the status must say so
         assert st == 5
+
+
+# --- bounded waits, ring depth and memory guards of the tensor-core path ------------------------
+
+def _call(x, algo="two_pass", **kw):
+    d = to_dev(x)
+    fn = gdn.kda_chunk_fwd if x["gate_per_channel"] else gdn.gdn_chunk_fwd
+    return fn(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=x["scale"], initial_state=d["initial_state"],
+              output_final_state=True, cu_seqlens=d["cu_seqlens"], chunk_size=x["chunk_size"], algo=algo, **kw)
+
+
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_a_state_pass_wait_that_runs_out_is_reported_and_the_context_stays_usable(kind):
+    """The test injection leaves out the state kernels' first record copy: their bounded waits give up (about 2 s
+    each), the call reports GDN_ERR_TIMEOUT through gdn_device_status, the status clears, and the next call on the
+    same context matches the oracle."""
+    x = W.chunk_inputs(W.config(3 if kind == "kda" else 1), seed=15, B=1, T=200, H=2)
+    lib = gdn.load()
+    gdn.device_status()                       # start from a clear status
+    assert lib.gdn_test_inject(2) == 0        # GDN_TEST_FWD_RECORD_STALL
+    _call(x)                                  # this call's outputs are unspecified
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 4           # GDN_ERR_TIMEOUT, and cleared
+    assert gdn.device_status() == 0
+    o, hT = _run(x, "two_pass")
+    o_ref, h_ref = oracle_on_heads(x)
+    assert_close(o, o_ref, torch.bfloat16, "o after the timeout")
+    assert_close(hT, h_ref, torch.bfloat16, "final state after the timeout")
+
+
+def test_a_one_chunk_deep_ring_gives_bitwise_the_same_result():
+    """The state kernel's two-stage ring run one chunk deep (test injection GDN_TEST_FWD_ONE_STAGE) changes only the
+    timing of its copies and conversions against its products: packed ragged sequences give the same bits."""
+    x = W.chunk_inputs(W.config(2), seed=16, T=3000, H=3)
+    o1, h1 = _run(x, "two_pass")
+    assert gdn.load().gdn_test_inject(3) == 0
+    o2, h2 = _run(x, "two_pass")
+    assert np.array_equal(o1, o2) and np.array_equal(h1, h2)
+
+
+GUARD = 4096          # bytes of guard before and after each buffer
+
+
+def _guarded(shape, dtype, fill=0xA5):
+    """A tensor of `shape` inside a larger byte buffer filled with `fill`; returns (view, buffer, offset, nbytes)."""
+    n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+    buf = torch.full((n + 2 * GUARD,), fill, dtype=torch.uint8, device="cuda")
+    view = buf[GUARD:GUARD + n].view(dtype).view(shape)
+    return view, buf, n
+
+
+def _guards_intact(buf, n, fill=0xA5):
+    host = buf.cpu()
+    return bool((host[:GUARD] == fill).all()) and bool((host[GUARD + n:] == fill).all())
+
+
+@pytest.mark.parametrize("case", ["gdn_ragged", "gdn_packed", "kda_ragged", "generic_f32", "gdn_bf16_o"])
+def test_guard_bytes_around_outputs_and_workspace_stay_untouched(case):
+    """Host canaries: o, the final state and the caller workspace sit inside larger buffers whose guard bytes hold a
+    sentinel; after the call every guard byte still holds it (no out-of-bounds store by a bulk copy, a tensor store
+    or a partial tail chunk), and the result still matches the oracle."""
+    if case == "gdn_packed":
+        x = W.chunk_inputs(W.config(2), seed=17, T=1500, H=2)
+    elif case == "kda_ragged":
+        x = W.chunk_inputs(W.config(3), seed=17, B=2, T=197, H=2)
+    elif case == "generic_f32":
+        x = W.chunk_inputs(W.config(0), seed=17, B=2, T=77, H=2)
+    else:
+        x = W.chunk_inputs(W.config(1), seed=17, B=2, T=333, H=3)
+    B, T, H, dk = x["q"].shape
+    dv = x["v"].shape[-1]
+    N = x["N"]
+    o_dtype = torch.bfloat16 if case == "gdn_bf16_o" else torch.float32
+    o, ob, on = _guarded((B, T, H, dv), o_dtype)
+    hT, hb, hn = _guarded((N, H, dk, dv), torch.float32)
+    algo = "generic" if case == "generic_f32" else "two_pass"
+    need = gdn.workspace_size(x["gate_per_channel"], B, T, H, dk, dv, x["chunk_size"], x["q"].dtype,
+                              0 if x["cu_seqlens"] is None else N, algo, o_dtype)
+    ws, wb, wn = _guarded((max(need, 1),), torch.uint8)
+    _call(x, algo, o=o, final_state=hT, o_dtype=o_dtype, workspace=ws if need > 0 else None)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    assert _guards_intact(ob, on), "o guard bytes changed"
+    assert _guards_intact(hb, hn), "final state guard bytes changed"
+    assert _guards_intact(wb, wn), "workspace guard bytes changed"
+    o_ref, h_ref = oracle_on_heads(x)
+    tol = torch.float32 if case == "generic_f32" else torch.bfloat16
+    if o_dtype == torch.float32:
+        assert_close(o.double().cpu().numpy(), o_ref, tol, "o")
+    else:   # a bf16 o is the round-to-nearest-even of the fp32 result (bf16 rounding alone exceeds the max bound)
+        o32, _ = _call(x, algo)
+        torch.cuda.synchronize()
+        assert torch.equal(o.cpu(), o32.to(torch.bfloat16).cpu())
+    assert_close(hT.double().cpu().numpy(), h_ref, tol, "final state")
