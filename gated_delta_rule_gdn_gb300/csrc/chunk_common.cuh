@@ -112,8 +112,9 @@ __device__ __forceinline__ void stg_h8(uint8_t* p, const float* f) {
 
 // Epilogue of D0 = [K; Q] K^T.  Rows 0-63 (token i): A[i][j] = beta_i 2^(lg_i - lg_j) (K K^T)_ij for j < i, in
 // fp32 for the solve, plus (IDENTITY) row i of the identity in [I; P].  Rows 64-127 (token i = row - 64):
-// P[i][j] = scale 2^(lg_i - lg_j) (Q K^T)_ij for j <= i, in fp16 in [I; P].  Column blocks wholly above the
-// diagonal for every row of the warp are skipped (warp-uniform); the solve never reads A above the diagonal.
+// P[i][j] = scale 2^(lg_i - lg_j) (Q K^T)_ij for j <= i, in fp16, stored transposed: element (j, i) at row 64 + j,
+// column i of [I; P^T] (128-byte swizzled rows).  Column blocks wholly above the diagonal for every row of the warp
+// are skipped (warp-uniform); the solve never reads A above the diagonal.
 template <bool IDENTITY>
 __device__ __forceinline__ void epilogue_kkt(uint32_t tl, int row, int q4, int pw, const float* lg, const float* bb, float scale,
                                              float* Am, uint8_t* a1) {
@@ -168,8 +169,16 @@ __device__ __forceinline__ void epilogue_kkt(uint32_t tl, int row, int q4, int p
                     v[q] = (j <= i) ? scale * e * __uint_as_float(r[cb][q]) : 0.f;
                 }
             }
-            st_h8(a1 + sw128_off(row, c0 + cb * 16), v);
-            st_h8(a1 + sw128_off(row, c0 + cb * 16 + 8), v + 8);
+            // neighbouring lanes (rows i, i + 1 with i even) swap one value per column pair: the even lane stores
+            // (P[i][j], P[i+1][j]) into row j of P^T, the odd lane (P[i][j+1], P[i+1][j+1]) into row j + 1
+            const bool odd = row & 1;
+#pragma unroll
+            for (int q = 0; q < 16; q += 2) {
+                const int j = c0 + cb * 16 + q;
+                const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[q] : v[q + 1], 1);
+                const uint32_t w = odd ? pack_h2(recv, v[q + 1]) : pack_h2(v[q], recv);
+                *reinterpret_cast<uint32_t*>(a1 + sw128_off(64 + j + odd, (i & ~1))) = w;
+            }
         }
     }
 }

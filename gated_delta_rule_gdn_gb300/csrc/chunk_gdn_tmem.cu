@@ -18,21 +18,28 @@
 //
 // Pass 2, gdn_state_kernel: one CTA per (sequence, head) chain over the whole d_v.  It works in the transposed
 // orientation (tensor-memory lane = d_v row), so that the operands that change along the chain stay in tensor memory:
-//   MMA_U  D3 = U^T = V^T (T diag beta)^T            (V converted to fp16 in the kernel)
-//   MMA3   D3 += h~^T [-W; Q]^T                      (A = h~^T, the state's fp16 copy, read from tensor memory):
-//          columns 0-63 become Delta^T, columns 64-127 (Q h~)^T
-//   Delta epilogue: Delta^T and (diag(gamma_C / gamma) Delta)^T to fp16, in place in tensor memory
-//   MMA4   D4 = (K~^T Delta)^T = (diag(gamma_C / gamma) Delta)^T K      (K converted to fp16)
-//   MMA5   D5 = (P Delta)^T
-//   h <- gamma_C h + D4 (registers, thread = d_v row; h~^T back to tensor memory);  O = scale gamma_i (Q h~) + P Delta.
-// The serial chain is MMA3 -> Delta epilogue -> MMA4 -> state update, with no shared-memory round trip.
+//   MMA_U  D3[:, 0:64] = U^T = V^T (T diag beta)^T                 (V converted to fp16 in the kernel)
+//   MMA3   D3 += h~^T [-W; Q~]^T,  Q~ = diag(scale gamma) Q         (A = h~^T, the state's fp16 copy, in tensor
+//          memory; Q scaled and converted to fp16 in the kernel): columns 0-63 become Delta^T, 64-127 (Q~ h~)^T
+//   Delta epilogue: Delta^T to fp16, in place in tensor memory
+//   MMA45  D45 = Delta^T [K~ | P^T],  K~ = diag(gamma_C / gamma) K  (K scaled and converted to fp16 in the kernel):
+//          columns 0-127 (K~^T Delta)^T, 128-191 (P Delta)^T
+//   h <- gamma_C h + D45[:, 0:128] (registers, thread = d_v row; h~^T back to tensor memory);
+//   O^T = D3[:, 64:128] + D45[:, 128:192].
+// The serial chain is MMA3 -> Delta epilogue -> MMA45 -> state update, with no shared-memory round trip.  The tensor
+// core instructions of a chunk are few and wide (8 + 4 + 4: a single issuing thread spends about as long on an
+// instruction of N <= 128 as the tensor core spends on one of N = 256).  Sixteen warps share the work: eight lane
+// warps (two per tensor-memory lane quarter) hold h in registers, write the Delta and h~ operands and convert Q and
+// K; one issues the products, one the copies; two compute the gate vectors and convert V; four (one per lane quarter)
+// copy O out of tensor memory and store it.  The lane warps run with 168 registers, the rest with 88.
 //
-// Operand precision: every operand of the state pass is fp16 (h~, -W, P, T diag(beta), Delta and its decayed copy, and
-// q, k, v converted from bf16 in the kernel); the per-chunk kernel's products read the raw bf16 q and k, with
-// T diag(beta gamma) rounded to bf16 for W (a rounding that changes the error measurably nowhere: W itself is stored
-// in fp16).  A bf16 copy of the state for the output product Q h~ would break the 2e-2 max-error bound.  fp16 saturates at 65,504: an intermediate
-// beyond that becomes inf and the output or final state non-finite; the state kernel checks what it writes and sets
-// the non-finite bit of the device status (gdn_device_status then reports GDN_ERR_NONFINITE).
+// Operand precision: every operand of the state pass is fp16 (h~, -W, P, T diag(beta), Delta, and q, k, v converted
+// from bf16 in the kernel, q and k with their gate factors applied first); the per-chunk kernel's products read the
+// raw bf16 q and k, with T diag(beta gamma) rounded to bf16 for W (a rounding that changes the error measurably
+// nowhere: W itself is stored in fp16).  A bf16 copy of the state for the output product Q h~ would break the 2e-2
+// max-error bound.  fp16 saturates at 65,504: an intermediate beyond that becomes inf and the output or final state
+// non-finite; the state kernel checks what it writes and sets the non-finite bit of the device status
+// (gdn_device_status then reports GDN_ERR_NONFINITE).
 //
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets a status bit, the CTA drops its work, lands its copies
 // in flight, frees its tensor memory and exits.
@@ -56,7 +63,7 @@ namespace {
 
 // workspace record of one (chunk slot, head) item
 constexpr uint32_t GW_W = 0;         // -W fp16 [token][d_k], two 64-column slabs of 64 rows x 128 B, 128-byte swizzle
-constexpr uint32_t GW_P = 16384;     // P fp16 [i][j], 64 rows x 128 B, 128-byte swizzle
+constexpr uint32_t GW_P = 16384;     // P^T fp16 [j][i], 64 rows x 128 B, 128-byte swizzle
 constexpr uint32_t GW_TB = 24576;    // T diag(beta) fp16 [i][j], 64 rows x 128 B, 128-byte swizzle
 constexpr uint32_t GW_ITEM = 32768;
 
@@ -81,16 +88,6 @@ __device__ __forceinline__ void gate_prefix2(float g0, float g1, int lane, float
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// 8 bf16 (16 bytes) to 8 fp16, in place; rows past the end become exact zeros
-__device__ __forceinline__ void bf16_to_f16_inplace(uint8_t* p, bool zero) {
-    const uint4 v = ld16(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = zero ? 0u : pack_h2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-    st16(p, o[0], o[1], o[2], o[3]);
 }
 
 // ==================================================================== pass 1: per-chunk products
@@ -377,37 +374,47 @@ struct GStateParams {
 struct GL {
     static constexpr uint32_t QW = 0;          // [-W; Q] bf16 K-major, two 64-column slabs of 128 rows (16 KB each):
                                                // rows 0-63 -W (from the record), rows 64-127 Q (TMA)
-    static constexpr uint32_t KF = 32768;      // K tile (TMA, bf16) -> fp16 in place; MN-major operand of MMA4
-    static constexpr uint32_t VF = 49152;      // V tile (TMA, bf16) -> fp16 in place; MN-major operand of MMA_U
-    static constexpr uint32_t PP = 65536;      // P fp16 (record)
+    static constexpr uint32_t KF = 32768;      // [K~ | P^T] MN-major operand of MMA45, three 64-column slabs of 64
+                                               // rows: K (TMA, bf16) -> K~ fp16 in place, then P^T (record)
+    static constexpr uint32_t VF = 57344;      // V tile (TMA, bf16) -> fp16 in place; MN-major operand of MMA_U
     static constexpr uint32_t TB = 73728;      // T diag(beta) fp16 (record)
     static constexpr uint32_t STAGE = 81920;
     static constexpr uint32_t OST = 2 * STAGE; // o of one chunk, [64 tokens][128] in o's dtype (32 KB for fp32)
     static constexpr uint32_t VEC = OST + 32768;   // 4 x GVec
     static constexpr int LW = 256;             // the lane warps: 8, two per tensor-memory lane quarter
-    static constexpr int THREADS = 384;        // + issuer warp, producer warp, 2 converter warps
+    static constexpr int OW = 128;             // the output warps: 4, one per lane quarter
+    static constexpr int THREADS = 512;        // + issuer, producer, 2 converter warps, then the output warps
+    // registers per thread: 128 at launch; the lane warps raise theirs, the other two warpgroups lower theirs
+    static constexpr uint32_t REG_LAUNCH = 128, REG_LANE = 168, REG_REST = 88;
     // tensor memory columns
-    static constexpr uint32_t TM_HT = 0, TM_D3 = 64, TM_D4 = 320, TM_D5 = 448, TM_COLS = 512;
+    static constexpr uint32_t TM_HT = 0, TM_D3 = 64, TM_D45 = 320, TM_COLS = 512;
 };
 struct GVec {
-    float qs[C];     // scale gamma_i (output)
-    float kd[C];     // gamma_C / gamma_i (decayed Delta)
+    float qs[C];     // scale gamma_i (the rows of Q)
+    float kd[C];     // gamma_C / gamma_i (the rows of K)
     float gC;
     float pad[3];
 };
 struct GSmall {
-    uint64_t fullU[2], fullQ[2], fullK[2];     // TMA / bulk copies landed: V + T diag(beta); Q + -W; K + P
+    uint64_t fullU[2], fullQ[2], fullK[2];     // TMA / bulk copies landed: V + T diag(beta); Q + -W; K + P^T
     uint64_t emptyU[2], emptyQ[2], emptyK[2];  // the products that read them have completed
-    uint64_t convU[2], convQ[2], convK[2];     // V, Q and K converted to fp16
-    uint64_t m3, m4, m5;                       // product completions
+    uint64_t convU[2], convQ[2], convK[2];     // V, Q and K converted to fp16 (one arrival per converter, output or
+                                               // lane warp)
+    uint64_t m3, m4;                           // product completions (MMA3; MMA45)
+    uint64_t ofree;                            // the output warps have zeroed the output halves of D3 (phase 0), then
+                                               // read D45 and the output half of chunk t (phase t + 1); one arrival
+                                               // per output warp
     uint64_t hready, dready;                   // h~ / Delta operands stored in tensor memory (one arrival per lane warp)
     uint64_t vready[4];                        // gate vectors of the ring slot written (one phase per four chunks)
+    uint64_t vfree[4];                         // ... and read for the last time (one arrival per lane warp)
     uint32_t tmem_base;
     uint32_t pad;
     float gbuf[C];
 };
 constexpr uint32_t gs_smem_bytes() { return GL::VEC + 4 * sizeof(GVec) + sizeof(GSmall) + 1024; }
 static_assert(gs_smem_bytes() <= 227 * 1024, "state kernel shared memory");
+static_assert(GL::LW * GL::REG_LANE + (GL::THREADS - GL::LW) * GL::REG_REST <= GL::THREADS * GL::REG_LAUNCH,
+              "register split above the launch budget");
 
 struct GChain {
     int n, h, len;
@@ -443,25 +450,27 @@ __device__ GChain g_resolve_chain(const Geo& g) {
     return c;
 }
 
-// 16 packed 32-bit columns per call: thread t writes lane (lane field of taddr) + t
 __device__ __forceinline__ void tmem_st_zero16(uint32_t taddr) {
     const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     tmem_st16(taddr, z);
 }
 
-// One 16 KB tile (two 64-column bf16 slabs of 64 rows, 128-byte swizzled) to fp16 in place by NTHR threads; rows past
-// the end become zeros.  `stride` is the distance of the second slab.  The loads of a batch of 8 chunks are issued
-// before their stores, so that their latencies overlap.
-template <int NTHR>
-__device__ __forceinline__ void tile_to_f16(uint8_t* base, uint32_t stride, int L, int idx) {
+// One 16 KB tile at shared address `base` (two 64-column bf16 slabs of 64 rows, 128-byte swizzled, the second at
+// base + stride) to fp16 in place by NTHR threads; rows past the end become zeros, and with SCALE row r is multiplied
+// by the fp32 rs[r] (shared address rs) first.  The loads of a batch of 8 chunks are issued before their stores, so
+// that their latencies overlap.
+template <int NTHR, bool SCALE>
+__device__ __forceinline__ void tile_to_f16(uint32_t base, uint32_t stride, int L, int idx, uint32_t rs) {
     constexpr int PER = 1024 / NTHR, BATCH = PER < 8 ? PER : 8;
 #pragma unroll 1
     for (int u0 = 0; u0 < PER; u0 += BATCH) {
         uint4 v[BATCH];
+        float f[BATCH];
 #pragma unroll
         for (int u = 0; u < BATCH; ++u) {
             const int e = idx + NTHR * (u0 + u);
-            v[u] = ld16(base + (e >> 9) * stride + (e & 511) * 16);
+            v[u] = lds128(base + (e >> 9) * stride + (e & 511) * 16);
+            f[u] = SCALE ? lds32f(rs + 4 * ((e >> 3) & 63)) : 1.f;
         }
 #pragma unroll
         for (int u = 0; u < BATCH; ++u) {
@@ -471,8 +480,9 @@ __device__ __forceinline__ void tile_to_f16(uint8_t* base, uint32_t stride, int 
             uint32_t o[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                o[i] = zero ? 0u : pack_h2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-            st16(base + (e >> 9) * stride + (e & 511) * 16, o[0], o[1], o[2], o[3]);
+                o[i] = zero ? 0u
+                            : pack_h2(f[u] * __uint_as_float(w[i] << 16), f[u] * __uint_as_float(w[i] & 0xFFFF0000u));
+            sts128(base + (e >> 9) * stride + (e & 511) * 16, o[0], o[1], o[2], o[3]);
         }
     }
 }
@@ -509,16 +519,19 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             mbar_init(&S.emptyU[s], 1);
             mbar_init(&S.emptyQ[s], 1);
             mbar_init(&S.emptyK[s], 1);
-            mbar_init(&S.convU[s], 1);
+            mbar_init(&S.convU[s], 2);
             mbar_init(&S.convQ[s], GL::LW / 32);
-            mbar_init(&S.convK[s], 1);
+            mbar_init(&S.convK[s], GL::LW / 32);
         }
         mbar_init(&S.m3, 1);
         mbar_init(&S.m4, 1);
-        mbar_init(&S.m5, 1);
+        mbar_init(&S.ofree, GL::OW / 32);
         mbar_init(&S.hready, GL::LW / 32);
         mbar_init(&S.dready, GL::LW / 32);
-        for (int v = 0; v < 4; ++v) mbar_init(&S.vready[v], 1);
+        for (int v = 0; v < 4; ++v) {
+            mbar_init(&S.vready[v], 1);
+            mbar_init(&S.vfree[v], GL::LW / 32);
+        }
         fence_mbar_init();
     }
     tc_fence_before();
@@ -529,9 +542,12 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
     // started before that; everything above reads only inputs)
     griddep_wait();
 
+    if (warp < 8) setmaxnreg_inc<GL::REG_LANE>();
+    else setmaxnreg_dec<GL::REG_REST>();
+
     bool ok = true;
     if (warp < 8) {
-        // ---------------------------------------------------------------- lane warps
+        // ---------------------------------------------------------------- lane warps: the state chain
         const int q4 = warp & 3, hf = warp >> 2;
         const int dvr = 32 * q4 + lane;                  // d_v row of this thread
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
@@ -539,44 +555,47 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
         float h[64];                                     // h[64 hf + c][dvr]
 #pragma unroll
         for (int c = 0; c < 64; ++c) h[c] = p.h0 ? __ldg(p.h0 + sbase_idx + (size_t)(64 * hf + c) * DV) : 0.f;
-        {   // h~^T to tensor memory (bf16 pairs along d_k), and zeros in both output halves of D3
+        {   // h~^T to tensor memory (fp16 pairs along d_k)
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) pk[c] = pack_h2(h[2 * c], h[2 * c + 1]);
             tmem_st16(tl + GL::TM_HT + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(pk));
             tmem_st16(tl + GL::TM_HT + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
-            for (int s = 0; s < 2; ++s) {
-                tmem_st_zero16(tl + GL::TM_D3 + 128 * s + 64 + 32 * hf);
-                tmem_st_zero16(tl + GL::TM_D3 + 128 * s + 64 + 32 * hf + 16);
-            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.hready);
         }
-        // Q of chunk u to fp16 in place (rows past the end: zeros), in the lane warps' wait for MMA4
-        auto convert_q = [&](int u) -> bool {
+        // Q or K of chunk u to fp16 in place, row i of Q scaled by scale gamma_i, row j of K by gamma_C / gamma_j (rows
+        // past the end: zeros), so that MMA3 gives the output's inter-chunk term and MMA45 the state's increment
+        // directly.  K of chunk t + 1 is converted in the wait for MMA45 of chunk t, Q of chunk t + 2 in the wait for
+        // MMA3 of chunk t + 1.
+        auto convert = [&](bool is_q, int u) -> bool {
             const int su = u & 1;
-            bool okc = mbar_wait(&S.fullQ[su], (u >> 1) & 1, kWaitNs);
+            bool okc = mbar_wait(is_q ? &S.fullQ[su] : &S.fullK[su], (u >> 1) & 1, kWaitNs);
+            if (okc) okc = mbar_wait(&S.vready[u & 3], (u >> 2) & 1, kWaitNs);
             okc = __all_sync(0xffffffffu, okc);
             if (!okc) return false;
-            tile_to_f16<GL::LW>(smem + su * GL::STAGE + GL::QW + 8192, 16384, min(C, ch.len - u * C), tid);
+            if (is_q)
+                tile_to_f16<GL::LW, true>(sbase + su * GL::STAGE + GL::QW + 8192, 16384, min(C, ch.len - u * C), tid,
+                                          smem_u32(vec[u & 3].qs));
+            else
+                tile_to_f16<GL::LW, true>(sbase + su * GL::STAGE + GL::KF, 8192, min(C, ch.len - u * C), tid,
+                                          smem_u32(vec[u & 3].kd));
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.convQ[su]);
+            if (lane == 0) mbar_arrive(is_q ? &S.convQ[su] : &S.convK[su]);
             return true;
         };
-        if (n_chunks > 0 && !convert_q(0)) {
-            ok = false;
-            if (lane == 0) gt_status(1u << 15);
-        }
+        for (int u = 0; u < min(n_chunks, 2) && ok; ++u) ok = convert(true, u);
+        if (ok && n_chunks > 0) ok = convert(false, 0);
+        if (!ok && lane == 0) gt_status(1u << 15);
         bool finite = true;
         for (int t = 0; t < n_chunks && ok; ++t) {
             const int s = t & 1;
             const GVec& V = vec[t & 3];
             const uint32_t d3 = tl + GL::TM_D3 + 128 * s;
-            // Delta epilogue: Delta^T (columns 32 hf .. + 31 of D3) -> fp16 Delta^T and decayed Delta^T, in place:
-            // Delta at columns 32 hf .. + 15, the decayed copy at 32 hf + 16 .. + 31
+            // Delta epilogue: Delta^T (columns 32 hf .. + 31 of D3) -> fp16 Delta^T in place, at columns 32 hf .. + 15
             if (ok) ok = mbar_wait(&S.m3, t & 1, kWaitNs);
             if (ok) ok = mbar_wait(&S.vready[t & 3], (t >> 2) & 1, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
@@ -591,28 +610,27 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 tmem_ld16(d3 + 32 * hf, r[0]);
                 tmem_ld16(d3 + 32 * hf + 16, r[1]);
                 tmem_ld_wait();
-                gC = V.gC;
-                uint32_t da[16], dt[16];
+                gC = V.gC;   // the last read of this chunk's gate vectors
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.vfree[t & 3]);
+                uint32_t da[16];
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
                     const int k = 2 * m;
-                    const float a0 = __uint_as_float(r[k >> 4][k & 15]), a1 = __uint_as_float(r[(k + 1) >> 4][(k + 1) & 15]);
-                    da[m] = pack_h2(a0, a1);
-                    dt[m] = pack_h2(a0 * V.kd[32 * hf + k], a1 * V.kd[32 * hf + k + 1]);
+                    da[m] = pack_h2(__uint_as_float(r[k >> 4][k & 15]), __uint_as_float(r[(k + 1) >> 4][(k + 1) & 15]));
                 }
                 tmem_st16(d3 + 32 * hf, da);
-                tmem_st16(d3 + 32 * hf + 16, dt);
                 tmem_st_wait();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.dready);
-            if (t + 1 < n_chunks && !convert_q(t + 1)) {   // while MMA4 runs
+            if (t + 1 < n_chunks && !convert(false, t + 1)) {   // while MMA45 runs
                 ok = false;
                 if (lane == 0) gt_status(1u << 15);
                 break;
             }
-            // state update: h <- gamma_C h + D4 (columns 64 hf .. + 63), h~^T back to tensor memory
+            // state update: h <- gamma_C h + D4 (columns 64 hf .. + 63 of D45), h~^T back to tensor memory
             if (ok) ok = mbar_wait(&S.m4, t & 1, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -623,8 +641,8 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t r[2][16];
-                tmem_ld16(tl + GL::TM_D4 + 64 * hf + 32 * half, r[0]);
-                tmem_ld16(tl + GL::TM_D4 + 64 * hf + 32 * half + 16, r[1]);
+                tmem_ld16(tl + GL::TM_D45 + 64 * hf + 32 * half, r[0]);
+                tmem_ld16(tl + GL::TM_D45 + 64 * hf + 32 * half + 16, r[1]);
                 tmem_ld_wait();
                 uint32_t pk[16];
 #pragma unroll
@@ -640,64 +658,12 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.hready);
-            // output of this chunk: O = scale gamma_i (Q h~)_i + (P Delta)_i for the tokens 32 hf .. + 31, staged in
-            // shared memory as [token][d_v] rows and written by one bulk copy per valid token row; then the (Q h~)
-            // half of D3 goes back to zero for MMA3 two chunks on
-            if (ok) ok = mbar_wait(&S.m5, t & 1, kWaitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) gt_status(64u);
+            if (t + 2 < n_chunks && !convert(true, t + 2)) {   // while MMA3 of chunk t + 1 runs
+                ok = false;
+                if (lane == 0) gt_status(1u << 15);
                 break;
             }
-            tc_fence_after();
-            {
-                const int L = min(C, ch.len - t * C);
-                if (tid == 0 || tid < C) bulk_wait_read();   // the previous chunk's copies have read the staging
-                named_bar(1, GL::LW);
-                float nf = 0.f;    // stays 0 unless a written value is not finite (x * 0 is NaN for inf and NaN)
-#pragma unroll
-                for (int hq = 0; hq < 2; ++hq) {   // 16 tokens at a time
-                    const int i0 = 32 * hf + 16 * hq;
-                    uint32_t a[16], b[16];
-                    tmem_ld16(d3 + 64 + i0, a);
-                    tmem_ld16(tl + GL::TM_D5 + i0, b);
-                    float qs[16];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float4 v4 = ld4(V.qs + i0 + 4 * u);
-                        qs[4 * u] = v4.x; qs[4 * u + 1] = v4.y; qs[4 * u + 2] = v4.z; qs[4 * u + 3] = v4.w;
-                    }
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const float ov = fmaf(qs[k], __uint_as_float(a[k]), __uint_as_float(b[k]));
-                        nf = i0 + k < L ? fmaf(ov, 0.f, nf) : nf;
-                        if (O_F32) reinterpret_cast<float*>(smem + GL::OST)[(i0 + k) * DV + dvr] = ov;
-                        else reinterpret_cast<__nv_bfloat16*>(smem + GL::OST)[(i0 + k) * DV + dvr] = __float2bfloat16_rn(ov);
-                    }
-                }
-                finite = finite && nf == 0.f;
-                tmem_st_zero16(d3 + 64 + 32 * hf);
-                tmem_st_zero16(d3 + 64 + 32 * hf + 16);
-                fence_async_smem();
-                named_bar(1, GL::LW);
-                const long orow0 = ch.row0 + (long)t * C;
-                if (L == C) {   // a full chunk: one tensor store of the [64][128] tile
-                    if (tid == 0) {
-                        tma_store_3d(&tmap_o, smem + GL::OST, 0, ch.h, (int)orow0);
-                        bulk_commit();
-                    }
-                } else if (tid < L) {   // a sequence's last, partial chunk: its valid rows one by one
-                    constexpr uint32_t RB = DV * (O_F32 ? 4 : 2);   // bytes of one o row
-                    uint8_t* orow = static_cast<uint8_t*>(p.o) + ((size_t)(orow0 + tid) * H + ch.h) * RB;
-                    bulk_s2g(orow, smem + GL::OST + tid * RB, RB);
-                    bulk_commit();
-                }
-                tmem_st_wait();
-                tc_fence_before();
-            }
         }
-        if (tid < C) bulk_wait_all();                   // the o rows are written before the CTA exits
         if (ok && p.hT) {
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
@@ -706,73 +672,153 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             }
         }
         if (__any_sync(0xffffffffu, !finite) && lane == 0) gt_status(kStatusNonfinite);
+    } else if (warp >= 12) {
+        // ---------------------------------------------------------------- output warps: O of each chunk
+        const int q4 = warp & 3;
+        const int dvr = 32 * q4 + lane;                  // d_v row of this thread
+        const int otid = tid - (GL::THREADS - GL::OW);   // 0 .. 127
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        // zeros in the output halves of both D3 buffers (MMA3 accumulates onto them), published to the issuer by a
+        // first arrival on ofree
+        for (int s = 0; s < 2; ++s)
+            for (int c = 0; c < 64; c += 16) tmem_st_zero16(tl + GL::TM_D3 + 128 * s + 64 + c);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.ofree);
+        bool finite = true;
+        for (int t = 0; t < n_chunks && ok; ++t) {
+            const int s = t & 1;
+            const uint32_t d3 = tl + GL::TM_D3 + 128 * s;
+            const int L = min(C, ch.len - t * C);
+            // O^T = h~^T (diag(scale gamma) Q)^T (columns 64 .. 127 of D3, from MMA3) + Delta^T P^T (columns 128 ..
+            // 191 of D45, from MMA45; both complete at m4), staged in shared memory as [token][d_v] rows and written
+            // by one tensor store (a partial chunk: one bulk copy per valid token row)
+            ok = mbar_wait(&S.m4, t & 1, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) gt_status(64u);
+                break;
+            }
+            tc_fence_after();
+            if (otid < C) bulk_wait_read();   // the previous chunk's copies have read the staging
+            named_bar(2, GL::OW);
+            float nf = 0.f;    // stays 0 unless a written value is not finite (x * 0 is NaN for inf and NaN)
+#pragma unroll
+            for (int i0 = 0; i0 < C; i0 += 16) {   // 16 tokens at a time
+                uint32_t a[16], b[16];
+                tmem_ld16(d3 + 64 + i0, a);
+                tmem_ld16(tl + GL::TM_D45 + 128 + i0, b);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float ov = __uint_as_float(a[k]) + __uint_as_float(b[k]);
+                    nf = i0 + k < L ? fmaf(ov, 0.f, nf) : nf;
+                    if (O_F32) sts32(sbase + GL::OST + 4 * ((i0 + k) * DV + dvr), __float_as_uint(ov));
+                    else sts16(sbase + GL::OST + 2 * ((i0 + k) * DV + dvr), __bfloat16_as_ushort(__float2bfloat16_rn(ov)));
+                }
+            }
+            finite = finite && nf == 0.f;
+            // the output half of D3 back to zero for MMA3 two chunks on; D45 may be overwritten from here
+            for (int c = 0; c < 64; c += 16) tmem_st_zero16(d3 + 64 + c);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.ofree);
+            fence_async_smem();
+            named_bar(2, GL::OW);
+            const long orow0 = ch.row0 + (long)t * C;
+            if (L == C) {   // a full chunk: one tensor store of the [64][128] tile
+                if (otid == 0) {
+                    tma_store_3d(&tmap_o, smem + GL::OST, 0, ch.h, (int)orow0);
+                    bulk_commit();
+                }
+            } else if (otid < L) {   // a sequence's last, partial chunk: its valid rows one by one
+                constexpr uint32_t RB = DV * (O_F32 ? 4 : 2);   // bytes of one o row
+                uint8_t* orow = static_cast<uint8_t*>(p.o) + ((size_t)(orow0 + otid) * H + ch.h) * RB;
+                bulk_s2g(orow, smem + GL::OST + otid * RB, RB);
+                bulk_commit();
+            }
+        }
+        if (otid < C) bulk_wait_all();                 // the o rows are written before the CTA exits
+        if (__any_sync(0xffffffffu, !finite) && lane == 0) gt_status(kStatusNonfinite);
     } else if (warp == 8) {
         // ---------------------------------------------------------------- MMA issuer
         const uint32_t idU = idesc_f16(128, 64, false, true, false);    // V^T (MN-major) x (T diag beta)^T
-        const uint32_t id3 = idesc_f16(128, 128, false, false, false);  // h~^T (TMEM) x [-W; Q]^T (K-major)
-        const uint32_t id4 = idesc_f16(128, 128, false, false, true);   // decayed Delta^T (TMEM) x K (MN-major)
-        const uint32_t id5 = idesc_f16(128, 64, false, false, false);   // Delta^T (TMEM) x P^T (K-major)
+        const uint32_t id3 = idesc_f16(128, 128, false, false, false);  // h~^T (TMEM) x [-W; Q~]^T (K-major)
+        const uint32_t id45 = idesc_f16(128, 192, false, false, true);  // Delta^T (TMEM) x [K~ | P^T] (MN-major)
         if (lane == 0 && n_chunks > 0) {
-            auto mma_u = [&](int t) -> bool {
-                const int s = t & 1;
-                if (!mbar_wait(&S.convU[s], (t >> 1) & 1, kWaitNs)) return false;
-                tc_fence_after();
-                const uint32_t st = sbase + s * GL::STAGE;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16(tmem + GL::TM_D3 + 128 * s, sdesc(st + GL::VF + ks * 2048, 8192, 1024),
+            // MMA_U of chunk u, K steps k0 .. k1 - 1 of 4: D3[0:64] = V^T (T diag beta)^T
+            auto mma_u = [&](int u, int k0, int k1) {
+                const uint32_t st = sbase + (u & 1) * GL::STAGE;
+                for (int ks = k0; ks < k1; ++ks)
+                    mma_f16(tmem + GL::TM_D3 + 128 * (u & 1), sdesc(st + GL::VF + ks * 2048, 8192, 1024),
                             sdesc(st + GL::TB + ks * 32, 16, 1024), idU, ks > 0);
-                mma_commit(&S.emptyU[s]);
-                return true;
             };
-            ok = mma_u(0);
-            if (!ok) gt_status(128u);
+            // V of chunk 0 converted, and the output halves of D3 zeroed (phase 0 of ofree)
+            ok = mbar_wait(&S.convU[0], 0, kWaitNs) && mbar_wait(&S.ofree, 0, kWaitNs);
+            if (ok) {
+                tc_fence_after();
+                mma_u(0, 0, 4);
+                mma_commit(&S.emptyU[0]);
+            } else {
+                gt_status(128u);
+            }
             for (int t = 0; t < n_chunks && ok; ++t) {
                 const int s = t & 1;
                 const uint32_t st = sbase + s * GL::STAGE;
                 const uint32_t d3 = tmem + GL::TM_D3 + 128 * s;
+                const bool next = t + 1 < n_chunks;
                 ok = mbar_spin(&S.hready, t & 1, kWaitNs) && mbar_wait(&S.convQ[s], (t >> 1) & 1, kWaitNs);
                 if (!ok) {
                     gt_status(1u << 14);
                     break;
                 }
                 tc_fence_after();
-                // MMA3: D3 += h~^T [-W; Q]^T (N = 128: -W rows then Q rows of each slab; K = 128 = d_k)
+                // MMA3: D3 += h~^T [-W; Q~]^T (N = 128, K = 128 = d_k): columns 0-63 become Delta^T, columns 64-127
+                // (zero before) the output's inter-chunk term
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_f16_ts(d3, tmem + GL::TM_HT + ks * 8,
                                sdesc(st + GL::QW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id3, 1u);
                 mma_commit(&S.m3);
                 mma_commit(&S.emptyQ[s]);
-                // the next chunk's U^T, so that it runs during this chunk's Delta epilogue (its D3 half held Delta of
-                // chunk t - 1, whose products completed before m3 of chunk t)
-                if (t + 1 < n_chunks) {
-                    ok = t == 0 || mbar_wait(&S.m5, (t - 1) & 1, kWaitNs);   // MMA5 of chunk t - 1 read that half
-                    if (ok) ok = mma_u(t + 1);
+                // the first half of the next chunk's U^T, into the other D3 buffer during the Delta epilogue.  Its
+                // Delta operand was read by MMA45 of chunk t - 1; that phase of m4 is the last one committed, so the
+                // wait is unambiguous.
+                if (next) {
+                    ok = (t == 0 || mbar_spin(&S.m4, (t - 1) & 1, kWaitNs)) &&
+                         mbar_wait(&S.convU[s ^ 1], ((t + 1) >> 1) & 1, kWaitNs);
                     if (!ok) {
                         gt_status(1024u);
                         break;
                     }
+                    tc_fence_after();
+                    mma_u(t + 1, 0, 2);
                 }
-                ok = mbar_spin(&S.dready, t & 1, kWaitNs) && mbar_wait(&S.convK[s], (t >> 1) & 1, kWaitNs);
+                // (MMA45 overwrites D45, which the output warps read for chunk t - 1: phase t of ofree, after the
+                // initial zeroing's phase 0)
+                ok = mbar_spin(&S.dready, t & 1, kWaitNs) && mbar_wait(&S.convK[s], (t >> 1) & 1, kWaitNs) &&
+                     mbar_wait(&S.ofree, t & 1, kWaitNs);
                 if (!ok) {
                     gt_status(512u);
                     break;
                 }
                 tc_fence_after();
-                // MMA4: D4 = (decayed Delta)^T K; A = the fp16 columns 32 hb + 16 .. of D3 for the tokens 32 hb ..
+                // MMA45: D45 = Delta^T [K~ | P^T] (N = 192 = d_k + C, K = 64 tokens): columns 0-127 (K~^T Delta)^T for
+                // the state update, 128-191 (P Delta)^T for the output.  A = the fp16 columns 32 hb .. + 15 of D3
+                // (tokens 32 hb .. + 31).
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16_ts(tmem + GL::TM_D4, d3 + (ks >> 1) * 32 + 16 + (ks & 1) * 8,
-                               sdesc(st + GL::KF + ks * 2048, 8192, 1024), id4, ks > 0);
+                    mma_f16_ts(tmem + GL::TM_D45, d3 + (ks >> 1) * 32 + (ks & 1) * 8,
+                               sdesc(st + GL::KF + ks * 2048, 8192, 1024), id45, ks > 0);
                 mma_commit(&S.m4);
-                // MMA5: D5 = Delta^T P^T
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16_ts(tmem + GL::TM_D5, d3 + (ks >> 1) * 32 + (ks & 1) * 8, sdesc(st + GL::PP + ks * 32, 16, 1024),
-                               id5, ks > 0);
-                mma_commit(&S.m5);
                 mma_commit(&S.emptyK[s]);
+                // the second half of the next chunk's U^T, during the state update
+                if (next) {
+                    mma_u(t + 1, 2, 4);
+                    mma_commit(&S.emptyU[s ^ 1]);
+                }
             }
         }
     } else if (warp == 9) {
@@ -817,7 +863,7 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 mbar_arrive_expect_tx(&S.fullK[s], 16384 + 8192);
                 tma_load_3d(st + GL::KF, &tmap_k, &S.fullK[s], 0, hk, r);
                 tma_load_3d(st + GL::KF + 8192, &tmap_k, &S.fullK[s], 64, hk, r);
-                bulk_g2s(st + GL::PP, rec + GW_P, 8192, &S.fullK[s]);
+                bulk_g2s(st + GL::KF + 16384, rec + GW_P, 8192, &S.fullK[s]);
                 issK = t + 1;
             }
             if (!ok) gt_status(2048u);
@@ -829,23 +875,30 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             for (int t = (issK > 2 ? issK - 2 : 0); t < issK; ++t) mbar_wait(&S.fullK[t & 1], (t >> 1) & 1, kWaitNs);
         }
     } else {
-        // ---------------------------------------------------------------- warp 10: the gate vectors and K to fp16;
-        // warp 11: V to fp16
-        if (warp == 10) {
-            float gn[2] = {0.f, 0.f};
-            auto load_g = [&](int t, float (&gg)[2]) {
-                const int Lt = min(C, ch.len - t * C);
+        // ---------------------------------------------------------------- warps 10 and 11: V to fp16, half of each
+        // tile per warp (rows past the end: zeros); warp 10 first computes the gate vectors
+        const int cidx = tid - 10 * 32;   // 0 .. 63
+        float gn[2] = {0.f, 0.f};
+        auto load_g = [&](int t, float (&gg)[2]) {
+            const int Lt = min(C, ch.len - t * C);
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int r = lane + 32 * k;
-                    gg[k] = r < Lt ? act_gate(p.act, __ldg(p.g + (size_t)(ch.row0 + (long)t * C + r) * H + ch.h), ch.h) : 0.f;
+            for (int k = 0; k < 2; ++k) {
+                const int r = lane + 32 * k;
+                gg[k] = r < Lt ? act_gate(p.act, __ldg(p.g + (size_t)(ch.row0 + (long)t * C + r) * H + ch.h), ch.h) : 0.f;
+            }
+        };
+        if (warp == 10 && n_chunks > 0) load_g(0, gn);
+        for (int t = 0; t < n_chunks; ++t) {
+            const int s = t & 1;
+            const int L = min(C, ch.len - t * C);
+            if (warp == 10) {
+                // the gate vectors of chunk t, into ring slot t % 4 once the lane warps have released it (chunk t - 4)
+                if (t >= 4) ok = mbar_wait(&S.vfree[t & 3], ((t >> 2) + 1) & 1, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) gt_status(8192u);
+                    break;
                 }
-            };
-            if (n_chunks > 0) load_g(0, gn);
-            for (int t = 0; t < n_chunks; ++t) {
-                const int s = t & 1;
-                // the gate vectors of chunk t (ring slot t % 4: its chunk t - 4 was read before the K tile of chunk t - 2
-                // could be refilled, which this warp waited for below)
                 S.gbuf[lane] = gn[0];
                 S.gbuf[lane + 32] = gn[1];
                 __syncwarp();
@@ -860,31 +913,17 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.vready[t & 3]);
                 if (t + 1 < n_chunks) load_g(t + 1, gn);
-                if (ok) ok = mbar_wait(&S.fullK[s], (t >> 1) & 1, kWaitNs);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) {
-                    if (lane == 0) gt_status(8192u);
-                    break;
-                }
-                tile_to_f16<32>(smem + s * GL::STAGE + GL::KF, 8192, min(C, ch.len - t * C), lane);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.convK[s]);
             }
-        } else {
-            for (int t = 0; t < n_chunks; ++t) {
-                const int s = t & 1;
-                if (ok) ok = mbar_wait(&S.fullU[s], (t >> 1) & 1, kWaitNs);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) {
-                    if (lane == 0) gt_status(4096u);
-                    break;
-                }
-                tile_to_f16<32>(smem + s * GL::STAGE + GL::VF, 8192, min(C, ch.len - t * C), lane);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.convU[s]);
+            if (ok) ok = mbar_wait(&S.fullU[s], (t >> 1) & 1, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) gt_status(4096u);
+                break;
             }
+            tile_to_f16<64, false>(sbase + s * GL::STAGE + GL::VF, 8192, L, cidx, 0u);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.convU[s]);
         }
     }
     tc_fence_before();
@@ -942,7 +981,13 @@ cudaError_t launch_chunk_gdn_tmem(const ChunkArgs& a, void* workspace, size_t wo
     CUtensorMap mo;
     if (!make_map_rows(&mo, a.o, rows, a.H, DV, a.o_f32 != 0)) return cudaErrorInvalidValue;
     auto launch2 = [&](auto kern) -> cudaError_t {
-        cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gs_smem_bytes());
+        // the warpgroups' register targets add up to the launch budget only at exactly REG_LAUNCH registers per
+        // thread; with fewer, the lane warps' raise would wait forever
+        cudaFuncAttributes fa{};
+        cudaError_t e2 = cudaFuncGetAttributes(&fa, kern);
+        if (e2 != cudaSuccess) return e2;
+        if (fa.numRegs != (int)GL::REG_LAUNCH) return cudaErrorInvalidConfiguration;
+        e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gs_smem_bytes());
         if (e2 != cudaSuccess) return e2;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3((unsigned)chains);
