@@ -90,9 +90,7 @@ struct IntraParams {
 
 // shared memory of pass 1 (bytes from a 1024-aligned base)
 constexpr uint32_t I_KQ = 0;        // [K; Q] rows, two K-slabs of 16 KB (K rows 0-63, Q rows 64-127)
-constexpr uint32_t I_B2 = 32768;    // X = [beta V | beta gamma K], fp16 MN-major 64 x 256 in four 8 KB slabs.  GDN: V
-                                    // lands in slabs 0-1 by TMA (bf16) and is scaled there in place.  KDA: the
-                                    // [64][128] fp32 gate tile lands here first
+constexpr uint32_t I_B2 = 32768;    // X = [beta V | beta gamma K], fp16 MN-major 64 x 256 in four 8 KB slabs
 constexpr uint32_t I_A1 = 65536;    // [-; P] (rows 64-127, copied to the workspace) then [T; T], fp16 K-major 128 x 64
 constexpr uint32_t I_B1 = 81920;    // the solve's scratch
 constexpr uint32_t I_AM = 90112;    // fp32 A, then T in place (row stride TS)
@@ -102,8 +100,9 @@ static_assert(32 * RS * 4 <= 8192, "the solve scratch must fit in the T buffer")
 // KDA only: V tile, and the per-element gate factors (row stride ES floats)
 constexpr int ES = 132;
 constexpr uint32_t I_VB = I_END;                      // V, two 64-column bf16 slabs (TMA)
-constexpr uint32_t I_EF = I_VB + 16384;               // E = exp(G - R_block), fp32 [64][ES]
-constexpr uint32_t I_FF = I_EF + 64 * ES * 4;         // F = exp(R_block - G) (fallback: log2 of the cumulative gate)
+constexpr uint32_t I_EF = I_VB + 16384;               // the [64][128] fp32 gate tile (TMA), then
+                                                      // E = exp(G - R_block), fp32 [64][ES]
+constexpr uint32_t I_FF = I_EF + 64 * ES * 4;         // F = k exp(R_block - G) (fallback: log2 of the cumulative gate)
 
 struct ISmall {
     uint64_t full_kq;         // K, Q of the item landed (TMA transaction bytes)
@@ -156,10 +155,10 @@ __device__ __forceinline__ void intra_issue_v(uint8_t* smem, ISmall& S, const CU
                                               const Item& x) {
     const int row = (int)x.row;
     mbar_arrive_expect_tx(&S.full_v, KDA ? 16384 + 32768 : 16384);
-    uint8_t* vb = smem + (KDA ? I_VB : I_B2);
+    uint8_t* vb = smem + (KDA ? I_VB : I_B2);   // KDA: the gate tile goes to the E table's place
     tma_load_3d(vb, mv, &S.full_v, 0, x.h, row);
     tma_load_3d(vb + 8192, mv, &S.full_v, 64, x.h, row);
-    if (KDA) tma_load_3d(smem + I_B2, mg, &S.full_v, 0, x.h, row);
+    if (KDA) tma_load_3d(smem + I_EF, mg, &S.full_v, 0, x.h, row);
 }
 
 // g (scalar gate only) and beta of an item (0 past its end): lane l holds tokens l and l + 32
@@ -195,15 +194,16 @@ __device__ __forceinline__ float ld_bf16_sw(const uint8_t* base, int r, int c) {
 
 // KDA: within-chunk cumulative gate per channel (thread c < 128 owns channel c), its 16-row block references
 // and the factors of the factored K K^T / Q K^T products:
-//   E[i][c] = 2^(G_ic - R_a),  F[i][c] = 2^(R_a - G_ic)   (i in block a; R_a = G at the end of block a - 1, R_0 = 0)
+//   E[i][c] = 2^(G_ic - R_a),  F[i][c] = k_ic 2^(R_a - G_ic)   (i in block a; R_a = G at the end of block a - 1,
+//   R_0 = 0; F carries the key itself, the column operand of the products and the decayed key of the record)
 // The fast path needs every gate <= 0 (G non-increasing: E <= 1, F <= 2^(block spread)) and every block spread
 // <= KDA_SPREAD_MAX.  Otherwise F keeps G itself and the products are formed exactly, one exponential per term.
-// Also writes gamma_C.
+// Also writes gamma_C.  The gate tile sits where E goes: every thread reads its 32 gates before any writes E.
 __device__ void kda_gate_tables(uint8_t* smem, KSmall& K, int L, float* gc_out, int tid) {
     const float LOG2E = 1.4426950408889634f;
     // thread (half, c): channel c, rows 32 half .. 32 half + 31; the second half's sums start at row 32
     const int c = tid & 127, half = tid >> 7, i0 = 32 * half;
-    const float* gt = reinterpret_cast<const float*>(smem + I_B2);
+    const float* gt = reinterpret_cast<const float*>(smem + I_EF);
     float* E = reinterpret_cast<float*>(smem + I_EF);
     float* F = reinterpret_cast<float*>(smem + I_FF);
     bool fine = true;
@@ -216,6 +216,7 @@ __device__ void kda_gate_tables(uint8_t* smem, KSmall& K, int L, float* gc_out, 
         acc += gi;
         part[i] = acc * LOG2E;
     }
+    __syncthreads();   // the gate tile is read
     // block references relative to this half's start: R_{2 half} = 0, R_{2 half + 1} = part[15]
 #pragma unroll
     for (int bb = 0; bb < 2; ++bb) {
@@ -224,7 +225,7 @@ __device__ void kda_gate_tables(uint8_t* smem, KSmall& K, int L, float* gc_out, 
 #pragma unroll
         for (int i = 16 * bb; i < 16 * bb + 16; ++i) {
             E[(i0 + i) * ES + c] = ex2(part[i] - R);
-            F[(i0 + i) * ES + c] = ex2(R - part[i]);
+            F[(i0 + i) * ES + c] = ld_bf16_sw(smem + I_KQ, i0 + i, c) * ex2(R - part[i]);
         }
     }
     if (half == 0) K.tot1[c] = part[31];
@@ -283,7 +284,7 @@ __device__ __forceinline__ void ld_f32_chunks(const float* row, int t, float (&f
 // step ks reduces over its channels 2 ks and 2 ks + 1 (the same permutation on both operands leaves the sum alone),
 // which makes every operand load a 16-byte vector.  For row block a against column block b <= a:
 //   row operand x_ic 2^(G_ic - R_a) = x_ic E_ic;   column operand k_jc 2^(R_a - G_jc) =
-//   k_jc F_jc (b = a),   (k_jc F_jc) 2^(R_a - R_b) (b < a; F_jc <= 2^(block spread), 2^(R_a - R_b) <= 1).
+//   F_jc (b = a),   F_jc 2^(R_a - R_b) (b < a; F_jc <= |k_jc| 2^(block spread), 2^(R_a - R_b) <= 1).
 // Warp w: product op = w % 2 (K or Q rows), row blocks {0, 3} or {1, 2} ((w / 2) % 2), 8-column half nt = w / 4 of
 // every column block: five 16 x 8 output tiles per warp.
 __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* bb, float scale, int warp, int lane) {
@@ -291,7 +292,6 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
     const int g8 = lane >> 2, t4 = lane & 3;
     const float* E = reinterpret_cast<const float*>(smem + I_EF);
     const float* F = reinterpret_cast<const float*>(smem + I_FF);
-    const uint8_t* kb = smem + I_KQ;                 // K rows 0-63
     const uint8_t* xb = smem + I_KQ + op * 8192;     // K or Q rows
     float* Am = reinterpret_cast<float*>(smem + I_AM);
     uint8_t* a1 = smem + I_A1;
@@ -321,8 +321,7 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
 #pragma unroll 1
         for (int b = 0; b <= a; ++b) {
             const int j = 16 * b + 8 * nt + g8;
-            float kv[32], f[32];
-            ld_bf16_chunks(kb, j, t4, kv);
+            float f[32];
             ld_f32_chunks(F + j * ES, t4, f);
             if (b < a) {   // 2^(R_a - G_j) = F_j 2^(R_a - R_b); where the second factor underflows the product is < 2^-26
                 float dd[32];
@@ -333,7 +332,7 @@ __device__ void kda_products_fast(uint8_t* smem, const KSmall& K, const float* b
             float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};   // two independent chains
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {
-                const uint32_t b0 = to_tf32(kv[2 * ks] * f[2 * ks]), b1 = to_tf32(kv[2 * ks + 1] * f[2 * ks + 1]);
+                const uint32_t b0 = to_tf32(f[2 * ks]), b1 = to_tf32(f[2 * ks + 1]);
                 float (&acc)[4] = (ks & 1) ? d2 : d;
                 asm volatile(
                     "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
@@ -398,13 +397,12 @@ __device__ void kda_products_direct(uint8_t* smem, const float* bb, float scale,
     }
 }
 
-// Per item.  Scalar gate (GDN): [A] gate prefix; [B] MMA0 = [K; Q] K^T runs while the threads build X (beta gamma K,
-// and beta V in place), write Ktilde and gamma_C, and stash [0; scale gamma Q] into TMEM columns 128-255; the epilogue
-// of D0 gives A and [I; P].  Per-channel gate (KDA): [B] the gate tables; A and [I; P] from the factored warp
-// products; X, Ktilde and the Q stash with per-element decays.  Then [C] K and Q are dead and the next item's K, Q
-// load is issued; the solve; T to fp16; MMA1 = [I; P] T; [T; -P T] to fp16; MMA2 = D2 + [T; -PT] [beta V | beta
-// gamma K] = [U | W; -U' | Q']; once MMA2 has read X the next item's V (and gate tile) load is issued; the epilogue
-// writes [W; Q'] and [U; U'] to the workspace.
+// Per item (per-channel gate): [A] its tiles have landed (K and Q; V; the fp32 gate tile, in the E table's place);
+// [B] the gate tables (E, F, the 16-row block references); A and [I; P] from the factored warp products; X =
+// [beta V | beta 2^G K] in shared memory, Ktilde and Q^ with their per-element decays straight to the workspace.
+// [C] K, Q, V, E and F are dead: the next item's tiles are loaded, a whole solve ahead of their use; P to the
+// workspace; the solve; [T; T] in fp16; MMA2 = [T; T] X = [U | W; U | W]; the epilogue writes U and W to the
+// workspace.
 template <bool KDA>
 __global__ void __launch_bounds__(I_THREADS, KDA ? 1 : 2)
 chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -495,8 +493,8 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             ok = __all_sync(0xffffffffu, ok);
             if (!ok && tid == 0) set_status(2u);
             if (ok && loader) v_waited = ic + 1;
-            if (lane == 0) bulk_wait_read();   // the previous item's staging rows (E, A1) have been read
-            __syncthreads();                   // ... by every warp's copies, before any thread writes E
+            if (lane == 0) bulk_wait_read();   // the previous item's staging rows (F, A1) have been read
+            __syncthreads();                   // ... by every warp's copies, before any thread writes F
             // [B] the gate tables (contains the barrier that decides the fast path)
             kda_gate_tables(smem, KS, ok ? L : 0, ws.gc + (size_t)it.it * 128, tid);
             __syncthreads();
@@ -519,6 +517,7 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     const uint32_t off = (uint32_t)(r * 128 + pos * 16);
                     const uint32_t m = r < L ? 0xFFFFFFFFu : 0u;
                     float f[8], v[8], qv[8], eg[8], ek[8], eq[8];
+                    uint4 kd;
                     bf16x8_to_f32(ld16(smem + I_VB + slab * 8192 + off), v);
                     const uint4 xv = scale_chunk_h(v, S.bbuf[r], m);
                     st16(smem + I_B2 + slab * 8192 + off, xv.x, xv.y, xv.z, xv.w);
@@ -535,8 +534,9 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                             const float g2 = e8[q] * er[q];   // 2^(G - R_a) 2^(R_a)
                             eg[q] = S.bbuf[r] * g2;
                             eq[q] = p.scale * g2;
-                            ek[q] = f8[q] * el[q];   // 2^(R_a - G) 2^(G_last - R_a)
+                            ek[q] = f8[q] * el[q];   // k 2^(R_a - G) 2^(G_last - R_a)
                         }
+                        kd = scale_chunk_h(ek, 1.f, m);
                     } else {
                         float g8[8], l8[8];
                         ld_f8(F + r * ES + c, g8);
@@ -548,8 +548,9 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                             eq[q] = p.scale * g2;
                             ek[q] = ex2(l8[q] - g8[q]);
                         }
+                        kd = scale_chunk_hv(f, ek, m);
                     }
-                    const uint4 xk = scale_chunk_hv(f, eg, m), kd = scale_chunk_hv(f, ek, m), qh = scale_chunk_hv(qv, eq, m);
+                    const uint4 xk = scale_chunk_hv(f, eg, m), qh = scale_chunk_hv(qv, eq, m);
                     st16(smem + I_B2 + 16384 + slab * 8192 + off, xk.x, xk.y, xk.z, xk.w);
                     stg16(kt + slab * 8192 + off, kd.x, kd.y, kd.z, kd.w);
                     stg16(wq + slab * 16384 + off, qh.x, qh.y, qh.z, qh.w);
@@ -558,11 +559,14 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             fence_async_smem();
             tmem_st_wait();
             tc_fence_before();
-            __syncthreads();   // [C] A, [I; P] and X are in shared memory; K and Q are dead
+            __syncthreads();   // [C] A, [I; P] and X are in shared memory; K, Q, V, E and F are dead
             tc_fence_after();
+            // the next item's tiles: K and Q, V, and its gate tile into E's place, a whole solve ahead of their use
             if (ok && loader && have_next) {
                 intra_issue_kq(smem, S, &tmap_q, &tmap_k, nx, p.group);
+                intra_issue_v<KDA>(smem, S, &tmap_v, &tmap_g, nx);
                 kq_issued = ic + 2;
+                v_issued = ic + 2;
             }
         // P (rows 64-127 of A1, fp16 K-major) to the workspace, one bulk copy; its rows are overwritten with T below
         if (ok && tid == 96) {
@@ -604,19 +608,14 @@ chunk_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         if (ok) ok = mbar_wait(&S.m2, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) set_status(16u);
-        if (ok && loader && have_next) {   // MMA2 has read X: the next item's V (and gate tile) can land
-            intra_issue_v<KDA>(smem, S, &tmap_v, &tmap_g, nx);
-            v_issued = ic + 2;
-        }
         tc_fence_after();
         // epilogue 2: U and W to the workspace, one 32-row x 64-column tile per warp.  D2's two row halves are alike,
         // so warp (q4, pw) takes token rows 32 (q4 % 2) .. + 31 of column quarter 2 (q4 / 2) + pw: U of d_v half 0 or
         // 1, W of d_k slab 0 or 1.  It stages the tile (4 KB, the workspace's swizzled row layout) in shared memory
-        // nothing reads or loads into any more this item (A1 after MMA2; the beta gamma K half of X for the scalar
-        // gate, whose next V lands in the other half; the E table for KDA, whose next gate tile fills all of X), then
-        // writes it out as 512-byte runs.
+        // nothing reads or loads into any more this item (A1 after MMA2; the F table, which the next item's gate tables
+        // rewrite only after waiting for these copies), then writes it out as 512-byte runs.
         if (ok) {
-            uint8_t* stg = smem + (pw == 0 ? I_A1 : (KDA ? I_EF : I_B2 + 16384)) + q4 * 4096;
+            uint8_t* stg = smem + (pw == 0 ? I_A1 : I_FF) + q4 * 4096;
             const int rh = q4 & 1, cq = ((q4 >> 1) << 1) | pw;
             uint8_t* dst = cq < 2 ? ws.u + (size_t)it.it * WS_U + cq * 8192 + rh * 4096
                                   : ws.wq + (size_t)it.it * WS_WQ + (cq - 2) * 16384 + 8192 + rh * 4096;
