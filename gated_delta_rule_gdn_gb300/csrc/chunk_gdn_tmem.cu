@@ -102,19 +102,19 @@ struct GIntraParams {
     int group;    // value heads per key head
 };
 
-// shared memory of pass 1 (byte offsets from a 1024-aligned base)
-constexpr uint32_t GI_KQ = 0;         // two buffers of [K; Q]: per 64-column slab 64 K rows then 64 Q rows (16 KB)
-constexpr uint32_t GI_KQ_BYTES = 32768;
-constexpr uint32_t GI_A1 = 65536;     // [T diag(beta gamma); same] bf16 K-major 128 x 64 (operand A of MMA2); the
+// shared memory of pass 1 (byte offsets from a 1024-aligned base); 65 KB, so that three CTAs fit on an SM
+constexpr uint32_t GI_KQ = 0;         // [K; Q]: per 64-column slab 64 K rows then 64 Q rows (16 KB)
+constexpr uint32_t GI_A1 = 32768;     // [T diag(beta gamma); same] bf16 K-major 128 x 64 (operand A of MMA2); the
                                       // solve's scratch before that
-constexpr uint32_t GI_PS = 81920;     // P fp16 staging for the bulk copy
-constexpr uint32_t GI_AM = 90112;     // fp32 A, then T in place (row stride TS); then -W staging (16 KB)
+constexpr uint32_t GI_PS = 8192;      // P fp16 staging for the bulk copy, in the Q rows of the first slab (dead once
+                                      // MMA0 has read them)
+constexpr uint32_t GI_AM = 49152;     // fp32 A, then T in place (row stride TS); then -W staging (16 KB)
 constexpr uint32_t GI_END = GI_AM + 64 * TS * 4;
 static_assert(32 * RS * 4 <= 16384, "the solve scratch must fit in A1");
 static_assert(64 * TS * 4 >= 16384, "-W staging must fit in the A buffer");
 
 struct GISmall {
-    uint64_t full_kq[2];
+    uint64_t full_kq;
     uint64_t m0, m2;
     uint32_t tmem_base;
     uint32_t pad;
@@ -125,9 +125,10 @@ struct GISmall {
 };
 constexpr uint32_t GI_SMEM = GI_END + sizeof(GISmall) + 1024;
 constexpr int GI_THREADS = 256;
+constexpr int GI_CTAS_PER_SM = 3;
 constexpr uint32_t GI_TM_COLS = 128;   // D0 (64 columns) and, after the solve, D2 (128 columns) at column 0
 
-__global__ void __launch_bounds__(GI_THREADS, 2)
+__global__ void __launch_bounds__(GI_THREADS, GI_CTAS_PER_SM)
 gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                  const GIntraParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -151,8 +152,7 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         tmem_relinquish();
     }
     if (tid == 32) {
-        mbar_init(&S.full_kq[0], 1);
-        mbar_init(&S.full_kq[1], 1);
+        mbar_init(&S.full_kq, 1);
         mbar_init(&S.m0, 1);
         mbar_init(&S.m2, 1);
         fence_mbar_init();
@@ -163,14 +163,14 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     const uint32_t tmem = S.tmem_base;
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
 
-    auto issue_kq = [&](const Item& x, int b) {
+    auto issue_kq = [&](const Item& x) {
         const int r = (int)x.row, hk = x.h / p.group;
-        uint8_t* kq = smem + GI_KQ + b * GI_KQ_BYTES;
-        mbar_arrive_expect_tx(&S.full_kq[b], 32768);
-        tma_load_3d(kq, &tmap_k, &S.full_kq[b], 0, hk, r);
-        tma_load_3d(kq + 8192, &tmap_q, &S.full_kq[b], 0, hk, r);
-        tma_load_3d(kq + 16384, &tmap_k, &S.full_kq[b], 64, hk, r);
-        tma_load_3d(kq + 16384 + 8192, &tmap_q, &S.full_kq[b], 64, hk, r);
+        uint8_t* kq = smem + GI_KQ;
+        mbar_arrive_expect_tx(&S.full_kq, 32768);
+        tma_load_3d(kq, &tmap_k, &S.full_kq, 0, hk, r);
+        tma_load_3d(kq + 8192, &tmap_q, &S.full_kq, 0, hk, r);
+        tma_load_3d(kq + 16384, &tmap_k, &S.full_kq, 64, hk, r);
+        tma_load_3d(kq + 16384 + 8192, &tmap_q, &S.full_kq, 64, hk, r);
     };
     auto load_gb = [&](const Item& x, float (&g)[2], float (&b)[2]) {
 #pragma unroll
@@ -193,7 +193,7 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         if (loader) {
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
-            issue_kq(x, 0);
+            issue_kq(x);
             issued = 1;
         }
         if (warp == 1) {
@@ -213,16 +213,10 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         cursor_step(nc, ds, dh, H);
         Item nx;
         const bool have_next = cursor_next_valid(p.geo, nc, ds, dh, nx);
-        const int b = ic & 1;
         const uint32_t par = ic & 1;
-        uint8_t* kq = smem + GI_KQ + b * GI_KQ_BYTES;
+        uint8_t* kq = smem + GI_KQ;
         uint8_t* rec = p.ws + (size_t)it.it * GW_ITEM;
         __syncthreads();   // [A] g, beta of this item in shared memory; the previous item is retired
-        // the next item's K and Q go to the other buffer (the previous item's MMA2 has read it)
-        if (ok && loader && have_next) {
-            issue_kq(nx, b ^ 1);
-            issued = ic + 2;
-        }
         if (warp == 1) {
             float G0, G1, Gl;
             gate_prefix2(S.gbuf[2 * lane], S.gbuf[2 * lane + 1], lane, G0, G1, Gl);
@@ -232,7 +226,7 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
             S.bg[2 * lane + 1] = S.bbuf[2 * lane + 1] * ex2(G1);
             if (have_next) load_gb(nx, ng, nb);
         }
-        if (ok) ok = mbar_wait(&S.full_kq[b], (ic >> 1) & 1, kWaitNs);
+        if (ok) ok = mbar_wait(&S.full_kq, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) gt_status(1u);
         if (ok && loader) waited = ic + 1;
@@ -247,7 +241,7 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
             }
             mma_commit(&S.m0);
         }
-        // the previous item's P and -W copies have read their staging (P staging, the A buffer)
+        // the previous item's -W copy has read its staging (the A buffer)
         if (lane == 0) bulk_wait_read();
         if (ok && leader) ok = mbar_wait(&S.m0, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
@@ -292,7 +286,8 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();   // [D] A1 ready; every read of T is done
+        if (tid == 96) bulk_wait_read();   // the copy of P has read its staging in the [K; Q] buffer
+        __syncthreads();   // [D] A1 ready; every read of T is done; P is out of the [K; Q] buffer
         // MMA2: D2 = A1 K (M = 128, N = 128 = d_k, K = 64 tokens; K is the MN-major view of the raw K tile)
         if (ok && leader) {
             tc_fence_after();
@@ -306,6 +301,12 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         if (ok) ok = mbar_wait(&S.m2, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) gt_status(4u);
+        // MMA2 has read K: the next item's K and Q can land (its loads overlap this item's epilogue and the next
+        // item's gate prefix; the other CTAs on the SM cover the rest of their latency)
+        if (ok && loader && have_next) {
+            issue_kq(nx);
+            issued = ic + 2;
+        }
         tc_fence_after();
         // epilogue 2: -W in fp16 into the A buffer (now dead) as [token][d_k] in two swizzled 64-column slabs.  D2's
         // two row halves are alike, so warp (q4, pw) takes token rows 32 (q4 % 2) .. + 31 and d_k columns
@@ -348,7 +349,7 @@ gdn_intra_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     }
     if (lane == 0) bulk_wait_all();   // the record writes are complete before the CTA exits
     if (loader) {
-        for (uint32_t k = waited; k < issued; ++k) mbar_wait(&S.full_kq[k & 1], (k >> 1) & 1, kWaitNs);
+        for (uint32_t k = waited; k < issued; ++k) mbar_wait(&S.full_kq, k & 1, kWaitNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -971,7 +972,7 @@ cudaError_t launch_chunk_gdn_tmem(const ChunkArgs& a, void* workspace, size_t wo
     GIntraParams ip{geo, a.g, a.beta, a.scale, g_n_slots(a), static_cast<uint8_t*>(workspace), a.act, a.H / a.HK()};
     e = cudaFuncSetAttribute(gdn_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GI_SMEM);
     if (e != cudaSuccess) return e;
-    const long grid1 = items < 2L * sms ? items : 2L * sms;
+    const long grid1 = items < (long)GI_CTAS_PER_SM * sms ? items : (long)GI_CTAS_PER_SM * sms;
     gdn_intra_kernel<<<(unsigned)grid1, GI_THREADS, GI_SMEM, s>>>(mq, mk, ip);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
