@@ -749,12 +749,18 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
         const uint32_t id3 = idesc_f16(128, 128, false, false, false);  // h~^T (TMEM) x [-W; Q~]^T (K-major)
         const uint32_t id45 = idesc_f16(128, 192, false, false, true);  // Delta^T (TMEM) x [K~ | P^T] (MN-major)
         if (lane == 0 && n_chunks > 0) {
+            // the shared-memory descriptors of both stages, built once: a K step's offset goes into the start-address
+            // field (16-byte units, no carry below 256 KB) by a plain add, so the issue loops stay short
+            const uint64_t dQW0 = sdesc(sbase + GL::QW, 16, 1024), dQW1 = sdesc(sbase + GL::STAGE + GL::QW, 16, 1024);
+            const uint64_t dKF0 = sdesc(sbase + GL::KF, 8192, 1024), dKF1 = sdesc(sbase + GL::STAGE + GL::KF, 8192, 1024);
+            const uint64_t dVF0 = sdesc(sbase + GL::VF, 8192, 1024), dVF1 = sdesc(sbase + GL::STAGE + GL::VF, 8192, 1024);
+            const uint64_t dTB0 = sdesc(sbase + GL::TB, 16, 1024), dTB1 = sdesc(sbase + GL::STAGE + GL::TB, 16, 1024);
             // MMA_U of chunk u, K steps k0 .. k1 - 1 of 4: D3[0:64] = V^T (T diag beta)^T
             auto mma_u = [&](int u, int k0, int k1) {
-                const uint32_t st = sbase + (u & 1) * GL::STAGE;
+                const uint64_t dv = (u & 1) ? dVF1 : dVF0, dt = (u & 1) ? dTB1 : dTB0;
+#pragma unroll
                 for (int ks = k0; ks < k1; ++ks)
-                    mma_f16(tmem + GL::TM_D3 + 128 * (u & 1), sdesc(st + GL::VF + ks * 2048, 8192, 1024),
-                            sdesc(st + GL::TB + ks * 32, 16, 1024), idU, ks > 0);
+                    mma_f16(tmem + GL::TM_D3 + 128 * (u & 1), dv + ks * 128, dt + ks * 2, idU, ks > 0);
             };
             // V of chunk 0 converted, and the output halves of D3 zeroed (phase 0 of ofree)
             ok = mbar_wait(&S.convU[0], 0, kWaitNs) && mbar_wait(&S.ofree, 0, kWaitNs);
@@ -767,7 +773,7 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             }
             for (int t = 0; t < n_chunks && ok; ++t) {
                 const int s = t & 1;
-                const uint32_t st = sbase + s * GL::STAGE;
+                const uint64_t dqw = s ? dQW1 : dQW0, dkf = s ? dKF1 : dKF0;
                 const uint32_t d3 = tmem + GL::TM_D3 + 128 * s;
                 const bool next = t + 1 < n_chunks;
                 ok = mbar_spin(&S.hready, t & 1, kWaitNs) && mbar_wait(&S.convQ[s], (t >> 1) & 1, kWaitNs);
@@ -780,8 +786,7 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 // (zero before) the output's inter-chunk term
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_f16_ts(d3, tmem + GL::TM_HT + ks * 8,
-                               sdesc(st + GL::QW + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id3, 1u);
+                    mma_f16_ts(d3, tmem + GL::TM_HT + ks * 8, dqw + (ks >> 2) * 1024 + (ks & 3) * 2, id3, 1u);
                 mma_commit(&S.m3);
                 mma_commit(&S.emptyQ[s]);
                 // the first half of the next chunk's U^T, into the other D3 buffer during the Delta epilogue.  Its
@@ -811,8 +816,7 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 // (tokens 32 hb .. + 31).
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16_ts(tmem + GL::TM_D45, d3 + (ks >> 1) * 32 + (ks & 1) * 8,
-                               sdesc(st + GL::KF + ks * 2048, 8192, 1024), id45, ks > 0);
+                    mma_f16_ts(tmem + GL::TM_D45, d3 + (ks >> 1) * 32 + (ks & 1) * 8, dkf + ks * 128, id45, ks > 0);
                 mma_commit(&S.m4);
                 mma_commit(&S.emptyK[s]);
                 // the second half of the next chunk's U^T, during the state update
