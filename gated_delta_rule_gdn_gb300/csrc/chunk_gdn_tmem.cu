@@ -373,8 +373,8 @@ struct GStateParams {
 
 // Shared memory of pass 2: two stages of a chunk's operands, then a four-deep ring of its gate vectors.
 struct GL {
-    static constexpr uint32_t QW = 0;          // [-W; Q] bf16 K-major, two 64-column slabs of 128 rows (16 KB each):
-                                               // rows 0-63 -W (from the record), rows 64-127 Q (TMA)
+    static constexpr uint32_t QW = 0;          // [-W; Q~] fp16 K-major, two 64-column slabs of 128 rows (16 KB each):
+                                               // rows 0-63 -W (record), rows 64-127 Q (TMA, bf16) -> Q~ in place
     static constexpr uint32_t KF = 32768;      // [K~ | P^T] MN-major operand of MMA45, three 64-column slabs of 64
                                                // rows: K (TMA, bf16) -> K~ fp16 in place, then P^T (record)
     static constexpr uint32_t VF = 57344;      // V tile (TMA, bf16) -> fp16 in place; MN-major operand of MMA_U
