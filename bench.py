@@ -32,6 +32,9 @@ workloads 1 and 3: one step is one backward call (three launches: the
 per-chunk prep, the two state walks, the per-chunk gradients).  It is fp32 SIMT arithmetic, so its roofline is the fp32
 FMA rate (152 SMs x 128 lanes x 2 flops x 2.07 GHz), against the algorithmic
 flops of the chunkwise backward given in _bwd_flops.
+Workload 0 (B1 T64 H1 d16 C16, fp32 inputs) runs on the generic fp32 kernel,
+workload 8 (B4 T4096 H8 at head size 256) on the head-size-256 tensor-core pair;
+their lines take the same form.
 With N > 1 (torchrun), every rank runs its own replica: weak scaling, and no
 collective on the data path.  A barrier and a max over ranks bracket the
 timing.
@@ -91,14 +94,22 @@ def _alg_bytes(w, o_bytes: int = 2) -> int:
 
 # The kernel sources each recorded traffic figure depends on (the files that make the timed kernels' code).
 TRAFFIC_SOURCES = {
-    "chunk_gdn": ("chunk_gdn_tmem.cu", "chunk_wy_common.cuh", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh"),
+    "chunk_gdn": ("chunk_gdn_tmem.cu", "chunk_gdn_common.cuh", "chunk_wy_common.cuh", "chunk_common.cuh",
+                  "tc_common.cuh", "gate_act.cuh"),
+    "chunk_gdn_d256": ("chunk_gdn_d256.cu", "chunk_gdn_common.cuh", "chunk_wy_common.cuh", "chunk_common.cuh",
+                       "tc_common.cuh", "gate_act.cuh"),
     "chunk_kda": ("chunk_two_pass.cu", "chunk_wy_common.cuh", "chunk_common.cuh", "tc_common.cuh", "gate_act.cuh"),
     "decode": ("recurrent_step.cu", "gate_act.cuh"),
     "bwd": ("chunk_bwd.cu", "tc_common.cuh"),
+    "chunk_generic": ("chunk_generic.cu",),
 }
 
 
 def _traffic_kind(workload: str) -> str:
+    if "_f32" in workload:
+        return "chunk_generic"
+    if "_d256_" in workload:
+        return "chunk_gdn_d256"
     if "_bwd_" in workload:
         return "bwd"
     if workload.startswith("decode") or "_decode_" in workload:
@@ -326,13 +337,13 @@ def run_reference(args):
     if ws > 1:
         if rank != 0:
             return 0
-    if args.workload >= 4:
+    if args.workload in DECODE:
         return run_reference_decode(args)
     from gated_delta_rule_gdn_gb300 import workloads as W
     import oracle
-    w = W.config(args.workload)
+    w = _chunk_workload(args.workload)
     x = W.chunk_inputs(w, seed=0)
-    heads = [0, 1, 2, 3]                 # one step = 4 heads of every sequence
+    heads = list(range(min(4, w.H)))     # one step = (up to) 4 heads of every sequence
     arr = _oracle_inputs(x, heads)
     oracle.load()
     run = lambda: oracle.recurrence(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], x["scale"], arr["h0"],
@@ -359,6 +370,8 @@ def run_reference(args):
 
 
 BWD_OF = {6: 1, 7: 3}      # backward workload -> the forward workload it differentiates
+DECODE = (4, 5)            # decode-step workloads
+HEAD256 = 8                # GDN prefill at head size 256 (generic kernel)
 ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
 
@@ -586,7 +599,7 @@ def run_ours(args):
         libbuild.build()
     barrier(ws)
     gdn.load()
-    w = W.config(args.workload)
+    w = _chunk_workload(args.workload)
     x = W.chunk_inputs(w, seed=0)
     keys = [k for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens") if x[k] is not None]
     host = {k: x[k].pin_memory() for k in keys}
@@ -700,17 +713,21 @@ def run_ours(args):
     tokens = w.B * w.T
     value = tokens * ws / (ms / 1e3)
     peak, peak_kind = _peaks()
-    alg = _alg_bytes(w)
+    f32_in = w.dtype == "f32"
+    alg = _alg_bytes(w, 4 if f32_in else 2)     # fp32 inputs: o is fp32 in the survey's count too
     alg32 = _alg_bytes(w, 4)
     achieved = alg / (ms / 1e3) / 1e9
-    plan = gdn.chunk_plan(w.kind == "kda", w.B, w.T, w.H, w.dk, w.dv, w.chunk_size, torch.bfloat16,
+    plan = gdn.chunk_plan(w.kind == "kda", w.B, w.T, w.H, w.dk, w.dv, w.chunk_size,
+                          torch.float32 if f32_in else torch.bfloat16,
                           x["cu_seqlens"] is not None, args.algo)
     two_pass = "chunk_two_pass (chunk_intra_kernel, chunk_state_kernel)" if w.kind == "kda" else \
+        "chunk_gdn_d256 (gdn_intra256_kernel, gdn_state256_kernel)" if w.dk == 256 else \
         "chunk_gdn_tmem (gdn_intra_kernel, gdn_state_kernel)"
     kernel, launches = {"two_pass": (two_pass, 2)}.get(plan, ("chunk_generic", 1))
     line = {
         "metric": _metric(w), "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if f32_in else "bf16",
         "data": "synthetic (seeded; q,k unit-norm N(0,1), v N(0,1), beta=sigmoid(N), log alpha=-A softplus(N+dt_bias))",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "chunk_size": w.chunk_size, "initial_state": x["initial_state"] is not None,
@@ -721,7 +738,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": _traffic_for(w.name), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6800 GB/s",
-                     "algorithmic_bytes_per_launch": alg, "o_bytes_counted": "bf16 (the survey's count)",
+                     "algorithmic_bytes_per_launch": alg,
+                     "o_bytes_counted": "f32 (fp32 inputs)" if f32_in else "bf16 (the survey's count)",
                      "frac_o_f32": alg32 / (ms / 1e3) / 1e9 / peak, "algorithmic_bytes_o_f32": alg32},
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -738,6 +756,12 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def _chunk_workload(which: int):
+    """Chunk-forward workload `which`: 0-3 as listed in workloads.CONFIGS, 8 the head-size-256 prefill."""
+    from gated_delta_rule_gdn_gb300 import workloads as W
+    return W.HEAD256 if which == HEAD256 else W.config(which)
 
 
 def _decode_workload(which: int):
@@ -862,10 +886,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--algo", choices=["auto", "generic", "two_pass"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4, 5, 6, 7], default=WORKLOAD,
-                    help="1: GDN B4 T4096 H16 (the headline), 2: packed GDN 8 seqs 65536 tokens H32, 3: KDA B2 T8192 "
-                         "H32, 4: GDN decode step 256 seqs H32, 5: KDA decode step 256 seqs H32, 6: GDN chunk "
-                         "backward B4 T4096 H16, 7: KDA chunk backward B2 T8192 H32")
+    ap.add_argument("--workload", type=int, choices=[0, 1, 2, 3, 4, 5, 6, 7, 8], default=WORKLOAD,
+                    help="0: GDN B1 T64 H1 d16 C16 fp32 (tiny), 1: GDN B4 T4096 H16 (the headline), 2: packed GDN 8 "
+                         "seqs 65536 tokens H32, 3: KDA B2 T8192 H32, 4: GDN decode step 256 seqs H32, 5: KDA decode "
+                         "step 256 seqs H32, 6: GDN chunk backward B4 T4096 H16, 7: KDA chunk backward B2 T8192 H32, "
+                         "8: GDN B4 T4096 H8 at head size 256")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -876,7 +901,7 @@ def main(argv=None):
         return run_reference(args)
     if args.workload in BWD_OF:
         return run_bwd(args)
-    if args.workload >= 4:
+    if args.workload in DECODE:
         return run_decode(args)
     return run_ours(args)
 

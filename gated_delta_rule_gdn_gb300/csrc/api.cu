@@ -132,11 +132,11 @@ gdn_status chunk_common(const void* q, const void* k, const void* v, const float
     st = resolve_algo(a, algo, fn, &chosen);
     if (st != GDN_OK) return st;
     if (a.act.any() && chosen != GDN_ALGO_TWO_PASS)
-        return fail(GDN_ERR_UNSUPPORTED, "%s: the gate and beta activation run on the two-pass path only (bf16, d = 128, "
-                    "chunk 64)", fn);
+        return fail(GDN_ERR_UNSUPPORTED, "%s: the gate and beta activation run on the two-pass path only (bf16, chunk 64, "
+                    "d = 128, or d = 256 with the scalar gate)", fn);
     if (a.HK() != a.H && chosen != GDN_ALGO_TWO_PASS)
-        return fail(GDN_ERR_UNSUPPORTED, "%s: grouped value heads run on the two-pass path only (bf16, d = 128, "
-                    "chunk 64)", fn);
+        return fail(GDN_ERR_UNSUPPORTED, "%s: grouped value heads run on the two-pass path only (bf16, chunk 64, d = 128, "
+                    "or d = 256 with the scalar gate)", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (chosen == GDN_ALGO_TWO_PASS) {
@@ -556,9 +556,11 @@ gdn_status gdn_test_inject(int what) {
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 gdn_status gdn_device_status(int clear) {
-    unsigned tp = 0, gt = 0, bw = 0;
+    unsigned tp = 0, gt = 0, bw = 0, d2 = 0;
     cudaError_t e = gdn::tp_read_and_clear_status(&tp, clear != 0);
     if (e == cudaSuccess) e = gdn::gt_read_and_clear_status(&gt, clear != 0);
+    if (e == cudaSuccess) e = gdn::d256_read_and_clear_status(&d2, clear != 0);
+    gt |= d2;   // the scalar-gate forward at either head size
     if (e == cudaSuccess) e = gdn::bwd_read_and_clear_status(&bw, clear != 0);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_status");
     const unsigned nf = gdn::kStatusNonfinite;

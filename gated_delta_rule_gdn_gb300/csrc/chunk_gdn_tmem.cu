@@ -54,6 +54,7 @@
 #include "chunk_common.cuh"
 #include "gate_act.cuh"
 #include "chunk_wy_common.cuh"
+#include "chunk_gdn_common.cuh"
 
 namespace gdn {
 
@@ -69,26 +70,6 @@ constexpr uint32_t GW_ITEM = 32768;
 
 
 __device__ __forceinline__ void gt_status(unsigned bit) { atomicOr(&g_gt_status, bit); }
-
-// Within-chunk cumulative gate, log2 units: lane l holds tokens 2l and 2l + 1 (natural-log gates g0, g1; 0 past the
-// sequence end).  Both passes use this one function, so their gate factors agree bitwise.
-__device__ __forceinline__ void gate_prefix2(float g0, float g1, int lane, float& G0, float& G1, float& Glast) {
-    const float LOG2E = 1.4426950408889634f;
-    float x = g0 + g1;
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, m);
-        if (lane >= m) x += y;
-    }
-    G1 = x * LOG2E;
-    G0 = (x - g1) * LOG2E;
-    Glast = __shfl_sync(0xffffffffu, G1, 31);
-}
-
-__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
 
 // ==================================================================== pass 1: per-chunk products
 struct GIntraParams {
@@ -417,75 +398,9 @@ static_assert(gs_smem_bytes() <= 227 * 1024, "state kernel shared memory");
 static_assert(GL::LW * GL::REG_LANE + (GL::THREADS - GL::LW) * GL::REG_REST <= GL::THREADS * GL::REG_LAUNCH,
               "register split above the launch budget");
 
-struct GChain {
-    int n, h, len;
-    long row0;
-};
-
-// CTA -> (sequence, head); packed sequences longest first (their chains are the longest serial paths)
-__device__ GChain g_resolve_chain(const Geo& g) {
-    GChain c;
-    const int seq_rank = blockIdx.x / g.H;
-    c.h = blockIdx.x % g.H;
-    int n = seq_rank;
-    if (g.cu && g.n_seqs <= 32) {
-        const int lane = threadIdx.x & 31;
-        int rank = -1;
-        if (lane < g.n_seqs) {
-            long s0;
-            int lm;
-            g.seq(lane, s0, lm);
-            rank = 0;
-            for (int m2 = 0; m2 < g.n_seqs; ++m2) {
-                long s2;
-                int l2;
-                g.seq(m2, s2, l2);
-                rank += (l2 > lm) || (l2 == lm && m2 < lane);
-            }
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, rank == seq_rank);
-        if (hit) n = __ffs(hit) - 1;
-    }
-    c.n = n;
-    g.seq(n, c.row0, c.len);
-    return c;
-}
-
 __device__ __forceinline__ void tmem_st_zero16(uint32_t taddr) {
     const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     tmem_st16(taddr, z);
-}
-
-// One 16 KB tile at shared address `base` (two 64-column bf16 slabs of 64 rows, 128-byte swizzled, the second at
-// base + stride) to fp16 in place by NTHR threads; rows past the end become zeros, and with SCALE row r is multiplied
-// by the fp32 rs[r] (shared address rs) first.  The loads of a batch of 8 chunks are issued before their stores, so
-// that their latencies overlap.
-template <int NTHR, bool SCALE>
-__device__ __forceinline__ void tile_to_f16(uint32_t base, uint32_t stride, int L, int idx, uint32_t rs) {
-    constexpr int PER = 1024 / NTHR, BATCH = PER < 8 ? PER : 8;
-#pragma unroll 1
-    for (int u0 = 0; u0 < PER; u0 += BATCH) {
-        uint4 v[BATCH];
-        float f[BATCH];
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const int e = idx + NTHR * (u0 + u);
-            v[u] = lds128(base + (e >> 9) * stride + (e & 511) * 16);
-            f[u] = SCALE ? lds32f(rs + 4 * ((e >> 3) & 63)) : 1.f;
-        }
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const int e = idx + NTHR * (u0 + u);
-            const bool zero = ((e >> 3) & 63) >= L;
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                o[i] = zero ? 0u
-                            : pack_h2(f[u] * __uint_as_float(w[i] << 16), f[u] * __uint_as_float(w[i] & 0xFFFF0000u));
-            sts128(base + (e >> 9) * stride + (e & 511) * 16, o[0], o[1], o[2], o[3]);
-        }
-    }
 }
 
 template <bool O_F32>
@@ -502,7 +417,7 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const GChain ch = g_resolve_chain(p.geo);
+    const GChain ch = g_resolve_chain(p.geo, blockIdx.x);
     const int n_chunks = (ch.len + C - 1) / C;
     const long slot0 = ch.row0 / C + ch.n;
     const int H = p.geo.H;
@@ -578,11 +493,11 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
             okc = __all_sync(0xffffffffu, okc);
             if (!okc) return false;
             if (is_q)
-                tile_to_f16<GL::LW, true>(sbase + su * GL::STAGE + GL::QW + 8192, 16384, min(C, ch.len - u * C), tid,
-                                          smem_u32(vec[u & 3].qs));
+                tile_to_f16<GL::LW, true>(sbase + su * GL::STAGE + GL::QW + 8192, sbase + su * GL::STAGE + GL::QW + 8192,
+                                          16384, min(C, ch.len - u * C), tid, smem_u32(vec[u & 3].qs));
             else
-                tile_to_f16<GL::LW, true>(sbase + su * GL::STAGE + GL::KF, 8192, min(C, ch.len - u * C), tid,
-                                          smem_u32(vec[u & 3].kd));
+                tile_to_f16<GL::LW, true>(sbase + su * GL::STAGE + GL::KF, sbase + su * GL::STAGE + GL::KF, 8192,
+                                          min(C, ch.len - u * C), tid, smem_u32(vec[u & 3].kd));
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(is_q ? &S.convQ[su] : &S.convK[su]);
@@ -925,7 +840,7 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 if (lane == 0) gt_status(4096u);
                 break;
             }
-            tile_to_f16<64, false>(sbase + s * GL::STAGE + GL::VF, 8192, L, cidx, 0u);
+            tile_to_f16<64, false>(sbase + s * GL::STAGE + GL::VF, sbase + s * GL::STAGE + GL::VF, 8192, L, cidx, 0u);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.convU[s]);

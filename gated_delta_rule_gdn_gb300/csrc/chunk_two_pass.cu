@@ -987,7 +987,9 @@ long n_slots(const ChunkArgs& a) { return (long)a.B * a.T / C + a.N() + 1; }
 const char* two_pass_unsupported_reason(const ChunkArgs& a) {
     if (a.per_channel && a.act.gate()) return "the gate activation applies to the scalar gate only";
     if (!a.bf16) return "q, k, v must be bf16";
-    if (a.dk != DK || a.dv != DV) return "d_k and d_v must be 128";
+    const bool d256 = !a.per_channel && a.dk == 256 && a.dv == 256;
+    if ((a.dk != DK || a.dv != DV) && !d256)
+        return a.per_channel ? "d_k and d_v must be 128" : "d_k and d_v must both be 128 or both be 256";
     if (a.C != C) return "chunk_size must be 64";
     auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0; };
     if (!al16(a.q) || !al16(a.k) || !al16(a.v) || !al16(a.o) || (a.h0 && !al16(a.h0)) || (a.hT && !al16(a.hT)) ||
@@ -997,13 +999,15 @@ const char* two_pass_unsupported_reason(const ChunkArgs& a) {
 }
 
 size_t two_pass_workspace_bytes(const ChunkArgs& a) {
-    if (!a.per_channel) return gdn_tmem_workspace_bytes(a);
+    if (!a.per_channel) return a.dk == 256 ? gdn_d256_workspace_bytes(a) : gdn_tmem_workspace_bytes(a);
     if ((long)a.B * a.T == 0) return 0;
     return (size_t)n_slots(a) * a.H * WS_ITEM;
 }
 
 cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s) {
-    if (!a.per_channel) return launch_chunk_gdn_tmem(a, workspace, workspace_bytes, s);
+    if (!a.per_channel)
+        return a.dk == 256 ? launch_chunk_gdn_d256(a, workspace, workspace_bytes, s)
+                           : launch_chunk_gdn_tmem(a, workspace, workspace_bytes, s);
     const long chains = (long)a.N() * a.H;
     if (chains == 0) return cudaSuccess;
     if (!device_is_sm100_family()) return cudaErrorNoKernelImageForDevice;

@@ -76,6 +76,10 @@ size_t two_pass_workspace_bytes(const ChunkArgs& a);
 cudaError_t launch_chunk_two_pass(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s);
 size_t gdn_tmem_workspace_bytes(const ChunkArgs& a);
 cudaError_t launch_chunk_gdn_tmem(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s);
+// The scalar gate at d_k = d_v = 256 (chunk_gdn_d256.cu): the same two passes, the state kernel per (chain, d_v half)
+// with the fp32 state in tensor memory.
+size_t gdn_d256_workspace_bytes(const ChunkArgs& a);
+cudaError_t launch_chunk_gdn_d256(const ChunkArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s);
 // The statically allocated two-pass workspace: its size, and its device address on the current device (looked up
 // once per device with cudaGetSymbolAddress).
 size_t static_workspace_capacity();
@@ -99,6 +103,7 @@ cudaError_t launch_recurrent_step(const StepArgs& a, cudaStream_t s);
 constexpr unsigned kStatusNonfinite = 1u << 8;
 cudaError_t tp_read_and_clear_status(unsigned* value, bool clear);
 cudaError_t gt_read_and_clear_status(unsigned* value, bool clear);
+cudaError_t d256_read_and_clear_status(unsigned* value, bool clear);
 
 // One chunk-backward request, already validated by api.cu.  Gradients are of
 // L = <dO, o> + <dhT, final state> with respect to every input of the forward.

@@ -37,7 +37,7 @@ import torch
 
 __all__ = [
     "ChunkWorkload", "DecodeWorkload", "CONFIGS", "chunk_inputs", "chunk_output_grads", "decode_constants",
-    "decode_step_inputs", "varlen_lengths", "config",
+    "decode_step_inputs", "varlen_lengths", "config", "HEAD256",
 ]
 
 
@@ -95,6 +95,12 @@ CONFIGS = {
     3: ChunkWorkload("kda_b2_t8192_h32_d128_c64_bf16", "kda", 2, 8192, 32, 128, 128, 64, "bf16", h0_std=0.0),
     4: DecodeWorkload("decode_n256_h32_d128_1024steps", 256, 32, 128, 128, 1024),
 }
+
+
+# Head size 256, the largest the gated delta rule's head-size range allows ("Gated Delta Network (GDN)", §4.3), at
+# the model width of config 1 (H x d = 2048).
+HEAD256 = ChunkWorkload("gdn_prefill_b4_t4096_h8_d256_c64_bf16", "gdn", 4, 4096, 8, 256, 256, 64, "bf16",
+                        h0_std=0.02)
 
 
 def config(i: int):

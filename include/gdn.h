@@ -78,8 +78,10 @@ typedef enum gdn_algo {
                                path): always GDN_ERR_UNSUPPORTED */
     GDN_ALGO_TWO_PASS = 3   /* tcgen05 in two passes: a per-chunk kernel over all SMs writes the
                                state-independent products to a device workspace, then a state
-                               kernel walks each chain.  bf16, d_k = d_v = 128, chunk 64;
-                               GDN_ERR_UNSUPPORTED when the request does not fit it.
+                               kernel walks each chain.  bf16, chunk 64, d_k = d_v = 128, or
+                               d_k = d_v = 256 with the scalar gate (its state kernel walks each
+                               (chain, half of d_v)); GDN_ERR_UNSUPPORTED when the request does
+                               not fit it.
                                Range: these kernels round some intermediates to fp16, whose
                                largest finite value is 65,504: the k and v values (scalar
                                gate), the per-chunk products P = scale (Gamma * Q K^T),
@@ -124,7 +126,8 @@ typedef enum gdn_algo {
  *   o           [B, T, H, d_v]   o_dtype (output)
  *   chunk_size  16, 32 or 64 (the pages' kernels use these; 64 is the default there)
  *   sizes       B >= 1, T >= 0, H >= 1, 1 <= d_k, d_v <= 256 (the pages' bound on
- *               the head sizes; above 128 only the generic kernel applies)
+ *               the head sizes; the tensor-core path takes 128 and, for this scalar
+ *               gate, 256; other sizes run on the generic kernel)
  *
  * Packed sequences give results bitwise equal to running each sequence alone.
  */

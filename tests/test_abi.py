@@ -176,8 +176,11 @@ def test_beta_activation_mode_checks(lib):
 def test_head_sizes_up_to_256_and_the_generic_kernels_shared_memory(lib):
     import torch
     bf, f32 = torch.bfloat16, torch.float32
-    # d_k = d_v = 256 runs on the generic kernel: chunk 64 for the scalar gate ...
-    assert _binding.chunk_plan(False, 1, 300, 2, 256, 256, 64, bf) == "generic"
+    # d_k = d_v = 256 in bf16 with the scalar gate and chunk 64 has its tensor-core pair; other head sizes above 128
+    # run on the generic kernel: chunk 64 for the scalar gate ...
+    assert _binding.chunk_plan(False, 1, 300, 2, 256, 256, 64, bf) == "two_pass"
+    assert _binding.chunk_plan(False, 1, 300, 2, 256, 256, 64, bf, algo="generic") == "generic"
+    assert _binding.chunk_plan(False, 1, 300, 2, 256, 128, 64, bf) == "generic"
     assert _binding.chunk_plan(False, 1, 300, 2, 256, 64, 64, f32) == "generic"
     # ... chunk 32 or less for the per-channel gate; chunk 64 would not fit one CTA's shared memory
     assert _binding.chunk_plan(True, 1, 300, 2, 256, 256, 32, bf) == "generic"

@@ -79,6 +79,27 @@ def test_roofline_counts_of_the_headline_workloads():
     assert bench._alg_bytes(W.config(1), 4) == 262_144 * 1288 + 64 * 2 * 65_536 == 346_030_080
     # KDA: the per-channel gate adds 4 (d_k - 1) B per token-head; no initial state, so the state is written only
     assert bench._alg_bytes(W.config(3)) == 524_288 * (1032 + 4 * 127) + 64 * 65_536 == 811_597_824
+    # head size 256: 131,072 token-heads x (3 x 512 B q, k, v + 512 B o + 8 B g, beta) plus 32 states of 256 KiB
+    # read and written
+    assert bench._alg_bytes(W.HEAD256) == 131_072 * 2056 + 32 * 2 * 262_144 == 286_261_248
+    # the fp32 tiny case: 64 token-heads x (3 x 64 B + 64 B o + 8 B) plus one 1 KiB state, written only
+    assert bench._alg_bytes(W.config(0), 4) == 64 * 264 + 1024 == 17_920
     macs = 3 * 16 * 16 * 128 + 8 * 16 * 128 * 128 + 5 * 16 * 16 * 128 // 2
     assert macs == 2_277_376
     assert bench._bwd_flops(W.config(1), 16) == 2 * macs * 16_384 == 74_625_056_768
+
+
+def test_reference_arm_on_the_tiny_and_head256_workloads(capsys):
+    # the reference arm samples up to four heads, so a one-head workload runs too; the head-256 workload maps to
+    # its own shape
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    assert bench.main(["--impl", "reference", "--workload", "0", "--steps", "1", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"]["workload"] == "gdn_tiny_b1_t64_h1_d16_c16_f32"
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
+    w = bench._chunk_workload(8)
+    assert (w.dk, w.dv, w.H, w.B, w.T) == (256, 256, 8, 4, 4096)
+    assert bench._traffic_kind(w.name) == "chunk_gdn_d256"
+    assert bench._traffic_kind(bench._chunk_workload(0).name) == "chunk_generic"

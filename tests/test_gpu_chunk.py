@@ -3,7 +3,8 @@
 Every call goes through the C ABI (ctypes binding), on seeded synthetic inputs
 from gated_delta_rule_gdn_gb300.workloads, in element-by-element comparison:
 * small cases the oracle runs whole, spanning several chunks and a ragged tail;
-* the full-size workloads (configs 1, 2 and 3), with the oracle run on every head;
+* the full-size workloads (configs 1, 2 and 3, and the head-size-256 prefill), with the oracle run on every head;
+* head size 256 on its tensor-core pair: ragged, packed, grouped value heads, in-kernel activations;
 * edge cases: T < C, T = 0, zero-length packed sequences, extreme decay, beta
   near 0 and 1.
 Packed sequences must match separate runs bitwise; so must a state hand-off at
@@ -331,6 +332,90 @@ def test_full_config3_kda_all_heads():
     assert_close(hT, h_ref, torch.bfloat16, "final state")
 
 
+@pytest.mark.parametrize("algo", ["auto", "generic"])
+def test_full_head256_all_heads(algo):
+    # head size 256 at full size (B4 T4096 H8): the tensor-core pair (the launch the bench times) and the generic
+    # kernel
+    x = W.chunk_inputs(W.HEAD256, seed=0)
+    assert gdn.chunk_plan(False, 4, 4096, 8, 256, 256, 64, torch.bfloat16) == "two_pass"
+    o_ref, h_ref = _oracle_cached("head256", x)
+    o, hT = _run(x, algo)
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
+# --- head size 256 on the tensor-core pair ----------------------------------------------------
+
+def _w256(h0_std=0.02):
+    return _workload("gdn", "bf16", 256, 256, 64, h0_std)
+
+
+@pytest.mark.parametrize("B,T,H,h0", [(2, 333, 2, 0.02), (1, 64, 2, 0.02), (3, 5, 2, 0.0), (1, 1, 1, 0.02),
+                                      (2, 4096 + 37, 8, 0.02)],
+                         ids=["ragged", "one_chunk", "shorter_than_a_chunk", "one_token", "several_items_per_cta"])
+def test_head256_tensor_core_pair(B, T, H, h0):
+    x = W.chunk_inputs(_w256(h0), seed=21, B=B, T=T, H=H)
+    assert _fits(x, "two_pass")
+    o_ref, h_ref = oracle_on_heads(x)
+    o, hT = _run(x, "two_pass")
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
+def test_head256_packed_sequences_match_separate_runs_bitwise():
+    lens = [130, 0, 64, 1, 200, 63, 65]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    x = W.chunk_inputs(_w256(), seed=22, B=1, T=int(cu[-1]), H=2)
+    x["cu_seqlens"] = torch.from_numpy(cu)
+    x["initial_state"] = torch.randn(len(lens), 2, 256, 256, generator=torch.Generator().manual_seed(3)) * 0.02
+    o, hT = _run(x, "two_pass")
+    for n, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        xn = {**x, "cu_seqlens": None, "initial_state": x["initial_state"][n:n + 1]}
+        for key in ("q", "k", "v", "g", "beta"):
+            xn[key] = x[key][:, a:b].contiguous()
+        on, hn = _run(xn, "two_pass")
+        assert np.array_equal(o[:, a:b], on), n
+        assert np.array_equal(hT[n], hn[0]), n
+    assert np.array_equal(hT[1], x["initial_state"][1].double().numpy())
+    o_ref, h_ref = oracle_on_heads(x)
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
+def test_head256_bf16_output_and_no_final_state():
+    # a bf16 o is the round-to-nearest-even of the same fp32 result; leaving out the final state changes nothing else
+    x = W.chunk_inputs(_w256(), seed=23, B=2, T=150, H=2)
+    o32, h32 = _run(x, "two_pass")
+    o16, h16 = _run(x, "two_pass", o_dtype=torch.bfloat16)
+    assert np.array_equal(o16, torch.from_numpy(o32).float().to(torch.bfloat16).double().numpy())
+    assert np.array_equal(h16, h32)
+    on, hn = _run(x, "two_pass", out_final=False)
+    assert hn is None and np.array_equal(on, o32)
+
+
+def test_head256_grouped_value_heads_and_activations():
+    """H_v = 2 H_k at head size 256, with the gate and beta activated in the kernel: checked against the oracle on
+    q, k repeated per value head and the oracle's own activations."""
+    Hk, G = 2, 2
+    x = W.chunk_inputs(_w256(), seed=24, B=2, T=200, H=Hk * G)
+    gl, bl, A_log, dt_bias, g64, b64 = _raw_gates(x, 24)
+    xr = dict(x)
+    xr["q"] = x["q"][:, :, ::G].repeat_interleave(G, dim=2)
+    xr["k"] = x["k"][:, :, ::G].repeat_interleave(G, dim=2)
+    xr["g"], xr["beta"] = torch.from_numpy(g64), torch.from_numpy(b64)
+    o_ref, h_ref = oracle_on_heads(xr)
+    d = to_dev(x)
+    o, hT = gdn.gdn_chunk_fwd(d["q"][:, :, ::G].contiguous(), d["k"][:, :, ::G].contiguous(), d["v"],
+                              torch.from_numpy(gl).cuda(), torch.from_numpy(bl).cuda(), scale=x["scale"],
+                              initial_state=d["initial_state"], output_final_state=True,
+                              A_log=torch.from_numpy(A_log).cuda(), dt_bias=torch.from_numpy(dt_bias).cuda(),
+                              beta_sigmoid=True, algo="two_pass")
+    torch.cuda.synchronize()
+    assert gdn.device_status() == 0
+    assert_close(o.double().cpu().numpy(), o_ref, torch.bfloat16, "o")
+    assert_close(hT.double().cpu().numpy(), h_ref, torch.bfloat16, "final state")
+
+
 def _raw_gates(x, seed):
     """Raw gate and beta logits plus A_log, dt_bias per head, and the activated log alpha and beta the oracle takes,
     formed by the oracle's own pinned activations (oracle.gate_activation, oracle.beta_activation)."""
@@ -407,14 +492,15 @@ def test_beta_in_zero_two_from_logits(kind):
 
 # --- the fp16 range of the tensor-core path ---------------------------------------------------
 
-@pytest.mark.parametrize("kind", ["gdn", "kda"])
+@pytest.mark.parametrize("kind", ["gdn", "kda", "gdn256"])
 @pytest.mark.parametrize("v_scale", [1e2, 3e4, 1e6])
 def test_fp16_range_limit_is_reported_never_silent(kind, v_scale):
     """The two-pass kernels round some intermediates to fp16 (largest finite value 65,504).  Values v scaled by up
     to 1e6, with beta near its upper bound 2 ("Gated Delta Network (GDN)", §5: beta in (0, 2)), either match the
     oracle or leave a non-finite value in o or the final state, which gdn_device_status reports as
     GDN_ERR_NONFINITE.  A non-finite output without that status is a failure."""
-    x = W.chunk_inputs(W.config(3 if kind == "kda" else 1), seed=14, B=1, T=256, H=2)
+    w = W.HEAD256 if kind == "gdn256" else W.config(3 if kind == "kda" else 1)
+    x = W.chunk_inputs(w, seed=14, B=1, T=256, H=2)
     x["v"] = (x["v"].float() * v_scale).to(torch.bfloat16)
     x["beta"] = torch.full_like(x["beta"], 1.95)
     d = to_dev(x)
@@ -445,12 +531,13 @@ def _call(x, algo="two_pass", **kw):
               output_final_state=True, cu_seqlens=d["cu_seqlens"], chunk_size=x["chunk_size"], algo=algo, **kw)
 
 
-@pytest.mark.parametrize("kind", ["gdn", "kda"])
+@pytest.mark.parametrize("kind", ["gdn", "kda", "gdn256"])
 def test_a_state_pass_wait_that_runs_out_is_reported_and_the_context_stays_usable(kind):
     """The test injection leaves out the state kernels' first record copy: their bounded waits give up (about 2 s
     each), the call reports GDN_ERR_TIMEOUT through gdn_device_status, the status clears, and the next call on the
     same context matches the oracle."""
-    x = W.chunk_inputs(W.config(3 if kind == "kda" else 1), seed=15, B=1, T=200, H=2)
+    w = W.HEAD256 if kind == "gdn256" else W.config(3 if kind == "kda" else 1)
+    x = W.chunk_inputs(w, seed=15, B=1, T=200, H=2)
     lib = gdn.load()
     gdn.device_status()                       # start from a clear status
     assert lib.gdn_test_inject(2) == 0        # GDN_TEST_FWD_RECORD_STALL
@@ -464,10 +551,15 @@ def test_a_state_pass_wait_that_runs_out_is_reported_and_the_context_stays_usabl
     assert_close(hT, h_ref, torch.bfloat16, "final state after the timeout")
 
 
-def test_a_one_chunk_deep_ring_gives_bitwise_the_same_result():
+@pytest.mark.parametrize("head", [128, 256])
+def test_a_one_chunk_deep_ring_gives_bitwise_the_same_result(head):
     """The state kernel's two-stage ring run one chunk deep (test injection GDN_TEST_FWD_ONE_STAGE) changes only the
     timing of its copies and conversions against its products: packed ragged sequences give the same bits."""
     x = W.chunk_inputs(W.config(2), seed=16, T=3000, H=3)
+    if head == 256:
+        x = {**x, **{k: v for k, v in W.chunk_inputs(_w256(), seed=16, B=1, T=3000, H=3).items()
+                     if k in ("q", "k", "v", "initial_state")}}
+        x["initial_state"] = torch.randn(x["N"], 3, 256, 256, generator=torch.Generator().manual_seed(5)) * 0.02
     o1, h1 = _run(x, "two_pass")
     assert gdn.load().gdn_test_inject(3) == 0
     o2, h2 = _run(x, "two_pass")
@@ -490,13 +582,19 @@ def _guards_intact(buf, n, fill=0xA5):
     return bool((host[:GUARD] == fill).all()) and bool((host[GUARD + n:] == fill).all())
 
 
-@pytest.mark.parametrize("case", ["gdn_ragged", "gdn_packed", "kda_ragged", "generic_f32", "gdn_bf16_o"])
+@pytest.mark.parametrize("case", ["gdn_ragged", "gdn_packed", "kda_ragged", "generic_f32", "gdn_bf16_o",
+                                  "gdn256_packed"])
 def test_guard_bytes_around_outputs_and_workspace_stay_untouched(case):
     """Host canaries: o, the final state and the caller workspace sit inside larger buffers whose guard bytes hold a
     sentinel; after the call every guard byte still holds it (no out-of-bounds store by a bulk copy, a tensor store
     or a partial tail chunk), and the result still matches the oracle."""
     if case == "gdn_packed":
         x = W.chunk_inputs(W.config(2), seed=17, T=1500, H=2)
+    elif case == "gdn256_packed":
+        x = W.chunk_inputs(W.config(2), seed=17, T=1500, H=2)
+        x = {**x, **{k: v for k, v in W.chunk_inputs(_w256(), seed=17, B=1, T=1500, H=2).items()
+                     if k in ("q", "k", "v")}}
+        x["initial_state"] = torch.randn(x["N"], 2, 256, 256, generator=torch.Generator().manual_seed(6)) * 0.02
     elif case == "kda_ragged":
         x = W.chunk_inputs(W.config(3), seed=17, B=2, T=197, H=2)
     elif case == "generic_f32":
