@@ -11,26 +11,30 @@
 //
 // Pass 1, gdn_intra256_kernel: one item per (chunk slot, head), persistent CTAs, two per SM.  MMA0 = [K; Q] K^T over
 // d_k = 256 (16 K steps) gives A and P; the blocked inverse T in place; MMA2 = [T diag(beta gamma); same] K (N = 256)
-// gives W.  The item's record is -W (32 KB), P^T and T diag(beta) (8 KB each), in the operand layouts of pass 2.
+// gives W.  The item's record, 112 KB in the operand layouts of pass 2: [-W; Q~] (64 KB), K~ (32 KB), P^T and
+// T diag(beta) (8 KB each), with Q~ = diag(scale gamma) Q and K~ = diag(gamma_C / gamma) K converted to fp16 here,
+// from the tiles the per-chunk products already hold.  (Converted in the state kernel instead, the two tiles cost
+// that kernel 128 KB of shared-memory traffic per chunk, about a quarter of all of it, and slowed every chain step.)
 //
 // Pass 2, gdn_state256_kernel: one CTA per (sequence, head, d_v half of 128 columns).  It works in the transposed
 // orientation (tensor-memory lane = d_v row).  The half's state, 128 d_v rows x 256 d_k columns of fp32, is too large
 // for registers: it lives in tensor memory, scaled ahead by the next chunk's gamma_C (H = gamma_C h), and the state
 // update is a product accumulating onto it.  Per chunk:
-//   MMA3   D3 = h~^T [-W; Q~]^T (A = h~^T, the state's fp16 copy in tensor memory, K = d_k = 256; Q~ = diag(scale
-//          gamma) Q, converted from bf16 in the kernel): columns 0-63 -(W h)^T, 64-127 (Q~ h)^T
+//   MMA3   D3 = h~^T [-W; Q~]^T (A = h~^T, the state's fp16 copy in tensor memory, K = d_k = 256): columns 0-63
+//          -(W h)^T, 64-127 (Q~ h)^T
 //   MMA_U  D3[:, 0:64] += V^T (T diag beta)^T: Delta^T          (V converted to fp16 in the kernel)
 //   Delta epilogue: Delta^T to fp16 in place
 //   MMA4   H += Delta^T K~ (N = 256): H becomes h of the chunk's end
 //   MMA5   D3[:, 64:128] += Delta^T P^T: O^T
 //   lane warps: h~ = fp16(H) for the next MMA3, H <- gamma_C' H for the next MMA4 (the final state unscaled)
+//   output warps: O^T from tensor memory to a staging tile, out by tensor stores of 32 tokens (plain per-thread
+//   stores of the same rows were several times slower)
 // Tensor memory holds H (256 columns), h~ (128) and D3 (128): all 512.  Sixteen warps: eight lane warps (two per lane
-// quarter, 128 d_k columns each) run the Delta epilogue and the state scaling; four output warps (one per lane quarter)
-// write O straight from tensor memory to o and convert V; one warp issues the products, one the copies; two convert Q
-// and K (one of them first computes the gate vectors).
+// quarter, 128 d_k columns each) run the Delta epilogue and the state scaling; four output warps (one per lane
+// quarter) write O; one warp issues the products, one the copies; two convert V (one of them first computes gamma_C).
 //
 // Operand precision is that of the head-size-128 pair: fp16 operands (h~, -W, P, T diag(beta), Delta, and q, k, v
-// converted in the kernel, with their gate factors applied first), fp32 accumulation, the state itself fp32.  fp16
+// converted to fp16 with their gate factors applied first), fp32 accumulation, the state itself fp32.  fp16
 // saturates at 65,504; the state kernel checks what it writes and reports a non-finite value through the device
 // status (GDN_ERR_NONFINITE).
 //
@@ -58,11 +62,14 @@ namespace {
 constexpr int D2 = 256;      // d_k = d_v
 constexpr int VT = 128;      // d_v columns of one state CTA
 
-// workspace record of one (chunk slot, head) item
-constexpr uint32_t R_W = 0;         // -W fp16 [token][d_k], four 64-column slabs of 64 rows x 128 B, 128-byte swizzle
-constexpr uint32_t R_P = 32768;     // P^T fp16 [j][i], 64 rows x 128 B, 128-byte swizzle
-constexpr uint32_t R_TB = 40960;    // T diag(beta) fp16 [i][j], 64 rows x 128 B, 128-byte swizzle
-constexpr uint32_t R_ITEM = 49152;
+// workspace record of one (chunk slot, head) item, in the operand layouts of the state kernel (rows of 128 B,
+// 128-byte swizzle)
+constexpr uint32_t R_WQ = 0;        // [-W; Q~] fp16 [token][d_k]: per 64-column slab (four, 16 KB apart) 64 rows of -W,
+                                    // then 64 rows of Q~ = diag(scale gamma) Q
+constexpr uint32_t R_K = 65536;     // K~ = diag(gamma_C / gamma) K fp16 [token][d_k], four 64-column slabs of 64 rows
+constexpr uint32_t R_P = 98304;     // P^T fp16 [j][i]
+constexpr uint32_t R_TB = 106496;   // T diag(beta) fp16 [i][j]
+constexpr uint32_t R_ITEM = 114688;
 
 __device__ __forceinline__ void d_status(unsigned bit) { atomicOr(&g_d256_status, bit); }
 
@@ -80,14 +87,14 @@ struct IParams {
 
 // shared memory of pass 1 (byte offsets from a 1024-aligned base); about 98 KB, two CTAs per SM
 constexpr uint32_t I_KQ = 0;          // [K; Q]: per 64-column slab (four), 64 K rows then 64 Q rows (16 KB)
-constexpr uint32_t I_PS = 8192;       // P fp16 staging for the bulk copy, in the Q rows of the first slab (dead once
-                                      // MMA0 has read them)
 constexpr uint32_t I_A1 = 65536;      // [T diag(beta gamma); same] bf16 K-major 128 x 64 (operand A of MMA2); the
                                       // solve's scratch before that
+constexpr uint32_t I_PS = I_A1 + 8192;   // P fp16 staging for the bulk copy, in the second half of A1 (past the solve's
+                                         // scratch; the T scalings overwrite it once the copy has read it)
 constexpr uint32_t I_AM = 81920;      // fp32 A, then T in place (row stride TS)
 constexpr uint32_t I_WST = I_A1;      // -W staging (32 KB, over A1 and A: both dead once MMA2 has completed)
 constexpr uint32_t I_END = I_AM + 64 * TS * 4;
-static_assert(32 * RS * 4 <= 16384, "the solve scratch must fit in A1");
+static_assert(32 * RS * 4 <= 8192, "the solve scratch must fit in the first half of A1");
 static_assert(I_END - I_WST >= 32768, "-W staging must fit over A1 and A");
 
 struct ISmall {
@@ -234,8 +241,10 @@ gdn_intra256_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             bulk_s2g(rec + R_P, smem + I_PS, 8192);
             bulk_commit();
         }
-        // UT transform, T = (I + A)^{-1} in place (the scratch is A1, dead until the scalings below)
+        // UT transform, T = (I + A)^{-1} in place (the scratch is the first half of A1)
         solve_unit_lower_inplace(Am, Rt, tid, ok);
+        if (tid == 96) bulk_wait_read();   // the copy of P has read its staging, which the scalings overwrite
+        __syncthreads();
         // T diag(beta gamma) in bf16 into both row halves of A1 (operand A of MMA2), and T diag(beta) in fp16 straight
         // to the record.  Thread e: row i = e / 8, physical 16-byte chunk pc = e % 8 of the swizzled row.
         if (ok) {
@@ -262,8 +271,7 @@ gdn_intra256_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         }
         fence_async_smem();
         tc_fence_before();
-        if (tid == 96) bulk_wait_read();   // the copy of P has read its staging in the [K; Q] buffer
-        __syncthreads();   // [D] A1 ready; every read of T is done; P is out of the [K; Q] buffer
+        __syncthreads();   // [D] A1 ready; every read of T is done
         // MMA2: D2 = A1 K (M = 128, N = 256 = d_k, K = 64 tokens; K is the MN-major view of the raw K tile, its four
         // 64-column slabs 16 KB apart)
         if (ok && leader) {
@@ -274,6 +282,23 @@ gdn_intra256_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                 mma_f16(tmem, sdesc(sbase + I_A1 + ks * 32, 16, 1024), sdesc(smem_u32(kq) + ks * 2048, 16384, 1024),
                         id, ks > 0);
             mma_commit(&S.m2);
+        }
+        // Q~ = diag(scale gamma) Q and K~ = diag(gamma_C / gamma) K in fp16 straight to the record, in the layout of
+        // their tiles (rows past the end: zeros), while MMA2 runs (it reads only the K rows).  Piece c (16 bytes):
+        // tile c / 2048 (Q, K), slab (c / 512) % 4, byte offset 16 (c % 512) of the slab's 64 rows.
+        if (ok) {
+            const float Gl = S.lg[C - 1];
+#pragma unroll 4
+            for (int k2 = 0; k2 < 16; ++k2) {
+                const int c = tid + I_THREADS * k2;
+                const int isk = c >> 11, sl = (c >> 9) & 3, off = (c & 511) * 16, r = off >> 7;
+                float x[8];
+                bf16x8_to_f32(ld16(kq + sl * 16384 + (isk ? 0 : 8192) + off), x);
+                const float f = isk ? ex2(Gl - S.lg[r]) : p.scale * ex2(S.lg[r]);
+                const uint32_t m = r < it.L ? 0xFFFFFFFFu : 0u;
+                stg16(rec + (isk ? R_K + sl * 8192 : R_WQ + sl * 16384 + 8192) + off, pack_h2(f * x[0], f * x[1]) & m,
+                      pack_h2(f * x[2], f * x[3]) & m, pack_h2(f * x[4], f * x[5]) & m, pack_h2(f * x[6], f * x[7]) & m);
+            }
         }
         if (ok) ok = mbar_wait(&S.m2, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
@@ -314,7 +339,8 @@ gdn_intra256_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         tc_fence_before();
         __syncthreads();   // [E] -W staged
         if (ok && tid == 0) {
-            bulk_s2g(rec + R_W, smem + I_WST, 32768);
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) bulk_s2g(rec + R_WQ + sl * 16384, smem + I_WST + sl * 8192, 8192);
             bulk_commit();
         }
         if (warp == 1 && have_next) {
@@ -354,40 +380,40 @@ struct SParams {
 
 // Shared memory of pass 2 (byte offsets from a 1024-aligned base; every operand base is 1024-aligned)
 struct SL {
-    static constexpr uint32_t QW = 0;          // two stages of [-W; Q~] fp16 K-major, four 64-column slabs of 128 rows
-                                               // (16 KB each): rows 0-63 -W (record), rows 64-127 Q (TMA, bf16) -> Q~
-                                               // in place
+    static constexpr uint32_t QW = 0;          // two stages of [-W; Q~] fp16 K-major (record, one copy), four
+                                               // 64-column slabs of 128 rows (16 KB each)
     static constexpr uint32_t QW_STAGE = 65536;
-    static constexpr uint32_t KF = 131072;     // K~ fp16, MN-major operand of MMA4, four 64-column slabs of 64 rows
+    static constexpr uint32_t KF = 131072;     // K~ fp16 (record), MN-major operand of MMA4, four 64-column slabs of
+                                               // 64 rows
     static constexpr uint32_t PT = 163840;     // P^T fp16 (record), MN-major operand of MMA5
-    static constexpr uint32_t KS = 172032;     // K tile (TMA, bf16), four slabs; converted into KF once the products of
-                                               // the previous chunk that read KF have completed
-    static constexpr uint32_t VF = 204800;     // V tile of the d_v half (TMA, bf16) -> fp16 in place; MN-major operand
-                                               // of MMA_U
+    static constexpr uint32_t OST = 172032;    // half of O of a chunk for the tensor store, [32 tokens][128] in o's
+                                               // dtype
+    static constexpr uint32_t VF = 188416;     // two stages of the V tile of the d_v half (TMA, bf16) -> fp16 in place;
+                                               // MN-major operand of MMA_U (16 KB each)
     static constexpr uint32_t TB = 221184;     // T diag(beta) fp16 (record)
-    static constexpr uint32_t VEC = 229376;    // 2 x SVec
+    static constexpr uint32_t VEC = 229376;    // 2 x SVec (gamma_C of the chunk)
     static constexpr int THREADS = 512;        // lane warps 0-7, output warps 8-11, issuer 12, producer 13,
-                                               // converters 14 and 15
+                                               // gate and V warps 14 and 15
     static constexpr int LW = 256, OW = 128, CW = 64;
     // tensor memory columns
     static constexpr uint32_t TM_H = 0, TM_HF = 256, TM_D3 = 384, TM_COLS = 512;
 };
 struct SVec {
-    float qs[C];     // scale gamma_i (the rows of Q)
-    float kd[C];     // gamma_C / gamma_i (the rows of K)
     float gC;
     float pad[3];
 };
 struct SSmall {
-    uint64_t fullU, fullQ[2], fullKS, fullP;   // copies landed: V + T diag(beta); -W + Q; K; P^T
-    uint64_t emptyU, emptyQ[2], emptyK;        // the products that read them have completed (MMA_U; MMA3; MMA4 + MMA5)
-    uint64_t convU, convQ[2], convK;           // V, Q~, K~ written in fp16 (one arrival per converting warp)
-    uint64_t ksfree;                           // the converters have read the K tile
+    uint64_t fullV[2], fullTB, fullQ[2], fullK, fullP;   // copies landed: V; T diag(beta); [-W; Q~]; K~; P^T
+    uint64_t emptyV[2], emptyTB, emptyQ[2], emptyK;      // the products that read them have completed (MMA_U; MMA_U;
+                                                         // MMA3; MMA4 + MMA5)
+    uint64_t convU[2];                         // V written in fp16 (one arrival per converting warp)
     uint64_t m3, m4, m5;                       // product completions: Delta^T ready; H updated; O^T ready
     uint64_t ofree;                            // the output warps have read O of chunk t (phase t), one arrival each
+    uint64_t staged, sfree;                    // O of chunk t is in the staging (one arrival per output warp); the
+                                               // copies of chunk t have read it (output thread 0)
     uint64_t hready, dready;                   // h~ / Delta operands stored in tensor memory (one arrival per lane warp)
     uint64_t vready[2];                        // gate vectors of the ring slot written (one phase per two chunks)
-    uint64_t vfree[2];                         // ... and read for the last time (lane warps and converters)
+    uint64_t vfree[2];                         // ... and read for the last time (one arrival per lane warp)
     uint32_t tmem_base;
     uint32_t pad;
     float gbuf[C];
@@ -396,9 +422,8 @@ constexpr uint32_t s_smem_bytes() { return SL::VEC + 2 * sizeof(SVec) + sizeof(S
 static_assert(s_smem_bytes() <= 227 * 1024, "state kernel shared memory");
 
 template <bool O_F32>
-__global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                                                                      const __grid_constant__ CUtensorMap tmap_k,
-                                                                      const __grid_constant__ CUtensorMap tmap_v,
+__global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __grid_constant__ CUtensorMap tmap_v,
+                                                                      const __grid_constant__ CUtensorMap tmap_o,
                                                                       const SParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -413,32 +438,32 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
     const int n_chunks = (ch.len + C - 1) / C;
     const long slot0 = ch.row0 / C + ch.n;
     const int H = p.geo.H;
-    const int hk = ch.h / p.group;
 
     if (warp == 12) {
         tmem_alloc(&S.tmem_base, SL::TM_COLS);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&S.fullU, 1);
-        mbar_init(&S.fullKS, 1);
+        mbar_init(&S.fullTB, 1);
+        mbar_init(&S.fullK, 1);
         mbar_init(&S.fullP, 1);
-        mbar_init(&S.emptyU, 1);
+        mbar_init(&S.emptyTB, 1);
         mbar_init(&S.emptyK, 1);
-        mbar_init(&S.convU, SL::OW / 32);
-        mbar_init(&S.convK, SL::CW / 32);
-        mbar_init(&S.ksfree, SL::CW / 32);
         for (int s = 0; s < 2; ++s) {
+            mbar_init(&S.fullV[s], 1);
+            mbar_init(&S.emptyV[s], 1);
+            mbar_init(&S.convU[s], SL::CW / 32);
             mbar_init(&S.fullQ[s], 1);
             mbar_init(&S.emptyQ[s], 1);
-            mbar_init(&S.convQ[s], SL::CW / 32);
             mbar_init(&S.vready[s], 1);
-            mbar_init(&S.vfree[s], (SL::LW + SL::CW) / 32);
+            mbar_init(&S.vfree[s], SL::LW / 32);
         }
         mbar_init(&S.m3, 1);
         mbar_init(&S.m4, 1);
         mbar_init(&S.m5, 1);
         mbar_init(&S.ofree, SL::OW / 32);
+        mbar_init(&S.staged, SL::OW / 32);
+        mbar_init(&S.sfree, 1);
         mbar_init(&S.hready, SL::LW / 32);
         mbar_init(&S.dready, SL::LW / 32);
         fence_mbar_init();
@@ -471,9 +496,7 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
             float gC = ok ? vec[0].gC : 0.f;
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.vfree[0]);
-            if (!ok) {
-                if (lane == 0) d_status(1u << 16);
-            } else {
+            if (ok) {
 #pragma unroll 1
                 for (int gq = 0; gq < 4; ++gq) {
                     const int c0 = 128 * hf + 32 * gq;
@@ -496,6 +519,7 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.hready);
             }
+            if (!ok && lane == 0) d_status(1u << 16);
             const uint32_t d3 = tl + SL::TM_D3;
             for (int t = 0; t < n_chunks && ok; ++t) {
                 // Delta epilogue: Delta^T (columns 32 hf .. + 31 of D3) -> fp16 Delta^T in place, at columns 32 hf ..
@@ -526,20 +550,21 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.dready);
                 const bool last = t + 1 == n_chunks;
-                if (!last) {   // gamma_C of the next chunk, the last read of its ring slot by this warp
+                if (!last) {   // gamma_C of the next chunk
                     const int u = t + 1;
                     ok = mbar_wait(&S.vready[u & 1], (u >> 1) & 1, kWaitNs);
                     ok = __all_sync(0xffffffffu, ok);
-                    gC = ok ? vec[u & 1].gC : 0.f;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&S.vfree[u & 1]);
                     if (!ok) {
                         if (lane == 0) d_status(1u << 17);
                         break;
                     }
+                    gC = vec[u & 1].gC;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.vfree[u & 1]);
                 }
-                // the state of the chunk's end: h~ = fp16(H) for MMA3 of the next chunk and H <- gamma_C' H for its
-                // MMA4; after the last chunk, the final state
+                // the state of the chunk's end: h~ = fp16(H) for MMA3 of the next chunk, 64 columns per tensor-memory
+                // round trip (after the last chunk, the final state); then H <- gamma_C' H for its MMA4 while that MMA3
+                // runs (MMA3 reads only h~; MMA4 is issued after this warp's next Delta epilogue)
                 ok = mbar_wait(&S.m4, t & 1, kWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
@@ -548,37 +573,31 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int gq = 0; gq < 4; ++gq) {
-                    const int c0 = 128 * hf + 32 * gq;
-                    uint32_t r[2][16];
-                    tmem_ld16(tl + SL::TM_H + c0, r[0]);
-                    tmem_ld16(tl + SL::TM_H + c0 + 16, r[1]);
+                for (int hb = 0; hb < 2; ++hb) {
+                    const int c0 = 128 * hf + 64 * hb;
+                    uint32_t r[4][16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) tmem_ld16(tl + SL::TM_H + c0 + 16 * i, r[i]);
                     tmem_ld_wait();
                     if (last) {
                         if (p.hT) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
+                            for (int j = 0; j < 64; ++j) {
                                 const float hv = __uint_as_float(r[j >> 4][j & 15]);
                                 finite = finite && isfinite(hv);
                                 p.hT[sidx + (size_t)(c0 + j) * D2] = hv;
                             }
                         }
                     } else {
-                        uint32_t pk[16];
+                        uint32_t pk[2][16];
 #pragma unroll
-                        for (int m = 0; m < 16; ++m) {
+                        for (int m = 0; m < 32; ++m) {
                             const int k = 2 * m;
-                            pk[m] = pack_h2(__uint_as_float(r[k >> 4][k & 15]),
-                                            __uint_as_float(r[(k + 1) >> 4][(k + 1) & 15]));
+                            pk[m >> 4][m & 15] = pack_h2(__uint_as_float(r[k >> 4][k & 15]),
+                                                         __uint_as_float(r[(k + 1) >> 4][(k + 1) & 15]));
                         }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            r[0][j] = __float_as_uint(gC * __uint_as_float(r[0][j]));
-                            r[1][j] = __float_as_uint(gC * __uint_as_float(r[1][j]));
-                        }
-                        tmem_st16(tl + SL::TM_HF + c0 / 2, pk);
-                        tmem_st16(tl + SL::TM_H + c0, r[0]);
-                        tmem_st16(tl + SL::TM_H + c0 + 16, r[1]);
+                        tmem_st16(tl + SL::TM_HF + c0 / 2, pk[0]);
+                        tmem_st16(tl + SL::TM_HF + c0 / 2 + 16, pk[1]);
                     }
                 }
                 if (!last) {
@@ -586,29 +605,31 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&S.hready);
+#pragma unroll 1
+                    for (int hb = 0; hb < 2; ++hb) {
+                        const int c0 = 128 * hf + 64 * hb;
+                        uint32_t r[4][16];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) tmem_ld16(tl + SL::TM_H + c0 + 16 * i, r[i]);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) r[i][j] = __float_as_uint(gC * __uint_as_float(r[i][j]));
+                            tmem_st16(tl + SL::TM_H + c0 + 16 * i, r[i]);
+                        }
+                    }
+                    tmem_st_wait();
                 }
             }
         }
         if (__any_sync(0xffffffffu, !finite) && lane == 0) d_status(kStatusNonfinite);
     } else if (warp < 12) {
-        // ---------------------------------------------------------------- output warps: O of each chunk, and V
+        // ---------------------------------------------------------------- output warps: O of each chunk
         const int q4 = warp & 3;
         const int dvr = 32 * q4 + lane;                  // d_v row of this thread within the half
         const int otid = tid - SL::LW;                   // 0 .. 127
         const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
-        // V of chunk u to fp16 in place (rows past the end: zeros)
-        auto convert_v = [&](int u) -> bool {
-            bool okc = mbar_wait(&S.fullU, u & 1, kWaitNs);
-            okc = __all_sync(0xffffffffu, okc);
-            if (!okc) return false;
-            tile_to_f16<SL::OW, false>(sbase + SL::VF, sbase + SL::VF, 8192, min(C, ch.len - u * C), otid, 0u);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.convU);
-            return true;
-        };
-        if (n_chunks > 0) ok = convert_v(0);
-        if (!ok && lane == 0) d_status(4096u);
         bool finite = true;
         for (int t = 0; t < n_chunks && ok; ++t) {
             const int L = min(C, ch.len - t * C);
@@ -626,27 +647,55 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.ofree);
-            // o[row][head][d_v]: for each token a warp writes 32 consecutive d_v values
-            const size_t obase = ((size_t)(ch.row0 + (long)t * C) * H + ch.h) * D2 + (size_t)vh * VT + dvr;
+            if (lane == 0) mbar_arrive(&S.ofree);   // D3 may be overwritten from here
+            // O^T to the staging as [token][d_v] rows in o's dtype, 32 tokens per round, each round out by one tensor
+            // store (a partial half: its valid rows one by one) issued by output thread 0
             float nf = 0.f;    // stays 0 unless a written value is not finite (x * 0 is NaN for inf and NaN)
+            const long orow0 = ch.row0 + (long)t * C;
 #pragma unroll
-            for (int i = 0; i < C; ++i) {
-                if (i < L) {
-                    const float ov = __uint_as_float(a[i >> 4][i & 15]);
-                    nf = fmaf(ov, 0.f, nf);
-                    const size_t oi = obase + (size_t)i * H * D2;
-                    if (O_F32) static_cast<float*>(p.o)[oi] = ov;
-                    else static_cast<__nv_bfloat16*>(p.o)[oi] = __float2bfloat16_rn(ov);
+            for (int hb = 0; hb < 2; ++hb) {
+                const int rnd = 2 * t + hb;
+                if (ok && otid == 0 && rnd >= 1) {   // the previous round's copies have read the staging
+                    bulk_wait_read();
+                    mbar_arrive(&S.sfree);
                 }
+                if (ok && rnd >= 1) ok = mbar_wait(&S.sfree, (rnd - 1) & 1, kWaitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int tok = 32 * hb + i;
+                    const float ov = __uint_as_float(a[tok >> 4][tok & 15]);
+                    nf = tok < L ? fmaf(ov, 0.f, nf) : nf;
+                    if (O_F32) sts32(sbase + SL::OST + 4 * (i * VT + dvr), __float_as_uint(ov));
+                    else sts16(sbase + SL::OST + 2 * (i * VT + dvr), __bfloat16_as_ushort(__float2bfloat16_rn(ov)));
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.staged);
+                if (otid == 0) {   // once all four warps' rows are staged
+                    ok = mbar_wait(&S.staged, rnd & 1, kWaitNs);
+                    const int nv = min(32, max(0, L - 32 * hb));   // valid rows of the round
+                    if (ok && nv == 32) {
+                        tma_store_3d(&tmap_o, smem + SL::OST, VT * vh, ch.h, (int)(orow0 + 32 * hb));
+                    } else if (ok) {
+                        constexpr uint32_t ES = O_F32 ? 4 : 2, RB = VT * ES;   // bytes of one staged row
+                        for (int i = 0; i < nv; ++i)
+                            bulk_s2g(static_cast<uint8_t*>(p.o) +
+                                         (((size_t)(orow0 + 32 * hb + i) * H + ch.h) * D2 + (size_t)VT * vh) * ES,
+                                     smem + SL::OST + i * RB, RB);
+                    }
+                    bulk_commit();
+                }
+                ok = __all_sync(0xffffffffu, ok);
             }
             finite = finite && nf == 0.f;
-            if (t + 1 < n_chunks && !convert_v(t + 1)) {
-                ok = false;
-                if (lane == 0) d_status(4096u);
+            if (!ok) {
+                if (lane == 0) d_status(1u << 21);
                 break;
             }
         }
+        if (otid == 0) bulk_wait_all();                // the o rows are written before the CTA exits
         if (__any_sync(0xffffffffu, !finite) && lane == 0) d_status(kStatusNonfinite);
     } else if (warp == 12) {
         // ---------------------------------------------------------------- MMA issuer
@@ -659,15 +708,19 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
             // units, no carry below 256 KB) by a plain add
             const uint64_t dQW0 = sdesc(sbase + SL::QW, 16, 1024), dQW1 = sdesc(sbase + SL::QW + SL::QW_STAGE, 16, 1024);
             const uint64_t dKF = sdesc(sbase + SL::KF, 8192, 1024), dPT = sdesc(sbase + SL::PT, 8192, 1024);
-            const uint64_t dVF = sdesc(sbase + SL::VF, 8192, 1024), dTB = sdesc(sbase + SL::TB, 16, 1024);
+            const uint64_t dVF0 = sdesc(sbase + SL::VF, 8192, 1024), dVF1 = sdesc(sbase + SL::VF + 16384, 8192, 1024);
+            const uint64_t dTB = sdesc(sbase + SL::TB, 16, 1024);
             const uint32_t d3 = tmem + SL::TM_D3;
             for (int t = 0; t < n_chunks && ok; ++t) {
                 const int s = t & 1;
                 const uint64_t dqw = s ? dQW1 : dQW0;
                 // MMA3 overwrites D3, whose output half the output warps read for chunk t - 1 (and whose Delta half
-                // MMA4 and MMA5 of chunk t - 1 read: they completed before that read)
-                ok = mbar_spin(&S.hready, t & 1, kWaitNs) && mbar_wait(&S.convQ[s], (t >> 1) & 1, kWaitNs) &&
-                     (t == 0 || mbar_wait(&S.ofree, (t - 1) & 1, kWaitNs));
+                // MMA4 and MMA5 of chunk t - 1 read: they completed before that read).  The waits that have normally
+                // completed come first and the one on the lane warps last: each wait is a shared-memory access, slow
+                // under this kernel's traffic, and only the last one is then on the chain.
+                ok = (t == 0 || mbar_wait(&S.ofree, (t - 1) & 1, kWaitNs)) &&
+                     mbar_wait(&S.fullQ[s], (t >> 1) & 1, kWaitNs) && mbar_wait(&S.convU[s], (t >> 1) & 1, kWaitNs) &&
+                     mbar_wait(&S.fullTB, t & 1, kWaitNs) && mbar_spin(&S.hready, t & 1, kWaitNs);
                 if (!ok) {
                     d_status(1u << 14);
                     break;
@@ -679,19 +732,15 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
                     mma_f16_ts(d3, tmem + SL::TM_HF + ks * 8, dqw + (ks >> 2) * 1024 + (ks & 3) * 2, id3, ks > 0);
                 mma_commit(&S.emptyQ[s]);
                 // MMA_U: D3[:, 0:64] += V^T (T diag beta)^T, completing Delta^T
-                ok = mbar_wait(&S.convU, t & 1, kWaitNs);
-                if (!ok) {
-                    d_status(1024u);
-                    break;
-                }
-                tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) mma_f16(d3, dVF + ks * 128, dTB + ks * 2, idU, 1u);
+                for (int ks = 0; ks < 4; ++ks) mma_f16(d3, (s ? dVF1 : dVF0) + ks * 128, dTB + ks * 2, idU, 1u);
                 mma_commit(&S.m3);
-                mma_commit(&S.emptyU);
+                mma_commit(&S.emptyV[s]);
+                mma_commit(&S.emptyTB);
                 // MMA4: H += Delta^T K~ (N = 256, K = 64 tokens); A = the fp16 columns 32 hb .. + 15 of D3 (tokens
                 // 32 hb .. + 31)
-                ok = mbar_spin(&S.dready, t & 1, kWaitNs) && mbar_wait(&S.convK, t & 1, kWaitNs);
+                ok = mbar_wait(&S.fullK, t & 1, kWaitNs) && mbar_wait(&S.fullP, t & 1, kWaitNs) &&
+                     mbar_spin(&S.dready, t & 1, kWaitNs);
                 if (!ok) {
                     d_status(512u);
                     break;
@@ -702,11 +751,6 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
                     mma_f16_ts(tmem + SL::TM_H, d3 + (ks >> 1) * 32 + (ks & 1) * 8, dKF + ks * 128, id4, 1u);
                 mma_commit(&S.m4);
                 // MMA5: D3[:, 64:128] += Delta^T P^T
-                ok = mbar_wait(&S.fullP, t & 1, kWaitNs);
-                if (!ok) {
-                    d_status(1u << 19);
-                    break;
-                }
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_f16_ts(d3 + 64, d3 + (ks >> 1) * 32 + (ks & 1) * 8, dPT + ks * 128, id5, 1u);
@@ -717,62 +761,85 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
     } else if (warp == 13) {
         // ---------------------------------------------------------------- producer: TMA tiles and record copies
         if (lane == 0 && n_chunks > 0) {
-            prefetch_tmap(&tmap_q);
-            prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            int issU = 0, issQ = 0, issK = 0, issP = 0;   // chunks whose loads were issued, per group
-            for (int t = 0; t < n_chunks && ok; ++t) {
-                const int s = t & 1;
-                const int r = (int)(ch.row0 + (long)t * C);
-                const uint8_t* rec = p.ws + (size_t)((slot0 + t) * H + ch.h) * R_ITEM;
-                // V and T diag(beta), one stage: MMA_U of chunk t - 1 has read them
-                if (t >= 1) ok = mbar_wait(&S.emptyU, (t - 1) & 1, kWaitNs);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&S.fullU, 16384 + 8192);
-                tma_load_3d(smem + SL::VF, &tmap_v, &S.fullU, VT * vh, ch.h, r);
-                tma_load_3d(smem + SL::VF + 8192, &tmap_v, &S.fullU, VT * vh + 64, ch.h, r);
-                bulk_g2s(smem + SL::TB, rec + R_TB, 8192, &S.fullU);
-                issU = t + 1;
-                // -W and Q, two stages: MMA3 of chunk t - 2 has read the stage (test 2: chunk t - 1's too)
-                if (p.test == 2 && t >= 1) ok = mbar_wait(&S.emptyQ[s ^ 1], ((t - 1) >> 1) & 1, kWaitNs);
-                if (ok && t >= 2) ok = mbar_wait(&S.emptyQ[s], ((t >> 1) + 1) & 1, kWaitNs);
-                if (!ok) break;
-                if (!(p.test == 1 && t == 0)) {   // test: the first chunk's -W and Q never arrive
-                    uint8_t* qw = smem + SL::QW + s * SL::QW_STAGE;
-                    mbar_arrive_expect_tx(&S.fullQ[s], 65536);
-#pragma unroll
-                    for (int sl = 0; sl < 4; ++sl) {
-                        bulk_g2s(qw + sl * 16384, rec + R_W + sl * 8192, 8192, &S.fullQ[s]);
-                        tma_load_3d(qw + sl * 16384 + 8192, &tmap_q, &S.fullQ[s], 64 * sl, hk, r);
+            // Three streams, each refilled as soon as the products that read its buffers have completed: polled
+            // without blocking, so that no stream waits behind another's buffer.  (-W, Q), two stages: MMA3 of chunk
+            // t - 2 has read the stage (test 2: chunk t - 1's too).  V, two stages: MMA_U of chunk t - 2.  T diag(beta),
+            // one stage: MMA_U of chunk t - 1.  (K~, P^T), one stage: MMA4 and MMA5 of chunk t - 1.
+            int issQ = 0, issU = 0, issT = 0, issK = 0;   // chunks whose loads were issued, per stream
+            uint64_t t_last = globaltimer_ns();            // the last progress
+            while (issQ < n_chunks || issU < n_chunks || issT < n_chunks || issK < n_chunks) {
+                bool progress = false;
+                if (issQ < n_chunks) {
+                    const int t = issQ, s = t & 1;
+                    if ((t < 2 || mbar_test(&S.emptyQ[s], ((t >> 1) + 1) & 1)) &&
+                        (p.test != 2 || t < 1 || mbar_test(&S.emptyQ[s ^ 1], ((t - 1) >> 1) & 1))) {
+                        if (!(p.test == 1 && t == 0)) {   // test: the first chunk's -W and Q never arrive
+                            const uint8_t* rec = p.ws + (size_t)((slot0 + t) * H + ch.h) * R_ITEM;
+                            mbar_arrive_expect_tx(&S.fullQ[s], 65536);
+                            bulk_g2s(smem + SL::QW + s * SL::QW_STAGE, rec + R_WQ, 65536, &S.fullQ[s]);
+                        }
+                        issQ = t + 1;
+                        progress = true;
                     }
                 }
-                issQ = t + 1;
-                // K, one stage: the converters have read the previous tile
-                if (t >= 1) ok = mbar_wait(&S.ksfree, (t - 1) & 1, kWaitNs);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&S.fullKS, 32768);
-#pragma unroll
-                for (int sl = 0; sl < 4; ++sl) tma_load_3d(smem + SL::KS + sl * 8192, &tmap_k, &S.fullKS, 64 * sl, hk, r);
-                issK = t + 1;
-                // P^T, one stage: MMA5 of chunk t - 1 has read it
-                if (t >= 1) ok = mbar_wait(&S.emptyK, (t - 1) & 1, kWaitNs);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&S.fullP, 8192);
-                bulk_g2s(smem + SL::PT, rec + R_P, 8192, &S.fullP);
-                issP = t + 1;
+                if (issU < n_chunks) {
+                    const int t = issU, s = t & 1;
+                    if (t < 2 || mbar_test(&S.emptyV[s], ((t >> 1) + 1) & 1)) {
+                        const int r = (int)(ch.row0 + (long)t * C);
+                        uint8_t* vf = smem + SL::VF + s * 16384;
+                        mbar_arrive_expect_tx(&S.fullV[s], 16384);
+                        tma_load_3d(vf, &tmap_v, &S.fullV[s], VT * vh, ch.h, r);
+                        tma_load_3d(vf + 8192, &tmap_v, &S.fullV[s], VT * vh + 64, ch.h, r);
+                        issU = t + 1;
+                        progress = true;
+                    }
+                }
+                if (issT < n_chunks) {
+                    const int t = issT;
+                    if (t < 1 || mbar_test(&S.emptyTB, (t - 1) & 1)) {
+                        const uint8_t* rec = p.ws + (size_t)((slot0 + t) * H + ch.h) * R_ITEM;
+                        mbar_arrive_expect_tx(&S.fullTB, 8192);
+                        bulk_g2s(smem + SL::TB, rec + R_TB, 8192, &S.fullTB);
+                        issT = t + 1;
+                        progress = true;
+                    }
+                }
+                if (issK < n_chunks) {
+                    const int t = issK;
+                    if (t < 1 || mbar_test(&S.emptyK, (t - 1) & 1)) {
+                        const uint8_t* rec = p.ws + (size_t)((slot0 + t) * H + ch.h) * R_ITEM;
+                        mbar_arrive_expect_tx(&S.fullK, 32768);
+                        bulk_g2s(smem + SL::KF, rec + R_K, 32768, &S.fullK);
+                        mbar_arrive_expect_tx(&S.fullP, 8192);
+                        bulk_g2s(smem + SL::PT, rec + R_P, 8192, &S.fullP);
+                        issK = t + 1;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    t_last = globaltimer_ns();
+                } else {
+                    if (globaltimer_ns() - t_last > kWaitNs) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(32);
+                }
             }
             if (!ok) d_status(2048u);
             // copies issued whose barrier nobody waited on must land before the CTA exits: wait for every issued
             // phase (bounded)
-            if (issU > 0) mbar_wait(&S.fullU, (issU - 1) & 1, kWaitNs);
-            if (issK > 0) mbar_wait(&S.fullKS, (issK - 1) & 1, kWaitNs);
-            if (issP > 0) mbar_wait(&S.fullP, (issP - 1) & 1, kWaitNs);
+            for (int t = (issU > 2 ? issU - 2 : 0); t < issU; ++t) mbar_wait(&S.fullV[t & 1], (t >> 1) & 1, kWaitNs);
+            if (issT > 0) mbar_wait(&S.fullTB, (issT - 1) & 1, kWaitNs);
+            if (issK > 0) mbar_wait(&S.fullK, (issK - 1) & 1, kWaitNs);
+            if (issK > 0) mbar_wait(&S.fullP, (issK - 1) & 1, kWaitNs);
             for (int t = (issQ > 2 ? issQ - 2 : 0); t < issQ; ++t)
                 if (!(p.test == 1 && t == 0)) mbar_wait(&S.fullQ[t & 1], (t >> 1) & 1, kWaitNs);
         }
     } else {
-        // ---------------------------------------------------------------- warps 14 and 15: Q~ and K~ in fp16, half of
-        // each tile per warp (rows past the end: zeros); warp 15 first computes the gate vectors
+        // ---------------------------------------------------------------- warps 14 and 15: V in fp16, half of each
+        // tile per warp (rows past the end: zeros); warp 15 first computes the gate vectors
         const int cidx = tid - (SL::THREADS - SL::CW);   // 0 .. 63
         float gn[2] = {0.f, 0.f};
         auto load_g = [&](int t, float (&gg)[2]) {
@@ -785,10 +852,9 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
         };
         if (warp == 15 && n_chunks > 0) load_g(0, gn);
         for (int u = 0; u < n_chunks && ok; ++u) {
-            const int s = u & 1, slot = u & 1;
-            const int L = min(C, ch.len - u * C);
+            const int slot = u & 1;
             if (warp == 15) {
-                // the gate vectors of chunk u, into ring slot u % 2 once everyone has released it (chunk u - 2)
+                // the gate vectors of chunk u, into ring slot u % 2 once its readers have released it (chunk u - 2)
                 if (u >= 2) ok = mbar_wait(&S.vfree[slot], ((u >> 1) + 1) & 1, kWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
@@ -800,46 +866,23 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
                 __syncwarp();
                 float G0, G1, Gl;
                 gate_prefix2(S.gbuf[2 * lane], S.gbuf[2 * lane + 1], lane, G0, G1, Gl);
-                SVec& V = vec[slot];
-                V.qs[2 * lane] = p.scale * ex2(G0);
-                V.qs[2 * lane + 1] = p.scale * ex2(G1);
-                V.kd[2 * lane] = ex2(Gl - G0);
-                V.kd[2 * lane + 1] = ex2(Gl - G1);
-                if (lane == 0) V.gC = ex2(Gl);
+                if (lane == 0) vec[slot].gC = ex2(Gl);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.vready[slot]);
                 if (u + 1 < n_chunks) load_g(u + 1, gn);
             }
-            // Q~ = diag(scale gamma) Q, in place in the stage's Q rows
-            ok = mbar_wait(&S.vready[slot], (u >> 1) & 1, kWaitNs) && mbar_wait(&S.fullQ[s], (u >> 1) & 1, kWaitNs);
+            // V of chunk u, in place in its stage
+            ok = mbar_wait(&S.fullV[u & 1], (u >> 1) & 1, kWaitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
-                if (lane == 0) d_status(1u << 15);
+                if (lane == 0) d_status(4096u);
                 break;
             }
-            const uint32_t qrows = sbase + SL::QW + s * SL::QW_STAGE + 8192;
-            tile_to_f16<SL::CW, true>(qrows, qrows, 16384, L, cidx, smem_u32(vec[slot].qs));
-            tile_to_f16<SL::CW, true>(qrows + 32768, qrows + 32768, 16384, L, cidx, smem_u32(vec[slot].qs));
+            const uint32_t vf = sbase + SL::VF + (u & 1) * 16384;
+            tile_to_f16<SL::CW, false>(vf, vf, 8192, min(C, ch.len - u * C), cidx, 0u);
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.convQ[s]);
-            // K~ = diag(gamma_C / gamma) K, from the K tile into KF once MMA4 and MMA5 of chunk u - 1 have completed
-            ok = mbar_wait(&S.fullKS, u & 1, kWaitNs) && (u == 0 || mbar_wait(&S.emptyK, (u - 1) & 1, kWaitNs));
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) d_status(1u << 18);
-                break;
-            }
-            tile_to_f16<SL::CW, true>(sbase + SL::KS, sbase + SL::KF, 8192, L, cidx, smem_u32(vec[slot].kd));
-            tile_to_f16<SL::CW, true>(sbase + SL::KS + 16384, sbase + SL::KF + 16384, 8192, L, cidx,
-                                      smem_u32(vec[slot].kd));
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&S.convK);
-                mbar_arrive(&S.ksfree);
-                mbar_arrive(&S.vfree[slot]);
-            }
+            if (lane == 0) mbar_arrive(&S.convU[u & 1]);
         }
     }
     tc_fence_before();
@@ -894,6 +937,8 @@ cudaError_t launch_chunk_gdn_d256(const ChunkArgs& a, void* workspace, size_t wo
 
     SParams sp{geo, a.g, a.scale, a.h0, a.hT, a.o, static_cast<const uint8_t*>(workspace), a.act, a.H / a.HK(),
                a.test_fwd};
+    CUtensorMap mo;
+    if (!make_map_rows(&mo, a.o, rows, a.H, D2, a.o_f32 != 0, VT, 32)) return cudaErrorInvalidValue;
     auto launch2 = [&](auto kern) -> cudaError_t {
         cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem_bytes());
         if (e2 != cudaSuccess) return e2;
@@ -907,7 +952,7 @@ cudaError_t launch_chunk_gdn_d256(const ChunkArgs& a, void* workspace, size_t wo
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, sp);
+        return cudaLaunchKernelEx(&cfg, kern, mv, mo, sp);
     };
     e = a.o_f32 ? launch2(gdn_state256_kernel<true>) : launch2(gdn_state256_kernel<false>);
     if (e != cudaSuccess) return e;

@@ -91,8 +91,10 @@ bool make_map(CUtensorMap* m, const void* base, long rows, int H, int d);
 // TMA map of a [rows][H][d] fp32 tensor (d <= 256), box d x 1 head x 64 rows, no swizzle: a 64-row tile lands
 // as a dense row-major [64][d] block.
 bool make_map_f32_rows(CUtensorMap* m, const float* base, long rows, int H, int d);
-// The same for fp32 or bf16 (f32 false), for loads and stores.
-bool make_map_rows(CUtensorMap* m, const void* base, long rows, int H, int d, bool f32);
+// The same for fp32 or bf16 (f32 false), for loads and stores; box_d > 0 narrows the box to box_d elements of d, and
+// box_rows sets its height.
+bool make_map_rows(CUtensorMap* m, const void* base, long rows, int H, int d, bool f32, int box_d = 0,
+                   int box_rows = 64);
 bool device_is_sm100_family();
 
 // Decode step (recurrent_step.cu).

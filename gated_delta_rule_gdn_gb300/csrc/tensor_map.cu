@@ -37,15 +37,17 @@ bool make_map(CUtensorMap* m, const void* base, long rows, int H, int d) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][H][d] fp32 or bf16 tensor, box d x 1 head x 64 rows, no swizzle: a 64-row tile is a dense row-major [64][d]
-// block in shared memory (used for loads and stores)
-bool make_map_rows(CUtensorMap* m, const void* base, long rows, int H, int d, bool f32) {
+// [rows][H][d] fp32 or bf16 tensor, box w x 1 head x box_rows rows (w = box_d, or d when box_d is 0), no swizzle: a
+// tile is a dense row-major [box_rows][w] block in shared memory (used for loads and stores)
+bool make_map_rows(CUtensorMap* m, const void* base, long rows, int H, int d, bool f32, int box_d, int box_rows) {
     auto enc = get_encode();
     const cuuint64_t es = f32 ? 4 : 2;
-    if (!enc || d > 256 || (d * es) % 16 != 0) return false;
+    const int w = box_d > 0 ? box_d : d;
+    if (!enc || d > 256 || w > d || (d * es) % 16 != 0 || (w * es) % 16 != 0 || box_rows < 1 || box_rows > 256)
+        return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)d * es, (cuuint64_t)H * d * es};
-    cuuint32_t box[3] = {(cuuint32_t)d, 1, 64};
+    cuuint32_t box[3] = {(cuuint32_t)w, 1, (cuuint32_t)box_rows};
     cuuint32_t el[3] = {1, 1, 1};
     return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
                dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
