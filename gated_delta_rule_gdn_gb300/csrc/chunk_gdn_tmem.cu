@@ -691,7 +691,7 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 const uint64_t dqw = s ? dQW1 : dQW0, dkf = s ? dKF1 : dKF0;
                 const uint32_t d3 = tmem + GL::TM_D3 + 128 * s;
                 const bool next = t + 1 < n_chunks;
-                ok = mbar_spin(&S.hready, t & 1, kWaitNs) && mbar_wait(&S.convQ[s], (t >> 1) & 1, kWaitNs);
+                ok = mbar_wait(&S.convQ[s], (t >> 1) & 1, kWaitNs) && mbar_spin(&S.hready, t & 1, kWaitNs);
                 if (!ok) {
                     gt_status(1u << 14);
                     break;
@@ -708,8 +708,8 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 // Delta operand was read by MMA45 of chunk t - 1; that phase of m4 is the last one committed, so the
                 // wait is unambiguous.
                 if (next) {
-                    ok = (t == 0 || mbar_spin(&S.m4, (t - 1) & 1, kWaitNs)) &&
-                         mbar_wait(&S.convU[s ^ 1], ((t + 1) >> 1) & 1, kWaitNs);
+                    ok = mbar_wait(&S.convU[s ^ 1], ((t + 1) >> 1) & 1, kWaitNs) &&
+                         (t == 0 || mbar_spin(&S.m4, (t - 1) & 1, kWaitNs));
                     if (!ok) {
                         gt_status(1024u);
                         break;
@@ -719,8 +719,8 @@ __global__ void __launch_bounds__(GL::THREADS, 1) gdn_state_kernel(const __grid_
                 }
                 // (MMA45 overwrites D45, which the output warps read for chunk t - 1: phase t of ofree, after the
                 // initial zeroing's phase 0)
-                ok = mbar_spin(&S.dready, t & 1, kWaitNs) && mbar_wait(&S.convK[s], (t >> 1) & 1, kWaitNs) &&
-                     mbar_wait(&S.ofree, t & 1, kWaitNs);
+                ok = mbar_wait(&S.convK[s], (t >> 1) & 1, kWaitNs) && mbar_wait(&S.ofree, t & 1, kWaitNs) &&
+                     mbar_spin(&S.dready, t & 1, kWaitNs);
                 if (!ok) {
                     gt_status(512u);
                     break;

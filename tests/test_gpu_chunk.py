@@ -362,6 +362,15 @@ def test_head256_tensor_core_pair(B, T, H, h0):
     assert_close(hT, h_ref, torch.bfloat16, "final state")
 
 
+def test_head256_more_state_ctas_than_sms():
+    """90 chains, two state CTAs each (180 on 152 SMs): the state pass runs in two waves."""
+    x = W.chunk_inputs(_w256(), seed=25, B=3, T=150, H=30)
+    o_ref, h_ref = oracle_on_heads(x)
+    o, hT = _run(x, "two_pass")
+    assert_close(o, o_ref, torch.bfloat16, "o")
+    assert_close(hT, h_ref, torch.bfloat16, "final state")
+
+
 def test_head256_packed_sequences_match_separate_runs_bitwise():
     lens = [130, 0, 64, 1, 200, 63, 65]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)

@@ -24,13 +24,13 @@ def lib():
     return gdn.load()
 
 
-def _need(per_channel, B, T, H, n_seqs=0):
-    return _binding.workspace_size(per_channel, B, T, H, 128, 128, 64, torch.bfloat16, n_seqs=n_seqs)
+def _need(per_channel, B, T, H, n_seqs=0, d=128):
+    return _binding.workspace_size(per_channel, B, T, H, d, d, 64, torch.bfloat16, n_seqs=n_seqs)
 
 
-def _noalloc_fake(lib, per_channel, B, T, H):
+def _noalloc_fake(lib, per_channel, B, T, H, d=128):
     return lib.gdn_chunk_fwd_noalloc(int(per_channel), FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, None, 0, None, None, 0,
-                                     FAKE, B, T, H, 128, 128, 64, 1, 0, None)
+                                     FAKE, B, T, H, d, d, 64, 1, 0, None)
 
 
 def test_oversized_request_is_refused_before_any_launch(lib):
@@ -41,18 +41,18 @@ def test_oversized_request_is_refused_before_any_launch(lib):
     assert "scratch" in msg and str(SCRATCH_BYTES) in msg
 
 
-@pytest.mark.parametrize("per_channel, H_fit", [(False, 31), (True, 13)])
-def test_capacity_boundary(lib, per_channel, H_fit):
+@pytest.mark.parametrize("per_channel, d, H_fit", [(False, 128, 31), (True, 128, 13), (False, 256, 8)])
+def test_capacity_boundary(lib, per_channel, d, H_fit):
     """One 4096-token sequence has 4096 / 64 + 2 = 66 slots: the largest head count whose records fit the scratch
-    is accepted by the size check, one more head is refused."""
+    is accepted by the size check, one more head is refused (the head-256 record is 112 KB: 8 heads x 66 slots)."""
     T = 4096
-    assert _need(per_channel, 1, T, H_fit) <= SCRATCH_BYTES < _need(per_channel, 1, T, H_fit + 1)
-    assert _noalloc_fake(lib, per_channel, 1, T, H_fit + 1) == 2
+    assert _need(per_channel, 1, T, H_fit, d=d) <= SCRATCH_BYTES < _need(per_channel, 1, T, H_fit + 1, d=d)
+    assert _noalloc_fake(lib, per_channel, 1, T, H_fit + 1, d) == 2
     assert "scratch" in _binding.last_error()
 
 
 def _inputs(kind, seed, T, H, packed=False):
-    cfg = W.config(2 if packed else (3 if kind == "kda" else 1))
+    cfg = W.HEAD256 if kind == "gdn256" else W.config(2 if packed else (3 if kind == "kda" else 1))
     x = W.chunk_inputs(cfg, seed=seed, B=1, T=T, H=H)
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}, kind == "kda"
 
@@ -71,7 +71,7 @@ def _noalloc(x, pc):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("kind", ["gdn", "kda"])
+@pytest.mark.parametrize("kind", ["gdn", "kda", "gdn256"])
 def test_two_consecutive_calls_match_the_workspace_entry_point(lib, kind):
     T, H = 1000, 4                  # (15 + 1 + 1) * 4 records: well inside the scratch
     xa, pc = _inputs(kind, 11, T, H)
