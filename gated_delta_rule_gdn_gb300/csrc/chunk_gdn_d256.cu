@@ -375,7 +375,7 @@ struct SParams {
     const uint8_t* ws;
     GateAct act;
     int group;
-    int test;     // 1: leave out the first record copy (the waits for it run out); 2: a one-chunk-deep [-W; Q] ring
+    int test;     // 1: leave out the first record copy (the waits for it run out); 2: a one-chunk-deep [-W; Q~] ring
 };
 
 // Shared memory of pass 2 (byte offsets from a 1024-aligned base; every operand base is 1024-aligned)
@@ -392,8 +392,8 @@ struct SL {
                                                // MN-major operand of MMA_U (16 KB each)
     static constexpr uint32_t TB = 221184;     // T diag(beta) fp16 (record)
     static constexpr uint32_t VEC = 229376;    // 2 x SVec (gamma_C of the chunk)
-    static constexpr int THREADS = 512;        // lane warps 0-7, output warps 8-11, issuer 12, producer 13,
-                                               // gate and V warps 14 and 15
+    static constexpr int THREADS = 512;        // lane warps 0-7, output warps 8-11, issuer 12, copies 13, gate and
+                                               // V warps 14 and 15
     static constexpr int LW = 256, OW = 128, CW = 64;
     // tensor memory columns
     static constexpr uint32_t TM_H = 0, TM_HF = 256, TM_D3 = 384, TM_COLS = 512;
@@ -412,7 +412,7 @@ struct SSmall {
     uint64_t staged, sfree;                    // O of chunk t is in the staging (one arrival per output warp); the
                                                // copies of chunk t have read it (output thread 0)
     uint64_t hready, dready;                   // h~ / Delta operands stored in tensor memory (one arrival per lane warp)
-    uint64_t vready[2];                        // gate vectors of the ring slot written (one phase per two chunks)
+    uint64_t vready[2];                        // gamma_C of the ring slot written (one phase per two chunks)
     uint64_t vfree[2];                         // ... and read for the last time (one arrival per lane warp)
     uint32_t tmem_base;
     uint32_t pad;
@@ -839,7 +839,7 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
         }
     } else {
         // ---------------------------------------------------------------- warps 14 and 15: V in fp16, half of each
-        // tile per warp (rows past the end: zeros); warp 15 first computes the gate vectors
+        // tile per warp (rows past the end: zeros); warp 15 first computes each chunk's gamma_C
         const int cidx = tid - (SL::THREADS - SL::CW);   // 0 .. 63
         float gn[2] = {0.f, 0.f};
         auto load_g = [&](int t, float (&gg)[2]) {
@@ -854,7 +854,7 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
         for (int u = 0; u < n_chunks && ok; ++u) {
             const int slot = u & 1;
             if (warp == 15) {
-                // the gate vectors of chunk u, into ring slot u % 2 once its readers have released it (chunk u - 2)
+                // gamma_C of chunk u, into ring slot u % 2 once its readers have released it (chunk u - 2)
                 if (u >= 2) ok = mbar_wait(&S.vfree[slot], ((u >> 1) + 1) & 1, kWaitNs);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
