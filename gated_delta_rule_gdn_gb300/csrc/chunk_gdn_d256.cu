@@ -20,9 +20,9 @@
 // orientation (tensor-memory lane = d_v row).  The half's state, 128 d_v rows x 256 d_k columns of fp32, is too large
 // for registers: it lives in tensor memory, scaled ahead by the next chunk's gamma_C (H = gamma_C h), and the state
 // update is a product accumulating onto it.  Per chunk:
-//   MMA3   D3 = h~^T [-W; Q~]^T (A = h~^T, the state's fp16 copy in tensor memory, K = d_k = 256): columns 0-63
-//          -(W h)^T, 64-127 (Q~ h)^T
-//   MMA_U  D3[:, 0:64] += V^T (T diag beta)^T: Delta^T          (V converted to fp16 in the kernel)
+//   MMA_U  D3[:, 0:64] = V^T (T diag beta)^T                   (V converted to fp16 in the kernel; off the chain)
+//   MMA3   D3 += h~^T [-W; Q~]^T (A = h~^T, the state's fp16 copy in tensor memory, K = d_k = 256): columns 0-63
+//          become Delta^T, 64-127 (Q~ h)^T
 //   Delta epilogue: Delta^T to fp16 in place
 //   MMA4   H += Delta^T K~ (N = 256): H becomes h of the chunk's end
 //   MMA5   D3[:, 64:128] += Delta^T P^T: O^T
@@ -700,6 +700,7 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
     } else if (warp == 12) {
         // ---------------------------------------------------------------- MMA issuer
         const uint32_t id3 = idesc_f16(128, 128, false, false, false);  // h~^T (TMEM) x [-W; Q~]^T (K-major)
+        const uint32_t id3h = idesc_f16(128, 64, false, false, false);  // the same, one half of [-W; Q~] (rows 0-63 or 64-127)
         const uint32_t idU = idesc_f16(128, 64, false, true, false);    // V^T (MN-major) x (T diag beta)^T
         const uint32_t id4 = idesc_f16(128, 256, false, false, true);   // Delta^T (TMEM) x K~ (MN-major)
         const uint32_t id5 = idesc_f16(128, 64, false, false, true);    // Delta^T (TMEM) x P^T (MN-major)
@@ -714,29 +715,37 @@ __global__ void __launch_bounds__(SL::THREADS, 1) gdn_state256_kernel(const __gr
             for (int t = 0; t < n_chunks && ok; ++t) {
                 const int s = t & 1;
                 const uint64_t dqw = s ? dQW1 : dQW0;
-                // MMA3 overwrites D3, whose output half the output warps read for chunk t - 1 (and whose Delta half
-                // MMA4 and MMA5 of chunk t - 1 read: they completed before that read).  The waits that have normally
-                // completed come first and the one on the lane warps last: each wait is a shared-memory access, slow
-                // under this kernel's traffic, and only the last one is then on the chain.
+                // MMA_U: D3[:, 0:64] = V^T (T diag beta)^T, off the chain: it needs only D3 free (the output warps have
+                // read O of chunk t - 1, which was complete with MMA4 and MMA5 of chunk t - 1, the readers of the Delta
+                // half).  Each wait is a shared-memory access, slow under this kernel's traffic: the ones that have
+                // normally completed come first, the one on the lane warps last.
                 ok = (t == 0 || mbar_wait(&S.ofree, (t - 1) & 1, kWaitNs)) &&
-                     mbar_wait(&S.fullQ[s], (t >> 1) & 1, kWaitNs) && mbar_wait(&S.convU[s], (t >> 1) & 1, kWaitNs) &&
-                     mbar_wait(&S.fullTB, t & 1, kWaitNs) && mbar_spin(&S.hready, t & 1, kWaitNs);
+                     mbar_wait(&S.convU[s], (t >> 1) & 1, kWaitNs) && mbar_wait(&S.fullTB, t & 1, kWaitNs);
+                if (!ok) {
+                    d_status(1024u);
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16(d3, (s ? dVF1 : dVF0) + ks * 128, dTB + ks * 2, idU, ks > 0 ? 1u : 0u);
+                mma_commit(&S.emptyV[s]);
+                mma_commit(&S.emptyTB);
+                // MMA3: D3 += h~^T [-W; Q~]^T (N = 128, K = 256 = d_k): columns 0-63 become Delta^T; the first K step
+                // starts columns 64-127 (the output's inter-chunk term) afresh
+                ok = mbar_wait(&S.fullQ[s], (t >> 1) & 1, kWaitNs) && mbar_spin(&S.hready, t & 1, kWaitNs);
                 if (!ok) {
                     d_status(1u << 14);
                     break;
                 }
                 tc_fence_after();
-                // MMA3: D3 = h~^T [-W; Q~]^T (N = 128, K = 256 = d_k)
+                mma_f16_ts(d3, tmem + SL::TM_HF, dqw, id3h, 1u);
+                mma_f16_ts(d3 + 64, tmem + SL::TM_HF, dqw + 512, id3h, 0u);
 #pragma unroll
-                for (int ks = 0; ks < 16; ++ks)
-                    mma_f16_ts(d3, tmem + SL::TM_HF + ks * 8, dqw + (ks >> 2) * 1024 + (ks & 3) * 2, id3, ks > 0);
+                for (int ks = 1; ks < 16; ++ks)
+                    mma_f16_ts(d3, tmem + SL::TM_HF + ks * 8, dqw + (ks >> 2) * 1024 + (ks & 3) * 2, id3, 1u);
                 mma_commit(&S.emptyQ[s]);
-                // MMA_U: D3[:, 0:64] += V^T (T diag beta)^T, completing Delta^T
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) mma_f16(d3, (s ? dVF1 : dVF0) + ks * 128, dTB + ks * 2, idU, 1u);
                 mma_commit(&S.m3);
-                mma_commit(&S.emptyV[s]);
-                mma_commit(&S.emptyTB);
                 // MMA4: H += Delta^T K~ (N = 256, K = 64 tokens); A = the fp16 columns 32 hb .. + 15 of D3 (tokens
                 // 32 hb .. + 31)
                 ok = mbar_wait(&S.fullK, t & 1, kWaitNs) && mbar_wait(&S.fullP, t & 1, kWaitNs) &&
