@@ -261,9 +261,10 @@ gdn_status kda_chunk_fwd_ws(const void* q, const void* k, const void* v, const f
  * allocate (for example inside a captured graph's replay loop).
  *   Limit: the static scratch holds 64 MiB: (floor(B*T / 64) + N + 1) * H
  *   records of gdn_chunk_workspace_size's per-item size (32,768 bytes for the
- *   scalar gate, 74,240 for the per-channel gate) must fit in 67,108,864
- *   bytes: 2,048 scalar-gate items (e.g. one 4096-token sequence with 31
- *   heads) or 903 per-channel ones (e.g. 13 heads).  A larger request returns
+ *   scalar gate at d = 128, 114,688 at d = 256, 74,240 for the per-channel
+ *   gate) must fit in 67,108,864 bytes: 2,048 scalar-gate items at d = 128
+ *   (e.g. one 4096-token sequence with 31 heads), 585 at d = 256 (8 heads), or
+ *   903 per-channel ones (13 heads).  A larger request returns
  *   GDN_ERR_UNSUPPORTED with the sizes in the message and launches nothing.
  *   Sharing: every call on a device uses the same scratch, so calls whose work
  *   can overlap (different streams, or threads without ordering) race and give
@@ -346,9 +347,11 @@ gdn_status gdn_chunk_plan(int per_channel, int B, int T, int H, int d_k, int d_v
  * with these sizes and kernel request (0 when the resolved kernel needs
  * none).  n_seqs is 0 for a call without cu_seqlens, else its number of
  * packed sequences.  The two-pass kernels keep a record per (chunk slot,
- * head): for the scalar gate 32,768 bytes (-W in bf16, P and T diag(beta) in
- * fp16, with W = T diag(beta gamma) K); for the per-channel gate 74,240 bytes
- * ([Q^; W] with Q^ = scale gamma Q, Ktilde, U and P in fp16, and gamma_C).
+ * head): for the scalar gate at d = 128 32,768 bytes (-W, P^T and
+ * T diag(beta) in fp16, with W = T diag(beta gamma) K); at d = 256 114,688
+ * bytes (the same plus Q~ = diag(scale gamma) Q and K~ = diag(gamma_C/gamma) K
+ * in fp16); for the per-channel gate 74,240 bytes ([Q^; W] with
+ * Q^ = scale gamma Q, Ktilde, U and P in fp16, and gamma_C).
  * There are floor(B*T / 64) + N + 1 slots.  Same status rules as
  * gdn_chunk_plan.
  */
