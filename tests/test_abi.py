@@ -182,6 +182,10 @@ def test_head_sizes_up_to_256_and_the_generic_kernels_shared_memory(lib):
     assert _binding.chunk_plan(False, 1, 300, 2, 256, 256, 64, bf, algo="generic") == "generic"
     assert _binding.chunk_plan(False, 1, 300, 2, 256, 128, 64, bf) == "generic"
     assert _binding.chunk_plan(False, 1, 300, 2, 256, 64, 64, f32) == "generic"
+    # the head-256 pair's workspace: (floor(B T / 64) + N + 1) slots x H records of 114,688 bytes ([-W; Q~] 64 KB,
+    # K~ 32 KB, P^T and T diag(beta) 8 KB each); the d = 128 pair's records are 32,768 bytes
+    assert _binding.workspace_size(False, 2, 4096, 8, 256, 256, 64, bf) == (128 + 2 + 1) * 8 * 114_688
+    assert _binding.workspace_size(False, 2, 4096, 8, 128, 128, 64, bf) == (128 + 2 + 1) * 8 * 32_768
     # ... chunk 32 or less for the per-channel gate; chunk 64 would not fit one CTA's shared memory
     assert _binding.chunk_plan(True, 1, 300, 2, 256, 256, 32, bf) == "generic"
     with pytest.raises(_binding.GdnError) as e:
