@@ -300,6 +300,7 @@ gdn_intra256_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                       pack_h2(f * x[2], f * x[3]) & m, pack_h2(f * x[4], f * x[5]) & m, pack_h2(f * x[6], f * x[7]) & m);
             }
         }
+        __syncthreads();   // [D'] every thread has read the K and Q tiles: the next item's may land over them
         if (ok) ok = mbar_wait(&S.m2, par, kWaitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && tid == 0) d_status(4u);
