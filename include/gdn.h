@@ -474,10 +474,11 @@ gdn_status gdn_chunk_bwd_workspace_size(int per_channel, int B, int T, int H, in
  * copies of the first chunk record of every chain, so their bounded waits give
  * up, gdn_device_status reports GDN_ERR_TIMEOUT and that call's outputs are
  * unspecified.  Nothing is left in flight and the context stays usable.
- * GDN_TEST_FWD_ONE_STAGE: the next scalar-gate two-pass forward refills each
- * buffer of its state kernel's two-stage ring only after the previous chunk's
- * products have completed (one chunk in flight instead of two).  This changes
- * the timing only: the result must be bitwise the same.
+ * GDN_TEST_FWD_ONE_STAGE: the next scalar-gate two-pass forward refills the
+ * two-stage buffers of its state kernel (at d = 128 every one of them, at
+ * d = 256 those of [-W; Q~]) only after the previous chunk's products have
+ * completed (one chunk in flight instead of two).  This changes the timing
+ * only: the result must be bitwise the same.
  */
 #define GDN_TEST_FWD_RECORD_STALL 2
 #define GDN_TEST_FWD_ONE_STAGE 3
