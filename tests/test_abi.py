@@ -173,6 +173,31 @@ def test_beta_activation_mode_checks(lib):
     assert "scalar gate" in _binding.last_error()
 
 
+@pytest.mark.parametrize("per_channel, dk, dv, C, dtype, varlen, expect", [
+    # the tensor-core pairs: bf16, chunk 64, d_k = d_v = 128 (either gate) or 256 (scalar gate), packed or not
+    (False, 128, 128, 64, "bf16", False, "two_pass"),
+    (False, 128, 128, 64, "bf16", True, "two_pass"),
+    (True, 128, 128, 64, "bf16", False, "two_pass"),
+    (False, 256, 256, 64, "bf16", False, "two_pass"),
+    (False, 256, 256, 64, "bf16", True, "two_pass"),
+    # everything else on the generic kernel
+    (True, 256, 256, 32, "bf16", False, "generic"),
+    (False, 256, 128, 64, "bf16", False, "generic"),
+    (False, 128, 256, 64, "bf16", False, "generic"),
+    (False, 192, 192, 64, "bf16", False, "generic"),
+    (False, 64, 64, 64, "bf16", False, "generic"),
+    (False, 128, 128, 32, "bf16", False, "generic"),
+    (False, 128, 128, 64, "f32", False, "generic"),
+    (False, 256, 256, 64, "f32", False, "generic"),
+    (True, 128, 128, 64, "f32", False, "generic"),
+])
+def test_auto_dispatch_table(lib, per_channel, dk, dv, C, dtype, varlen, expect):
+    # which kernel the default (auto) request resolves to, for the shapes the documentation lists
+    import torch
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    assert _binding.chunk_plan(per_channel, 1, 300, 2, dk, dv, C, dt, varlen) == expect
+
+
 def test_head_sizes_up_to_256_and_the_generic_kernels_shared_memory(lib):
     import torch
     bf, f32 = torch.bfloat16, torch.float32
